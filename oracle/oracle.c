@@ -1,0 +1,505 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for the MagicDec self-speculative
+ * decoding hot path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg load this library.  It shares no
+ * code, header, table or helper with the CUDA library; the two meet only in
+ * the seeded inputs they are both given.
+ *
+ * Every function restates, in plain loops and in double precision, a
+ * definition from "MagicDec: Breaking the Latency-Throughput Tradeoff for Long
+ * Context Generation with Speculative Decoding" (arXiv 2408.11049v5) and the
+ * method statement that accompanies the build:
+ *   - verification attention: the gamma+1 speculated queries attend to the
+ *     full KV cache, causal inside the speculated block (section 3.1, the
+ *     verification cost T_V(B,S,gamma); section 3.2);
+ *   - draft attention: one query over the K-row sparse draft cache
+ *     (section 4.1, Eq. 3, the decoding cost T_D(B,K));
+ *   - StreamingLLM selection: attention sinks plus a recent window
+ *     (section 4.4 and section 5.1);
+ *   - SnapKV selection: observation-window attention scores, summed over the
+ *     window rows and the query heads of a KV group, max-pooled, per-KV-head
+ *     top-k, observation window always kept (section 4.4, section 5.2);
+ *   - the "pre-gather a sparse KV cache" copy (section 4.4);
+ *   - speculative sampling (Leviathan et al., cited in section 3.1 for
+ *     Eq. 1): accept draft token x when u < p(x)/q(x), otherwise resample
+ *     from norm(max(0, p - q)); a bonus token from the last target
+ *     distribution when all gamma drafts are accepted.  Greedy verification
+ *     (the decoding used in section 5.1) accepts while x equals argmax p.
+ *
+ * Inputs arrive exactly as the GPU path consumes them: bf16 bit patterns
+ * (uint16) for Q/K/V, fp32 logits and uniforms, int32 lengths and tokens.
+ * Each bf16 value widens exactly to double.
+ *
+ * Parity pins for every function live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 is the upper half of an IEEE-754 binary32; widening is exact. */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int clamp_len(int32_t len, int hi)
+{
+    if (len < 0) return 0;
+    if (len > hi) return hi;
+    return (int)len;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Softmax attention of one query row over n_vis key/value rows.             */
+/*   o = sum_j softmax_j(scale * q . k_j) v_j                                 */
+/* k_j sits at k0 + j*kstride, v_j at v0 + j*vstride (elements).  An empty    */
+/* visible set yields a zero row.                                             */
+/* ------------------------------------------------------------------------ */
+static void attend_one(const uint16_t *qrow, int d, double scale,
+                       const uint16_t *k0, long kstride,
+                       const uint16_t *v0, long vstride,
+                       int n_vis, double *out)
+{
+    int c;
+    long j;
+    for (c = 0; c < d; ++c) out[c] = 0.0;
+    if (n_vis <= 0) return;
+
+    double *s = (double *)malloc(sizeof(double) * (size_t)n_vis);
+    double *q = (double *)malloc(sizeof(double) * (size_t)d);
+    for (c = 0; c < d; ++c) q[c] = bf16_value(qrow[c]);
+
+    double smax = -INFINITY;
+    for (j = 0; j < n_vis; ++j) {
+        const uint16_t *kr = k0 + j * kstride;
+        double acc = 0.0;
+        for (c = 0; c < d; ++c) acc += q[c] * bf16_value(kr[c]);
+        s[j] = scale * acc;
+        if (s[j] > smax) smax = s[j];
+    }
+    double den = 0.0;
+    for (j = 0; j < n_vis; ++j) {
+        double w = exp(s[j] - smax);
+        const uint16_t *vr = v0 + j * vstride;
+        den += w;
+        for (c = 0; c < d; ++c) out[c] += w * bf16_value(vr[c]);
+    }
+    for (c = 0; c < d; ++c) out[c] /= den;
+    free(q);
+    free(s);
+}
+
+/*
+ * Verification attention.  q [B, n_q, H_q, d], k/v [B, L_cap, H_kv, d],
+ * out [B, n_q, H_q, d] (double).  The n_q = gamma+1 speculated tokens occupy
+ * cache positions [len-n_q, len); query row i sees positions 0..len-n_q+i.
+ * Query head hq reads KV head hq / (H_q/H_kv).  len = seq_len[b] clamped to
+ * [0, L_cap].
+ */
+int oracle_verify_attn(int B, int H_q, int H_kv, int d, int L_cap, int n_q,
+                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const int32_t *seq_len, double *out)
+{
+    if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || d <= 0 || n_q <= 0) return -1;
+    const int G = H_q / H_kv;
+    const double scale = 1.0 / sqrt((double)d);
+    long total = (long)B * n_q * H_q;
+    long t;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (t = 0; t < total; ++t) {
+        int hq = (int)(t % H_q);
+        int i = (int)((t / H_q) % n_q);
+        int b = (int)(t / ((long)H_q * n_q));
+        int h = hq / G;
+        int len = clamp_len(seq_len[b], L_cap);
+        int n_vis = len - n_q + i + 1;
+        if (n_vis > len) n_vis = len;
+        const uint16_t *qrow = q + (((long)b * n_q + i) * H_q + hq) * d;
+        const uint16_t *k0 = k + ((long)b * L_cap * H_kv + h) * d;
+        const uint16_t *v0 = v + ((long)b * L_cap * H_kv + h) * d;
+        attend_one(qrow, d, scale, k0, (long)H_kv * d, v0, (long)H_kv * d, n_vis,
+                   out + (((long)b * n_q + i) * H_q + hq) * d);
+    }
+    return 0;
+}
+
+/*
+ * Draft attention over the compact draft cache.  q [B, 1, H_q, d],
+ * kc/vc [B, H_kv, cap, d] (head-major), out [B, 1, H_q, d].  The single query
+ * sees rows 0..len-1 of its KV head, len = draft_len[b] clamped to [0, cap].
+ */
+int oracle_draft_attn(int B, int H_q, int H_kv, int d, int cap,
+                      const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
+                      const int32_t *draft_len, double *out)
+{
+    if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || d <= 0 || cap < 0) return -1;
+    const int G = H_q / H_kv;
+    const double scale = 1.0 / sqrt((double)d);
+    long total = (long)B * H_q;
+    long t;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (t = 0; t < total; ++t) {
+        int hq = (int)(t % H_q);
+        int b = (int)(t / H_q);
+        int h = hq / G;
+        int len = clamp_len(draft_len[b], cap);
+        const uint16_t *k0 = kc + ((long)b * H_kv + h) * cap * d;
+        const uint16_t *v0 = vc + ((long)b * H_kv + h) * cap * d;
+        attend_one(q + ((long)b * H_q + hq) * d, d, scale, k0, d, v0, d, len,
+                   out + ((long)b * H_q + hq) * d);
+    }
+    return 0;
+}
+
+/*
+ * StreamingLLM selection: the first n_sink positions (attention sinks) and the
+ * last n_recent positions of each sequence, ascending, without duplicates.
+ * idx [B, H_kv, n_sink+n_recent] (the same set for every KV head), entries
+ * past n_sel[b] are -1.
+ */
+int oracle_streaming_select(const int32_t *seq_len, int B, int H_kv,
+                            int n_sink, int n_recent, int32_t *idx, int32_t *n_sel)
+{
+    if (B < 0 || H_kv <= 0 || n_sink < 0 || n_recent < 0) return -1;
+    const int width = n_sink + n_recent;
+    int b, h, j;
+    for (b = 0; b < B; ++b) {
+        int len = seq_len[b] < 0 ? 0 : seq_len[b];
+        int32_t *row0 = idx + (long)b * H_kv * width;
+        int n = 0;
+        int sink_end = len < n_sink ? len : n_sink;
+        for (j = 0; j < sink_end; ++j) row0[n++] = j;
+        int rec_begin = len - n_recent;
+        if (rec_begin < n_sink) rec_begin = n_sink;
+        for (j = rec_begin; j < len; ++j) row0[n++] = j;
+        for (j = n; j < width; ++j) row0[j] = -1;
+        for (h = 1; h < H_kv; ++h) memcpy(row0 + (long)h * width, row0, sizeof(int32_t) * width);
+        n_sel[b] = n;
+    }
+    return 0;
+}
+
+/*
+ * Gather of selected KV rows into the compact draft cache:
+ *   kc[b, h, i] = k[b, idx[b, h, i], h], vc likewise, for i < n_idx.
+ * idx [B, H_kv, n_idx].  An index outside [0, L_cap) (the -1 padding of a
+ * short selection) writes a zero row.  Rows n_idx..cap-1 are left untouched.
+ */
+int oracle_gather_kv(int B, int H_kv, int d, int L_cap, const uint16_t *k, const uint16_t *v,
+                     const int32_t *idx, int n_idx, int cap, uint16_t *kc, uint16_t *vc)
+{
+    if (B < 0 || H_kv <= 0 || d <= 0 || n_idx < 0 || n_idx > cap) return -1;
+    int b, h, i;
+    for (b = 0; b < B; ++b)
+        for (h = 0; h < H_kv; ++h)
+            for (i = 0; i < n_idx; ++i) {
+                int32_t pos = idx[((long)b * H_kv + h) * n_idx + i];
+                uint16_t *kd = kc + (((long)b * H_kv + h) * cap + i) * d;
+                uint16_t *vd = vc + (((long)b * H_kv + h) * cap + i) * d;
+                if (pos < 0 || pos >= L_cap) {
+                    memset(kd, 0, sizeof(uint16_t) * d);
+                    memset(vd, 0, sizeof(uint16_t) * d);
+                } else {
+                    memcpy(kd, k + (((long)b * L_cap + pos) * H_kv + h) * d, sizeof(uint16_t) * d);
+                    memcpy(vd, v + (((long)b * L_cap + pos) * H_kv + h) * d, sizeof(uint16_t) * d);
+                }
+            }
+    return 0;
+}
+
+/*
+ * SnapKV observation-window scores.  For each sequence (length L = seq_len[b]
+ * clamped to [0, L_cap]) and KV head h, the last w prompt positions are the
+ * observation window; window row r sits at position L-w+r and its query for
+ * head hq is q_win[b, r, hq, :] (q_win is [B, w, H_q, d]).  Row r attends
+ * causally to positions 0..L-w+r with the full softmax.  The score of
+ * position j is the sum, over the window rows and the G query heads of the KV
+ * group, of that row's softmax probability at j:
+ *   score[b, h, j] = sum_{hq in group h} sum_r softmax_r(j).
+ * Written for every j < L (window positions included), zero for j >= L;
+ * score is [B, H_kv, L_cap].  Sequences with L < w score nothing.
+ */
+int oracle_snapkv_scores(int B, int H_q, int H_kv, int d, int L_cap, int w,
+                         const uint16_t *q_win, const uint16_t *k,
+                         const int32_t *seq_len, double *score)
+{
+    if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || d <= 0 || w <= 0) return -1;
+    const int G = H_q / H_kv;
+    const double scale = 1.0 / sqrt((double)d);
+    long pairs = (long)B * H_kv;
+    long p;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (p = 0; p < pairs; ++p) {
+        int b = (int)(p / H_kv), h = (int)(p % H_kv);
+        int L = clamp_len(seq_len[b], L_cap);
+        double *sc = score + p * L_cap;
+        long j;
+        int c, g, r;
+        for (j = 0; j < L_cap; ++j) sc[j] = 0.0;
+        if (L < w) continue;
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        double *q = (double *)malloc(sizeof(double) * (size_t)d);
+        for (g = 0; g < G; ++g) {
+            int hq = h * G + g;
+            for (r = 0; r < w; ++r) {
+                const uint16_t *qrow = q_win + (((long)b * w + r) * H_q + hq) * d;
+                int n_vis = L - w + r + 1;
+                for (c = 0; c < d; ++c) q[c] = bf16_value(qrow[c]);
+                double smax = -INFINITY;
+                for (j = 0; j < n_vis; ++j) {
+                    const uint16_t *kr = k + (((long)b * L_cap + j) * H_kv + h) * d;
+                    double acc = 0.0;
+                    for (c = 0; c < d; ++c) acc += q[c] * bf16_value(kr[c]);
+                    s[j] = scale * acc;
+                    if (s[j] > smax) smax = s[j];
+                }
+                double den = 0.0;
+                for (j = 0; j < n_vis; ++j) den += exp(s[j] - smax);
+                for (j = 0; j < n_vis; ++j) sc[j] += exp(s[j] - smax) / den;
+            }
+        }
+        free(q);
+        free(s);
+    }
+    return 0;
+}
+
+/*
+ * One-dimensional max pooling with stride 1 and an odd kernel, window clipped
+ * at both ends: out[j] = max_{|t-j| <= kernel/2, 0 <= t < n} in[t].
+ */
+int oracle_maxpool1d(const double *in, int n, int kernel, double *out)
+{
+    if (n < 0 || kernel <= 0 || (kernel & 1) == 0) return -1;
+    const int half = kernel / 2;
+    int j, t;
+    for (j = 0; j < n; ++j) {
+        double m = -INFINITY;
+        for (t = j - half; t <= j + half; ++t)
+            if (t >= 0 && t < n && in[t] > m) m = in[t];
+        out[j] = m;
+    }
+    return 0;
+}
+
+typedef struct { double key; int pos; } ranked_t;
+
+/* Larger pooled score first; equal scores by smaller position. */
+static int by_score_desc(const void *a, const void *b)
+{
+    const ranked_t *x = (const ranked_t *)a, *y = (const ranked_t *)b;
+    if (x->key > y->key) return -1;
+    if (x->key < y->key) return 1;
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+static int by_int_asc(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * SnapKV selection.  Scores (oracle_snapkv_scores) over the prefix
+ * [0, L-w) are max-pooled with pool_kernel, the budget-w positions with the
+ * largest pooled score are kept (ties to the smaller position), sorted
+ * ascending, and the w observation-window positions [L-w, L) are appended.
+ * When L <= budget every position 0..L-1 is kept.  idx [B, H_kv, budget],
+ * entries past n_sel[b] are -1.  pooled (optional, [B, H_kv, L_cap]) receives
+ * the pooled prefix scores (zero elsewhere) for margin analysis.
+ */
+int oracle_snapkv_select(int B, int H_q, int H_kv, int d, int L_cap,
+                         const uint16_t *q_win, const uint16_t *k, const int32_t *seq_len,
+                         int w, int pool_kernel, int budget,
+                         int32_t *idx, int32_t *n_sel, double *pooled)
+{
+    if (budget < w || w <= 0 || pool_kernel <= 0 || (pool_kernel & 1) == 0) return -1;
+    long pairs = (long)B * H_kv;
+    double *score = (double *)malloc(sizeof(double) * (size_t)(pairs * L_cap));
+    int rc = oracle_snapkv_scores(B, H_q, H_kv, d, L_cap, w, q_win, k, seq_len, score);
+    if (rc) { free(score); return rc; }
+    const int k_top = budget - w;
+    long p;
+    for (p = 0; p < pairs; ++p) {
+        int b = (int)(p / H_kv);
+        int L = clamp_len(seq_len[b], L_cap);
+        int32_t *out = idx + p * budget;
+        double *pool_row = pooled ? pooled + p * L_cap : NULL;
+        int j, n = 0;
+        if (pool_row) for (j = 0; j < L_cap; ++j) pool_row[j] = 0.0;
+        if (L <= budget) {
+            for (j = 0; j < L; ++j) out[n++] = j;
+        } else {
+            int m = L - w;
+            double *pl = (double *)malloc(sizeof(double) * (size_t)m);
+            ranked_t *rk = (ranked_t *)malloc(sizeof(ranked_t) * (size_t)m);
+            oracle_maxpool1d(score + p * L_cap, m, pool_kernel, pl);
+            for (j = 0; j < m; ++j) { rk[j].key = pl[j]; rk[j].pos = j; }
+            qsort(rk, (size_t)m, sizeof(ranked_t), by_score_desc);
+            for (j = 0; j < k_top; ++j) out[n++] = rk[j].pos;
+            qsort(out, (size_t)k_top, sizeof(int32_t), by_int_asc);
+            for (j = m; j < L; ++j) out[n++] = j;
+            if (pool_row) for (j = 0; j < m; ++j) pool_row[j] = pl[j];
+            free(rk);
+            free(pl);
+        }
+        for (j = n; j < budget; ++j) out[j] = -1;
+        if ((p % H_kv) == 0) n_sel[b] = n;
+    }
+    free(score);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Speculative sampling.                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* p = softmax(logits) at temperature 1, in double. */
+static void softmax_row(const float *logits, int V, double *p)
+{
+    double m = -INFINITY, s = 0.0;
+    int t;
+    for (t = 0; t < V; ++t) if ((double)logits[t] > m) m = logits[t];
+    for (t = 0; t < V; ++t) { p[t] = exp((double)logits[t] - m); s += p[t]; }
+    for (t = 0; t < V; ++t) p[t] /= s;
+}
+
+/*
+ * Inverse-CDF draw from unnormalised weights wt: the smallest t whose running
+ * sum exceeds u * W, W = sum of the weights.  If rounding leaves no such t,
+ * the last token with positive weight.  *amb is raised when u*W lies within
+ * 1e-4 * W of the running sum at either edge of the chosen token.
+ */
+static int inverse_cdf(const double *wt, int V, double u, int *amb)
+{
+    double W = 0.0, c = 0.0, prev;
+    int t, last = V - 1;
+    for (t = 0; t < V; ++t) W += wt[t];
+    for (t = V - 1; t >= 0; --t) if (wt[t] > 0.0) { last = t; break; }
+    const double target = u * W, tol = 1e-4 * W;
+    for (t = 0; t < V; ++t) {
+        prev = c;
+        c += wt[t];
+        if (c > target) {
+            if ((t > 0 && target - prev < tol) || (t < V - 1 && c - target < tol)) ++*amb;
+            return t;
+        }
+    }
+    ++*amb;
+    return last;
+}
+
+static int argmax_row(const float *logits, int V, int *amb)
+{
+    int t, a = 0;
+    for (t = 1; t < V; ++t) if (logits[t] > logits[a]) a = t;
+    double second = -INFINITY;
+    for (t = 0; t < V; ++t) if (t != a && (double)logits[t] > second) second = logits[t];
+    if ((double)logits[a] - second < 1e-4) ++*amb;
+    return a;
+}
+
+/*
+ * Accept / resample for one verification step.
+ *   target [B, gamma+1, V], draft [B, gamma, V] fp32 logits; draft_tok
+ *   [B, gamma]; u_acc [B, gamma] and u_res [B] uniforms in [0, 1).
+ * Sampling mode (greedy == 0): for i = 0..gamma-1 with p = softmax(target_i),
+ *   q = softmax(draft_i), x = draft_tok_i: accept iff u_acc_i < p(x)/q(x)
+ *   (q(x) = 0 accepts iff p(x) > 0; an x outside [0, V) is rejected).  At the
+ *   first rejection emit an inverse-CDF draw (u_res) from max(0, p - q),
+ *   or from p when that residual is all zero, and stop.  If all gamma are
+ *   accepted emit a bonus draw from softmax(target_gamma).
+ * Greedy mode: accept while x equals argmax target_i (ties to the smaller
+ *   token); at the first mismatch emit that argmax; bonus = argmax target_gamma.
+ * Outputs: n_acc [B] in [0, gamma]; out_tok [B, gamma+1] holds the n_acc
+ *   accepted tokens then the emitted one, -1 after; n_amb [B] (nullable)
+ *   counts decisions taken within 1e-4 of their boundary.
+ */
+int oracle_spec_accept(int B, int gamma, int V, const float *target, const float *draft,
+                       const int32_t *draft_tok, const float *u_acc, const float *u_res,
+                       int greedy, int32_t *n_acc, int32_t *out_tok, int32_t *n_amb)
+{
+    if (B < 0 || gamma < 0 || V <= 0) return -1;
+    int b;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (b = 0; b < B; ++b) {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        int32_t *out = out_tok + (long)b * (gamma + 1);
+        int amb = 0, i, t, acc = gamma, emitted = -1;
+        for (i = 0; i <= gamma; ++i) out[i] = -1;
+        for (i = 0; i < gamma; ++i) {
+            const float *tl = target + ((long)b * (gamma + 1) + i) * V;
+            int x = draft_tok[(long)b * gamma + i];
+            int ok;
+            if (greedy) {
+                int a = argmax_row(tl, V, &amb);
+                ok = (x == a);
+                if (!ok) emitted = a;
+            } else {
+                const float *dl = draft + ((long)b * gamma + i) * V;
+                softmax_row(tl, V, p);
+                softmax_row(dl, V, q);
+                if (x < 0 || x >= V) {
+                    ok = 0;
+                } else if (q[x] > 0.0) {
+                    double ratio = p[x] / q[x];
+                    double u = u_acc[(long)b * gamma + i];
+                    ok = (u < ratio);
+                    if (fabs(u - ratio) < 1e-4) ++amb;
+                } else {
+                    ok = (p[x] > 0.0);
+                }
+                if (!ok) {
+                    double W = 0.0;
+                    for (t = 0; t < V; ++t) { q[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0; W += q[t]; }
+                    emitted = inverse_cdf(W > 0.0 ? q : p, V, u_res[b], &amb);
+                }
+            }
+            if (!ok) { acc = i; break; }
+            out[i] = x;
+        }
+        if (acc == gamma) {
+            const float *tl = target + ((long)b * (gamma + 1) + gamma) * V;
+            if (greedy) {
+                emitted = argmax_row(tl, V, &amb);
+            } else {
+                softmax_row(tl, V, p);
+                emitted = inverse_cdf(p, V, u_res[b], &amb);
+            }
+        }
+        out[acc] = emitted;
+        n_acc[b] = acc;
+        if (n_amb) n_amb[b] = amb;
+        free(q);
+        free(p);
+    }
+    return 0;
+}

@@ -1,0 +1,358 @@
+"""Pins for the CPU oracle against facts fixed outside it.
+
+Each test ties one oracle function to something other than its own formula: a
+library routine on a special case (torch's scaled-dot-product attention,
+softmax, max-pool), a brute-force enumeration, a closed form from the paper
+(Eq. 1 of "MagicDec: Breaking the Latency-Throughput Tradeoff for Long Context
+Generation with Speculative Decoding", section 3.1), or an invariant that any
+correct implementation satisfies.  CPU only.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f64(u: np.ndarray) -> np.ndarray:
+    return (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def sdpa_reference(q, k, v, mask):
+    """torch SDPA in fp64 on CPU with a boolean keep-mask; rows with nothing visible -> 0."""
+    qt, kt, vt = (torch.from_numpy(a) for a in (q, k, v))
+    m = torch.from_numpy(mask)
+    empty = ~m.any(-1, keepdim=True)
+    m_safe = m | empty
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m_safe)
+    return torch.where(empty, torch.zeros_like(out), out).numpy()
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("B,H_q,H_kv,d,L_cap,n_q", [(3, 8, 2, 64, 40, 4), (2, 5, 1, 32, 17, 3), (2, 4, 4, 16, 9, 1)])
+def test_verify_attn_matches_torch_sdpa(B, H_q, H_kv, d, L_cap, n_q):
+    rng = np.random.default_rng(7)
+    q = bf16_bits(rng.standard_normal((B, n_q, H_q, d)))
+    k = bf16_bits(rng.standard_normal((B, L_cap, H_kv, d)))
+    v = bf16_bits(rng.standard_normal((B, L_cap, H_kv, d)))
+    seq_len = rng.integers(1, L_cap + 1, size=B).astype(np.int32)
+    seq_len[0] = L_cap
+    if B > 1:
+        seq_len[1] = max(1, n_q - 2)      # shorter than the speculated block: leading rows see nothing
+    got = oracle.verify_attn(q, k, v, seq_len, n_q)
+
+    G = H_q // H_kv
+    qf = bits_to_f64(q).transpose(0, 2, 1, 3)                       # [B,H_q,n_q,d]
+    kf = np.repeat(bits_to_f64(k).transpose(0, 2, 1, 3), G, axis=1)  # repeat_kv -> [B,H_q,L,d]
+    vf = np.repeat(bits_to_f64(v).transpose(0, 2, 1, 3), G, axis=1)
+    mask = np.zeros((B, 1, n_q, L_cap), bool)
+    for b in range(B):
+        for i in range(n_q):
+            mask[b, 0, i, : max(0, seq_len[b] - n_q + i + 1)] = True
+    ref = sdpa_reference(qf, kf, vf, np.broadcast_to(mask, (B, H_q, n_q, L_cap)).copy())
+    np.testing.assert_allclose(got, ref.transpose(0, 2, 1, 3), rtol=1e-11, atol=1e-12)
+
+
+def test_draft_attn_matches_torch_sdpa():
+    rng = np.random.default_rng(8)
+    B, H_q, H_kv, d, cap = 3, 8, 2, 64, 24
+    q = bf16_bits(rng.standard_normal((B, 1, H_q, d)))
+    kc = bf16_bits(rng.standard_normal((B, H_kv, cap, d)))
+    vc = bf16_bits(rng.standard_normal((B, H_kv, cap, d)))
+    dl = np.array([cap, 5, 0], np.int32)
+    got = oracle.draft_attn(q, kc, vc, dl)
+    G = H_q // H_kv
+    qf = bits_to_f64(q).transpose(0, 2, 1, 3)
+    kf = np.repeat(bits_to_f64(kc), G, axis=1)
+    vf = np.repeat(bits_to_f64(vc), G, axis=1)
+    mask = np.zeros((B, H_q, 1, cap), bool)
+    for b in range(B):
+        mask[b, :, :, : dl[b]] = True
+    ref = sdpa_reference(qf, kf, vf, mask)
+    np.testing.assert_allclose(got, ref.transpose(0, 2, 1, 3), rtol=1e-11, atol=1e-12)
+    assert np.all(got[2] == 0.0)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(9)
+    d, cap = 32, 16
+    q = bf16_bits(rng.standard_normal((3, 1, 1, d)))
+    kc = bf16_bits(rng.standard_normal((3, 1, cap, d)))
+    vc = bf16_bits(rng.standard_normal((3, 1, cap, d)))
+    # (a) a single visible row returns that value row exactly
+    # (b) identical keys give the plain mean of the values
+    kc[1, 0, :, :] = kc[1, 0, 0, :]
+    # (c) one key aligned with a huge query dominates: output equals its value row
+    q[2, 0, 0, :] = bf16_bits(np.full(d, 8.0))
+    kc[2, 0, :, :] = bf16_bits(np.zeros((cap, d)))
+    kc[2, 0, 11, :] = bf16_bits(np.full(d, 8.0))
+    dl = np.array([1, cap, cap], np.int32)
+    out = oracle.draft_attn(q, kc, vc, dl)
+    vf = bits_to_f64(vc)
+    np.testing.assert_array_equal(out[0, 0, 0], vf[0, 0, 0])
+    np.testing.assert_allclose(out[1, 0, 0], vf[1, 0].mean(0), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(out[2, 0, 0], vf[2, 0, 11], rtol=1e-12, atol=1e-12)
+
+
+def test_verify_equals_draft_on_last_row():
+    """The last verification row sees the whole sequence: it is plain decode attention over
+    the full prefix, which the draft kernel computes when its cache is the identity gather."""
+    rng = np.random.default_rng(10)
+    B, H_q, H_kv, d, L, n_q = 2, 4, 2, 32, 30, 3
+    q = bf16_bits(rng.standard_normal((B, n_q, H_q, d)))
+    k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    v = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    sl = np.array([L, 21], np.int32)
+    ver = oracle.verify_attn(q, k, v, sl, n_q)
+    kc = np.ascontiguousarray(k.transpose(0, 2, 1, 3))
+    vc = np.ascontiguousarray(v.transpose(0, 2, 1, 3))
+    dr = oracle.draft_attn(np.ascontiguousarray(q[:, n_q - 1 : n_q]), kc, vc, sl)
+    np.testing.assert_allclose(ver[:, n_q - 1], dr[:, 0], rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# StreamingLLM selection and gather
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("n_sink,n_recent", [(4, 60), (16, 496), (0, 8), (5, 0)])
+def test_streaming_select_is_sinks_plus_recent(n_sink, n_recent):
+    lens = np.array([0, 1, 3, n_sink + n_recent - 1, n_sink + n_recent, n_sink + n_recent + 1, 1000, 32000], np.int32)
+    idx, n_sel = oracle.streaming_select(lens, 3, n_sink, n_recent)
+    for b, L in enumerate(lens):
+        want = sorted(set(range(min(n_sink, L))) | set(range(max(0, L - n_recent), L)))
+        assert n_sel[b] == len(want)
+        for h in range(3):
+            assert list(idx[b, h, : n_sel[b]]) == want
+            assert np.all(idx[b, h, n_sel[b]:] == -1)
+        if L <= n_sink + n_recent:
+            assert want == list(range(L))
+
+
+def test_gather_identity_and_padding():
+    rng = np.random.default_rng(11)
+    B, L, H, d, cap = 2, 12, 3, 16, 14
+    k = bf16_bits(rng.standard_normal((B, L, H, d)))
+    v = bf16_bits(rng.standard_normal((B, L, H, d)))
+    idx = np.broadcast_to(np.arange(L, dtype=np.int32), (B, H, L)).copy()
+    kc, vc = oracle.gather_kv(k, v, idx, cap)
+    np.testing.assert_array_equal(kc[:, :, :L], k.transpose(0, 2, 1, 3))
+    np.testing.assert_array_equal(vc[:, :, :L], v.transpose(0, 2, 1, 3))
+    idx2 = idx.copy()
+    idx2[:, :, 5:] = -1
+    kc2, _ = oracle.gather_kv(k, v, idx2, cap)
+    assert np.all(kc2[:, :, 5:L] == 0)
+
+
+# --------------------------------------------------------------------------
+# SnapKV
+# --------------------------------------------------------------------------
+def _snap_inputs(B=2, H_q=4, H_kv=1, d=64, L=256, w=16, seed=12):
+    rng = np.random.default_rng(seed)
+    q_win = bf16_bits(rng.standard_normal((B, w, H_q, d)))
+    k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    return q_win, k
+
+
+def test_snapkv_scores_match_torch_softmax():
+    q_win, k = _snap_inputs(B=2, H_q=4, H_kv=2, d=32, L=50, w=8)
+    sl = np.array([50, 31], np.int32)
+    got = oracle.snapkv_scores(q_win, k, sl)
+    B, w, H_q, d = q_win.shape
+    H_kv = k.shape[2]
+    G = H_q // H_kv
+    for b in range(B):
+        L = sl[b]
+        for h in range(H_kv):
+            qf = torch.from_numpy(bits_to_f64(q_win[b, :, h * G : (h + 1) * G]))   # [w,G,d]
+            kf = torch.from_numpy(bits_to_f64(k[b, :L, h]))                      # [L,d]
+            s = torch.einsum("wgd,ld->gwl", qf, kf) / math.sqrt(d)
+            pos = torch.arange(L)
+            qpos = L - w + torch.arange(w)
+            s = s.masked_fill(pos[None, None, :] > qpos[None, :, None], float("-inf"))
+            ref = torch.softmax(s, dim=-1).sum(dim=(0, 1)).numpy()
+            np.testing.assert_allclose(got[b, h, :L], ref, rtol=1e-11, atol=1e-14)
+            assert np.all(got[b, h, L:] == 0)
+            # every softmax row sums to one: the scores sum to w * G
+            assert abs(got[b, h].sum() - w * G) < 1e-9
+
+
+def test_maxpool_matches_torch_and_naive():
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal(101)
+    x[40:45] = 3.0                                                     # a plateau: exact ties
+    got = oracle.maxpool1d(x, 7)
+    ref = torch.nn.functional.max_pool1d(torch.from_numpy(x)[None, None], 7, stride=1, padding=3)[0, 0].numpy()
+    np.testing.assert_array_equal(got, ref)
+    naive = [max(x[max(0, j - 3) : j + 4]) for j in range(len(x))]
+    np.testing.assert_array_equal(got, naive)
+
+
+def test_snapkv_select_equals_exhaustive_sort():
+    q_win, k = _snap_inputs()
+    sl = np.array([256, 200], np.int32)
+    w, pool, budget = 16, 7, 64
+    idx, n_sel, pooled = oracle.snapkv_select(q_win, k, sl, pool, budget)
+    scores = oracle.snapkv_scores(q_win, k, sl)
+    for b in range(2):
+        L = sl[b]
+        m = L - w
+        pl = np.array([max(scores[b, 0, max(0, j - 3) : min(m, j + 4)]) for j in range(m)])
+        np.testing.assert_array_equal(pooled[b, 0, :m], pl)
+        order = np.lexsort((np.arange(m), -pl))           # score descending, position ascending
+        want = sorted(order[: budget - w].tolist()) + list(range(m, L))
+        assert n_sel[b] == budget
+        assert idx[b, 0].tolist() == want
+
+
+def test_snapkv_keeps_planted_heavy_hitter_and_neighbours():
+    B, H_q, H_kv, d, L, w = 1, 4, 1, 64, 256, 16
+    rng = np.random.default_rng(14)
+    hhat = rng.standard_normal(d)
+    hhat /= np.linalg.norm(hhat)
+    k = rng.standard_normal((B, L, H_kv, d)) * 0.2
+    k[0, 100, 0] = hhat * 8.0 * math.sqrt(d)
+    qw = np.broadcast_to(hhat * math.sqrt(d), (B, w, H_q, d))
+    idx, n_sel, _ = oracle.snapkv_select(bf16_bits(qw), bf16_bits(k), np.array([L], np.int32), 7, 24)
+    chosen = set(idx[0, 0, : n_sel[0]].tolist())
+    assert set(range(97, 104)) <= chosen
+    assert set(range(L - w, L)) <= chosen
+
+
+def test_snapkv_short_sequence_keeps_everything():
+    q_win, k = _snap_inputs()
+    sl = np.array([64, 10], np.int32)
+    idx, n_sel, _ = oracle.snapkv_select(q_win, k, sl, 7, 64)
+    assert n_sel.tolist() == [64, 10]
+    assert idx[0, 0].tolist() == list(range(64))
+    assert idx[1, 0].tolist() == list(range(10)) + [-1] * 54
+
+
+# --------------------------------------------------------------------------
+# Speculative sampling
+# --------------------------------------------------------------------------
+def _softmax(x):
+    e = np.exp(x - x.max())
+    return e / e.sum()
+
+
+def _pieces(breaks):
+    pts = sorted(set([0.0, 1.0] + [float(b) for b in breaks if 0.0 < b < 1.0]))
+    return [((lo + hi) / 2.0, hi - lo) for lo, hi in zip(pts[:-1], pts[1:]) if hi > lo]
+
+
+def _cum_breaks(wts):
+    W = wts.sum()
+    return [] if W <= 0 else list(np.cumsum(wts)[:-1] / W)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_spec_sampling_exact_enumeration_gamma1(seed):
+    """Integrate the accept/resample rule over u exactly: the first emitted token is ~ p_1,
+    and the bonus token after an acceptance is ~ p_2 (Leviathan et al.'s guarantee)."""
+    rng = np.random.default_rng(100 + seed)
+    V = 4
+    tl = (rng.standard_normal((2, V)) * 1.5).astype(np.float32)
+    dl = (rng.standard_normal((1, V)) * 1.5).astype(np.float32)
+    p1, p2 = _softmax(tl[0].astype(np.float64)), _softmax(tl[1].astype(np.float64))
+    q1 = _softmax(dl[0].astype(np.float64))
+    res_breaks = _cum_breaks(np.maximum(p1 - q1, 0)) + _cum_breaks(p2)
+    rows, weights = [], []
+    for x in range(V):
+        for ua, wa in _pieces([p1[x] / q1[x]]):
+            for ur, wr in _pieces(res_breaks):
+                rows.append((x, ua, ur))
+                weights.append(q1[x] * wa * wr)
+    n = len(rows)
+    target = np.broadcast_to(tl, (n, 2, V)).copy()
+    draft = np.broadcast_to(dl, (n, 1, V)).copy()
+    toks = np.array([[r[0]] for r in rows], np.int32)
+    ua = np.array([[r[1]] for r in rows], np.float32)
+    ur = np.array([r[2] for r in rows], np.float32)
+    n_acc, out, _ = oracle.spec_accept(target, draft, toks, ua, ur, greedy=False)
+    wts = np.array(weights)
+    first = np.zeros(V)
+    np.add.at(first, out[:, 0], wts)
+    np.testing.assert_allclose(first, p1, atol=1e-12)
+    acc = n_acc == 1
+    bonus = np.zeros(V)
+    np.add.at(bonus, out[acc, 1], wts[acc])
+    np.testing.assert_allclose(bonus / wts[acc].sum(), p2, atol=1e-12)
+    assert np.all(out[~acc, 1] == -1)
+
+
+def test_spec_sampling_exact_enumeration_gamma2():
+    rng = np.random.default_rng(200)
+    V = 4
+    tl = (rng.standard_normal((3, V)) * 1.2).astype(np.float32)
+    dl = (rng.standard_normal((2, V)) * 1.2).astype(np.float32)
+    p = [_softmax(t.astype(np.float64)) for t in tl]
+    q = [_softmax(t.astype(np.float64)) for t in dl]
+    res_breaks = (_cum_breaks(np.maximum(p[0] - q[0], 0)) + _cum_breaks(np.maximum(p[1] - q[1], 0))
+                  + _cum_breaks(p[2]))
+    rows, weights = [], []
+    for x1, x2 in itertools.product(range(V), range(V)):
+        for u1, w1 in _pieces([p[0][x1] / q[0][x1]]):
+            for u2, w2 in _pieces([p[1][x2] / q[1][x2]]):
+                for ur, wr in _pieces(res_breaks):
+                    rows.append((x1, x2, u1, u2, ur))
+                    weights.append(q[0][x1] * q[1][x2] * w1 * w2 * wr)
+    n = len(rows)
+    r = np.array(rows)
+    n_acc, out, _ = oracle.spec_accept(np.broadcast_to(tl, (n, 3, V)).copy(), np.broadcast_to(dl, (n, 2, V)).copy(),
+                                       r[:, :2].astype(np.int32), r[:, 2:4].astype(np.float32),
+                                       r[:, 4].astype(np.float32), greedy=False)
+    wts = np.array(weights)
+    for pos in range(3):
+        sel = n_acc >= pos
+        dist = np.zeros(V)
+        np.add.at(dist, out[sel, pos], wts[sel])
+        np.testing.assert_allclose(dist / wts[sel].sum(), p[pos], atol=1e-12)
+
+
+def test_greedy_mode_is_argmax_chain():
+    rng = np.random.default_rng(300)
+    B, gamma, V = 64, 4, 50
+    target = rng.standard_normal((B, gamma + 1, V)).astype(np.float32)
+    am = target.argmax(-1)
+    toks = am[:, :gamma].copy()
+    flip = rng.random((B, gamma)) < 0.3
+    toks[flip] = (toks[flip] + 1) % V
+    n_acc, out, _ = oracle.spec_accept(target, None, toks.astype(np.int32), np.zeros((B, gamma), np.float32),
+                                       np.zeros(B, np.float32), greedy=True)
+    for b in range(B):
+        k = 0
+        while k < gamma and toks[b, k] == am[b, k]:
+            k += 1
+        assert n_acc[b] == k
+        assert out[b, :k].tolist() == toks[b, :k].tolist()
+        assert out[b, k] == am[b, k]
+        assert np.all(out[b, k + 1:] == -1)
+
+
+@pytest.mark.parametrize("gamma", [1, 3, 5])
+def test_expected_tokens_matches_eq1(gamma):
+    """Identical target and draft distributions at every position: acceptances are i.i.d. with
+    probability alpha = sum_t min(p_t, q_t), so E[#generated] = (1 - alpha^(gamma+1)) / (1 - alpha)
+    (Eq. 1, section 3.1)."""
+    rng = np.random.default_rng(400 + gamma)
+    V, B = 12, 40000
+    tl = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    dl = (tl + rng.standard_normal(V) * 0.8).astype(np.float32)
+    p, q = _softmax(tl.astype(np.float64)), _softmax(dl.astype(np.float64))
+    alpha = np.minimum(p, q).sum()
+    toks = rng.choice(V, size=(B, gamma), p=q).astype(np.int32)
+    n_acc, _, _ = oracle.spec_accept(np.broadcast_to(tl, (B, gamma + 1, V)).copy(),
+                                     np.broadcast_to(dl, (B, gamma, V)).copy(), toks,
+                                     rng.random((B, gamma)).astype(np.float32), rng.random(B).astype(np.float32),
+                                     greedy=False)
+    gen = n_acc + 1.0
+    omega = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    assert abs(gen.mean() - omega) < 4 * gen.std() / math.sqrt(B)
