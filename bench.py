@@ -1,0 +1,521 @@
+"""Benchmark of the MagicDec self-speculative decoding hot path on GB300.
+
+One timed step is one speculative-decoding step of the attention-only path over
+one batch, for every decoder layer (paper section 3.1: T_SD = gamma * T_D + T_V,
+then acceptance):
+
+    for each of `layers` layers:
+        StreamingLLM selection (sinks + recent window of the current lengths)
+        gather of the selected rows into the compact draft cache
+        gamma x draft attention over the compact cache
+        verification attention of the gamma+1 speculated queries over the full cache
+    speculative accept / resample over the vocabulary
+
+Each layer reuses one layer's KV cache (16.8 GB at B=128, L=32000, far larger
+than the 129 MB L2, so no layer sees another's data in cache).  SnapKV selection
+runs once after prefill in the method; it is timed once per run and reported
+beside the step.  Inputs are synthetic (seeded; see long_context_self_gb300.synth).
+
+`python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]` prints
+one JSON line.  Under torchrun each rank runs its own batch on its own GPU (the
+path shards by sequence with no exchange; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from long_context_self_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama8b_b128_l32k"
+METRIC = "verify/draft attn achieved HBM GB/s (% of peak); spec steps/s at B=128 L=32k"
+LAYERS = 32
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_attn_llama8b_b128_l32k.md")
+ATTN_SRC = os.path.join(ROOT, "long_context_self_gb300", "csrc", "attn.cu")
+
+
+# --------------------------------------------------------------------- helpers
+def spec_step_time(gamma_t_draft: float, t_verify: float, omega: float) -> float:
+    """Expected time per generated token, T_SD = (gamma*T_D + T_V) / Omega (paper section 3.1)."""
+    return (gamma_t_draft + t_verify) / omega
+
+
+def expected_tokens(alpha: float, gamma: int) -> float:
+    """Eq. 1: Omega(gamma, alpha) = (1 - alpha^(gamma+1)) / (1 - alpha)."""
+    if alpha >= 1.0:
+        return gamma + 1.0
+    return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def file_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes of verify_attn from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            key, _, val = line.strip()[2:].partition(":")
+            vals[key.strip()] = val.strip().strip("`")
+    if vals.get("workload") != workload or vals.get("attn.cu sha256[:16]") != file_sha(ATTN_SRC):
+        return None
+    try:
+        return float(vals["dram bytes per launch (full workload)"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"magicdec_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        try:
+            rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        except OSError:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our arm
+class Pipeline:
+    """Device buffers and the per-step call sequence, all through the C-ABI binding."""
+
+    def __init__(self, w: synth.Workload, device, layers: int):
+        from long_context_self_gb300 import binding as mb
+        self.mb = mb
+        self.w, self.dev, self.layers = w, device, layers
+        self.k, self.v, _ = synth.kv_cache(w, device)
+        self.seq_len = torch.full((w.B,), w.L, dtype=torch.int32, device=device)
+        self.q_draft = synth.queries(w, 1, device, seed=w.seed * 7 + 1)
+        self.q_verify = synth.queries(w, w.n_q, device, seed=w.seed * 7 + 2)
+        self.cap = w.stream_budget
+        self.idx = torch.empty((w.B, w.H_kv, self.cap), dtype=torch.int32, device=device)
+        self.n_sel = torch.empty((w.B,), dtype=torch.int32, device=device)
+        self.kc = torch.zeros((w.B, w.H_kv, self.cap, w.d), dtype=torch.bfloat16, device=device)
+        self.vc = torch.zeros_like(self.kc)
+        self.out_d = torch.empty_like(self.q_draft)
+        self.out_v = torch.empty_like(self.q_verify)
+        self.target, self.draft, self.tok, self.u_acc, self.u_res = synth.logits(w, device)
+        self.n_acc = torch.empty((w.B,), dtype=torch.int32, device=device)
+        self.out_tok = torch.empty((w.B, w.n_q), dtype=torch.int32, device=device)
+        self.n_amb = torch.empty((w.B,), dtype=torch.int32, device=device)
+        shape = mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L)
+        ws_attn = max(mb.magicdec_attn_workspace_size(shape, w.n_q),
+                      mb.magicdec_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, self.cap), 1))
+        self.ws_attn = torch.zeros(ws_attn, dtype=torch.uint8, device=device)
+        self.ws_acc = torch.zeros(mb.magicdec_spec_accept_workspace_size(w.B, w.gamma, w.V), dtype=torch.uint8,
+                                  device=device)
+        self.launches_per_step = layers * (3 + w.gamma) + 3
+        self.verify_events, self.draft_events = [], []
+
+    def step(self, record: bool = False):
+        mb, w = self.mb, self.w
+        for _ in range(self.layers):
+            mb.magicdec_streaming_select(self.seq_len, w.H_kv, w.n_sink, w.n_recent, idx=self.idx, n_sel=self.n_sel)
+            mb.magicdec_gather_kv(self.k, self.v, self.idx, self.cap, kc=self.kc, vc=self.vc)
+            for _g in range(w.gamma):
+                if record:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                mb.magicdec_draft_attn(self.q_draft, self.kc, self.vc, self.n_sel, out=self.out_d, ws=self.ws_attn)
+                if record:
+                    e1.record()
+                    self.draft_events.append((e0, e1))
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            mb.magicdec_verify_attn(self.q_verify, self.k, self.v, self.seq_len, out=self.out_v, ws=self.ws_attn)
+            if record:
+                e1.record()
+                self.verify_events.append((e0, e1))
+        mb.magicdec_spec_accept(self.target, self.draft, self.tok, self.u_acc, self.u_res, False, n_acc=self.n_acc,
+                                out_tok=self.out_tok, n_amb=self.n_amb, ws=self.ws_acc)
+
+    # algorithmic bytes
+    def verify_bytes(self) -> float:
+        w = self.w
+        kv = 2.0 * w.B * w.L * w.H_kv * w.d * 2
+        return kv + 2.0 * w.B * w.n_q * w.H_q * w.d * 2
+
+    def draft_bytes(self) -> float:
+        w = self.w
+        return 2.0 * w.B * self.cap * w.H_kv * w.d * 2 + 2.0 * w.B * w.H_q * w.d * 2
+
+    def accept_bytes(self) -> float:
+        w = self.w
+        return 4.0 * w.B * (2 * w.gamma + 1) * w.V
+
+
+def time_component(fn, reps: int) -> float:
+    """Mean device ms of fn() over reps launches (CUDA events on the current stream)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fn()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    from long_context_self_gb300 import binding as mb
+    from long_context_self_gb300 import build as lbuild
+    lbuild.build()
+    mb.lib()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    w = synth.WORKLOADS[args.workload]
+    pipe = Pipeline(w, device, args.layers)
+    torch.cuda.synchronize()
+
+    # SnapKV selection (once after prefill in the method) and its gather: timed separately.
+    snap = {}
+    if w.snap_budget:
+        sw = synth.Workload("snap", B=w.B, H_q=w.H_q, H_kv=w.H_kv, d=w.d, L=w.L, gamma=w.gamma, V=w.V,
+                            snap_window=w.snap_window, snap_pool=w.snap_pool, snap_budget=w.snap_budget,
+                            seed=w.seed)
+        q_win = synth.window_queries(sw, device)
+        ws_snap = torch.zeros(mb.magicdec_snapkv_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L),
+                                                                 w.snap_window), dtype=torch.uint8, device=device)
+        sidx = torch.empty((w.B, w.H_kv, w.snap_budget), dtype=torch.int32, device=device)
+        sn = torch.empty((w.B,), dtype=torch.int32, device=device)
+        skc = torch.zeros((w.B, w.H_kv, w.snap_budget, w.d), dtype=torch.bfloat16, device=device)
+        svc = torch.zeros_like(skc)
+        t_sel = time_component(lambda: mb.magicdec_snapkv_select(q_win, pipe.k, pipe.seq_len, w.snap_window,
+                                                                  w.snap_pool, w.snap_budget, idx=sidx, n_sel=sn,
+                                                                  ws=ws_snap), 3)
+        t_gat = time_component(lambda: mb.magicdec_gather_kv(pipe.k, pipe.v, sidx, w.snap_budget, kc=skc, vc=svc), 5)
+        snap = {"snapkv_select_ms_per_layer": round(t_sel, 4), "snapkv_gather_ms_per_layer": round(t_gat, 4),
+                "snapkv_budget": w.snap_budget, "snapkv_window": w.snap_window}
+        del q_win, ws_snap, sidx, sn, skc, svc
+        torch.cuda.empty_cache()
+
+    for _ in range(args.warmup):
+        pipe.step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    stream = torch.cuda.current_stream(device)
+    with ClockSampler(local_rank) as clocks:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(args.steps):
+            pipe.step(record=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    ver_ms = statistics.mean(a.elapsed_time(b) for a, b in pipe.verify_events)
+    dra_ms = statistics.mean(a.elapsed_time(b) for a, b in pipe.draft_events)
+    acc_ms = time_component(lambda: mb.magicdec_spec_accept(pipe.target, pipe.draft, pipe.tok, pipe.u_acc,
+                                                            pipe.u_res, False, n_acc=pipe.n_acc,
+                                                            out_tok=pipe.out_tok, n_amb=pipe.n_amb,
+                                                            ws=pipe.ws_acc), 5)
+    sel_ms = time_component(lambda: (mb.magicdec_streaming_select(pipe.seq_len, w.H_kv, w.n_sink, w.n_recent,
+                                                                  idx=pipe.idx, n_sel=pipe.n_sel),
+                                     mb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc,
+                                                           vc=pipe.vc)), 5)
+    omega_hat = float((pipe.n_acc.float() + 1).mean().item())
+
+    # ---------------------------------------------- end to end from host buffers
+    h_qd = pipe.q_draft.cpu().pin_memory()
+    h_qv = pipe.q_verify.cpu().pin_memory()
+    h_t, h_d = pipe.target.cpu().pin_memory(), pipe.draft.cpu().pin_memory()
+    h_tok, h_ua, h_ur = pipe.tok.cpu().pin_memory(), pipe.u_acc.cpu().pin_memory(), pipe.u_res.cpu().pin_memory()
+    h_nacc = torch.empty_like(pipe.n_acc, device="cpu").pin_memory()
+    h_out = torch.empty_like(pipe.out_tok, device="cpu").pin_memory()
+    h2d = (h_qd.numel() * 2 * w.gamma + h_qv.numel() * 2) * args.layers + \
+        (h_t.numel() + h_d.numel() + h_ua.numel() + h_ur.numel()) * 4 + h_tok.numel() * 4
+    d2h = (h_nacc.numel() + h_out.numel()) * 4
+
+    def e2e_step():
+        mbb = mb
+        for _ in range(args.layers):
+            mbb.magicdec_streaming_select(pipe.seq_len, w.H_kv, w.n_sink, w.n_recent, idx=pipe.idx, n_sel=pipe.n_sel)
+            mbb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc, vc=pipe.vc)
+            for _g in range(w.gamma):
+                pipe.q_draft.copy_(h_qd, non_blocking=True)
+                mbb.magicdec_draft_attn(pipe.q_draft, pipe.kc, pipe.vc, pipe.n_sel, out=pipe.out_d, ws=pipe.ws_attn)
+            pipe.q_verify.copy_(h_qv, non_blocking=True)
+            mbb.magicdec_verify_attn(pipe.q_verify, pipe.k, pipe.v, pipe.seq_len, out=pipe.out_v, ws=pipe.ws_attn)
+        pipe.target.copy_(h_t, non_blocking=True)
+        pipe.draft.copy_(h_d, non_blocking=True)
+        pipe.tok.copy_(h_tok, non_blocking=True)
+        pipe.u_acc.copy_(h_ua, non_blocking=True)
+        pipe.u_res.copy_(h_ur, non_blocking=True)
+        mbb.magicdec_spec_accept(pipe.target, pipe.draft, pipe.tok, pipe.u_acc, pipe.u_res, False, n_acc=pipe.n_acc,
+                                 out_tok=pipe.out_tok, n_amb=pipe.n_amb, ws=pipe.ws_acc)
+        h_nacc.copy_(pipe.n_acc, non_blocking=True)
+        h_out.copy_(pipe.out_tok, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    err_word = mb.magicdec_device_error()
+
+    peak, peak_kind = load_peaks()
+    vbytes, dbytes = pipe.verify_bytes(), pipe.draft_bytes()
+    ver_gbs = vbytes / (ver_ms * 1e-3) / 1e9
+    dra_gbs = dbytes / (dra_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    result = {
+        "metric": METRIC,
+        "value": round(world * args.steps / (ms_total * 1e-3), 4),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
+                   "gamma": w.gamma, "V": w.V, "layers": args.layers,
+                   "draft": f"StreamingLLM {w.n_sink}+{w.n_recent} (selection + gather every step)",
+                   "per_rank_batch": w.B, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (KV cache 16.8 GB per layer vs 129 MB L2)",
+                   "step": "layers x (select, gather, gamma x draft_attn, verify_attn) + spec_accept"},
+        "roofline": {"bound": "hbm", "kernel": "decode_attn_kernel (verify)", "achieved": round(ver_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(ver_gbs / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": vbytes, "peak_source": peak_kind},
+        "verify_gbs": round(ver_gbs, 1), "verify_pct_peak": round(100 * ver_gbs / peak, 2),
+        "verify_ms_per_layer": round(ver_ms, 4),
+        "draft_gbs": round(dra_gbs, 1), "draft_pct_peak": round(100 * dra_gbs / peak, 2),
+        "draft_us_per_layer": round(dra_ms * 1e3, 2),
+        "accept_us": round(acc_ms * 1e3, 2),
+        "accept_gbs": round(pipe.accept_bytes() / (acc_ms * 1e-3) / 1e9, 1),
+        "select_gather_us_per_layer": round(sel_ms * 1e3, 2),
+        **snap,
+        "omega_hat_synthetic": round(omega_hat, 4),
+        "tokens_per_s_synthetic": round(world * w.B * omega_hat * args.steps / (ms_total * 1e-3), 1),
+        "gpu_launches": pipe.launches_per_step * args.steps,
+        "device_error_word": err_word,
+        "e2e": {"value": round(world * args.steps / (e2e_ms * 1e-3), 4), "unit": "steps/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del pipe.kc, pipe.vc
+        result["cpu_baseline"] = cpu_baseline(w, args.layers, pipe)
+    return result
+
+
+# -------------------------------------------------------------- oracle on host
+def oracle_step_sample(w: synth.Workload, layers: int, host, nb_attn: int, nb_acc: int):
+    """Time the CPU oracle on a bounded sample of one step and scale it to the whole step.
+    host: dict of numpy inputs for the first sequences.  Returns (seconds per full step, detail)."""
+    import oracle
+    k, v, qd, qv, sl = host["k"][:nb_attn], host["v"][:nb_attn], host["qd"][:nb_attn], host["qv"][:nb_attn], \
+        host["sl"][:nb_attn]
+    t0 = time.perf_counter()
+    idx, n_sel = oracle.streaming_select(sl, w.H_kv, w.n_sink, w.n_recent)
+    kc, vc = oracle.gather_kv(k, v, idx, w.stream_budget)
+    t1 = time.perf_counter()
+    oracle.draft_attn(qd, kc, vc, n_sel)
+    t2 = time.perf_counter()
+    oracle.verify_attn(qv, k, v, sl, w.n_q)
+    t3 = time.perf_counter()
+    oracle.spec_accept(host["target"][:nb_acc], host["draft"][:nb_acc], host["tok"][:nb_acc],
+                       host["u_acc"][:nb_acc], host["u_res"][:nb_acc], False)
+    t4 = time.perf_counter()
+    f_attn, f_acc = w.B / nb_attn, w.B / nb_acc
+    per_step = layers * ((t1 - t0) + w.gamma * (t2 - t1) + (t3 - t2)) * f_attn + (t4 - t3) * f_acc
+    detail = {"select_gather_s": t1 - t0, "draft_s": t2 - t1, "verify_s": t3 - t2, "accept_s": t4 - t3}
+    return per_step, detail, (t4 - t0)
+
+
+def host_sample(w: synth.Workload, pipe, nb_attn: int, nb_acc: int):
+    def u16(t):
+        return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    return {"k": u16(pipe.k[:nb_attn]), "v": u16(pipe.v[:nb_attn]), "qd": u16(pipe.q_draft[:nb_attn]),
+            "qv": u16(pipe.q_verify[:nb_attn]), "sl": pipe.seq_len[:nb_attn].cpu().numpy(),
+            "target": pipe.target[:nb_acc].cpu().numpy(), "draft": pipe.draft[:nb_acc].cpu().numpy(),
+            "tok": pipe.tok[:nb_acc].cpu().numpy(), "u_acc": pipe.u_acc[:nb_acc].cpu().numpy(),
+            "u_res": pipe.u_res[:nb_acc].cpu().numpy()}
+
+
+def cpu_baseline(w: synth.Workload, layers: int, pipe):
+    import oracle
+    nb_attn, nb_acc = 8, 16
+    host = host_sample(w, pipe, nb_attn, nb_acc)
+    per_step, detail, spent = oracle_step_sample(w, layers, host, nb_attn, nb_acc)
+    return {"value": round(1.0 / per_step, 8), "unit": "steps/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"one step's calls on {nb_attn} of {w.B} sequences (attention, selection, gather; all "
+                      f"{layers} layers from one layer's time) and {nb_acc} sequences (accept), scaled "
+                      f"linearly to B={w.B}; {spent:.1f} s of CPU time",
+            "detail_s": {k: round(v, 4) for k, v in detail.items()}}
+
+
+def run_reference(args, rank: int):
+    """The oracle as the reference arm: each step times a bounded sample on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    nb_attn, nb_acc = 4, 8
+    # inputs for the sampled sequences, drawn on the host with the same recipes
+    sw = synth.Workload("sample", B=nb_attn, H_q=w.H_q, H_kv=w.H_kv, d=w.d, L=w.L, gamma=w.gamma, V=w.V,
+                        n_sink=w.n_sink, n_recent=w.n_recent, boost_frac=w.boost_frac, boost=w.boost,
+                        target_sigma=w.target_sigma, draft_noise=w.draft_noise, seed=w.seed)
+    k, v, _ = synth.kv_cache(sw, "cpu")
+    qd = synth.queries(sw, 1, "cpu", seed=1)
+    qv = synth.queries(sw, w.n_q, "cpu", seed=2)
+    target, draft, tok, u_acc, u_res = synth.logits(w, "cpu", B=nb_acc)
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    host = {"k": u16(k), "v": u16(v), "qd": u16(qd), "qv": u16(qv), "sl": np.full(nb_attn, w.L, np.int32),
+            "target": target.numpy(), "draft": draft.numpy(), "tok": tok.numpy(), "u_acc": u_acc.numpy(),
+            "u_res": u_res.numpy()}
+    for _ in range(args.warmup):
+        oracle_step_sample(w, args.layers, host, nb_attn, nb_acc)
+    times, spent = [], 0.0
+    for _ in range(args.steps):
+        per_step, _, s = oracle_step_sample(w, args.layers, host, nb_attn, nb_acc)
+        times.append(per_step)
+        spent += s
+    ms_step = 1e3 * statistics.mean(times)
+    value = 1e3 / ms_step
+    sample = (f"per step: one step's calls on {nb_attn} of {w.B} sequences (attention, selection, gather; "
+              f"{args.layers} layers from one layer's time) and {nb_acc} sequences (accept), scaled linearly "
+              f"to B={w.B}")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "steps/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
+                       "gamma": w.gamma, "V": w.V, "layers": args.layers},
+            "cpu_baseline": {"value": round(value, 8), "unit": "steps/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample + f"; {spent:.1f} s of CPU time in total"},
+            "e2e": {"value": round(value, 8), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * magicdec.h -- C ABI of the GB300 (sm_103a) hot path for MagicDec-style
+ * long-context self-speculative decoding.
+ *
+ * Method: "MagicDec: Breaking the Latency-Throughput Tradeoff for Long Context
+ * Generation with Speculative Decoding" (arXiv 2408.11049v5).  A target model
+ * drafts gamma tokens with attention over a sparse subset of its own KV cache
+ * (StreamingLLM sinks + recent window, or SnapKV observation-window top-k,
+ * section 4.4), then verifies them with attention of the gamma+1 speculated
+ * queries over the full KV cache (section 3.1, T_V(B,S,gamma)), and keeps the
+ * accepted prefix by speculative sampling (Leviathan et al., cited for Eq. 1)
+ * or greedy matching (section 5.1).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates nothing and keeps no state between calls, apart from one
+ *    device-side error word (see magicdec_device_error).
+ *  - bf16 tensors are passed as uint16_t bit patterns.  Layouts are dense
+ *    row-major with the shapes given beside each argument.
+ *  - Every pointer that a kernel reads or writes in 16-byte vectors must be
+ *    16-byte aligned (checked; MAGICDEC_ERR_ALIGN).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    validate their arguments on the host, enqueue kernels and return without
+ *    synchronising.  A status other than MAGICDEC_OK means nothing was
+ *    enqueued, except MAGICDEC_ERR_CUDA, which reports a launch error.
+ *  - Per-sequence lengths live on the device and cannot be checked on the
+ *    host: kernels clamp them to [0, capacity].
+ *  - Inputs must be finite.
+ *  - Workspaces are caller-owned device buffers of at least the size the
+ *    matching *_workspace_size() returns.  They must be zero-filled once
+ *    before first use; every call leaves them ready for the next call.  Calls
+ *    that share one workspace must not overlap on the GPU.
+ */
+#ifndef MAGICDEC_H
+#define MAGICDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MAGICDEC_API __attribute__((visibility("default")))
+#else
+#define MAGICDEC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MAGICDEC_OK = 0,
+    MAGICDEC_ERR_NULL = -1,        /* a required pointer is NULL */
+    MAGICDEC_ERR_SHAPE = -2,       /* a size is out of range or inconsistent */
+    MAGICDEC_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+    MAGICDEC_ERR_WORKSPACE = -4,   /* workspace smaller than *_workspace_size() */
+    MAGICDEC_ERR_UNSUPPORTED = -5, /* a valid shape this build has no kernel for */
+    MAGICDEC_ERR_CUDA = -6         /* the CUDA runtime reported an error */
+} magicdec_status;
+
+/* Attention problem shape.  KV cache K/V: [B, L_cap, H_kv, d].  Query head hq
+ * reads KV head hq / (H_q / H_kv) (grouped-query attention).  d is 64 or 128;
+ * H_q must be a multiple of H_kv. */
+typedef struct {
+    int B;
+    int H_q;
+    int H_kv;
+    int d;
+    int L_cap;
+} magicdec_kv_shape;
+
+/* Human-readable name of a status code (static string). */
+MAGICDEC_API const char *magicdec_status_string(int status);
+
+/* Copies the device error word of the current device into *out and clears it
+ * (synchronises the device).  Non-zero means a kernel gave up on a bounded
+ * wait (value 1) or met an inconsistent internal state (value 2); its outputs
+ * are then undefined.  Returns MAGICDEC_OK or MAGICDEC_ERR_CUDA. */
+MAGICDEC_API magicdec_status magicdec_device_error(int32_t *out);
+
+/*
+ * StreamingLLM draft-KV selection (paper section 4.4 and section 5.1:
+ * attention sinks plus a recent window; budget n_sink + n_recent).
+ *   seq_len [B] int32   current sequence lengths (clamped below at 0)
+ *   idx     [B, H_kv, n_sink + n_recent] int32 out: for each sequence the
+ *           positions [0, min(n_sink, len)) then [max(n_sink, len-n_recent),
+ *           len), ascending, identical for every KV head; -1 after n_sel[b].
+ *   n_sel   [B] int32 out: number of valid entries per sequence.
+ * Errors: NULL pointers, B <= 0, H_kv <= 0, n_sink < 0, n_recent < 0,
+ * n_sink + n_recent == 0.
+ */
+MAGICDEC_API magicdec_status magicdec_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink,
+                                          int n_recent, int32_t *idx, int32_t *n_sel, void *stream);
+
+/* Workspace bytes magicdec_snapkv_select needs for this shape and window. */
+MAGICDEC_API size_t magicdec_snapkv_workspace_size(magicdec_kv_shape shape, int window);
+
+/*
+ * SnapKV draft-KV selection, run once after prefill (paper section 4.4: a
+ * static method that pre-gathers a sparse KV cache; section 5.2: best budget
+ * about 2048).  For each sequence of length L = seq_len[b] (clamped to
+ * [0, L_cap]) and KV head h, the last `window` positions form the
+ * observation window; window row r (position L-window+r) of query head hq has
+ * query q_win[b, r, hq, :] and attends causally over positions 0..L-window+r.
+ * The score of a prefix position j < L-window is the sum over window rows and
+ * over the H_q/H_kv query heads of the group of the softmax probability at j.
+ * Scores are max-pooled (kernel pool_kernel, stride 1, clipped at the ends),
+ * the budget-window largest are kept (ties to the smaller position), sorted
+ * ascending, and the window positions [L-window, L) are appended.  When
+ * L <= budget all positions 0..L-1 are kept.
+ *   q_win [B, window, H_q, d] bf16;  k [B, L_cap, H_kv, d] bf16
+ *   idx   [B, H_kv, budget] int32 out (-1 after n_sel[b]);  n_sel [B] int32 out
+ *   ws    workspace of magicdec_snapkv_workspace_size(shape, window) bytes
+ * Errors: NULL pointers, bad shape, window <= 0, budget < window,
+ * pool_kernel even or <= 0, alignment, workspace too small;
+ * MAGICDEC_ERR_UNSUPPORTED when window * (H_q/H_kv) > 192.
+ */
+MAGICDEC_API magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, const uint16_t *q_win, const uint16_t *k,
+                                       const int32_t *seq_len, int window, int pool_kernel, int budget,
+                                       int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Gather of the selected rows into the compact draft cache (paper section
+ * 4.4, "pre-gather a sparse KV cache").
+ *   k, v   [B, L_cap, H_kv, d] bf16;  idx [B, H_kv, n_idx] int32
+ *   kc, vc [B, H_kv, cap, d] bf16 out: row i < n_idx of head h is
+ *          k[b, idx[b,h,i], h] (zero row when the index is outside [0, L_cap));
+ *          rows n_idx..cap-1 are not touched (room for appended tokens).
+ * Errors: NULL pointers, bad shape, n_idx < 0, n_idx > cap, alignment.
+ */
+MAGICDEC_API magicdec_status magicdec_gather_kv(magicdec_kv_shape shape, const uint16_t *k, const uint16_t *v,
+                                   const int32_t *idx, int n_idx, int cap, uint16_t *kc, uint16_t *vc,
+                                   void *stream);
+
+/* Workspace bytes magicdec_draft_attn / magicdec_verify_attn need for this
+ * shape and query count (n_q = 1 for draft) on the current device. */
+MAGICDEC_API size_t magicdec_attn_workspace_size(magicdec_kv_shape shape, int n_q);
+
+/*
+ * Draft attention (paper section 4.1, Eq. 3: decoding cost T_D(B,K) over the
+ * K-row draft cache).  One query token per sequence attends to rows
+ * 0..draft_len[b]-1 of its KV head in the compact cache (draft_len clamped to
+ * [0, cap]; an empty cache gives a zero row).  Softmax scale 1/sqrt(d).
+ *   shape.L_cap is the compact capacity `cap`.
+ *   q  [B, 1, H_q, d] bf16;  kc, vc [B, H_kv, cap, d] bf16;  draft_len [B] int32
+ *   out [B, 1, H_q, d] bf16
+ * Errors: NULL pointers, bad shape, alignment, workspace too small.
+ */
+MAGICDEC_API magicdec_status magicdec_draft_attn(magicdec_kv_shape shape, const uint16_t *q, const uint16_t *kc,
+                                    const uint16_t *vc, const int32_t *draft_len, uint16_t *out, void *ws,
+                                    size_t ws_bytes, void *stream);
+
+/*
+ * Verification attention (paper section 3.1, T_V(B,S,gamma); section 3.2:
+ * verification loads the same KV as decoding).  The n_q = gamma+1 speculated
+ * tokens already occupy cache positions [len-n_q, len), len = seq_len[b]
+ * clamped to [0, L_cap]; query row i sees positions 0..len-n_q+i (causal
+ * inside the speculated block; a row that sees nothing gives zeros).
+ *   q [B, n_q, H_q, d] bf16;  k, v [B, L_cap, H_kv, d] bf16;  seq_len [B] int32
+ *   out [B, n_q, H_q, d] bf16
+ * Supported: (H_q/H_kv) * n_q <= 32 (MAGICDEC_ERR_UNSUPPORTED beyond).
+ * Errors: NULL pointers, bad shape, alignment, workspace too small.
+ */
+MAGICDEC_API magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n_q, const uint16_t *q, const uint16_t *k,
+                                     const uint16_t *v, const int32_t *seq_len, uint16_t *out, void *ws,
+                                     size_t ws_bytes, void *stream);
+
+/* Workspace bytes magicdec_spec_accept needs. */
+MAGICDEC_API size_t magicdec_spec_accept_workspace_size(int B, int gamma, int V);
+
+/*
+ * Speculative-sampling accept / resample for one verification step
+ * (Leviathan et al., as used for Eq. 1 in paper section 3.1), or greedy
+ * verification (paper section 5.1).
+ *   target [B, gamma+1, V] fp32 logits of the target at the gamma+1 positions
+ *   draft  [B, gamma, V]   fp32 logits of the draft (may be NULL when greedy)
+ *   draft_tok [B, gamma] int32; u_acc [B, gamma], u_res [B] uniforms in [0,1)
+ * Sampling (greedy == 0), temperature 1, p = softmax(target_i),
+ *   q = softmax(draft_i): draft token x is accepted iff u_acc < p(x)/q(x)
+ *   (q(x) == 0 accepts iff p(x) > 0; x outside [0,V) is rejected).  At the
+ *   first rejection the emitted token is the smallest t whose running sum of
+ *   max(0, p - q) exceeds u_res times its total (of p if that total is 0).
+ *   If all gamma drafts are accepted, a bonus token is drawn the same way from
+ *   softmax(target_gamma).
+ * Greedy (greedy != 0): accept while x equals argmax target_i (ties to the
+ *   smaller token); emit that argmax at the first mismatch, else the argmax of
+ *   target_gamma.
+ * Outputs: n_acc [B] accepted count in [0, gamma]; out_tok [B, gamma+1]: the
+ *   accepted tokens, then the emitted one, -1 after; n_ambiguous [B]
+ *   (nullable): decisions taken near their boundary -- |u - p/q| < 1e-4, a
+ *   top-2 logit gap below 1e-4, or u * total within 1e-7 of the total from a
+ *   token edge of the inverse CDF.
+ * Precision: per-logit exponentials in fp32; normalisers, p/q ratios and
+ *   running sums in fp64 / double-float.
+ * Errors: NULL pointers, B <= 0, gamma < 0, V <= 0, workspace too small.
+ */
+MAGICDEC_API magicdec_status magicdec_spec_accept(int B, int gamma, int V, const float *target_logits,
+                                     const float *draft_logits, const int32_t *draft_tok, const float *u_acc,
+                                     const float *u_res, int greedy, int32_t *n_acc, int32_t *out_tok,
+                                     int32_t *n_ambiguous, void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAGICDEC_H */

@@ -1,0 +1,235 @@
+// api.cu -- the extern "C" boundary of libmagicdec: argument validation,
+// workspace sizing and dispatch to the sm_103a kernels.  Declarations and the
+// contract of every entry point are in include/magicdec.h.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace magicdec {
+magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, int n_q, int head_major,
+                                   const void *q, const void *k, const void *v, const int32_t *len, void *out,
+                                   void *ws, cudaStream_t st);
+size_t attn_workspace_bytes(int B, int H_kv, int D, int M);
+magicdec_status launch_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
+                                        int32_t *idx, int32_t *n_sel, cudaStream_t st);
+magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *k, const void *v,
+                                 const int32_t *idx, int n_idx, int cap, void *kc, void *vc, cudaStream_t st);
+size_t snapkv_workspace_bytes(int B, int H_q, int H_kv, int D, int L_cap, int w);
+magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
+                                     const int32_t *seq_len, int w, int pool, int budget, int32_t *idx,
+                                     int32_t *n_sel, void *ws, cudaStream_t st);
+size_t accept_workspace_bytes(int B, int gamma, int V);
+magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target, const float *draft,
+                                   const int32_t *draft_tok, const float *u_acc, const float *u_res, int greedy,
+                                   int32_t *n_acc, int32_t *out_tok, int32_t *n_amb, void *ws, cudaStream_t st);
+
+// The library's device error word (one per device that loads the library).
+__device__ int g_error_word;
+}  // namespace magicdec
+
+namespace magicdec_host {
+
+constexpr int kMaxDevices = 64;
+
+static int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+int sm_count() {
+    static int cache[kMaxDevices] = {0};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 1;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+int max_smem_optin() {
+    static int cache[kMaxDevices] = {0};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 48 * 1024;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cache[dev] = n > 0 ? n : 48 * 1024;
+    }
+    return cache[dev];
+}
+
+int *device_error_word() {
+    static int *cache[kMaxDevices] = {nullptr};
+    static std::mutex mu;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, magicdec::g_error_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int *>(ptr);
+    }
+    return cache[dev];
+}
+
+bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, const uint64_t dims[4], const uint64_t strides[3],
+                         const uint32_t box[4]) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!encode) return false;
+    cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+    cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
+    cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace magicdec_host
+
+using magicdec_host::aligned16;
+
+static bool shape_ok(const magicdec_kv_shape &s) {
+    return s.B > 0 && s.H_q > 0 && s.H_kv > 0 && s.H_q % s.H_kv == 0 && (s.d == 64 || s.d == 128) &&
+           s.L_cap > 0 && s.B <= 4096;
+}
+
+extern "C" {
+
+const char *magicdec_status_string(int status) {
+    switch (status) {
+        case MAGICDEC_OK: return "ok";
+        case MAGICDEC_ERR_NULL: return "null pointer";
+        case MAGICDEC_ERR_SHAPE: return "invalid shape";
+        case MAGICDEC_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case MAGICDEC_ERR_WORKSPACE: return "workspace too small";
+        case MAGICDEC_ERR_UNSUPPORTED: return "unsupported shape";
+        case MAGICDEC_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+magicdec_status magicdec_device_error(int32_t *out) {
+    if (!out) return MAGICDEC_ERR_NULL;
+    int *w = magicdec_host::device_error_word();
+    if (!w) return MAGICDEC_ERR_CUDA;
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MAGICDEC_ERR_CUDA;
+    if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MAGICDEC_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return MAGICDEC_ERR_CUDA;
+    *out = v;
+    return MAGICDEC_OK;
+}
+
+magicdec_status magicdec_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
+                                          int32_t *idx, int32_t *n_sel, void *stream) {
+    if (!seq_len || !idx || !n_sel) return MAGICDEC_ERR_NULL;
+    if (B <= 0 || H_kv <= 0 || n_sink < 0 || n_recent < 0 || n_sink + n_recent <= 0) return MAGICDEC_ERR_SHAPE;
+    return magicdec::launch_streaming_select(seq_len, B, H_kv, n_sink, n_recent, idx, n_sel,
+                                             static_cast<cudaStream_t>(stream));
+}
+
+size_t magicdec_snapkv_workspace_size(magicdec_kv_shape shape, int window) {
+    if (!shape_ok(shape) || window <= 0) return 0;
+    return magicdec::snapkv_workspace_bytes(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, window);
+}
+
+magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, const uint16_t *q_win, const uint16_t *k,
+                                       const int32_t *seq_len, int window, int pool_kernel, int budget,
+                                       int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes, void *stream) {
+    if (!q_win || !k || !seq_len || !idx || !n_sel || !ws) return MAGICDEC_ERR_NULL;
+    if (!shape_ok(shape) || window <= 0 || budget < window || pool_kernel <= 0 || (pool_kernel & 1) == 0)
+        return MAGICDEC_ERR_SHAPE;
+    if ((long long)window * (shape.H_q / shape.H_kv) > 192) return MAGICDEC_ERR_UNSUPPORTED;
+    if (!aligned16(q_win) || !aligned16(k) || !aligned16(ws)) return MAGICDEC_ERR_ALIGN;
+    if (ws_bytes < magicdec_snapkv_workspace_size(shape, window)) return MAGICDEC_ERR_WORKSPACE;
+    return magicdec::launch_snapkv_select(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, q_win, k, seq_len,
+                                          window, pool_kernel, budget, idx, n_sel, ws,
+                                          static_cast<cudaStream_t>(stream));
+}
+
+magicdec_status magicdec_gather_kv(magicdec_kv_shape shape, const uint16_t *k, const uint16_t *v,
+                                   const int32_t *idx, int n_idx, int cap, uint16_t *kc, uint16_t *vc,
+                                   void *stream) {
+    if (!k || !v || !idx || !kc || !vc) return MAGICDEC_ERR_NULL;
+    if (!shape_ok(shape) || n_idx < 0 || cap <= 0 || n_idx > cap) return MAGICDEC_ERR_SHAPE;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc)) return MAGICDEC_ERR_ALIGN;
+    return magicdec::launch_gather_kv(shape.B, shape.H_kv, shape.d, shape.L_cap, k, v, idx, n_idx, cap, kc, vc,
+                                      static_cast<cudaStream_t>(stream));
+}
+
+size_t magicdec_attn_workspace_size(magicdec_kv_shape shape, int n_q) {
+    if (!shape_ok(shape) || n_q <= 0) return 0;
+    return magicdec::attn_workspace_bytes(shape.B, shape.H_kv, shape.d, (shape.H_q / shape.H_kv) * n_q);
+}
+
+static magicdec_status attn_common(const magicdec_kv_shape &shape, int n_q, const uint16_t *q, const uint16_t *k,
+                                   const uint16_t *v, const int32_t *len, uint16_t *out, void *ws,
+                                   size_t ws_bytes) {
+    if (!q || !k || !v || !len || !out || !ws) return MAGICDEC_ERR_NULL;
+    if (!shape_ok(shape) || n_q <= 0) return MAGICDEC_ERR_SHAPE;
+    if ((shape.H_q / shape.H_kv) * n_q > 32) return MAGICDEC_ERR_UNSUPPORTED;
+    if ((long long)shape.B * shape.H_kv > magicdec::kAttnMaxPairs) return MAGICDEC_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws))
+        return MAGICDEC_ERR_ALIGN;
+    if (ws_bytes < magicdec_attn_workspace_size(shape, n_q)) return MAGICDEC_ERR_WORKSPACE;
+    return MAGICDEC_OK;
+}
+
+magicdec_status magicdec_draft_attn(magicdec_kv_shape shape, const uint16_t *q, const uint16_t *kc,
+                                    const uint16_t *vc, const int32_t *draft_len, uint16_t *out, void *ws,
+                                    size_t ws_bytes, void *stream) {
+    magicdec_status s = attn_common(shape, 1, q, kc, vc, draft_len, out, ws, ws_bytes);
+    if (s != MAGICDEC_OK) return s;
+    return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, 1, 1, q, kc, vc,
+                                        draft_len, out, ws, static_cast<cudaStream_t>(stream));
+}
+
+magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n_q, const uint16_t *q, const uint16_t *k,
+                                     const uint16_t *v, const int32_t *seq_len, uint16_t *out, void *ws,
+                                     size_t ws_bytes, void *stream) {
+    magicdec_status s = attn_common(shape, n_q, q, k, v, seq_len, out, ws, ws_bytes);
+    if (s != MAGICDEC_OK) return s;
+    return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, n_q, 0, q, k, v,
+                                        seq_len, out, ws, static_cast<cudaStream_t>(stream));
+}
+
+size_t magicdec_spec_accept_workspace_size(int B, int gamma, int V) {
+    if (B <= 0 || gamma < 0 || V <= 0) return 0;
+    return magicdec::accept_workspace_bytes(B, gamma, V);
+}
+
+magicdec_status magicdec_spec_accept(int B, int gamma, int V, const float *target_logits,
+                                     const float *draft_logits, const int32_t *draft_tok, const float *u_acc,
+                                     const float *u_res, int greedy, int32_t *n_acc, int32_t *out_tok,
+                                     int32_t *n_ambiguous, void *ws, size_t ws_bytes, void *stream) {
+    if (!target_logits || !n_acc || !out_tok || !ws) return MAGICDEC_ERR_NULL;
+    if (gamma > 0 && !draft_tok) return MAGICDEC_ERR_NULL;
+    if (!greedy && (!u_res || (gamma > 0 && (!draft_logits || !u_acc)))) return MAGICDEC_ERR_NULL;
+    if (B <= 0 || gamma < 0 || V <= 0) return MAGICDEC_ERR_SHAPE;
+    if (V > 256 * 16384 || B > magicdec::kAcceptMaxBatch) return MAGICDEC_ERR_UNSUPPORTED;
+    if (!aligned16(target_logits) || (draft_logits && !aligned16(draft_logits)) || !aligned16(ws))
+        return MAGICDEC_ERR_ALIGN;
+    if (ws_bytes < magicdec_spec_accept_workspace_size(B, gamma, V)) return MAGICDEC_ERR_WORKSPACE;
+    return magicdec::launch_spec_accept(B, gamma, V, target_logits, draft_logits, draft_tok, u_acc, u_res, greedy,
+                                        n_acc, out_tok, n_ambiguous, ws, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,590 @@
+// attn.cu -- batched GQA decode attention for the draft and verification
+// passes of MagicDec self-speculative decoding, sm_103a.
+//
+// Verification (paper section 3.1, T_V(B,S,gamma)): the gamma+1 speculated
+// queries of every query head in a KV group attend to the full KV cache
+// [B, L_cap, H_kv, d], causal inside the speculated block.  Draft (section
+// 4.1, Eq. 3, T_D(B,K)): one query per head over the compact draft cache
+// [B, H_kv, cap, d].  Both are the same problem -- M = G * n_q query rows per
+// (sequence, KV head) pair streaming that pair's K/V rows once -- so one kernel
+// serves both; only the tensor maps (and the order of their coordinates)
+// differ.
+//
+// Design (HBM-bound: every K/V byte is read exactly once):
+//  * Persistent grid, one CTA per SM.  The whole batch's work is a flat list of
+//    64-row tiles ordered (sequence, KV head, tile); CTA c takes the contiguous
+//    range [c*T/C, (c+1)*T/C), so every SM streams the same number of bytes
+//    whatever the length mix.  A pair split across CTAs produces partial
+//    (max, sum, unnormalised output) triples that the last CTA to finish the
+//    pair merges with the log-sum-exp rule (flash-decoding split-KV; the paper
+//    cites flash decoding in section 2).  "Last arriver merges": an atomic
+//    counter per pair, never a spin-wait.
+//  * One producer thread issues TMA tiled copies: per 64-row tile, one 4-D box
+//    of 64 rows x 64 channels per 128-byte half of K and of V, 128-byte
+//    swizzled so ldmatrix reads are bank-conflict free, into a ring of STAGES
+//    slots guarded by full/empty mbarriers.  Rows past the sequence end are
+//    masked (and their V rows zeroed in shared memory, so stale or
+//    uninitialised cache rows can never reach the output).
+//  * 4*MT consumer warps: warp (mt, pq) owns query rows mt*16..mt*16+15 and
+//    key columns pq*16..pq*16+15 of each tile.  S = Q K^T and O += P V run on
+//    bf16 mma.sync m16n8k16 with fp32 accumulation (the contraction is
+//    16 flop/byte, far below the tensor ridge); the online softmax runs in
+//    fp32 with exp2.  At the end of a pair the four column warps of a row tile
+//    merge in a fixed order through shared memory (deterministic).
+#include "common.cuh"
+
+namespace magicdec {
+
+constexpr int kTileN = 64;      // KV rows per pipeline stage
+constexpr int kMaxStages = 8;
+constexpr int kHalfBytes = kTileN * 128;   // one 64-row x 64-channel swizzled box
+
+struct AttnParams {
+    const __nv_bfloat16 *q;     // [B, n_q, H_q, D]
+    const int32_t *len;         // [B]
+    __nv_bfloat16 *out;         // [B, n_q, H_q, D]
+    float *part_o;              // [C, 2, MT*16, D]
+    float *part_ml;             // [C, 2, MT*16, 2]
+    int *counters;              // [B * H_kv], zero between calls
+    int *err;
+    int B, H_q, H_kv, G, n_q, L_cap, M;
+    int head_major;             // 0: verify layout [B, L_cap, H_kv, D]; 1: draft [B, H_kv, cap, D]
+    int stages;
+    float scale_log2;           // log2(e) / sqrt(D)
+};
+
+struct Segment {
+    int b, h, ti0, ntiles, len;
+    long long pair_t0;          // global index of the pair's first tile
+};
+
+__device__ __forceinline__ int clamp_len(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
+
+// Pair and tile holding global tile t.  prefix[b] = tiles of sequences < b
+// (per KV head); pairs of sequence b occupy [H_kv*prefix[b], H_kv*prefix[b+1]).
+__device__ __forceinline__ Segment decode_tile(long long t, const int *prefix, const AttnParams &p) {
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)p.H_kv * prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    Segment s;
+    s.b = lo;
+    s.ntiles = prefix[lo + 1] - prefix[lo];
+    const long long local = t - (long long)p.H_kv * prefix[lo];
+    s.h = (int)(local / s.ntiles);
+    s.ti0 = (int)(local - (long long)s.h * s.ntiles);
+    s.pair_t0 = (long long)p.H_kv * prefix[lo] + (long long)s.h * s.ntiles;
+    s.len = clamp_len(__ldg(p.len + lo), p.L_cap);
+    return s;
+}
+
+// CTA whose range [c*T/C, (c+1)*T/C) contains tile t.
+__device__ __forceinline__ int cta_of(long long t, long long T, int C) {
+    return (int)(((t + 1) * (long long)C - 1) / T);
+}
+
+__device__ __forceinline__ long long cta_start(int c, long long T, int C) { return T * c / C; }
+
+template <int D, int MT>
+__global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                       const AttnParams p) {
+    constexpr int HALVES = D / 64;
+    constexpr int TILE_BYTES = HALVES * kHalfBytes;
+    constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    constexpr uint32_t TX_BYTES = STAGE_BYTES;
+    constexpr int NCW = 4 * MT;                    // consumer warps
+    constexpr int CS = D + 4;                      // combine buffer row stride (floats)
+    constexpr int KS = D / 16;                     // k-steps of QK^T
+    constexpr int ND = D / 8;                      // n-tiles of PV
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int stages = p.stages;
+    uint8_t *stage_base = smem;
+    float *comb = reinterpret_cast<float *>(smem + (size_t)stages * STAGE_BYTES);
+    float *red_m = comb + MT * 16 * CS;            // [MT][4][16]
+    float *red_l = red_m + MT * 64;
+    float *row_m = red_l + MT * 64;                // [MT*16]
+    float *row_l = row_m + MT * 16;
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(row_l + MT * 16);
+    uint64_t *empty_bar = full_bar + kMaxStages;
+    int *flag = reinterpret_cast<int *>(empty_bar + kMaxStages);
+    int *prefix = flag + 4;                        // [B+1]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], NCW);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        int run = 0;
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            int nt = 0;
+            if (b < p.B) nt = (clamp_len(__ldg(p.len + b), p.L_cap) + kTileN - 1) / kTileN;
+            int x = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (b < p.B) prefix[b] = run + x - nt;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) prefix[p.B] = run;
+    }
+    __syncthreads();
+
+    const long long T = (long long)p.H_kv * prefix[p.B];
+    const int C = gridDim.x, c = blockIdx.x;
+    const long long t_begin = cta_start(c, T, C), t_end = cta_start(c + 1, T, C);
+    const long long q_head_stride = (long long)p.H_q * D;   // between query tokens of one sequence
+
+    if (warp == NCW) {
+        // ------------------------------------------------------- producer (1 thread)
+        if (lane != 0) return;
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        const uint64_t pol = policy_evict_first();
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (long long t = t_begin; t < t_end && ok;) {
+            const Segment s = decode_tile(t, prefix, p);
+            const int nseg = (int)min((long long)(s.ntiles - s.ti0), t_end - t);
+            for (int i = 0; i < nseg; ++i) {
+                if (!mbar_wait(&empty_bar[stage], phase ^ 1u, p.err)) { ok = false; break; }
+                mbar_arrive_expect_tx(&full_bar[stage], TX_BYTES);
+                uint8_t *sk = stage_base + (size_t)stage * STAGE_BYTES;
+                uint8_t *sv = sk + TILE_BYTES;
+                const int pos0 = (s.ti0 + i) * kTileN;
+#pragma unroll
+                for (int hf = 0; hf < HALVES; ++hf) {
+                    if (p.head_major) {
+                        tma_load_4d(sk + hf * kHalfBytes, &tmk, hf * 64, pos0, s.h, s.b, &full_bar[stage], pol);
+                        tma_load_4d(sv + hf * kHalfBytes, &tmv, hf * 64, pos0, s.h, s.b, &full_bar[stage], pol);
+                    } else {
+                        tma_load_4d(sk + hf * kHalfBytes, &tmk, hf * 64, s.h, pos0, s.b, &full_bar[stage], pol);
+                        tma_load_4d(sv + hf * kHalfBytes, &tmv, hf * 64, s.h, pos0, s.b, &full_bar[stage], pol);
+                    }
+                }
+                ++issued;
+                if (++stage == stages) { stage = 0; phase ^= 1u; }
+            }
+            t += nseg;
+        }
+        // Drain: do not leave the CTA while copies issued here may still land.
+        int st = stage;
+        uint32_t ph = phase;
+        for (int k = 0; k < min(issued, stages); ++k) {
+            if (st == 0) { st = stages - 1; ph ^= 1u; } else { --st; }
+            mbar_wait(&full_bar[st], ph, p.err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int mt = warp >> 2, pq = warp & 3;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int ctid = tid;                          // 0 .. NCW*32-1
+    const int gtid = pq * 32 + lane;               // within the row tile's 4 warps
+    const float sl = p.scale_log2;
+    const float NEG_INF = -INFINITY;
+
+    // Sequences with nothing to attend produce zero rows.
+    for (int b = c; b < p.B; b += C) {
+        if (prefix[b + 1] != prefix[b]) continue;
+        uint4 *o = reinterpret_cast<uint4 *>(p.out + (long long)b * p.n_q * q_head_stride);
+        const int n16 = p.n_q * p.H_q * D / 8;
+        for (int i = ctid; i < n16; i += NCW * 32) o[i] = make_uint4(0, 0, 0, 0);
+    }
+
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (long long t = t_begin; t < t_end;) {
+        const Segment s = decode_tile(t, prefix, p);
+        const int nseg = (int)min((long long)(s.ntiles - s.ti0), t_end - t);
+
+        // Rows owned by this thread: r0 = mt*16+g, r1 = r0+8.  Row r is query
+        // token r / G of head h*G + r % G and sees positions <= len-n_q+r/G.
+        const int r0 = mt * 16 + g, r1 = r0 + 8;
+        const int lim0 = r0 < p.M ? s.len - p.n_q + r0 / p.G : s.len - 1;
+        const int lim1 = r1 < p.M ? s.len - p.n_q + r1 / p.G : s.len - 1;
+        const __nv_bfloat16 *qb = p.q + (long long)s.b * p.n_q * q_head_stride + (long long)s.h * p.G * D;
+        uint32_t qa[KS][4];
+        {
+            const __nv_bfloat16 *q0 = r0 < p.M ? qb + (r0 / p.G) * q_head_stride + (r0 % p.G) * D : nullptr;
+            const __nv_bfloat16 *q1 = r1 < p.M ? qb + (r1 / p.G) * q_head_stride + (r1 % p.G) * D : nullptr;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int c0 = ks * 16 + 2 * t4;
+                qa[ks][0] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0)) : 0u;
+                qa[ks][1] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0)) : 0u;
+                qa[ks][2] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0 + 8)) : 0u;
+                qa[ks][3] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0 + 8)) : 0u;
+            }
+        }
+
+        float o[ND][4];
+#pragma unroll
+        for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+        for (int i = 0; i < nseg; ++i) {
+            if (ok) ok = mbar_wait(&full_bar[stage], phase, p.err);
+            if (ok) {
+                uint8_t *kt = stage_base + (size_t)stage * STAGE_BYTES;
+                uint8_t *vt = kt + TILE_BYTES;
+                const int tile_pos = (s.ti0 + i) * kTileN;
+                if (tile_pos + kTileN > s.len) {
+                    // Rows at or past the sequence end hold whatever the cache holds
+                    // there: zero this warp's V rows so P = 0 meets finite values.
+                    for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+                        const int r = pq * 16 + idx / (D / 8), ch = idx % (D / 8);
+                        if (tile_pos + r >= s.len)
+                            *reinterpret_cast<uint4 *>(vt + (ch >> 3) * kHalfBytes + swz128(r, ch & 7)) =
+                                make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+                float sc[2][4];
+#pragma unroll
+                for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                {
+                    const int mat = lane >> 3, rr = lane & 7;
+                    const int row = pq * 16 + (mat >> 1) * 8 + rr;
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int ch = ks * 2 + (mat & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kbase + (ch >> 3) * kHalfBytes + swz128(row, ch & 7), b0, b1, b2, b3);
+                        mma_bf16(sc[0], qa[ks], b0, b1);
+                        mma_bf16(sc[1], qa[ks], b2, b3);
+                    }
+                }
+                if (tile_pos + kTileN - 1 > s.len - p.n_q) {
+                    const int pb = tile_pos + pq * 16 + 2 * t4;
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int pos = pb + n * 8 + e;
+                            if (pos > lim0) sc[n][e] = NEG_INF;
+                            if (pos > lim1) sc[n][2 + e] = NEG_INF;
+                        }
+                }
+                float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+                float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float mu0 = mn0 == NEG_INF ? 0.f : mn0, mu1 = mn1 == NEG_INF ? 0.f : mn1;
+                const float al0 = fast_exp2((m0 - mu0) * sl), al1 = fast_exp2((m1 - mu1) * sl);
+                const float ms0 = mu0 * sl, ms1 = mu1 * sl;
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    sc[n][0] = fast_exp2(fmaf(sc[n][0], sl, -ms0));
+                    sc[n][1] = fast_exp2(fmaf(sc[n][1], sl, -ms0));
+                    sc[n][2] = fast_exp2(fmaf(sc[n][2], sl, -ms1));
+                    sc[n][3] = fast_exp2(fmaf(sc[n][3], sl, -ms1));
+                }
+                l0 = l0 * al0 + (sc[0][0] + sc[0][1] + sc[1][0] + sc[1][1]);
+                l1 = l1 * al1 + (sc[0][2] + sc[0][3] + sc[1][2] + sc[1][3]);
+                m0 = mn0;
+                m1 = mn1;
+#pragma unroll
+                for (int n = 0; n < ND; ++n) {
+                    o[n][0] *= al0; o[n][1] *= al0;
+                    o[n][2] *= al1; o[n][3] *= al1;
+                }
+                uint32_t pa[4];
+                pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+                pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+                pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+                pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+                {
+                    const int mat = lane >> 3, rr = lane & 7;
+                    const int row = pq * 16 + (mat & 1) * 8 + rr;
+#pragma unroll
+                    for (int n2 = 0; n2 < D / 16; ++n2) {
+                        const int ch = n2 * 2 + (mat >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_trans(vbase + (ch >> 3) * kHalfBytes + swz128(row, ch & 7), b0, b1, b2, b3);
+                        mma_bf16(o[2 * n2], pa, b0, b1);
+                        mma_bf16(o[2 * n2 + 1], pa, b2, b3);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);
+            if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+
+        // ----------------------------------------------- merge the 4 column warps
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        float *rm = red_m + mt * 64, *rl = red_l + mt * 64;
+        if (t4 == 0) {
+            rm[pq * 16 + g] = m0; rm[pq * 16 + g + 8] = m1;
+            rl[pq * 16 + g] = l0; rl[pq * 16 + g + 8] = l1;
+        }
+        named_bar_sync(2 + mt, 128);
+        float M0 = NEG_INF, M1 = NEG_INF;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            M0 = fmaxf(M0, rm[w * 16 + g]);
+            M1 = fmaxf(M1, rm[w * 16 + g + 8]);
+        }
+        const float Mu0 = M0 == NEG_INF ? 0.f : M0, Mu1 = M1 == NEG_INF ? 0.f : M1;
+        float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            L0 += rl[w * 16 + g] * fast_exp2((rm[w * 16 + g] - Mu0) * sl);
+            L1 += rl[w * 16 + g + 8] * fast_exp2((rm[w * 16 + g + 8] - Mu1) * sl);
+        }
+        const float f0 = fast_exp2((m0 - Mu0) * sl), f1 = fast_exp2((m1 - Mu1) * sl);
+        if (pq == 0 && t4 == 0) {
+            row_m[mt * 16 + g] = M0; row_m[mt * 16 + g + 8] = M1;
+            row_l[mt * 16 + g] = L0; row_l[mt * 16 + g + 8] = L1;
+        }
+        float *cb = comb + mt * 16 * CS;
+#pragma unroll 1
+        for (int w = 0; w < 4; ++w) {
+            if (pq == w) {
+#pragma unroll
+                for (int n = 0; n < ND; ++n) {
+                    float2 *d0 = reinterpret_cast<float2 *>(cb + g * CS + n * 8 + 2 * t4);
+                    float2 *d1 = reinterpret_cast<float2 *>(cb + (g + 8) * CS + n * 8 + 2 * t4);
+                    float2 v0 = make_float2(o[n][0] * f0, o[n][1] * f0);
+                    float2 v1 = make_float2(o[n][2] * f1, o[n][3] * f1);
+                    if (w) {
+                        const float2 a = *d0, bb = *d1;
+                        v0.x += a.x; v0.y += a.y; v1.x += bb.x; v1.y += bb.y;
+                    }
+                    *d0 = v0;
+                    *d1 = v1;
+                }
+            }
+            named_bar_sync(2 + mt, 128);
+        }
+
+        // ----------------------------------------------------- write or publish
+        const int c_first = cta_of(s.pair_t0, T, C);
+        const int c_last = cta_of(s.pair_t0 + s.ntiles - 1, T, C);
+        __nv_bfloat16 *ob = p.out + (long long)s.b * p.n_q * q_head_stride + (long long)s.h * p.G * D;
+        if (c_first == c_last) {
+            for (int idx = gtid; idx < 16 * (D / 8); idx += 128) {
+                const int row = idx / (D / 8), col = (idx % (D / 8)) * 8;
+                const int r = mt * 16 + row;
+                if (r >= p.M) continue;
+                const float L = row_l[r];
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                const float *src = cb + row * CS + col;
+                uint4 pk;
+                pk.x = pack_bf16(src[0] * inv, src[1] * inv);
+                pk.y = pack_bf16(src[2] * inv, src[3] * inv);
+                pk.z = pack_bf16(src[4] * inv, src[5] * inv);
+                pk.w = pack_bf16(src[6] * inv, src[7] * inv);
+                *reinterpret_cast<uint4 *>(ob + (r / p.G) * q_head_stride + (r % p.G) * D + col) = pk;
+            }
+            named_bar_sync(2 + mt, 128);
+        } else {
+            const int slot = (t_begin >= s.pair_t0) ? 0 : 1;
+            float *po = p.part_o + ((long long)c * 2 + slot) * (MT * 16) * D;
+            float *pml = p.part_ml + ((long long)c * 2 + slot) * (MT * 16) * 2;
+            for (int idx = gtid; idx < 16 * (D / 4); idx += 128) {
+                const int row = idx / (D / 4), col = (idx % (D / 4)) * 4;
+                const float *src = cb + row * CS + col;
+                *reinterpret_cast<float4 *>(po + (mt * 16 + row) * D + col) =
+                    make_float4(src[0], src[1], src[2], src[3]);
+            }
+            if (gtid < 16) {
+                pml[(mt * 16 + gtid) * 2] = row_m[mt * 16 + gtid];
+                pml[(mt * 16 + gtid) * 2 + 1] = row_l[mt * 16 + gtid];
+            }
+            __threadfence();
+            named_bar_sync(1, NCW * 32);
+            if (ctid == 0) {
+                const int pair = s.b * p.H_kv + s.h;
+                // CTAs with an empty range (fewer tiles than CTAs) own no tile
+                // of the pair and publish nothing.
+                int n_contrib = 0;
+                for (int cc = c_first; cc <= c_last; ++cc)
+                    n_contrib += cta_start(cc + 1, T, C) > cta_start(cc, T, C);
+                const int old = atomicAdd(p.counters + pair, 1);
+                const int last = (old == n_contrib - 1);
+                if (old >= n_contrib) raise_error(p.err, kErrState);
+                if (last) {
+                    __threadfence();
+                    p.counters[pair] = 0;
+                }
+                *flag = last;
+            }
+            named_bar_sync(1, NCW * 32);
+            if (*flag) {
+                __threadfence();
+                for (int idx = ctid; idx < p.M * (D / 4); idx += NCW * 32) {
+                    const int r = idx / (D / 4), col = (idx % (D / 4)) * 4;
+                    float Mx = NEG_INF;
+                    for (int cc = c_first; cc <= c_last; ++cc) {
+                        const long long st0 = cta_start(cc, T, C);
+                        if (cta_start(cc + 1, T, C) == st0) continue;
+                        const int sl2 = st0 >= s.pair_t0 ? 0 : 1;
+                        const float *ml = p.part_ml + ((long long)cc * 2 + sl2) * (MT * 16) * 2;
+                        Mx = fmaxf(Mx, __ldcg(ml + r * 2));
+                    }
+                    const float Mu = Mx == NEG_INF ? 0.f : Mx;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float Ls = 0.f;
+                    for (int cc = c_first; cc <= c_last; ++cc) {
+                        const long long st0 = cta_start(cc, T, C);
+                        if (cta_start(cc + 1, T, C) == st0) continue;
+                        const int sl2 = st0 >= s.pair_t0 ? 0 : 1;
+                        const long long base = ((long long)cc * 2 + sl2) * (MT * 16);
+                        const float mc = __ldcg(p.part_ml + (base + r) * 2);
+                        const float lc = __ldcg(p.part_ml + (base + r) * 2 + 1);
+                        const float wgt = fast_exp2((mc - Mu) * sl);
+                        const float4 oc = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + r) * D + col));
+                        Ls += wgt * lc;
+                        acc.x += wgt * oc.x; acc.y += wgt * oc.y; acc.z += wgt * oc.z; acc.w += wgt * oc.w;
+                    }
+                    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                    uint2 pk;
+                    pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+                    pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2 *>(ob + (r / p.G) * q_head_stride + (r % p.G) * D + col) = pk;
+                }
+            }
+            named_bar_sync(1, NCW * 32);
+        }
+        t += nseg;
+    }
+}
+
+// ------------------------------------------------------------------- host side
+
+static int env_int(const char *name, int dflt) {
+    const char *s = getenv(name);
+    if (!s || !*s) return dflt;
+    return atoi(s);
+}
+
+template <int D, int MT>
+static size_t attn_fixed_smem(int B) {
+    return 1024 /* alignment slack */ + (size_t)MT * 16 * (D + 4) * 4 + (size_t)MT * 64 * 4 * 2 +
+           (size_t)MT * 16 * 4 * 2 + 2 * kMaxStages * 8 + 16 + (size_t)(B + 1) * 4;
+}
+
+template <int D>
+static constexpr size_t attn_stage_bytes() {
+    return 2 * (size_t)(D / 64) * kHalfBytes;
+}
+
+// Workspace layout: [counters: kAttnMaxPairs int32, always left zero]
+//                   [part_o: C_max * 2 * 32 * D fp32][part_ml: C_max * 2 * 32 * 2 fp32]
+// The counter region has a fixed size so that calls of any shape can share one
+// workspace: every call leaves it zeroed and nothing else is ever stored there.
+size_t attn_workspace_bytes(int B, int H_kv, int D, int M) {
+    (void)B; (void)H_kv; (void)M;
+    const int C = magicdec_host::sm_count() * 2;   // room for up to 2 CTAs per SM
+    const int MP = 32;                              // largest row tile count * 16
+    size_t counters = (size_t)kAttnMaxPairs * 4;
+    size_t po = (size_t)C * 2 * MP * D * 4;
+    size_t pml = (size_t)C * 2 * MP * 2 * 4;
+    return counters + po + pml;
+}
+
+template <int D, int MT>
+static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const CUtensorMap &tmv, int B, void *ws,
+                                   cudaStream_t st) {
+    const size_t fixed = attn_fixed_smem<D, MT>(B);
+    const size_t sb = attn_stage_bytes<D>();
+    const int smem_cap = magicdec_host::max_smem_optin();
+    int ctas_per_sm = env_int("MAGICDEC_ATTN_CTAS_PER_SM", 1);
+    if (ctas_per_sm < 1) ctas_per_sm = 1;
+    if (ctas_per_sm > 2) ctas_per_sm = 2;
+    const size_t per_cta_cap = ctas_per_sm == 1 ? (size_t)smem_cap : (size_t)(smem_cap / 2 - 1024);
+    if (per_cta_cap <= fixed) return MAGICDEC_ERR_UNSUPPORTED;
+    int stages = (int)((per_cta_cap - fixed) / sb);
+    const int want = env_int("MAGICDEC_ATTN_STAGES", 0);
+    if (want > 0 && want < stages) stages = want;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return MAGICDEC_ERR_UNSUPPORTED;
+    const size_t smem = fixed + (size_t)stages * sb;
+
+    auto kern = decode_attn_kernel<D, MT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MAGICDEC_ERR_CUDA;
+    const int C = magicdec_host::sm_count() * ctas_per_sm;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    prm.counters = reinterpret_cast<int *>(w);
+    prm.part_o = reinterpret_cast<float *>(w + (size_t)kAttnMaxPairs * 4);
+    prm.part_ml = prm.part_o + (size_t)magicdec_host::sm_count() * 2 * 2 * 32 * D;
+    prm.stages = stages;
+    prm.err = magicdec_host::device_error_word();
+    kern<<<C, (4 * MT + 1) * 32, smem, st>>>(tmk, tmv, prm);
+    return magicdec_host::launch_status();
+}
+
+// Shared launcher for draft (head_major = 1, n_q = 1) and verify attention.
+magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, int n_q, int head_major,
+                                   const void *q, const void *k, const void *v, const int32_t *len, void *out,
+                                   void *ws, cudaStream_t st) {
+    AttnParams prm{};
+    prm.q = static_cast<const __nv_bfloat16 *>(q);
+    prm.len = len;
+    prm.out = static_cast<__nv_bfloat16 *>(out);
+    prm.B = B;
+    prm.H_q = H_q;
+    prm.H_kv = H_kv;
+    prm.G = H_q / H_kv;
+    prm.n_q = n_q;
+    prm.L_cap = L_cap;
+    prm.M = prm.G * n_q;
+    prm.head_major = head_major;
+    prm.scale_log2 = kLog2e / sqrtf((float)D);
+
+    // 4-D views, innermost first.  Verify: (d, H_kv, L_cap, B); draft: (d, cap, H_kv, B).
+    CUtensorMap tmk, tmv;
+    const uint64_t e = 2;
+    uint64_t dims[4], strides[3];
+    uint32_t box[4];
+    if (head_major) {
+        dims[0] = D; dims[1] = L_cap; dims[2] = H_kv; dims[3] = B;
+        strides[0] = D * e; strides[1] = (uint64_t)L_cap * D * e; strides[2] = (uint64_t)H_kv * L_cap * D * e;
+        box[0] = 64; box[1] = kTileN; box[2] = 1; box[3] = 1;
+    } else {
+        dims[0] = D; dims[1] = H_kv; dims[2] = L_cap; dims[3] = B;
+        strides[0] = D * e; strides[1] = (uint64_t)H_kv * D * e; strides[2] = (uint64_t)L_cap * H_kv * D * e;
+        box[0] = 64; box[1] = 1; box[2] = kTileN; box[3] = 1;
+    }
+    if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box) ||
+        !magicdec_host::encode_tmap_bf16_4d(&tmv, v, dims, strides, box))
+        return MAGICDEC_ERR_CUDA;
+
+    const int MT = (prm.M + 15) / 16;
+    if (D == 128) {
+        if (MT == 1) return launch_impl<128, 1>(prm, tmk, tmv, B, ws, st);
+        if (MT == 2) return launch_impl<128, 2>(prm, tmk, tmv, B, ws, st);
+    } else if (D == 64) {
+        if (MT == 1) return launch_impl<64, 1>(prm, tmk, tmv, B, ws, st);
+        if (MT == 2) return launch_impl<64, 2>(prm, tmk, tmv, B, ws, st);
+    }
+    return MAGICDEC_ERR_UNSUPPORTED;
+}
+
+}  // namespace magicdec

@@ -59,9 +59,10 @@ def _load():
             lib.oracle_maxpool1d.argtypes = [P, I, I, P]
             lib.oracle_snapkv_select.argtypes = [I, I, I, I, I, P, P, P, I, I, I, P, P, P]
             lib.oracle_spec_accept.argtypes = [I, I, I, P, P, P, P, P, I, P, P, P]
+            lib.oracle_resample_weights.argtypes = [P, P, I, P]
             for name in ("oracle_verify_attn", "oracle_draft_attn", "oracle_streaming_select",
                          "oracle_gather_kv", "oracle_snapkv_scores", "oracle_maxpool1d",
-                         "oracle_snapkv_select", "oracle_spec_accept"):
+                         "oracle_snapkv_select", "oracle_spec_accept", "oracle_resample_weights"):
                 getattr(lib, name).restype = I
             _lib = lib
     return _lib
@@ -189,3 +190,15 @@ def spec_accept(target, draft, draft_tok, u_acc, u_res, greedy: bool):
                                       _ptr(u_acc), _ptr(u_res), int(bool(greedy)), _ptr(n_acc),
                                       _ptr(out_tok), _ptr(n_amb)), "spec_accept")
     return n_acc, out_tok, n_amb
+
+
+def resample_weights(target_row, draft_row=None) -> np.ndarray:
+    """fp64 resample weights of one position: max(0, p - q) (p when that is all zero or there is
+    no draft row), unnormalised -- the weights the accept step draws from."""
+    t = _c(target_row, np.float32)
+    V = t.shape[0]
+    d = None if draft_row is None else _c(draft_row, np.float32)
+    w = np.empty((V,), np.float64)
+    _check(_load().oracle_resample_weights(_ptr(t), None if d is None else _ptr(d), V, _ptr(w)),
+           "resample_weights")
+    return w

@@ -395,7 +395,11 @@ static void softmax_row(const float *logits, int V, double *p)
  * Inverse-CDF draw from unnormalised weights wt: the smallest t whose running
  * sum exceeds u * W, W = sum of the weights.  If rounding leaves no such t,
  * the last token with positive weight.  *amb is raised when u*W lies within
- * 1e-4 * W of the running sum at either edge of the chosen token.
+ * 1e-7 * W of the running sum at either edge of the chosen token: a single
+ * token of a 128K vocabulary is narrower than 1e-4 of the total, so the edge
+ * margin is set by the precision of a single-precision evaluation of the same
+ * sums (per-logit errors ~1e-6, normalisers and running sums carried in higher
+ * precision), not by the 1e-4 acceptance margin.
  */
 static int inverse_cdf(const double *wt, int V, double u, int *amb)
 {
@@ -403,7 +407,7 @@ static int inverse_cdf(const double *wt, int V, double u, int *amb)
     int t, last = V - 1;
     for (t = 0; t < V; ++t) W += wt[t];
     for (t = V - 1; t >= 0; --t) if (wt[t] > 0.0) { last = t; break; }
-    const double target = u * W, tol = 1e-4 * W;
+    const double target = u * W, tol = 1e-7 * W;
     for (t = 0; t < V; ++t) {
         prev = c;
         c += wt[t];
@@ -427,6 +431,38 @@ static int argmax_row(const float *logits, int V, int *amb)
 }
 
 /*
+ * Resample weights of one position: max(0, p - q) with p = softmax(target_row)
+ * and q = softmax(draft_row), or p itself when that residual is all zero or
+ * draft_row is NULL (the bonus draw).  Unnormalised; the draw takes the
+ * smallest token whose running sum exceeds u times their total.
+ */
+static void resample_weights_into(const float *target_row, const float *draft_row, int V, double *p, double *q,
+                                  double *w)
+{
+    int t;
+    double W = 0.0;
+    softmax_row(target_row, V, p);
+    if (!draft_row) {
+        for (t = 0; t < V; ++t) w[t] = p[t];
+        return;
+    }
+    softmax_row(draft_row, V, q);
+    for (t = 0; t < V; ++t) { w[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0; W += w[t]; }
+    if (!(W > 0.0)) for (t = 0; t < V; ++t) w[t] = p[t];
+}
+
+int oracle_resample_weights(const float *target_row, const float *draft_row, int V, double *w)
+{
+    if (V <= 0) return -1;
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    double *q = (double *)malloc(sizeof(double) * (size_t)V);
+    resample_weights_into(target_row, draft_row, V, p, q, w);
+    free(q);
+    free(p);
+    return 0;
+}
+
+/*
  * Accept / resample for one verification step.
  *   target [B, gamma+1, V], draft [B, gamma, V] fp32 logits; draft_tok
  *   [B, gamma]; u_acc [B, gamma] and u_res [B] uniforms in [0, 1).
@@ -440,7 +476,9 @@ static int argmax_row(const float *logits, int V, int *amb)
  *   token); at the first mismatch emit that argmax; bonus = argmax target_gamma.
  * Outputs: n_acc [B] in [0, gamma]; out_tok [B, gamma+1] holds the n_acc
  *   accepted tokens then the emitted one, -1 after; n_amb [B] (nullable)
- *   counts decisions taken within 1e-4 of their boundary.
+ *   counts decisions taken near their boundary: |u - p(x)/q(x)| < 1e-4, a
+ *   top-2 logit gap below 1e-4, or an inverse-CDF edge within 1e-7 of the
+ *   total.
  */
 int oracle_spec_accept(int B, int gamma, int V, const float *target, const float *draft,
                        const int32_t *draft_tok, const float *u_acc, const float *u_res,
@@ -452,6 +490,7 @@ int oracle_spec_accept(int B, int gamma, int V, const float *target, const float
     for (b = 0; b < B; ++b) {
         double *p = (double *)malloc(sizeof(double) * (size_t)V);
         double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        double *wt = (double *)malloc(sizeof(double) * (size_t)V);
         int32_t *out = out_tok + (long)b * (gamma + 1);
         int amb = 0, i, t, acc = gamma, emitted = -1;
         for (i = 0; i <= gamma; ++i) out[i] = -1;
@@ -478,9 +517,8 @@ int oracle_spec_accept(int B, int gamma, int V, const float *target, const float
                     ok = (p[x] > 0.0);
                 }
                 if (!ok) {
-                    double W = 0.0;
-                    for (t = 0; t < V; ++t) { q[t] = p[t] - q[t] > 0.0 ? p[t] - q[t] : 0.0; W += q[t]; }
-                    emitted = inverse_cdf(W > 0.0 ? q : p, V, u_res[b], &amb);
+                    resample_weights_into(tl, dl, V, p, q, wt);
+                    emitted = inverse_cdf(wt, V, u_res[b], &amb);
                 }
             }
             if (!ok) { acc = i; break; }
@@ -491,13 +529,14 @@ int oracle_spec_accept(int B, int gamma, int V, const float *target, const float
             if (greedy) {
                 emitted = argmax_row(tl, V, &amb);
             } else {
-                softmax_row(tl, V, p);
-                emitted = inverse_cdf(p, V, u_res[b], &amb);
+                resample_weights_into(tl, NULL, V, p, q, wt);
+                emitted = inverse_cdf(wt, V, u_res[b], &amb);
             }
         }
         out[acc] = emitted;
         n_acc[b] = acc;
         if (n_amb) n_amb[b] = amb;
+        free(wt);
         free(q);
         free(p);
     }

@@ -1,0 +1,246 @@
+"""GPU path (through the C ABI) against the CPU oracle, element by element, on seeded
+inputs small enough for the oracle to finish in seconds but spanning several 64-row
+tiles, several CTAs per sequence, ragged tails and the degenerate cases."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_self_gb300 import binding as mb
+from long_context_self_gb300 import synth
+from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, to_u16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from long_context_self_gb300 import build
+    build.build()
+    mb.lib()
+    yield
+    assert mb.magicdec_device_error() == 0
+
+
+def rand_bf16(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------- verification
+VERIFY_CASES = [
+    # B, H_q, H_kv, d, L_cap, n_q, lengths
+    (2, 4, 1, 64, 256, 3, [256, 200]),                                 # the tiny workload
+    (5, 32, 8, 128, 1500, 4, [1500, 1, 0, 64, 65]),                    # Llama-3.1-8B heads, edge lengths
+    (3, 40, 8, 128, 700, 5, [700, 333, 129]),                          # Qwen-like G=5, 25 rows
+    (3, 32, 8, 128, 900, 5, [900, 5, 640]),                            # 20 rows
+    (2, 4, 4, 128, 300, 4, [300, 257]),                                # MHA: H_kv == H_q
+    (2, 16, 2, 64, 400, 4, [400, 390]),                                # d=64, 32 rows
+    (7, 32, 8, 128, 4100, 4, [4100, 4000, 3999, 128, 2050, 17, 4033]),  # many tiles and splits
+]
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,d,L_cap,n_q,lens", VERIFY_CASES)
+def test_verify_attn_matches_oracle(B, H_q, H_kv, d, L_cap, n_q, lens):
+    q = rand_bf16((B, n_q, H_q, d), 1)
+    k = rand_bf16((B, L_cap, H_kv, d), 2)
+    v = rand_bf16((B, L_cap, H_kv, d), 3)
+    k[:, ::97] *= 4                                                    # a few dominant keys
+    sl = torch.tensor(lens, dtype=torch.int32)
+    out = mb.magicdec_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.verify_attn(to_u16(q), to_u16(k), to_u16(v), sl.numpy(), n_q)
+    check_attention(bf16_out_to_f64(out), ref, "verify")
+
+
+def test_verify_attn_is_deterministic_and_split_invariant(monkeypatch):
+    B, H_q, H_kv, d, L_cap, n_q = 6, 32, 8, 128, 3000, 4
+    q, k, v = rand_bf16((B, n_q, H_q, d), 4).to(DEV), rand_bf16((B, L_cap, H_kv, d), 5).to(DEV), \
+        rand_bf16((B, L_cap, H_kv, d), 6).to(DEV)
+    sl = torch.tensor([3000, 2999, 1500, 64, 700, 2222], dtype=torch.int32, device=DEV)
+    a = mb.magicdec_verify_attn(q, k, v, sl)
+    b = mb.magicdec_verify_attn(q, k, v, sl)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    monkeypatch.setenv("MAGICDEC_ATTN_CTAS_PER_SM", "2")
+    monkeypatch.setenv("MAGICDEC_ATTN_STAGES", "2")
+    c = mb.magicdec_verify_attn(q, k, v, sl)
+    torch.cuda.synchronize()
+    check_attention(bf16_out_to_f64(c), bf16_out_to_f64(a).astype(np.float64), "split invariance")
+
+
+# ----------------------------------------------------------------------- draft
+DRAFT_CASES = [
+    (4, 32, 8, 128, 600, [512, 600, 1, 0]),
+    (2, 4, 1, 64, 64, [64, 30]),
+    (3, 40, 8, 128, 4096, [4096, 4000, 1234]),
+]
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,d,cap,lens", DRAFT_CASES)
+def test_draft_attn_matches_oracle(B, H_q, H_kv, d, cap, lens):
+    q = rand_bf16((B, 1, H_q, d), 7)
+    kc = rand_bf16((B, H_kv, cap, d), 8)
+    vc = rand_bf16((B, H_kv, cap, d), 9)
+    dl = torch.tensor(lens, dtype=torch.int32)
+    out = mb.magicdec_draft_attn(q.to(DEV), kc.to(DEV), vc.to(DEV), dl.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.draft_attn(to_u16(q), to_u16(kc), to_u16(vc), dl.numpy())
+    check_attention(bf16_out_to_f64(out), ref, "draft")
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(out[b]) == 0
+
+
+def test_draft_attn_ignores_row_order():
+    """Attention over a set: permuting the gathered rows leaves the output unchanged."""
+    B, H_q, H_kv, d, cap = 2, 32, 8, 128, 512
+    q, kc, vc = rand_bf16((B, 1, H_q, d), 10), rand_bf16((B, H_kv, cap, d), 11), rand_bf16((B, H_kv, cap, d), 12)
+    perm = torch.randperm(cap, generator=torch.Generator().manual_seed(13))
+    dl = torch.full((B,), cap, dtype=torch.int32)
+    a = mb.magicdec_draft_attn(q.to(DEV), kc.to(DEV), vc.to(DEV), dl.to(DEV))
+    b = mb.magicdec_draft_attn(q.to(DEV), kc[:, :, perm].contiguous().to(DEV), vc[:, :, perm].contiguous().to(DEV),
+                               dl.to(DEV))
+    torch.cuda.synchronize()
+    check_attention(bf16_out_to_f64(b), bf16_out_to_f64(a), "permutation")
+
+
+# ------------------------------------------------------ StreamingLLM and gather
+@pytest.mark.parametrize("n_sink,n_recent", [(4, 60), (16, 496), (0, 32), (7, 0)])
+def test_streaming_select_bit_exact(n_sink, n_recent):
+    lens = np.array([0, 1, 5, n_sink + n_recent - 1, n_sink + n_recent, n_sink + n_recent + 3, 32000, 100000],
+                    np.int32)
+    idx, n_sel = mb.magicdec_streaming_select(torch.from_numpy(lens).to(DEV), 8, n_sink, n_recent)
+    torch.cuda.synchronize()
+    idx_o, n_sel_o = oracle.streaming_select(lens, 8, n_sink, n_recent)
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    assert np.array_equal(n_sel.cpu().numpy(), n_sel_o)
+
+
+def test_gather_bit_exact_with_padding():
+    B, L, H, d, cap = 3, 700, 8, 128, 600
+    k, v = rand_bf16((B, L, H, d), 14), rand_bf16((B, L, H, d), 15)
+    lens = np.array([700, 300, 20], np.int32)
+    idx_o, _ = oracle.streaming_select(lens, H, 16, 496)
+    kc_g, vc_g = mb.magicdec_gather_kv(k.to(DEV), v.to(DEV), torch.from_numpy(idx_o).to(DEV), cap)
+    torch.cuda.synchronize()
+    kc_o, vc_o = oracle.gather_kv(to_u16(k), to_u16(v), idx_o, cap)
+    assert np.array_equal(to_u16(kc_g), kc_o)
+    assert np.array_equal(to_u16(vc_g), vc_o)
+
+
+def test_streaming_draft_pipeline_tiny():
+    """Select -> gather -> draft attention on the tiny workload, against the oracle chain."""
+    w = synth.WORKLOADS["tiny"]
+    k, v, _ = synth.kv_cache(w, "cpu")
+    q = synth.queries(w, 1, "cpu", seed=99)
+    lens = np.array([w.L, w.L - 40], np.int32)
+    sl = torch.from_numpy(lens).to(DEV)
+    idx, n_sel = mb.magicdec_streaming_select(sl, w.H_kv, w.n_sink, w.n_recent)
+    kc, vc = mb.magicdec_gather_kv(k.to(DEV), v.to(DEV), idx, w.stream_budget)
+    out = mb.magicdec_draft_attn(q.to(DEV), kc, vc, n_sel)
+    torch.cuda.synchronize()
+    idx_o, n_sel_o = oracle.streaming_select(lens, w.H_kv, w.n_sink, w.n_recent)
+    kc_o, vc_o = oracle.gather_kv(to_u16(k), to_u16(v), idx_o, w.stream_budget)
+    ref = oracle.draft_attn(to_u16(q), kc_o, vc_o, n_sel_o)
+    check_attention(bf16_out_to_f64(out), ref, "streaming draft")
+
+
+# ---------------------------------------------------------------------- SnapKV
+SNAP_CASES = [
+    # B, H_q, H_kv, d, L_cap, w, pool, budget, lens, heavy
+    (2, 4, 1, 64, 256, 16, 7, 64, [256, 200], False),                  # the tiny workload
+    (2, 4, 1, 64, 256, 16, 7, 64, [64, 30], False),                    # L <= budget keeps everything
+    (2, 32, 8, 128, 3000, 32, 7, 512, [3000, 2500], True),             # heavy hitters, 128 window rows
+    (2, 40, 8, 128, 2100, 32, 7, 256, [2100, 1800], True),             # G=5: 160 window rows
+    (1, 32, 8, 128, 1100, 32, 7, 32, [1100], True),                    # budget == window
+]
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,d,L_cap,w,pool,budget,lens,heavy", SNAP_CASES)
+def test_snapkv_select_matches_oracle(B, H_q, H_kv, d, L_cap, w, pool, budget, lens, heavy):
+    wl = synth.Workload("case", B=B, H_q=H_q, H_kv=H_kv, d=d, L=L_cap, gamma=1, V=8, snap_window=w,
+                        snap_pool=pool, snap_budget=budget, heavy_frac=0.005 if heavy else 0.0, seed=21)
+    k, _, dirs = synth.kv_cache(wl, "cpu")
+    q_win = synth.window_queries(wl, "cpu", heavy_dirs=dirs)
+    sl = np.array(lens, np.int32)
+    idx, n_sel = mb.magicdec_snapkv_select(q_win.to(DEV), k.to(DEV), torch.from_numpy(sl).to(DEV), w, pool, budget)
+    torch.cuda.synchronize()
+    idx_o, n_sel_o, pooled = oracle.snapkv_select(to_u16(q_win), to_u16(k), sl, pool, budget)
+    band = check_topk(idx.cpu().numpy(), n_sel.cpu().numpy(), idx_o, n_sel_o, pooled, sl, w, budget)
+    # max-pooling copies each local maximum to up to `pool` neighbours, so a
+    # plateau or two at the threshold per (sequence, KV head) is expected
+    assert band <= 2 * pool * B * H_kv + 8, f"too many band positions: {band}"
+
+
+# ------------------------------------------------------------------ acceptance
+ACCEPT_CASES = [
+    ("tiny", 64, False), ("tiny", 64, True),
+    ("llama8b_b128_l32k", 24, False), ("llama8b_b128_l32k", 24, True),
+    ("qwen32b_b16_l100k", 8, False),
+]
+
+
+@pytest.mark.parametrize("name,B,greedy", ACCEPT_CASES)
+def test_spec_accept_matches_oracle(name, B, greedy):
+    w = synth.WORKLOADS[name]
+    target, draft, tok, u_acc, u_res = synth.logits(w, "cpu", B=B, seed=31)
+    if greedy:
+        # make the chain non-trivial: half the draft tokens are the target argmax
+        am = target[:, : w.gamma].argmax(-1).to(torch.int32)
+        pick = torch.rand(tok.shape, generator=torch.Generator().manual_seed(5)) < 0.7
+        tok = torch.where(pick, am, tok)
+    got = mb.magicdec_spec_accept(target.to(DEV), draft.to(DEV), tok.to(DEV), u_acc.to(DEV), u_res.to(DEV), greedy)
+    torch.cuda.synchronize()
+    ref = oracle.spec_accept(target.numpy(), draft.numpy(), tok.numpy(), u_acc.numpy(), u_res.numpy(), greedy)
+    gpu = tuple(t.cpu().numpy() for t in got)
+    n_amb = check_accept(gpu, ref, name, inputs=(target.numpy(), draft.numpy(), u_res.numpy()))
+    assert n_amb <= max(2, B // 4)
+
+
+def test_spec_accept_edge_tokens():
+    """Out-of-range draft tokens are rejected; gamma = 0 only draws the bonus token."""
+    B, V = 8, 40
+    g = torch.Generator().manual_seed(3)
+    target = torch.randn((B, 3, V), generator=g) * 2
+    draft = target[:, :2] + torch.randn((B, 2, V), generator=g) * 0.5
+    tok = torch.randint(0, V, (B, 2), generator=g, dtype=torch.int32)
+    tok[0, 0] = -3
+    tok[1, 0] = V + 5
+    u_acc, u_res = torch.rand((B, 2), generator=g), torch.rand((B,), generator=g)
+    got = mb.magicdec_spec_accept(target.to(DEV), draft.to(DEV), tok.to(DEV), u_acc.to(DEV), u_res.to(DEV), False)
+    torch.cuda.synchronize()
+    ref = oracle.spec_accept(target.numpy(), draft.numpy(), tok.numpy(), u_acc.numpy(), u_res.numpy(), False)
+    check_accept(tuple(t.cpu().numpy() for t in got), ref)
+    assert got[0][0].item() == 0 and got[0][1].item() == 0
+    t0 = target[:, :1].contiguous()
+    got0 = mb.magicdec_spec_accept(t0.to(DEV), None, torch.zeros((B, 0), dtype=torch.int32, device=DEV),
+                                   torch.zeros((B, 0), device=DEV), u_res.to(DEV), False)
+    torch.cuda.synchronize()
+    ref0 = oracle.spec_accept(t0.numpy(), np.zeros((B, 0, V), np.float32), np.zeros((B, 0), np.int32),
+                              np.zeros((B, 0), np.float32), u_res.numpy(), False)
+    check_accept(tuple(t.cpu().numpy() for t in got0), ref0, "gamma=0")
+
+
+def test_rows_past_the_length_never_reach_the_output():
+    """Cache rows at or beyond a sequence's length may hold anything (here NaN): outputs
+    must equal the oracle's, which never reads them."""
+    B, H_q, H_kv, d, L_cap, n_q = 3, 32, 8, 128, 500, 4
+    q, k, v = rand_bf16((B, n_q, H_q, d), 40), rand_bf16((B, L_cap, H_kv, d), 41), rand_bf16((B, L_cap, H_kv, d), 42)
+    lens = [437, 64, 130]
+    for b, L in enumerate(lens):
+        k[b, L:] = float("nan")
+        v[b, L:] = float("nan")
+    sl = torch.tensor(lens, dtype=torch.int32)
+    out = mb.magicdec_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV))
+    kc, vc = k.transpose(1, 2).contiguous(), v.transpose(1, 2).contiguous()
+    dout = mb.magicdec_draft_attn(q[:, -1:].contiguous().to(DEV), kc.to(DEV), vc.to(DEV), sl.to(DEV))
+    torch.cuda.synchronize()
+    check_attention(bf16_out_to_f64(out), oracle.verify_attn(to_u16(q), to_u16(k), to_u16(v), sl.numpy(), n_q),
+                    "verify with NaN tail")
+    check_attention(bf16_out_to_f64(dout), oracle.draft_attn(to_u16(q[:, -1:]), to_u16(kc), to_u16(vc), sl.numpy()),
+                    "draft with NaN tail")
