@@ -164,6 +164,29 @@ MAGICDEC_API magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n
                                      const uint16_t *v, const int32_t *seq_len, uint16_t *out, void *ws,
                                      size_t ws_bytes, void *stream);
 
+/*
+ * Verification attention that allocates nothing (no counterpart in the paper;
+ * an addition for callers that cannot allocate device memory, such as a
+ * plug-in that receives only its input and output buffers from a host
+ * runtime, an engine whose memory plan is fixed before it starts, or a
+ * process whose device memory is owned by another allocator).  Same
+ * arguments, layouts and results as magicdec_verify_attn, without `ws`: its
+ * scratch is a 16 MiB array inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address and synchronously zeroes the part that must
+ *    start at zero (the merge counters); make that first
+ *    call before any stream capture.
+ *  - All calls on a device share the array and leave it ready for the next
+ *    call; calls that overlap on the GPU race, so order them (one stream).
+ *  - Returns MAGICDEC_ERR_UNSUPPORTED, and enqueues nothing, when the
+ *    kernel's scratch for the current device would not fit in the array.
+ * Errors otherwise as magicdec_verify_attn.
+ */
+MAGICDEC_API magicdec_status magicdec_verify_attn_noalloc(magicdec_kv_shape shape, int n_q, const uint16_t *q,
+                                                          const uint16_t *k, const uint16_t *v,
+                                                          const int32_t *seq_len, uint16_t *out, void *stream);
+
 /* Workspace bytes magicdec_spec_accept needs. */
 MAGICDEC_API size_t magicdec_spec_accept_workspace_size(int B, int gamma, int V);
 

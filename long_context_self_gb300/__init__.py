@@ -23,5 +23,6 @@ from .binding import (  # noqa: F401
     magicdec_spec_accept_workspace_size,
     magicdec_streaming_select,
     magicdec_verify_attn,
+    magicdec_verify_attn_noalloc,
     status_string,
 )

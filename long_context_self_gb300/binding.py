@@ -47,6 +47,7 @@ _SIGNATURES = {
     "magicdec_attn_workspace_size": ([KVShape, _I], _S),
     "magicdec_draft_attn": ([KVShape, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "magicdec_verify_attn": ([KVShape, _I, _P, _P, _P, _P, _P, _P, _S, _P], _I),
+    "magicdec_verify_attn_noalloc": ([KVShape, _I, _P, _P, _P, _P, _P, _P], _I),
     "magicdec_spec_accept_workspace_size": ([_I, _I, _I], _S),
     "magicdec_spec_accept": ([_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P], _I),
 }
@@ -251,6 +252,28 @@ def magicdec_verify_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_
     _check("magicdec_verify_attn",
            lib().magicdec_verify_attn(shape, n_q, _ptr(q), _ptr(k), _ptr(v), _ptr(seq_len), _ptr(out), _ptr(ws),
                                       ws.numel() * ws.element_size(), _stream(stream, dev)))
+    return out
+
+
+def magicdec_verify_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_len: torch.Tensor,
+                                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Verification attention whose scratch lives inside the library (for callers that
+    cannot allocate device memory); same shapes and results as magicdec_verify_attn."""
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev)
+    _need(seq_len, "seq_len", torch.int32, dev)
+    B, n_q, H_q, d = q.shape
+    L_cap, H_kv = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("q / k / v shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    _check("magicdec_verify_attn_noalloc",
+           lib().magicdec_verify_attn_noalloc(kv_shape(B, H_q, H_kv, d, L_cap), n_q, _ptr(q), _ptr(k), _ptr(v),
+                                              _ptr(seq_len), _ptr(out), _stream(stream, dev)))
     return out
 
 
