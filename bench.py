@@ -61,6 +61,23 @@ def expected_tokens(alpha: float, gamma: int) -> float:
     return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank float over the process group (identity without one)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world: int, steps: int, ms_max: float) -> float:
+    """Whole-job steps/s: every rank runs `steps` steps of its own batch; the job takes the
+    slowest rank's time."""
+    return world * steps / (ms_max * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -283,11 +300,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             pipe.step(record=True)
         t1.record(stream)
         torch.cuda.synchronize()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), device)
     ms_step = ms_total / args.steps
     ver_ms = statistics.mean(a.elapsed_time(b) for a, b in pipe.verify_events)
     dra_ms = statistics.mean(a.elapsed_time(b) for a, b in pipe.draft_events)
@@ -342,11 +355,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), device)
     err_word = mb.magicdec_device_error()
 
     peak, peak_kind = load_peaks()
@@ -356,7 +365,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     traffic = recorded_traffic(args.workload)
     result = {
         "metric": METRIC,
-        "value": round(world * args.steps / (ms_total * 1e-3), 4),
+        "value": round(aggregate_rate(world, args.steps, ms_total), 4),
         "unit": "steps/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -388,7 +397,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "tokens_per_s_synthetic": round(world * w.B * omega_hat * args.steps / (ms_total * 1e-3), 1),
         "gpu_launches": pipe.launches_per_step * args.steps,
         "device_error_word": err_word,
-        "e2e": {"value": round(world * args.steps / (e2e_ms * 1e-3), 4), "unit": "steps/s",
+        "e2e": {"value": round(aggregate_rate(world, args.steps, e2e_ms), 4), "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "clocks": clocks.summary(),
     }

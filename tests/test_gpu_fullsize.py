@@ -1,0 +1,128 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+Each workload runs the whole call at full size on the GPU (B up to 128, L up to
+100000, V up to 152064); the oracle recomputes sampled outputs one (sequence, KV head)
+pair or one sequence at a time from host copies of exactly the bytes the GPU read:
+  * verification attention: every query row of sampled pairs;
+  * StreamingLLM selection + gather + draft attention: sampled sequences;
+  * SnapKV selection: sampled pairs (band rule at the k-th pooled score);
+  * speculative accept: every sequence of the batch (sampling mode) or a sample (greedy).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_self_gb300 import binding as mb
+from long_context_self_gb300 import synth
+from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, to_u16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from long_context_self_gb300 import build
+    build.build()
+    mb.lib()
+    yield
+    torch.cuda.empty_cache()
+    assert mb.magicdec_device_error() == 0
+
+
+def sample_pairs(w, n, seed):
+    rng = np.random.default_rng(seed)
+    bs = rng.choice(w.B, size=min(n, w.B), replace=False)
+    return [(int(b), int(rng.integers(w.H_kv))) for b in bs]
+
+
+def check_verify_pairs(w, q, k, v, sl, out, pairs):
+    G = w.G
+    for b, h in pairs:
+        L = int(sl[b])
+        qo = to_u16(q[b:b + 1, :, h * G:(h + 1) * G])
+        ko = to_u16(k[b:b + 1, :L, h:h + 1])
+        vo = to_u16(v[b:b + 1, :L, h:h + 1])
+        ref = oracle.verify_attn(qo, ko, vo, np.array([L], np.int32), w.n_q)
+        got = bf16_out_to_f64(out[b:b + 1, :, h * G:(h + 1) * G])
+        check_attention(got, ref, f"{w.name} verify b={b} h={h}")
+
+
+@pytest.mark.parametrize("name", ["llama8b_b32_l32k", "llama8b_b64_l32k_snapkv", "llama8b_b128_l32k",
+                                  "qwen32b_b16_l100k"])
+def test_fullsize_verify_attn_sampled(name):
+    w = synth.WORKLOADS[name]
+    k, v, _ = synth.kv_cache(w, DEV)
+    q = synth.queries(w, w.n_q, DEV, seed=w.seed * 7 + 2)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=DEV)
+    out = mb.magicdec_verify_attn(q, k, v, sl)
+    torch.cuda.synchronize()
+    check_verify_pairs(w, q, k, v, sl.cpu().numpy(), out, sample_pairs(w, 3, w.seed))
+    del k, v
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["llama8b_b32_l32k", "llama8b_b128_l32k"])
+def test_fullsize_streaming_draft_sampled(name):
+    w = synth.WORKLOADS[name]
+    k, v, _ = synth.kv_cache(w, DEV)
+    qd = synth.queries(w, 1, DEV, seed=w.seed * 7 + 1)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=DEV)
+    idx, n_sel = mb.magicdec_streaming_select(sl, w.H_kv, w.n_sink, w.n_recent)
+    kc, vc = mb.magicdec_gather_kv(k, v, idx, w.stream_budget)
+    out = mb.magicdec_draft_attn(qd, kc, vc, n_sel)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(w.seed + 5)
+    for b in rng.choice(w.B, size=3, replace=False):
+        b = int(b)
+        L = int(sl[b])
+        idx_o, n_sel_o = oracle.streaming_select(np.array([L], np.int32), w.H_kv, w.n_sink, w.n_recent)
+        assert np.array_equal(idx[b:b + 1].cpu().numpy(), idx_o)
+        assert int(n_sel[b]) == int(n_sel_o[0])
+        # the gather reads only the selected rows: rebuild them on the host from the same cache bytes
+        kc_o, vc_o = oracle.gather_kv(to_u16(k[b:b + 1]), to_u16(v[b:b + 1]), idx_o, w.stream_budget)
+        assert np.array_equal(to_u16(kc[b:b + 1]), kc_o)
+        assert np.array_equal(to_u16(vc[b:b + 1]), vc_o)
+        ref = oracle.draft_attn(to_u16(qd[b:b + 1]), kc_o, vc_o, n_sel_o)
+        check_attention(bf16_out_to_f64(out[b:b + 1]), ref, f"{name} draft b={b}")
+    del k, v, kc, vc
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["llama8b_b64_l32k_snapkv", "llama8b_b128_l32k", "qwen32b_b16_l100k"])
+def test_fullsize_snapkv_select_sampled(name):
+    w = synth.WORKLOADS[name]
+    k, v, dirs = synth.kv_cache(w, DEV)
+    del v
+    q_win = synth.window_queries(w, DEV, heavy_dirs=dirs)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=DEV)
+    idx, n_sel = mb.magicdec_snapkv_select(q_win, k, sl, w.snap_window, w.snap_pool, w.snap_budget)
+    torch.cuda.synchronize()
+    G = w.G
+    band = 0
+    for b, h in sample_pairs(w, 2, w.seed + 9):
+        L = int(sl[b])
+        qo = to_u16(q_win[b:b + 1, :, h * G:(h + 1) * G])
+        ko = to_u16(k[b:b + 1, :L, h:h + 1])
+        sl_o = np.array([L], np.int32)
+        idx_o, n_sel_o, pooled = oracle.snapkv_select(qo, ko, sl_o, w.snap_pool, w.snap_budget)
+        band += check_topk(idx[b:b + 1, h:h + 1].cpu().numpy(), n_sel[b:b + 1].cpu().numpy(), idx_o, n_sel_o,
+                           pooled, sl_o, w.snap_window, w.snap_budget)
+    assert band <= 4 * w.snap_pool + 8
+    del k
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,greedy", [("llama8b_b128_l32k", False), ("llama8b_b128_l32k", True),
+                                         ("llama8b_b64_l32k_snapkv", False), ("qwen32b_b16_l100k", False)])
+def test_fullsize_spec_accept(name, greedy):
+    w = synth.WORKLOADS[name]
+    target, draft, tok, u_acc, u_res = synth.logits(w, DEV)
+    got = mb.magicdec_spec_accept(target, draft, tok, u_acc, u_res, greedy)
+    torch.cuda.synchronize()
+    t, d, x, ua, ur = (a.cpu().numpy() for a in (target, draft, tok, u_acc, u_res))
+    ref = oracle.spec_accept(t, d, x, ua, ur, greedy)
+    n_amb = check_accept(tuple(a.cpu().numpy() for a in got), ref, name, inputs=(t, d, ur))
+    assert n_amb <= max(2, w.B // 8)
