@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
     __shared__ double red_d[kAccThreads / 32];
     __shared__ float chunk_max;
     const int chunk = blockIdx.x, row = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
     const int b = row / p.rows_per_b, r = row % p.rows_per_b;
     const float *x = row_ptr(p, b, r);
     const int t0 = chunk * kAccChunk, t1 = min(t0 + kAccChunk, p.V);
@@ -246,6 +248,8 @@ __device__ RowAll row_stat(const AcceptParams &p, int b, int r) {
 // One thread per sequence (the chain is sequential; each step touches a few
 // chunk records and two logits).
 __global__ void accept_chain_kernel(const AcceptParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= p.B) return;
     const int gamma = p.gamma, V = p.V;
@@ -349,6 +353,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const Accept
     __shared__ double seg[kAccThreads];
     __shared__ int is_last;
     const int chunk = blockIdx.x, b = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
     const JobInfo job = p.job[b];
     if (job.kind == 0) return;
     WeightCtx w;
@@ -498,10 +504,12 @@ magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target,
     w += align256a((size_t)B * sizeof(JobInfo));
     prm.chunk_sum = reinterpret_cast<double *>(w);
 
-    accept_stats_kernel<<<dim3(prm.n_chunks, B * prm.rows_per_b), kAccThreads, 0, st>>>(prm);
-    accept_chain_kernel<<<(B + 127) / 128, 128, 0, st>>>(prm);
-    if (!greedy) accept_sample_kernel<<<dim3(prm.n_chunks, B), kAccThreads, 0, st>>>(prm);
-    return magicdec_host::launch_status();
+    magicdec_status s = magicdec_host::launch_pdl(accept_stats_kernel, dim3(prm.n_chunks, B * prm.rows_per_b),
+                                                  dim3(kAccThreads), 0, st, prm);
+    if (s != MAGICDEC_OK) return s;
+    s = magicdec_host::launch_pdl(accept_chain_kernel, dim3((B + 127) / 128), dim3(128), 0, st, prm);
+    if (s != MAGICDEC_OK || greedy) return s;
+    return magicdec_host::launch_pdl(accept_sample_kernel, dim3(prm.n_chunks, B), dim3(kAccThreads), 0, st, prm);
 }
 
 }  // namespace magicdec

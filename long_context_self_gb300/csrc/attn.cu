@@ -89,11 +89,13 @@ __device__ __forceinline__ long long cta_start(int c, long long T, int C) { retu
 template <int D, int MT>
 __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                       const AttnParams p) {
+                       const __grid_constant__ CUtensorMap tmq, const AttnParams p) {
     constexpr int HALVES = D / 64;
     constexpr int TILE_BYTES = HALVES * kHalfBytes;
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     constexpr uint32_t TX_BYTES = STAGE_BYTES;
+    constexpr int QHALF = MT * 16 * 128;           // one 64-channel half of the query rows
+    constexpr int QSLOT = HALVES * QHALF;
     constexpr int NCW = 4 * MT;                    // consumer warps
     constexpr int CS = D + 4;                      // combine buffer row stride (floats)
     constexpr int KS = D / 16;                     // k-steps of QK^T
@@ -103,31 +105,50 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int stages = p.stages;
     uint8_t *stage_base = smem;
-    float *comb = reinterpret_cast<float *>(smem + (size_t)stages * STAGE_BYTES);
+    uint8_t *qslots = smem + (size_t)stages * STAGE_BYTES;   // 2 slots, ring of segment queries
+    float *comb = reinterpret_cast<float *>(qslots + 2 * QSLOT);
     float *red_m = comb + MT * 16 * CS;            // [MT][4][16]
     float *red_l = red_m + MT * 64;
     float *row_m = red_l + MT * 64;                // [MT*16]
     float *row_l = row_m + MT * 16;
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(row_l + MT * 16);
     uint64_t *empty_bar = full_bar + kMaxStages;
-    int *flag = reinterpret_cast<int *>(empty_bar + kMaxStages);
+    uint64_t *qfull_bar = empty_bar + kMaxStages;  // [2]
+    uint64_t *qempty_bar = qfull_bar + 2;          // [2]
+    int *flag = reinterpret_cast<int *>(qempty_bar + 2);
     int *prefix = flag + 4;                        // [B+1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    pdl_trigger();
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], NCW);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qfull_bar[s], 1);
+            mbar_init(&qempty_bar[s], NCW);
+        }
         mbar_fence_init();
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        prefetch_tensormap(&tmq);
     }
+    // Query rows past M stay zero in both slots (the TMA box writes rows < M only).
+    for (int i = tid; i < 2 * QSLOT / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(qslots)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    pdl_wait();
+    // Tiles per sequence, loaded in parallel, then an exclusive scan by warp 0.
+    for (int b = tid; b < p.B; b += blockDim.x)
+        prefix[b] = (clamp_len(__ldg(p.len + b), p.L_cap) + kTileN - 1) / kTileN;
+    __syncthreads();
     if (warp == 0) {
         int run = 0;
         for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
-            int nt = 0;
-            if (b < p.B) nt = (clamp_len(__ldg(p.len + b), p.L_cap) + kTileN - 1) / kTileN;
+            const int nt = b < p.B ? prefix[b] : 0;
             int x = nt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -149,16 +170,26 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     if (warp == NCW) {
         // ------------------------------------------------------- producer (1 thread)
         if (lane != 0) return;
-        prefetch_tensormap(&tmk);
-        prefetch_tensormap(&tmv);
         const uint64_t pol = policy_evict_first();
+        const uint64_t pol_q = policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;
-        int issued = 0;
+        int issued = 0, seg_no = 0, q_issued = 0;
         bool ok = true;
-        for (long long t = t_begin; t < t_end && ok;) {
+        for (long long t = t_begin; t < t_end && ok; ++seg_no) {
             const Segment s = decode_tile(t, prefix, p);
             const int nseg = (int)min((long long)(s.ntiles - s.ti0), t_end - t);
+            {
+                // the segment's G*n_q query rows, one box per 64-channel half
+                const int qs = seg_no & 1;
+                if (!mbar_wait(&qempty_bar[qs], ((seg_no >> 1) & 1) ^ 1u, p.err)) { ok = false; break; }
+                mbar_arrive_expect_tx(&qfull_bar[qs], HALVES * p.M * 128);
+#pragma unroll
+                for (int hf = 0; hf < HALVES; ++hf)
+                    tma_load_4d(qslots + qs * QSLOT + hf * QHALF, &tmq, hf * 64, s.h * p.G, 0, s.b, &qfull_bar[qs],
+                                pol_q);
+                ++q_issued;
+            }
             for (int i = 0; i < nseg; ++i) {
                 if (!mbar_wait(&empty_bar[stage], phase ^ 1u, p.err)) { ok = false; break; }
                 mbar_arrive_expect_tx(&full_bar[stage], TX_BYTES);
@@ -187,6 +218,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
             if (st == 0) { st = stages - 1; ph ^= 1u; } else { --st; }
             mbar_wait(&full_bar[st], ph, p.err);
         }
+        for (int k = max(0, q_issued - 2); k < q_issued; ++k) mbar_wait(&qfull_bar[k & 1], (k >> 1) & 1, p.err);
         return;
     }
 
@@ -206,10 +238,10 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         for (int i = ctid; i < n16; i += NCW * 32) o[i] = make_uint4(0, 0, 0, 0);
     }
 
-    int stage = 0;
+    int stage = 0, seg_no = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (long long t = t_begin; t < t_end;) {
+    for (long long t = t_begin; t < t_end; ++seg_no) {
         const Segment s = decode_tile(t, prefix, p);
         const int nseg = (int)min((long long)(s.ntiles - s.ti0), t_end - t);
 
@@ -218,19 +250,20 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         const int r0 = mt * 16 + g, r1 = r0 + 8;
         const int lim0 = r0 < p.M ? s.len - p.n_q + r0 / p.G : s.len - 1;
         const int lim1 = r1 < p.M ? s.len - p.n_q + r1 / p.G : s.len - 1;
-        const __nv_bfloat16 *qb = p.q + (long long)s.b * p.n_q * q_head_stride + (long long)s.h * p.G * D;
         uint32_t qa[KS][4];
         {
-            const __nv_bfloat16 *q0 = r0 < p.M ? qb + (r0 / p.G) * q_head_stride + (r0 % p.G) * D : nullptr;
-            const __nv_bfloat16 *q1 = r1 < p.M ? qb + (r1 / p.G) * q_head_stride + (r1 % p.G) * D : nullptr;
+            const int qs = seg_no & 1;
+            if (ok) ok = mbar_wait(&qfull_bar[qs], (seg_no >> 1) & 1, p.err);
+            const uint32_t qbase = smem_u32(qslots + qs * QSLOT);
+            const int mat = lane >> 3, rr = lane & 7;
+            const int row = mt * 16 + (mat & 1) * 8 + rr;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const int c0 = ks * 16 + 2 * t4;
-                qa[ks][0] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0)) : 0u;
-                qa[ks][1] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0)) : 0u;
-                qa[ks][2] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0 + 8)) : 0u;
-                qa[ks][3] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0 + 8)) : 0u;
+                const int ch = ks * 2 + (mat >> 1);
+                ldsm_x4(qbase + (ch >> 3) * QHALF + swz128(row, ch & 7), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qempty_bar[qs]);
         }
 
         float o[ND][4];
@@ -485,8 +518,9 @@ static int env_int(const char *name, int dflt) {
 
 template <int D, int MT>
 static size_t attn_fixed_smem(int B) {
-    return 1024 /* alignment slack */ + (size_t)MT * 16 * (D + 4) * 4 + (size_t)MT * 64 * 4 * 2 +
-           (size_t)MT * 16 * 4 * 2 + 2 * kMaxStages * 8 + 16 + (size_t)(B + 1) * 4;
+    return 1024 /* alignment slack */ + 2 * (size_t)(D / 64) * MT * 16 * 128 /* query ring */ +
+           (size_t)MT * 16 * (D + 4) * 4 + (size_t)MT * 64 * 4 * 2 + (size_t)MT * 16 * 4 * 2 +
+           (2 * kMaxStages + 4) * 8 + 16 + (size_t)(B + 1) * 4;
 }
 
 template <int D>
@@ -509,8 +543,8 @@ size_t attn_workspace_bytes(int B, int H_kv, int D, int M) {
 }
 
 template <int D, int MT>
-static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const CUtensorMap &tmv, int B, void *ws,
-                                   cudaStream_t st) {
+static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   const CUtensorMap &tmq, int B, void *ws, cudaStream_t st) {
     const size_t fixed = attn_fixed_smem<D, MT>(B);
     const size_t sb = attn_stage_bytes<D>();
     const int smem_cap = magicdec_host::max_smem_optin();
@@ -536,8 +570,7 @@ static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const
     prm.part_ml = prm.part_o + (size_t)magicdec_host::sm_count() * 2 * 2 * 32 * D;
     prm.stages = stages;
     prm.err = magicdec_host::device_error_word();
-    kern<<<C, (4 * MT + 1) * 32, smem, st>>>(tmk, tmv, prm);
-    return magicdec_host::launch_status();
+    return magicdec_host::launch_pdl(kern, dim3(C), dim3((4 * MT + 1) * 32), smem, st, tmk, tmv, tmq, prm);
 }
 
 // Shared launcher for draft (head_major = 1, n_q = 1) and verify attention.
@@ -575,14 +608,20 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
     if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box) ||
         !magicdec_host::encode_tmap_bf16_4d(&tmv, v, dims, strides, box))
         return MAGICDEC_ERR_CUDA;
+    // Queries as (d, H_q, n_q, B); one box = the G*n_q rows of a KV group, rows ordered i*G + g.
+    CUtensorMap tmq;
+    const uint64_t qdims[4] = {(uint64_t)D, (uint64_t)H_q, (uint64_t)n_q, (uint64_t)B};
+    const uint64_t qstrides[3] = {(uint64_t)D * e, (uint64_t)H_q * D * e, (uint64_t)n_q * H_q * D * e};
+    const uint32_t qbox[4] = {64, (uint32_t)prm.G, (uint32_t)n_q, 1};
+    if (!magicdec_host::encode_tmap_bf16_4d(&tmq, q, qdims, qstrides, qbox)) return MAGICDEC_ERR_CUDA;
 
     const int MT = (prm.M + 15) / 16;
     if (D == 128) {
-        if (MT == 1) return launch_impl<128, 1>(prm, tmk, tmv, B, ws, st);
-        if (MT == 2) return launch_impl<128, 2>(prm, tmk, tmv, B, ws, st);
+        if (MT == 1) return launch_impl<128, 1>(prm, tmk, tmv, tmq, B, ws, st);
+        if (MT == 2) return launch_impl<128, 2>(prm, tmk, tmv, tmq, B, ws, st);
     } else if (D == 64) {
-        if (MT == 1) return launch_impl<64, 1>(prm, tmk, tmv, B, ws, st);
-        if (MT == 2) return launch_impl<64, 2>(prm, tmk, tmv, B, ws, st);
+        if (MT == 1) return launch_impl<64, 1>(prm, tmk, tmv, tmq, B, ws, st);
+        if (MT == 2) return launch_impl<64, 2>(prm, tmk, tmv, tmq, B, ws, st);
     }
     return MAGICDEC_ERR_UNSUPPORTED;
 }

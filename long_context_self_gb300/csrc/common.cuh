@@ -10,6 +10,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/magicdec.h"
 
 namespace magicdec {
@@ -144,6 +146,14 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Programmatic dependent launch: every kernel of the library is launched
+// with programmatic stream serialisation, so it may start while the previous
+// kernel in the stream drains.  pdl_wait() blocks until the previous grid has
+// completed and its memory is visible; nothing a previous kernel may have
+// written is read before it.  pdl_trigger() lets the next grid launch early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------- named barriers
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     __syncwarp();
@@ -222,6 +232,25 @@ bool encode_tmap_bf16_4d(CUtensorMap *map, const void *base, const uint64_t dims
 inline magicdec_status launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? MAGICDEC_OK : MAGICDEC_ERR_CUDA;
+}
+
+// Launch with programmatic stream serialisation (the kernel must call
+// magicdec::pdl_wait() before reading anything an earlier kernel wrote).
+template <typename... KArgs, typename... Args>
+inline magicdec_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                  Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess) return MAGICDEC_ERR_CUDA;
+    return launch_status();
 }
 
 }  // namespace magicdec_host

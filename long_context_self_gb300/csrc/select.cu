@@ -31,6 +31,8 @@ __device__ __forceinline__ int clamp_len_s(int v, int hi) { return v < 0 ? 0 : (
 // ------------------------------------------------------------ StreamingLLM
 __global__ void streaming_select_kernel(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
                                         int32_t *idx, int32_t *n_sel) {
+    pdl_trigger();
+    pdl_wait();
     const int width = n_sink + n_recent;
     const long long total = (long long)B * H_kv * width;
     for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
@@ -50,32 +52,46 @@ __global__ void streaming_select_kernel(const int32_t *seq_len, int B, int H_kv,
 }
 
 // ------------------------------------------------------------------ gather
-// One thread per 16-byte chunk of a destination row (K and V interleaved).
-__global__ void gather_kv_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
-                                 const int32_t *__restrict__ idx, int B, int H_kv, int D, int L_cap, int n_idx,
-                                 int cap, uint4 *__restrict__ kc, uint4 *__restrict__ vc) {
-    const int cpr = D / 8;                            // 16-byte chunks per row
-    const long long rows = (long long)B * H_kv * n_idx;
-    const long long total = rows * cpr * 2;
-    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
-         t += (long long)gridDim.x * blockDim.x) {
-        const int ch = (int)(t % cpr);
-        const int kv = (int)((t / cpr) & 1);
-        const long long row = t / (2 * cpr);        // (b*H_kv + h)*n_idx + i
-        const int i = (int)(row % n_idx);
-        const long long bh = row / n_idx;
-        const int h = (int)(bh % H_kv);
-        const int b = (int)(bh / H_kv);
-        const int pos = __ldg(idx + row);
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (pos >= 0 && pos < L_cap) {
-            const uint4 *src = (kv ? v : k) + (((long long)b * L_cap + pos) * H_kv + h) * cpr + ch;
-            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "l"(src));
+// Unit u = one 16-byte chunk of one destination row of K or V:
+//   ch = u % CPR, kv = (u / CPR) % 2, row = u / (2*CPR) = (b*H_kv + h)*n_idx + i.
+// Each thread moves UNROLL units per iteration so that many loads are in flight.
+template <int CPR>
+__global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                       const int32_t *__restrict__ idx, int H_kv, int L_cap,
+                                                       int n_idx, int cap, unsigned total,
+                                                       uint4 *__restrict__ kc, uint4 *__restrict__ vc) {
+    constexpr int UNROLL = 4;
+    pdl_trigger();
+    pdl_wait();
+    const unsigned stride = gridDim.x * blockDim.x;
+    for (unsigned base = blockIdx.x * blockDim.x + threadIdx.x; base < total; base += stride * UNROLL) {
+        uint4 val[UNROLL];
+        uint4 *dst[UNROLL];
+#pragma unroll
+        for (int j = 0; j < UNROLL; ++j) {
+            const unsigned u = base + j * stride;
+            dst[j] = nullptr;
+            val[j] = make_uint4(0, 0, 0, 0);
+            if (u < total) {
+                const unsigned ch = u % CPR;
+                const unsigned kv = (u / CPR) & 1u;
+                const unsigned row = u / (2 * CPR);
+                const unsigned bh = row / (unsigned)n_idx;
+                const unsigned i = row - bh * (unsigned)n_idx;
+                const unsigned h = bh % (unsigned)H_kv, b = bh / (unsigned)H_kv;
+                const int pos = __ldg(idx + row);
+                if (pos >= 0 && pos < L_cap) {
+                    const uint4 *src = (kv ? v : k) + (((size_t)b * L_cap + pos) * H_kv + h) * CPR + ch;
+                    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(val[j].x), "=r"(val[j].y), "=r"(val[j].z), "=r"(val[j].w)
+                                 : "l"(src));
+                }
+                dst[j] = (kv ? vc : kc) + ((size_t)bh * cap + i) * CPR + ch;
+            }
         }
-        uint4 *dst = (kv ? vc : kc) + (bh * cap + i) * cpr + ch;
-        *dst = val;
+#pragma unroll
+        for (int j = 0; j < UNROLL; ++j)
+            if (dst[j]) *dst[j] = val[j];
     }
 }
 
@@ -113,6 +129,8 @@ __global__ void __launch_bounds__((kSnapMaxMT + 1) * 32, 1)
     uint64_t *empty_bar = full_bar + kSnapStages;
 
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    pdl_trigger();
+    pdl_wait();
     const int L = clamp_len_s(__ldg(p.len + b), p.L_cap);
     if (L < p.w) return;
     const int end = PASS == 1 ? L : L - p.w;
@@ -356,6 +374,8 @@ __global__ void __launch_bounds__(1024) snapkv_topk_kernel(const float *__restri
     __shared__ int scratch[40];
     __shared__ int sel_digit, sel_remaining;
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
     const int L = clamp_len_s(__ldg(seq_len + b), L_cap);
     int32_t *out = idx + ((long long)b * H_kv + h) * budget;
     if (L <= budget) {
@@ -445,21 +465,25 @@ magicdec_status launch_streaming_select(const int32_t *seq_len, int B, int H_kv,
     const long long total = (long long)B * H_kv * (n_sink + n_recent);
     const int threads = 256;
     const int blocks = (int)std::min<long long>((total + threads - 1) / threads, 65535);
-    streaming_select_kernel<<<blocks, threads, 0, st>>>(seq_len, B, H_kv, n_sink, n_recent, idx, n_sel);
-    return magicdec_host::launch_status();
+    return magicdec_host::launch_pdl(streaming_select_kernel, dim3(blocks), dim3(threads), 0, st, seq_len, B, H_kv,
+                                     n_sink, n_recent, idx, n_sel);
 }
 
 magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *k, const void *v,
                                  const int32_t *idx, int n_idx, int cap, void *kc, void *vc, cudaStream_t st) {
     if (n_idx == 0 || B == 0) return MAGICDEC_OK;
     const long long total = (long long)B * H_kv * n_idx * 2 * (D / 8);
+    if (total >= (1ll << 32)) return MAGICDEC_ERR_UNSUPPORTED;
     const int threads = 256;
-    const long long want = (total + threads - 1) / threads;
-    const int blocks = (int)std::min<long long>(want, (long long)magicdec_host::sm_count() * 16);
-    gather_kv_kernel<<<blocks, threads, 0, st>>>(static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
-                                                 idx, B, H_kv, D, L_cap, n_idx, cap, static_cast<uint4 *>(kc),
-                                                 static_cast<uint4 *>(vc));
-    return magicdec_host::launch_status();
+    const long long want = (total + threads * 4 - 1) / (threads * 4);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>(want, (long long)magicdec_host::sm_count() * 8));
+    const uint4 *k4 = static_cast<const uint4 *>(k), *v4 = static_cast<const uint4 *>(v);
+    uint4 *kc4 = static_cast<uint4 *>(kc), *vc4 = static_cast<uint4 *>(vc);
+    if (D == 128)
+        return magicdec_host::launch_pdl(gather_kv_kernel<16>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx, H_kv,
+                                         L_cap, n_idx, cap, (unsigned)total, kc4, vc4);
+    return magicdec_host::launch_pdl(gather_kv_kernel<8>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx, H_kv,
+                                     L_cap, n_idx, cap, (unsigned)total, kc4, vc4);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -483,9 +507,8 @@ static magicdec_status launch_snap_pass(const CUtensorMap &tmk, const SnapParams
     auto kern = snapkv_pass_kernel<D, PASS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MAGICDEC_ERR_CUDA;
-    dim3 grid(prm.n_chunks, prm.H_kv, prm.B);
-    kern<<<grid, (prm.MT + 1) * 32, smem, st>>>(tmk, prm);
-    return magicdec_host::launch_status();
+    return magicdec_host::launch_pdl(kern, dim3(prm.n_chunks, prm.H_kv, prm.B), dim3((prm.MT + 1) * 32), smem, st,
+                                     tmk, prm);
 }
 
 magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
@@ -531,9 +554,9 @@ magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap,
     } else {
         return MAGICDEC_ERR_UNSUPPORTED;
     }
-    snapkv_topk_kernel<<<dim3(H_kv, B), 1024, 0, st>>>(prm.score, keys, seq_len, H_kv, L_cap, w, pool, budget,
-                                                        idx, n_sel);
-    return magicdec_host::launch_status();
+    return magicdec_host::launch_pdl(snapkv_topk_kernel, dim3(H_kv, B), dim3(1024), 0, st,
+                                     static_cast<const float *>(prm.score), keys, seq_len, H_kv, L_cap, w, pool,
+                                     budget, idx, n_sel);
 }
 
 }  // namespace magicdec
