@@ -25,9 +25,10 @@
 
 namespace magicdec {
 
-constexpr int kAccChunk = 16384;      // logits per stats / sample CTA
+constexpr int kStatChunk = 8192;      // logits per stats CTA
+constexpr int kAccChunk = 4096;       // logits per sample CTA
 constexpr int kAccThreads = 256;
-constexpr int kAccPer = kAccChunk / kAccThreads;   // 64 logits per thread
+constexpr int kAccPer = kStatChunk / kAccThreads;  // 32 logits per thread, held in registers
 
 // ------------------------------------------------------------ double-float
 struct dflt {
@@ -77,6 +78,18 @@ __device__ __forceinline__ dflt df_from_double(double x) {
 
 __device__ __forceinline__ double df_to_double(dflt a) { return (double)a.hi + (double)a.lo; }
 
+// Warp sum of double-float values in a fixed butterfly order (fp32 pipe only).
+__device__ __forceinline__ dflt warp_sum_df(dflt a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        dflt b;
+        b.hi = __shfl_xor_sync(0xffffffffu, a.hi, o);
+        b.lo = __shfl_xor_sync(0xffffffffu, a.lo, o);
+        a = df_add(a, b);
+    }
+    return a;
+}
+
 // ------------------------------------------------------------------- stats
 struct RowStat {
     double s;          // sum over the chunk of exp(x - m)
@@ -103,12 +116,12 @@ struct AcceptParams {
     int32_t *n_acc;
     int32_t *out_tok;
     int32_t *n_amb;
-    RowStat *stats;           // [B, rows_per_b, n_chunks]
+    RowStat *stats;           // [B, rows_per_b, n_stat_chunks]
     JobInfo *job;             // [B]
     double *chunk_sum;        // [B, n_chunks]
     int *counters;            // [B], zero between calls
     int *err;
-    int B, gamma, V, n_chunks, rows_per_b, greedy;
+    int B, gamma, V, n_chunks, n_stat_chunks, rows_per_b, greedy;
 };
 
 // Row r of sequence b: r <= gamma -> target row r; else draft row r-gamma-1.
@@ -132,18 +145,18 @@ __device__ __forceinline__ void top_merge(float &t1, float &t2, int &arg, float 
 __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptParams p) {
     __shared__ float red_f[kAccThreads / 32][3];
     __shared__ int red_i[kAccThreads / 32];
-    __shared__ double red_d[kAccThreads / 32];
+    __shared__ dflt red_df[kAccThreads / 32];
     __shared__ float chunk_max;
     const int chunk = blockIdx.x, row = blockIdx.y;
     pdl_trigger();
     pdl_wait();
     const int b = row / p.rows_per_b, r = row % p.rows_per_b;
     const float *x = row_ptr(p, b, r);
-    const int t0 = chunk * kAccChunk, t1 = min(t0 + kAccChunk, p.V);
+    const int t0 = chunk * kStatChunk, t1 = min(t0 + kStatChunk, p.V);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     float v[kAccPer];
-    const bool vec = ((p.V & 3) == 0) && (t1 - t0 == kAccChunk);
+    const bool vec = ((p.V & 3) == 0) && (t1 - t0 == kStatChunk);
     if (vec) {
         const float4 *x4 = reinterpret_cast<const float4 *>(x + t0);
 #pragma unroll
@@ -208,21 +221,20 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
     dflt acc = {0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < kAccPer; ++k) acc = df_add_f(acc, fast_exp2((v[k] - m) * kLog2e));
-    double s = df_to_double(acc);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) red_d[warp] = s;
+    acc = warp_sum_df(acc);
+    if (lane == 0) red_df[warp] = acc;
     __syncthreads();
     if (tid == 0) {
-        double tot = 0.0;
-        for (int w = 0; w < kAccThreads / 32; ++w) tot += red_d[w];
+        dflt t = red_df[0];
+        for (int w = 1; w < kAccThreads / 32; ++w) t = df_add(t, red_df[w]);
+        const double tot = df_to_double(t);
         RowStat st;
         st.s = tot;
         st.m = m;
         st.top1 = red_f[0][1];
         st.top2 = red_f[0][2];
         st.arg = red_i[0];
-        p.stats[((long long)b * p.rows_per_b + r) * p.n_chunks + chunk] = st;
+        p.stats[((long long)b * p.rows_per_b + r) * p.n_stat_chunks + chunk] = st;
     }
 }
 
@@ -233,56 +245,94 @@ struct RowAll {
     int arg;
 };
 
-__device__ RowAll row_stat(const AcceptParams &p, int b, int r) {
-    const RowStat *src = p.stats + ((long long)b * p.rows_per_b + r) * p.n_chunks;
-    RowAll a{0.0, -INFINITY, -INFINITY, -INFINITY, 0x7fffffff};
-    for (int c = 0; c < p.n_chunks; ++c) a.m = fmaxf(a.m, src[c].m);
-    for (int c = 0; c < p.n_chunks; ++c) {
-        const RowStat st = src[c];
-        if (st.m != -INFINITY) a.s += st.s * exp((double)st.m - (double)a.m);
-        top_merge(a.top1, a.top2, a.arg, st.top1, st.top2, st.arg);
-    }
-    return a;
-}
+constexpr int kMaxRows = 2 * 32 + 1;     // rows per sequence (gamma <= 32)
+constexpr int kChainThreads = 256;
 
-// One thread per sequence (the chain is sequential; each step touches a few
-// chunk records and two logits).
-__global__ void accept_chain_kernel(const AcceptParams p) {
+// One CTA per sequence.  Warp r merges row r's chunk records (lane c takes
+// chunk c: one fp64 exponential per lane, fixed-order butterfly sum); warp 0
+// then evaluates p(x)/q(x) for the gamma draft tokens (one position per
+// lane), and thread 0 runs the sequential accept chain on those numbers.
+__global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const AcceptParams p) {
+    __shared__ RowAll rs[kMaxRows];
+    __shared__ double ratio[32];
+    __shared__ int okq0[32];
     pdl_trigger();
     pdl_wait();
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= p.B) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x;
     const int gamma = p.gamma, V = p.V;
+    for (int r = warp; r < p.rows_per_b; r += kChainThreads / 32) {
+        const RowStat *src = p.stats + ((long long)b * p.rows_per_b + r) * p.n_stat_chunks;
+        float m = -INFINITY, t1 = -INFINITY, t2 = -INFINITY;
+        int arg = 0x7fffffff;
+        for (int c = lane; c < p.n_stat_chunks; c += 32) {
+            const RowStat st = src[c];
+            m = fmaxf(m, st.m);
+            top_merge(t1, t2, arg, st.top1, st.top2, st.arg);
+        }
+        m = warp_max(m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float u1 = __shfl_xor_sync(0xffffffffu, t1, o);
+            const float u2 = __shfl_xor_sync(0xffffffffu, t2, o);
+            const int ua = __shfl_xor_sync(0xffffffffu, arg, o);
+            top_merge(t1, t2, arg, u1, u2, ua);
+        }
+        double sum = 0.0;
+        for (int c = lane; c < p.n_stat_chunks; c += 32) {
+            const RowStat st = src[c];
+            if (st.m != -INFINITY) sum += st.s * exp((double)st.m - (double)m);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0) rs[r] = RowAll{sum, m, t1, t2, arg};
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    if (!p.greedy) {
+        // ratio_i = p_i(x_i) / q_i(x_i); okq0: 1 = accept (q = 0 < p), 2 = reject
+        for (int i = lane; i < gamma; i += 32) {
+            const int x = __ldg(p.draft_tok + (long long)b * gamma + i);
+            double rt = -1.0;
+            int oq = 0;
+            if (x >= 0 && x < V) {
+                const RowAll ts = rs[i], ds = rs[gamma + 1 + i];
+                const double px = exp((double)__ldg(row_ptr(p, b, i) + x) - (double)ts.m) / ts.s;
+                const double qx = exp((double)__ldg(row_ptr(p, b, gamma + 1 + i) + x) - (double)ds.m) / ds.s;
+                if (qx > 0.0) rt = px / qx;
+                else oq = px > 0.0 ? 1 : 2;
+            } else {
+                oq = 2;
+            }
+            ratio[i] = rt;
+            okq0[i] = oq;
+        }
+        __syncwarp();
+    }
+    if (lane != 0) return;
     int32_t *out = p.out_tok + (long long)b * (gamma + 1);
     JobInfo job{};
     int amb = 0, acc = gamma, emit = -1;
     for (int i = 0; i < gamma; ++i) {
-        const RowAll ts = row_stat(p, b, i);
         const int x = __ldg(p.draft_tok + (long long)b * gamma + i);
         bool ok;
         if (p.greedy) {
+            const RowAll ts = rs[i];
             if ((double)ts.top1 - (double)ts.top2 < 1e-4) ++amb;
             ok = (x == ts.arg);
             if (!ok) emit = ts.arg;
         } else {
-            const RowAll ds = row_stat(p, b, gamma + 1 + i);
-            if (x < 0 || x >= V) {
-                ok = false;
+            const int oq = okq0[i];
+            if (oq) {
+                ok = oq == 1;
             } else {
-                const double tx = __ldg(row_ptr(p, b, i) + x);
-                const double dx = __ldg(row_ptr(p, b, gamma + 1 + i) + x);
-                const double px = exp(tx - (double)ts.m) / ts.s;
-                const double qx = exp(dx - (double)ds.m) / ds.s;
-                if (qx > 0.0) {
-                    const double ratio = px / qx;
-                    const double u = __ldg(p.u_acc + (long long)b * gamma + i);
-                    ok = u < ratio;
-                    if (fabs(u - ratio) < 1e-4) ++amb;
-                } else {
-                    ok = px > 0.0;
-                }
+                const double rt = ratio[i];
+                const double u = __ldg(p.u_acc + (long long)b * gamma + i);
+                ok = u < rt;
+                if (fabs(u - rt) < 1e-4) ++amb;
             }
             if (!ok) {
+                const RowAll ts = rs[i], ds = rs[gamma + 1 + i];
                 job.kind = 1;
                 job.mt = ts.m; job.st = ts.s;
                 job.md = ds.m; job.sd = ds.s;
@@ -292,7 +342,7 @@ __global__ void accept_chain_kernel(const AcceptParams p) {
         out[i] = x;
     }
     if (acc == gamma) {
-        const RowAll ts = row_stat(p, b, gamma);
+        const RowAll ts = rs[gamma];
         if (p.greedy) {
             if ((double)ts.top1 - (double)ts.top2 < 1e-4) ++amb;
             emit = ts.arg;
@@ -329,27 +379,70 @@ __device__ __forceinline__ dflt weight_at(const WeightCtx &w, int t) {
     return d.hi > 0.f ? d : dflt{0.f, 0.f};
 }
 
-__device__ double block_sum_d(double v, double *scratch) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+// Block sum of double-float values in a fixed order; returned (as a double) to every thread.
+__device__ double block_sum_df(dflt v, dflt *scratch) {
+    v = warp_sum_df(v);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __syncthreads();
     if (lane == 0) scratch[warp] = v;
     __syncthreads();
-    double t = 0.0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += scratch[w];
-    return t;
+    dflt t = scratch[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = df_add(t, scratch[w]);
+    return df_to_double(t);
 }
 
-// Sum of weights over [t0, t1) (thread-strided double-float, then fp64 tree).
-__device__ double chunk_weight_sum(const WeightCtx &w, int t0, int t1, double *scratch) {
+// Resample weights of the four logits t..t+3 from float4 loads (t % 4 == 0).
+__device__ __forceinline__ dflt weight4_sum(const WeightCtx &w, int t) {
+    const float4 xt = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
+    const float tv[4] = {xt.x, xt.y, xt.z, xt.w};
+    float dv[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool resid = !(w.kind == 2 || w.use_p);
+    if (resid) {
+        const float4 xd = __ldg(reinterpret_cast<const float4 *>(w.dr + t));
+        dv[0] = xd.x; dv[1] = xd.y; dv[2] = xd.z; dv[3] = xd.w;
+    }
     dflt acc = {0.f, 0.f};
-    for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) acc = df_add(acc, weight_at(w, t));
-    return block_sum_d(df_to_double(acc), scratch);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const dflt pt = df_mul_f(fast_exp2((tv[j] - w.mt) * kLog2e), w.inv_st);
+        if (!resid) {
+            acc = df_add(acc, pt);
+        } else {
+            const dflt qt = df_mul_f(fast_exp2((dv[j] - w.md) * kLog2e), w.inv_sd);
+            const dflt d = df_sub(pt, qt);
+            if (d.hi > 0.f) acc = df_add(acc, d);
+        }
+    }
+    return acc;
+}
+
+// Sum of weights over [t0, t1) (thread-strided double-float, then a fixed tree).
+__device__ double chunk_weight_sum(const WeightCtx &w, int t0, int t1, bool vec4, dflt *scratch) {
+    dflt acc = {0.f, 0.f};
+    if (vec4 && ((t1 - t0) & 3) == 0 && (t0 & 3) == 0) {
+        for (int t = t0 + 4 * threadIdx.x; t < t1; t += 4 * blockDim.x) acc = df_add(acc, weight4_sum(w, t));
+    } else {
+        for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) acc = df_add(acc, weight_at(w, t));
+    }
+    return block_sum_df(acc, scratch);
+}
+
+// Inclusive block scan of one double per thread (fixed order).
+__device__ double block_scan_d(double v, double *buf) {
+    const int tid = threadIdx.x;
+    buf[tid] = v;
+    __syncthreads();
+    for (int off = 1; off < (int)blockDim.x; off <<= 1) {
+        const double add = tid >= off ? buf[tid - off] : 0.0;
+        __syncthreads();
+        buf[tid] += add;
+        __syncthreads();
+    }
+    return buf[tid];
 }
 
 __global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const AcceptParams p) {
-    __shared__ double scratch[kAccThreads / 32];
+    __shared__ dflt scratch[kAccThreads / 32];
     __shared__ double seg[kAccThreads];
     __shared__ int is_last;
     const int chunk = blockIdx.x, b = blockIdx.y;
@@ -367,7 +460,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const Accept
     w.inv_st = df_from_double(1.0 / job.st);
     w.inv_sd = df_from_double(job.kind == 1 ? 1.0 / job.sd : 0.0);
     const int t0 = chunk * kAccChunk, t1 = min(t0 + kAccChunk, p.V);
-    const double csum = chunk_weight_sum(w, t0, t1, scratch);
+    const bool vec4 = (p.V & 3) == 0;
+    const double csum = chunk_weight_sum(w, t0, t1, vec4, scratch);
     if (threadIdx.x == 0) {
         p.chunk_sum[(long long)b * p.n_chunks + chunk] = csum;
         __threadfence();
@@ -390,12 +484,13 @@ __global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const Accept
     bool use_p = false;
     if (!(W > 0.0)) {
         // Residual empty (p == q up to rounding): draw from p instead; the
-        // chunk sums of p are recomputed here into seg[] (n_chunks <= 256).
+        // chunk sums of p are recomputed here into seg[] (n_chunks <= 256 is
+        // checked at the entry point).
         use_p = true;
         w.use_p = true;
         W = 0.0;
         for (int c = 0; c < p.n_chunks; ++c) {
-            const double v = chunk_weight_sum(w, c * kAccChunk, min((c + 1) * kAccChunk, p.V), scratch);
+            const double v = chunk_weight_sum(w, c * kAccChunk, min((c + 1) * kAccChunk, p.V), vec4, scratch);
             if (threadIdx.x == 0) seg[c] = v;
             W += v;
         }
@@ -422,37 +517,42 @@ __global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const Accept
         ++amb;
     }
     __syncthreads();   // every thread has read seg[] for the chunk search
-    // Scan inside chunk cstar: each thread owns a contiguous run of logits.
+    // Scan inside chunk cstar: each thread owns a contiguous run of logits; an
+    // fp64 block scan of the run sums tells every thread where its run starts,
+    // and the one run containing the crossing walks its logits.
+    __shared__ int found_token, found_amb;
+    if (threadIdx.x == 0) { found_token = -1; found_amb = 0; }
     const int c0 = cstar * kAccChunk, c1 = min(c0 + kAccChunk, p.V);
     const int per = (c1 - c0 + kAccThreads - 1) / kAccThreads;
     const int my0 = c0 + threadIdx.x * per, my1 = min(my0 + per, c1);
     dflt mine = {0.f, 0.f};
     for (int t = my0; t < my1; ++t) mine = df_add(mine, weight_at(w, t));
-    seg[threadIdx.x] = df_to_double(mine);
+    const double my_sum = df_to_double(mine);
+    const double incl = block_scan_d(my_sum, seg);
+    const double start = before + (incl - my_sum);
+    if (my0 < my1 && start <= target && target < before + incl) {
+        double prev = start;
+        for (int t = my0; t < my1; ++t) {
+            const double nxt = prev + df_to_double(weight_at(w, t));
+            if (nxt > target) {
+                found_token = t;
+                found_amb = ((t > 0 && target - prev < tol) || (t < p.V - 1 && nxt - target < tol)) ? 1 : 0;
+                break;
+            }
+            prev = nxt;
+        }
+        if (found_token < 0) {   // rounding inside the run: its last positive weight
+            for (int t = my1 - 1; t >= my0; --t)
+                if (weight_at(w, t).hi > 0.f) { found_token = t; break; }
+            found_amb = 1;
+        }
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        double run = before;
-        int owner = -1;
-        for (int i = 0; i < kAccThreads; ++i) {
-            if (run + seg[i] > target) { owner = i; break; }
-            run += seg[i];
-        }
-        int token = -1;
-        if (owner >= 0) {
-            const int s0 = c0 + owner * per, s1 = min(s0 + per, c1);
-            double prev = run;
-            for (int t = s0; t < s1; ++t) {
-                const double nxt = prev + df_to_double(weight_at(w, t));
-                if (nxt > target) {
-                    token = t;
-                    if ((t > 0 && target - prev < tol) || (t < p.V - 1 && nxt - target < tol)) ++amb;
-                    break;
-                }
-                prev = nxt;
-            }
-        }
+        int token = found_token;
+        amb += found_amb;
         if (token < 0) {
-            // rounding: the last logit with positive weight in the chunk
+            // rounding pushed the target past the chunk: its last positive weight
             for (int t = c1 - 1; t >= c0; --t)
                 if (weight_at(w, t).hi > 0.f) { token = t; break; }
             if (token < 0) token = c1 - 1;
@@ -470,8 +570,9 @@ static size_t align256a(size_t x) { return (x + 255) & ~(size_t)255; }
 //                   [row stats][per-sequence job][per-chunk weight sums]
 size_t accept_workspace_bytes(int B, int gamma, int V) {
     const int n_chunks = (V + kAccChunk - 1) / kAccChunk;
+    const int n_stat = (V + kStatChunk - 1) / kStatChunk;
     const int rows = 2 * gamma + 1;
-    return (size_t)kAcceptMaxBatch * 4 + align256a((size_t)B * rows * n_chunks * sizeof(RowStat)) +
+    return (size_t)kAcceptMaxBatch * 4 + align256a((size_t)B * rows * n_stat * sizeof(RowStat)) +
            align256a((size_t)B * sizeof(JobInfo)) + align256a((size_t)B * n_chunks * sizeof(double));
 }
 
@@ -492,22 +593,24 @@ magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target,
     prm.V = V;
     prm.greedy = greedy ? 1 : 0;
     prm.n_chunks = (V + kAccChunk - 1) / kAccChunk;
+    prm.n_stat_chunks = (V + kStatChunk - 1) / kStatChunk;
     prm.rows_per_b = greedy ? gamma + 1 : 2 * gamma + 1;
+    if (2 * gamma + 1 > kMaxRows) return MAGICDEC_ERR_UNSUPPORTED;
     prm.err = magicdec_host::device_error_word();
     const int rows_alloc = 2 * gamma + 1;
     uint8_t *w = static_cast<uint8_t *>(ws);
     prm.counters = reinterpret_cast<int *>(w);
     w += (size_t)kAcceptMaxBatch * 4;
     prm.stats = reinterpret_cast<RowStat *>(w);
-    w += align256a((size_t)B * rows_alloc * prm.n_chunks * sizeof(RowStat));
+    w += align256a((size_t)B * rows_alloc * prm.n_stat_chunks * sizeof(RowStat));
     prm.job = reinterpret_cast<JobInfo *>(w);
     w += align256a((size_t)B * sizeof(JobInfo));
     prm.chunk_sum = reinterpret_cast<double *>(w);
 
-    magicdec_status s = magicdec_host::launch_pdl(accept_stats_kernel, dim3(prm.n_chunks, B * prm.rows_per_b),
+    magicdec_status s = magicdec_host::launch_pdl(accept_stats_kernel, dim3(prm.n_stat_chunks, B * prm.rows_per_b),
                                                   dim3(kAccThreads), 0, st, prm);
     if (s != MAGICDEC_OK) return s;
-    s = magicdec_host::launch_pdl(accept_chain_kernel, dim3((B + 127) / 128), dim3(128), 0, st, prm);
+    s = magicdec_host::launch_pdl(accept_chain_kernel, dim3(B), dim3(kChainThreads), 0, st, prm);
     if (s != MAGICDEC_OK || greedy) return s;
     return magicdec_host::launch_pdl(accept_sample_kernel, dim3(prm.n_chunks, B), dim3(kAccThreads), 0, st, prm);
 }

@@ -224,7 +224,7 @@ magicdec_status magicdec_spec_accept(int B, int gamma, int V, const float *targe
     if (gamma > 0 && !draft_tok) return MAGICDEC_ERR_NULL;
     if (!greedy && (!u_res || (gamma > 0 && (!draft_logits || !u_acc)))) return MAGICDEC_ERR_NULL;
     if (B <= 0 || gamma < 0 || V <= 0) return MAGICDEC_ERR_SHAPE;
-    if (V > 256 * 16384 || B > magicdec::kAcceptMaxBatch) return MAGICDEC_ERR_UNSUPPORTED;
+    if (V > 256 * 4096 || B > magicdec::kAcceptMaxBatch || gamma > 32) return MAGICDEC_ERR_UNSUPPORTED;
     if (!aligned16(target_logits) || (draft_logits && !aligned16(draft_logits)) || !aligned16(ws))
         return MAGICDEC_ERR_ALIGN;
     if (ws_bytes < magicdec_spec_accept_workspace_size(B, gamma, V)) return MAGICDEC_ERR_WORKSPACE;

@@ -38,6 +38,7 @@ namespace magicdec {
 constexpr int kTileN = 64;      // KV rows per pipeline stage
 constexpr int kMaxStages = 8;
 constexpr int kHalfBytes = kTileN * 128;   // one 64-row x 64-channel swizzled box
+constexpr int kMaxContrib = 32;            // contributors a merge lists in shared memory
 
 struct AttnParams {
     const __nv_bfloat16 *q;     // [B, n_q, H_q, D]
@@ -116,7 +117,8 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     uint64_t *qfull_bar = empty_bar + kMaxStages;  // [2]
     uint64_t *qempty_bar = qfull_bar + 2;          // [2]
     int *flag = reinterpret_cast<int *>(qempty_bar + 2);
-    int *prefix = flag + 4;                        // [B+1]
+    int *contrib = flag + 4;                       // [kMaxContrib] partial-slot bases of a merged pair
+    int *prefix = contrib + kMaxContrib;           // [B+1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -449,49 +451,45 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
                 pml[(mt * 16 + gtid) * 2] = row_m[mt * 16 + gtid];
                 pml[(mt * 16 + gtid) * 2 + 1] = row_l[mt * 16 + gtid];
             }
-            __threadfence();
             named_bar_sync(1, NCW * 32);
             if (ctid == 0) {
                 const int pair = s.b * p.H_kv + s.h;
-                // CTAs with an empty range (fewer tiles than CTAs) own no tile
-                // of the pair and publish nothing.
+                // Contributors: the CTAs with a non-empty range in [c_first, c_last]
+                // (with fewer tiles than CTAs some ranges are empty).  A contributor
+                // whose range starts inside the pair published its first segment
+                // (slot 0), one that started before it its last segment (slot 1).
                 int n_contrib = 0;
-                for (int cc = c_first; cc <= c_last; ++cc)
-                    n_contrib += cta_start(cc + 1, T, C) > cta_start(cc, T, C);
-                const int old = atomicAdd(p.counters + pair, 1);
-                const int last = (old == n_contrib - 1);
-                if (old >= n_contrib) raise_error(p.err, kErrState);
-                if (last) {
-                    __threadfence();
-                    p.counters[pair] = 0;
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                    const long long st0 = cta_start(cc, T, C);
+                    if (cta_start(cc + 1, T, C) == st0) continue;
+                    if (n_contrib < kMaxContrib) contrib[n_contrib] = cc * 2 + (st0 >= s.pair_t0 ? 0 : 1);
+                    ++n_contrib;
                 }
-                *flag = last;
+                // release: this CTA's partial (ordered by the barrier above);
+                // acquire: for the last arriver, every other contributor's partial
+                const int old = atomic_add_acq_rel_gpu(p.counters + pair, 1);
+                const int last = (old == n_contrib - 1);
+                if (old >= n_contrib || n_contrib > kMaxContrib) raise_error(p.err, kErrState);
+                if (last) p.counters[pair] = 0;
+                *flag = last ? n_contrib : 0;
             }
             named_bar_sync(1, NCW * 32);
-            if (*flag) {
-                __threadfence();
+            const int n_merge = min(*flag, kMaxContrib);
+            if (n_merge) {
                 for (int idx = ctid; idx < p.M * (D / 4); idx += NCW * 32) {
                     const int r = idx / (D / 4), col = (idx % (D / 4)) * 4;
                     float Mx = NEG_INF;
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        const long long st0 = cta_start(cc, T, C);
-                        if (cta_start(cc + 1, T, C) == st0) continue;
-                        const int sl2 = st0 >= s.pair_t0 ? 0 : 1;
-                        const float *ml = p.part_ml + ((long long)cc * 2 + sl2) * (MT * 16) * 2;
-                        Mx = fmaxf(Mx, __ldcg(ml + r * 2));
-                    }
+                    for (int j = 0; j < n_merge; ++j)
+                        Mx = fmaxf(Mx, __ldcg(p.part_ml + ((long long)contrib[j] * (MT * 16) + r) * 2));
                     const float Mu = Mx == NEG_INF ? 0.f : Mx;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                     float Ls = 0.f;
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        const long long st0 = cta_start(cc, T, C);
-                        if (cta_start(cc + 1, T, C) == st0) continue;
-                        const int sl2 = st0 >= s.pair_t0 ? 0 : 1;
-                        const long long base = ((long long)cc * 2 + sl2) * (MT * 16);
-                        const float mc = __ldcg(p.part_ml + (base + r) * 2);
-                        const float lc = __ldcg(p.part_ml + (base + r) * 2 + 1);
+                    for (int j = 0; j < n_merge; ++j) {
+                        const long long base = (long long)contrib[j] * (MT * 16) + r;
+                        const float mc = __ldcg(p.part_ml + base * 2);
+                        const float lc = __ldcg(p.part_ml + base * 2 + 1);
                         const float wgt = fast_exp2((mc - Mu) * sl);
-                        const float4 oc = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (base + r) * D + col));
+                        const float4 oc = __ldcg(reinterpret_cast<const float4 *>(p.part_o + base * D + col));
                         Ls += wgt * lc;
                         acc.x += wgt * oc.x; acc.y += wgt * oc.y; acc.z += wgt * oc.z; acc.w += wgt * oc.w;
                     }
@@ -520,7 +518,7 @@ template <int D, int MT>
 static size_t attn_fixed_smem(int B) {
     return 1024 /* alignment slack */ + 2 * (size_t)(D / 64) * MT * 16 * 128 /* query ring */ +
            (size_t)MT * 16 * (D + 4) * 4 + (size_t)MT * 64 * 4 * 2 + (size_t)MT * 16 * 4 * 2 +
-           (2 * kMaxStages + 4) * 8 + 16 + (size_t)(B + 1) * 4;
+           (2 * kMaxStages + 4) * 8 + 16 + kMaxContrib * 4 + (size_t)(B + 1) * 4;
 }
 
 template <int D>

@@ -154,6 +154,15 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Device-scope acquire-release add: publishes this thread's (and, through a
+// preceding CTA barrier, its CTA's) writes and, for the last arriver, makes
+// the other arrivers' published writes visible.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // ----------------------------------------------------------- named barriers
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     __syncwarp();
