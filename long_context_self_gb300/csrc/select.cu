@@ -4,20 +4,13 @@
 //  * StreamingLLM selection (paper section 4.4 / section 5.1): attention sinks
 //    plus a recent window; pure index arithmetic.
 //  * SnapKV selection (paper section 4.4 / section 5.2), once after prefill:
-//      pass 1  per (sequence, KV head, 1024-position chunk): the M = w*G
-//              observation-window query rows stream the chunk's K rows and
-//              keep an online (max, sum) of their causal softmax; partials
-//              go to the workspace;
-//      pass 2  per chunk of the prefix [0, L-w): merge the partials into each
-//              row's log-sum-exp, recompute the logits, and sum the softmax
-//              probabilities over the M rows per position -> score;
+//    the observation-window scores come from the two tcgen05 passes in
+//    snapkv_tc.cu; here
 //      top-k   one CTA per (sequence, KV head): max-pool (kernel k, clipped),
 //              an 8-bit-digit MSB-first radix select of the k-th largest
 //              pooled score, then an order-preserving block compaction that
 //              keeps everything above the threshold and the smallest
 //              positions among ties; the window is appended.
-//    Passes 1-2 stream K once each (bulk copies into padded shared rows, an
-//    mbarrier ring) and contract on bf16 mma.sync with fp32 accumulation.
 //  * Gather ("pre-gather a sparse KV cache", section 4.4): 16-byte vector
 //    row copies into the head-major compact draft cache.
 #include <algorithm>
@@ -92,244 +85,6 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict_
 #pragma unroll
         for (int j = 0; j < UNROLL; ++j)
             if (dst[j]) *dst[j] = val[j];
-    }
-}
-
-// ---------------------------------------------------------- SnapKV scoring
-constexpr int kSnapTile = 64;
-constexpr int kSnapChunk = 1024;                      // positions per CTA
-constexpr int kSnapStages = 4;
-constexpr int kSnapMaxMT = 12;                        // up to 192 window rows per KV head
-
-struct SnapParams {
-    const __nv_bfloat16 *q;     // [B, w, H_q, D]
-    const int32_t *len;
-    float *part;                // [B, H_kv, n_chunks, MP, 2]  (max, sum) per row and chunk
-    float *score;               // [B, H_kv, L_cap]
-    int *err;
-    int B, H_q, H_kv, G, w, L_cap, M, MT, n_chunks;
-    float scale_log2;
-};
-
-constexpr int kSnapHalf = kSnapTile * 128;           // one 64-row x 64-channel swizzled box
-
-template <int D, int PASS>
-__global__ void __launch_bounds__((kSnapMaxMT + 1) * 32, 1)
-    snapkv_pass_kernel(const __grid_constant__ CUtensorMap tmk, const SnapParams p) {
-    constexpr int HALVES = D / 64;
-    constexpr int TILE_BYTES = HALVES * kSnapHalf;
-    constexpr int KS = D / 16;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int MT = p.MT, MP = MT * 16;
-    uint8_t *stage_base = smem;
-    float *colsum = reinterpret_cast<float *>(smem + kSnapStages * TILE_BYTES);     // [MT][64]
-    float *lse = colsum + kSnapMaxMT * 64;                                           // [MP]
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(lse + kSnapMaxMT * 16);
-    uint64_t *empty_bar = full_bar + kSnapStages;
-
-    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    pdl_trigger();
-    pdl_wait();
-    const int L = clamp_len_s(__ldg(p.len + b), p.L_cap);
-    if (L < p.w) return;
-    const int end = PASS == 1 ? L : L - p.w;
-    const int pos_begin = chunk * kSnapChunk;
-    const int pos_end = min(pos_begin + kSnapChunk, end);
-    if (pos_begin >= pos_end) return;
-    const int ntiles = (pos_end - pos_begin + kSnapTile - 1) / kSnapTile;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float sl = p.scale_log2;
-    const float NEG_INF = -INFINITY;
-
-    if (tid == 0) {
-        for (int s = 0; s < kSnapStages; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], MT);
-        }
-        mbar_fence_init();
-    }
-    if (PASS == 2) {
-        // Merge pass-1 partials into each row's log2-sum-exp2 (scaled units).
-        const int nvalid = (L + kSnapChunk - 1) / kSnapChunk;
-        const float *pb = p.part + ((long long)b * p.H_kv + h) * p.n_chunks * MP * 2;
-        for (int r = tid; r < MP; r += blockDim.x) {
-            if (r >= p.M) { lse[r] = INFINITY; continue; }
-            float mx = NEG_INF;
-            for (int cc = 0; cc < nvalid; ++cc) mx = fmaxf(mx, pb[((long long)cc * MP + r) * 2]);
-            float sm = 0.f;
-            for (int cc = 0; cc < nvalid; ++cc)
-                sm += pb[((long long)cc * MP + r) * 2 + 1] * fast_exp2((pb[((long long)cc * MP + r) * 2] - mx) * sl);
-            lse[r] = mx * sl + __log2f(sm);
-        }
-    }
-    __syncthreads();
-
-    if (warp == MT) {
-        // producer (one thread): TMA boxes of 64 positions x 64 channels of K
-        if (lane != 0) return;
-        prefetch_tensormap(&tmk);
-        const uint64_t pol = policy_evict_first();
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        for (int ti = 0; ti < ntiles; ++ti) {
-            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, p.err)) break;
-            mbar_arrive_expect_tx(&full_bar[stage], TILE_BYTES);
-            uint8_t *sk = stage_base + stage * TILE_BYTES;
-            const int pos0 = pos_begin + ti * kSnapTile;
-#pragma unroll
-            for (int hf = 0; hf < HALVES; ++hf)
-                tma_load_4d(sk + hf * kSnapHalf, &tmk, hf * 64, h, pos0, b, &full_bar[stage], pol);
-            ++issued;
-            if (++stage == kSnapStages) { stage = 0; phase ^= 1u; }
-        }
-        int st = stage;
-        uint32_t ph = phase;
-        for (int kk = 0; kk < min(issued, kSnapStages); ++kk) {
-            if (st == 0) { st = kSnapStages - 1; ph ^= 1u; } else { --st; }
-            mbar_wait(&full_bar[st], ph, p.err);
-        }
-        return;
-    }
-
-    // consumers: warp mt owns window rows mt*16 .. mt*16+15 over all 64 columns
-    const int mt = warp, g = lane >> 2, t4 = lane & 3;
-    const int r0 = mt * 16 + g, r1 = r0 + 8;
-    const int lim0 = r0 < p.M ? L - p.w + r0 / p.G : L - 1;
-    const int lim1 = r1 < p.M ? L - p.w + r1 / p.G : L - 1;
-    const long long qstride = (long long)p.H_q * D;
-    const __nv_bfloat16 *qb = p.q + (long long)b * p.w * qstride + (long long)h * p.G * D;
-    uint32_t qa[KS][4];
-    {
-        const __nv_bfloat16 *q0 = r0 < p.M ? qb + (r0 / p.G) * qstride + (r0 % p.G) * D : nullptr;
-        const __nv_bfloat16 *q1 = r1 < p.M ? qb + (r1 / p.G) * qstride + (r1 % p.G) * D : nullptr;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int c0 = ks * 16 + 2 * t4;
-            qa[ks][0] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0)) : 0u;
-            qa[ks][1] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0)) : 0u;
-            qa[ks][2] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0 + 8)) : 0u;
-            qa[ks][3] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0 + 8)) : 0u;
-        }
-    }
-    const float lse0 = PASS == 2 ? lse[r0] : 0.f, lse1 = PASS == 2 ? lse[r1] : 0.f;
-    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-    float *score_row = p.score + ((long long)b * p.H_kv + h) * p.L_cap;
-
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int ti = 0; ti < ntiles; ++ti) {
-        if (ok) ok = mbar_wait(&full_bar[stage], phase, p.err);
-        const uint32_t kbase = smem_u32(stage_base + stage * TILE_BYTES);
-        float sc[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-        if (ok) {
-            const int mat = lane >> 3, rr = lane & 7;
-#pragma unroll
-            for (int nb = 0; nb < 4; ++nb) {
-                const int row = nb * 16 + (mat >> 1) * 8 + rr;
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int ch = ks * 2 + (mat & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kbase + (ch >> 3) * kSnapHalf + swz128(row, ch & 7), b0, b1, b2, b3);
-                    mma_bf16(sc[2 * nb], qa[ks], b0, b1);
-                    mma_bf16(sc[2 * nb + 1], qa[ks], b2, b3);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[stage]);
-        if (++stage == kSnapStages) { stage = 0; phase ^= 1u; }
-
-        const int tile_pos = pos_begin + ti * kSnapTile;
-        if (PASS == 1) {
-            if (tile_pos + kSnapTile - 1 > L - p.w) {
-#pragma unroll
-                for (int n = 0; n < 8; ++n)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int pos = tile_pos + n * 8 + 2 * t4 + e;
-                        if (pos > lim0 || pos >= pos_end) sc[n][e] = NEG_INF;
-                        if (pos > lim1 || pos >= pos_end) sc[n][2 + e] = NEG_INF;
-                    }
-            } else if (tile_pos + kSnapTile > pos_end) {
-#pragma unroll
-                for (int n = 0; n < 8; ++n)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int pos = tile_pos + n * 8 + 2 * t4 + e;
-                        if (pos >= pos_end) { sc[n][e] = NEG_INF; sc[n][2 + e] = NEG_INF; }
-                    }
-            }
-            float mx0 = NEG_INF, mx1 = NEG_INF;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-                mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = mn0 == NEG_INF ? 0.f : mn0, mu1 = mn1 == NEG_INF ? 0.f : mn1;
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                s0 += fast_exp2((sc[n][0] - mu0) * sl) + fast_exp2((sc[n][1] - mu0) * sl);
-                s1 += fast_exp2((sc[n][2] - mu1) * sl) + fast_exp2((sc[n][3] - mu1) * sl);
-            }
-            l0 = l0 * fast_exp2((m0 - mu0) * sl) + s0;
-            l1 = l1 * fast_exp2((m1 - mu1) * sl) + s1;
-            m0 = mn0;
-            m1 = mn1;
-        } else {
-            // column sums of softmax probabilities over this warp's 16 rows
-            float cs[8][2];
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float v = fast_exp2(fmaf(sc[n][e], sl, -lse0)) + fast_exp2(fmaf(sc[n][2 + e], sl, -lse1));
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    v += __shfl_xor_sync(0xffffffffu, v, 8);
-                    v += __shfl_xor_sync(0xffffffffu, v, 16);
-                    cs[n][e] = v;
-                }
-            if (g == 0) {
-#pragma unroll
-                for (int n = 0; n < 8; ++n) {
-                    colsum[mt * 64 + n * 8 + 2 * t4] = cs[n][0];
-                    colsum[mt * 64 + n * 8 + 2 * t4 + 1] = cs[n][1];
-                }
-            }
-            named_bar_sync(1, MT * 32);
-            for (int col = tid; col < kSnapTile; col += MT * 32) {
-                float acc = 0.f;
-                for (int w2 = 0; w2 < MT; ++w2) acc += colsum[w2 * 64 + col];
-                const int pos = tile_pos + col;
-                if (pos < pos_end) score_row[pos] = acc;
-            }
-            named_bar_sync(1, MT * 32);
-        }
-    }
-    if (PASS == 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        if (t4 == 0) {
-            float *pb = p.part + (((long long)b * p.H_kv + h) * p.n_chunks + chunk) * MP * 2;
-            pb[r0 * 2] = m0;
-            pb[r0 * 2 + 1] = l0;
-            pb[r1 * 2] = m1;
-            pb[r1 * 2 + 1] = l1;
-        }
     }
 }
 
@@ -486,77 +241,27 @@ magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *
                                      L_cap, n_idx, cap, (unsigned)total, kc4, vc4);
 }
 
-static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t snapkv_tc_workspace_bytes(int B, int H_q, int H_kv, int L_cap, int w);
+magicdec_status launch_snapkv_scores_tc(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
+                                        const int32_t *seq_len, int w, void *ws, float **score_out, cudaStream_t st);
 
+// Workspace: [pass-1 partials][scores B x H_kv x L_cap fp32][pooled keys B x H_kv x L_cap u32]
 size_t snapkv_workspace_bytes(int B, int H_q, int H_kv, int D, int L_cap, int w) {
     (void)D;
-    const int G = H_q / H_kv;
-    const int M = w * G;
-    const int MP = ((M + 15) / 16) * 16;
-    const int n_chunks = (L_cap + kSnapChunk - 1) / kSnapChunk;
-    const size_t part = align256((size_t)B * H_kv * n_chunks * MP * 2 * 4);
-    const size_t score = align256((size_t)B * H_kv * L_cap * 4);
-    const size_t keys = align256((size_t)B * H_kv * L_cap * 4);
-    return part + score + keys;
-}
-
-template <int D, int PASS>
-static magicdec_status launch_snap_pass(const CUtensorMap &tmk, const SnapParams &prm, cudaStream_t st) {
-    const size_t smem = 1024 + (size_t)kSnapStages * (D / 64) * kSnapHalf + kSnapMaxMT * 64 * 4 +
-                        kSnapMaxMT * 16 * 4 + 2 * kSnapStages * 8;
-    auto kern = snapkv_pass_kernel<D, PASS>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return MAGICDEC_ERR_CUDA;
-    return magicdec_host::launch_pdl(kern, dim3(prm.n_chunks, prm.H_kv, prm.B), dim3((prm.MT + 1) * 32), smem, st,
-                                     tmk, prm);
+    return snapkv_tc_workspace_bytes(B, H_q, H_kv, L_cap, w);
 }
 
 magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
                                      const int32_t *seq_len, int w, int pool, int budget, int32_t *idx,
                                      int32_t *n_sel, void *ws, cudaStream_t st) {
-    SnapParams prm{};
-    prm.q = static_cast<const __nv_bfloat16 *>(q_win);
-    prm.len = seq_len;
-    prm.B = B;
-    prm.H_q = H_q;
-    prm.H_kv = H_kv;
-    prm.G = H_q / H_kv;
-    prm.w = w;
-    prm.L_cap = L_cap;
-    prm.M = w * prm.G;
-    prm.MT = (prm.M + 15) / 16;
-    if (prm.MT > kSnapMaxMT) return MAGICDEC_ERR_UNSUPPORTED;
-    prm.n_chunks = (L_cap + kSnapChunk - 1) / kSnapChunk;
-    prm.scale_log2 = kLog2e / sqrtf((float)D);
-    prm.err = magicdec_host::device_error_word();
-    const int MP = prm.MT * 16;
-    uint8_t *wsb = static_cast<uint8_t *>(ws);
-    prm.part = reinterpret_cast<float *>(wsb);
-    wsb += align256((size_t)B * H_kv * prm.n_chunks * MP * 2 * 4);
-    prm.score = reinterpret_cast<float *>(wsb);
-    wsb += align256((size_t)B * H_kv * L_cap * 4);
-    uint32_t *keys = reinterpret_cast<uint32_t *>(wsb);
-
-    // K as a 4-D view (d, H_kv, L_cap, B); boxes of 64 channels x 64 positions.
-    CUtensorMap tmk;
-    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H_kv, (uint64_t)L_cap, (uint64_t)B};
-    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)H_kv * D * 2, (uint64_t)L_cap * H_kv * D * 2};
-    const uint32_t box[4] = {64, 1, (uint32_t)kSnapTile, 1};
-    if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box)) return MAGICDEC_ERR_CUDA;
-
-    magicdec_status s;
-    if (D == 128) {
-        if ((s = launch_snap_pass<128, 1>(tmk, prm, st)) != MAGICDEC_OK) return s;
-        if ((s = launch_snap_pass<128, 2>(tmk, prm, st)) != MAGICDEC_OK) return s;
-    } else if (D == 64) {
-        if ((s = launch_snap_pass<64, 1>(tmk, prm, st)) != MAGICDEC_OK) return s;
-        if ((s = launch_snap_pass<64, 2>(tmk, prm, st)) != MAGICDEC_OK) return s;
-    } else {
-        return MAGICDEC_ERR_UNSUPPORTED;
-    }
+    float *score = nullptr;
+    magicdec_status s = launch_snapkv_scores_tc(B, H_q, H_kv, D, L_cap, q_win, k, seq_len, w, ws, &score, st);
+    if (s != MAGICDEC_OK) return s;
+    uint32_t *keys = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(score) +
+                                                  (((size_t)B * H_kv * L_cap * 4 + 255) & ~(size_t)255));
     return magicdec_host::launch_pdl(snapkv_topk_kernel, dim3(H_kv, B), dim3(1024), 0, st,
-                                     static_cast<const float *>(prm.score), keys, seq_len, H_kv, L_cap, w, pool,
-                                     budget, idx, n_sel);
+                                     static_cast<const float *>(score), keys, seq_len, H_kv, L_cap, w, pool, budget,
+                                     idx, n_sel);
 }
 
 }  // namespace magicdec
