@@ -23,6 +23,7 @@ path shards by sequence with no exchange; weak scaling).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -255,6 +256,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch)
     pipe = Pipeline(w, device, args.layers)
     torch.cuda.synchronize()
 
@@ -503,6 +506,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (profiling runs on smaller cases)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

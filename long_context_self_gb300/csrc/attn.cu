@@ -107,8 +107,8 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     const int stages = p.stages;
     uint8_t *stage_base = smem;
     uint8_t *qslots = smem + (size_t)stages * STAGE_BYTES;   // 2 slots, ring of segment queries
-    float *comb = reinterpret_cast<float *>(qslots + 2 * QSLOT);
-    float *red_m = comb + MT * 16 * CS;            // [MT][4][16]
+    float *comb = reinterpret_cast<float *>(qslots + 2 * QSLOT);   // [MT][4 warps][16][CS] partial outputs
+    float *red_m = comb + MT * 4 * 16 * CS;        // [MT][4][16]
     float *red_l = red_m + MT * 64;
     float *row_m = red_l + MT * 64;                // [MT*16]
     float *row_l = row_m + MT * 16;
@@ -368,6 +368,9 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         }
 
         // ----------------------------------------------- merge the 4 column warps
+        // Each warp leaves its unnormalised partial (o, m, l) in shared memory;
+        // after one barrier every thread of the row tile combines the four
+        // partials of its output elements with the log-sum-exp weights.
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -377,80 +380,66 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
             rm[pq * 16 + g] = m0; rm[pq * 16 + g + 8] = m1;
             rl[pq * 16 + g] = l0; rl[pq * 16 + g + 8] = l1;
         }
-        named_bar_sync(2 + mt, 128);
-        float M0 = NEG_INF, M1 = NEG_INF;
+        float *cbase = comb + mt * 4 * 16 * CS;
+        {
+            float *pw = cbase + pq * 16 * CS;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            M0 = fmaxf(M0, rm[w * 16 + g]);
-            M1 = fmaxf(M1, rm[w * 16 + g + 8]);
-        }
-        const float Mu0 = M0 == NEG_INF ? 0.f : M0, Mu1 = M1 == NEG_INF ? 0.f : M1;
-        float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            L0 += rl[w * 16 + g] * fast_exp2((rm[w * 16 + g] - Mu0) * sl);
-            L1 += rl[w * 16 + g + 8] * fast_exp2((rm[w * 16 + g + 8] - Mu1) * sl);
-        }
-        const float f0 = fast_exp2((m0 - Mu0) * sl), f1 = fast_exp2((m1 - Mu1) * sl);
-        if (pq == 0 && t4 == 0) {
-            row_m[mt * 16 + g] = M0; row_m[mt * 16 + g + 8] = M1;
-            row_l[mt * 16 + g] = L0; row_l[mt * 16 + g + 8] = L1;
-        }
-        float *cb = comb + mt * 16 * CS;
-#pragma unroll 1
-        for (int w = 0; w < 4; ++w) {
-            if (pq == w) {
-#pragma unroll
-                for (int n = 0; n < ND; ++n) {
-                    float2 *d0 = reinterpret_cast<float2 *>(cb + g * CS + n * 8 + 2 * t4);
-                    float2 *d1 = reinterpret_cast<float2 *>(cb + (g + 8) * CS + n * 8 + 2 * t4);
-                    float2 v0 = make_float2(o[n][0] * f0, o[n][1] * f0);
-                    float2 v1 = make_float2(o[n][2] * f1, o[n][3] * f1);
-                    if (w) {
-                        const float2 a = *d0, bb = *d1;
-                        v0.x += a.x; v0.y += a.y; v1.x += bb.x; v1.y += bb.y;
-                    }
-                    *d0 = v0;
-                    *d1 = v1;
-                }
+            for (int n = 0; n < ND; ++n) {
+                *reinterpret_cast<float2 *>(pw + g * CS + n * 8 + 2 * t4) = make_float2(o[n][0], o[n][1]);
+                *reinterpret_cast<float2 *>(pw + (g + 8) * CS + n * 8 + 2 * t4) = make_float2(o[n][2], o[n][3]);
             }
-            named_bar_sync(2 + mt, 128);
         }
+        named_bar_sync(2 + mt, 128);
 
-        // ----------------------------------------------------- write or publish
         const int c_first = cta_of(s.pair_t0, T, C);
         const int c_last = cta_of(s.pair_t0 + s.ntiles - 1, T, C);
+        const bool whole = c_first == c_last;
         __nv_bfloat16 *ob = p.out + (long long)s.b * p.n_q * q_head_stride + (long long)s.h * p.G * D;
-        if (c_first == c_last) {
-            for (int idx = gtid; idx < 16 * (D / 8); idx += 128) {
-                const int row = idx / (D / 8), col = (idx % (D / 8)) * 8;
-                const int r = mt * 16 + row;
-                if (r >= p.M) continue;
-                const float L = row_l[r];
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                const float *src = cb + row * CS + col;
-                uint4 pk;
-                pk.x = pack_bf16(src[0] * inv, src[1] * inv);
-                pk.y = pack_bf16(src[2] * inv, src[3] * inv);
-                pk.z = pack_bf16(src[4] * inv, src[5] * inv);
-                pk.w = pack_bf16(src[6] * inv, src[7] * inv);
-                *reinterpret_cast<uint4 *>(ob + (r / p.G) * q_head_stride + (r % p.G) * D + col) = pk;
+        const int slot = (t_begin >= s.pair_t0) ? 0 : 1;
+        float *po = p.part_o + ((long long)c * 2 + slot) * (MT * 16) * D;
+        float *pml = p.part_ml + ((long long)c * 2 + slot) * (MT * 16) * 2;
+        for (int idx = gtid; idx < 16 * (D / 8); idx += 128) {
+            const int row = idx / (D / 8), col = (idx % (D / 8)) * 8;
+            const int r = mt * 16 + row;
+            if (whole && r >= p.M) continue;
+            float mw[4], Mx = NEG_INF;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                mw[w] = rm[w * 16 + row];
+                Mx = fmaxf(Mx, mw[w]);
             }
+            const float Mu = Mx == NEG_INF ? 0.f : Mx;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float Lr = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float f = fast_exp2((mw[w] - Mu) * sl);
+                Lr += f * rl[w * 16 + row];
+                const float4 a = *reinterpret_cast<const float4 *>(cbase + (w * 16 + row) * CS + col);
+                const float4 bq = *reinterpret_cast<const float4 *>(cbase + (w * 16 + row) * CS + col + 4);
+                acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
+                acc[4] += f * bq.x; acc[5] += f * bq.y; acc[6] += f * bq.z; acc[7] += f * bq.w;
+            }
+            if (whole) {
+                const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
+                uint4 pk;
+                pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                pk.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+                pk.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+                *reinterpret_cast<uint4 *>(ob + (r / p.G) * q_head_stride + (r % p.G) * D + col) = pk;
+            } else {
+                *reinterpret_cast<float4 *>(po + r * D + col) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4 *>(po + r * D + col + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                if (col == 0) {
+                    pml[r * 2] = Mx;
+                    pml[r * 2 + 1] = Lr;
+                }
+            }
+        }
+        if (whole) {
             named_bar_sync(2 + mt, 128);
         } else {
-            const int slot = (t_begin >= s.pair_t0) ? 0 : 1;
-            float *po = p.part_o + ((long long)c * 2 + slot) * (MT * 16) * D;
-            float *pml = p.part_ml + ((long long)c * 2 + slot) * (MT * 16) * 2;
-            for (int idx = gtid; idx < 16 * (D / 4); idx += 128) {
-                const int row = idx / (D / 4), col = (idx % (D / 4)) * 4;
-                const float *src = cb + row * CS + col;
-                *reinterpret_cast<float4 *>(po + (mt * 16 + row) * D + col) =
-                    make_float4(src[0], src[1], src[2], src[3]);
-            }
-            if (gtid < 16) {
-                pml[(mt * 16 + gtid) * 2] = row_m[mt * 16 + gtid];
-                pml[(mt * 16 + gtid) * 2 + 1] = row_l[mt * 16 + gtid];
-            }
             named_bar_sync(1, NCW * 32);
             if (ctid == 0) {
                 const int pair = s.b * p.H_kv + s.h;
@@ -517,7 +506,7 @@ static int env_int(const char *name, int dflt) {
 template <int D, int MT>
 static size_t attn_fixed_smem(int B) {
     return 1024 /* alignment slack */ + 2 * (size_t)(D / 64) * MT * 16 * 128 /* query ring */ +
-           (size_t)MT * 16 * (D + 4) * 4 + (size_t)MT * 64 * 4 * 2 + (size_t)MT * 16 * 4 * 2 +
+           (size_t)MT * 4 * 16 * (D + 4) * 4 + (size_t)MT * 64 * 4 * 2 + (size_t)MT * 16 * 4 * 2 +
            (2 * kMaxStages + 4) * 8 + 16 + kMaxContrib * 4 + (size_t)(B + 1) * 4;
 }
 
