@@ -315,31 +315,52 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     omega_hat = float((pipe.n_acc.float() + 1).mean().item())
 
     # ---------------------------------------------- end to end from host buffers
+    # Every step copies that step's inputs from pinned host memory -- the
+    # queries of every layer and draft step, the logits, draft tokens and
+    # uniforms -- and reads n_acc / out_tok back.  The copies run on a copy
+    # stream into per-layer buffers; the compute stream waits on per-layer
+    # events, so the transfer overlaps the attention of earlier layers.
     h_qd = pipe.q_draft.cpu().pin_memory()
     h_qv = pipe.q_verify.cpu().pin_memory()
     h_t, h_d = pipe.target.cpu().pin_memory(), pipe.draft.cpu().pin_memory()
     h_tok, h_ua, h_ur = pipe.tok.cpu().pin_memory(), pipe.u_acc.cpu().pin_memory(), pipe.u_res.cpu().pin_memory()
     h_nacc = torch.empty_like(pipe.n_acc, device="cpu").pin_memory()
     h_out = torch.empty_like(pipe.out_tok, device="cpu").pin_memory()
+    d_qd = [[torch.empty_like(pipe.q_draft) for _ in range(w.gamma)] for _ in range(args.layers)]
+    d_qv = [torch.empty_like(pipe.q_verify) for _ in range(args.layers)]
+    copy_stream = torch.cuda.Stream(device)
     h2d = (h_qd.numel() * 2 * w.gamma + h_qv.numel() * 2) * args.layers + \
         (h_t.numel() + h_d.numel() + h_ua.numel() + h_ur.numel()) * 4 + h_tok.numel() * 4
     d2h = (h_nacc.numel() + h_out.numel()) * 4
 
     def e2e_step():
         mbb = mb
-        for _ in range(args.layers):
+        compute = torch.cuda.current_stream(device)
+        layer_ready = []
+        copy_stream.wait_stream(compute)            # the previous step no longer reads these buffers
+        with torch.cuda.stream(copy_stream):
+            for ly in range(args.layers):
+                for g in range(w.gamma):
+                    d_qd[ly][g].copy_(h_qd, non_blocking=True)
+                d_qv[ly].copy_(h_qv, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_stream)
+                layer_ready.append(ev)
+            pipe.target.copy_(h_t, non_blocking=True)
+            pipe.draft.copy_(h_d, non_blocking=True)
+            pipe.tok.copy_(h_tok, non_blocking=True)
+            pipe.u_acc.copy_(h_ua, non_blocking=True)
+            pipe.u_res.copy_(h_ur, non_blocking=True)
+            logits_ready = torch.cuda.Event()
+            logits_ready.record(copy_stream)
+        for ly in range(args.layers):
             mbb.magicdec_streaming_select(pipe.seq_len, w.H_kv, w.n_sink, w.n_recent, idx=pipe.idx, n_sel=pipe.n_sel)
             mbb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc, vc=pipe.vc)
-            for _g in range(w.gamma):
-                pipe.q_draft.copy_(h_qd, non_blocking=True)
-                mbb.magicdec_draft_attn(pipe.q_draft, pipe.kc, pipe.vc, pipe.n_sel, out=pipe.out_d, ws=pipe.ws_attn)
-            pipe.q_verify.copy_(h_qv, non_blocking=True)
-            mbb.magicdec_verify_attn(pipe.q_verify, pipe.k, pipe.v, pipe.seq_len, out=pipe.out_v, ws=pipe.ws_attn)
-        pipe.target.copy_(h_t, non_blocking=True)
-        pipe.draft.copy_(h_d, non_blocking=True)
-        pipe.tok.copy_(h_tok, non_blocking=True)
-        pipe.u_acc.copy_(h_ua, non_blocking=True)
-        pipe.u_res.copy_(h_ur, non_blocking=True)
+            compute.wait_event(layer_ready[ly])
+            for g in range(w.gamma):
+                mbb.magicdec_draft_attn(d_qd[ly][g], pipe.kc, pipe.vc, pipe.n_sel, out=pipe.out_d, ws=pipe.ws_attn)
+            mbb.magicdec_verify_attn(d_qv[ly], pipe.k, pipe.v, pipe.seq_len, out=pipe.out_v, ws=pipe.ws_attn)
+        compute.wait_event(logits_ready)
         mbb.magicdec_spec_accept(pipe.target, pipe.draft, pipe.tok, pipe.u_acc, pipe.u_res, False, n_acc=pipe.n_acc,
                                  out_tok=pipe.out_tok, n_amb=pipe.n_amb, ws=pipe.ws_acc)
         h_nacc.copy_(pipe.n_acc, non_blocking=True)
@@ -356,6 +377,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), device)
+    del d_qd, d_qv
     err_word = mb.magicdec_device_error()
 
     peak, peak_kind = load_peaks()
