@@ -279,7 +279,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                                                   ws=ws_snap), 3)
         t_gat = time_component(lambda: mb.magicdec_gather_kv(pipe.k, pipe.v, sidx, w.snap_budget, kc=skc, vc=svc), 5)
         snap = {"snapkv_select_ms_per_layer": round(t_sel, 4), "snapkv_gather_ms_per_layer": round(t_gat, 4),
-                "snapkv_budget": w.snap_budget, "snapkv_window": w.snap_window}
+                "snapkv_budget": w.snap_budget, "snapkv_window": w.snap_window,
+                # algorithmic bytes: K read once per scoring pass (prefix for the second) + scores
+                "_snap_bytes": 2.0 * w.B * w.L * w.H_kv * w.d * 2 + 8.0 * w.B * w.H_kv * w.L,
+                "_snap_ms": t_sel}
         del q_win, ws_snap, sidx, sn, skc, svc
         torch.cuda.empty_cache()
 
@@ -378,6 +381,32 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), device)
     del d_qd, d_qv
+    graph = None
+    if args.graph:
+        # The same step captured once into a CUDA graph (kernels keep their
+        # programmatic-dependency edges) and replayed: no host work per step.
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            pipe.step()
+        torch.cuda.current_stream(device).wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            pipe.step()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ge0, ge1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ge0.record()
+        for _ in range(args.steps):
+            g.replay()
+        ge1.record()
+        torch.cuda.synchronize()
+        g_ms = max_over_ranks(ge0.elapsed_time(ge1), device)
+        graph = {"value": round(aggregate_rate(world, args.steps, g_ms), 4), "unit": "steps/s",
+                 "ms_per_step": round(g_ms / args.steps, 4)}
+        del g
     err_word = mb.magicdec_device_error()
 
     peak, peak_kind = load_peaks()
@@ -385,6 +414,16 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ver_gbs = vbytes / (ver_ms * 1e-3) / 1e9
     dra_gbs = dbytes / (dra_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
+
+    def row(nbytes, ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "us": round(ms * 1e3, 2),
+                "algorithmic_bytes": nbytes}
+    sg_bytes = 2.0 * 2 * w.B * pipe.cap * w.H_kv * w.d * 2       # gather: read + write K and V rows
+    rows = {"verify_attn": row(vbytes, ver_ms), "draft_attn": row(dbytes, dra_ms),
+            "streaming_select+gather_kv": row(sg_bytes, sel_ms), "spec_accept": row(pipe.accept_bytes(), acc_ms)}
+    if snap:
+        rows["snapkv_select (once per prefill)"] = row(snap.pop("_snap_bytes"), snap.pop("_snap_ms"))
     result = {
         "metric": METRIC,
         "value": round(aggregate_rate(world, args.steps, ms_total), 4),
@@ -407,6 +446,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "roofline": {"bound": "hbm", "kernel": "decode_attn_kernel (verify)", "achieved": round(ver_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(ver_gbs / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": vbytes, "peak_source": peak_kind},
+        "rows_roofline": rows,
         "verify_gbs": round(ver_gbs, 1), "verify_pct_peak": round(100 * ver_gbs / peak, 2),
         "verify_ms_per_layer": round(ver_ms, 4),
         "draft_gbs": round(dra_gbs, 1), "draft_pct_peak": round(100 * dra_gbs / peak, 2),
@@ -423,6 +463,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "clocks": clocks.summary(),
     }
+    if graph:
+        result["cuda_graph"] = graph
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del pipe.kc, pipe.vc
         result["cpu_baseline"] = cpu_baseline(w, args.layers, pipe)
@@ -533,6 +575,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="also time the step captured in a CUDA graph")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling runs on smaller cases)")
     args = ap.parse_args()

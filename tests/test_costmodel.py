@@ -1,0 +1,98 @@
+"""Drafting-strategy selector (MagicDec section 3.1 Eq. 1-2, section 4.1 Eq. 3-4).
+
+Pinned to Eq. 1's series, to the paper's Table 6 (the acceptance rate is recovered from
+the printed Omega by inverting Eq. 1, then the selector's objective must reproduce the
+printed T_SD and speedup), and to exhaustive search for the argmin."""
+import itertools
+import math
+import os
+import random
+
+import pytest
+
+from long_context_self_gb300 import costmodel as cm
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "magicdec_table6.tsv")
+
+
+def table6():
+    lines = [l for l in open(GOLDEN) if l.strip() and not l.startswith("#")]
+    hdr = lines[0].split()
+    return [dict(zip(hdr, l.split())) for l in lines[1:]]
+
+
+def alpha_from_omega(gamma, omega):
+    lo, hi = 0.0, 1.0 - 1e-12
+    for _ in range(200):
+        mid = (lo + hi) / 2
+        if cm.expected_tokens(gamma, mid) < omega:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+@pytest.mark.parametrize("gamma", [0, 1, 3, 7])
+@pytest.mark.parametrize("alpha", [0.0, 0.3, 0.8, 0.99])
+def test_eq1_equals_geometric_series(gamma, alpha):
+    assert math.isclose(cm.expected_tokens(gamma, alpha), sum(alpha ** k for k in range(gamma + 1)), rel_tol=1e-12)
+
+
+def test_eq1_limits():
+    assert cm.expected_tokens(4, 1.0) == 5.0
+    assert cm.expected_tokens(4, 0.0) == 1.0
+
+
+def test_objective_reproduces_table6():
+    rows = table6()
+    assert len(rows) == 8
+    for r in rows:
+        g = int(r["gamma"])
+        a = alpha_from_omega(g, float(r["Omega"]))
+        t_sd = cm.avg_time_per_token(g, a, float(r["gT_D"]) / g, 0.0, float(r["T_V"]))
+        assert abs(t_sd - float(r["T_SD"])) / float(r["T_SD"]) < 0.06, r
+        assert abs(float(r["T_AR"]) / t_sd - float(r["x"])) < 0.08, r
+
+
+def test_select_is_the_exhaustive_argmin():
+    rnd = random.Random(5)
+    for _ in range(50):
+        budgets = [256, 512, 1024, 2048]
+        gammas = [1, 2, 3, 4, 5, 6]
+        t_t = rnd.uniform(1, 3)
+        tim = cm.Timings(t_target=t_t, t_verify={g: t_t * (1 + 0.05 * g * rnd.random()) for g in gammas},
+                         t_draft={K: 0.02 + K / 32000 * t_t for K in budgets},
+                         t_select={("snapkv", K): rnd.uniform(0, 0.05) for K in budgets})
+        alpha = {(m, K): rnd.uniform(0.3, 0.95) for m in ("streaming", "snapkv") for K in budgets}
+        c = cm.select(tim, alpha)
+        best = min(((m, K, g) for (m, K) in alpha for g in gammas),
+                   key=lambda x: cm.avg_time_per_token(x[2], alpha[(x[0], x[1])], tim.t_draft[x[1]],
+                                                       tim.t_select.get((x[0], x[1]), 0.0), tim.t_verify[x[2]]))
+        assert (c.method, c.budget, c.gamma) == best
+        assert math.isclose(c.speedup * c.ratio, 1.0)
+
+
+def test_free_draft_and_kv_bound_verify_give_omega():
+    """T_D -> 0 and T_V = T_T (the long-context, KV-bound limit of section 3.2): speedup = Omega."""
+    tim = cm.Timings(t_target=1.0, t_verify={3: 1.0}, t_draft={512: 0.0})
+    c = cm.select(tim, {("streaming", 512): 0.8})
+    assert math.isclose(c.speedup, cm.expected_tokens(3, 0.8))
+
+
+def test_higher_acceptance_prefers_longer_speculation():
+    gammas = range(1, 12)
+    tim = cm.Timings(t_target=1.0, t_verify={g: 1.0 + 0.02 * g for g in gammas}, t_draft={512: 0.05})
+    g_lo = cm.select(tim, {("streaming", 512): 0.5}).gamma
+    g_hi = cm.select(tim, {("streaming", 512): 0.95}).gamma
+    assert g_hi > g_lo
+
+
+@pytest.mark.gpu
+def test_calibrated_times_show_the_kv_bound_regime():
+    """Section 3.2: at long context verification and decoding load the same KV, so
+    T_V(gamma) / T_T stays close to 1, and a 512-row draft costs a small fraction."""
+    tim = cm.calibrate(B=32, S=32000, budgets=[512], gammas=[3], reps=5)
+    assert 0.9 < tim.t_verify[3] / tim.t_target < 1.3
+    assert tim.t_draft[512] / tim.t_target < 0.2
+    c = cm.select(tim, {("streaming", 512): 0.8})
+    assert c.speedup > 1.0
