@@ -25,10 +25,10 @@
 
 namespace magicdec {
 
-constexpr int kStatChunk = 8192;      // logits per stats CTA
+constexpr int kStatChunk = 1024;      // logits per statistics record (one warp)
 constexpr int kAccChunk = 4096;       // logits per sample CTA
 constexpr int kAccThreads = 256;
-constexpr int kAccPer = kStatChunk / kAccThreads;  // 32 logits per thread, held in registers
+constexpr int kAccPer = kStatChunk / 32;  // 32 logits per lane of a statistics warp, held in registers
 
 // ------------------------------------------------------------ double-float
 struct dflt {
@@ -142,49 +142,58 @@ __device__ __forceinline__ void top_merge(float &t1, float &t2, int &arg, float 
     t2 = fmaxf(fmaxf(t2, u2), lose);
 }
 
+// One record per warp and 1024-logit slice: lane l holds logits
+// t0 + k*128 + 4l .. +3 (float4 path) or t0 + k*32 + l (scalar path), so each
+// load instruction of the warp is coalesced and no block-level reduction is
+// needed.
 __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptParams p) {
-    __shared__ float red_f[kAccThreads / 32][3];
-    __shared__ int red_i[kAccThreads / 32];
-    __shared__ dflt red_df[kAccThreads / 32];
-    __shared__ float chunk_max;
-    const int chunk = blockIdx.x, row = blockIdx.y;
     pdl_trigger();
     pdl_wait();
-    const int b = row / p.rows_per_b, r = row % p.rows_per_b;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * (kAccThreads / 32) + warp;     // (row, record)
+    const long long n_work = (long long)p.B * p.rows_per_b * p.n_stat_chunks;
+    if (gw >= n_work) return;
+    const long long row = gw / p.n_stat_chunks;
+    const int rec = (int)(gw - row * p.n_stat_chunks);
+    const int b = (int)(row / p.rows_per_b), r = (int)(row % p.rows_per_b);
     const float *x = row_ptr(p, b, r);
-    const int t0 = chunk * kStatChunk, t1 = min(t0 + kStatChunk, p.V);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = rec * kStatChunk, t1 = min(t0 + kStatChunk, p.V);
 
     float v[kAccPer];
-    const bool vec = ((p.V & 3) == 0) && (t1 - t0 == kStatChunk);
+    int idx0[kAccPer];
+    const bool vec = ((p.V & 3) == 0);
     if (vec) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(x + t0);
 #pragma unroll
-        for (int k = 0; k < kAccPer / 4; ++k) {
-            float4 q;
-            asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                         : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
-                         : "l"(x4 + k * kAccThreads + tid));
-            v[4 * k] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
+        for (int k2 = 0; k2 < kAccPer / 4; ++k2) {
+            const int t = t0 + k2 * 128 + 4 * lane;
+            float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (t < t1)
+                asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                             : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                             : "l"(x + t));
+            v[4 * k2] = q.x; v[4 * k2 + 1] = q.y; v[4 * k2 + 2] = q.z; v[4 * k2 + 3] = q.w;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) idx0[4 * k2 + e] = t + e;
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < kAccPer; ++k) {
-            const int t = t0 + k * kAccThreads + tid;
-            v[k] = t < t1 ? __ldg(x + t) : -INFINITY;
+        for (int k2 = 0; k2 < kAccPer; ++k2) {
+            const int t = t0 + k2 * 32 + lane;
+            v[k2] = t < t1 ? __ldg(x + t) : -INFINITY;
+            idx0[k2] = t;
         }
     }
-    // index of v[k]: vec -> t0 + 4*(k/4*256 + tid) + k%4; else t0 + k*256 + tid (both increasing in k)
+    // each lane sees its logits in increasing index order: strict ">" keeps the smallest index
     float mx = -INFINITY, top1 = -INFINITY, top2 = -INFINITY;
     int arg = 0x7fffffff;
 #pragma unroll
-    for (int k = 0; k < kAccPer; ++k) {
-        const float e = v[k];
+    for (int k2 = 0; k2 < kAccPer; ++k2) {
+        const float e = v[k2];
         mx = fmaxf(mx, e);
         if (e > top1) {
             top2 = top1;
             top1 = e;
-            arg = vec ? t0 + 4 * ((k >> 2) * kAccThreads + tid) + (k & 3) : t0 + k * kAccThreads + tid;
+            arg = idx0[k2];
         } else if (e > top2) {
             top2 = e;
         }
@@ -196,45 +205,19 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
         const int ua = __shfl_xor_sync(0xffffffffu, arg, o);
         top_merge(top1, top2, arg, u1, u2, ua);
     }
-    mx = warp_max(mx);
-    if (lane == 0) {
-        red_f[warp][0] = mx;
-        red_f[warp][1] = top1;
-        red_f[warp][2] = top2;
-        red_i[warp] = arg;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float m = red_f[0][0], a1 = red_f[0][1], a2 = red_f[0][2];
-        int aa = red_i[0];
-        for (int w = 1; w < kAccThreads / 32; ++w) {
-            m = fmaxf(m, red_f[w][0]);
-            top_merge(a1, a2, aa, red_f[w][1], red_f[w][2], red_i[w]);
-        }
-        chunk_max = m;
-        red_f[0][1] = a1;
-        red_f[0][2] = a2;
-        red_i[0] = aa;
-    }
-    __syncthreads();
-    const float m = chunk_max;
+    const float m = warp_max(mx);
     dflt acc = {0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < kAccPer; ++k) acc = df_add_f(acc, fast_exp2((v[k] - m) * kLog2e));
+    for (int k2 = 0; k2 < kAccPer; ++k2) acc = df_add_f(acc, fast_exp2((v[k2] - m) * kLog2e));
     acc = warp_sum_df(acc);
-    if (lane == 0) red_df[warp] = acc;
-    __syncthreads();
-    if (tid == 0) {
-        dflt t = red_df[0];
-        for (int w = 1; w < kAccThreads / 32; ++w) t = df_add(t, red_df[w]);
-        const double tot = df_to_double(t);
+    if (lane == 0) {
         RowStat st;
-        st.s = tot;
+        st.s = df_to_double(acc);
         st.m = m;
-        st.top1 = red_f[0][1];
-        st.top2 = red_f[0][2];
-        st.arg = red_i[0];
-        p.stats[((long long)b * p.rows_per_b + r) * p.n_stat_chunks + chunk] = st;
+        st.top1 = top1;
+        st.top2 = top2;
+        st.arg = arg;
+        p.stats[row * p.n_stat_chunks + rec] = st;
     }
 }
 
@@ -607,7 +590,9 @@ magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target,
     w += align256a((size_t)B * sizeof(JobInfo));
     prm.chunk_sum = reinterpret_cast<double *>(w);
 
-    magicdec_status s = magicdec_host::launch_pdl(accept_stats_kernel, dim3(prm.n_stat_chunks, B * prm.rows_per_b),
+    const long long n_work = (long long)B * prm.rows_per_b * prm.n_stat_chunks;
+    magicdec_status s = magicdec_host::launch_pdl(accept_stats_kernel,
+                                                  dim3((unsigned)((n_work + kAccThreads / 32 - 1) / (kAccThreads / 32))),
                                                   dim3(kAccThreads), 0, st, prm);
     if (s != MAGICDEC_OK) return s;
     s = magicdec_host::launch_pdl(accept_chain_kernel, dim3(B), dim3(kChainThreads), 0, st, prm);

@@ -45,46 +45,58 @@ __global__ void streaming_select_kernel(const int32_t *seq_len, int B, int H_kv,
 }
 
 // ------------------------------------------------------------------ gather
-// Unit u = one 16-byte chunk of one destination row of K or V:
-//   ch = u % CPR, kv = (u / CPR) % 2, row = u / (2*CPR) = (b*H_kv + h)*n_idx + i.
-// Each thread moves UNROLL units per iteration so that many loads are in flight.
-template <int CPR>
+// A warp moves rows: each lane owns one 16-byte chunk of K or V of a row
+// (2*CPR lanes per row), and each iteration moves RPI rows per row slot so
+// that RPI loads per lane are in flight.  The row -> (sequence, head, slot)
+// decode is done once per row by one lane and broadcast.
+template <int CPR, int RPI>
 __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                                        const int32_t *__restrict__ idx, int H_kv, int L_cap,
-                                                       int n_idx, int cap, unsigned total,
-                                                       uint4 *__restrict__ kc, uint4 *__restrict__ vc) {
-    constexpr int UNROLL = 4;
+                                                       int n_idx, int cap, int rows, uint4 *__restrict__ kc,
+                                                       uint4 *__restrict__ vc) {
+    constexpr int LPR = 2 * CPR;                 // lanes per row (K and V)
+    constexpr int SLOTS = 32 / LPR;              // rows side by side in a warp
+    constexpr int RPW = SLOTS * RPI;             // rows per warp per iteration
+    static_assert(RPW <= 32, "one decoding lane per row");
     pdl_trigger();
     pdl_wait();
-    const unsigned stride = gridDim.x * blockDim.x;
-    for (unsigned base = blockIdx.x * blockDim.x + threadIdx.x; base < total; base += stride * UNROLL) {
-        uint4 val[UNROLL];
-        uint4 *dst[UNROLL];
-#pragma unroll
-        for (int j = 0; j < UNROLL; ++j) {
-            const unsigned u = base + j * stride;
-            dst[j] = nullptr;
-            val[j] = make_uint4(0, 0, 0, 0);
-            if (u < total) {
-                const unsigned ch = u % CPR;
-                const unsigned kv = (u / CPR) & 1u;
-                const unsigned row = u / (2 * CPR);
-                const unsigned bh = row / (unsigned)n_idx;
-                const unsigned i = row - bh * (unsigned)n_idx;
-                const unsigned h = bh % (unsigned)H_kv, b = bh / (unsigned)H_kv;
+    const int lane = threadIdx.x & 31;
+    const int slot = lane / LPR, sub = lane % LPR;
+    const int kv = sub / CPR, ch = sub % CPR;
+    const long long warp0 = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long base = warp0 * RPW; base < rows; base += nwarps * RPW) {
+        // lane j < RPW decodes row base + j
+        long long src_off = -1, dst_off = -1;
+        {
+            const long long row = base + lane;
+            if (lane < RPW && row < rows) {
+                const int bh = (int)(row / n_idx);
+                const int i = (int)(row - (long long)bh * n_idx);
+                const int h = bh % H_kv, b = bh / H_kv;
                 const int pos = __ldg(idx + row);
-                if (pos >= 0 && pos < L_cap) {
-                    const uint4 *src = (kv ? v : k) + (((size_t)b * L_cap + pos) * H_kv + h) * CPR + ch;
-                    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(val[j].x), "=r"(val[j].y), "=r"(val[j].z), "=r"(val[j].w)
-                                 : "l"(src));
-                }
-                dst[j] = (kv ? vc : kc) + ((size_t)bh * cap + i) * CPR + ch;
+                dst_off = ((long long)bh * cap + i) * CPR;
+                if (pos >= 0 && pos < L_cap) src_off = (((long long)b * L_cap + pos) * H_kv + h) * CPR;
+            }
+        }
+        uint4 val[RPI];
+        long long dsto[RPI];
+#pragma unroll
+        for (int r = 0; r < RPI; ++r) {
+            const int j = r * SLOTS + slot;
+            const long long so = __shfl_sync(0xffffffffu, src_off, j);
+            dsto[r] = __shfl_sync(0xffffffffu, dst_off, j);
+            val[r] = make_uint4(0, 0, 0, 0);
+            if (dsto[r] >= 0 && so >= 0) {
+                const uint4 *src = (kv ? v : k) + so + ch;
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(val[r].x), "=r"(val[r].y), "=r"(val[r].z), "=r"(val[r].w)
+                             : "l"(src));
             }
         }
 #pragma unroll
-        for (int j = 0; j < UNROLL; ++j)
-            if (dst[j]) *dst[j] = val[j];
+        for (int r = 0; r < RPI; ++r)
+            if (dsto[r] >= 0) (kv ? vc : kc)[dsto[r] + ch] = val[r];
     }
 }
 
@@ -227,18 +239,18 @@ magicdec_status launch_streaming_select(const int32_t *seq_len, int B, int H_kv,
 magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *k, const void *v,
                                  const int32_t *idx, int n_idx, int cap, void *kc, void *vc, cudaStream_t st) {
     if (n_idx == 0 || B == 0) return MAGICDEC_OK;
-    const long long total = (long long)B * H_kv * n_idx * 2 * (D / 8);
-    if (total >= (1ll << 32)) return MAGICDEC_ERR_UNSUPPORTED;
+    const long long rows = (long long)B * H_kv * n_idx;
+    if (rows >= (1ll << 31)) return MAGICDEC_ERR_UNSUPPORTED;
     const int threads = 256;
-    const long long want = (total + threads * 4 - 1) / (threads * 4);
+    const long long want = (rows + 8 * 8 - 1) / (8 * 8);                // 8 warps x 8 rows per CTA iteration
     const int blocks = (int)std::max<long long>(1, std::min<long long>(want, (long long)magicdec_host::sm_count() * 8));
     const uint4 *k4 = static_cast<const uint4 *>(k), *v4 = static_cast<const uint4 *>(v);
     uint4 *kc4 = static_cast<uint4 *>(kc), *vc4 = static_cast<uint4 *>(vc);
     if (D == 128)
-        return magicdec_host::launch_pdl(gather_kv_kernel<16>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx, H_kv,
-                                         L_cap, n_idx, cap, (unsigned)total, kc4, vc4);
-    return magicdec_host::launch_pdl(gather_kv_kernel<8>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx, H_kv,
-                                     L_cap, n_idx, cap, (unsigned)total, kc4, vc4);
+        return magicdec_host::launch_pdl(gather_kv_kernel<16, 8>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx,
+                                         H_kv, L_cap, n_idx, cap, (int)rows, kc4, vc4);
+    return magicdec_host::launch_pdl(gather_kv_kernel<8, 4>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx, H_kv,
+                                     L_cap, n_idx, cap, (int)rows, kc4, vc4);
 }
 
 size_t snapkv_tc_workspace_bytes(int B, int H_q, int H_kv, int L_cap, int w);
