@@ -60,9 +60,11 @@ def _load():
             lib.oracle_snapkv_select.argtypes = [I, I, I, I, I, P, P, P, I, I, I, P, P, P]
             lib.oracle_spec_accept.argtypes = [I, I, I, P, P, P, P, P, I, P, P, P]
             lib.oracle_resample_weights.argtypes = [P, P, I, P]
+            lib.oracle_topk_attn.argtypes = [I, I, I, I, I, P, P, P, P, I, P, P, P]
             for name in ("oracle_verify_attn", "oracle_draft_attn", "oracle_streaming_select",
                          "oracle_gather_kv", "oracle_snapkv_scores", "oracle_maxpool1d",
-                         "oracle_snapkv_select", "oracle_spec_accept", "oracle_resample_weights"):
+                         "oracle_snapkv_select", "oracle_spec_accept", "oracle_resample_weights",
+                         "oracle_topk_attn"):
                 getattr(lib, name).restype = I
             _lib = lib
     return _lib
@@ -172,6 +174,24 @@ def snapkv_select(q_win, k, seq_len, pool_kernel: int, budget: int):
                                         w, pool_kernel, budget, _ptr(idx), _ptr(n_sel), _ptr(pooled)),
            "snapkv_select")
     return idx, n_sel, pooled
+
+
+def topk_attn(q, k, v, seq_len, top_k: int, want_scores: bool = False):
+    """Top-K attention draft.  q [B,1,H_q,d] u16, k/v [B,L_cap,H_kv,d] u16, seq_len [B]
+    -> (out fp64 [B,1,H_q,d], idx int32 [B,H_q,top_k] ascending, -1 padded,
+        scores fp64 [B,H_q,L_cap] or None)."""
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    seq_len = _c(seq_len, np.int32)
+    B, one, H_q, d = q.shape
+    assert one == 1 and k.shape == v.shape and k.shape[0] == B and k.shape[3] == d
+    L_cap, H_kv = k.shape[1], k.shape[2]
+    out = np.zeros((B, 1, H_q, d), np.float64)
+    idx = np.empty((B, H_q, top_k), np.int32)
+    scores = np.zeros((B, H_q, L_cap), np.float64) if want_scores else None
+    _check(_load().oracle_topk_attn(B, H_q, H_kv, d, L_cap, _ptr(q), _ptr(k), _ptr(v), _ptr(seq_len),
+                                    int(top_k), _ptr(out), _ptr(idx),
+                                    _ptr(scores) if scores is not None else None), "topk_attn")
+    return out, idx, scores
 
 
 def spec_accept(target, draft, draft_tok, u_acc, u_res, greedy: bool):

@@ -22,6 +22,9 @@
  *     window rows and the query heads of a KV group, max-pooled, per-KV-head
  *     top-k, observation window always kept (section 4.4, section 5.2);
  *   - the "pre-gather a sparse KV cache" copy (section 4.4);
+ *   - Top-K attention drafting: each draft query attends to its own top_k
+ *     highest-scoring positions of the full cache (section 1, Figure 1(c);
+ *     section 4.4);
  *   - speculative sampling (Leviathan et al., cited in section 3.1 for
  *     Eq. 1): accept draft token x when u < p(x)/q(x), otherwise resample
  *     from norm(max(0, p - q)); a bonus token from the last target
@@ -374,6 +377,71 @@ int oracle_snapkv_select(int B, int H_q, int H_kv, int d, int L_cap,
         if ((p % H_kv) == 0) n_sel[b] = n;
     }
     free(score);
+    return 0;
+}
+
+/*
+ * Top-K attention draft (section 1, Figure 1(c) and section 4.4: the
+ * dynamic per-query selection that the pages use as the acceptance-rate
+ * upper bound).  For query head hq of sequence b, with len = seq_len[b]
+ * clamped to [0, L_cap], the scores are s_j = scale * q . k_j over the whole
+ * prefix j < len (KV head hq / (H_q/H_kv)).  The top_k positions with the
+ * largest s_j are kept (equal scores: the smaller position first); when
+ * len <= top_k every position is kept.  The output is softmax attention over
+ * the kept positions only:  o = sum_{j in S} softmax_{S}(s)_j v_j.
+ * q [B, 1, H_q, d], k/v [B, L_cap, H_kv, d], out [B, 1, H_q, d] (double).
+ * idx [B, H_q, top_k] receives the kept positions in ascending order, -1
+ * past min(len, top_k).  scores (optional, [B, H_q, L_cap]) receives s_j for
+ * j < len and 0 elsewhere, for margin analysis.
+ */
+int oracle_topk_attn(int B, int H_q, int H_kv, int d, int L_cap,
+                     const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const int32_t *seq_len, int top_k,
+                     double *out, int32_t *idx, double *scores)
+{
+    if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || d <= 0 || L_cap < 0 || top_k <= 0) return -1;
+    const int G = H_q / H_kv;
+    const double scale = 1.0 / sqrt((double)d);
+    long unit;
+#pragma omp parallel for schedule(dynamic)
+    for (unit = 0; unit < (long)B * H_q; ++unit) {
+        const int b = (int)(unit / H_q), hq = (int)(unit % H_q), hk = hq / G;
+        const int len = clamp_len(seq_len[b], L_cap);
+        const uint16_t *qrow = q + ((long)b * H_q + hq) * d;
+        double *o = out + ((long)b * H_q + hq) * d;
+        int32_t *sel = idx + unit * top_k;
+        double *srow = scores ? scores + unit * L_cap : NULL;
+        int c, j, n;
+        for (c = 0; c < d; ++c) o[c] = 0.0;
+        if (srow) for (j = 0; j < L_cap; ++j) srow[j] = 0.0;
+        for (j = 0; j < top_k; ++j) sel[j] = -1;
+        if (len == 0) continue;
+
+        ranked_t *rk = (ranked_t *)malloc(sizeof(ranked_t) * (size_t)len);
+        for (j = 0; j < len; ++j) {
+            const uint16_t *kr = k + (((long)b * L_cap + j) * H_kv + hk) * d;
+            double acc = 0.0;
+            for (c = 0; c < d; ++c) acc += bf16_value(qrow[c]) * bf16_value(kr[c]);
+            rk[j].key = scale * acc;
+            rk[j].pos = j;
+            if (srow) srow[j] = rk[j].key;
+        }
+        n = len <= top_k ? len : top_k;
+        if (len > top_k) qsort(rk, (size_t)len, sizeof(ranked_t), by_score_desc);
+        for (j = 0; j < n; ++j) sel[j] = rk[j].pos;
+        qsort(sel, (size_t)n, sizeof(int32_t), by_int_asc);
+
+        double smax = -INFINITY, den = 0.0;
+        for (j = 0; j < n; ++j) if (rk[j].key > smax) smax = rk[j].key;
+        for (j = 0; j < n; ++j) {
+            const double wgt = exp(rk[j].key - smax);
+            const uint16_t *vr = v + (((long)b * L_cap + rk[j].pos) * H_kv + hk) * d;
+            den += wgt;
+            for (c = 0; c < d; ++c) o[c] += wgt * bf16_value(vr[c]);
+        }
+        for (c = 0; c < d; ++c) o[c] /= den;
+        free(rk);
+    }
     return 0;
 }
 

@@ -120,6 +120,92 @@ def test_verify_equals_draft_on_last_row():
 
 
 # --------------------------------------------------------------------------
+# Top-K attention draft
+# --------------------------------------------------------------------------
+def _topk_reference(q, k, v, seq_len, top_k):
+    """Scores by numpy einsum, the kept set by a lexicographic sort (score desc, position asc),
+    the attention by torch SDPA in fp64 under that keep-mask."""
+    B, _, H_q, d = q.shape
+    H_kv = k.shape[2]
+    G = H_q // H_kv
+    qf = bits_to_f64(q)[:, 0]                                          # [B,H_q,d]
+    kf = np.repeat(bits_to_f64(k).transpose(0, 2, 1, 3), G, axis=1)    # [B,H_q,L,d]
+    vf = np.repeat(bits_to_f64(v).transpose(0, 2, 1, 3), G, axis=1)
+    s = np.einsum("bhd,bhld->bhl", qf, kf) / math.sqrt(d)
+    L_cap = k.shape[1]
+    mask = np.zeros((B, H_q, 1, L_cap), bool)
+    idx = np.full((B, H_q, top_k), -1, np.int32)
+    for b in range(B):
+        n = int(seq_len[b])
+        for h in range(H_q):
+            order = np.lexsort((np.arange(n), -s[b, h, :n]))[:top_k]
+            keep = np.sort(order)
+            mask[b, h, 0, keep] = True
+            idx[b, h, : keep.size] = keep
+    out = sdpa_reference(qf[:, :, None, :], kf, vf, mask)[:, :, 0]     # [B,H_q,d]
+    return out[:, None], idx, s
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,top_k", [(8, 2, 32, 7), (5, 1, 64, 3), (4, 4, 16, 12)])
+def test_topk_attn_matches_masked_sdpa(H_q, H_kv, d, top_k):
+    rng = np.random.default_rng(21)
+    B, L_cap = 4, 50
+    q = bf16_bits(rng.standard_normal((B, 1, H_q, d)))
+    k = bf16_bits(rng.standard_normal((B, L_cap, H_kv, d)))
+    v = bf16_bits(rng.standard_normal((B, L_cap, H_kv, d)))
+    seq_len = np.array([L_cap, top_k - 1 if top_k > 1 else 1, 0, 33], np.int32)
+    got, idx, scores = oracle.topk_attn(q, k, v, seq_len, top_k, want_scores=True)
+    ref, ref_idx, ref_s = _topk_reference(q, k, v, seq_len, top_k)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_array_equal(idx, ref_idx)
+    for b in range(B):
+        n = int(seq_len[b])
+        np.testing.assert_allclose(scores[b, :, :n], ref_s[b, :, :n], rtol=1e-12, atol=1e-13)
+    assert np.all(got[2] == 0.0) and np.all(idx[2] == -1)
+
+
+def test_topk_attn_with_budget_covering_prefix_is_dense_decode():
+    """top_k >= len keeps every position: plain decode attention over the prefix."""
+    rng = np.random.default_rng(22)
+    B, H_q, H_kv, d, L = 2, 4, 2, 32, 30
+    q = bf16_bits(rng.standard_normal((B, 1, H_q, d)))
+    k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    v = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    sl = np.array([L, 17], np.int32)
+    got, idx, _ = oracle.topk_attn(q, k, v, sl, L)
+    G = H_q // H_kv
+    qf = bits_to_f64(q).transpose(0, 2, 1, 3)
+    kf = np.repeat(bits_to_f64(k).transpose(0, 2, 1, 3), G, axis=1)
+    vf = np.repeat(bits_to_f64(v).transpose(0, 2, 1, 3), G, axis=1)
+    mask = np.zeros((B, H_q, 1, L), bool)
+    for b in range(B):
+        mask[b, :, :, : sl[b]] = True
+    ref = sdpa_reference(qf, kf, vf, mask).transpose(0, 2, 1, 3)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_array_equal(idx[1, :, :17], np.broadcast_to(np.arange(17), (H_q, 17)))
+    assert np.all(idx[1, :, 17:] == -1)
+
+
+def test_topk_attn_ties_and_single_winner():
+    rng = np.random.default_rng(23)
+    d, L = 32, 20
+    q = bf16_bits(rng.standard_normal((2, 1, 1, d)))
+    k = bf16_bits(rng.standard_normal((2, L, 1, d)))
+    v = bf16_bits(rng.standard_normal((2, L, 1, d)))
+    # sequence 0: every key identical -> all scores tie -> the smallest positions win
+    k[0, :, 0, :] = k[0, 0, 0, :]
+    # sequence 1: key 13 aligned with the query and twice as long -> top-1 is position 13
+    k[1, 13, 0, :] = bf16_bits(2.0 * bits_to_f64(q[1, 0, 0, :]))
+    sl = np.array([L, L], np.int32)
+    out5, idx5, _ = oracle.topk_attn(q[:1], k[:1], v[:1], sl[:1], 5)
+    np.testing.assert_array_equal(idx5[0, 0], np.arange(5))
+    np.testing.assert_allclose(out5[0, 0, 0], bits_to_f64(v[0, :5, 0, :]).mean(0), rtol=1e-12, atol=1e-13)
+    out1, idx1, _ = oracle.topk_attn(q[1:], k[1:], v[1:], sl[1:], 1)
+    assert idx1[0, 0, 0] == 13
+    np.testing.assert_array_equal(out1[0, 0, 0], bits_to_f64(v[1, 13, 0, :]))
+
+
+# --------------------------------------------------------------------------
 # StreamingLLM selection and gather
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("n_sink,n_recent", [(4, 60), (16, 496), (0, 8), (5, 0)])
