@@ -164,6 +164,35 @@ MAGICDEC_API magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n
                                      const uint16_t *v, const int32_t *seq_len, uint16_t *out, void *ws,
                                      size_t ws_bytes, void *stream);
 
+/* Workspace bytes magicdec_topk_draft_attn needs: fp32 scores of every query
+ * head over the whole cache, B * H_q * (L_cap rounded up to 4) * 4. */
+MAGICDEC_API size_t magicdec_topk_attn_workspace_size(magicdec_kv_shape shape);
+
+/*
+ * Top-K attention draft (paper section 1 and Figure 1(c); section 4.4,
+ * "Static vs Dynamic": the dynamic per-query selection whose acceptance rate
+ * the static methods are compared against, and whose search over the whole
+ * cache is its selection cost).  For query head h of sequence b, with
+ * len = seq_len[b] clamped to [0, L_cap], the scores s_j = q . k_j / sqrt(d)
+ * over j < len are ranked, the top_k largest are kept (equal scores: the
+ * smaller position first; every position when len <= top_k), and
+ *   out = sum_{j kept} softmax(s over the kept positions)_j v_j
+ * (a zero row when len == 0).  Query head h reads KV head h / (H_q/H_kv).
+ *   q [B, 1, H_q, d] bf16;  k, v [B, L_cap, H_kv, d] bf16;  seq_len [B] int32
+ *   out [B, 1, H_q, d] bf16
+ *   idx (nullable) [B, H_q, top_k] int32 out: the kept positions in ascending
+ *       order, -1 after min(len, top_k)
+ *   ws  workspace of magicdec_topk_attn_workspace_size(shape) bytes; no
+ *       initial contents needed
+ * Supported: H_q/H_kv <= 8 and top_k <= 8192 (MAGICDEC_ERR_UNSUPPORTED).
+ * Errors: NULL pointers, bad shape, top_k <= 0, alignment (q, k, v, out, ws),
+ * workspace too small.
+ */
+MAGICDEC_API magicdec_status magicdec_topk_draft_attn(magicdec_kv_shape shape, const uint16_t *q, const uint16_t *k,
+                                                      const uint16_t *v, const int32_t *seq_len, int top_k,
+                                                      uint16_t *out, int32_t *idx, void *ws, size_t ws_bytes,
+                                                      void *stream);
+
 /*
  * Verification attention that allocates nothing (no counterpart in the paper;
  * an addition for callers that cannot allocate device memory, such as a

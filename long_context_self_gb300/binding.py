@@ -48,6 +48,8 @@ _SIGNATURES = {
     "magicdec_draft_attn": ([KVShape, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "magicdec_verify_attn": ([KVShape, _I, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "magicdec_verify_attn_noalloc": ([KVShape, _I, _P, _P, _P, _P, _P, _P], _I),
+    "magicdec_topk_attn_workspace_size": ([KVShape], _S),
+    "magicdec_topk_draft_attn": ([KVShape, _P, _P, _P, _P, _I, _P, _P, _P, _S, _P], _I),
     "magicdec_spec_accept_workspace_size": ([_I, _I, _I], _S),
     "magicdec_spec_accept": ([_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P], _I),
 }
@@ -274,6 +276,41 @@ def magicdec_verify_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tens
     _check("magicdec_verify_attn_noalloc",
            lib().magicdec_verify_attn_noalloc(kv_shape(B, H_q, H_kv, d, L_cap), n_q, _ptr(q), _ptr(k), _ptr(v),
                                               _ptr(seq_len), _ptr(out), _stream(stream, dev)))
+    return out
+
+
+def magicdec_topk_attn_workspace_size(shape: KVShape) -> int:
+    return int(lib().magicdec_topk_attn_workspace_size(shape))
+
+
+def magicdec_topk_draft_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_len: torch.Tensor, top_k: int,
+                             out: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                             ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Top-K attention draft.  q [B, 1, H_q, d], k/v [B, L_cap, H_kv, d], seq_len [B] -> out [B, 1, H_q, d]
+    bf16.  `idx` (optional int32 [B, H_q, top_k]) receives the kept positions, ascending, -1 padded."""
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev)
+    _need(seq_len, "seq_len", torch.int32, dev)
+    B, one, H_q, d = q.shape
+    L_cap, H_kv = k.shape[1], k.shape[2]
+    if one != 1 or k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("q / k / v shapes disagree")
+    shape = kv_shape(B, H_q, H_kv, d, L_cap)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if idx is not None:
+        _need(idx, "idx", torch.int32, dev)
+        if tuple(idx.shape) != (B, H_q, int(top_k)):
+            raise ValueError("idx must be [B, H_q, top_k]")
+    if ws is None:
+        ws = workspace(magicdec_topk_attn_workspace_size(shape), dev, "topk")
+    _check("magicdec_topk_draft_attn",
+           lib().magicdec_topk_draft_attn(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(seq_len), int(top_k), _ptr(out),
+                                          _ptr(idx), _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(stream, dev)))
     return out
 
 

@@ -13,6 +13,10 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
                                    const void *q, const void *k, const void *v, const int32_t *len, void *out,
                                    void *ws, cudaStream_t st);
 size_t attn_workspace_bytes(int B, int H_kv, int D, int M);
+size_t topk_workspace_bytes(int B, int H_q, int L_cap);
+magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,
+                                       const void *v, const int32_t *len, int top_k, void *out, int32_t *idx,
+                                       void *ws, cudaStream_t st);
 magicdec_status launch_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
                                         int32_t *idx, int32_t *n_sel, cudaStream_t st);
 magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *k, const void *v,
@@ -209,6 +213,23 @@ magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n_q, const uin
     if (s != MAGICDEC_OK) return s;
     return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, n_q, 0, q, k, v,
                                         seq_len, out, ws, static_cast<cudaStream_t>(stream));
+}
+
+size_t magicdec_topk_attn_workspace_size(magicdec_kv_shape shape) {
+    if (!shape_ok(shape)) return 0;
+    return magicdec::topk_workspace_bytes(shape.B, shape.H_q, shape.L_cap);
+}
+
+magicdec_status magicdec_topk_draft_attn(magicdec_kv_shape shape, const uint16_t *q, const uint16_t *k,
+                                         const uint16_t *v, const int32_t *seq_len, int top_k, uint16_t *out,
+                                         int32_t *idx, void *ws, size_t ws_bytes, void *stream) {
+    if (!q || !k || !v || !seq_len || !out || !ws) return MAGICDEC_ERR_NULL;
+    if (!shape_ok(shape) || top_k <= 0) return MAGICDEC_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws))
+        return MAGICDEC_ERR_ALIGN;
+    if (ws_bytes < magicdec_topk_attn_workspace_size(shape)) return MAGICDEC_ERR_WORKSPACE;
+    return magicdec::launch_topk_draft_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, q, k, v, seq_len,
+                                            top_k, out, idx, ws, static_cast<cudaStream_t>(stream));
 }
 
 size_t magicdec_spec_accept_workspace_size(int B, int gamma, int V) {

@@ -68,6 +68,42 @@ def check_topk(idx_gpu: np.ndarray, n_sel_gpu: np.ndarray, idx_ora: np.ndarray, 
     return band_total
 
 
+def check_topk_attn(out_gpu: np.ndarray, idx_gpu: np.ndarray, out_ora: np.ndarray, idx_ora: np.ndarray,
+                    scores: np.ndarray, seq_len: np.ndarray, top_k: int, what: str = "topk attention"):
+    """Top-K attention draft under the band rule.  Outside the band |s - tau| <= MARGIN * max(|tau|, 1)
+    (tau = the oracle's top_k-th score) membership must match exactly; inside it only the count.
+    Heads whose kept set differs from the oracle's (inside the band) are left out of the element-wise
+    output comparison.  Returns (heads with a band swap, band positions)."""
+    B, H, _ = idx_ora.shape
+    swapped, band_total = 0, 0
+    keep = np.ones((B, H), bool)
+    for b in range(B):
+        L = int(seq_len[b])
+        n = min(L, top_k)
+        for h in range(H):
+            g, o = idx_gpu[b, h], idx_ora[b, h]
+            assert np.all(g[n:] == -1), (b, h, "padding")
+            if L <= top_k:
+                assert np.array_equal(g, o), (b, h)
+                continue
+            gs = g[:n]
+            assert np.all(np.diff(gs) > 0) and gs[0] >= 0 and gs[-1] < L, (b, h, "not ascending / out of range")
+            sc = scores[b, h, :L]
+            tau = np.sort(sc)[::-1][top_k - 1]
+            band = np.abs(sc - tau) <= MARGIN * max(abs(tau), 1.0)
+            band_total += int(band.sum())
+            sel_g = np.zeros(L, bool)
+            sel_g[gs] = True
+            sel_o = np.zeros(L, bool)
+            sel_o[o[:n]] = True
+            assert np.array_equal(sel_g[~band], sel_o[~band]), (b, h, "membership outside band")
+            if not np.array_equal(sel_g, sel_o):
+                swapped += 1
+                keep[b, h] = False
+    check_attention(out_gpu[:, 0][keep], out_ora[:, 0][keep], what)
+    return swapped, band_total
+
+
 SAMPLE_EDGE_TOL = 1e-7     # inverse-CDF edge margin, relative to the total weight
 
 

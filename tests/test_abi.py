@@ -85,6 +85,16 @@ def test_null_and_shape_errors_are_reported_before_launch(lib):
                                     1 << 30, NULL) == -2
     assert lib.magicdec_spec_accept(4, 3, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, NULL, FAKE,
                                     8, NULL) == -4
+    big = 1 << 40
+    assert lib.magicdec_topk_draft_attn(shape(), NULL, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, big, NULL) == -1
+    assert lib.magicdec_topk_draft_attn(shape(), FAKE, FAKE, FAKE, FAKE, 0, FAKE, NULL, FAKE, big, NULL) == -2
+    assert lib.magicdec_topk_draft_attn(shape(d=96), FAKE, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, big, NULL) == -2
+    assert lib.magicdec_topk_draft_attn(shape(), FAKE, MISALIGNED, FAKE, FAKE, 16, FAKE, NULL, FAKE, big, NULL) == -3
+    assert lib.magicdec_topk_draft_attn(shape(), FAKE, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, 64, NULL) == -4
+    # more than 8 query heads per KV head, or a budget past 8192: valid shapes with no kernel
+    assert lib.magicdec_topk_draft_attn(shape(H_q=32, H_kv=2), FAKE, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, big,
+                                        NULL) == -5
+    assert lib.magicdec_topk_draft_attn(shape(), FAKE, FAKE, FAKE, FAKE, 8193, FAKE, NULL, FAKE, big, NULL) == -5
 
 
 def test_workspace_sizes_are_positive_and_monotone(lib):
@@ -92,6 +102,8 @@ def test_workspace_sizes_are_positive_and_monotone(lib):
     b = lib.magicdec_snapkv_workspace_size(shape(L=4000), 32)
     assert 0 < a < b
     assert lib.magicdec_snapkv_workspace_size(shape(d=80), 32) == 0
+    assert lib.magicdec_topk_attn_workspace_size(shape(B=2, H_q=8, L=61)) == 2 * 8 * 64 * 4
+    assert lib.magicdec_topk_attn_workspace_size(shape(d=80)) == 0
     s1 = lib.magicdec_spec_accept_workspace_size(4, 3, 128256)
     s2 = lib.magicdec_spec_accept_workspace_size(8, 3, 128256)
     assert 0 < s1 < s2

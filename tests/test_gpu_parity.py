@@ -10,7 +10,7 @@ import torch
 import oracle
 from long_context_self_gb300 import binding as mb
 from long_context_self_gb300 import synth
-from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, to_u16
+from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, check_topk_attn, to_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -175,6 +175,55 @@ def test_snapkv_select_matches_oracle(B, H_q, H_kv, d, L_cap, w, pool, budget, l
     # max-pooling copies each local maximum to up to `pool` neighbours, so a
     # plateau or two at the threshold per (sequence, KV head) is expected
     assert band <= 2 * pool * B * H_kv + 8, f"too many band positions: {band}"
+
+
+# ------------------------------------------------------------ Top-K attention
+TOPK_CASES = [
+    # B, H_q, H_kv, d, L_cap, top_k, lens
+    (2, 4, 1, 64, 256, 48, [256, 200]),                                # the tiny workload's shape
+    (4, 32, 8, 128, 3000, 512, [3000, 2999, 513, 0]),                  # Llama-3.1-8B heads, k+1, empty
+    (3, 40, 8, 128, 2100, 256, [2100, 256, 100]),                      # G=5; len == k; len < k
+    (2, 16, 2, 64, 1500, 1, [1500, 1]),                                # G=8, top-1
+    (2, 8, 2, 128, 70000, 2048, [70000, 41000]),                       # keys too long for shared memory
+]
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,d,L_cap,top_k,lens", TOPK_CASES)
+def test_topk_draft_attn_matches_oracle(B, H_q, H_kv, d, L_cap, top_k, lens):
+    q = rand_bf16((B, 1, H_q, d), 41)
+    k = rand_bf16((B, L_cap, H_kv, d), 42)
+    v = rand_bf16((B, L_cap, H_kv, d), 43)
+    k[:, ::97] *= 4                                                    # a few dominant keys
+    sl = np.array(lens, np.int32)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_topk_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, scores = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, top_k, want_scores=True)
+    swapped, band = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, scores, sl, top_k)
+    assert swapped <= max(1, B * H_q // 50), f"{swapped} heads swapped a position inside the band"
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(out[b]) == 0
+
+
+def test_topk_draft_attn_ties_go_to_smaller_positions():
+    """Thirty copies of one dominant key and top_k = 10: exactly the ten smallest copies are kept."""
+    B, H_q, H_kv, d, L = 2, 8, 2, 128, 1000
+    q = rand_bf16((B, 1, H_q, d), 44)
+    k = rand_bf16((B, L, H_kv, d), 45)
+    v = rand_bf16((B, L, H_kv, d), 46)
+    pos = torch.randperm(L, generator=torch.Generator().manual_seed(47))[:30]
+    for h in range(H_kv):
+        k[:, pos, h, :] = (q[:, 0, h * (H_q // H_kv), :] * 4).unsqueeze(1)
+    sl = np.array([L, L - 3], np.int32)
+    idx = torch.empty((B, H_q, 10), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_topk_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV), 10, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, _ = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, 10)
+    g = idx.cpu().numpy()
+    for h in range(0, H_q, H_q // H_kv):     # the query head the copies were aligned with
+        assert np.array_equal(g[:, h], idx_o[:, h]), h
+    check_attention(bf16_out_to_f64(out)[:, 0, :: H_q // H_kv], ref[:, 0, :: H_q // H_kv], "topk ties")
 
 
 # ------------------------------------------------------------------ acceptance
