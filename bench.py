@@ -316,6 +316,22 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                      mb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc,
                                                            vc=pipe.vc)), 5)
     omega_hat = float((pipe.n_acc.float() + 1).mean().item())
+    # Top-K attention draft at the same budget: the dynamic-selection draft whose
+    # per-step search reads the whole K cache (timed per call, outside the step)
+    topk = {}
+    if not args.no_topk:
+        tk_idx = torch.empty((w.B, w.H_q, pipe.cap), dtype=torch.int32, device=device)
+        tk_out = torch.empty_like(pipe.q_draft)
+        tk_ws = torch.empty(mb.magicdec_topk_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L)),
+                            dtype=torch.uint8, device=device)
+        tk_ms = time_component(lambda: mb.magicdec_topk_draft_attn(pipe.q_draft, pipe.k, pipe.v, pipe.seq_len,
+                                                                   pipe.cap, out=tk_out, idx=tk_idx, ws=tk_ws), 5)
+        topk = {"topk_draft_us_per_layer": round(tk_ms * 1e3, 2), "topk_budget": pipe.cap,
+                "_topk_bytes": (float(w.B) * w.L * w.H_kv * w.d * 2 + float(w.B) * w.H_q * pipe.cap * w.d * 2
+                                + 2.0 * w.B * w.H_q * w.d * 2),
+                "_topk_ms": tk_ms}
+        del tk_idx, tk_out, tk_ws
+        torch.cuda.empty_cache()
 
     # ---------------------------------------------- end to end from host buffers
     # Every step copies that step's inputs from pinned host memory -- the
@@ -424,6 +440,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "streaming_select+gather_kv": row(sg_bytes, sel_ms), "spec_accept": row(pipe.accept_bytes(), acc_ms)}
     if snap:
         rows["snapkv_select (once per prefill)"] = row(snap.pop("_snap_bytes"), snap.pop("_snap_ms"))
+    if topk:
+        tk_ms = topk.pop("_topk_ms")
+        rows["topk_draft_attn (scores + select + attend, per draft step)"] = row(topk.pop("_topk_bytes"), tk_ms)
+        topk["topk_over_verify"] = round(tk_ms / ver_ms, 4)
     result = {
         "metric": METRIC,
         "value": round(aggregate_rate(world, args.steps, ms_total), 4),
@@ -455,6 +475,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "accept_gbs": round(pipe.accept_bytes() / (acc_ms * 1e-3) / 1e9, 1),
         "select_gather_us_per_layer": round(sel_ms * 1e3, 2),
         **snap,
+        **topk,
         "omega_hat_synthetic": round(omega_hat, 4),
         "tokens_per_s_synthetic": round(world * w.B * omega_hat * args.steps / (ms_total * 1e-3), 1),
         "gpu_launches": pipe.launches_per_step * args.steps,
@@ -575,6 +596,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-topk", action="store_true", help="skip the Top-K attention draft row")
     ap.add_argument("--graph", action="store_true", help="also time the step captured in a CUDA graph")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling runs on smaller cases)")

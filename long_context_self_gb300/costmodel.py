@@ -84,9 +84,13 @@ def select(tim: Timings, alpha: Dict[Tuple[str, int], float], gammas: Optional[I
 
 def calibrate(B: int, S: int, budgets: Sequence[int], gammas: Sequence[int], H_q: int = 32, H_kv: int = 8,
               d: int = 128, reps: int = 10, device: str = "cuda:0", snapkv_window: int = 32,
-              snapkv_steps: Optional[int] = None) -> Timings:
+              snapkv_steps: Optional[int] = None, topk: bool = False) -> Timings:
     """Measure T_T, T_V(gamma), T_D(K) (and the SnapKV selection cost spread over
-    `snapkv_steps` draft steps) for one layer on the current GPU, in ms."""
+    `snapkv_steps` draft steps) for one layer on the current GPU, in ms.  With
+    `topk`, the Top-K attention draft is timed too: its per-step search over the
+    whole cache is charged as T_select = (measured Top-K call) - T_D(K), so that
+    T_D + T_select is the call's time (section 4.4: dynamic selection pays a
+    batch-dependent search at every draft step)."""
     import torch
 
     from . import binding as mb
@@ -122,6 +126,12 @@ def calibrate(B: int, S: int, budgets: Sequence[int], gammas: Sequence[int], H_q
     t_select: Dict[Tuple[str, int], float] = {}
     for K in budgets:
         t_select[("streaming", K)] = 0.0      # sinks + window of the current length: no search
+    if topk:
+        for K in budgets:
+            if K > S:
+                continue
+            t = timed(lambda: mb.magicdec_topk_draft_attn(qd, k, v, sl, K))
+            t_select[("topk", K)] = max(0.0, t - t_draft[K])
     if snapkv_steps:
         q_win = torch.randn((B, snapkv_window, H_q, d), generator=g, device=device).to(torch.bfloat16)
         for K in budgets:
@@ -144,8 +154,10 @@ def main(argv: Optional[Sequence[str]] = None) -> None:
     ap.add_argument("--alpha", type=str, default="{}",
                     help='JSON {"streaming:512": 0.8, "snapkv:2048": 0.9, ...}; default: no selection')
     ap.add_argument("--snapkv-steps", type=int, default=0)
+    ap.add_argument("--topk", action="store_true", help="also time the Top-K attention draft")
     args = ap.parse_args(argv)
-    tim = calibrate(args.B, args.S, args.budgets, args.gammas, snapkv_steps=args.snapkv_steps or None)
+    tim = calibrate(args.B, args.S, args.budgets, args.gammas, snapkv_steps=args.snapkv_steps or None,
+                    topk=args.topk)
     out = {"B": args.B, "S": args.S, "t_target_ms": tim.t_target, "t_verify_ms": tim.t_verify,
            "t_draft_ms": tim.t_draft, "T_V_over_T_T": {g: t / tim.t_target for g, t in tim.t_verify.items()},
            "T_D_over_T_T": {K: t / tim.t_target for K, t in tim.t_draft.items()},

@@ -17,11 +17,15 @@
 //                            stores the fp32 scores [B, H_q, L_sc].
 //   topk_select_attn_kernel  one CTA per (sequence, query head): radix select of
 //                            the top_k scores on the order-preserving 32-bit key
-//                            (12 + 12 + 8 bit digits), ascending compaction, then
+//                            (12 + 12 + 8 bit digits).  The first digit is
+//                            histogrammed from the only DRAM read of the row;
+//                            one L2 re-read collects the positions at or above
+//                            the threshold bin, in ascending order, into a
+//                            short shared-memory list, on which the last two
+//                            digits and the ordered selection run (the whole
+//                            row is searched when the list overflows).  Then the
 //                            softmax over the kept scores and the weighted sum
-//                            of the kept V rows.  The keys stay in shared memory
-//                            when the row fits, else they are re-derived from
-//                            the scores in global memory on every pass.
+//                            of the kept V rows.
 #include "common.cuh"
 
 namespace magicdec {
@@ -30,7 +34,8 @@ constexpr int kTkTileN = 64;                     // positions per K tile
 constexpr int kTkHalfBytes = kTkTileN * 128;     // 64 positions x 64 channels, bf16
 constexpr int kTkConsumers = 4;                  // warps, 16 positions each
 constexpr int kTkMaxStages = 8;
-constexpr int kTkSelThreads = 1024;              // the block scans below assume exactly 32 warps
+constexpr int kTkNT = 512;                       // threads of the select kernel
+constexpr int kTkNW = kTkNT / 32;
 constexpr int kTkBins = 4096;
 constexpr int kTkMaxTopK = 8192;
 constexpr int kTkMaxGroup = 8;                   // query heads per KV head (the mma N extent)
@@ -51,6 +56,7 @@ struct TopkSelParams {
     __nv_bfloat16 *out;       // [B, 1, H_q, D]
     int32_t *idx;             // [B, H_q, top_k] or null
     int B, H_q, H_kv, G, L_cap, L_sc, top_k;
+    int cand_cap;             // shared-memory candidate slots
 };
 
 __device__ __forceinline__ int tk_clamp_len(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
@@ -229,7 +235,7 @@ __device__ __forceinline__ float tk_unkey(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Inclusive block-wide scan (32 warps) in thread order; *total = block sum.
+// Inclusive block-wide scan in thread order over kTkNW warps; *total = block sum.
 __device__ __forceinline__ int tk_block_scan(int v, int *wsum, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
@@ -241,30 +247,31 @@ __device__ __forceinline__ int tk_block_scan(int v, int *wsum, int *total) {
     if (lane == 31) wsum[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int y = wsum[lane];
+        int y = lane < kTkNW ? wsum[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int z = __shfl_up_sync(0xffffffffu, y, o);
             if (lane >= o) y += z;
         }
-        wsum[lane] = y;
+        if (lane < kTkNW) wsum[lane] = y;
     }
     __syncthreads();
     const int excl = warp ? wsum[warp - 1] : 0;
-    *total = wsum[31];
+    *total = wsum[kTkNW - 1];
     __syncthreads();
     return x + excl;
 }
 
-// The digit (bin) holding the remaining-th largest candidate, scanning the
+// The digit (bin) holding the remaining-th largest counted key, scanning the
 // 4096 bins from the top; returns it and the rank left inside that bin.
 __device__ __forceinline__ void tk_find_digit(const int *hist, int remaining, int *wsum, int *s_digit, int *s_rem,
                                               int &digit, int &rem_out) {
+    constexpr int BPT = kTkBins / kTkNT;
     const int tid = threadIdx.x;
-    int cnt[4], sum = 0;
+    int cnt[BPT], sum = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        cnt[j] = hist[kTkBins - 1 - 4 * tid - j];
+    for (int j = 0; j < BPT; ++j) {
+        cnt[j] = hist[kTkBins - 1 - BPT * tid - j];
         sum += cnt[j];
     }
     int total;
@@ -272,9 +279,9 @@ __device__ __forceinline__ void tk_find_digit(const int *hist, int remaining, in
     int above = incl - sum;
     if (above < remaining && remaining <= incl) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < BPT; ++j) {
             if (above < remaining && remaining <= above + cnt[j]) {
-                *s_digit = kTkBins - 1 - 4 * tid - j;
+                *s_digit = kTkBins - 1 - BPT * tid - j;
                 *s_rem = remaining - above;
             }
             above += cnt[j];
@@ -286,17 +293,89 @@ __device__ __forceinline__ void tk_find_digit(const int *hist, int remaining, in
     __syncthreads();
 }
 
-template <int D, bool SMEM_KEYS>
-__global__ void __launch_bounds__(kTkSelThreads, 1) topk_select_attn_kernel(const TopkSelParams p) {
-    constexpr int CPL = D / 32;                  // value channels per lane
+// Keys of 4 consecutive positions j..j+3 (j % 4 == 0) of a score row; positions
+// at or past `hi` give key 0.  The row holds at least len rounded up to 4.
+__device__ __forceinline__ void tk_load4(const float *srow, int j, int hi, uint32_t (&k)[4]) {
+    if (j < hi) {
+        const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + j));
+        k[0] = tk_key(f.x);
+        k[1] = j + 1 < hi ? tk_key(f.y) : 0u;
+        k[2] = j + 2 < hi ? tk_key(f.z) : 0u;
+        k[3] = j + 3 < hi ? tk_key(f.w) : 0u;
+    } else {
+        k[0] = k[1] = k[2] = k[3] = 0u;
+    }
+}
+
+// Selection when more than `cand_cap` positions share or pass the first digit
+// (long runs of equal scores): the last two digits and the ordered
+// compaction run over the whole row, re-read from L2.
+__device__ void tk_select_full_row(const float *srow, int len, int top_k, int d1, int rem, int *hist, int *sel,
+                                   int *wsum, int *s_digit, int *s_rem) {
+    const int tid = threadIdx.x;
+    int d2, d3;
+    for (int i = tid; i < kTkBins; i += kTkNT) hist[i] = 0;
+    __syncthreads();
+    for (int j = tid; j < len; j += kTkNT) {
+        const uint32_t k = tk_key(srow[j]);
+        if ((int)(k >> 20) == d1) atomicAdd(&hist[(k >> 8) & 4095u], 1);
+    }
+    __syncthreads();
+    tk_find_digit(hist, rem, wsum, s_digit, s_rem, d2, rem);
+    for (int i = tid; i < kTkBins; i += kTkNT) hist[i] = 0;
+    __syncthreads();
+    const uint32_t pre = ((uint32_t)d1 << 12) | (uint32_t)d2;
+    for (int j = tid; j < len; j += kTkNT) {
+        const uint32_t k = tk_key(srow[j]);
+        if ((k >> 8) == pre) atomicAdd(&hist[k & 255u], 1);
+    }
+    __syncthreads();
+    tk_find_digit(hist, rem, wsum, s_digit, s_rem, d3, rem);
+    const uint32_t tau = (pre << 8) | (uint32_t)d3;
+    const int need_eq = rem;
+    int gt_seen = 0, eq_seen = 0;
+    for (int base = 0; base < len; base += 4 * kTkNT) {
+        const int j0 = base + 4 * tid;
+        uint32_t kk[4];
+        tk_load4(srow, j0, len, kk);
+        int ngt = 0, neq = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ngt += kk[e] > tau;
+            neq += kk[e] == tau;
+        }
+        const int packed = (ngt << 16) | neq;
+        int total;
+        const int excl = tk_block_scan(packed, wsum, &total) - packed;
+        int gb = gt_seen + (excl >> 16), eb = eq_seen + (excl & 0xffff);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (kk[e] > tau) {
+                sel[gb + min(eb, need_eq)] = j0 + e;
+                ++gb;
+            } else if (kk[e] == tau) {
+                if (eb < need_eq) sel[gb + eb] = j0 + e;
+                ++eb;
+            }
+        }
+        gt_seen += total >> 16;
+        eq_seen += total & 0xffff;
+    }
+    (void)top_k;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSelParams p) {
+    constexpr int NW = kTkNW;
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    int *hist = reinterpret_cast<int *>(smem_raw);                 // [4096]; later [32][D] partial outputs
-    int *sel = hist + kTkBins;                                     // [top_k rounded to 4]
-    uint32_t *ky = reinterpret_cast<uint32_t *>(sel + ((p.top_k + 3) & ~3));   // [L_sc] (SMEM_KEYS)
-    __shared__ int wsum[32];
-    __shared__ int s_digit, s_rem;
+    int *hist = reinterpret_cast<int *>(smem_raw);                    // [4096]; later [NW][D] partial outputs
+    int *cand_pos = hist + kTkBins;                                   // [cand_cap]
+    uint32_t *cand_key = reinterpret_cast<uint32_t *>(cand_pos + p.cand_cap);   // [cand_cap]
+    int *sel = reinterpret_cast<int *>(cand_key + p.cand_cap);        // [top_k]
+    __shared__ int wsum[32], woff[NW], wcnt[NW];
+    __shared__ int s_digit, s_rem, s_total, s_over;
     __shared__ unsigned s_maxkey;
-    __shared__ float zsum[32];
+    __shared__ float zsum[NW];
 
     const int hq = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -310,37 +389,33 @@ __global__ void __launch_bounds__(kTkSelThreads, 1) topk_select_attn_kernel(cons
     int32_t *idx_row = p.idx ? p.idx + row * p.top_k : nullptr;
     const int n = min(len, p.top_k);
     if (len == 0) {
-        for (int c = tid; c < D; c += blockDim.x) o[c] = __float2bfloat16(0.f);
+        for (int c = tid; c < D; c += kTkNT) o[c] = __float2bfloat16(0.f);
         if (idx_row)
-            for (int i = tid; i < p.top_k; i += blockDim.x) idx_row[i] = -1;
+            for (int i = tid; i < p.top_k; i += kTkNT) idx_row[i] = -1;
         return;
     }
     const bool select = len > p.top_k;
-    auto key_at = [&](int j) -> uint32_t {
-        if (SMEM_KEYS) return ky[j];
-        return tk_key(srow[j]);
-    };
+    // warp w owns positions [lo, hi): contiguous segments keep the ascending order
+    const int seg = (((len + NW - 1) / NW) + 3) & ~3;
+    const int lo = min(len, warp * seg), hi = min(len, lo + seg);
 
-    // Keys, the first-digit histogram and the largest key.  The row starts on
-    // a 16-byte boundary (L_sc % 4 == 0) and L_sc >= len rounded up to 4.
-    for (int i = tid; i < kTkBins; i += blockDim.x) hist[i] = 0;
+    // 1. first-digit histogram and the largest key (the scores' only DRAM read)
+    for (int i = tid; i < kTkBins; i += kTkNT) hist[i] = 0;
     if (tid == 0) s_maxkey = 0u;
     __syncthreads();
     uint32_t mk = 0u;
-    const int n4 = (len + 3) >> 2;
-    for (int i4 = tid; i4 < n4; i4 += blockDim.x) {
-        const float4 f = __ldg(reinterpret_cast<const float4 *>(srow) + i4);
-        uint32_t k4[4] = {tk_key(f.x), tk_key(f.y), tk_key(f.z), tk_key(f.w)};
+    for (int base = lo; base < hi; base += 4 * 128) {
+        uint32_t kk[4][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (4 * i4 + e >= len) {
-                k4[e] = 0u;
-            } else {
-                mk = max(mk, k4[e]);
-                if (select) atomicAdd(&hist[k4[e] >> 20], 1);
+        for (int u = 0; u < 4; ++u) tk_load4(srow, base + 128 * u + 4 * lane, hi, kk[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (kk[u][e] == 0u) continue;
+                mk = max(mk, kk[u][e]);
+                if (select) atomicAdd(&hist[kk[u][e] >> 20], 1);
             }
-        }
-        if (SMEM_KEYS) reinterpret_cast<uint4 *>(ky)[i4] = make_uint4(k4[0], k4[1], k4[2], k4[3]);
     }
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o2));
@@ -348,124 +423,190 @@ __global__ void __launch_bounds__(kTkSelThreads, 1) topk_select_attn_kernel(cons
     __syncthreads();
 
     if (select) {
-        // radix select of the top_k-th key tau; need_eq = how many keys equal
-        // to tau are kept (the ones at the smallest positions)
-        int d1, d2, d3, rem;
-        tk_find_digit(hist, p.top_k, wsum, &s_digit, &s_rem, d1, rem);
-        for (int i = tid; i < kTkBins; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
-        for (int j = tid; j < len; j += blockDim.x) {
-            const uint32_t k = key_at(j);
-            if ((int)(k >> 20) == d1) atomicAdd(&hist[(k >> 8) & 4095u], 1);
-        }
-        __syncthreads();
-        tk_find_digit(hist, rem, wsum, &s_digit, &s_rem, d2, rem);
-        for (int i = tid; i < kTkBins; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
-        const uint32_t pre = ((uint32_t)d1 << 12) | (uint32_t)d2;
-        for (int j = tid; j < len; j += blockDim.x) {
-            const uint32_t k = key_at(j);
-            if ((k >> 8) == pre) atomicAdd(&hist[k & 255u], 1);
-        }
-        __syncthreads();
-        tk_find_digit(hist, rem, wsum, &s_digit, &s_rem, d3, rem);
-        const uint32_t tau = (pre << 8) | (uint32_t)d3;
-        const int need_eq = rem;
-
-        // ascending compaction: a kept position's slot is (#greater before it)
-        // + min(#equal before it, need_eq)
-        int gt_seen = 0, eq_seen = 0;
-        for (int base = 0; base < len; base += 4 * kTkSelThreads) {
-            const int j0 = base + 4 * tid;
-            uint32_t kk[4];
-            int ngt = 0, neq = 0;
+        int d1, rem1;
+        tk_find_digit(hist, p.top_k, wsum, &s_digit, &s_rem, d1, rem1);
+        // 2. candidates = positions whose first digit is >= d1.  One L2 re-read;
+        //    warp w appends its segment's candidates, in ascending order, to its
+        //    own R slots of the list.
+        const int R = p.cand_cap / NW;
+        int *my_pos = cand_pos + warp * R;
+        uint32_t *my_key = cand_key + warp * R;
+        int cnt = 0;
+        for (int base = lo; base < hi; base += 4 * 128) {
+            uint32_t kk[4][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                kk[e] = j0 + e < len ? key_at(j0 + e) : 0u;
-                ngt += kk[e] > tau;
-                neq += kk[e] == tau;
+            for (int u = 0; u < 4; ++u) tk_load4(srow, base + 128 * u + 4 * lane, hi, kk[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                int c = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c += kk[u][e] != 0u && (int)(kk[u][e] >> 20) >= d1;
+                int x = c;
+#pragma unroll
+                for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o2);
+                    if (lane >= o2) x += y;
+                }
+                int at = cnt + x - c;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (kk[u][e] != 0u && (int)(kk[u][e] >> 20) >= d1) {
+                        if (at < R) {
+                            my_pos[at] = base + 128 * u + 4 * lane + e;
+                            my_key[at] = kk[u][e];
+                        }
+                        ++at;
+                    }
+                cnt += __shfl_sync(0xffffffffu, x, 31);
+            }
+        }
+        if (lane == 0) wcnt[warp] = cnt;
+        __syncthreads();
+        if (warp == 0) {
+            const int c = lane < NW ? wcnt[lane] : 0;
+            const bool over = __any_sync(0xffffffffu, c > R);
+            int x = c;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o2);
+                if (lane >= o2) x += y;
+            }
+            if (lane < NW) woff[lane] = x - c;
+            if (lane == 31) {
+                s_total = x;
+                s_over = over ? 1 : 0;
+            }
+        }
+        __syncthreads();
+        const int n_cand = s_total;
+        if (s_over) {
+            tk_select_full_row(srow, len, p.top_k, d1, rem1, hist, sel, wsum, &s_digit, &s_rem);
+        } else {
+            // 3. the last two digits, over the candidates of bin d1 only
+            int d2, d3, rem;
+            for (int i = tid; i < kTkBins; i += kTkNT) hist[i] = 0;
+            __syncthreads();
+            for (int i = tid; i < NW * R; i += kTkNT) {
+                if (i - (i / R) * R >= wcnt[i / R]) continue;
+                const uint32_t k = cand_key[i];
+                if ((int)(k >> 20) == d1) atomicAdd(&hist[(k >> 8) & 4095u], 1);
+            }
+            __syncthreads();
+            tk_find_digit(hist, rem1, wsum, &s_digit, &s_rem, d2, rem);
+            for (int i = tid; i < kTkBins; i += kTkNT) hist[i] = 0;
+            __syncthreads();
+            const uint32_t pre = ((uint32_t)d1 << 12) | (uint32_t)d2;
+            for (int i = tid; i < NW * R; i += kTkNT) {
+                if (i - (i / R) * R >= wcnt[i / R]) continue;
+                const uint32_t k = cand_key[i];
+                if ((k >> 8) == pre) atomicAdd(&hist[k & 255u], 1);
+            }
+            __syncthreads();
+            tk_find_digit(hist, rem, wsum, &s_digit, &s_rem, d3, rem);
+            const uint32_t tau = (pre << 8) | (uint32_t)d3;
+            const int need_eq = rem;
+            // 4. ordered selection over the candidates: list index g lives in
+            //    warp w's slots where woff[w] <= g < woff[w] + wcnt[w]; thread t
+            //    takes g in [t*E, (t+1)*E)
+            const int E = (n_cand + kTkNT - 1) / kTkNT;
+            const int c0 = min(n_cand, tid * E), c1 = min(n_cand, c0 + E);
+            int w0 = 0;
+            while (w0 + 1 < NW && c0 >= woff[w0 + 1]) ++w0;
+            int ngt = 0, neq = 0;
+            for (int g = c0, w = w0; g < c1; ++g) {
+                while (w + 1 < NW && g >= woff[w + 1]) ++w;
+                const uint32_t k = cand_key[w * R + g - woff[w]];
+                ngt += k > tau;
+                neq += k == tau;
             }
             const int packed = (ngt << 16) | neq;
             int total;
             const int excl = tk_block_scan(packed, wsum, &total) - packed;
-            int gb = gt_seen + (excl >> 16), eb = eq_seen + (excl & 0xffff);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (kk[e] > tau) {
-                    sel[gb + min(eb, need_eq)] = j0 + e;
+            int gb = excl >> 16, eb = excl & 0xffff;
+            for (int g = c0, w = w0; g < c1; ++g) {
+                while (w + 1 < NW && g >= woff[w + 1]) ++w;
+                const int slot = w * R + g - woff[w];
+                const uint32_t k = cand_key[slot];
+                if (k > tau) {
+                    sel[gb + min(eb, need_eq)] = cand_pos[slot];
                     ++gb;
-                } else if (kk[e] == tau) {
-                    if (eb < need_eq) sel[gb + eb] = j0 + e;
+                } else if (k == tau) {
+                    if (eb < need_eq) sel[gb + eb] = cand_pos[slot];
                     ++eb;
                 }
             }
-            gt_seen += total >> 16;
-            eq_seen += total & 0xffff;
         }
     } else {
-        for (int i = tid; i < len; i += blockDim.x) sel[i] = i;
+        for (int i = tid; i < len; i += kTkNT) sel[i] = i;
     }
     __syncthreads();
 
-    // softmax over the kept scores (the largest key is always kept) and the
-    // weighted sum of their V rows; warp w takes kept entries w, w+32, ...
+    // 5. softmax over the kept scores (the largest key is always kept) and the
+    //    weighted sum of their V rows.  A V row is LPR lanes x 16 bytes, so one
+    //    load instruction of a warp covers RPI rows; part r of warp w takes kept
+    //    entries w + NW * (RPI * t + r).
+    constexpr int LPR = D / 8;
+    constexpr int RPI = 32 / LPR;
+    const int sub = lane % LPR, part = lane / LPR;
     const float m_log2 = tk_unkey(s_maxkey) * kLog2e;
-    float acc[CPL];
+    float acc[8];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    for (int c = 0; c < 8; ++c) acc[c] = 0.f;
     float z = 0.f;
-    const __nv_bfloat16 *vb = p.v + ((long long)b * p.L_cap * p.H_kv + kvh) * D + lane * CPL;
+    const __nv_bfloat16 *vb = p.v + ((long long)b * p.L_cap * p.H_kv + kvh) * D + sub * 8;
     const long long vstride = (long long)p.H_kv * D;
-    constexpr int U = 4;
-    for (int i0 = warp; i0 < n; i0 += 32 * U) {
-        float wgt[U];
-        uint32_t raw[U][CPL / 2];
+    constexpr int U = 2;
+    for (int t0 = 0; warp + NW * RPI * t0 < n; t0 += U) {
+        float sc[U];
+        uint4 raw[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * 32;
-            wgt[u] = 0.f;
-#pragma unroll
-            for (int c = 0; c < CPL / 2; ++c) raw[u][c] = 0u;
+            const int i = warp + NW * (RPI * (t0 + u) + part);
+            sc[u] = -INFINITY;
+            raw[u] = make_uint4(0u, 0u, 0u, 0u);
             if (i < n) {
                 const int j = sel[i];
-                wgt[u] = fast_exp2(tk_unkey(key_at(j)) * kLog2e - m_log2);
-                const uint32_t *src = reinterpret_cast<const uint32_t *>(vb + (long long)j * vstride);
-                if (CPL == 4) {
-                    const uint2 t = __ldg(reinterpret_cast<const uint2 *>(src));
-                    raw[u][0] = t.x;
-                    raw[u][CPL / 2 - 1] = t.y;
-                } else {
-                    raw[u][0] = __ldg(src);
-                }
+                sc[u] = __ldg(srow + j);
+                raw[u] = __ldg(reinterpret_cast<const uint4 *>(vb + (long long)j * vstride));
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            z += wgt[u];
+            const float wgt = fast_exp2(sc[u] * kLog2e - m_log2);
+            z += wgt;
+            const uint32_t w4[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
-            for (int c = 0; c < CPL / 2; ++c) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[u][c]));
-                acc[2 * c] = fmaf(wgt[u], f.x, acc[2 * c]);
-                acc[2 * c + 1] = fmaf(wgt[u], f.y, acc[2 * c + 1]);
+            for (int c = 0; c < 4; ++c) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[c]));
+                acc[2 * c] = fmaf(wgt, f.x, acc[2 * c]);
+                acc[2 * c + 1] = fmaf(wgt, f.y, acc[2 * c + 1]);
             }
         }
     }
-    float *red = reinterpret_cast<float *>(hist);   // [32][D]; the histogram is no longer read
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) red[warp * D + lane * CPL + c] = acc[c];
+    for (int o2 = LPR; o2 < 32; o2 <<= 1) {
+        z += __shfl_xor_sync(0xffffffffu, z, o2);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], o2);
+    }
+    float *red = reinterpret_cast<float *>(hist);   // [NW][D]; the histogram is no longer read
+    if (part == 0) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) red[warp * D + sub * 8 + c] = acc[c];
+    }
     if (lane == 0) zsum[warp] = z;
     __syncthreads();
     if (tid < D) {
         float s = 0.f, zz = 0.f;
-#pragma unroll 8
-        for (int w = 0; w < 32; ++w) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
             s += red[w * D + tid];
             zz += zsum[w];
         }
         o[tid] = __float2bfloat16(s / zz);
     }
     if (idx_row)
-        for (int i = tid; i < p.top_k; i += blockDim.x) idx_row[i] = i < n ? sel[i] : -1;
+        for (int i = tid; i < p.top_k; i += kTkNT) idx_row[i] = i < n ? sel[i] : -1;
 }
 
 // ------------------------------------------------------------------- host side
@@ -495,20 +636,15 @@ static magicdec_status launch_topk_impl(const TopkScoreParams &sp, const TopkSel
                                                   dim3((kTkConsumers + 1) * 32), smem1, st, tmk, s1);
     if (s != MAGICDEC_OK) return s;
 
-    const size_t sel_bytes = (size_t)kTkBins * 4 + (size_t)((tp.top_k + 3) & ~3) * 4;
-    const size_t key_bytes = (size_t)tp.L_sc * 4;
-    const size_t static_reserve = 2048;
-    if (sel_bytes + key_bytes + static_reserve <= (size_t)smem_cap) {
-        auto k2 = topk_select_attn_kernel<D, true>;
-        const size_t smem2 = sel_bytes + key_bytes;
-        if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
-            return MAGICDEC_ERR_CUDA;
-        return magicdec_host::launch_pdl(k2, dim3(tp.H_q, tp.B), dim3(kTkSelThreads), smem2, st, tp);
-    }
-    auto k2 = topk_select_attn_kernel<D, false>;
-    if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_bytes) != cudaSuccess)
+    // candidates: the top_k plus room for the threshold bin's other members
+    TopkSelParams t2 = tp;
+    t2.cand_cap = tp.top_k + 4096;
+    const size_t smem2 = (size_t)kTkBins * 4 + (size_t)t2.cand_cap * 8 + (size_t)((tp.top_k + 3) & ~3) * 4;
+    if (smem2 + 2048 > (size_t)smem_cap) return MAGICDEC_ERR_UNSUPPORTED;
+    auto k2 = topk_select_attn_kernel<D>;
+    if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
         return MAGICDEC_ERR_CUDA;
-    return magicdec_host::launch_pdl(k2, dim3(tp.H_q, tp.B), dim3(kTkSelThreads), sel_bytes, st, tp);
+    return magicdec_host::launch_pdl(k2, dim3(tp.H_q, tp.B), dim3(kTkNT), smem2, st, t2);
 }
 
 magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,

@@ -96,3 +96,15 @@ def test_calibrated_times_show_the_kv_bound_regime():
     assert tim.t_draft[512] / tim.t_target < 0.2
     c = cm.select(tim, {("streaming", 512): 0.8})
     assert c.speedup > 1.0
+
+
+@pytest.mark.gpu
+def test_topk_draft_search_cost_dominates_at_large_batch():
+    """Section 4.4: Top-K attention keeps a small budget but searches the whole cache at every
+    draft step, so its draft cost approaches verification; with an equal acceptance rate the
+    static StreamingLLM draft wins."""
+    tim = cm.calibrate(B=32, S=32000, budgets=[512], gammas=[3], reps=3, topk=True)
+    t_topk = tim.t_draft[512] + tim.t_select[("topk", 512)]
+    assert t_topk / tim.t_target > 0.3
+    c = cm.select(tim, {("streaming", 512): 0.8, ("topk", 512): 0.8})
+    assert c.method == "streaming"

@@ -6,6 +6,8 @@ pair or one sequence at a time from host copies of exactly the bytes the GPU rea
   * verification attention: every query row of sampled pairs;
   * StreamingLLM selection + gather + draft attention: sampled sequences;
   * SnapKV selection: sampled pairs (band rule at the k-th pooled score);
+  * Top-K attention draft: every query head of sampled sequences (band rule at the
+    top_k-th score);
   * speculative accept: every sequence of the batch (sampling mode) or a sample (greedy).
 """
 import numpy as np
@@ -15,7 +17,7 @@ import torch
 import oracle
 from long_context_self_gb300 import binding as mb
 from long_context_self_gb300 import synth
-from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, to_u16
+from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, check_topk_attn, to_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -112,6 +114,31 @@ def test_fullsize_snapkv_select_sampled(name):
                            pooled, sl_o, w.snap_window, w.snap_budget)
     assert band <= 4 * w.snap_pool + 8
     del k
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,top_k", [("llama8b_b128_l32k", 512), ("qwen32b_b16_l100k", 4096)])
+def test_fullsize_topk_draft_sampled(name, top_k):
+    w = synth.WORKLOADS[name]
+    k, v, _ = synth.kv_cache(w, DEV)
+    qd = synth.queries(w, 1, DEV, seed=w.seed * 7 + 3)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=DEV)
+    idx = torch.empty((w.B, w.H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_topk_draft_attn(qd, k, v, sl, top_k, idx=idx)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(w.seed + 11)
+    swapped = 0
+    for b in rng.choice(w.B, size=2, replace=False):
+        b = int(b)
+        L = int(sl[b])
+        sl_o = np.array([L], np.int32)
+        ref, idx_o, scores = oracle.topk_attn(to_u16(qd[b:b + 1]), to_u16(k[b:b + 1, :L]), to_u16(v[b:b + 1, :L]),
+                                              sl_o, top_k, want_scores=True)
+        sw, _ = check_topk_attn(bf16_out_to_f64(out[b:b + 1]), idx[b:b + 1].cpu().numpy(), ref, idx_o, scores, sl_o,
+                                top_k, f"{name} topk b={b}")
+        swapped += sw
+    assert swapped <= 2
+    del k, v
     torch.cuda.empty_cache()
 
 

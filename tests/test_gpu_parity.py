@@ -184,7 +184,8 @@ TOPK_CASES = [
     (4, 32, 8, 128, 3000, 512, [3000, 2999, 513, 0]),                  # Llama-3.1-8B heads, k+1, empty
     (3, 40, 8, 128, 2100, 256, [2100, 256, 100]),                      # G=5; len == k; len < k
     (2, 16, 2, 64, 1500, 1, [1500, 1]),                                # G=8, top-1
-    (2, 8, 2, 128, 70000, 2048, [70000, 41000]),                       # keys too long for shared memory
+    (2, 8, 2, 128, 70000, 2048, [70000, 41000]),                       # long rows
+    (1, 40, 8, 128, 20000, 4096, [20000]),                             # G=5, a 4096 budget
 ]
 
 
@@ -224,6 +225,23 @@ def test_topk_draft_attn_ties_go_to_smaller_positions():
     for h in range(0, H_q, H_q // H_kv):     # the query head the copies were aligned with
         assert np.array_equal(g[:, h], idx_o[:, h]), h
     check_attention(bf16_out_to_f64(out)[:, 0, :: H_q // H_kv], ref[:, 0, :: H_q // H_kv], "topk ties")
+
+
+def test_topk_draft_attn_all_scores_equal():
+    """Every key identical: all scores tie, so the first top_k positions are kept and the output is
+    the mean of their values (the candidate list overflows and the whole row is searched)."""
+    B, H_q, H_kv, d, L, top_k = 2, 8, 2, 128, 6000, 100
+    q = rand_bf16((B, 1, H_q, d), 48)
+    k = rand_bf16((B, 1, H_kv, d), 49).expand(B, L, H_kv, d).contiguous()
+    v = rand_bf16((B, L, H_kv, d), 50)
+    sl = np.array([L, 4500], np.int32)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_topk_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, _ = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, top_k)
+    assert np.array_equal(idx_o, np.broadcast_to(np.arange(top_k, dtype=np.int32), idx_o.shape))
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    check_attention(bf16_out_to_f64(out), ref, "topk all-equal")
 
 
 # ------------------------------------------------------------------ acceptance
