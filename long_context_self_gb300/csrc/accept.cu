@@ -145,7 +145,11 @@ __device__ __forceinline__ void top_merge(float &t1, float &t2, int &arg, float 
 // One record per warp and 1024-logit slice: lane l holds logits
 // t0 + k*128 + 4l .. +3 (float4 path) or t0 + k*32 + l (scalar path), so each
 // load instruction of the warp is coalesced and no block-level reduction is
-// needed.
+// needed.  Sampling mode records the slice's max m and S = sum exp(x - m):
+// each lane sums its 32 exponentials pairwise in fp32 (error ~1e-7 relative,
+// the order of the exponential's own), lanes merge in fp64.  Greedy mode
+// records only the top two logits and the argmax (smallest index on ties).
+template <bool GREEDY>
 __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptParams p) {
     pdl_trigger();
     pdl_wait();
@@ -160,8 +164,9 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
     const int t0 = rec * kStatChunk, t1 = min(t0 + kStatChunk, p.V);
 
     float v[kAccPer];
-    int idx0[kAccPer];
     const bool vec = ((p.V & 3) == 0);
+    // index of v[k2]: t0 + (k2 >> 2) * 128 + 4 * lane + (k2 & 3) (float4 path),
+    //                 t0 + k2 * 32 + lane (scalar path); increasing in k2
     if (vec) {
 #pragma unroll
         for (int k2 = 0; k2 < kAccPer / 4; ++k2) {
@@ -172,53 +177,65 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
                              : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
                              : "l"(x + t));
             v[4 * k2] = q.x; v[4 * k2 + 1] = q.y; v[4 * k2 + 2] = q.z; v[4 * k2 + 3] = q.w;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) idx0[4 * k2 + e] = t + e;
         }
     } else {
 #pragma unroll
         for (int k2 = 0; k2 < kAccPer; ++k2) {
             const int t = t0 + k2 * 32 + lane;
             v[k2] = t < t1 ? __ldg(x + t) : -INFINITY;
-            idx0[k2] = t;
         }
     }
-    // each lane sees its logits in increasing index order: strict ">" keeps the smallest index
-    float mx = -INFINITY, top1 = -INFINITY, top2 = -INFINITY;
-    int arg = 0x7fffffff;
+    RowStat st;
+    if (GREEDY) {
+        float top1 = -INFINITY, top2 = -INFINITY;
+        int arg = 0x7fffffff;
 #pragma unroll
-    for (int k2 = 0; k2 < kAccPer; ++k2) {
-        const float e = v[k2];
-        mx = fmaxf(mx, e);
-        if (e > top1) {
-            top2 = top1;
-            top1 = e;
-            arg = idx0[k2];
-        } else if (e > top2) {
-            top2 = e;
+        for (int k2 = 0; k2 < kAccPer; ++k2) {
+            const float e = v[k2];
+            const int idx = vec ? t0 + (k2 >> 2) * 128 + 4 * lane + (k2 & 3) : t0 + k2 * 32 + lane;
+            if (e > top1) {     // strict: the smallest index keeps a tie
+                top2 = top1;
+                top1 = e;
+                arg = idx;
+            } else if (e > top2) {
+                top2 = e;
+            }
         }
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float u1 = __shfl_xor_sync(0xffffffffu, top1, o);
-        const float u2 = __shfl_xor_sync(0xffffffffu, top2, o);
-        const int ua = __shfl_xor_sync(0xffffffffu, arg, o);
-        top_merge(top1, top2, arg, u1, u2, ua);
-    }
-    const float m = warp_max(mx);
-    dflt acc = {0.f, 0.f};
-#pragma unroll
-    for (int k2 = 0; k2 < kAccPer; ++k2) acc = df_add_f(acc, fast_exp2((v[k2] - m) * kLog2e));
-    acc = warp_sum_df(acc);
-    if (lane == 0) {
-        RowStat st;
-        st.s = df_to_double(acc);
-        st.m = m;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float u1 = __shfl_xor_sync(0xffffffffu, top1, o);
+            const float u2 = __shfl_xor_sync(0xffffffffu, top2, o);
+            const int ua = __shfl_xor_sync(0xffffffffu, arg, o);
+            top_merge(top1, top2, arg, u1, u2, ua);
+        }
+        st.s = 0.0;
+        st.m = top1;
         st.top1 = top1;
         st.top2 = top2;
         st.arg = arg;
-        p.stats[row * p.n_stat_chunks + rec] = st;
+    } else {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k2 = 0; k2 < kAccPer; ++k2) mx = fmaxf(mx, v[k2]);
+        const float m = warp_max(mx);
+        const float mb = m * kLog2e;
+        float e[kAccPer];
+#pragma unroll
+        for (int k2 = 0; k2 < kAccPer; ++k2) e[k2] = fast_exp2(fmaf(v[k2], kLog2e, -mb));
+#pragma unroll
+        for (int w = kAccPer / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) e[i] += e[i + w];
+        double sum = (double)e[0];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        st.s = sum;
+        st.m = m;
+        st.top1 = m;
+        st.top2 = m;
+        st.arg = 0;
     }
+    if (lane == 0) p.stats[row * p.n_stat_chunks + rec] = st;
 }
 
 // Whole-row statistics, merged in fp64: max m and S = sum exp(x - m).
@@ -374,16 +391,10 @@ __device__ double block_sum_df(dflt v, dflt *scratch) {
     return df_to_double(t);
 }
 
-// Resample weights of the four logits t..t+3 from float4 loads (t % 4 == 0).
-__device__ __forceinline__ dflt weight4_sum(const WeightCtx &w, int t) {
-    const float4 xt = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
+// Resample weights of four logits (target xt, draft xd) summed in double-float.
+__device__ __forceinline__ dflt weight4_vals(const WeightCtx &w, const float4 xt, const float4 xd, bool resid) {
     const float tv[4] = {xt.x, xt.y, xt.z, xt.w};
-    float dv[4] = {0.f, 0.f, 0.f, 0.f};
-    const bool resid = !(w.kind == 2 || w.use_p);
-    if (resid) {
-        const float4 xd = __ldg(reinterpret_cast<const float4 *>(w.dr + t));
-        dv[0] = xd.x; dv[1] = xd.y; dv[2] = xd.z; dv[3] = xd.w;
-    }
+    const float dv[4] = {xd.x, xd.y, xd.z, xd.w};
     dflt acc = {0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -400,10 +411,27 @@ __device__ __forceinline__ dflt weight4_sum(const WeightCtx &w, int t) {
 }
 
 // Sum of weights over [t0, t1) (thread-strided double-float, then a fixed tree).
+// A full, aligned chunk issues all its loads before any arithmetic.
 __device__ double chunk_weight_sum(const WeightCtx &w, int t0, int t1, bool vec4, dflt *scratch) {
+    constexpr int NV = kAccChunk / (4 * kAccThreads);     // float4 per thread in a full chunk
     dflt acc = {0.f, 0.f};
-    if (vec4 && ((t1 - t0) & 3) == 0 && (t0 & 3) == 0) {
-        for (int t = t0 + 4 * threadIdx.x; t < t1; t += 4 * blockDim.x) acc = df_add(acc, weight4_sum(w, t));
+    const bool resid = !(w.kind == 2 || w.use_p);
+    if (vec4 && t1 - t0 == kAccChunk && (t0 & 3) == 0 && blockDim.x == kAccThreads) {
+        float4 xt[NV], xd[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int t = t0 + 4 * (int)threadIdx.x + i * 4 * kAccThreads;
+            xt[i] = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
+            xd[i] = resid ? __ldg(reinterpret_cast<const float4 *>(w.dr + t)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc = df_add(acc, weight4_vals(w, xt[i], xd[i], resid));
+    } else if (vec4 && ((t1 - t0) & 3) == 0 && (t0 & 3) == 0) {
+        for (int t = t0 + 4 * threadIdx.x; t < t1; t += 4 * blockDim.x) {
+            const float4 xt = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
+            const float4 xd = resid ? __ldg(reinterpret_cast<const float4 *>(w.dr + t)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            acc = df_add(acc, weight4_vals(w, xt, xd, resid));
+        }
     } else {
         for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) acc = df_add(acc, weight_at(w, t));
     }
@@ -591,7 +619,7 @@ magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target,
     prm.chunk_sum = reinterpret_cast<double *>(w);
 
     const long long n_work = (long long)B * prm.rows_per_b * prm.n_stat_chunks;
-    magicdec_status s = magicdec_host::launch_pdl(accept_stats_kernel,
+    magicdec_status s = magicdec_host::launch_pdl(greedy ? accept_stats_kernel<true> : accept_stats_kernel<false>,
                                                   dim3((unsigned)((n_work + kAccThreads / 32 - 1) / (kAccThreads / 32))),
                                                   dim3(kAccThreads), 0, st, prm);
     if (s != MAGICDEC_OK) return s;
