@@ -26,8 +26,7 @@
 namespace magicdec {
 
 constexpr int kStatChunk = 1024;      // logits per statistics record (one warp)
-constexpr int kAccChunk = 4096;       // logits per sample CTA
-constexpr int kAccThreads = 256;
+constexpr int kAccThreads = 128;     // statistics CTA: 4 warps, one record per 4 slices
 constexpr int kAccPer = kStatChunk / 32;  // 32 logits per lane of a statistics warp, held in registers
 
 // ------------------------------------------------------------ double-float
@@ -49,12 +48,6 @@ __device__ __forceinline__ dflt two_sum(float a, float b) {
 __device__ __forceinline__ dflt df_add_f(dflt a, float b) {
     dflt s = two_sum(a.hi, b);
     s.lo += a.lo;
-    return quick_two_sum(s.hi, s.lo);
-}
-
-__device__ __forceinline__ dflt df_sub(dflt a, dflt b) {
-    dflt s = two_sum(a.hi, -b.hi);
-    s.lo += a.lo - b.lo;
     return quick_two_sum(s.hi, s.lo);
 }
 
@@ -100,6 +93,7 @@ struct RowStat {
 
 struct JobInfo {
     double st, sd;     // target / draft normalisers relative to mt / md
+    float inv_st_hi, inv_st_lo, inv_sd_hi, inv_sd_lo;   // 1/st, 1/sd as double-float (one division per sequence)
     float mt, md;
     int kind;          // 0 = nothing to sample, 1 = residual at row acc, 2 = bonus from target row gamma
     int acc;
@@ -116,11 +110,10 @@ struct AcceptParams {
     int32_t *n_acc;
     int32_t *out_tok;
     int32_t *n_amb;
-    RowStat *stats;           // [B, rows_per_b, n_stat_chunks]
+    RowStat *stats;           // [B, rows_per_b, n_stat_chunks]: one record per 4 slices of 1024 logits
     JobInfo *job;             // [B]
-    double *chunk_sum;        // [B, n_chunks]
-    int *counters;            // [B], zero between calls
     int *err;
+    double *chunk_sum;        // [B, n_chunks] weight sums of the sampled row(s)
     int B, gamma, V, n_chunks, n_stat_chunks, rows_per_b, greedy;
 };
 
@@ -142,26 +135,30 @@ __device__ __forceinline__ void top_merge(float &t1, float &t2, int &arg, float 
     t2 = fmaxf(fmaxf(t2, u2), lose);
 }
 
-// One record per warp and 1024-logit slice: lane l holds logits
+// One record per CTA: the CTA of (row, blockIdx.y) covers the row's 1024-logit
+// slices 4*blockIdx.y .. +3, one per warp.  Lane l of a warp holds logits
 // t0 + k*128 + 4l .. +3 (float4 path) or t0 + k*32 + l (scalar path), so each
-// load instruction of the warp is coalesced and no block-level reduction is
-// needed.  Sampling mode records the slice's max m and S = sum exp(x - m):
-// each lane sums its 32 exponentials pairwise in fp32 (error ~1e-7 relative,
-// the order of the exponential's own), lanes merge in fp64.  Greedy mode
-// records only the top two logits and the argmax (smallest index on ties).
+// load instruction is coalesced.  Sampling mode records the CTA's max m and
+// S = sum exp(x - m): the warps agree on m through shared memory, each lane
+// sums its 32 exponentials pairwise in fp32 (error ~1e-7 relative, the order
+// of the exponential's own), lanes and warps merge in fp64 in a fixed order.
+// Greedy mode records only the top two logits and the argmax (smallest index
+// on ties).
 template <bool GREEDY>
 __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptParams p) {
+    constexpr int NW = kAccThreads / 32;
+    __shared__ float s_max[NW], s_t1[NW], s_t2[NW];
+    __shared__ int s_arg[NW];
+    __shared__ double s_sum[NW];
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * (kAccThreads / 32) + warp;     // (row, record)
-    const long long n_work = (long long)p.B * p.rows_per_b * p.n_stat_chunks;
-    if (gw >= n_work) return;
-    const long long row = gw / p.n_stat_chunks;
-    const int rec = (int)(gw - row * p.n_stat_chunks);
+    const long long row = blockIdx.x;
+    const int rec = blockIdx.y;
+    const int slice = rec * NW + warp;
     const int b = (int)(row / p.rows_per_b), r = (int)(row % p.rows_per_b);
     const float *x = row_ptr(p, b, r);
-    const int t0 = rec * kStatChunk, t1 = min(t0 + kStatChunk, p.V);
+    const int t0 = slice * kStatChunk, t1 = min(t0 + kStatChunk, p.V);   // empty past the row's end
 
     float v[kAccPer];
     const bool vec = ((p.V & 3) == 0);
@@ -208,6 +205,14 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
             const int ua = __shfl_xor_sync(0xffffffffu, arg, o);
             top_merge(top1, top2, arg, u1, u2, ua);
         }
+        if (lane == 0) {
+            s_t1[warp] = top1;
+            s_t2[warp] = top2;
+            s_arg[warp] = arg;
+        }
+        __syncthreads();
+        if (threadIdx.x != 0) return;
+        for (int w2 = 1; w2 < NW; ++w2) top_merge(top1, top2, arg, s_t1[w2], s_t2[w2], s_arg[w2]);
         st.s = 0.0;
         st.m = top1;
         st.top1 = top1;
@@ -217,25 +222,38 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
         float mx = -INFINITY;
 #pragma unroll
         for (int k2 = 0; k2 < kAccPer; ++k2) mx = fmaxf(mx, v[k2]);
-        const float m = warp_max(mx);
-        const float mb = m * kLog2e;
-        float e[kAccPer];
+        mx = warp_max(mx);
+        if (lane == 0) s_max[warp] = mx;
+        __syncthreads();
+        float m = s_max[0];
 #pragma unroll
-        for (int k2 = 0; k2 < kAccPer; ++k2) e[k2] = fast_exp2(fmaf(v[k2], kLog2e, -mb));
+        for (int w2 = 1; w2 < NW; ++w2) m = fmaxf(m, s_max[w2]);
+        double sum = 0.0;
+        if (m != -INFINITY) {
+            const float mb = m * kLog2e;
+            float e[kAccPer];
 #pragma unroll
-        for (int w = kAccPer / 2; w > 0; w >>= 1)
+            for (int k2 = 0; k2 < kAccPer; ++k2) e[k2] = fast_exp2(fmaf(v[k2], kLog2e, -mb));
 #pragma unroll
-            for (int i = 0; i < w; ++i) e[i] += e[i + w];
-        double sum = (double)e[0];
+            for (int w = kAccPer / 2; w > 0; w >>= 1)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        st.s = sum;
+                for (int i = 0; i < w; ++i) e[i] += e[i + w];
+            sum = (double)e[0];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        }
+        if (lane == 0) s_sum[warp] = sum;
+        __syncthreads();
+        if (threadIdx.x != 0) return;
+        double S = s_sum[0];
+        for (int w2 = 1; w2 < NW; ++w2) S += s_sum[w2];
+        st.s = S;
         st.m = m;
         st.top1 = m;
         st.top2 = m;
         st.arg = 0;
     }
-    if (lane == 0) p.stats[row * p.n_stat_chunks + rec] = st;
+    p.stats[row * p.n_stat_chunks + rec] = st;
 }
 
 // Whole-row statistics, merged in fp64: max m and S = sum exp(x - m).
@@ -359,6 +377,14 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
     }
     job.acc = acc;
     job.amb = amb;
+    if (job.kind != 0) {
+        const dflt it = df_from_double(1.0 / job.st);
+        job.inv_st_hi = it.hi;
+        job.inv_st_lo = it.lo;
+        const dflt id = df_from_double(job.kind == 1 ? 1.0 / job.sd : 0.0);
+        job.inv_sd_hi = id.hi;
+        job.inv_sd_lo = id.lo;
+    }
     p.job[b] = job;
 }
 
@@ -371,13 +397,43 @@ struct WeightCtx {
     bool use_p;
 };
 
-__device__ __forceinline__ dflt weight_at(const WeightCtx &w, int t) {
-    const dflt pt = df_mul_f(fast_exp2((__ldg(w.tr + t) - w.mt) * kLog2e), w.inv_st);
-    if (w.kind == 2 || w.use_p) return pt;
-    const dflt qt = df_mul_f(fast_exp2((__ldg(w.dr + t) - w.md) * kLog2e), w.inv_sd);
-    const dflt d = df_sub(pt, qt);
-    return d.hi > 0.f ? d : dflt{0.f, 0.f};
+// Weight of one logit pair as an unnormalised double-float pair hi + lo.
+// p = e_t * (1/S_t) and q = e_d * (1/S_d) are split exactly into hi + lo (one
+// FMA each), p - q is one two-sum of the high parts plus the low parts, and a
+// pair whose value is not positive weighs 0.  Every term is within ~1e-14 of
+// the exact product difference of the fp32 exponentials.
+__device__ __forceinline__ dflt weight_of(const WeightCtx &w, float xt, float xd, bool resid) {
+    const float et = fast_exp2((xt - w.mt) * kLog2e);
+    const float ph = et * w.inv_st.hi;
+    const float pl = fmaf(et, w.inv_st.hi, -ph) + et * w.inv_st.lo;
+    if (!resid) return dflt{ph, pl};
+    const float ed = fast_exp2((xd - w.md) * kLog2e);
+    const float qh = ed * w.inv_sd.hi;
+    const float ql = fmaf(ed, w.inv_sd.hi, -qh) + ed * w.inv_sd.lo;
+    const float sh = ph - qh;
+    const float bb = sh - ph;
+    const float lo = ((ph - (sh - bb)) + (-qh - bb)) + (pl - ql);
+    return sh + lo > 0.f ? dflt{sh, lo} : dflt{0.f, 0.f};
 }
+
+// A weight that is not positive is returned as exactly {0, 0}.
+__device__ __forceinline__ bool weight_positive(dflt d) { return d.hi != 0.f || d.lo != 0.f; }
+
+__device__ __forceinline__ dflt weight_at(const WeightCtx &w, int t) {
+    const bool resid = !(w.kind == 2 || w.use_p);
+    return weight_of(w, __ldg(w.tr + t), resid ? __ldg(w.dr + t) : 0.f, resid);
+}
+
+// Running sum of non-negative unnormalised pairs: a two-sum of the high parts,
+// the low parts and rounding errors gathered in lo (renormalised by the caller).
+__device__ __forceinline__ void acc_add(dflt &acc, dflt d) {
+    const float sh = acc.hi + d.hi;
+    const float bb = sh - acc.hi;
+    acc.lo += ((acc.hi - (sh - bb)) + (d.hi - bb)) + d.lo;
+    acc.hi = sh;
+}
+
+__device__ __forceinline__ dflt acc_done(dflt acc) { return quick_two_sum(acc.hi, acc.lo); }
 
 // Block sum of double-float values in a fixed order; returned (as a double) to every thread.
 __device__ double block_sum_df(dflt v, dflt *scratch) {
@@ -391,72 +447,115 @@ __device__ double block_sum_df(dflt v, dflt *scratch) {
     return df_to_double(t);
 }
 
-// Resample weights of four logits (target xt, draft xd) summed in double-float.
-__device__ __forceinline__ dflt weight4_vals(const WeightCtx &w, const float4 xt, const float4 xd, bool resid) {
-    const float tv[4] = {xt.x, xt.y, xt.z, xt.w};
-    const float dv[4] = {xd.x, xd.y, xd.z, xd.w};
-    dflt acc = {0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const dflt pt = df_mul_f(fast_exp2((tv[j] - w.mt) * kLog2e), w.inv_st);
-        if (!resid) {
-            acc = df_add(acc, pt);
-        } else {
-            const dflt qt = df_mul_f(fast_exp2((dv[j] - w.md) * kLog2e), w.inv_sd);
-            const dflt d = df_sub(pt, qt);
-            if (d.hi > 0.f) acc = df_add(acc, d);
-        }
-    }
-    return acc;
+// Resample weights of four logits (target xt, draft xd) added to acc.
+__device__ __forceinline__ void weight4_acc(dflt &acc, const WeightCtx &w, const float4 xt, const float4 xd,
+                                            bool resid) {
+    acc_add(acc, weight_of(w, xt.x, xd.x, resid));
+    acc_add(acc, weight_of(w, xt.y, xd.y, resid));
+    acc_add(acc, weight_of(w, xt.z, xd.z, resid));
+    acc_add(acc, weight_of(w, xt.w, xd.w, resid));
 }
 
-// Sum of weights over [t0, t1) (thread-strided double-float, then a fixed tree).
-// A full, aligned chunk issues all its loads before any arithmetic.
-__device__ double chunk_weight_sum(const WeightCtx &w, int t0, int t1, bool vec4, dflt *scratch) {
-    constexpr int NV = kAccChunk / (4 * kAccThreads);     // float4 per thread in a full chunk
-    dflt acc = {0.f, 0.f};
-    const bool resid = !(w.kind == 2 || w.use_p);
-    if (vec4 && t1 - t0 == kAccChunk && (t0 & 3) == 0 && blockDim.x == kAccThreads) {
-        float4 xt[NV], xd[NV];
+// Inclusive scan of one double per thread in thread order: shuffle scans in
+// each warp, a scan of the warp totals by warp 0, two barriers.
+__device__ double block_scan_warps(double v, double *wtot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    double x = v;
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int t = t0 + 4 * (int)threadIdx.x + i * 4 * kAccThreads;
-            xt[i] = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
-            xd[i] = resid ? __ldg(reinterpret_cast<const float4 *>(w.dr + t)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int i = 0; i < NV; ++i) acc = df_add(acc, weight4_vals(w, xt[i], xd[i], resid));
-    } else if (vec4 && ((t1 - t0) & 3) == 0 && (t0 & 3) == 0) {
-        for (int t = t0 + 4 * threadIdx.x; t < t1; t += 4 * blockDim.x) {
-            const float4 xt = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
-            const float4 xd = resid ? __ldg(reinterpret_cast<const float4 *>(w.dr + t)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            acc = df_add(acc, weight4_vals(w, xt, xd, resid));
-        }
-    } else {
-        for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) acc = df_add(acc, weight_at(w, t));
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    return block_sum_df(acc, scratch);
-}
-
-// Inclusive block scan of one double per thread (fixed order).
-__device__ double block_scan_d(double v, double *buf) {
-    const int tid = threadIdx.x;
-    buf[tid] = v;
+    if (lane == 31) wtot[warp] = x;
     __syncthreads();
-    for (int off = 1; off < (int)blockDim.x; off <<= 1) {
-        const double add = tid >= off ? buf[tid - off] : 0.0;
-        __syncthreads();
-        buf[tid] += add;
-        __syncthreads();
+    if (warp == 0) {
+        double t = lane < nw ? wtot[lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) wtot[lane] = t;
     }
-    return buf[tid];
+    __syncthreads();
+    return x + (warp ? wtot[warp - 1] : 0.0);
 }
 
-__global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const AcceptParams p) {
-    __shared__ dflt scratch[kAccThreads / 32];
-    __shared__ double seg[kAccThreads];
-    __shared__ int is_last;
-    const int chunk = blockIdx.x, b = blockIdx.y;
+// Sum of the chunk sums in a fixed order, computed by one warp (every lane
+// returns it): lane l adds its contiguous block, then a shuffle scan.
+__device__ double warp_chunk_total(const double *csum, int n, int lane) {
+    const int per = (n + 31) / 32;
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    double part = 0.0;
+    for (int c = lo; c < hi; ++c) part += csum[c];
+    double incl = part;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+constexpr int kSmpThreads = 1024;
+constexpr int kSmpChunk = 4 * kSmpThreads;   // logits per chunk: one float4 of each row per thread
+constexpr int kSmpBatch = 4;                 // chunks whose loads are in flight together
+constexpr int kSmpMaxChunks = 256;
+
+// Chunk sums of the weights of chunks c0 .. c0+kSmpBatch-1 into csum[].
+// Thread t holds logits 4t .. 4t+3 of each chunk; a chunk's per-thread sums
+// are reduced in a fixed order (warps by shuffles, then warp 0's lanes).
+__device__ __forceinline__ void batch_chunk_sums(const WeightCtx &w, bool resid, int V, bool vec4, int c0,
+                                                 int n_chunks, dflt (*wred)[32], double *csum) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float4 xt[kSmpBatch], xd[kSmpBatch];
+    const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+    for (int u = 0; u < kSmpBatch; ++u) {
+        const int t = (c0 + u) * kSmpChunk + 4 * tid;
+        xt[u] = none;
+        xd[u] = none;
+        if (c0 + u < n_chunks && t < V) {
+            if (vec4) {
+                xt[u] = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
+                if (resid) xd[u] = __ldg(reinterpret_cast<const float4 *>(w.dr + t));
+            } else {
+                float a[4], d[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a[e] = t + e < V ? __ldg(w.tr + t + e) : -INFINITY;
+                    d[e] = (resid && t + e < V) ? __ldg(w.dr + t + e) : -INFINITY;
+                }
+                xt[u] = make_float4(a[0], a[1], a[2], a[3]);
+                xd[u] = make_float4(d[0], d[1], d[2], d[3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kSmpBatch; ++u) {
+        dflt acc = {0.f, 0.f};
+        weight4_acc(acc, w, xt[u], xd[u], resid);
+        acc = warp_sum_df(acc_done(acc));
+        if (lane == 0) wred[u][warp] = acc;
+    }
+    __syncthreads();
+    if (warp < kSmpBatch) {
+        dflt v = wred[warp][lane];
+        v = warp_sum_df(v);
+        if (lane == 0 && c0 + warp < n_chunks) csum[c0 + warp] = df_to_double(v);
+    }
+    __syncthreads();
+}
+
+constexpr int kChkThreads = 256;
+constexpr int kChkPer = kSmpChunk / (4 * kChkThreads);   // float4 of each row per thread (4)
+
+// Weight sum of chunk blockIdx.x of sequence blockIdx.y into chunk_sum[b][c]
+// (kind 1: residual max(0, p - q); kind 2: p).  All loads of a thread are
+// issued before any arithmetic; the block sum is reduced in a fixed order.
+__global__ void __launch_bounds__(kChkThreads) accept_chunk_kernel(const AcceptParams p) {
+    __shared__ dflt wred[kChkThreads / 32];
+    const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
     pdl_wait();
     const JobInfo job = p.job[b];
@@ -468,105 +567,187 @@ __global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const Accept
     w.dr = job.kind == 1 ? row_ptr(p, b, p.gamma + 1 + job.acc) : nullptr;
     w.mt = job.mt;
     w.md = job.md;
-    w.inv_st = df_from_double(1.0 / job.st);
-    w.inv_sd = df_from_double(job.kind == 1 ? 1.0 / job.sd : 0.0);
-    const int t0 = chunk * kAccChunk, t1 = min(t0 + kAccChunk, p.V);
-    const bool vec4 = (p.V & 3) == 0;
-    const double csum = chunk_weight_sum(w, t0, t1, vec4, scratch);
-    if (threadIdx.x == 0) {
-        p.chunk_sum[(long long)b * p.n_chunks + chunk] = csum;
-        __threadfence();
-        const int old = atomicAdd(p.counters + b, 1);
-        is_last = (old == p.n_chunks - 1);
-        if (is_last) {
-            __threadfence();
-            p.counters[b] = 0;
-        }
-    }
-    __syncthreads();
-    if (!is_last) return;
-
-    // Last CTA of this sequence: find the token.
-    __threadfence();
-    const double u = __ldg(p.u_res + b);
-    const double *cs = p.chunk_sum + (long long)b * p.n_chunks;
-    double W = 0.0;
-    for (int c = 0; c < p.n_chunks; ++c) W += __ldcg(cs + c);
-    bool use_p = false;
-    if (!(W > 0.0)) {
-        // Residual empty (p == q up to rounding): draw from p instead; the
-        // chunk sums of p are recomputed here into seg[] (n_chunks <= 256 is
-        // checked at the entry point).
-        use_p = true;
-        w.use_p = true;
-        W = 0.0;
-        for (int c = 0; c < p.n_chunks; ++c) {
-            const double v = chunk_weight_sum(w, c * kAccChunk, min((c + 1) * kAccChunk, p.V), vec4, scratch);
-            if (threadIdx.x == 0) seg[c] = v;
-            W += v;
-        }
-        __syncthreads();
-    }
-    const double target = u * W, tol = 1e-7 * W;
-    double before = 0.0;
-    int cstar = -1;
-    for (int c = 0; c < p.n_chunks; ++c) {
-        const double v = use_p ? seg[c] : __ldcg(cs + c);
-        if (before + v > target) { cstar = c; break; }
-        before += v;
-    }
-    int amb = job.amb;
-    if (cstar < 0) {
-        // rounding pushed target past the total: the last chunk with weight
-        before = 0.0;
-        for (int c = 0; c < p.n_chunks; ++c) {
-            const double v = use_p ? seg[c] : __ldcg(cs + c);
-            if (v > 0.0) cstar = c;
-        }
-        if (cstar < 0) cstar = p.n_chunks - 1;
-        for (int c = 0; c < cstar; ++c) before += use_p ? seg[c] : __ldcg(cs + c);
-        ++amb;
-    }
-    __syncthreads();   // every thread has read seg[] for the chunk search
-    // Scan inside chunk cstar: each thread owns a contiguous run of logits; an
-    // fp64 block scan of the run sums tells every thread where its run starts,
-    // and the one run containing the crossing walks its logits.
-    __shared__ int found_token, found_amb;
-    if (threadIdx.x == 0) { found_token = -1; found_amb = 0; }
-    const int c0 = cstar * kAccChunk, c1 = min(c0 + kAccChunk, p.V);
-    const int per = (c1 - c0 + kAccThreads - 1) / kAccThreads;
-    const int my0 = c0 + threadIdx.x * per, my1 = min(my0 + per, c1);
-    dflt mine = {0.f, 0.f};
-    for (int t = my0; t < my1; ++t) mine = df_add(mine, weight_at(w, t));
-    const double my_sum = df_to_double(mine);
-    const double incl = block_scan_d(my_sum, seg);
-    const double start = before + (incl - my_sum);
-    if (my0 < my1 && start <= target && target < before + incl) {
-        double prev = start;
-        for (int t = my0; t < my1; ++t) {
-            const double nxt = prev + df_to_double(weight_at(w, t));
-            if (nxt > target) {
-                found_token = t;
-                found_amb = ((t > 0 && target - prev < tol) || (t < p.V - 1 && nxt - target < tol)) ? 1 : 0;
-                break;
+    w.inv_st = dflt{job.inv_st_hi, job.inv_st_lo};
+    w.inv_sd = dflt{job.inv_sd_hi, job.inv_sd_lo};
+    const bool resid = job.kind == 1;
+    const int V = p.V, t0 = c * kSmpChunk;
+    const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 xt[kChkPer], xd[kChkPer];
+#pragma unroll
+    for (int i = 0; i < kChkPer; ++i) {
+        const int t = t0 + 4 * tid + i * 4 * kChkThreads;
+        xt[i] = none;
+        xd[i] = none;
+        if (t < V) {
+            if ((V & 3) == 0) {
+                xt[i] = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
+                if (resid) xd[i] = __ldg(reinterpret_cast<const float4 *>(w.dr + t));
+            } else {
+                float a[4], d[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a[e] = t + e < V ? __ldg(w.tr + t + e) : -INFINITY;
+                    d[e] = (resid && t + e < V) ? __ldg(w.dr + t + e) : -INFINITY;
+                }
+                xt[i] = make_float4(a[0], a[1], a[2], a[3]);
+                xd[i] = make_float4(d[0], d[1], d[2], d[3]);
             }
-            prev = nxt;
         }
-        if (found_token < 0) {   // rounding inside the run: its last positive weight
-            for (int t = my1 - 1; t >= my0; --t)
-                if (weight_at(w, t).hi > 0.f) { found_token = t; break; }
+    }
+    dflt acc = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kChkPer; ++i) weight4_acc(acc, w, xt[i], xd[i], resid);
+    acc = warp_sum_df(acc_done(acc));
+    if (lane == 0) wred[warp] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        dflt t = wred[0];
+        for (int i = 1; i < kChkThreads / 32; ++i) t = df_add(t, wred[i]);
+        p.chunk_sum[(long long)b * p.n_chunks + c] = df_to_double(t);
+    }
+}
+
+// One CTA per sequence with something to draw (job kind 1: the residual
+// norm(max(0, p - q)) at the rejected position; kind 2: the bonus token from
+// the last target row).  From the chunk sums it finds the chunk where the
+// cumulative weight passes u * total and walks it.  An empty residual (p == q
+// up to rounding) is redrawn from p, whose chunk sums this CTA recomputes.
+__global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const AcceptParams p) {
+    __shared__ double csum[kSmpMaxChunks];
+    __shared__ dflt wred[kSmpBatch][32];
+    __shared__ double wtot[32];
+    __shared__ double s_W, s_before;
+    __shared__ int s_cstar, s_amb;
+    __shared__ int found_token, found_amb;
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    pdl_wait();
+    const JobInfo job = p.job[b];
+    if (job.kind == 0) return;
+    WeightCtx w;
+    w.kind = job.kind;
+    w.use_p = false;
+    w.tr = row_ptr(p, b, job.kind == 2 ? p.gamma : job.acc);
+    w.dr = job.kind == 1 ? row_ptr(p, b, p.gamma + 1 + job.acc) : nullptr;
+    w.mt = job.mt;
+    w.md = job.md;
+    w.inv_st = dflt{job.inv_st_hi, job.inv_st_lo};
+    w.inv_sd = dflt{job.inv_sd_hi, job.inv_sd_lo};
+    const int V = p.V, n_chunks = p.n_chunks;
+    const bool vec4 = (V & 3) == 0;
+    bool resid = job.kind == 1;
+    for (int c = tid; c < n_chunks; c += kSmpThreads) csum[c] = p.chunk_sum[(long long)b * n_chunks + c];
+    __syncthreads();
+    if (warp == 0) s_W = warp_chunk_total(csum, n_chunks, lane);
+    __syncthreads();
+    double W = s_W;
+    if (!(W > 0.0)) {
+        // Residual empty (p == q up to rounding): draw from p instead.
+        w.use_p = true;
+        resid = false;
+        for (int c = 0; c < n_chunks; c += kSmpBatch) batch_chunk_sums(w, resid, V, vec4, c, n_chunks, wred, csum);
+        if (warp == 0) s_W = warp_chunk_total(csum, n_chunks, lane);
+        __syncthreads();
+        W = s_W;
+    }
+    const double u = __ldg(p.u_res + b);
+    const double target = u * W, tol = 1e-7 * W;
+    int amb = job.amb;
+    if (warp == 0) {
+        // lane l sums its contiguous block of chunks; a shuffle scan over the
+        // lanes and a ballot find the lane whose block holds the crossing
+        const int per = (n_chunks + 31) / 32;
+        const int lo = min(n_chunks, lane * per), hi = min(n_chunks, lo + per);
+        double part = 0.0;
+        for (int c = lo; c < hi; ++c) part += csum[c];
+        double incl = part;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const double excl = incl - part;
+        const unsigned own = __ballot_sync(0xffffffffu, hi > lo && excl <= target && target < incl);
+        int cs = -1;
+        double before = 0.0;
+        if (own && lane == __ffs(own) - 1) {
+            before = excl;
+            for (int c = lo; c < hi; ++c) {
+                if (before + csum[c] > target) { cs = c; break; }
+                before += csum[c];
+            }
+            if (cs >= 0) {
+                s_cstar = cs;
+                s_before = before;
+                s_amb = 0;
+            }
+        }
+        cs = __shfl_sync(0xffffffffu, cs, own ? __ffs(own) - 1 : 0);
+        if (cs < 0 && lane == 0) {
+            // rounding pushed the target past the total: the last chunk with weight
+            int last = -1;
+            for (int c = 0; c < n_chunks; ++c)
+                if (csum[c] > 0.0) last = c;
+            if (last < 0) last = n_chunks - 1;
+            double bf = 0.0;
+            for (int c = 0; c < last; ++c) bf += csum[c];
+            s_cstar = last;
+            s_before = bf;
+            s_amb = 1;
+        }
+    }
+    if (tid == 0) { found_token = -1; found_amb = 0; }
+    __syncthreads();
+    const int cstar = s_cstar;
+    const double before = s_before;
+    amb += s_amb;
+    if (tid == 0) { found_token = -1; found_amb = 0; }
+    // Walk chunk cstar: thread t owns its logits 4t .. 4t+3; an fp64 block scan
+    // of the per-thread sums tells every thread where its run starts, and the
+    // one run containing the crossing walks its four weights.
+    const int cb = cstar * kSmpChunk, ce = min(cb + kSmpChunk, V);
+    const int my0 = cb + 4 * tid;
+    dflt wt[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        wt[e] = my0 + e < ce ? weight_of(w, __ldg(w.tr + my0 + e), resid ? __ldg(w.dr + my0 + e) : 0.f, resid)
+                             : dflt{0.f, 0.f};
+    dflt mine = {0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc_add(mine, wt[e]);
+    const double my_sum = df_to_double(acc_done(mine));
+    const double incl = block_scan_warps(my_sum, wtot);
+    const double start = before + (incl - my_sum);
+    if (my0 < ce && start <= target && target < before + incl) {
+        double prev = start;
+        int tok = -1, last_pos = -1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (weight_positive(wt[e])) last_pos = e;
+            const double nxt = prev + df_to_double(wt[e]);
+            if (tok < 0 && nxt > target) {
+                tok = e;
+                const int t = my0 + e;
+                found_amb = ((t > 0 && target - prev < tol) || (t < V - 1 && nxt - target < tol)) ? 1 : 0;
+            }
+            if (tok < 0) prev = nxt;
+        }
+        if (tok >= 0) {
+            found_token = my0 + tok;
+        } else if (last_pos >= 0) {   // rounding inside the run: its last positive weight
+            found_token = my0 + last_pos;
             found_amb = 1;
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         int token = found_token;
         amb += found_amb;
         if (token < 0) {
             // rounding pushed the target past the chunk: its last positive weight
-            for (int t = c1 - 1; t >= c0; --t)
-                if (weight_at(w, t).hi > 0.f) { token = t; break; }
-            if (token < 0) token = c1 - 1;
+            for (int t = ce - 1; t >= cb; --t)
+                if (weight_positive(weight_at(w, t))) { token = t; break; }
+            if (token < 0) token = ce - 1;
             ++amb;
         }
         p.out_tok[(long long)b * (p.gamma + 1) + job.acc] = token;
@@ -577,14 +758,14 @@ __global__ void __launch_bounds__(kAccThreads) accept_sample_kernel(const Accept
 // ------------------------------------------------------------------- host side
 static size_t align256a(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace layout: [counters: kAcceptMaxBatch int32, always left zero]
-//                   [row stats][per-sequence job][per-chunk weight sums]
+// Workspace layout: [row stats][per-sequence job][chunk sums]; no initial
+// contents needed.
 size_t accept_workspace_bytes(int B, int gamma, int V) {
-    const int n_chunks = (V + kAccChunk - 1) / kAccChunk;
-    const int n_stat = (V + kStatChunk - 1) / kStatChunk;
+    const int n_stat = ((V + kStatChunk - 1) / kStatChunk + kAccThreads / 32 - 1) / (kAccThreads / 32);
+    const int n_chunks = (V + kSmpChunk - 1) / kSmpChunk;
     const int rows = 2 * gamma + 1;
-    return (size_t)kAcceptMaxBatch * 4 + align256a((size_t)B * rows * n_stat * sizeof(RowStat)) +
-           align256a((size_t)B * sizeof(JobInfo)) + align256a((size_t)B * n_chunks * sizeof(double));
+    return align256a((size_t)B * rows * n_stat * sizeof(RowStat)) + align256a((size_t)B * sizeof(JobInfo)) +
+           align256a((size_t)B * n_chunks * sizeof(double));
 }
 
 magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target, const float *draft,
@@ -603,29 +784,28 @@ magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target,
     prm.gamma = gamma;
     prm.V = V;
     prm.greedy = greedy ? 1 : 0;
-    prm.n_chunks = (V + kAccChunk - 1) / kAccChunk;
-    prm.n_stat_chunks = (V + kStatChunk - 1) / kStatChunk;
+    prm.n_stat_chunks = ((V + kStatChunk - 1) / kStatChunk + kAccThreads / 32 - 1) / (kAccThreads / 32);
+    prm.n_chunks = (V + kSmpChunk - 1) / kSmpChunk;
     prm.rows_per_b = greedy ? gamma + 1 : 2 * gamma + 1;
     if (2 * gamma + 1 > kMaxRows) return MAGICDEC_ERR_UNSUPPORTED;
     prm.err = magicdec_host::device_error_word();
     const int rows_alloc = 2 * gamma + 1;
     uint8_t *w = static_cast<uint8_t *>(ws);
-    prm.counters = reinterpret_cast<int *>(w);
-    w += (size_t)kAcceptMaxBatch * 4;
     prm.stats = reinterpret_cast<RowStat *>(w);
     w += align256a((size_t)B * rows_alloc * prm.n_stat_chunks * sizeof(RowStat));
     prm.job = reinterpret_cast<JobInfo *>(w);
     w += align256a((size_t)B * sizeof(JobInfo));
     prm.chunk_sum = reinterpret_cast<double *>(w);
 
-    const long long n_work = (long long)B * prm.rows_per_b * prm.n_stat_chunks;
     magicdec_status s = magicdec_host::launch_pdl(greedy ? accept_stats_kernel<true> : accept_stats_kernel<false>,
-                                                  dim3((unsigned)((n_work + kAccThreads / 32 - 1) / (kAccThreads / 32))),
+                                                  dim3((unsigned)(B * prm.rows_per_b), (unsigned)prm.n_stat_chunks),
                                                   dim3(kAccThreads), 0, st, prm);
     if (s != MAGICDEC_OK) return s;
     s = magicdec_host::launch_pdl(accept_chain_kernel, dim3(B), dim3(kChainThreads), 0, st, prm);
     if (s != MAGICDEC_OK || greedy) return s;
-    return magicdec_host::launch_pdl(accept_sample_kernel, dim3(prm.n_chunks, B), dim3(kAccThreads), 0, st, prm);
+    s = magicdec_host::launch_pdl(accept_chunk_kernel, dim3(prm.n_chunks, B), dim3(kChkThreads), 0, st, prm);
+    if (s != MAGICDEC_OK) return s;
+    return magicdec_host::launch_pdl(accept_sample_kernel, dim3(B), dim3(kSmpThreads), 0, st, prm);
 }
 
 }  // namespace magicdec

@@ -367,7 +367,7 @@ __device__ void tk_select_full_row(const float *srow, int len, int top_k, int d1
 template <int D>
 __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSelParams p) {
     constexpr int NW = kTkNW;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     int *hist = reinterpret_cast<int *>(smem_raw);                    // [4096]; later [NW][D] partial outputs
     int *cand_pos = hist + kTkBins;                                   // [cand_cap]
     uint32_t *cand_key = reinterpret_cast<uint32_t *>(cand_pos + p.cand_cap);   // [cand_cap]
