@@ -200,7 +200,9 @@ class Pipeline:
         self.ws_attn = torch.zeros(ws_attn, dtype=torch.uint8, device=device)
         self.ws_acc = torch.zeros(mb.magicdec_spec_accept_workspace_size(w.B, w.gamma, w.V), dtype=torch.uint8,
                                   device=device)
-        self.launches_per_step = layers * (3 + w.gamma) + 3
+        # per layer: streaming select, gather, gamma draft attentions, verification;
+        # accept (sampling mode): statistics, chain, chunk sums, draw
+        self.launches_per_step = layers * (3 + w.gamma) + 4
         self.verify_events = []
 
     def step(self, record: bool = False):

@@ -141,7 +141,8 @@ __device__ __forceinline__ void top_merge(float &t1, float &t2, int &arg, float 
 // load instruction is coalesced.  Sampling mode records the CTA's max m and
 // S = sum exp(x - m): the warps agree on m through shared memory, each lane
 // sums its 32 exponentials pairwise in fp32 (error ~1e-7 relative, the order
-// of the exponential's own), lanes and warps merge in fp64 in a fixed order.
+// of the exponential's own), lanes merge in double-float and warps in fp64, in
+// a fixed order.
 // Greedy mode records only the top two logits and the argmax (smallest index
 // on ties).
 template <bool GREEDY>
@@ -238,9 +239,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
             for (int w = kAccPer / 2; w > 0; w >>= 1)
 #pragma unroll
                 for (int i = 0; i < w; ++i) e[i] += e[i + w];
-            sum = (double)e[0];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            // lanes merge in double-float on the FP32 pipe (fp64 throughput is scarce)
+            sum = df_to_double(warp_sum_df(dflt{e[0], 0.f}));
         }
         if (lane == 0) s_sum[warp] = sum;
         __syncthreads();
