@@ -61,10 +61,11 @@ def _load():
             lib.oracle_spec_accept.argtypes = [I, I, I, P, P, P, P, P, I, P, P, P]
             lib.oracle_resample_weights.argtypes = [P, P, I, P]
             lib.oracle_topk_attn.argtypes = [I, I, I, I, I, P, P, P, P, I, P, P, P]
+            lib.oracle_draft_cache_update.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I, I, P, P, P]
             for name in ("oracle_verify_attn", "oracle_draft_attn", "oracle_streaming_select",
                          "oracle_gather_kv", "oracle_snapkv_scores", "oracle_maxpool1d",
                          "oracle_snapkv_select", "oracle_spec_accept", "oracle_resample_weights",
-                         "oracle_topk_attn"):
+                         "oracle_topk_attn", "oracle_draft_cache_update"):
                 getattr(lib, name).restype = I
             _lib = lib
     return _lib
@@ -192,6 +193,26 @@ def topk_attn(q, k, v, seq_len, top_k: int, want_scores: bool = False):
                                     int(top_k), _ptr(out), _ptr(idx),
                                     _ptr(scores) if scores is not None else None), "topk_attn")
     return out, idx, scores
+
+
+def draft_cache_update(k, v, kc, vc, len_valid, len_old, len_new, origin, base, ring: int):
+    """Update the compact draft cache kc/vc [B,H_kv,cap,d] u16 IN PLACE from the full cache
+    k/v [B,L_cap,H_kv,d] u16.  ring > 0: StreamingLLM ring layout (base unused); ring == 0:
+    SnapKV linear layout.  -> (draft_len int32 [B], number of writes skipped past cap)."""
+    k, v = _c(k, np.uint16), _c(v, np.uint16)
+    assert kc.flags.c_contiguous and vc.flags.c_contiguous and kc.dtype == np.uint16 and vc.dtype == np.uint16
+    B, L_cap, H_kv, d = k.shape
+    cap = kc.shape[2]
+    lv, lo, ln = (_c(a, np.int32) for a in (len_valid, len_old, len_new))
+    org = _c(origin, np.int32)
+    bs = _c(base, np.int32) if base is not None else None
+    draft_len = np.empty((B,), np.int32)
+    rc = _load().oracle_draft_cache_update(B, H_kv, d, L_cap, _ptr(k), _ptr(v), _ptr(lv), _ptr(lo), _ptr(ln),
+                                           _ptr(org), _ptr(bs) if bs is not None else None, int(ring), int(cap),
+                                           _ptr(kc), _ptr(vc), _ptr(draft_len))
+    if rc < 0:
+        raise ValueError("draft_cache_update: invalid arguments")
+    return draft_len, int(rc)
 
 
 def spec_accept(target, draft, draft_tok, u_acc, u_res, greedy: bool):

@@ -21,7 +21,9 @@
  *   - SnapKV selection: observation-window attention scores, summed over the
  *     window rows and the query heads of a KV group, max-pooled, per-KV-head
  *     top-k, observation window always kept (section 4.4, section 5.2);
- *   - the "pre-gather a sparse KV cache" copy (section 4.4);
+ *   - the "pre-gather a sparse KV cache" copy (section 4.4) and the
+ *     append / rollback of the compact cache as tokens are accepted or
+ *     rejected (sections 3.1, 4.4);
  *   - Top-K attention drafting: each draft query attends to its own top_k
  *     highest-scoring positions of the full cache (section 1, Figure 1(c);
  *     section 4.4);
@@ -378,6 +380,88 @@ int oracle_snapkv_select(int B, int H_q, int H_kv, int d, int L_cap,
     }
     free(score);
     return 0;
+}
+
+/*
+ * Draft-cache update: keeps the compact draft cache equal to the static
+ * selection as the sequence grows by accepted tokens and shrinks when
+ * speculated tokens are rejected (section 4.4: the static drafts select once
+ * and then only append; section 3.1: after verification the cache keeps the
+ * accepted prefix).  Two layouts of kc/vc [B, H_kv, cap, d]:
+ *   ring > 0 (StreamingLLM, section 5.1): position q < origin[b] (a sink)
+ *     sits at slot q; position q >= origin[b] at slot
+ *     origin[b] + (q - origin[b]) mod ring, so the ring holds the last `ring`
+ *     positions; after the update the occupied slots hold exactly positions
+ *     [0, min(len, origin)) and [max(origin, len - ring), len).
+ *   ring == 0 (SnapKV, section 5.2): slots [0, base[b]) hold the rows chosen
+ *     at selection time; position q >= origin[b] (the length at selection)
+ *     is appended at slot base[b] + q - origin[b].
+ * Rows of positions >= len_valid[b] in the compact cache are stale (drafted
+ * by the sparse model, or never written); len_old[b] is the length the
+ * cache was last brought to, len_new[b] the new length; all three clamp to
+ * [0, L_cap] and len_valid to at most min(len_old, len_new).  The update
+ * copies from the full cache k/v [B, L_cap, H_kv, d] every position of the
+ * new window at or past len_valid, and (ring layout) restores each slot that
+ * a position in [len_new, len_old) overwrote with the window position it had
+ * displaced (p - ring).  draft_len[b] receives the occupied slot count,
+ * clamped to cap.  Returns the number of row writes skipped because their
+ * slot was at or past cap, or -1 on invalid arguments.
+ */
+int oracle_draft_cache_update(int B, int H_kv, int d, int L_cap, const uint16_t *k, const uint16_t *v,
+                              const int32_t *len_valid, const int32_t *len_old, const int32_t *len_new,
+                              const int32_t *origin, const int32_t *base, int ring, int cap,
+                              uint16_t *kc, uint16_t *vc, int32_t *draft_len)
+{
+    if (B < 0 || H_kv <= 0 || d <= 0 || L_cap < 0 || ring < 0 || cap <= 0) return -1;
+    if (ring == 0 && !base) return -1;
+    int skipped = 0, b, h;
+    for (b = 0; b < B; ++b) {
+        const int lo = clamp_len(len_old[b], L_cap), ln = clamp_len(len_new[b], L_cap);
+        int lv = clamp_len(len_valid[b], L_cap);
+        if (lv > lo) lv = lo;
+        if (lv > ln) lv = ln;
+        const int o = origin[b] < 0 ? 0 : origin[b];
+        long n_ops = 0, cap_ops = 2L * (ring > 0 ? ring : 0) + (ln > lv ? ln - lv : 0) + 1;
+        long *src = (long *)malloc(sizeof(long) * (size_t)cap_ops);
+        long *dst = (long *)malloc(sizeof(long) * (size_t)cap_ops);
+        int q, p, dl;
+        if (ring > 0) {
+            for (q = lv; q < ln; ++q) {
+                if (q >= o && q < ln - ring) continue;          /* displaced before the end */
+                src[n_ops] = q;
+                dst[n_ops++] = q < o ? q : o + (q - o) % ring;
+            }
+            for (p = ln; p < lo && p < ln + ring; ++p) {
+                if (p < o) continue;
+                q = p - ring;
+                if (q < o || q >= lv) continue;
+                src[n_ops] = q;
+                dst[n_ops++] = o + (p - o) % ring;
+            }
+            dl = ln <= o ? ln : o + ((ln - o) < ring ? (ln - o) : ring);
+        } else {
+            const int bs = base[b] < 0 ? 0 : base[b];
+            for (q = (lv > o ? lv : o); q < ln; ++q) {
+                src[n_ops] = q;
+                dst[n_ops++] = bs + (q - o);
+            }
+            dl = bs + (ln > o ? ln - o : 0);
+        }
+        long i;
+        for (i = 0; i < n_ops; ++i) {
+            if (dst[i] >= cap) { ++skipped; continue; }
+            for (h = 0; h < H_kv; ++h) {
+                const size_t from = (((size_t)b * L_cap + (size_t)src[i]) * H_kv + h) * d;
+                const size_t to = (((size_t)b * H_kv + h) * cap + (size_t)dst[i]) * d;
+                memcpy(kc + to, k + from, sizeof(uint16_t) * (size_t)d);
+                memcpy(vc + to, v + from, sizeof(uint16_t) * (size_t)d);
+            }
+        }
+        draft_len[b] = dl < cap ? dl : cap;
+        free(src);
+        free(dst);
+    }
+    return skipped;
 }
 
 /*

@@ -206,6 +206,117 @@ def test_topk_attn_ties_and_single_winner():
 
 
 # --------------------------------------------------------------------------
+# Draft-cache update (append / rollback)
+# --------------------------------------------------------------------------
+def _encoded_cache(B, L, H_kv, d, version):
+    """Rows whose first channels spell (position // 256, position % 256, head, version): exact in bf16."""
+    k = np.zeros((B, L, H_kv, d), np.float32)
+    pos = np.arange(L)
+    k[:, :, :, 0] = (pos // 256)[None, :, None]
+    k[:, :, :, 1] = (pos % 256)[None, :, None]
+    k[:, :, :, 2] = np.arange(H_kv)[None, None, :]
+    k[:, :, :, 3] = version
+    return bf16_bits(k)
+
+
+def _decode(kc_row):
+    f = bits_to_f64(kc_row)
+    return int(f[0]) * 256 + int(f[1]), int(f[2]), int(f[3])
+
+
+def _slots(kc, b, n):
+    """(positions, versions) held by slots [0, n) of every head of sequence b (heads must agree)."""
+    out = []
+    for h in range(kc.shape[1]):
+        rows = [_decode(kc[b, h, i]) for i in range(n)]
+        assert all(r[1] == h for r in rows)
+        out.append(sorted((r[0], r[2]) for r in rows))
+    assert all(o == out[0] for o in out)
+    return [p for p, _ in out[0]], [v for _, v in out[0]]
+
+
+def test_draft_cache_ring_tracks_streaming_selection():
+    """Drafting appends, then after each verification the cache is refreshed to the accepted length:
+    the occupied slots always hold exactly the StreamingLLM selection, as verified rows."""
+    rng = np.random.default_rng(31)
+    B, H_kv, d, L, S, W, gamma = 3, 2, 16, 400, 4, 20, 3
+    drafted = _encoded_cache(B, L, H_kv, d, 0)
+    verified = _encoded_cache(B, L, H_kv, d, 1)
+    kc = np.zeros((B, H_kv, S + W, d), np.uint16)
+    vc = np.zeros_like(kc)
+    origin = np.full(B, S, np.int32)
+    length = np.array([2, 10, 100], np.int32)
+    z = np.zeros(B, np.int32)
+    dl, skipped = oracle.draft_cache_update(verified, verified, kc, vc, z, z, length, origin, None, W)
+    assert skipped == 0
+    for _ in range(30):
+        for i in range(gamma):           # drafted rows of the sparse model
+            dl, _ = oracle.draft_cache_update(drafted, drafted, kc, vc, length + i, length + i, length + i + 1,
+                                              origin, None, W)
+            for b in range(B):
+                idx, n_sel = oracle.streaming_select(length[b:b + 1] + i + 1, 1, S, W)
+                pos, _ = _slots(kc, b, dl[b])
+                assert pos == sorted(idx[0, 0, : n_sel[0]].tolist())
+        n_acc = rng.integers(0, gamma + 1, size=B).astype(np.int32)
+        new = length + n_acc + 1
+        dl, skipped = oracle.draft_cache_update(verified, verified, kc, vc, length, length + gamma, new, origin,
+                                                None, W)
+        assert skipped == 0
+        for b in range(B):
+            idx, n_sel = oracle.streaming_select(new[b:b + 1], 1, S, W)
+            assert dl[b] == n_sel[0]
+            pos, ver = _slots(kc, b, dl[b])
+            assert pos == sorted(idx[0, 0, : n_sel[0]].tolist())
+            assert all(x == 1 for x in ver), "a drafted row survived verification"
+        length = new
+
+
+def test_draft_cache_rollback_restores_the_ring():
+    B, H_kv, d, L, S, W = 2, 1, 16, 200, 3, 16
+    full = _encoded_cache(B, L, H_kv, d, 1)
+    kc = np.zeros((B, H_kv, S + W, d), np.uint16)
+    vc = np.zeros_like(kc)
+    origin = np.full(B, S, np.int32)
+    z = np.zeros(B, np.int32)
+    length = np.array([60, 18], np.int32)
+    oracle.draft_cache_update(full, full, kc, vc, z, z, length, origin, None, W)
+    before, dl0 = kc.copy(), None
+    for grow in (1, 5, W + 7):
+        dl, _ = oracle.draft_cache_update(full, full, kc, vc, length, length, length + grow, origin, None, W)
+        dl, _ = oracle.draft_cache_update(full, full, kc, vc, length, length + grow, length, origin, None, W)
+        for b in range(B):
+            np.testing.assert_array_equal(kc[b, :, : dl[b]], before[b, :, : dl[b]])
+            np.testing.assert_array_equal(vc[b, :, : dl[b]], before[b, :, : dl[b]])
+
+
+def test_draft_cache_linear_appends_after_selection():
+    rng = np.random.default_rng(32)
+    B, H_kv, d, L, L0, n_sel, cap = 2, 2, 16, 300, 120, 40, 100
+    full = _encoded_cache(B, L, H_kv, d, 1)
+    kc = np.zeros((B, H_kv, cap, d), np.uint16)
+    vc = np.zeros_like(kc)
+    sel = np.stack([np.sort(rng.choice(L0, n_sel, replace=False)) for _ in range(B)]).astype(np.int32)
+    idx = np.repeat(sel[:, None, :], H_kv, axis=1)
+    kc0, vc0 = oracle.gather_kv(full, full, idx, cap)
+    kc[:], vc[:] = kc0, vc0
+    origin = np.full(B, L0, np.int32)
+    base = np.full(B, n_sel, np.int32)
+    length = np.full(B, L0, np.int32)
+    for step in range(6):
+        new = length + rng.integers(1, 5, size=B).astype(np.int32)
+        dl, skipped = oracle.draft_cache_update(full, full, kc, vc, length, length, new, origin, base, 0)
+        assert skipped == 0
+        for b in range(B):
+            pos, _ = _slots(kc, b, dl[b])
+            assert pos == sorted(sel[b].tolist() + list(range(L0, int(new[b]))))
+        length = new
+    # capacity: an append past cap is skipped, reported, and draft_len clamps to cap
+    big = np.full(B, L0 + (cap - n_sel) + 3, np.int32)
+    dl, skipped = oracle.draft_cache_update(full, full, kc, vc, length, length, big, origin, base, 0)
+    assert skipped == 3 * B and np.all(dl == cap)
+
+
+# --------------------------------------------------------------------------
 # StreamingLLM selection and gather
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("n_sink,n_recent", [(4, 60), (16, 496), (0, 8), (5, 0)])
