@@ -73,8 +73,11 @@ MAGICDEC_API const char *magicdec_status_string(int status);
 
 /* Copies the device error word of the current device into *out and clears it
  * (synchronises the device).  Non-zero means a kernel gave up on a bounded
- * wait (value 1) or met an inconsistent internal state (value 2); its outputs
- * are then undefined.  Returns MAGICDEC_OK or MAGICDEC_ERR_CUDA. */
+ * wait (value 1) or met an inconsistent internal state (value 2), and its
+ * outputs are then undefined; or that magicdec_draft_cache_update skipped a
+ * row whose slot was at or past the cache capacity (value 3).  The first
+ * error since the last read is kept.  Returns MAGICDEC_OK or
+ * MAGICDEC_ERR_CUDA. */
 MAGICDEC_API magicdec_status magicdec_device_error(int32_t *out);
 
 /*
@@ -130,6 +133,42 @@ MAGICDEC_API magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, con
 MAGICDEC_API magicdec_status magicdec_gather_kv(magicdec_kv_shape shape, const uint16_t *k, const uint16_t *v,
                                    const int32_t *idx, int n_idx, int cap, uint16_t *kc, uint16_t *vc,
                                    void *stream);
+
+/*
+ * Draft-cache update: append, post-verification refresh and rollback of the
+ * compact draft cache (paper section 4.4: the static drafts select once and
+ * afterwards only take in new tokens; section 3.1: verification keeps the
+ * accepted prefix, so rows the sparse draft wrote for rejected or
+ * re-verified positions are replaced).  Layouts of kc, vc [B, H_kv, cap, d]:
+ *   ring > 0 (StreamingLLM, sinks + recent window): position q < origin[b]
+ *     at slot q; position q >= origin[b] at slot
+ *     origin[b] + (q - origin[b]) mod ring.  The occupied slots hold exactly
+ *     positions [0, min(len, origin)) and [max(origin, len - ring), len);
+ *     from an empty cache, update(0, 0, L) builds the StreamingLLM selection
+ *     for length L.  base is not read (may be NULL).
+ *   ring == 0 (SnapKV): slots [0, base[b]) hold the rows kept at selection
+ *     (magicdec_gather_kv); position q >= origin[b] (the length at selection)
+ *     is appended at slot base[b] + q - origin[b].
+ * Lengths (device int32 [B], clamped to [0, L_cap]; len_valid to at most
+ * min(len_old, len_new)): rows of positions >= len_valid in the compact cache
+ * are stale (drafted, or never written); len_old is the length the cache was
+ * last brought to, len_new the new one.  The call copies from k, v
+ * [B, L_cap, H_kv, d] every position of the new window at or past len_valid,
+ * and (ring layout) restores every slot that a position in [len_new, len_old)
+ * overwrote with the window position it displaced.  Typical use, per layer:
+ * drafting appends position L+i as update(L+i, L+i, L+i+1); after
+ * verification with n_acc accepted, update(L, L+gamma, L+n_acc+1).
+ *   draft_len [B] int32 out: occupied slots (the draft attention's length),
+ *   clamped to cap.
+ * Errors: NULL pointers, bad shape, ring < 0, cap <= 0, base NULL when
+ * ring == 0, ring > 0 with ring > cap, alignment.  A copy whose slot is at or
+ * past cap is skipped and sets the device error word to 3.
+ */
+MAGICDEC_API magicdec_status magicdec_draft_cache_update(magicdec_kv_shape shape, const uint16_t *k, const uint16_t *v,
+                                                         const int32_t *len_valid, const int32_t *len_old,
+                                                         const int32_t *len_new, const int32_t *origin,
+                                                         const int32_t *base, int ring, int cap, uint16_t *kc,
+                                                         uint16_t *vc, int32_t *draft_len, void *stream);
 
 /* Workspace bytes magicdec_draft_attn / magicdec_verify_attn need for this
  * shape and query count (n_q = 1 for draft) on the current device. */

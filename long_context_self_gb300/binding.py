@@ -48,6 +48,7 @@ _SIGNATURES = {
     "magicdec_draft_attn": ([KVShape, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "magicdec_verify_attn": ([KVShape, _I, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "magicdec_verify_attn_noalloc": ([KVShape, _I, _P, _P, _P, _P, _P, _P], _I),
+    "magicdec_draft_cache_update": ([KVShape, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P], _I),
     "magicdec_topk_attn_workspace_size": ([KVShape], _S),
     "magicdec_topk_draft_attn": ([KVShape, _P, _P, _P, _P, _I, _P, _P, _P, _S, _P], _I),
     "magicdec_spec_accept_workspace_size": ([_I, _I, _I], _S),
@@ -277,6 +278,37 @@ def magicdec_verify_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tens
            lib().magicdec_verify_attn_noalloc(kv_shape(B, H_q, H_kv, d, L_cap), n_q, _ptr(q), _ptr(k), _ptr(v),
                                               _ptr(seq_len), _ptr(out), _stream(stream, dev)))
     return out
+
+
+def magicdec_draft_cache_update(k: torch.Tensor, v: torch.Tensor, kc: torch.Tensor, vc: torch.Tensor,
+                                len_valid: torch.Tensor, len_old: torch.Tensor, len_new: torch.Tensor,
+                                origin: torch.Tensor, base: Optional[torch.Tensor], ring: int,
+                                draft_len: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Update the compact draft cache kc/vc [B, H_kv, cap, d] in place from k/v [B, L_cap, H_kv, d];
+    ring > 0: StreamingLLM ring layout, ring == 0: SnapKV linear layout (base required).
+    Returns draft_len int32 [B]."""
+    _need(k, "k", torch.bfloat16)
+    dev = k.device
+    _need(v, "v", torch.bfloat16, dev)
+    _need(kc, "kc", torch.bfloat16, dev)
+    _need(vc, "vc", torch.bfloat16, dev)
+    for name, t in (("len_valid", len_valid), ("len_old", len_old), ("len_new", len_new), ("origin", origin)):
+        _need(t, name, torch.int32, dev)
+    if base is not None:
+        _need(base, "base", torch.int32, dev)
+    B, L_cap, H_kv, d = k.shape
+    if v.shape != k.shape or kc.shape != vc.shape or kc.shape[0] != B or kc.shape[1] != H_kv or kc.shape[3] != d:
+        raise ValueError("k / v / kc / vc shapes disagree")
+    cap = kc.shape[2]
+    if draft_len is None:
+        draft_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(draft_len, "draft_len", torch.int32, dev)
+    shape = kv_shape(B, H_kv, H_kv, d, L_cap)
+    _check("magicdec_draft_cache_update",
+           lib().magicdec_draft_cache_update(shape, _ptr(k), _ptr(v), _ptr(len_valid), _ptr(len_old), _ptr(len_new),
+                                             _ptr(origin), _ptr(base), int(ring), int(cap), _ptr(kc), _ptr(vc),
+                                             _ptr(draft_len), _stream(stream, dev)))
+    return draft_len
 
 
 def magicdec_topk_attn_workspace_size(shape: KVShape) -> int:

@@ -14,6 +14,10 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
                                    void *ws, cudaStream_t st);
 size_t attn_workspace_bytes(int B, int H_kv, int D, int M);
 size_t topk_workspace_bytes(int B, int H_q, int L_cap);
+magicdec_status launch_draft_cache_update(int B, int H_kv, int D, int L_cap, const void *k, const void *v,
+                                          const int32_t *len_valid, const int32_t *len_old, const int32_t *len_new,
+                                          const int32_t *origin, const int32_t *base, int ring, int cap, void *kc,
+                                          void *vc, int32_t *draft_len, cudaStream_t st);
 magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,
                                        const void *v, const int32_t *len, int top_k, void *out, int32_t *idx,
                                        void *ws, cudaStream_t st);
@@ -213,6 +217,20 @@ magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n_q, const uin
     if (s != MAGICDEC_OK) return s;
     return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, n_q, 0, q, k, v,
                                         seq_len, out, ws, static_cast<cudaStream_t>(stream));
+}
+
+magicdec_status magicdec_draft_cache_update(magicdec_kv_shape shape, const uint16_t *k, const uint16_t *v,
+                                            const int32_t *len_valid, const int32_t *len_old, const int32_t *len_new,
+                                            const int32_t *origin, const int32_t *base, int ring, int cap,
+                                            uint16_t *kc, uint16_t *vc, int32_t *draft_len, void *stream) {
+    if (!k || !v || !len_valid || !len_old || !len_new || !origin || !kc || !vc || !draft_len)
+        return MAGICDEC_ERR_NULL;
+    if (ring == 0 && !base) return MAGICDEC_ERR_NULL;
+    if (!shape_ok(shape) || ring < 0 || cap <= 0 || ring > cap) return MAGICDEC_ERR_SHAPE;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc)) return MAGICDEC_ERR_ALIGN;
+    return magicdec::launch_draft_cache_update(shape.B, shape.H_kv, shape.d, shape.L_cap, k, v, len_valid, len_old,
+                                               len_new, origin, base, ring, cap, kc, vc, draft_len,
+                                               static_cast<cudaStream_t>(stream));
 }
 
 size_t magicdec_topk_attn_workspace_size(magicdec_kv_shape shape) {

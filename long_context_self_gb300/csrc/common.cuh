@@ -17,9 +17,11 @@
 namespace magicdec {
 
 // Device error word codes (the word itself lives in api.cu; kernels get its
-// address): 1 = a bounded wait gave up, 2 = inconsistent internal state.
+// address): 1 = a bounded wait gave up, 2 = inconsistent internal state,
+// 3 = a draft-cache copy needed a slot at or past the cache capacity.
 constexpr int kErrTimeout = 1;
 constexpr int kErrState = 2;
+constexpr int kErrCapacity = 3;
 
 // Fixed-size counter regions at the start of the caller's workspaces: the
 // attention kernels keep one counter per (sequence, KV head) pair, the

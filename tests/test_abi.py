@@ -86,6 +86,15 @@ def test_null_and_shape_errors_are_reported_before_launch(lib):
     assert lib.magicdec_spec_accept(4, 3, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, NULL, FAKE,
                                     8, NULL) == -4
     big = 1 << 40
+    I32 = P(0x20000)
+    assert lib.magicdec_draft_cache_update(shape(), FAKE, FAKE, I32, I32, I32, I32, NULL, 0, 64, FAKE, FAKE, I32,
+                                           NULL) == -1
+    assert lib.magicdec_draft_cache_update(shape(), FAKE, FAKE, I32, I32, I32, I32, NULL, 80, 64, FAKE, FAKE, I32,
+                                           NULL) == -2
+    assert lib.magicdec_draft_cache_update(shape(), FAKE, FAKE, I32, I32, I32, I32, NULL, -1, 64, FAKE, FAKE, I32,
+                                           NULL) == -2
+    assert lib.magicdec_draft_cache_update(shape(), FAKE, FAKE, I32, I32, I32, I32, NULL, 16, 64, MISALIGNED, FAKE,
+                                           I32, NULL) == -3
     assert lib.magicdec_topk_draft_attn(shape(), NULL, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, big, NULL) == -1
     assert lib.magicdec_topk_draft_attn(shape(), FAKE, FAKE, FAKE, FAKE, 0, FAKE, NULL, FAKE, big, NULL) == -2
     assert lib.magicdec_topk_draft_attn(shape(d=96), FAKE, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, big, NULL) == -2

@@ -8,6 +8,7 @@ pair or one sequence at a time from host copies of exactly the bytes the GPU rea
   * SnapKV selection: sampled pairs (band rule at the k-th pooled score);
   * Top-K attention draft: every query head of sampled sequences (band rule at the
     top_k-th score);
+  * draft-cache update: the StreamingLLM ring of sampled sequences, byte for byte;
   * speculative accept: every sequence of the batch (sampling mode) or a sample (greedy).
 """
 import numpy as np
@@ -139,6 +140,43 @@ def test_fullsize_topk_draft_sampled(name, top_k):
         swapped += sw
     assert swapped <= 2
     del k, v
+    torch.cuda.empty_cache()
+
+
+def test_fullsize_draft_cache_ring_sampled():
+    """The StreamingLLM ring built from an empty cache at B=128, L=32000, then one draft/verify
+    cycle (3 appends, refresh to n_acc = 1): sampled sequences equal the oracle byte for byte."""
+    w = synth.WORKLOADS["llama8b_b128_l32k"]
+    k, v, _ = synth.kv_cache(w, DEV)
+    cap = w.stream_budget
+    kc = torch.zeros((w.B, w.H_kv, cap, w.d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    i32 = lambda x: torch.full((w.B,), int(x), dtype=torch.int32, device=DEV)
+    L0 = w.L - 8
+    org = i32(w.n_sink)
+    mb.magicdec_draft_cache_update(k, v, kc, vc, i32(0), i32(0), i32(L0), org, None, w.n_recent)
+    for g in range(3):
+        mb.magicdec_draft_cache_update(k, v, kc, vc, i32(L0 + g), i32(L0 + g), i32(L0 + g + 1), org, None, w.n_recent)
+    dl = mb.magicdec_draft_cache_update(k, v, kc, vc, i32(L0), i32(L0 + 3), i32(L0 + 2), org, None, w.n_recent)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(w.seed + 13)
+    for b in rng.choice(w.B, size=2, replace=False):
+        b = int(b)
+        ko, vo = to_u16(k[b:b + 1]), to_u16(v[b:b + 1])
+        kc_o = np.zeros((1, w.H_kv, cap, w.d), np.uint16)
+        vc_o = np.zeros_like(kc_o)
+        one = lambda x: np.array([x], np.int32)
+        oo = one(w.n_sink)
+        oracle.draft_cache_update(ko, vo, kc_o, vc_o, one(0), one(0), one(L0), oo, None, w.n_recent)
+        for g in range(3):
+            oracle.draft_cache_update(ko, vo, kc_o, vc_o, one(L0 + g), one(L0 + g), one(L0 + g + 1), oo, None,
+                                      w.n_recent)
+        dl_o, _ = oracle.draft_cache_update(ko, vo, kc_o, vc_o, one(L0), one(L0 + 3), one(L0 + 2), oo, None,
+                                            w.n_recent)
+        assert int(dl[b]) == int(dl_o[0]) == cap
+        assert np.array_equal(to_u16(kc[b:b + 1]), kc_o)
+        assert np.array_equal(to_u16(vc[b:b + 1]), vc_o)
+    del k, v, kc, vc
     torch.cuda.empty_cache()
 
 

@@ -177,6 +177,80 @@ def test_snapkv_select_matches_oracle(B, H_q, H_kv, d, L_cap, w, pool, budget, l
     assert band <= 2 * pool * B * H_kv + 8, f"too many band positions: {band}"
 
 
+# ------------------------------------------------------- draft-cache update
+def _dc_step(k, v, kc, vc, kc_o, vc_o, lv, lo, ln, origin, base, ring):
+    dev = torch.device(DEV)
+    t = lambda a: torch.from_numpy(np.asarray(a, np.int32)).to(dev)
+    dl = mb.magicdec_draft_cache_update(k, v, kc, vc, t(lv), t(lo), t(ln), t(origin),
+                                        None if base is None else t(base), ring)
+    dl_o, _ = oracle.draft_cache_update(to_u16(k), to_u16(v), kc_o, vc_o, lv, lo, ln, origin, base, ring)
+    torch.cuda.synchronize()
+    dl_g = dl.cpu().numpy()
+    assert np.array_equal(dl_g, dl_o)
+    kg, vg = to_u16(kc), to_u16(vc)
+    for b in range(kc.shape[0]):
+        assert np.array_equal(kg[b, :, : dl_o[b]], kc_o[b, :, : dl_o[b]]), b
+        assert np.array_equal(vg[b, :, : dl_o[b]], vc_o[b, :, : dl_o[b]]), b
+    return dl
+
+
+def test_draft_cache_update_ring_walk_matches_oracle():
+    """StreamingLLM 16+496 ring: build from empty, then draft appends and post-verification refreshes
+    with random acceptance; every state equals the oracle's byte for byte, and draft attention over the
+    ring equals the oracle's attention over the ascending StreamingLLM gather."""
+    rng = np.random.default_rng(61)
+    B, H_q, H_kv, d, L, S, W, gamma = 4, 32, 8, 128, 3000, 16, 496, 3
+    k = rand_bf16((B, L, H_kv, d), 62).to(DEV)
+    v = rand_bf16((B, L, H_kv, d), 63).to(DEV)
+    cap = S + W
+    kc = torch.zeros((B, H_kv, cap, d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    kc_o = np.zeros((B, H_kv, cap, d), np.uint16)
+    vc_o = np.zeros_like(kc_o)
+    origin = np.full(B, S, np.int32)
+    length = np.array([5, 300, 512, 2500], np.int32)
+    z = np.zeros(B, np.int32)
+    _dc_step(k, v, kc, vc, kc_o, vc_o, z, z, length, origin, None, W)
+    for _ in range(12):
+        for i in range(gamma):
+            _dc_step(k, v, kc, vc, kc_o, vc_o, length + i, length + i, length + i + 1, origin, None, W)
+        new = length + rng.integers(0, gamma + 1, size=B).astype(np.int32) + 1
+        dl = _dc_step(k, v, kc, vc, kc_o, vc_o, length, length + gamma, new, origin, None, W)
+        length = new
+    q = rand_bf16((B, 1, H_q, d), 64)
+    out = mb.magicdec_draft_attn(q.to(DEV), kc, vc, dl)
+    torch.cuda.synchronize()
+    idx, n_sel = oracle.streaming_select(length, H_kv, S, W)
+    kg_o, vg_o = oracle.gather_kv(to_u16(k), to_u16(v), idx, cap)
+    ref = oracle.draft_attn(to_u16(q), kg_o, vg_o, n_sel)
+    check_attention(bf16_out_to_f64(out), ref, "draft over the ring cache")
+
+
+def test_draft_cache_update_linear_and_capacity():
+    B, H_kv, d, L, L0, n_sel, cap = 3, 8, 64, 900, 600, 100, 160
+    k = rand_bf16((B, L, H_kv, d), 65).to(DEV)
+    v = rand_bf16((B, L, H_kv, d), 66).to(DEV)
+    kc = torch.zeros((B, H_kv, cap, d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    kc_o = np.zeros((B, H_kv, cap, d), np.uint16)
+    vc_o = np.zeros_like(kc_o)
+    origin = np.full(B, L0, np.int32)
+    base = np.array([n_sel, n_sel - 7, n_sel], np.int32)
+    length = origin.copy()
+    for grow in (3, 1, 20):
+        _dc_step(k, v, kc, vc, kc_o, vc_o, length, length, length + grow, origin, base, 0)
+        length = length + grow
+    # roll back 10 then re-append 4 (lengths shrink: nothing to restore in the linear layout)
+    _dc_step(k, v, kc, vc, kc_o, vc_o, length - 10, length, length - 6, origin, base, 0)
+    length = length - 6
+    assert mb.magicdec_device_error() == 0
+    # past the capacity: rows skipped, draft_len clamped, error word 3 reported once
+    over = np.full(B, L0 + cap, np.int32)
+    _dc_step(k, v, kc, vc, kc_o, vc_o, length, length, over, origin, base, 0)
+    assert mb.magicdec_device_error() == 3
+    assert mb.magicdec_device_error() == 0
+
+
 # ------------------------------------------------------------ Top-K attention
 TOPK_CASES = [
     # B, H_q, H_kv, d, L_cap, top_k, lens
