@@ -99,7 +99,7 @@ MAGICDEC_API size_t magicdec_snapkv_workspace_size(magicdec_kv_shape shape, int 
 
 /*
  * SnapKV draft-KV selection, run once after prefill (paper section 4.4: a
- * static method that pre-gathers a sparse KV cache; section 5.2: best budget
+ * static method whose compact cache is built once; section 5.2: best budget
  * about 2048).  For each sequence of length L = seq_len[b] (clamped to
  * [0, L_cap]) and KV head h, the last `window` positions form the
  * observation window; window row r (position L-window+r) of query head hq has
@@ -123,7 +123,7 @@ MAGICDEC_API magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, con
 
 /*
  * Gather of the selected rows into the compact draft cache (paper section
- * 4.4, "pre-gather a sparse KV cache").
+ * 4.4: the static selections copy their rows into a compact cache once).
  *   k, v   [B, L_cap, H_kv, d] bf16;  idx [B, H_kv, n_idx] int32
  *   kc, vc [B, H_kv, cap, d] bf16 out: row i < n_idx of head h is
  *          k[b, idx[b,h,i], h] (zero row when the index is outside [0, L_cap));

@@ -11,7 +11,7 @@
 //              pooled score, then an order-preserving block compaction that
 //              keeps everything above the threshold and the smallest
 //              positions among ties; the window is appended.
-//  * Gather ("pre-gather a sparse KV cache", section 4.4): 16-byte vector
+//  * Gather of the selected rows into the compact cache (section 4.4): 16-byte vector
 //    row copies into the head-major compact draft cache.
 #include <algorithm>
 

@@ -21,7 +21,8 @@
  *   - SnapKV selection: observation-window attention scores, summed over the
  *     window rows and the query heads of a KV group, max-pooled, per-KV-head
  *     top-k, observation window always kept (section 4.4, section 5.2);
- *   - the "pre-gather a sparse KV cache" copy (section 4.4) and the
+ *   - the copy of the selected rows into the compact draft cache
+ *     (section 4.4) and the
  *     append / rollback of the compact cache as tokens are accepted or
  *     rejected (sections 3.1, 4.4);
  *   - Top-K attention drafting: each draft query attends to its own top_k
