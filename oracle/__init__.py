@@ -62,10 +62,14 @@ def _load():
             lib.oracle_resample_weights.argtypes = [P, P, I, P]
             lib.oracle_topk_attn.argtypes = [I, I, I, I, I, P, P, P, P, I, P, P, P]
             lib.oracle_draft_cache_update.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I, I, P, P, P]
+            lib.oracle_pq_encode.argtypes = [I, I, I, I, P, I, I, P, P, P]
+            lib.oracle_pq_update.argtypes = [I, I, I, I, P, P, I, I, P, P]
+            lib.oracle_pq_attn.argtypes = [I, I, I, I, I, P, P, P, P, I, I, P, P, I, P, P, P]
             for name in ("oracle_verify_attn", "oracle_draft_attn", "oracle_streaming_select",
                          "oracle_gather_kv", "oracle_snapkv_scores", "oracle_maxpool1d",
                          "oracle_snapkv_select", "oracle_spec_accept", "oracle_resample_weights",
-                         "oracle_topk_attn", "oracle_draft_cache_update"):
+                         "oracle_topk_attn", "oracle_draft_cache_update", "oracle_pq_encode",
+                         "oracle_pq_update", "oracle_pq_attn"):
                 getattr(lib, name).restype = I
             _lib = lib
     return _lib
@@ -213,6 +217,46 @@ def draft_cache_update(k, v, kc, vc, len_valid, len_old, len_new, origin, base, 
     if rc < 0:
         raise ValueError("draft_cache_update: invalid arguments")
     return draft_len, int(rc)
+
+
+def pq_encode(k, codebook, want_gap: bool = False):
+    """k [B,L_cap,H_kv,d] u16, codebook [B,H_kv,M,C,d/M] fp32 -> (codes u8 [B,L_cap,H_kv,M], gap fp64 or None)."""
+    k = _c(k, np.uint16)
+    cb = _c(codebook, np.float32)
+    B, L_cap, H_kv, d = k.shape
+    M, C = cb.shape[2], cb.shape[3]
+    codes = np.empty((B, L_cap, H_kv, M), np.uint8)
+    gap = np.empty((B, L_cap, H_kv, M), np.float64) if want_gap else None
+    _check(_load().oracle_pq_encode(B, H_kv, d, L_cap, _ptr(k), M, C, _ptr(cb), _ptr(codes),
+                                    _ptr(gap) if gap is not None else None), "pq_encode")
+    return codes, gap
+
+
+def pq_update(k, seq_len, codes, codebook):
+    """One Lloyd update: returns a new codebook (fp32) from codes u8 [B,L_cap,H_kv,M]."""
+    k, seq_len, codes = _c(k, np.uint16), _c(seq_len, np.int32), _c(codes, np.uint8)
+    cb = np.array(codebook, dtype=np.float32, copy=True, order="C")
+    B, L_cap, H_kv, d = k.shape
+    M, C = cb.shape[2], cb.shape[3]
+    _check(_load().oracle_pq_update(B, H_kv, d, L_cap, _ptr(k), _ptr(seq_len), M, C, _ptr(codes), _ptr(cb)),
+           "pq_update")
+    return cb
+
+
+def pq_attn(q, k, v, seq_len, codebook, codes, top_k: int, want_approx: bool = False):
+    """-> (out fp64 [B,1,H_q,d], idx int32 [B,H_q,top_k], approx fp64 [B,H_q,L_cap] or None)."""
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    seq_len, codes, cb = _c(seq_len, np.int32), _c(codes, np.uint8), _c(codebook, np.float32)
+    B, one, H_q, d = q.shape
+    L_cap, H_kv = k.shape[1], k.shape[2]
+    M, C = cb.shape[2], cb.shape[3]
+    out = np.zeros((B, 1, H_q, d), np.float64)
+    idx = np.empty((B, H_q, top_k), np.int32)
+    approx = np.zeros((B, H_q, L_cap), np.float64) if want_approx else None
+    _check(_load().oracle_pq_attn(B, H_q, H_kv, d, L_cap, _ptr(q), _ptr(k), _ptr(v), _ptr(seq_len), M, C, _ptr(cb),
+                                  _ptr(codes), int(top_k), _ptr(out), _ptr(idx),
+                                  _ptr(approx) if approx is not None else None), "pq_attn")
+    return out, idx, approx
 
 
 def spec_accept(target, draft, draft_tok, u_acc, u_res, greedy: bool):

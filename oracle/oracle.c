@@ -25,6 +25,9 @@
  *     (section 4.4) and the
  *     append / rollback of the compact cache as tokens are accepted or
  *     rejected (sections 3.1, 4.4);
+ *   - PQCache-style dynamic selection: product-quantised keys (encode and
+ *     Lloyd update of the codebooks), approximate scores from per-query
+ *     lookup tables, exact attention over the top_k (section 4.4, Figure 5);
  *   - Top-K attention drafting: each draft query attends to its own top_k
  *     highest-scoring positions of the full cache (section 1, Figure 1(c);
  *     section 4.4);
@@ -526,6 +529,166 @@ int oracle_topk_attn(int B, int H_q, int H_kv, int d, int L_cap,
         }
         for (c = 0; c < d; ++c) o[c] /= den;
         free(rk);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* PQCache-style dynamic selection (section 4.4, Figure 5: dynamic KV          */
+/* selection by product quantisation of the keys).  Keys of each (sequence,   */
+/* KV head) split into M sub-vectors of d/M channels; subspace m has C         */
+/* centroids.  codebook [B, H_kv, M, C, d/M] fp32, codes [B, L_cap, H_kv, M]   */
+/* uint8.                                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Encode: code[j][m] = the centroid c minimising sum_i (k_j[m*ds+i] - c_i)^2
+ * (fp64 from the bf16 key and fp32 centroid; equal distances: the smaller c),
+ * for every position j < L_cap.  gap (optional, [B, L_cap, H_kv, M]) receives
+ * second-best minus best distance for margin analysis.
+ */
+int oracle_pq_encode(int B, int H_kv, int d, int L_cap, const uint16_t *k, int M, int C,
+                     const float *codebook, uint8_t *codes, double *gap)
+{
+    if (B < 0 || H_kv <= 0 || d <= 0 || M <= 0 || d % M || C <= 0 || C > 256 || L_cap < 0) return -1;
+    const int ds = d / M;
+    long unit;
+#pragma omp parallel for schedule(static)
+    for (unit = 0; unit < (long)B * L_cap * H_kv; ++unit) {
+        const int h = (int)(unit % H_kv);
+        const long bj = unit / H_kv;
+        const int b = (int)(bj / L_cap);
+        const uint16_t *kr = k + unit * d;
+        int m, c, i;
+        for (m = 0; m < M; ++m) {
+            const float *cb = codebook + (((size_t)b * H_kv + h) * M + m) * (size_t)C * ds;
+            double best = INFINITY, second = INFINITY;
+            int arg = 0;
+            for (c = 0; c < C; ++c) {
+                double dist = 0.0;
+                for (i = 0; i < ds; ++i) {
+                    const double t = bf16_value(kr[m * ds + i]) - (double)cb[(size_t)c * ds + i];
+                    dist += t * t;
+                }
+                if (dist < best) { second = best; best = dist; arg = c; }
+                else if (dist < second) second = dist;
+            }
+            codes[unit * M + m] = (uint8_t)arg;
+            if (gap) gap[unit * M + m] = second - best;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Update (one Lloyd step after an encode): centroid c of subspace m becomes
+ * the fp64 mean of the sub-vectors of the positions j < seq_len[b] coded c,
+ * rounded to fp32; a centroid with no position keeps its value.
+ */
+int oracle_pq_update(int B, int H_kv, int d, int L_cap, const uint16_t *k, const int32_t *seq_len, int M, int C,
+                     const uint8_t *codes, float *codebook)
+{
+    if (B < 0 || H_kv <= 0 || d <= 0 || M <= 0 || d % M || C <= 0 || C > 256 || L_cap < 0) return -1;
+    const int ds = d / M;
+    long unit;
+#pragma omp parallel for schedule(static)
+    for (unit = 0; unit < (long)B * H_kv * M; ++unit) {
+        const int m = (int)(unit % M);
+        const int h = (int)((unit / M) % H_kv);
+        const int b = (int)(unit / ((long)M * H_kv));
+        const int len = clamp_len(seq_len[b], L_cap);
+        double *sum = (double *)calloc((size_t)C * ds, sizeof(double));
+        long *cnt = (long *)calloc((size_t)C, sizeof(long));
+        int j, i, c;
+        for (j = 0; j < len; ++j) {
+            const size_t row = ((size_t)b * L_cap + j) * H_kv + h;
+            c = codes[row * M + m];
+            if (c >= C) continue;
+            cnt[c]++;
+            for (i = 0; i < ds; ++i) sum[(size_t)c * ds + i] += bf16_value(k[row * d + m * ds + i]);
+        }
+        float *cb = codebook + (size_t)unit * C * ds;
+        for (c = 0; c < C; ++c)
+            if (cnt[c] > 0)
+                for (i = 0; i < ds; ++i) cb[(size_t)c * ds + i] = (float)(sum[(size_t)c * ds + i] / (double)cnt[c]);
+        free(sum);
+        free(cnt);
+    }
+    return 0;
+}
+
+/*
+ * PQ draft attention.  For query head hq (KV head hk = hq / G) of sequence b:
+ * LUT[m][c] = scale * sum_i q[m*ds+i] * codebook[b,hk,m,c,i]; approximate
+ * score a_j = sum_m LUT[m][codes[b,j,hk,m]] for j < len; the top_k positions
+ * by a_j are kept (equal: the smaller position; all when len <= top_k); the
+ * output is softmax attention with the EXACT scores scale * q . k_j over the
+ * kept positions.  idx [B, H_q, top_k] ascending, -1 padded; approx
+ * (optional, [B, H_q, L_cap]) receives a_j (0 past len).
+ */
+int oracle_pq_attn(int B, int H_q, int H_kv, int d, int L_cap, const uint16_t *q, const uint16_t *k,
+                   const uint16_t *v, const int32_t *seq_len, int M, int C, const float *codebook,
+                   const uint8_t *codes, int top_k, double *out, int32_t *idx, double *approx)
+{
+    if (B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv || d <= 0 || M <= 0 || d % M || C <= 0 || C > 256 ||
+        top_k <= 0 || L_cap < 0)
+        return -1;
+    const int G = H_q / H_kv, ds = d / M;
+    const double scale = 1.0 / sqrt((double)d);
+    long unit;
+#pragma omp parallel for schedule(dynamic)
+    for (unit = 0; unit < (long)B * H_q; ++unit) {
+        const int b = (int)(unit / H_q), hq = (int)(unit % H_q), hk = hq / G;
+        const int len = clamp_len(seq_len[b], L_cap);
+        const uint16_t *qr = q + ((long)b * H_q + hq) * d;
+        double *o = out + unit * d;
+        int32_t *sel = idx + unit * top_k;
+        double *arow = approx ? approx + unit * L_cap : NULL;
+        int c, i, j, m, n;
+        for (i = 0; i < d; ++i) o[i] = 0.0;
+        for (j = 0; j < top_k; ++j) sel[j] = -1;
+        if (arow) for (j = 0; j < L_cap; ++j) arow[j] = 0.0;
+        if (len == 0) continue;
+        double *lut = (double *)malloc(sizeof(double) * (size_t)M * C);
+        for (m = 0; m < M; ++m)
+            for (c = 0; c < C; ++c) {
+                const float *cv = codebook + ((((size_t)b * H_kv + hk) * M + m) * C + c) * ds;
+                double acc = 0.0;
+                for (i = 0; i < ds; ++i) acc += bf16_value(qr[m * ds + i]) * (double)cv[i];
+                lut[(size_t)m * C + c] = scale * acc;
+            }
+        ranked_t *rk = (ranked_t *)malloc(sizeof(ranked_t) * (size_t)len);
+        for (j = 0; j < len; ++j) {
+            const uint8_t *cr = codes + (((size_t)b * L_cap + j) * H_kv + hk) * M;
+            double a = 0.0;
+            for (m = 0; m < M; ++m) a += lut[(size_t)m * C + (cr[m] < C ? cr[m] : 0)];
+            rk[j].key = a;
+            rk[j].pos = j;
+            if (arow) arow[j] = a;
+        }
+        n = len <= top_k ? len : top_k;
+        if (len > top_k) qsort(rk, (size_t)len, sizeof(ranked_t), by_score_desc);
+        for (j = 0; j < n; ++j) sel[j] = rk[j].pos;
+        qsort(sel, (size_t)n, sizeof(int32_t), by_int_asc);
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
+        double smax = -INFINITY, den = 0.0;
+        for (j = 0; j < n; ++j) {
+            const uint16_t *kr = k + (((size_t)b * L_cap + sel[j]) * H_kv + hk) * d;
+            double acc = 0.0;
+            for (i = 0; i < d; ++i) acc += bf16_value(qr[i]) * bf16_value(kr[i]);
+            s[j] = scale * acc;
+            if (s[j] > smax) smax = s[j];
+        }
+        for (j = 0; j < n; ++j) {
+            const double w = exp(s[j] - smax);
+            const uint16_t *vr = v + (((size_t)b * L_cap + sel[j]) * H_kv + hk) * d;
+            den += w;
+            for (i = 0; i < d; ++i) o[i] += w * bf16_value(vr[i]);
+        }
+        for (i = 0; i < d; ++i) o[i] /= den;
+        free(s);
+        free(rk);
+        free(lut);
     }
     return 0;
 }

@@ -206,6 +206,125 @@ def test_topk_attn_ties_and_single_winner():
 
 
 # --------------------------------------------------------------------------
+# PQCache-style selection
+# --------------------------------------------------------------------------
+def test_pq_encode_matches_numpy_argmin():
+    rng = np.random.default_rng(41)
+    B, L, H_kv, d, M, C = 2, 50, 2, 32, 4, 10
+    ds = d // M
+    k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    cb = rng.standard_normal((B, H_kv, M, C, ds)).astype(np.float32)
+    cb[:, :, :, 7] = cb[:, :, :, 3]                      # duplicate: the smaller index must win
+    codes, gap = oracle.pq_encode(k, cb, want_gap=True)
+    kf = bits_to_f64(k).reshape(B, L, H_kv, M, ds)
+    dist = ((kf[:, :, :, :, None, :] - cb.astype(np.float64).transpose(0, 1, 2, 3, 4)[:, None]
+             .reshape(B, 1, H_kv, M, C, ds)) ** 2).sum(-1)
+    np.testing.assert_array_equal(codes, np.argmin(dist, axis=-1))
+    assert not np.any(codes == 7)
+    srt = np.sort(dist, axis=-1)
+    np.testing.assert_allclose(gap, srt[..., 1] - srt[..., 0], rtol=1e-12, atol=1e-12)
+
+
+def test_pq_update_matches_groupby_mean():
+    rng = np.random.default_rng(42)
+    B, L, H_kv, d, M, C = 2, 60, 2, 16, 2, 6
+    ds = d // M
+    k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    codes = rng.integers(0, C - 1, size=(B, L, H_kv, M)).astype(np.uint8)   # centroid C-1 stays empty
+    sl = np.array([L, 37], np.int32)
+    cb0 = rng.standard_normal((B, H_kv, M, C, ds)).astype(np.float32)
+    cb = oracle.pq_update(k, sl, codes, cb0)
+    kf = bits_to_f64(k).reshape(B, L, H_kv, M, ds)
+    for b in range(B):
+        for h in range(H_kv):
+            for m in range(M):
+                for c in range(C):
+                    sel = codes[b, : sl[b], h, m] == c
+                    if sel.any():
+                        want = kf[b, : sl[b]][sel, h, m].mean(0).astype(np.float32)
+                        np.testing.assert_array_equal(cb[b, h, m, c], want)
+                    else:
+                        np.testing.assert_array_equal(cb[b, h, m, c], cb0[b, h, m, c])
+
+
+def test_pq_attn_with_the_keys_as_codebook_is_topk_attention():
+    """One centroid per position equal to that key: approximate scores are exact, so PQ attention
+    reduces to Top-K attention (itself pinned to masked SDPA)."""
+    rng = np.random.default_rng(43)
+    B, H_q, H_kv, d, L, M, top_k = 2, 8, 2, 32, 40, 4, 9
+    ds = d // M
+    q = bf16_bits(rng.standard_normal((B, 1, H_q, d)))
+    k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    v = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    cb = bits_to_f64(k).reshape(B, L, H_kv, M, ds).transpose(0, 2, 3, 1, 4).astype(np.float32)   # C = L
+    codes = np.broadcast_to(np.arange(L, dtype=np.uint8)[None, :, None, None], (B, L, H_kv, M)).copy()
+    sl = np.array([L, 23], np.int32)
+    out, idx, _ = oracle.pq_attn(q, k, v, sl, cb, codes, top_k)
+    ref, ref_idx, _ = oracle.topk_attn(q, k, v, sl, top_k)
+    np.testing.assert_array_equal(idx, ref_idx)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_pq_attn_matches_masked_sdpa():
+    rng = np.random.default_rng(44)
+    B, H_q, H_kv, d, L, M, C, top_k = 3, 8, 2, 32, 70, 4, 16, 11
+    ds = d // M
+    G = H_q // H_kv
+    q = bf16_bits(rng.standard_normal((B, 1, H_q, d)))
+    k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    v = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
+    cb = rng.standard_normal((B, H_kv, M, C, ds)).astype(np.float32)
+    codes = rng.integers(0, C, size=(B, L, H_kv, M)).astype(np.uint8)
+    sl = np.array([L, 5, 40], np.int32)
+    out, idx, approx = oracle.pq_attn(q, k, v, sl, cb, codes, top_k, want_approx=True)
+    qf = bits_to_f64(q)[:, 0].reshape(B, H_q, M, ds)
+    cbf = np.repeat(cb.astype(np.float64), G, axis=1)                          # [B,H_q,M,C,ds]
+    lut = np.einsum("bhmi,bhmci->bhmc", qf, cbf) / math.sqrt(d)
+    codes_q = np.repeat(codes.transpose(0, 2, 1, 3), G, axis=1)                # [B,H_q,L,M]
+    a = np.take_along_axis(lut[:, :, None, :, :], codes_q[..., None].astype(np.int64), axis=-1)[..., 0].sum(-1)
+    kf = np.repeat(bits_to_f64(k).transpose(0, 2, 1, 3), G, axis=1)
+    vf = np.repeat(bits_to_f64(v).transpose(0, 2, 1, 3), G, axis=1)
+    mask = np.zeros((B, H_q, 1, L), bool)
+    want_idx = np.full((B, H_q, top_k), -1, np.int32)
+    for b in range(B):
+        n = int(sl[b])
+        for h in range(H_q):
+            keep = np.sort(np.lexsort((np.arange(n), -a[b, h, :n]))[:top_k])
+            mask[b, h, 0, keep] = True
+            want_idx[b, h, : keep.size] = keep
+            np.testing.assert_allclose(approx[b, h, :n], a[b, h, :n], rtol=1e-12, atol=1e-12)
+    ref = sdpa_reference(bits_to_f64(q).transpose(0, 2, 1, 3), kf, vf, mask).transpose(0, 2, 1, 3)
+    np.testing.assert_array_equal(idx, want_idx)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_pq_lloyd_steps_recover_planted_clusters():
+    """Sub-vectors drawn around 6 well-separated prototypes per subspace: from one member of each
+    cluster as the initial centroids, encode + update twice labels every key by its prototype and the
+    centroids settle on the cluster means."""
+    rng = np.random.default_rng(45)
+    B, L, H_kv, d, M, C = 1, 300, 2, 16, 2, 6
+    ds = d // M
+    proto = rng.standard_normal((B, H_kv, M, C, ds)) * 4.0
+    label = rng.integers(0, C, size=(B, L, H_kv, M))
+    label[:, :C] = np.arange(C)[None, :, None, None]                        # positions 0..C-1 seed the clusters
+    sub = np.take_along_axis(proto[:, None], label.reshape(B, L, H_kv, M, 1, 1).repeat(ds, -1), axis=4)[..., 0, :]
+    k = bf16_bits((sub + 0.05 * rng.standard_normal(sub.shape)).reshape(B, L, H_kv, d))
+    kf = bits_to_f64(k).reshape(B, L, H_kv, M, ds)
+    cb = kf[:, :C].transpose(0, 2, 3, 1, 4).astype(np.float32).copy()     # [B,H_kv,M,C,ds]
+    sl = np.array([L], np.int32)
+    for _ in range(2):
+        codes, _ = oracle.pq_encode(k, cb)
+        cb = oracle.pq_update(k, sl, codes, cb)
+    np.testing.assert_array_equal(codes, label)
+    for h in range(H_kv):
+        for m in range(M):
+            for c in range(C):
+                np.testing.assert_allclose(cb[0, h, m, c], kf[0][label[0, :, h, m] == c, h, m].mean(0),
+                                           rtol=1e-6, atol=1e-6)
+
+
+# --------------------------------------------------------------------------
 # Draft-cache update (append / rollback)
 # --------------------------------------------------------------------------
 def _encoded_cache(B, L, H_kv, d, version):
