@@ -220,20 +220,20 @@ def draft_cache_update(k, v, kc, vc, len_valid, len_old, len_new, origin, base, 
 
 
 def pq_encode(k, codebook, want_gap: bool = False):
-    """k [B,L_cap,H_kv,d] u16, codebook [B,H_kv,M,C,d/M] fp32 -> (codes u8 [B,L_cap,H_kv,M], gap fp64 or None)."""
+    """k [B,L_cap,H_kv,d] u16, codebook [B,H_kv,M,C,d/M] fp32 -> (codes u8 [B,H_kv,L_cap,M], gap fp64 or None)."""
     k = _c(k, np.uint16)
     cb = _c(codebook, np.float32)
     B, L_cap, H_kv, d = k.shape
     M, C = cb.shape[2], cb.shape[3]
-    codes = np.empty((B, L_cap, H_kv, M), np.uint8)
-    gap = np.empty((B, L_cap, H_kv, M), np.float64) if want_gap else None
+    codes = np.empty((B, H_kv, L_cap, M), np.uint8)
+    gap = np.empty((B, H_kv, L_cap, M), np.float64) if want_gap else None
     _check(_load().oracle_pq_encode(B, H_kv, d, L_cap, _ptr(k), M, C, _ptr(cb), _ptr(codes),
                                     _ptr(gap) if gap is not None else None), "pq_encode")
     return codes, gap
 
 
 def pq_update(k, seq_len, codes, codebook):
-    """One Lloyd update: returns a new codebook (fp32) from codes u8 [B,L_cap,H_kv,M]."""
+    """One Lloyd update: returns a new codebook (fp32) from codes u8 [B,H_kv,L_cap,M]."""
     k, seq_len, codes = _c(k, np.uint16), _c(seq_len, np.int32), _c(codes, np.uint8)
     cb = np.array(codebook, dtype=np.float32, copy=True, order="C")
     B, L_cap, H_kv, d = k.shape

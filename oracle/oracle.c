@@ -537,14 +537,14 @@ int oracle_topk_attn(int B, int H_q, int H_kv, int d, int L_cap,
 /* PQCache-style dynamic selection (section 4.4, Figure 5: dynamic KV          */
 /* selection by product quantisation of the keys).  Keys of each (sequence,   */
 /* KV head) split into M sub-vectors of d/M channels; subspace m has C         */
-/* centroids.  codebook [B, H_kv, M, C, d/M] fp32, codes [B, L_cap, H_kv, M]   */
-/* uint8.                                                                      */
+/* centroids.  codebook [B, H_kv, M, C, d/M] fp32, codes [B, H_kv, L_cap, M]   */
+/* uint8 (head-major: one (sequence, head)'s codes are contiguous).            */
 /* ------------------------------------------------------------------------ */
 
 /*
  * Encode: code[j][m] = the centroid c minimising sum_i (k_j[m*ds+i] - c_i)^2
  * (fp64 from the bf16 key and fp32 centroid; equal distances: the smaller c),
- * for every position j < L_cap.  gap (optional, [B, L_cap, H_kv, M]) receives
+ * for every position j < L_cap.  gap (optional, [B, H_kv, L_cap, M]) receives
  * second-best minus best distance for margin analysis.
  */
 int oracle_pq_encode(int B, int H_kv, int d, int L_cap, const uint16_t *k, int M, int C,
@@ -557,8 +557,9 @@ int oracle_pq_encode(int B, int H_kv, int d, int L_cap, const uint16_t *k, int M
     for (unit = 0; unit < (long)B * L_cap * H_kv; ++unit) {
         const int h = (int)(unit % H_kv);
         const long bj = unit / H_kv;
-        const int b = (int)(bj / L_cap);
+        const int b = (int)(bj / L_cap), j = (int)(bj % L_cap);
         const uint16_t *kr = k + unit * d;
+        const size_t out_row = ((size_t)b * H_kv + h) * L_cap + j;
         int m, c, i;
         for (m = 0; m < M; ++m) {
             const float *cb = codebook + (((size_t)b * H_kv + h) * M + m) * (size_t)C * ds;
@@ -573,8 +574,8 @@ int oracle_pq_encode(int B, int H_kv, int d, int L_cap, const uint16_t *k, int M
                 if (dist < best) { second = best; best = dist; arg = c; }
                 else if (dist < second) second = dist;
             }
-            codes[unit * M + m] = (uint8_t)arg;
-            if (gap) gap[unit * M + m] = second - best;
+            codes[out_row * M + m] = (uint8_t)arg;
+            if (gap) gap[out_row * M + m] = second - best;
         }
     }
     return 0;
@@ -602,7 +603,7 @@ int oracle_pq_update(int B, int H_kv, int d, int L_cap, const uint16_t *k, const
         int j, i, c;
         for (j = 0; j < len; ++j) {
             const size_t row = ((size_t)b * L_cap + j) * H_kv + h;
-            c = codes[row * M + m];
+            c = codes[(((size_t)b * H_kv + h) * L_cap + j) * M + m];
             if (c >= C) continue;
             cnt[c]++;
             for (i = 0; i < ds; ++i) sum[(size_t)c * ds + i] += bf16_value(k[row * d + m * ds + i]);
@@ -659,7 +660,7 @@ int oracle_pq_attn(int B, int H_q, int H_kv, int d, int L_cap, const uint16_t *q
             }
         ranked_t *rk = (ranked_t *)malloc(sizeof(ranked_t) * (size_t)len);
         for (j = 0; j < len; ++j) {
-            const uint8_t *cr = codes + (((size_t)b * L_cap + j) * H_kv + hk) * M;
+            const uint8_t *cr = codes + (((size_t)b * H_kv + hk) * L_cap + j) * M;
             double a = 0.0;
             for (m = 0; m < M; ++m) a += lut[(size_t)m * C + (cr[m] < C ? cr[m] : 0)];
             rk[j].key = a;

@@ -219,10 +219,10 @@ def test_pq_encode_matches_numpy_argmin():
     kf = bits_to_f64(k).reshape(B, L, H_kv, M, ds)
     dist = ((kf[:, :, :, :, None, :] - cb.astype(np.float64).transpose(0, 1, 2, 3, 4)[:, None]
              .reshape(B, 1, H_kv, M, C, ds)) ** 2).sum(-1)
-    np.testing.assert_array_equal(codes, np.argmin(dist, axis=-1))
+    np.testing.assert_array_equal(codes, np.argmin(dist, axis=-1).transpose(0, 2, 1, 3))   # head-major
     assert not np.any(codes == 7)
     srt = np.sort(dist, axis=-1)
-    np.testing.assert_allclose(gap, srt[..., 1] - srt[..., 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gap, (srt[..., 1] - srt[..., 0]).transpose(0, 2, 1, 3), rtol=1e-12, atol=1e-12)
 
 
 def test_pq_update_matches_groupby_mean():
@@ -230,7 +230,7 @@ def test_pq_update_matches_groupby_mean():
     B, L, H_kv, d, M, C = 2, 60, 2, 16, 2, 6
     ds = d // M
     k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
-    codes = rng.integers(0, C - 1, size=(B, L, H_kv, M)).astype(np.uint8)   # centroid C-1 stays empty
+    codes = rng.integers(0, C - 1, size=(B, H_kv, L, M)).astype(np.uint8)   # centroid C-1 stays empty
     sl = np.array([L, 37], np.int32)
     cb0 = rng.standard_normal((B, H_kv, M, C, ds)).astype(np.float32)
     cb = oracle.pq_update(k, sl, codes, cb0)
@@ -239,7 +239,7 @@ def test_pq_update_matches_groupby_mean():
         for h in range(H_kv):
             for m in range(M):
                 for c in range(C):
-                    sel = codes[b, : sl[b], h, m] == c
+                    sel = codes[b, h, : sl[b], m] == c
                     if sel.any():
                         want = kf[b, : sl[b]][sel, h, m].mean(0).astype(np.float32)
                         np.testing.assert_array_equal(cb[b, h, m, c], want)
@@ -257,7 +257,7 @@ def test_pq_attn_with_the_keys_as_codebook_is_topk_attention():
     k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
     v = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
     cb = bits_to_f64(k).reshape(B, L, H_kv, M, ds).transpose(0, 2, 3, 1, 4).astype(np.float32)   # C = L
-    codes = np.broadcast_to(np.arange(L, dtype=np.uint8)[None, :, None, None], (B, L, H_kv, M)).copy()
+    codes = np.broadcast_to(np.arange(L, dtype=np.uint8)[None, None, :, None], (B, H_kv, L, M)).copy()
     sl = np.array([L, 23], np.int32)
     out, idx, _ = oracle.pq_attn(q, k, v, sl, cb, codes, top_k)
     ref, ref_idx, _ = oracle.topk_attn(q, k, v, sl, top_k)
@@ -274,13 +274,13 @@ def test_pq_attn_matches_masked_sdpa():
     k = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
     v = bf16_bits(rng.standard_normal((B, L, H_kv, d)))
     cb = rng.standard_normal((B, H_kv, M, C, ds)).astype(np.float32)
-    codes = rng.integers(0, C, size=(B, L, H_kv, M)).astype(np.uint8)
+    codes = rng.integers(0, C, size=(B, H_kv, L, M)).astype(np.uint8)
     sl = np.array([L, 5, 40], np.int32)
     out, idx, approx = oracle.pq_attn(q, k, v, sl, cb, codes, top_k, want_approx=True)
     qf = bits_to_f64(q)[:, 0].reshape(B, H_q, M, ds)
     cbf = np.repeat(cb.astype(np.float64), G, axis=1)                          # [B,H_q,M,C,ds]
     lut = np.einsum("bhmi,bhmci->bhmc", qf, cbf) / math.sqrt(d)
-    codes_q = np.repeat(codes.transpose(0, 2, 1, 3), G, axis=1)                # [B,H_q,L,M]
+    codes_q = np.repeat(codes, G, axis=1)                                      # [B,H_q,L,M]
     a = np.take_along_axis(lut[:, :, None, :, :], codes_q[..., None].astype(np.int64), axis=-1)[..., 0].sum(-1)
     kf = np.repeat(bits_to_f64(k).transpose(0, 2, 1, 3), G, axis=1)
     vf = np.repeat(bits_to_f64(v).transpose(0, 2, 1, 3), G, axis=1)
@@ -316,7 +316,7 @@ def test_pq_lloyd_steps_recover_planted_clusters():
     for _ in range(2):
         codes, _ = oracle.pq_encode(k, cb)
         cb = oracle.pq_update(k, sl, codes, cb)
-    np.testing.assert_array_equal(codes, label)
+    np.testing.assert_array_equal(codes, label.transpose(0, 2, 1, 3))
     for h in range(H_kv):
         for m in range(M):
             for c in range(C):
