@@ -233,6 +233,60 @@ MAGICDEC_API magicdec_status magicdec_topk_draft_attn(magicdec_kv_shape shape, c
                                                       void *stream);
 
 /*
+ * PQCache-style dynamic selection (paper section 4.4 and Figure 5: a dynamic
+ * KV selection that searches the cache per query through product-quantised
+ * keys, with a search cost that grows with the batch).  Keys of each
+ * (sequence, KV head) split into M = d/8 sub-vectors of 8 channels; subspace
+ * m has C (1..256) centroids.
+ *   codebook [B, H_kv, M, C, 8] fp32;  codes [B, H_kv, L_cap, M] uint8
+ * A codebook is built at prefill by Lloyd iterations: encode, then update,
+ * repeated, from initial centroids chosen by the caller.
+ *
+ * Encode: codes[b,h,j,m] = the centroid c of subspace m nearest to the key's
+ * sub-vector (squared distance, evaluated as |c|^2 - 2 k.c in fp32; equal
+ * values: the smaller c), for every position j < L_cap.
+ * Errors: NULL pointers, bad shape, M != d/8, C outside [1, 256], alignment
+ * (k, codebook); MAGICDEC_ERR_UNSUPPORTED when the codebook of one
+ * (sequence, head) does not fit in shared memory.
+ */
+MAGICDEC_API magicdec_status magicdec_pq_encode(magicdec_kv_shape shape, const uint16_t *k, int M, int C,
+                                                const float *codebook, uint8_t *codes, void *stream);
+
+/*
+ * Update (one Lloyd step after an encode): centroid c of subspace m becomes
+ * the mean of the sub-vectors of positions j < seq_len[b] coded c (exact sum,
+ * correctly rounded mean, rounded to fp32); a centroid without positions
+ * keeps its value.  codebook is updated in place.
+ * Errors as magicdec_pq_encode.
+ */
+MAGICDEC_API magicdec_status magicdec_pq_update(magicdec_kv_shape shape, const uint16_t *k, const int32_t *seq_len,
+                                                int M, int C, const uint8_t *codes, float *codebook, void *stream);
+
+/* Workspace bytes magicdec_pq_draft_attn needs: fp32 approximate scores,
+ * B * H_q * (L_cap rounded up to 4) * 4. */
+MAGICDEC_API size_t magicdec_pq_attn_workspace_size(magicdec_kv_shape shape);
+
+/*
+ * PQ draft attention.  For query head h of sequence b (KV head h/(H_q/H_kv)),
+ * with len = seq_len[b] clamped to [0, L_cap]: LUT[m][c] = q_m . centroid(m,c)
+ * / sqrt(d); approximate score a_j = sum_m LUT[m][codes[b,h,j,m]] for j < len;
+ * the top_k positions by a_j are kept (equal: the smaller position; all when
+ * len <= top_k) and
+ *   out = sum_{j kept} softmax(q . k_j / sqrt(d) over the kept j) v_j
+ * with the EXACT scores (a zero row when len == 0).
+ *   q [B, 1, H_q, d] bf16;  k, v [B, L_cap, H_kv, d] bf16;  out [B, 1, H_q, d] bf16
+ *   idx (nullable) [B, H_q, top_k] int32 out: kept positions, ascending, -1 padded
+ *   ws  workspace of magicdec_pq_attn_workspace_size(shape) bytes
+ * Supported: top_k <= 8192.  Errors: as magicdec_pq_encode, plus top_k <= 0,
+ * alignment of q, v, out, ws, workspace too small.
+ */
+MAGICDEC_API magicdec_status magicdec_pq_draft_attn(magicdec_kv_shape shape, const uint16_t *q, const uint16_t *k,
+                                                    const uint16_t *v, const int32_t *seq_len, int M, int C,
+                                                    const float *codebook, const uint8_t *codes, int top_k,
+                                                    uint16_t *out, int32_t *idx, void *ws, size_t ws_bytes,
+                                                    void *stream);
+
+/*
  * Verification attention that allocates nothing (no counterpart in the paper;
  * an addition for callers that cannot allocate device memory, such as a
  * plug-in that receives only its input and output buffers from a host

@@ -49,6 +49,10 @@ _SIGNATURES = {
     "magicdec_verify_attn": ([KVShape, _I, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "magicdec_verify_attn_noalloc": ([KVShape, _I, _P, _P, _P, _P, _P, _P], _I),
     "magicdec_draft_cache_update": ([KVShape, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P], _I),
+    "magicdec_pq_encode": ([KVShape, _P, _I, _I, _P, _P, _P], _I),
+    "magicdec_pq_update": ([KVShape, _P, _P, _I, _I, _P, _P, _P], _I),
+    "magicdec_pq_attn_workspace_size": ([KVShape], _S),
+    "magicdec_pq_draft_attn": ([KVShape, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _S, _P], _I),
     "magicdec_topk_attn_workspace_size": ([KVShape], _S),
     "magicdec_topk_draft_attn": ([KVShape, _P, _P, _P, _P, _I, _P, _P, _P, _S, _P], _I),
     "magicdec_spec_accept_workspace_size": ([_I, _I, _I], _S),
@@ -309,6 +313,79 @@ def magicdec_draft_cache_update(k: torch.Tensor, v: torch.Tensor, kc: torch.Tens
                                              _ptr(origin), _ptr(base), int(ring), int(cap), _ptr(kc), _ptr(vc),
                                              _ptr(draft_len), _stream(stream, dev)))
     return draft_len
+
+
+def _pq_dims(k: torch.Tensor, codebook: torch.Tensor):
+    B, L_cap, H_kv, d = k.shape
+    if codebook.dim() != 5 or codebook.shape[0] != B or codebook.shape[1] != H_kv or codebook.shape[4] != 8:
+        raise ValueError("codebook must be [B, H_kv, M, C, 8]")
+    return B, L_cap, H_kv, d, codebook.shape[2], codebook.shape[3]
+
+
+def magicdec_pq_encode(k: torch.Tensor, codebook: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """k [B, L_cap, H_kv, d] bf16, codebook [B, H_kv, M, C, 8] fp32 -> codes uint8 [B, H_kv, L_cap, M]."""
+    _need(k, "k", torch.bfloat16)
+    dev = k.device
+    _need(codebook, "codebook", torch.float32, dev)
+    B, L_cap, H_kv, d, M, C = _pq_dims(k, codebook)
+    if codes is None:
+        codes = torch.empty((B, H_kv, L_cap, M), dtype=torch.uint8, device=dev)
+    _need(codes, "codes", torch.uint8, dev)
+    _check("magicdec_pq_encode", lib().magicdec_pq_encode(kv_shape(B, H_kv, H_kv, d, L_cap), _ptr(k), M, C,
+                                                          _ptr(codebook), _ptr(codes), _stream(stream, dev)))
+    return codes
+
+
+def magicdec_pq_update(k: torch.Tensor, seq_len: torch.Tensor, codes: torch.Tensor, codebook: torch.Tensor,
+                       stream=None) -> torch.Tensor:
+    """One Lloyd update of codebook [B, H_kv, M, C, 8] fp32 in place from codes [B, H_kv, L_cap, M]."""
+    _need(k, "k", torch.bfloat16)
+    dev = k.device
+    _need(seq_len, "seq_len", torch.int32, dev)
+    _need(codes, "codes", torch.uint8, dev)
+    _need(codebook, "codebook", torch.float32, dev)
+    B, L_cap, H_kv, d, M, C = _pq_dims(k, codebook)
+    _check("magicdec_pq_update", lib().magicdec_pq_update(kv_shape(B, H_kv, H_kv, d, L_cap), _ptr(k), _ptr(seq_len),
+                                                          M, C, _ptr(codes), _ptr(codebook), _stream(stream, dev)))
+    return codebook
+
+
+def magicdec_pq_attn_workspace_size(shape: KVShape) -> int:
+    return int(lib().magicdec_pq_attn_workspace_size(shape))
+
+
+def magicdec_pq_draft_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_len: torch.Tensor,
+                           codebook: torch.Tensor, codes: torch.Tensor, top_k: int,
+                           out: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                           ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """PQ draft attention.  q [B, 1, H_q, d] -> out [B, 1, H_q, d] bf16; idx optional int32 [B, H_q, top_k]."""
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev)
+    _need(seq_len, "seq_len", torch.int32, dev)
+    _need(codebook, "codebook", torch.float32, dev)
+    _need(codes, "codes", torch.uint8, dev)
+    B, L_cap, H_kv, d, M, C = _pq_dims(k, codebook)
+    H_q = q.shape[2]
+    if q.shape[0] != B or q.shape[1] != 1 or q.shape[3] != d or v.shape != k.shape:
+        raise ValueError("q / k / v shapes disagree")
+    shape = kv_shape(B, H_q, H_kv, d, L_cap)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if idx is not None:
+        _need(idx, "idx", torch.int32, dev)
+        if tuple(idx.shape) != (B, H_q, int(top_k)):
+            raise ValueError("idx must be [B, H_q, top_k]")
+    if ws is None:
+        ws = workspace(magicdec_pq_attn_workspace_size(shape), dev, "pq")
+    _check("magicdec_pq_draft_attn",
+           lib().magicdec_pq_draft_attn(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(seq_len), M, C, _ptr(codebook),
+                                        _ptr(codes), int(top_k), _ptr(out), _ptr(idx), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream, dev)))
+    return out
 
 
 def magicdec_topk_attn_workspace_size(shape: KVShape) -> int:

@@ -14,6 +14,13 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
                                    void *ws, cudaStream_t st);
 size_t attn_workspace_bytes(int B, int H_kv, int D, int M);
 size_t topk_workspace_bytes(int B, int H_q, int L_cap);
+magicdec_status launch_pq_encode(int B, int H_kv, int D, int L_cap, int C, const void *k, const float *codebook,
+                                 uint8_t *codes, cudaStream_t st);
+magicdec_status launch_pq_update(int B, int H_kv, int D, int L_cap, int C, const void *k, const int32_t *len,
+                                 const uint8_t *codes, float *codebook, cudaStream_t st);
+magicdec_status launch_pq_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, int C, const void *q, const void *k,
+                                     const void *v, const int32_t *len, const float *codebook, const uint8_t *codes,
+                                     int top_k, void *out, int32_t *idx, void *ws, cudaStream_t st);
 magicdec_status launch_draft_cache_update(int B, int H_kv, int D, int L_cap, const void *k, const void *v,
                                           const int32_t *len_valid, const int32_t *len_old, const int32_t *len_new,
                                           const int32_t *origin, const int32_t *base, int ring, int cap, void *kc,
@@ -231,6 +238,51 @@ magicdec_status magicdec_draft_cache_update(magicdec_kv_shape shape, const uint1
     return magicdec::launch_draft_cache_update(shape.B, shape.H_kv, shape.d, shape.L_cap, k, v, len_valid, len_old,
                                                len_new, origin, base, ring, cap, kc, vc, draft_len,
                                                static_cast<cudaStream_t>(stream));
+}
+
+static magicdec_status pq_common(const magicdec_kv_shape &shape, const void *k, int M, int C, const void *codebook,
+                                 const void *codes) {
+    if (!k || !codebook || !codes) return MAGICDEC_ERR_NULL;
+    if (!shape_ok(shape) || M * 8 != shape.d || C < 1 || C > 256) return MAGICDEC_ERR_SHAPE;
+    if (!aligned16(k) || !aligned16(codebook) || !aligned16(codes)) return MAGICDEC_ERR_ALIGN;
+    return MAGICDEC_OK;
+}
+
+magicdec_status magicdec_pq_encode(magicdec_kv_shape shape, const uint16_t *k, int M, int C, const float *codebook,
+                                   uint8_t *codes, void *stream) {
+    magicdec_status s = pq_common(shape, k, M, C, codebook, codes);
+    if (s != MAGICDEC_OK) return s;
+    return magicdec::launch_pq_encode(shape.B, shape.H_kv, shape.d, shape.L_cap, C, k, codebook, codes,
+                                      static_cast<cudaStream_t>(stream));
+}
+
+magicdec_status magicdec_pq_update(magicdec_kv_shape shape, const uint16_t *k, const int32_t *seq_len, int M, int C,
+                                   const uint8_t *codes, float *codebook, void *stream) {
+    if (!seq_len) return MAGICDEC_ERR_NULL;
+    magicdec_status s = pq_common(shape, k, M, C, codebook, codes);
+    if (s != MAGICDEC_OK) return s;
+    return magicdec::launch_pq_update(shape.B, shape.H_kv, shape.d, shape.L_cap, C, k, seq_len, codes, codebook,
+                                      static_cast<cudaStream_t>(stream));
+}
+
+size_t magicdec_pq_attn_workspace_size(magicdec_kv_shape shape) {
+    if (!shape_ok(shape)) return 0;
+    return magicdec::topk_workspace_bytes(shape.B, shape.H_q, shape.L_cap);
+}
+
+magicdec_status magicdec_pq_draft_attn(magicdec_kv_shape shape, const uint16_t *q, const uint16_t *k,
+                                       const uint16_t *v, const int32_t *seq_len, int M, int C, const float *codebook,
+                                       const uint8_t *codes, int top_k, uint16_t *out, int32_t *idx, void *ws,
+                                       size_t ws_bytes, void *stream) {
+    if (!q || !v || !seq_len || !out || !ws) return MAGICDEC_ERR_NULL;
+    magicdec_status s = pq_common(shape, k, M, C, codebook, codes);
+    if (s != MAGICDEC_OK) return s;
+    if (top_k <= 0) return MAGICDEC_ERR_SHAPE;
+    if (top_k > 8192) return MAGICDEC_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(v) || !aligned16(out) || !aligned16(ws)) return MAGICDEC_ERR_ALIGN;
+    if (ws_bytes < magicdec_pq_attn_workspace_size(shape)) return MAGICDEC_ERR_WORKSPACE;
+    return magicdec::launch_pq_draft_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, C, q, k, v, seq_len,
+                                          codebook, codes, top_k, out, idx, ws, static_cast<cudaStream_t>(stream));
 }
 
 size_t magicdec_topk_attn_workspace_size(magicdec_kv_shape shape) {

@@ -1,0 +1,388 @@
+// PQCache-style dynamic KV selection.
+//
+// MagicDec (arXiv 2408.11049) section 4.4 with Figure 5: a dynamic selection
+// that searches the KV cache per query through product-quantised keys; its
+// search cost grows with the batch.  Keys of each (sequence, KV head) are
+// split into M = d/8 sub-vectors of 8 channels; subspace m has C <= 256 fp32
+// centroids (codebook [B, H_kv, M, C, 8]); a key's code is the index of the
+// nearest centroid per subspace (codes [B, H_kv, L_cap, M] uint8).
+//   pq_encode_kernel  nearest centroid (argmin of |c|^2 - 2 k.c in fp32;
+//                     ties to the smaller index), the codebook of one
+//                     (sequence, head) in shared memory, two keys per thread.
+//   pq_update_kernel  one Lloyd update: centroid = mean of its keys.  The keys
+//                     are bf16, so the sums are exact and order-independent
+//                     as 2^-32 fixed point in shared-memory int64 atomics
+//                     (every bf16 value of magnitude >= 2^-25 is a whole
+//                     number of units; sums stay below 2^63 for |k| < 2^14
+//                     over up to 2^17 positions); the
+//                     mean is a correctly rounded fp64 division, rounded to
+//                     fp32.  A centroid without keys keeps its value.
+//   pq_scores_kernel  per draft step: persistent over 256-position tiles of
+//                     (sequence, KV head); each (sequence, head) builds the
+//                     lookup table LUT[m][c][g] = scale * q_g,m . c_m,c for
+//                     its G query heads once, then a position's approximate
+//                     score for head g is sum_m LUT[m][code_m][g].
+// Selection and exact attention over the kept positions run in the Top-K
+// select kernel (topk.cu) in its exact-score mode.
+#include "common.cuh"
+
+namespace magicdec {
+
+constexpr int kPqDs = 8;              // channels per subspace
+constexpr int kPqEncThreads = 256;
+constexpr int kPqEncChunk = 2048;     // positions per encode CTA
+constexpr int kPqUpdThreads = 512;
+constexpr int kPqScThreads = 256;     // = positions per score tile
+
+struct PqScoreParams {
+    const __nv_bfloat16 *q;    // [B, 1, H_q, D]
+    const float *codebook;     // [B, H_kv, M, C, 8]
+    const uint8_t *codes;      // [B, H_kv, L_cap, M]
+    const int32_t *len;
+    float *score;              // [B, H_q, L_sc]
+    int B, H_q, H_kv, G, L_cap, L_sc, C;
+    float scale;
+};
+
+__device__ __forceinline__ int pq_clamp(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4 u, float (&x)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+// ------------------------------------------------------------------ encode
+template <int D>
+__global__ void __launch_bounds__(kPqEncThreads) pq_encode_kernel(const __nv_bfloat16 *__restrict__ k,
+                                                                 const float *__restrict__ codebook,
+                                                                 uint8_t *__restrict__ codes, int H_kv, int L_cap,
+                                                                 int C) {
+    constexpr int M = D / kPqDs;
+    extern __shared__ __align__(16) float pq_smem[];
+    float *cb = pq_smem;                         // [M][C][8]
+    float *nrm = cb + (size_t)M * C * kPqDs;     // [M][C]
+    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    const float4 *src = reinterpret_cast<const float4 *>(codebook + ((size_t)b * H_kv + h) * M * C * kPqDs);
+    for (int i = tid; i < M * C * kPqDs / 4; i += kPqEncThreads) reinterpret_cast<float4 *>(cb)[i] = __ldg(src + i);
+    __syncthreads();
+    for (int i = tid; i < M * C; i += kPqEncThreads) {
+        const float *c = cb + (size_t)i * kPqDs;
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < kPqDs; ++e) s = fmaf(c[e], c[e], s);
+        nrm[i] = s;
+    }
+    __syncthreads();
+    const int j0 = chunk * kPqEncChunk, j1 = min(L_cap, j0 + kPqEncChunk);
+    // positions j and j + kPqEncThreads together: each centroid read feeds two keys
+    for (int base = j0; base < j1; base += 2 * kPqEncThreads) {
+        const int ja = base + tid, jb = ja + kPqEncThreads;
+        const bool va = ja < j1, vb = jb < j1;
+        const uint4 *ka = reinterpret_cast<const uint4 *>(k + (((size_t)b * L_cap + (va ? ja : j0)) * H_kv + h) * D);
+        const uint4 *kb = reinterpret_cast<const uint4 *>(k + (((size_t)b * L_cap + (vb ? jb : j0)) * H_kv + h) * D);
+        uint8_t ca[M], cbb[M];
+#pragma unroll 1
+        for (int m = 0; m < M; ++m) {
+            float xa[8], xb[8];
+            bf16x8_to_float(__ldg(ka + m), xa);
+            bf16x8_to_float(__ldg(kb + m), xb);
+            float besta = INFINITY, bestb = INFINITY;
+            int arga = 0, argb = 0;
+            const float *cm = cb + (size_t)m * C * kPqDs;
+            const float *nm = nrm + (size_t)m * C;
+            for (int c = 0; c < C; ++c) {
+                const float4 c0 = *reinterpret_cast<const float4 *>(cm + c * kPqDs);
+                const float4 c1 = *reinterpret_cast<const float4 *>(cm + c * kPqDs + 4);
+                float da = xa[0] * c0.x, db = xb[0] * c0.x;
+                da = fmaf(xa[1], c0.y, da); db = fmaf(xb[1], c0.y, db);
+                da = fmaf(xa[2], c0.z, da); db = fmaf(xb[2], c0.z, db);
+                da = fmaf(xa[3], c0.w, da); db = fmaf(xb[3], c0.w, db);
+                da = fmaf(xa[4], c1.x, da); db = fmaf(xb[4], c1.x, db);
+                da = fmaf(xa[5], c1.y, da); db = fmaf(xb[5], c1.y, db);
+                da = fmaf(xa[6], c1.z, da); db = fmaf(xb[6], c1.z, db);
+                da = fmaf(xa[7], c1.w, da); db = fmaf(xb[7], c1.w, db);
+                const float n = nm[c];
+                const float ea = fmaf(-2.f, da, n), eb = fmaf(-2.f, db, n);
+                if (ea < besta) { besta = ea; arga = c; }   // strict: the smaller index keeps a tie
+                if (eb < bestb) { bestb = eb; argb = c; }
+            }
+            ca[m] = (uint8_t)arga;
+            cbb[m] = (uint8_t)argb;
+        }
+        if (va) {
+            uint8_t *dst = codes + (((size_t)b * H_kv + h) * L_cap + ja) * M;
+#pragma unroll
+            for (int m = 0; m < M; ++m) dst[m] = ca[m];
+        }
+        if (vb) {
+            uint8_t *dst = codes + (((size_t)b * H_kv + h) * L_cap + jb) * M;
+#pragma unroll
+            for (int m = 0; m < M; ++m) dst[m] = cbb[m];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ update
+template <int D>
+__global__ void __launch_bounds__(kPqUpdThreads) pq_update_kernel(const __nv_bfloat16 *__restrict__ k,
+                                                                 const int32_t *__restrict__ len_p,
+                                                                 const uint8_t *__restrict__ codes,
+                                                                 float *__restrict__ codebook, int H_kv, int L_cap,
+                                                                 int C) {
+    constexpr int M = D / kPqDs;
+    constexpr int MH = M / 2;                     // subspaces per CTA (blockIdx.x picks the half)
+    extern __shared__ __align__(16) unsigned long long pq_acc[];
+    unsigned long long *sum = pq_acc;             // [MH][C][8], 2^-32 fixed point (two's complement)
+    int *cnt = reinterpret_cast<int *>(sum + (size_t)MH * C * kPqDs);   // [MH][C]
+    const int half = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const int m0 = half * MH;
+    pdl_trigger();
+    pdl_wait();
+    for (int i = tid; i < MH * C * kPqDs; i += kPqUpdThreads) sum[i] = 0ull;
+    for (int i = tid; i < MH * C; i += kPqUpdThreads) cnt[i] = 0;
+    __syncthreads();
+    const int len = pq_clamp(__ldg(len_p + b), L_cap);
+    for (int j = tid; j < len; j += kPqUpdThreads) {
+        const uint8_t *cr = codes + (((size_t)b * H_kv + h) * L_cap + j) * M + m0;
+        const uint4 *kr = reinterpret_cast<const uint4 *>(k + (((size_t)b * L_cap + j) * H_kv + h) * D) + m0;
+#pragma unroll 1
+        for (int mm = 0; mm < MH; ++mm) {
+            const int c = __ldg(cr + mm);
+            if (c >= C) continue;
+            float x[8];
+            bf16x8_to_float(__ldg(kr + mm), x);
+            atomicAdd(cnt + mm * C + c, 1);
+            unsigned long long *s = sum + ((size_t)mm * C + c) * kPqDs;
+#pragma unroll
+            for (int e = 0; e < kPqDs; ++e)
+                atomicAdd(s + e, (unsigned long long)__float2ll_rn(x[e] * 4294967296.0f));
+        }
+    }
+    __syncthreads();
+    float *cbo = codebook + (((size_t)b * H_kv + h) * M + m0) * C * kPqDs;
+    for (int t = tid; t < MH * C * kPqDs; t += kPqUpdThreads) {
+        const int mc = t / kPqDs;
+        const int n = cnt[mc];
+        if (n == 0) continue;
+        const double total = (double)(long long)sum[t] * (1.0 / 4294967296.0);
+        cbo[t] = (float)__ddiv_rn(total, (double)n);
+    }
+}
+
+// ------------------------------------------------------------------ scores
+__device__ __forceinline__ int pq_locate(long long t, const int *prefix, int B, int H_kv, int &h, int &ti) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)H_kv * prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int nt = prefix[lo + 1] - prefix[lo];
+    const long long local = t - (long long)H_kv * prefix[lo];
+    h = (int)(local / nt);
+    ti = (int)(local - (long long)h * nt);
+    return lo;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScoreParams p) {
+    constexpr int M = D / kPqDs;
+    extern __shared__ __align__(16) float pq_sm[];
+    const int G = p.G, C = p.C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *lut = pq_sm;                                   // [M][C][G]
+    float *qs = lut + (size_t)M * C * G;                  // [G][D]
+    int *prefix = reinterpret_cast<int *>(qs + (size_t)G * D);   // [B + 1]
+    pdl_trigger();
+    pdl_wait();
+    for (int b = tid; b < p.B; b += kPqScThreads)
+        prefix[b] = (pq_clamp(__ldg(p.len + b), p.L_cap) + kPqScThreads - 1) / kPqScThreads;
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            const int nt = b < p.B ? prefix[b] : 0;
+            int x = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (b < p.B) prefix[b] = run + x - nt;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) prefix[p.B] = run;
+    }
+    __syncthreads();
+    const long long T = (long long)p.H_kv * prefix[p.B];
+    const long long t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
+    int cur_b = -1, cur_h = -1;
+    for (long long t = t0; t < t1; ++t) {
+        int h, ti;
+        const int b = pq_locate(t, prefix, p.B, p.H_kv, h, ti);
+        if (b != cur_b || h != cur_h) {
+            // lookup table of this (sequence, KV head) for its G query heads
+            __syncthreads();
+            for (int i = tid; i < G * D; i += kPqScThreads) {
+                const int g = i / D, e = i - g * D;
+                qs[i] = __bfloat162float(p.q[((size_t)b * p.H_q + (size_t)h * G + g) * D + e]);
+            }
+            __syncthreads();
+            const float *cbh = p.codebook + ((size_t)b * p.H_kv + h) * M * C * kPqDs;
+            for (int mc = tid; mc < M * C; mc += kPqScThreads) {
+                const int m = mc / C;
+                const float4 c0 = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs));
+                const float4 c1 = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs + 4));
+                for (int g = 0; g < G; ++g) {
+                    const float *qq = qs + g * D + m * kPqDs;
+                    float s = qq[0] * c0.x;
+                    s = fmaf(qq[1], c0.y, s);
+                    s = fmaf(qq[2], c0.z, s);
+                    s = fmaf(qq[3], c0.w, s);
+                    s = fmaf(qq[4], c1.x, s);
+                    s = fmaf(qq[5], c1.y, s);
+                    s = fmaf(qq[6], c1.z, s);
+                    s = fmaf(qq[7], c1.w, s);
+                    lut[(size_t)mc * G + g] = s * p.scale;
+                }
+            }
+            __syncthreads();
+            cur_b = b;
+            cur_h = h;
+        }
+        const int len = pq_clamp(__ldg(p.len + b), p.L_cap);
+        const int j = ti * kPqScThreads + tid;
+        if (j >= len) continue;
+        const uint8_t *cr = p.codes + (((size_t)b * p.H_kv + h) * p.L_cap + j) * M;
+        uint8_t cc[M];
+        if (M == 16) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(cr));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int m = 0; m < M; ++m) cc[m] = (uint8_t)(w[m >> 2] >> (8 * (m & 3)));
+        } else {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(cr));
+            const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+            for (int m = 0; m < M; ++m) cc[m] = (uint8_t)(w[m >> 2] >> (8 * (m & 3)));
+        }
+        float *srow = p.score + ((size_t)b * p.H_q + (size_t)h * G) * p.L_sc + j;
+        if (G == 4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const int c = cc[m] < C ? cc[m] : 0;
+                const float4 l = *reinterpret_cast<const float4 *>(lut + ((size_t)m * C + c) * 4);
+                acc.x += l.x; acc.y += l.y; acc.z += l.z; acc.w += l.w;
+            }
+            srow[0] = acc.x;
+            srow[(size_t)p.L_sc] = acc.y;
+            srow[2 * (size_t)p.L_sc] = acc.z;
+            srow[3 * (size_t)p.L_sc] = acc.w;
+        } else {
+            for (int g = 0; g < G; ++g) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const int c = cc[m] < C ? cc[m] : 0;
+                    acc += lut[((size_t)m * C + c) * G + g];
+                }
+                srow[(size_t)g * p.L_sc] = acc;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------- host side
+magicdec_status launch_pq_encode(int B, int H_kv, int D, int L_cap, int C, const void *k, const float *codebook,
+                                 uint8_t *codes, cudaStream_t st) {
+    const int M = D / kPqDs;
+    const size_t smem = (size_t)M * C * kPqDs * 4 + (size_t)M * C * 4;
+    if (smem > (size_t)magicdec_host::max_smem_optin()) return MAGICDEC_ERR_UNSUPPORTED;
+    const dim3 grid((L_cap + kPqEncChunk - 1) / kPqEncChunk, H_kv, B);
+    auto kb = static_cast<const __nv_bfloat16 *>(k);
+    if (D == 128) {
+        if (cudaFuncSetAttribute(pq_encode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MAGICDEC_ERR_CUDA;
+        return magicdec_host::launch_pdl(pq_encode_kernel<128>, grid, dim3(kPqEncThreads), smem, st, kb, codebook,
+                                         codes, H_kv, L_cap, C);
+    }
+    if (cudaFuncSetAttribute(pq_encode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return MAGICDEC_ERR_CUDA;
+    return magicdec_host::launch_pdl(pq_encode_kernel<64>, grid, dim3(kPqEncThreads), smem, st, kb, codebook, codes,
+                                     H_kv, L_cap, C);
+}
+
+magicdec_status launch_pq_update(int B, int H_kv, int D, int L_cap, int C, const void *k, const int32_t *len,
+                                 const uint8_t *codes, float *codebook, cudaStream_t st) {
+    const int MH = D / kPqDs / 2;
+    const size_t smem = (size_t)MH * C * kPqDs * 8 + (size_t)MH * C * 4;
+    if (smem > (size_t)magicdec_host::max_smem_optin()) return MAGICDEC_ERR_UNSUPPORTED;
+    const dim3 grid(2, H_kv, B);
+    auto kb = static_cast<const __nv_bfloat16 *>(k);
+    if (D == 128) {
+        if (cudaFuncSetAttribute(pq_update_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MAGICDEC_ERR_CUDA;
+        return magicdec_host::launch_pdl(pq_update_kernel<128>, grid, dim3(kPqUpdThreads), smem, st, kb, len, codes,
+                                         codebook, H_kv, L_cap, C);
+    }
+    if (cudaFuncSetAttribute(pq_update_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return MAGICDEC_ERR_CUDA;
+    return magicdec_host::launch_pdl(pq_update_kernel<64>, grid, dim3(kPqUpdThreads), smem, st, kb, len, codes,
+                                     codebook, H_kv, L_cap, C);
+}
+
+magicdec_status launch_topk_select_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,
+                                        const void *v, const int32_t *len, int top_k, bool exact, const float *score,
+                                        void *out, int32_t *idx, cudaStream_t st);
+
+magicdec_status launch_pq_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, int C, const void *q, const void *k,
+                                     const void *v, const int32_t *len, const float *codebook, const uint8_t *codes,
+                                     int top_k, void *out, int32_t *idx, void *ws, cudaStream_t st) {
+    const int M = D / kPqDs, G = H_q / H_kv;
+    PqScoreParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.codebook = codebook;
+    p.codes = codes;
+    p.len = len;
+    p.score = static_cast<float *>(ws);
+    p.B = B;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.G = G;
+    p.L_cap = L_cap;
+    p.L_sc = (L_cap + 3) & ~3;
+    p.C = C;
+    p.scale = 1.0f / sqrtf((float)D);
+    const size_t smem = (size_t)M * C * G * 4 + (size_t)G * D * 4 + (size_t)(B + 1) * 4;
+    if (smem > (size_t)magicdec_host::max_smem_optin()) return MAGICDEC_ERR_UNSUPPORTED;
+    int per_sm = (int)((size_t)magicdec_host::max_smem_optin() / (smem + 1024));
+    per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+    const int grid = magicdec_host::sm_count() * per_sm;
+    magicdec_status s;
+    if (D == 128) {
+        if (cudaFuncSetAttribute(pq_scores_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MAGICDEC_ERR_CUDA;
+        s = magicdec_host::launch_pdl(pq_scores_kernel<128>, dim3(grid), dim3(kPqScThreads), smem, st, p);
+    } else {
+        if (cudaFuncSetAttribute(pq_scores_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MAGICDEC_ERR_CUDA;
+        s = magicdec_host::launch_pdl(pq_scores_kernel<64>, dim3(grid), dim3(kPqScThreads), smem, st, p);
+    }
+    if (s != MAGICDEC_OK) return s;
+    return launch_topk_select_attn(B, H_q, H_kv, D, L_cap, q, k, v, len, top_k, true, p.score, out, idx, st);
+}
+
+}  // namespace magicdec

@@ -50,13 +50,16 @@ struct TopkScoreParams {
 };
 
 struct TopkSelParams {
-    const float *score;       // [B, H_q, L_sc]
+    const float *score;       // [B, H_q, L_sc] selection scores
+    const __nv_bfloat16 *q;   // [B, 1, H_q, D]   (exact-score mode)
+    const __nv_bfloat16 *k;   // [B, L_cap, H_kv, D] (exact-score mode)
     const __nv_bfloat16 *v;   // [B, L_cap, H_kv, D]
     const int32_t *len;       // [B]
     __nv_bfloat16 *out;       // [B, 1, H_q, D]
     int32_t *idx;             // [B, H_q, top_k] or null
     int B, H_q, H_kv, G, L_cap, L_sc, top_k;
     int cand_cap;             // shared-memory candidate slots
+    float scale;              // 1/sqrt(D) (exact-score mode)
 };
 
 __device__ __forceinline__ int tk_clamp_len(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
@@ -364,7 +367,11 @@ __device__ void tk_select_full_row(const float *srow, int len, int top_k, int d1
     (void)top_k;
 }
 
-template <int D>
+// EXACT = false: the selection scores are the exact scaled scores (Top-K
+// attention) and weight the kept rows directly.  EXACT = true: they are
+// approximate (PQ lookup sums) and only choose the rows; the kept rows' exact
+// scores are recomputed from K before the softmax.
+template <int D, bool EXACT>
 __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSelParams p) {
     constexpr int NW = kTkNW;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -372,7 +379,9 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     int *cand_pos = hist + kTkBins;                                   // [cand_cap]
     uint32_t *cand_key = reinterpret_cast<uint32_t *>(cand_pos + p.cand_cap);   // [cand_cap]
     int *sel = reinterpret_cast<int *>(cand_key + p.cand_cap);        // [top_k]
+    float *ex = reinterpret_cast<float *>(sel + ((p.top_k + 3) & ~3)); // [top_k] exact scores (EXACT)
     __shared__ int wsum[32], woff[NW], wcnt[NW];
+    __shared__ float s_exmax[NW];
     __shared__ int s_digit, s_rem, s_total, s_over;
     __shared__ unsigned s_maxkey;
     __shared__ float zsum[NW];
@@ -548,7 +557,61 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     constexpr int LPR = D / 8;
     constexpr int RPI = 32 / LPR;
     const int sub = lane % LPR, part = lane / LPR;
-    const float m_log2 = tk_unkey(s_maxkey) * kLog2e;
+    float m_log2 = tk_unkey(s_maxkey) * kLog2e;
+    if (EXACT) {
+        // exact scaled scores of the kept rows: lane `sub` of a row group dots
+        // channels sub*8 .. +7 of q and the K row, the group's lanes sum
+        float qv[8];
+        {
+            const uint4 qq = __ldg(reinterpret_cast<const uint4 *>(p.q + row * D + sub * 8));
+            const uint32_t w4[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[c]));
+                qv[2 * c] = f.x;
+                qv[2 * c + 1] = f.y;
+            }
+        }
+        const __nv_bfloat16 *kb = p.k + ((long long)b * p.L_cap * p.H_kv + kvh) * D + sub * 8;
+        const long long kstride = (long long)p.H_kv * D;
+        float mx = -INFINITY;
+        constexpr int UK = 2;
+        for (int t0 = 0; warp + NW * RPI * t0 < n; t0 += UK) {
+            uint4 raw[UK];
+#pragma unroll
+            for (int u = 0; u < UK; ++u) {
+                const int i = warp + NW * (RPI * (t0 + u) + part);
+                raw[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < n) raw[u] = __ldg(reinterpret_cast<const uint4 *>(kb + (long long)sel[i] * kstride));
+            }
+#pragma unroll
+            for (int u = 0; u < UK; ++u) {
+                const int i = warp + NW * (RPI * (t0 + u) + part);
+                const uint32_t w4[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+                float dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[c]));
+                    dot = fmaf(qv[2 * c], f.x, dot);
+                    dot = fmaf(qv[2 * c + 1], f.y, dot);
+                }
+#pragma unroll
+                for (int o2 = LPR / 2; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o2);
+                if (i < n) {
+                    const float sc = dot * p.scale;
+                    mx = fmaxf(mx, sc);
+                    if (sub == 0) ex[i] = sc;
+                }
+            }
+        }
+        mx = warp_max(mx);
+        if (lane == 0) s_exmax[warp] = mx;
+        __syncthreads();
+        float m = s_exmax[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) m = fmaxf(m, s_exmax[w]);
+        m_log2 = m * kLog2e;
+    }
     float acc[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[c] = 0.f;
@@ -566,7 +629,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
             raw[u] = make_uint4(0u, 0u, 0u, 0u);
             if (i < n) {
                 const int j = sel[i];
-                sc[u] = __ldg(srow + j);
+                sc[u] = EXACT ? ex[i] : __ldg(srow + j);
                 raw[u] = __ldg(reinterpret_cast<const uint4 *>(vb + (long long)j * vstride));
             }
         }
@@ -616,6 +679,21 @@ size_t topk_workspace_bytes(int B, int H_q, int L_cap) {
     return (size_t)B * H_q * tk_row_stride(L_cap) * sizeof(float);
 }
 
+// Selection + attention kernel: candidates are the top_k plus room for the
+// threshold bin's other members.
+template <int D>
+static magicdec_status launch_select_attn(TopkSelParams tp, bool exact, cudaStream_t st) {
+    const int smem_cap = magicdec_host::max_smem_optin();
+    tp.cand_cap = tp.top_k + 4096;
+    const size_t k4 = (size_t)((tp.top_k + 3) & ~3) * 4;
+    const size_t smem2 = (size_t)kTkBins * 4 + (size_t)tp.cand_cap * 8 + k4 + (exact ? k4 : 0);
+    if (smem2 + 2048 > (size_t)smem_cap) return MAGICDEC_ERR_UNSUPPORTED;
+    auto k2 = exact ? topk_select_attn_kernel<D, true> : topk_select_attn_kernel<D, false>;
+    if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
+        return MAGICDEC_ERR_CUDA;
+    return magicdec_host::launch_pdl(k2, dim3(tp.H_q, tp.B), dim3(kTkNT), smem2, st, tp);
+}
+
 template <int D>
 static magicdec_status launch_topk_impl(const TopkScoreParams &sp, const TopkSelParams &tp, const CUtensorMap &tmk,
                                         cudaStream_t st) {
@@ -636,15 +714,7 @@ static magicdec_status launch_topk_impl(const TopkScoreParams &sp, const TopkSel
                                                   dim3((kTkConsumers + 1) * 32), smem1, st, tmk, s1);
     if (s != MAGICDEC_OK) return s;
 
-    // candidates: the top_k plus room for the threshold bin's other members
-    TopkSelParams t2 = tp;
-    t2.cand_cap = tp.top_k + 4096;
-    const size_t smem2 = (size_t)kTkBins * 4 + (size_t)t2.cand_cap * 8 + (size_t)((tp.top_k + 3) & ~3) * 4;
-    if (smem2 + 2048 > (size_t)smem_cap) return MAGICDEC_ERR_UNSUPPORTED;
-    auto k2 = topk_select_attn_kernel<D>;
-    if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
-        return MAGICDEC_ERR_CUDA;
-    return magicdec_host::launch_pdl(k2, dim3(tp.H_q, tp.B), dim3(kTkNT), smem2, st, t2);
+    return launch_select_attn<D>(tp, false, st);
 }
 
 magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,
@@ -667,7 +737,10 @@ magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_ca
     sp.scale = 1.0f / sqrtf((float)D);
     TopkSelParams tp{};
     tp.score = sp.score;
+    tp.q = static_cast<const __nv_bfloat16 *>(q);
+    tp.k = static_cast<const __nv_bfloat16 *>(k);
     tp.v = static_cast<const __nv_bfloat16 *>(v);
+    tp.scale = sp.scale;
     tp.len = len;
     tp.out = static_cast<__nv_bfloat16 *>(out);
     tp.idx = idx;
@@ -688,6 +761,34 @@ magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_ca
     if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box)) return MAGICDEC_ERR_CUDA;
     if (D == 128) return launch_topk_impl<128>(sp, tp, tmk, st);
     if (D == 64) return launch_topk_impl<64>(sp, tp, tmk, st);
+    return MAGICDEC_ERR_UNSUPPORTED;
+}
+
+// Selection by precomputed scores [B, H_q, L_cap rounded to 4] and attention
+// over the kept rows; exact = true recomputes the kept rows' scores from K.
+magicdec_status launch_topk_select_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,
+                                        const void *v, const int32_t *len, int top_k, bool exact, const float *score,
+                                        void *out, int32_t *idx, cudaStream_t st) {
+    const int G = H_q / H_kv;
+    if (top_k > kTkMaxTopK) return MAGICDEC_ERR_UNSUPPORTED;
+    TopkSelParams tp{};
+    tp.score = score;
+    tp.q = static_cast<const __nv_bfloat16 *>(q);
+    tp.k = static_cast<const __nv_bfloat16 *>(k);
+    tp.v = static_cast<const __nv_bfloat16 *>(v);
+    tp.len = len;
+    tp.out = static_cast<__nv_bfloat16 *>(out);
+    tp.idx = idx;
+    tp.B = B;
+    tp.H_q = H_q;
+    tp.H_kv = H_kv;
+    tp.G = G;
+    tp.L_cap = L_cap;
+    tp.L_sc = tk_row_stride(L_cap);
+    tp.top_k = top_k;
+    tp.scale = 1.0f / sqrtf((float)D);
+    if (D == 128) return launch_select_attn<128>(tp, exact, st);
+    if (D == 64) return launch_select_attn<64>(tp, exact, st);
     return MAGICDEC_ERR_UNSUPPORTED;
 }
 

@@ -86,6 +86,16 @@ def test_null_and_shape_errors_are_reported_before_launch(lib):
     assert lib.magicdec_spec_accept(4, 3, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, NULL, FAKE,
                                     8, NULL) == -4
     big = 1 << 40
+    assert lib.magicdec_pq_encode(shape(), FAKE, 16, 256, NULL, FAKE, NULL) == -1
+    assert lib.magicdec_pq_encode(shape(), FAKE, 8, 256, FAKE, FAKE, NULL) == -2        # M must be d/8
+    assert lib.magicdec_pq_encode(shape(), FAKE, 16, 257, FAKE, FAKE, NULL) == -2
+    assert lib.magicdec_pq_update(shape(), FAKE, NULL, 16, 256, FAKE, FAKE, NULL) == -1
+    assert lib.magicdec_pq_draft_attn(shape(), FAKE, FAKE, FAKE, FAKE, 16, 256, FAKE, FAKE, 0, FAKE, NULL, FAKE,
+                                      big, NULL) == -2
+    assert lib.magicdec_pq_draft_attn(shape(), FAKE, FAKE, FAKE, FAKE, 16, 256, FAKE, FAKE, 64, FAKE, NULL, FAKE,
+                                      64, NULL) == -4
+    assert lib.magicdec_pq_draft_attn(shape(), MISALIGNED, FAKE, FAKE, FAKE, 16, 256, FAKE, FAKE, 64, FAKE, NULL,
+                                      FAKE, big, NULL) == -3
     I32 = P(0x20000)
     assert lib.magicdec_draft_cache_update(shape(), FAKE, FAKE, I32, I32, I32, I32, NULL, 0, 64, FAKE, FAKE, I32,
                                            NULL) == -1

@@ -177,6 +177,107 @@ def test_snapkv_select_matches_oracle(B, H_q, H_kv, d, L_cap, w, pool, budget, l
     assert band <= 2 * pool * B * H_kv + 8, f"too many band positions: {band}"
 
 
+# ------------------------------------------------------------ PQCache-style
+PQ_MARGIN = 1e-5      # relative to |k_m|^2 + |c|^2: fp32 dot-product distances vs the oracle's fp64
+
+
+def _pq_codebook(rng, B, H_kv, M, C, scale=1.0):
+    return (scale * rng.standard_normal((B, H_kv, M, C, 8))).astype(np.float32)
+
+
+@pytest.mark.parametrize("B,H_kv,L,C", [(2, 8, 3000, 64), (2, 2, 1500, 256), (1, 8, 700, 7)])
+def test_pq_encode_matches_oracle(B, H_kv, L, C):
+    rng = np.random.default_rng(71)
+    d, M = 128, 16
+    k = rand_bf16((B, L, H_kv, d), 72)
+    cb = _pq_codebook(rng, B, H_kv, M, C)
+    codes = mb.magicdec_pq_encode(k.to(DEV), torch.from_numpy(cb).to(DEV))
+    torch.cuda.synchronize()
+    codes_o, gap = oracle.pq_encode(to_u16(k), cb, want_gap=True)
+    g = codes.cpu().numpy()
+    kf = bf16_out_to_f64(k).reshape(B, L, H_kv, M, 8).transpose(0, 2, 1, 3, 4)      # [B,H_kv,L,M,8]
+    kn = (kf ** 2).sum(-1)
+    cn = (cb.astype(np.float64) ** 2).sum(-1)                                       # [B,H_kv,M,C]
+    cbest = np.take_along_axis(cn[:, :, None, :, :], codes_o[..., None].astype(np.int64), axis=-1)[..., 0]
+    margin = gap <= PQ_MARGIN * (kn + cbest)
+    assert np.array_equal(g[~margin], codes_o[~margin])
+    assert margin.mean() < 1e-3, f"{margin.sum()} margin codes"
+
+
+def test_pq_update_matches_oracle_exactly():
+    rng = np.random.default_rng(73)
+    B, H_kv, d, L, M, C = 2, 8, 128, 2500, 16, 64
+    k = rand_bf16((B, L, H_kv, d), 74)
+    cb = _pq_codebook(rng, B, H_kv, M, C)
+    codes, _ = oracle.pq_encode(to_u16(k), cb)
+    codes[0, 0, :, 3] = 5                  # crowd one centroid, empty another
+    codes[codes == 9] = 10
+    sl = np.array([L, 1777], np.int32)
+    cb_g = torch.from_numpy(cb.copy()).to(DEV)
+    mb.magicdec_pq_update(k.to(DEV), torch.from_numpy(sl).to(DEV), torch.from_numpy(codes).to(DEV), cb_g)
+    torch.cuda.synchronize()
+    cb_o = oracle.pq_update(to_u16(k), sl, codes, cb)
+    np.testing.assert_array_equal(cb_g.cpu().numpy(), cb_o)
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,L,C,top_k,lens", [
+    (3, 32, 8, 3000, 64, 256, [3000, 2000, 100]),
+    (2, 40, 8, 2100, 256, 512, [2100, 1500]),
+    (2, 16, 2, 1200, 32, 64, [1200, 0]),
+])
+def test_pq_draft_attn_matches_oracle(B, H_q, H_kv, L, C, top_k, lens):
+    rng = np.random.default_rng(75)
+    d, M = 128, 16
+    q = rand_bf16((B, 1, H_q, d), 76)
+    k = rand_bf16((B, L, H_kv, d), 77)
+    v = rand_bf16((B, L, H_kv, d), 78)
+    k[:, ::61] *= 3
+    cb = _pq_codebook(rng, B, H_kv, M, C)
+    sl = np.array(lens, np.int32)
+    codes, _ = oracle.pq_encode(to_u16(k), cb)
+    cb = oracle.pq_update(to_u16(k), np.full(B, L, np.int32), codes, cb)
+    codes, _ = oracle.pq_encode(to_u16(k), cb)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_pq_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV),
+                                    torch.from_numpy(cb).to(DEV), torch.from_numpy(codes).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, approx = oracle.pq_attn(to_u16(q), to_u16(k), to_u16(v), sl, cb, codes, top_k, want_approx=True)
+    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, approx, sl, top_k, "pq")
+    assert swapped <= max(1, B * H_q // 50)
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.count_nonzero(out[b]) == 0
+
+
+def test_pq_lloyd_pipeline_on_planted_clusters():
+    """GPU encode + update twice from one member per planted cluster: codes equal the oracle's and the
+    planted labels, codebooks equal the oracle's."""
+    rng = np.random.default_rng(79)
+    B, L, H_kv, d, M, C = 2, 2000, 4, 128, 16, 12
+    proto = rng.standard_normal((B, H_kv, M, C, 8)) * 4.0
+    label = rng.integers(0, C, size=(B, H_kv, L, M))
+    label[:, :, :C] = np.arange(C)[None, None, :, None]
+    sub = np.take_along_axis(proto[:, :, None], label[..., None, None].repeat(8, -1), axis=4)[..., 0, :]
+    kf = (sub + 0.05 * rng.standard_normal(sub.shape)).transpose(0, 2, 1, 3, 4).reshape(B, L, H_kv, d)
+    k = torch.from_numpy(np.ascontiguousarray(kf, dtype=np.float32)).to(torch.bfloat16)
+    ku = to_u16(k)
+    kb = bf16_out_to_f64(k).reshape(B, L, H_kv, M, 8)
+    cb0 = kb[:, :C].transpose(0, 2, 3, 1, 4).astype(np.float32).copy()
+    sl = np.full(B, L, np.int32)
+    cb_g = torch.from_numpy(cb0.copy()).to(DEV)
+    k_g, sl_g = k.to(DEV), torch.from_numpy(sl).to(DEV)
+    cb_o = cb0
+    for _ in range(2):
+        codes_g = mb.magicdec_pq_encode(k_g, cb_g)
+        mb.magicdec_pq_update(k_g, sl_g, codes_g, cb_g)
+        codes_o, _ = oracle.pq_encode(ku, cb_o)
+        cb_o = oracle.pq_update(ku, sl, codes_o, cb_o)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(codes_g.cpu().numpy(), codes_o)
+    np.testing.assert_array_equal(codes_o, label)
+    np.testing.assert_array_equal(cb_g.cpu().numpy(), cb_o)
+
+
 # ------------------------------------------------------- draft-cache update
 def _dc_step(k, v, kc, vc, kc_o, vc_o, lv, lo, ln, origin, base, ring):
     dev = torch.device(DEV)
