@@ -385,6 +385,44 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                                                   idx=pipe.idx, n_sel=pipe.n_sel),
                                      mb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc,
                                                            vc=pipe.vc)), 5)
+    # PQCache-style draft at the same budget: codebook built once (2 Lloyd
+    # iterations from seeded key samples, then the final encode), then the
+    # per-draft-step search (LUT scores over the codes, select, exact attention)
+    pq = {}
+    if not args.no_pq:
+        M, C, iters = w.d // 8, 256, 2
+        gen = torch.Generator(device="cpu").manual_seed(w.seed * 11 + 5)
+        pick = torch.randint(0, w.L, (w.B, w.H_kv, C), generator=gen).to(device)
+        bidx = torch.arange(w.B, device=device)[:, None, None]
+        hidx = torch.arange(w.H_kv, device=device)[None, :, None]
+        init = pipe.k[bidx, pick, hidx].float().reshape(w.B, w.H_kv, C, M, 8).permute(0, 1, 3, 2, 4).contiguous()
+        cb = init.clone()
+        codes = torch.empty((w.B, w.H_kv, w.L, M), dtype=torch.uint8, device=device)
+
+        def pq_build():
+            cb.copy_(init)
+            for _ in range(iters):
+                mb.magicdec_pq_encode(pipe.k, cb, codes=codes)
+                mb.magicdec_pq_update(pipe.k, pipe.seq_len, codes, cb)
+            mb.magicdec_pq_encode(pipe.k, cb, codes=codes)
+        build_ms = time_component(pq_build, 1)
+        pq_idx = torch.empty((w.B, w.H_q, pipe.cap), dtype=torch.int32, device=device)
+        pq_out = torch.empty_like(pipe.q_draft)
+        pq_ws = torch.empty(mb.magicdec_pq_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L)),
+                            dtype=torch.uint8, device=device)
+        pq_ms = time_component(lambda: mb.magicdec_pq_draft_attn(pipe.q_draft, pipe.k, pipe.v, pipe.seq_len, cb, codes,
+                                                                 pipe.cap, out=pq_out, idx=pq_idx, ws=pq_ws), 5)
+        kv_bytes = float(w.B) * w.L * w.H_kv * w.d * 2
+        pq = {"pq_draft_us_per_layer": round(pq_ms * 1e3, 2), "pq_build_ms_per_layer": round(build_ms, 3),
+              "pq_M": M, "pq_C": C, "pq_lloyd_iterations": iters,
+              "_pq_bytes": (float(w.B) * w.H_kv * w.L * M + float(w.B) * w.H_kv * M * C * 8 * 4
+                            + 2.0 * w.B * w.H_q * pipe.cap * w.d * 2 + 2.0 * w.B * w.H_q * w.d * 2),
+              "_pq_ms": pq_ms,
+              # each encode and each update reads K once; codes written per encode
+              "_pq_build_bytes": (2 * iters + 1) * kv_bytes + (iters + 1) * float(w.B) * w.H_kv * w.L * M,
+              "_pq_build_ms": build_ms}
+        del init, cb, codes, pq_idx, pq_out, pq_ws, pick
+        torch.cuda.empty_cache()
     ring_ms = time_graph(pipe.ring_updates, 20)
     # the step with the ring-maintained draft cache, timed like the headline step
     for _ in range(args.warmup):
@@ -530,6 +568,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 row(pipe.ring_update_bytes(), ring_ms)}
     if snap:
         rows["snapkv_select (once per prefill)"] = row(snap.pop("_snap_bytes"), snap.pop("_snap_ms"))
+    if pq:
+        pq_ms = pq.pop("_pq_ms")
+        rows["pq_draft_attn (LUT scores + select + exact attend, per draft step)"] = row(pq.pop("_pq_bytes"), pq_ms)
+        rows["pq_build (2 Lloyd iterations + encode, once per prefill)"] = row(pq.pop("_pq_build_bytes"),
+                                                                               pq.pop("_pq_build_ms"))
+        pq["pq_over_verify"] = round(pq_ms / ver_ms, 4)
     if topk:
         tk_ms = topk.pop("_topk_ms")
         rows["topk_draft_attn (scores + select + attend, per draft step)"] = row(topk.pop("_topk_bytes"), tk_ms)
@@ -566,6 +610,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "select_gather_us_per_layer": round(sel_ms * 1e3, 2),
         **snap,
         **topk,
+        **pq,
         "omega_hat_synthetic": round(omega_hat, 4),
         "tokens_per_s_synthetic": round(world * w.B * omega_hat * args.steps / (ms_total * 1e-3), 1),
         "gpu_launches": pipe.launches_per_step * args.steps,
@@ -688,6 +733,7 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-topk", action="store_true", help="skip the Top-K attention draft row")
+    ap.add_argument("--no-pq", action="store_true", help="skip the PQCache-style draft rows")
     ap.add_argument("--graph", action="store_true", help="also time the step captured in a CUDA graph")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling runs on smaller cases)")

@@ -17,7 +17,7 @@
 //                     over up to 2^17 positions); the
 //                     mean is a correctly rounded fp64 division, rounded to
 //                     fp32.  A centroid without keys keeps its value.
-//   pq_scores_kernel  per draft step: persistent over 256-position tiles of
+//   pq_scores_kernel  per draft step: persistent over 1024-position tiles of
 //                     (sequence, KV head); each (sequence, head) builds the
 //                     lookup table LUT[m][c][g] = scale * q_g,m . c_m,c for
 //                     its G query heads once, then a position's approximate
@@ -32,7 +32,9 @@ constexpr int kPqDs = 8;              // channels per subspace
 constexpr int kPqEncThreads = 256;
 constexpr int kPqEncChunk = 2048;     // positions per encode CTA
 constexpr int kPqUpdThreads = 512;
-constexpr int kPqScThreads = 256;     // = positions per score tile
+constexpr int kPqScThreads = 256;
+constexpr int kPqScPer = 4;           // positions per thread in a score tile
+constexpr int kPqScTile = kPqScThreads * kPqScPer;
 
 struct PqScoreParams {
     const __nv_bfloat16 *q;    // [B, 1, H_q, D]
@@ -81,50 +83,69 @@ __global__ void __launch_bounds__(kPqEncThreads) pq_encode_kernel(const __nv_bfl
     }
     __syncthreads();
     const int j0 = chunk * kPqEncChunk, j1 = min(L_cap, j0 + kPqEncChunk);
-    // positions j and j + kPqEncThreads together: each centroid read feeds two keys
-    for (int base = j0; base < j1; base += 2 * kPqEncThreads) {
-        const int ja = base + tid, jb = ja + kPqEncThreads;
-        const bool va = ja < j1, vb = jb < j1;
-        const uint4 *ka = reinterpret_cast<const uint4 *>(k + (((size_t)b * L_cap + (va ? ja : j0)) * H_kv + h) * D);
-        const uint4 *kb = reinterpret_cast<const uint4 *>(k + (((size_t)b * L_cap + (vb ? jb : j0)) * H_kv + h) * D);
-        uint8_t ca[M], cbb[M];
+    // KPT positions j + r * kPqEncThreads together: each centroid read feeds KPT keys
+    constexpr int KPT = 4;
+    for (int base = j0; base < j1; base += KPT * kPqEncThreads) {
+        const uint4 *kr[KPT];
+        bool valid[KPT];
+#pragma unroll
+        for (int r = 0; r < KPT; ++r) {
+            const int j = base + r * kPqEncThreads + tid;
+            valid[r] = j < j1;
+            kr[r] = reinterpret_cast<const uint4 *>(k + (((size_t)b * L_cap + (valid[r] ? j : j0)) * H_kv + h) * D);
+        }
+        uint32_t packed[KPT][M / 4];
+#pragma unroll
+        for (int r = 0; r < KPT; ++r)
+#pragma unroll
+            for (int wi = 0; wi < M / 4; ++wi) packed[r][wi] = 0u;
 #pragma unroll 1
         for (int m = 0; m < M; ++m) {
-            float xa[8], xb[8];
-            bf16x8_to_float(__ldg(ka + m), xa);
-            bf16x8_to_float(__ldg(kb + m), xb);
-            float besta = INFINITY, bestb = INFINITY;
-            int arga = 0, argb = 0;
+            float x[KPT][8];
+#pragma unroll
+            for (int r = 0; r < KPT; ++r) bf16x8_to_float(__ldg(kr[r] + m), x[r]);
+            float best[KPT];
+            int arg[KPT];
+#pragma unroll
+            for (int r = 0; r < KPT; ++r) { best[r] = INFINITY; arg[r] = 0; }
             const float *cm = cb + (size_t)m * C * kPqDs;
             const float *nm = nrm + (size_t)m * C;
             for (int c = 0; c < C; ++c) {
                 const float4 c0 = *reinterpret_cast<const float4 *>(cm + c * kPqDs);
                 const float4 c1 = *reinterpret_cast<const float4 *>(cm + c * kPqDs + 4);
-                float da = xa[0] * c0.x, db = xb[0] * c0.x;
-                da = fmaf(xa[1], c0.y, da); db = fmaf(xb[1], c0.y, db);
-                da = fmaf(xa[2], c0.z, da); db = fmaf(xb[2], c0.z, db);
-                da = fmaf(xa[3], c0.w, da); db = fmaf(xb[3], c0.w, db);
-                da = fmaf(xa[4], c1.x, da); db = fmaf(xb[4], c1.x, db);
-                da = fmaf(xa[5], c1.y, da); db = fmaf(xb[5], c1.y, db);
-                da = fmaf(xa[6], c1.z, da); db = fmaf(xb[6], c1.z, db);
-                da = fmaf(xa[7], c1.w, da); db = fmaf(xb[7], c1.w, db);
                 const float n = nm[c];
-                const float ea = fmaf(-2.f, da, n), eb = fmaf(-2.f, db, n);
-                if (ea < besta) { besta = ea; arga = c; }   // strict: the smaller index keeps a tie
-                if (eb < bestb) { bestb = eb; argb = c; }
+#pragma unroll
+                for (int r = 0; r < KPT; ++r) {
+                    float dd = x[r][0] * c0.x;
+                    dd = fmaf(x[r][1], c0.y, dd);
+                    dd = fmaf(x[r][2], c0.z, dd);
+                    dd = fmaf(x[r][3], c0.w, dd);
+                    dd = fmaf(x[r][4], c1.x, dd);
+                    dd = fmaf(x[r][5], c1.y, dd);
+                    dd = fmaf(x[r][6], c1.z, dd);
+                    dd = fmaf(x[r][7], c1.w, dd);
+                    const float e = fmaf(-2.f, dd, n);
+                    if (e < best[r]) { best[r] = e; arg[r] = c; }   // strict: the smaller index keeps a tie
+                }
             }
-            ca[m] = (uint8_t)arga;
-            cbb[m] = (uint8_t)argb;
-        }
-        if (va) {
-            uint8_t *dst = codes + (((size_t)b * H_kv + h) * L_cap + ja) * M;
 #pragma unroll
-            for (int m = 0; m < M; ++m) dst[m] = ca[m];
-        }
-        if (vb) {
-            uint8_t *dst = codes + (((size_t)b * H_kv + h) * L_cap + jb) * M;
+            for (int r = 0; r < KPT; ++r) {
+                // byte m of the key's code word (M/4 words of 4 codes)
 #pragma unroll
-            for (int m = 0; m < M; ++m) dst[m] = cbb[m];
+                for (int wi = 0; wi < M / 4; ++wi)
+                    if (wi == (m >> 2)) {
+                        const uint32_t sh = 8u * (uint32_t)(m & 3);
+                        packed[r][wi] = (packed[r][wi] & ~(255u << sh)) | ((uint32_t)arg[r] << sh);
+                    }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < KPT; ++r) {
+            if (!valid[r]) continue;
+            uint32_t *dst = reinterpret_cast<uint32_t *>(
+                codes + (((size_t)b * H_kv + h) * L_cap + base + r * kPqEncThreads + tid) * M);
+#pragma unroll
+            for (int wi = 0; wi < M / 4; ++wi) dst[wi] = packed[r][wi];
         }
     }
 }
@@ -139,7 +160,9 @@ __global__ void __launch_bounds__(kPqUpdThreads) pq_update_kernel(const __nv_bfl
     constexpr int M = D / kPqDs;
     constexpr int MH = M / 2;                     // subspaces per CTA (blockIdx.x picks the half)
     extern __shared__ __align__(16) unsigned long long pq_acc[];
-    unsigned long long *sum = pq_acc;             // [MH][C][8], 2^-32 fixed point (two's complement)
+    // [MH][8][C]: the code is the fastest index, so lanes with different codes
+    // fall in different banks.  2^-32 fixed point (two's complement).
+    unsigned long long *sum = pq_acc;
     int *cnt = reinterpret_cast<int *>(sum + (size_t)MH * C * kPqDs);   // [MH][C]
     const int half = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
     const int m0 = half * MH;
@@ -159,19 +182,20 @@ __global__ void __launch_bounds__(kPqUpdThreads) pq_update_kernel(const __nv_bfl
             float x[8];
             bf16x8_to_float(__ldg(kr + mm), x);
             atomicAdd(cnt + mm * C + c, 1);
-            unsigned long long *s = sum + ((size_t)mm * C + c) * kPqDs;
+            unsigned long long *s = sum + (size_t)mm * kPqDs * C + c;
 #pragma unroll
             for (int e = 0; e < kPqDs; ++e)
-                atomicAdd(s + e, (unsigned long long)__float2ll_rn(x[e] * 4294967296.0f));
+                atomicAdd(s + (size_t)e * C, (unsigned long long)__float2ll_rn(x[e] * 4294967296.0f));
         }
     }
     __syncthreads();
     float *cbo = codebook + (((size_t)b * H_kv + h) * M + m0) * C * kPqDs;
     for (int t = tid; t < MH * C * kPqDs; t += kPqUpdThreads) {
-        const int mc = t / kPqDs;
+        const int mc = t / kPqDs, e = t - mc * kPqDs;       // output order [MH][C][8]
+        const int mm = mc / C, c = mc - mm * C;
         const int n = cnt[mc];
         if (n == 0) continue;
-        const double total = (double)(long long)sum[t] * (1.0 / 4294967296.0);
+        const double total = (double)(long long)sum[((size_t)mm * kPqDs + e) * C + c] * (1.0 / 4294967296.0);
         cbo[t] = (float)__ddiv_rn(total, (double)n);
     }
 }
@@ -201,7 +225,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     pdl_trigger();
     pdl_wait();
     for (int b = tid; b < p.B; b += kPqScThreads)
-        prefix[b] = (pq_clamp(__ldg(p.len + b), p.L_cap) + kPqScThreads - 1) / kPqScThreads;
+        prefix[b] = (pq_clamp(__ldg(p.len + b), p.L_cap) + kPqScTile - 1) / kPqScTile;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -223,11 +247,37 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     const long long T = (long long)p.H_kv * prefix[p.B];
     const long long t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
     int cur_b = -1, cur_h = -1;
+    // codes of tile t are loaded during tile t-1 (software pipeline)
+    auto load_codes = [&](long long tt, uint4 (&dst)[kPqScPer]) {
+        int hh, tti;
+        const int bb = pq_locate(tt, prefix, p.B, p.H_kv, hh, tti);
+        const int ll = pq_clamp(__ldg(p.len + bb), p.L_cap);
+        const uint8_t *cbase = p.codes + ((size_t)bb * p.H_kv + hh) * p.L_cap * M;
+#pragma unroll
+        for (int i = 0; i < kPqScPer; ++i) {
+            const int j = tti * kPqScTile + i * kPqScThreads + tid;
+            dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (j < ll) {
+                if (M == 16) {
+                    dst[i] = __ldg(reinterpret_cast<const uint4 *>(cbase + (size_t)j * M));
+                } else {
+                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(cbase + (size_t)j * M));
+                    dst[i].x = u.x;
+                    dst[i].y = u.y;
+                }
+            }
+        }
+    };
+    uint4 raw[kPqScPer], nxt[kPqScPer];
+#pragma unroll
+    for (int i = 0; i < kPqScPer; ++i) raw[i] = nxt[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (t0 < t1) load_codes(t0, raw);
     for (long long t = t0; t < t1; ++t) {
         int h, ti;
         const int b = pq_locate(t, prefix, p.B, p.H_kv, h, ti);
-        if (b != cur_b || h != cur_h) {
-            // lookup table of this (sequence, KV head) for its G query heads
+        const int len = pq_clamp(__ldg(p.len + b), p.L_cap);
+        if (t + 1 < t1) load_codes(t + 1, nxt);
+        if (b != cur_b || h != cur_h) {            // lookup table of this (sequence, KV head) for its G query heads
             __syncthreads();
             for (int i = tid; i < G * D; i += kPqScThreads) {
                 const int g = i / D, e = i - g * D;
@@ -235,67 +285,75 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
             }
             __syncthreads();
             const float *cbh = p.codebook + ((size_t)b * p.H_kv + h) * M * C * kPqDs;
-            for (int mc = tid; mc < M * C; mc += kPqScThreads) {
-                const int m = mc / C;
-                const float4 c0 = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs));
-                const float4 c1 = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs + 4));
-                for (int g = 0; g < G; ++g) {
-                    const float *qq = qs + g * D + m * kPqDs;
-                    float s = qq[0] * c0.x;
-                    s = fmaf(qq[1], c0.y, s);
-                    s = fmaf(qq[2], c0.z, s);
-                    s = fmaf(qq[3], c0.w, s);
-                    s = fmaf(qq[4], c1.x, s);
-                    s = fmaf(qq[5], c1.y, s);
-                    s = fmaf(qq[6], c1.z, s);
-                    s = fmaf(qq[7], c1.w, s);
-                    lut[(size_t)mc * G + g] = s * p.scale;
+            constexpr int BATCH = 4;
+            for (int mc0 = tid; mc0 < M * C; mc0 += BATCH * kPqScThreads) {
+                float4 c0[BATCH], c1[BATCH];
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    const int mc = mc0 + u * kPqScThreads;
+                    if (mc < M * C) {
+                        c0[u] = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs));
+                        c1[u] = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs + 4));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    const int mc = mc0 + u * kPqScThreads;
+                    if (mc >= M * C) continue;
+                    const int m = mc / C;
+                    for (int g = 0; g < G; ++g) {
+                        const float *qq = qs + g * D + m * kPqDs;
+                        float sdot = qq[0] * c0[u].x;
+                        sdot = fmaf(qq[1], c0[u].y, sdot);
+                        sdot = fmaf(qq[2], c0[u].z, sdot);
+                        sdot = fmaf(qq[3], c0[u].w, sdot);
+                        sdot = fmaf(qq[4], c1[u].x, sdot);
+                        sdot = fmaf(qq[5], c1[u].y, sdot);
+                        sdot = fmaf(qq[6], c1[u].z, sdot);
+                        sdot = fmaf(qq[7], c1[u].w, sdot);
+                        lut[(size_t)mc * G + g] = sdot * p.scale;
+                    }
                 }
             }
             __syncthreads();
             cur_b = b;
             cur_h = h;
         }
-        const int len = pq_clamp(__ldg(p.len + b), p.L_cap);
-        const int j = ti * kPqScThreads + tid;
-        if (j >= len) continue;
-        const uint8_t *cr = p.codes + (((size_t)b * p.H_kv + h) * p.L_cap + j) * M;
-        uint8_t cc[M];
-        if (M == 16) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(cr));
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float *srow0 = p.score + ((size_t)b * p.H_q + (size_t)h * G) * p.L_sc;
 #pragma unroll
-            for (int m = 0; m < M; ++m) cc[m] = (uint8_t)(w[m >> 2] >> (8 * (m & 3)));
-        } else {
-            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(cr));
-            const uint32_t w[2] = {u.x, u.y};
-#pragma unroll
-            for (int m = 0; m < M; ++m) cc[m] = (uint8_t)(w[m >> 2] >> (8 * (m & 3)));
-        }
-        float *srow = p.score + ((size_t)b * p.H_q + (size_t)h * G) * p.L_sc + j;
-        if (G == 4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                const int c = cc[m] < C ? cc[m] : 0;
-                const float4 l = *reinterpret_cast<const float4 *>(lut + ((size_t)m * C + c) * 4);
-                acc.x += l.x; acc.y += l.y; acc.z += l.z; acc.w += l.w;
-            }
-            srow[0] = acc.x;
-            srow[(size_t)p.L_sc] = acc.y;
-            srow[2 * (size_t)p.L_sc] = acc.z;
-            srow[3 * (size_t)p.L_sc] = acc.w;
-        } else {
-            for (int g = 0; g < G; ++g) {
-                float acc = 0.f;
+        for (int i = 0; i < kPqScPer; ++i) {
+            const int j = ti * kPqScTile + i * kPqScThreads + tid;
+            if (j >= len) continue;
+            const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+            float *srow = srow0 + j;
+            if (G == 4) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
-                    const int c = cc[m] < C ? cc[m] : 0;
-                    acc += lut[((size_t)m * C + c) * G + g];
+                    int c = (int)((w[m >> 2] >> (8 * (m & 3))) & 255u);
+                    c = c < C ? c : 0;
+                    const float4 l = *reinterpret_cast<const float4 *>(lut + ((size_t)m * C + c) * 4);
+                    acc.x += l.x; acc.y += l.y; acc.z += l.z; acc.w += l.w;
                 }
-                srow[(size_t)g * p.L_sc] = acc;
+                srow[0] = acc.x;
+                srow[(size_t)p.L_sc] = acc.y;
+                srow[2 * (size_t)p.L_sc] = acc.z;
+                srow[3 * (size_t)p.L_sc] = acc.w;
+            } else {
+                for (int g = 0; g < G; ++g) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        int c = (int)((w[m >> 2] >> (8 * (m & 3))) & 255u);
+                        c = c < C ? c : 0;
+                        acc += lut[((size_t)m * C + c) * G + g];
+                    }
+                    srow[(size_t)g * p.L_sc] = acc;
+                }
             }
         }
+#pragma unroll
+        for (int i = 0; i < kPqScPer; ++i) raw[i] = nxt[i];
     }
 }
 
@@ -366,21 +424,16 @@ magicdec_status launch_pq_draft_attn(int B, int H_q, int H_kv, int D, int L_cap,
     p.scale = 1.0f / sqrtf((float)D);
     const size_t smem = (size_t)M * C * G * 4 + (size_t)G * D * 4 + (size_t)(B + 1) * 4;
     if (smem > (size_t)magicdec_host::max_smem_optin()) return MAGICDEC_ERR_UNSUPPORTED;
-    int per_sm = (int)((size_t)magicdec_host::max_smem_optin() / (smem + 1024));
-    per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+    auto kern = D == 128 ? pq_scores_kernel<128> : pq_scores_kernel<64>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MAGICDEC_ERR_CUDA;
+    // persistent grid: exactly the CTAs that can be resident at once
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPqScThreads, smem) != cudaSuccess ||
+        per_sm < 1)
+        return MAGICDEC_ERR_UNSUPPORTED;
     const int grid = magicdec_host::sm_count() * per_sm;
-    magicdec_status s;
-    if (D == 128) {
-        if (cudaFuncSetAttribute(pq_scores_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MAGICDEC_ERR_CUDA;
-        s = magicdec_host::launch_pdl(pq_scores_kernel<128>, dim3(grid), dim3(kPqScThreads), smem, st, p);
-    } else {
-        if (cudaFuncSetAttribute(pq_scores_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MAGICDEC_ERR_CUDA;
-        s = magicdec_host::launch_pdl(pq_scores_kernel<64>, dim3(grid), dim3(kPqScThreads), smem, st, p);
-    }
+    magicdec_status s = magicdec_host::launch_pdl(kern, dim3(grid), dim3(kPqScThreads), smem, st, p);
     if (s != MAGICDEC_OK) return s;
     return launch_topk_select_attn(B, H_q, H_kv, D, L_cap, q, k, v, len, top_k, true, p.score, out, idx, st);
 }

@@ -9,6 +9,8 @@ pair or one sequence at a time from host copies of exactly the bytes the GPU rea
   * Top-K attention draft: every query head of sampled sequences (band rule at the
     top_k-th score);
   * draft-cache update: the StreamingLLM ring of sampled sequences, byte for byte;
+  * PQCache-style selection: the encode of sampled sequences (margin rule) and PQ draft
+    attention with host-drawn codes (band rule);
   * speculative accept: every sequence of the batch (sampling mode) or a sample (greedy).
 """
 import numpy as np
@@ -140,6 +142,54 @@ def test_fullsize_topk_draft_sampled(name, top_k):
         swapped += sw
     assert swapped <= 2
     del k, v
+    torch.cuda.empty_cache()
+
+
+def test_fullsize_pq_sampled():
+    """B=128, L=32000, M=16, C=256: the encode of sampled sequences equals the oracle's (margin rule),
+    and PQ draft attention with host-drawn codes matches the oracle on sampled sequences (band rule)."""
+    w = synth.WORKLOADS["llama8b_b128_l32k"]
+    k, v, _ = synth.kv_cache(w, DEV)
+    M, C, top_k = w.d // 8, 256, 512
+    gen = torch.Generator(device="cpu").manual_seed(91)
+    pick = torch.randint(0, w.L, (w.B, w.H_kv, C), generator=gen).to(DEV)
+    bidx = torch.arange(w.B, device=DEV)[:, None, None]
+    hidx = torch.arange(w.H_kv, device=DEV)[None, :, None]
+    cb = k[bidx, pick, hidx].float().reshape(w.B, w.H_kv, C, M, 8).permute(0, 1, 3, 2, 4).contiguous()
+    codes = mb.magicdec_pq_encode(k, cb)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(w.seed + 17)
+    for b in rng.choice(w.B, size=2, replace=False):
+        b = int(b)
+        cbo = cb[b:b + 1].cpu().numpy()
+        ko = to_u16(k[b:b + 1])
+        codes_o, gap = oracle.pq_encode(ko, cbo, want_gap=True)
+        kf = bf16_out_to_f64(k[b:b + 1]).reshape(1, w.L, w.H_kv, M, 8).transpose(0, 2, 1, 3, 4)
+        kn = (kf ** 2).sum(-1)
+        cn = (cbo.astype(np.float64) ** 2).sum(-1)
+        cbest = np.take_along_axis(cn[:, :, None], codes_o[..., None].astype(np.int64), axis=-1)[..., 0]
+        margin = gap <= 1e-5 * (kn + cbest)
+        g = codes[b:b + 1].cpu().numpy()
+        assert np.array_equal(g[~margin], codes_o[~margin])
+        # 256 centroids in 8 dimensions: the two nearest are often close, so a fraction of a
+        # percent of the decisions sits inside the margin
+        assert margin.mean() < 2e-2
+    rand_codes = torch.randint(0, C, (w.B, w.H_kv, w.L, M), generator=gen, dtype=torch.uint8)
+    qd = synth.queries(w, 1, DEV, seed=w.seed * 7 + 5)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=DEV)
+    idx = torch.empty((w.B, w.H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_pq_draft_attn(qd, k, v, sl, cb, rand_codes.to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    for b in rng.choice(w.B, size=2, replace=False):
+        b = int(b)
+        sl_o = np.array([w.L], np.int32)
+        ref, idx_o, approx = oracle.pq_attn(to_u16(qd[b:b + 1]), to_u16(k[b:b + 1]), to_u16(v[b:b + 1]), sl_o,
+                                            cb[b:b + 1].cpu().numpy(), rand_codes[b:b + 1].numpy(), top_k,
+                                            want_approx=True)
+        sw, _ = check_topk_attn(bf16_out_to_f64(out[b:b + 1]), idx[b:b + 1].cpu().numpy(), ref, idx_o, approx, sl_o,
+                                top_k, f"pq b={b}")
+        assert sw <= 2
+    del k, v, cb, codes, rand_codes
     torch.cuda.empty_cache()
 
 
