@@ -103,8 +103,8 @@ def recorded_traffic(workload: str):
         return None
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith("- "):
-            key, _, val = line.strip()[2:].partition(":")
+        if ": " in line and line.strip().startswith("- "):
+            key, _, val = line.strip()[2:].partition(": ")   # keys may contain ':' (e.g. "sha256[:16]")
             vals[key.strip()] = val.strip().strip("`")
     if vals.get("workload") != workload or vals.get("attn.cu sha256[:16]") != file_sha(ATTN_SRC):
         return None

@@ -84,13 +84,16 @@ def select(tim: Timings, alpha: Dict[Tuple[str, int], float], gammas: Optional[I
 
 def calibrate(B: int, S: int, budgets: Sequence[int], gammas: Sequence[int], H_q: int = 32, H_kv: int = 8,
               d: int = 128, reps: int = 10, device: str = "cuda:0", snapkv_window: int = 32,
-              snapkv_steps: Optional[int] = None, topk: bool = False) -> Timings:
+              snapkv_steps: Optional[int] = None, topk: bool = False, pq: bool = False,
+              pq_centroids: int = 256, pq_iters: int = 2) -> Timings:
     """Measure T_T, T_V(gamma), T_D(K) (and the SnapKV selection cost spread over
     `snapkv_steps` draft steps) for one layer on the current GPU, in ms.  With
     `topk`, the Top-K attention draft is timed too: its per-step search over the
     whole cache is charged as T_select = (measured Top-K call) - T_D(K), so that
     T_D + T_select is the call's time (section 4.4: dynamic selection pays a
-    batch-dependent search at every draft step)."""
+    batch-dependent search at every draft step).  With `pq`, the PQCache-style
+    draft is charged the same way (its codebook, built once at prefill from
+    seeded key samples, is not charged per step)."""
     import torch
 
     from . import binding as mb
@@ -132,6 +135,23 @@ def calibrate(B: int, S: int, budgets: Sequence[int], gammas: Sequence[int], H_q
                 continue
             t = timed(lambda: mb.magicdec_topk_draft_attn(qd, k, v, sl, K))
             t_select[("topk", K)] = max(0.0, t - t_draft[K])
+    if pq:
+        M, C = d // 8, pq_centroids
+        gen = torch.Generator(device="cpu").manual_seed(7)
+        pick = torch.randint(0, S, (B, H_kv, C), generator=gen).to(device)
+        bidx = torch.arange(B, device=device)[:, None, None]
+        hidx = torch.arange(H_kv, device=device)[None, :, None]
+        cb = k[bidx, pick, hidx].float().reshape(B, H_kv, C, M, 8).permute(0, 1, 3, 2, 4).contiguous()
+        codes = mb.magicdec_pq_encode(k, cb)
+        for _ in range(pq_iters):
+            mb.magicdec_pq_update(k, sl, codes, cb)
+            mb.magicdec_pq_encode(k, cb, codes=codes)
+        for K in budgets:
+            if K > S:
+                continue
+            t = timed(lambda: mb.magicdec_pq_draft_attn(qd, k, v, sl, cb, codes, K))
+            t_select[("pq", K)] = max(0.0, t - t_draft[K])
+        del cb, codes
     if snapkv_steps:
         q_win = torch.randn((B, snapkv_window, H_q, d), generator=g, device=device).to(torch.bfloat16)
         for K in budgets:
@@ -155,9 +175,10 @@ def main(argv: Optional[Sequence[str]] = None) -> None:
                     help='JSON {"streaming:512": 0.8, "snapkv:2048": 0.9, ...}; default: no selection')
     ap.add_argument("--snapkv-steps", type=int, default=0)
     ap.add_argument("--topk", action="store_true", help="also time the Top-K attention draft")
+    ap.add_argument("--pq", action="store_true", help="also time the PQCache-style draft")
     args = ap.parse_args(argv)
     tim = calibrate(args.B, args.S, args.budgets, args.gammas, snapkv_steps=args.snapkv_steps or None,
-                    topk=args.topk)
+                    topk=args.topk, pq=args.pq)
     out = {"B": args.B, "S": args.S, "t_target_ms": tim.t_target, "t_verify_ms": tim.t_verify,
            "t_draft_ms": tim.t_draft, "T_V_over_T_T": {g: t / tim.t_target for g, t in tim.t_verify.items()},
            "T_D_over_T_T": {K: t / tim.t_target for K, t in tim.t_draft.items()},

@@ -99,12 +99,14 @@ def test_calibrated_times_show_the_kv_bound_regime():
 
 
 @pytest.mark.gpu
-def test_topk_draft_search_cost_dominates_at_large_batch():
-    """Section 4.4: Top-K attention keeps a small budget but searches the whole cache at every
-    draft step, so its draft cost approaches verification; with an equal acceptance rate the
-    static StreamingLLM draft wins."""
-    tim = cm.calibrate(B=32, S=32000, budgets=[512], gammas=[3], reps=3, topk=True)
-    t_topk = tim.t_draft[512] + tim.t_select[("topk", 512)]
-    assert t_topk / tim.t_target > 0.3
-    c = cm.select(tim, {("streaming", 512): 0.8, ("topk", 512): 0.8})
+def test_dynamic_draft_search_cost_dominates_at_large_batch():
+    """Section 4.4: Top-K attention and the PQCache-style draft keep a small budget but search the
+    cache at every draft step, so their draft cost is a large fraction of verification; with equal
+    acceptance rates the static StreamingLLM draft wins, and a dynamic draft needs a clearly higher
+    acceptance rate to be chosen."""
+    tim = cm.calibrate(B=32, S=32000, budgets=[512], gammas=[3], reps=3, topk=True, pq=True)
+    for method in ("topk", "pq"):
+        t_dyn = tim.t_draft[512] + tim.t_select[(method, 512)]
+        assert t_dyn / tim.t_target > 0.2, method
+    c = cm.select(tim, {("streaming", 512): 0.8, ("topk", 512): 0.8, ("pq", 512): 0.8})
     assert c.method == "streaming"

@@ -37,3 +37,14 @@ def test_expected_tokens_closed_form():
 
 def test_aggregate_rate_is_whole_job():
     assert math.isclose(bench.aggregate_rate(4, 10, 2000.0), 20.0)
+
+
+def test_recorded_traffic_is_read_from_the_committed_profile():
+    """The bench reports the verification kernel's ncu DRAM bytes from profiles/ while attn.cu is the
+    source the capture was taken on; the recorded traffic equals the algorithmic bytes within 1 %."""
+    t = bench.recorded_traffic("llama8b_b128_l32k")
+    assert t is not None
+    w = bench.synth.WORKLOADS["llama8b_b128_l32k"]
+    algorithmic = 2.0 * w.B * w.L * w.H_kv * w.d * 2 + 2.0 * w.B * w.n_q * w.H_q * w.d * 2
+    assert abs(t / algorithmic - 1.0) < 0.01
+    assert bench.recorded_traffic("tiny") is None
