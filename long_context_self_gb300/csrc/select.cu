@@ -5,12 +5,10 @@
 //    plus a recent window; pure index arithmetic.
 //  * SnapKV selection (paper section 4.4 / section 5.2), once after prefill:
 //    the observation-window scores come from the two tcgen05 passes in
-//    snapkv_tc.cu; here
-//      top-k   one CTA per (sequence, KV head): max-pool (kernel k, clipped),
-//              an 8-bit-digit MSB-first radix select of the k-th largest
-//              pooled score, then an order-preserving block compaction that
-//              keeps everything above the threshold and the smallest
-//              positions among ties; the window is appended.
+//    snapkv_tc.cu; here the prefix scores are max-pooled (kernel k, clipped),
+//    and the select kernel of topk.cu (selection-only mode) keeps the
+//    budget - window largest pooled positions (ties: the smaller position)
+//    in ascending order and appends the window.
 //  * Gather of the selected rows into the compact cache (section 4.4): 16-byte vector
 //    row copies into the head-major compact draft cache.
 #include <algorithm>
@@ -100,130 +98,24 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict_
     }
 }
 
-// ----------------------------------------------------------- pool + top-k
-__device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Exclusive block-wide prefix count of `flag` over 1024 threads; returns the
-// thread's offset and writes the block total to *total.  Uses scratch[33].
-__device__ __forceinline__ int block_excl_count(bool flag, int *scratch, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) scratch[warp] = __popc(bal);
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        int x = lane < nw ? scratch[lane] : 0;
-        const int own = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane < nw) scratch[lane] = x - own;
-        if (lane == 31) scratch[32] = x;
-    }
-    __syncthreads();
-    const int off = scratch[warp] + in_warp;
-    *total = scratch[32];
-    __syncthreads();
-    return off;
-}
-
-__global__ void __launch_bounds__(1024) snapkv_topk_kernel(const float *__restrict__ score, uint32_t *keys,
-                                                          const int32_t *__restrict__ seq_len, int H_kv,
-                                                          int L_cap, int w, int pool, int budget, int32_t *idx,
-                                                          int32_t *n_sel) {
-    __shared__ int hist[256];
-    __shared__ int scratch[40];
-    __shared__ int sel_digit, sel_remaining;
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+// ------------------------------------------------------------------ pooling
+// pooled[j] = max of the prefix scores in [j - half, j + half] clipped to
+// [0, m), m = len - w; row stride L_sc (a multiple of 4 floats).
+__global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *__restrict__ score,
+                                                         const int32_t *__restrict__ seq_len, int H_kv, int L_cap,
+                                                         int L_sc, int w, int half, float *__restrict__ pooled) {
     pdl_trigger();
     pdl_wait();
-    const int L = clamp_len_s(__ldg(seq_len + b), L_cap);
-    int32_t *out = idx + ((long long)b * H_kv + h) * budget;
-    if (L <= budget) {
-        for (int j = tid; j < budget; j += blockDim.x) out[j] = j < L ? j : -1;
-        if (h == 0 && tid == 0) n_sel[b] = L;
-        return;
-    }
-    const int m = L - w, k_top = budget - w, half = pool / 2;
-    if (k_top == 0) {
-        for (int r = tid; r < w; r += blockDim.x) out[r] = m + r;
-        if (h == 0 && tid == 0) n_sel[b] = budget;
-        return;
-    }
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int m = clamp_len_s(__ldg(seq_len + b), L_cap) - w;
     const float *sc = score + ((long long)b * H_kv + h) * L_cap;
-    uint32_t *ky = keys + ((long long)b * H_kv + h) * L_cap;
-    for (int j = tid; j < m; j += blockDim.x) {
-        float mx = -INFINITY;
+    float *out = pooled + ((long long)b * H_kv + h) * L_sc;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < m; j += gridDim.x * blockDim.x) {
         const int lo = max(0, j - half), hi = min(m - 1, j + half);
-        for (int t = lo; t <= hi; ++t) mx = fmaxf(mx, sc[t]);
-        ky[j] = order_key(mx);
+        float mx = -INFINITY;
+        for (int t = lo; t <= hi; ++t) mx = fmaxf(mx, __ldg(sc + t));
+        out[j] = mx;
     }
-    __syncthreads();
-
-    uint32_t prefix = 0, pmask = 0;
-    int remaining = k_top;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
-        for (int j = tid; j < m; j += blockDim.x) {
-            const uint32_t kk = ky[j];
-            if ((kk & pmask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            // lane l covers digits 255-8l down to 248-8l
-            int cnt[8], gsum = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) { cnt[j] = hist[255 - (tid * 8 + j)]; gsum += cnt[j]; }
-            int x = gsum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (tid >= o) x += y;
-            }
-            int above = x - gsum;
-            if (above < remaining && remaining <= x) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (above < remaining && remaining <= above + cnt[j]) {
-                        sel_digit = 255 - (tid * 8 + j);
-                        sel_remaining = remaining - above;
-                    }
-                    above += cnt[j];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= (uint32_t)sel_digit << shift;
-        pmask |= 255u << shift;
-        remaining = sel_remaining;
-        __syncthreads();
-    }
-    const uint32_t tau = prefix;
-    const int need_eq = remaining;
-
-    int sel_count = 0, eq_seen = 0;
-    for (int base = 0; base < m; base += blockDim.x) {
-        const int j = base + tid;
-        const bool valid = j < m;
-        const uint32_t kk = valid ? ky[j] : 0u;
-        const bool gt = valid && kk > tau, eq = valid && kk == tau;
-        int eq_total, take_total;
-        const int eq_rank = eq_seen + block_excl_count(eq, scratch, &eq_total);
-        const bool take = gt || (eq && eq_rank < need_eq);
-        const int pos = sel_count + block_excl_count(take, scratch, &take_total);
-        if (take && pos < k_top) out[pos] = j;
-        sel_count += take_total;
-        eq_seen += eq_total;
-    }
-    for (int r = tid; r < w; r += blockDim.x) out[k_top + r] = m + r;
-    if (h == 0 && tid == 0) n_sel[b] = budget;
 }
 
 // ------------------------------------------------------------------- host side
@@ -257,11 +149,14 @@ size_t snapkv_tc_workspace_bytes(int B, int H_q, int H_kv, int L_cap, int w);
 magicdec_status launch_snapkv_scores_tc(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
                                         const int32_t *seq_len, int w, void *ws, float **score_out, cudaStream_t st);
 
-// Workspace: [pass-1 partials][scores B x H_kv x L_cap fp32][pooled keys B x H_kv x L_cap u32]
+// Workspace: [pass-1 partials][scores B x H_kv x L_cap fp32][pooled B x H_kv x L_sc fp32]
 size_t snapkv_workspace_bytes(int B, int H_q, int H_kv, int D, int L_cap, int w) {
     (void)D;
     return snapkv_tc_workspace_bytes(B, H_q, H_kv, L_cap, w);
 }
+
+magicdec_status launch_snapkv_pick(int B, int H_kv, int L_cap, const float *pooled, const int32_t *len, int window,
+                                   int budget, int32_t *idx, int32_t *n_sel, cudaStream_t st);
 
 magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
                                      const int32_t *seq_len, int w, int pool, int budget, int32_t *idx,
@@ -269,11 +164,14 @@ magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap,
     float *score = nullptr;
     magicdec_status s = launch_snapkv_scores_tc(B, H_q, H_kv, D, L_cap, q_win, k, seq_len, w, ws, &score, st);
     if (s != MAGICDEC_OK) return s;
-    uint32_t *keys = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(score) +
-                                                  (((size_t)B * H_kv * L_cap * 4 + 255) & ~(size_t)255));
-    return magicdec_host::launch_pdl(snapkv_topk_kernel, dim3(H_kv, B), dim3(1024), 0, st,
-                                     static_cast<const float *>(score), keys, seq_len, H_kv, L_cap, w, pool, budget,
-                                     idx, n_sel);
+    const int L_sc = (L_cap + 3) & ~3;
+    float *pooled = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(score) +
+                                              (((size_t)B * H_kv * L_cap * 4 + 255) & ~(size_t)255));
+    const int per = 256 * 8;
+    s = magicdec_host::launch_pdl(snapkv_pool_kernel, dim3((L_cap + per - 1) / per, H_kv, B), dim3(256), 0, st,
+                                  static_cast<const float *>(score), seq_len, H_kv, L_cap, L_sc, w, pool / 2, pooled);
+    if (s != MAGICDEC_OK) return s;
+    return launch_snapkv_pick(B, H_kv, L_cap, pooled, seq_len, w, budget, idx, n_sel, st);
 }
 
 }  // namespace magicdec

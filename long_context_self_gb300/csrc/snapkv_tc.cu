@@ -31,7 +31,7 @@ namespace magicdec {
 
 constexpr int kTcKeys = 128;                 // keys per K tile
 constexpr int kTcChunk = 4096;               // positions per CTA
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 2;           // 2 stages: two CTAs per SM, one streams while the other sets up
 constexpr int kTcThreads = 192;
 constexpr int kTcHalf = kTcKeys * 128;       // one 128-key x 64-channel swizzled box (16 KB)
 
@@ -310,7 +310,7 @@ size_t snapkv_tc_workspace_bytes(int B, int H_q, int H_kv, int L_cap, int w) {
     const int RP = snapkv_tc_row_blocks(M) * 128;
     const int n_chunks = (L_cap + kTcChunk - 1) / kTcChunk;
     return align256t((size_t)B * H_kv * n_chunks * RP * 2 * 4) + align256t((size_t)B * H_kv * L_cap * 4) +
-           align256t((size_t)B * H_kv * L_cap * 4);
+           align256t((size_t)B * H_kv * (size_t)((L_cap + 3) & ~3) * 4);
 }
 
 template <int D, int PASS>

@@ -39,6 +39,7 @@ constexpr int kTkNW = kTkNT / 32;
 constexpr int kTkBins = 4096;
 constexpr int kTkMaxTopK = 8192;
 constexpr int kTkMaxGroup = 8;                   // query heads per KV head (the mma N extent)
+constexpr int kSelScores = 0, kSelExact = 1, kSelOnly = 2;   // modes of the select kernel
 
 struct TopkScoreParams {
     const __nv_bfloat16 *q;   // [B, 1, H_q, D]
@@ -60,6 +61,8 @@ struct TopkSelParams {
     int B, H_q, H_kv, G, L_cap, L_sc, top_k;
     int cand_cap;             // shared-memory candidate slots
     float scale;              // 1/sqrt(D) (exact-score mode)
+    int len_sub;              // kSelOnly: window length kept after the selected prefix
+    int32_t *n_sel;           // kSelOnly: [B] kept count
 };
 
 __device__ __forceinline__ int tk_clamp_len(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
@@ -367,12 +370,16 @@ __device__ void tk_select_full_row(const float *srow, int len, int top_k, int d1
     (void)top_k;
 }
 
-// EXACT = false: the selection scores are the exact scaled scores (Top-K
-// attention) and weight the kept rows directly.  EXACT = true: they are
+// MODE kSelScores: the selection scores are the exact scaled scores (Top-K
+// attention) and weight the kept rows directly.  kSelExact: they are
 // approximate (PQ lookup sums) and only choose the rows; the kept rows' exact
-// scores are recomputed from K before the softmax.
-template <int D, bool EXACT>
+// scores are recomputed from K before the softmax.  kSelOnly (SnapKV): rows
+// are (sequence, KV head) pooled-score rows; the budget - len_sub largest of
+// the first len - len_sub positions are kept and the last len_sub positions
+// (the observation window) appended; no attention.
+template <int D, int MODE>
 __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSelParams p) {
+    constexpr bool EXACT = MODE == kSelExact;
     constexpr int NW = kTkNW;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     int *hist = reinterpret_cast<int *>(smem_raw);                    // [4096]; later [NW][D] partial outputs
@@ -380,6 +387,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     uint32_t *cand_key = reinterpret_cast<uint32_t *>(cand_pos + p.cand_cap);   // [cand_cap]
     int *sel = reinterpret_cast<int *>(cand_key + p.cand_cap);        // [top_k]
     float *ex = reinterpret_cast<float *>(sel + ((p.top_k + 3) & ~3)); // [top_k] exact scores (EXACT)
+    // (in kSelOnly mode p.top_k is the budget, an upper bound of the kept count)
     __shared__ int wsum[32], woff[NW], wcnt[NW];
     __shared__ float s_exmax[NW];
     __shared__ int s_digit, s_rem, s_total, s_over;
@@ -390,20 +398,35 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
     pdl_wait();
-    const int len = tk_clamp_len(__ldg(p.len + b), p.L_cap);
+    const int full = tk_clamp_len(__ldg(p.len + b), p.L_cap);
     const int kvh = hq / p.G;
     const long long row = (long long)b * p.H_q + hq;
     const float *srow = p.score + row * p.L_sc;
-    __nv_bfloat16 *o = p.out + row * D;
+    __nv_bfloat16 *o = MODE == kSelOnly ? nullptr : p.out + row * D;
     int32_t *idx_row = p.idx ? p.idx + row * p.top_k : nullptr;
-    const int n = min(len, p.top_k);
+    int len = full, top_k = p.top_k;
+    if (MODE == kSelOnly) {
+        // SnapKV: everything when the sequence fits the budget; else the
+        // window is always kept and budget - window prefix positions compete
+        const int budget = p.top_k, w = p.len_sub;
+        if (full <= budget || budget == w) {
+            const int keep_from = full <= budget ? 0 : full - w;
+            const int n_keep = full - keep_from;
+            for (int i = tid; i < budget; i += kTkNT) idx_row[i] = i < n_keep ? keep_from + i : -1;
+            if (hq == 0 && tid == 0) p.n_sel[b] = n_keep;
+            return;
+        }
+        len = full - w;
+        top_k = budget - w;
+    }
+    const int n = min(len, top_k);
     if (len == 0) {
         for (int c = tid; c < D; c += kTkNT) o[c] = __float2bfloat16(0.f);
         if (idx_row)
-            for (int i = tid; i < p.top_k; i += kTkNT) idx_row[i] = -1;
+            for (int i = tid; i < top_k; i += kTkNT) idx_row[i] = -1;
         return;
     }
-    const bool select = len > p.top_k;
+    const bool select = len > top_k;
     // warp w owns positions [lo, hi): contiguous segments keep the ascending order
     const int seg = (((len + NW - 1) / NW) + 3) & ~3;
     const int lo = min(len, warp * seg), hi = min(len, lo + seg);
@@ -433,7 +456,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
 
     if (select) {
         int d1, rem1;
-        tk_find_digit(hist, p.top_k, wsum, &s_digit, &s_rem, d1, rem1);
+        tk_find_digit(hist, top_k, wsum, &s_digit, &s_rem, d1, rem1);
         // 2. candidates = positions whose first digit is >= d1.  One L2 re-read;
         //    warp w appends its segment's candidates, in ascending order, to its
         //    own R slots of the list.
@@ -489,7 +512,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
         __syncthreads();
         const int n_cand = s_total;
         if (s_over) {
-            tk_select_full_row(srow, len, p.top_k, d1, rem1, hist, sel, wsum, &s_digit, &s_rem);
+            tk_select_full_row(srow, len, top_k, d1, rem1, hist, sel, wsum, &s_digit, &s_rem);
         } else {
             // 3. the last two digits, over the candidates of bin d1 only
             int d2, d3, rem;
@@ -549,6 +572,12 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
         for (int i = tid; i < len; i += kTkNT) sel[i] = i;
     }
     __syncthreads();
+    if (MODE == kSelOnly) {
+        // kept prefix positions (ascending), then the window [len, full)
+        for (int i = tid; i < p.top_k; i += kTkNT) idx_row[i] = i < n ? sel[i] : (i < n + (full - len) ? len + (i - n) : -1);
+        if (hq == 0 && tid == 0) p.n_sel[b] = n + (full - len);
+        return;
+    }
 
     // 5. softmax over the kept scores (the largest key is always kept) and the
     //    weighted sum of their V rows.  A V row is LPR lanes x 16 bytes, so one
@@ -682,13 +711,15 @@ size_t topk_workspace_bytes(int B, int H_q, int L_cap) {
 // Selection + attention kernel: candidates are the top_k plus room for the
 // threshold bin's other members.
 template <int D>
-static magicdec_status launch_select_attn(TopkSelParams tp, bool exact, cudaStream_t st) {
+static magicdec_status launch_select_attn(TopkSelParams tp, int mode, cudaStream_t st) {
     const int smem_cap = magicdec_host::max_smem_optin();
     tp.cand_cap = tp.top_k + 4096;
     const size_t k4 = (size_t)((tp.top_k + 3) & ~3) * 4;
-    const size_t smem2 = (size_t)kTkBins * 4 + (size_t)tp.cand_cap * 8 + k4 + (exact ? k4 : 0);
+    const size_t smem2 = (size_t)kTkBins * 4 + (size_t)tp.cand_cap * 8 + k4 + (mode == kSelExact ? k4 : 0);
     if (smem2 + 2048 > (size_t)smem_cap) return MAGICDEC_ERR_UNSUPPORTED;
-    auto k2 = exact ? topk_select_attn_kernel<D, true> : topk_select_attn_kernel<D, false>;
+    auto k2 = mode == kSelExact  ? topk_select_attn_kernel<D, kSelExact>
+              : mode == kSelOnly ? topk_select_attn_kernel<D, kSelOnly>
+                                 : topk_select_attn_kernel<D, kSelScores>;
     if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
         return MAGICDEC_ERR_CUDA;
     return magicdec_host::launch_pdl(k2, dim3(tp.H_q, tp.B), dim3(kTkNT), smem2, st, tp);
@@ -714,7 +745,7 @@ static magicdec_status launch_topk_impl(const TopkScoreParams &sp, const TopkSel
                                                   dim3((kTkConsumers + 1) * 32), smem1, st, tmk, s1);
     if (s != MAGICDEC_OK) return s;
 
-    return launch_select_attn<D>(tp, false, st);
+    return launch_select_attn<D>(tp, kSelScores, st);
 }
 
 magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,
@@ -787,9 +818,30 @@ magicdec_status launch_topk_select_attn(int B, int H_q, int H_kv, int D, int L_c
     tp.L_sc = tk_row_stride(L_cap);
     tp.top_k = top_k;
     tp.scale = 1.0f / sqrtf((float)D);
-    if (D == 128) return launch_select_attn<128>(tp, exact, st);
-    if (D == 64) return launch_select_attn<64>(tp, exact, st);
+    if (D == 128) return launch_select_attn<128>(tp, exact ? kSelExact : kSelScores, st);
+    if (D == 64) return launch_select_attn<64>(tp, exact ? kSelExact : kSelScores, st);
     return MAGICDEC_ERR_UNSUPPORTED;
+}
+
+// SnapKV selection over pooled prefix scores [B, H_kv, L_cap rounded to 4]:
+// rows (sequence, KV head); keeps budget - window prefix positions, appends
+// the window; idx [B, H_kv, budget], n_sel [B].
+magicdec_status launch_snapkv_pick(int B, int H_kv, int L_cap, const float *pooled, const int32_t *len, int window,
+                                   int budget, int32_t *idx, int32_t *n_sel, cudaStream_t st) {
+    TopkSelParams tp{};
+    tp.score = pooled;
+    tp.len = len;
+    tp.idx = idx;
+    tp.n_sel = n_sel;
+    tp.B = B;
+    tp.H_q = H_kv;        // one row per (sequence, KV head)
+    tp.H_kv = H_kv;
+    tp.G = 1;
+    tp.L_cap = L_cap;
+    tp.L_sc = tk_row_stride(L_cap);
+    tp.top_k = budget;
+    tp.len_sub = window;
+    return launch_select_attn<128>(tp, kSelOnly, st);
 }
 
 }  // namespace magicdec
