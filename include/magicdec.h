@@ -115,7 +115,7 @@ MAGICDEC_API size_t magicdec_snapkv_workspace_size(magicdec_kv_shape shape, int 
  *   ws    workspace of magicdec_snapkv_workspace_size(shape, window) bytes
  * Errors: NULL pointers, bad shape, window <= 0, budget < window,
  * pool_kernel even or <= 0, alignment, workspace too small;
- * MAGICDEC_ERR_UNSUPPORTED when window * (H_q/H_kv) > 256.
+ * MAGICDEC_ERR_UNSUPPORTED when window * (H_q/H_kv) > 256 or pool_kernel > 9.
  */
 MAGICDEC_API magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, const uint16_t *q_win, const uint16_t *k,
                                        const int32_t *seq_len, int window, int pool_kernel, int budget,

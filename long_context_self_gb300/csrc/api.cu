@@ -172,6 +172,7 @@ magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, const uint16_t *
     if (!q_win || !k || !seq_len || !idx || !n_sel || !ws) return MAGICDEC_ERR_NULL;
     if (!shape_ok(shape) || window <= 0 || budget < window || pool_kernel <= 0 || (pool_kernel & 1) == 0)
         return MAGICDEC_ERR_SHAPE;
+    if (pool_kernel > 9) return MAGICDEC_ERR_UNSUPPORTED;
     if ((long long)window * (shape.H_q / shape.H_kv) > 256) return MAGICDEC_ERR_UNSUPPORTED;
     if (!aligned16(q_win) || !aligned16(k) || !aligned16(ws)) return MAGICDEC_ERR_ALIGN;
     if (ws_bytes < magicdec_snapkv_workspace_size(shape, window)) return MAGICDEC_ERR_WORKSPACE;

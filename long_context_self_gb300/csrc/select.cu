@@ -100,7 +100,9 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict_
 
 // ------------------------------------------------------------------ pooling
 // pooled[j] = max of the prefix scores in [j - half, j + half] clipped to
-// [0, m), m = len - w; row stride L_sc (a multiple of 4 floats).
+// [0, m), m = len - w (half <= 4); row stride L_sc (a multiple of 4 floats).
+// A thread pools 4 consecutive positions 4t..4t+3 from the three aligned
+// float4 groups around them.
 __global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *__restrict__ score,
                                                          const int32_t *__restrict__ seq_len, int H_kv, int L_cap,
                                                          int L_sc, int w, int half, float *__restrict__ pooled) {
@@ -110,11 +112,23 @@ __global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *__restric
     const int m = clamp_len_s(__ldg(seq_len + b), L_cap) - w;
     const float *sc = score + ((long long)b * H_kv + h) * L_cap;
     float *out = pooled + ((long long)b * H_kv + h) * L_sc;
-    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < m; j += gridDim.x * blockDim.x) {
-        const int lo = max(0, j - half), hi = min(m - 1, j + half);
-        float mx = -INFINITY;
-        for (int t = lo; t <= hi; ++t) mx = fmaxf(mx, __ldg(sc + t));
-        out[j] = mx;
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; 4 * g < m; g += gridDim.x * blockDim.x) {
+        const int j0 = 4 * g;
+        float x[12];                                  // positions j0-4 .. j0+7, -inf outside [0, m)
+#pragma unroll
+        for (int e = 0; e < 12; ++e) {
+            const int t = j0 - 4 + e;
+            x[e] = (t >= 0 && t < m) ? __ldg(sc + t) : -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (j0 + e >= m) break;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int o = -4; o <= 4; ++o)
+                if (o >= -half && o <= half) mx = fmaxf(mx, x[4 + e + o]);
+            out[j0 + e] = mx;
+        }
     }
 }
 
@@ -161,13 +175,14 @@ magicdec_status launch_snapkv_pick(int B, int H_kv, int L_cap, const float *pool
 magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
                                      const int32_t *seq_len, int w, int pool, int budget, int32_t *idx,
                                      int32_t *n_sel, void *ws, cudaStream_t st) {
+    if (pool / 2 > 4) return MAGICDEC_ERR_UNSUPPORTED;   // before anything is launched
     float *score = nullptr;
     magicdec_status s = launch_snapkv_scores_tc(B, H_q, H_kv, D, L_cap, q_win, k, seq_len, w, ws, &score, st);
     if (s != MAGICDEC_OK) return s;
     const int L_sc = (L_cap + 3) & ~3;
     float *pooled = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(score) +
                                               (((size_t)B * H_kv * L_cap * 4 + 255) & ~(size_t)255));
-    const int per = 256 * 8;
+    const int per = 256 * 4 * 4;                      // positions per CTA: 4 per thread, 4 grid-stride steps
     s = magicdec_host::launch_pdl(snapkv_pool_kernel, dim3((L_cap + per - 1) / per, H_kv, B), dim3(256), 0, st,
                                   static_cast<const float *>(score), seq_len, H_kv, L_cap, L_sc, w, pool / 2, pooled);
     if (s != MAGICDEC_OK) return s;
