@@ -122,6 +122,22 @@ MAGICDEC_API magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, con
                                        int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * SnapKV selection with a budget per sequence (heterogeneous batches; paper
+ * section 4.3 discusses draft budgets per sequence length).  As
+ * magicdec_snapkv_select, except that sequence b keeps budgets[b] positions
+ * (device int32 [B], clamped to [window, max_budget]) and idx rows have
+ * max_budget entries ([B, H_kv, max_budget], -1 after n_sel[b]); the gather
+ * and the draft attention then take n_idx = cap = max_budget and
+ * draft_len = n_sel.
+ * Errors: as magicdec_snapkv_select, with max_budget in the role of budget.
+ */
+MAGICDEC_API magicdec_status magicdec_snapkv_select_budgets(magicdec_kv_shape shape, const uint16_t *q_win,
+                                                            const uint16_t *k, const int32_t *seq_len, int window,
+                                                            int pool_kernel, const int32_t *budgets, int max_budget,
+                                                            int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes,
+                                                            void *stream);
+
+/*
  * Gather of the selected rows into the compact draft cache (paper section
  * 4.4: the static selections copy their rows into a compact cache once).
  *   k, v   [B, L_cap, H_kv, d] bf16;  idx [B, H_kv, n_idx] int32

@@ -43,6 +43,7 @@ _SIGNATURES = {
     "magicdec_streaming_select": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
     "magicdec_snapkv_workspace_size": ([KVShape, _I], _S),
     "magicdec_snapkv_select": ([KVShape, _P, _P, _P, _I, _I, _I, _P, _P, _P, _S, _P], _I),
+    "magicdec_snapkv_select_budgets": ([KVShape, _P, _P, _P, _I, _I, _P, _I, _P, _P, _P, _S, _P], _I),
     "magicdec_gather_kv": ([KVShape, _P, _P, _P, _I, _I, _P, _P, _P], _I),
     "magicdec_attn_workspace_size": ([KVShape, _I], _S),
     "magicdec_draft_attn": ([KVShape, _P, _P, _P, _P, _P, _P, _S, _P], _I),
@@ -182,6 +183,39 @@ def magicdec_snapkv_select(q_win: torch.Tensor, k: torch.Tensor, seq_len: torch.
            lib().magicdec_snapkv_select(shape, _ptr(q_win), _ptr(k), _ptr(seq_len), window, pool_kernel, budget,
                                         _ptr(idx), _ptr(n_sel), _ptr(ws), ws.numel() * ws.element_size(),
                                         _stream(stream, dev)))
+    return idx, n_sel
+
+
+def magicdec_snapkv_select_budgets(q_win: torch.Tensor, k: torch.Tensor, seq_len: torch.Tensor, window: int,
+                                   pool_kernel: int, budgets: torch.Tensor, max_budget: int,
+                                   idx: Optional[torch.Tensor] = None, n_sel: Optional[torch.Tensor] = None,
+                                   ws: Optional[torch.Tensor] = None,
+                                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """SnapKV selection with per-sequence budgets (int32 [B], clamped to [window, max_budget])
+    -> (idx int32 [B, H_kv, max_budget], n_sel int32 [B])."""
+    _need(q_win, "q_win", torch.bfloat16)
+    dev = q_win.device
+    _need(k, "k", torch.bfloat16, dev)
+    _need(seq_len, "seq_len", torch.int32, dev)
+    _need(budgets, "budgets", torch.int32, dev)
+    B, w, H_q, d = q_win.shape
+    L_cap, H_kv = k.shape[1], k.shape[2]
+    if w != window:
+        raise ValueError("q_win must hold `window` query rows")
+    shape = kv_shape(B, H_q, H_kv, d, L_cap)
+    if idx is None:
+        idx = torch.empty((B, H_kv, max_budget), dtype=torch.int32, device=dev)
+    if n_sel is None:
+        n_sel = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(n_sel, "n_sel", torch.int32, dev)
+    if ws is None:
+        ws = workspace(magicdec_snapkv_workspace_size(shape, window), dev, "snapkv")
+    _check("magicdec_snapkv_select_budgets",
+           lib().magicdec_snapkv_select_budgets(shape, _ptr(q_win), _ptr(k), _ptr(seq_len), int(window),
+                                                int(pool_kernel), _ptr(budgets), int(max_budget), _ptr(idx),
+                                                _ptr(n_sel), _ptr(ws), ws.numel() * ws.element_size(),
+                                                _stream(stream, dev)))
     return idx, n_sel
 
 

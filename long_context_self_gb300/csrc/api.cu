@@ -34,8 +34,8 @@ magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *
                                  const int32_t *idx, int n_idx, int cap, void *kc, void *vc, cudaStream_t st);
 size_t snapkv_workspace_bytes(int B, int H_q, int H_kv, int D, int L_cap, int w);
 magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
-                                     const int32_t *seq_len, int w, int pool, int budget, int32_t *idx,
-                                     int32_t *n_sel, void *ws, cudaStream_t st);
+                                     const int32_t *seq_len, int w, int pool, int budget, const int32_t *budgets,
+                                     int32_t *idx, int32_t *n_sel, void *ws, cudaStream_t st);
 size_t accept_workspace_bytes(int B, int gamma, int V);
 magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target, const float *draft,
                                    const int32_t *draft_tok, const float *u_acc, const float *u_res, int greedy,
@@ -166,9 +166,9 @@ size_t magicdec_snapkv_workspace_size(magicdec_kv_shape shape, int window) {
     return magicdec::snapkv_workspace_bytes(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, window);
 }
 
-magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, const uint16_t *q_win, const uint16_t *k,
-                                       const int32_t *seq_len, int window, int pool_kernel, int budget,
-                                       int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes, void *stream) {
+static magicdec_status snapkv_common(const magicdec_kv_shape &shape, const uint16_t *q_win, const uint16_t *k,
+                                     const int32_t *seq_len, int window, int pool_kernel, int budget,
+                                     const int32_t *idx, const int32_t *n_sel, const void *ws, size_t ws_bytes) {
     if (!q_win || !k || !seq_len || !idx || !n_sel || !ws) return MAGICDEC_ERR_NULL;
     if (!shape_ok(shape) || window <= 0 || budget < window || pool_kernel <= 0 || (pool_kernel & 1) == 0)
         return MAGICDEC_ERR_SHAPE;
@@ -176,8 +176,29 @@ magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, const uint16_t *
     if ((long long)window * (shape.H_q / shape.H_kv) > 256) return MAGICDEC_ERR_UNSUPPORTED;
     if (!aligned16(q_win) || !aligned16(k) || !aligned16(ws)) return MAGICDEC_ERR_ALIGN;
     if (ws_bytes < magicdec_snapkv_workspace_size(shape, window)) return MAGICDEC_ERR_WORKSPACE;
+    return MAGICDEC_OK;
+}
+
+magicdec_status magicdec_snapkv_select(magicdec_kv_shape shape, const uint16_t *q_win, const uint16_t *k,
+                                       const int32_t *seq_len, int window, int pool_kernel, int budget,
+                                       int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes, void *stream) {
+    magicdec_status s = snapkv_common(shape, q_win, k, seq_len, window, pool_kernel, budget, idx, n_sel, ws, ws_bytes);
+    if (s != MAGICDEC_OK) return s;
     return magicdec::launch_snapkv_select(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, q_win, k, seq_len,
-                                          window, pool_kernel, budget, idx, n_sel, ws,
+                                          window, pool_kernel, budget, nullptr, idx, n_sel, ws,
+                                          static_cast<cudaStream_t>(stream));
+}
+
+magicdec_status magicdec_snapkv_select_budgets(magicdec_kv_shape shape, const uint16_t *q_win, const uint16_t *k,
+                                               const int32_t *seq_len, int window, int pool_kernel,
+                                               const int32_t *budgets, int max_budget, int32_t *idx, int32_t *n_sel,
+                                               void *ws, size_t ws_bytes, void *stream) {
+    if (!budgets) return MAGICDEC_ERR_NULL;
+    magicdec_status s =
+        snapkv_common(shape, q_win, k, seq_len, window, pool_kernel, max_budget, idx, n_sel, ws, ws_bytes);
+    if (s != MAGICDEC_OK) return s;
+    return magicdec::launch_snapkv_select(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, q_win, k, seq_len,
+                                          window, pool_kernel, max_budget, budgets, idx, n_sel, ws,
                                           static_cast<cudaStream_t>(stream));
 }
 

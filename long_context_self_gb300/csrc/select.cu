@@ -170,11 +170,11 @@ size_t snapkv_workspace_bytes(int B, int H_q, int H_kv, int D, int L_cap, int w)
 }
 
 magicdec_status launch_snapkv_pick(int B, int H_kv, int L_cap, const float *pooled, const int32_t *len, int window,
-                                   int budget, int32_t *idx, int32_t *n_sel, cudaStream_t st);
+                                   int budget, const int32_t *budgets, int32_t *idx, int32_t *n_sel, cudaStream_t st);
 
 magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap, const void *q_win, const void *k,
-                                     const int32_t *seq_len, int w, int pool, int budget, int32_t *idx,
-                                     int32_t *n_sel, void *ws, cudaStream_t st) {
+                                     const int32_t *seq_len, int w, int pool, int budget, const int32_t *budgets,
+                                     int32_t *idx, int32_t *n_sel, void *ws, cudaStream_t st) {
     if (pool / 2 > 4) return MAGICDEC_ERR_UNSUPPORTED;   // before anything is launched
     float *score = nullptr;
     magicdec_status s = launch_snapkv_scores_tc(B, H_q, H_kv, D, L_cap, q_win, k, seq_len, w, ws, &score, st);
@@ -186,7 +186,7 @@ magicdec_status launch_snapkv_select(int B, int H_q, int H_kv, int D, int L_cap,
     s = magicdec_host::launch_pdl(snapkv_pool_kernel, dim3((L_cap + per - 1) / per, H_kv, B), dim3(256), 0, st,
                                   static_cast<const float *>(score), seq_len, H_kv, L_cap, L_sc, w, pool / 2, pooled);
     if (s != MAGICDEC_OK) return s;
-    return launch_snapkv_pick(B, H_kv, L_cap, pooled, seq_len, w, budget, idx, n_sel, st);
+    return launch_snapkv_pick(B, H_kv, L_cap, pooled, seq_len, w, budget, budgets, idx, n_sel, st);
 }
 
 }  // namespace magicdec

@@ -63,6 +63,7 @@ struct TopkSelParams {
     float scale;              // 1/sqrt(D) (exact-score mode)
     int len_sub;              // kSelOnly: window length kept after the selected prefix
     int32_t *n_sel;           // kSelOnly: [B] kept count
+    const int32_t *budgets;   // kSelOnly: [B] per-sequence budgets (null: top_k for all)
 };
 
 __device__ __forceinline__ int tk_clamp_len(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
@@ -408,11 +409,12 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     if (MODE == kSelOnly) {
         // SnapKV: everything when the sequence fits the budget; else the
         // window is always kept and budget - window prefix positions compete
-        const int budget = p.top_k, w = p.len_sub;
+        const int w = p.len_sub;
+        const int budget = p.budgets ? min(max(__ldg(p.budgets + b), w), p.top_k) : p.top_k;
         if (full <= budget || budget == w) {
             const int keep_from = full <= budget ? 0 : full - w;
             const int n_keep = full - keep_from;
-            for (int i = tid; i < budget; i += kTkNT) idx_row[i] = i < n_keep ? keep_from + i : -1;
+            for (int i = tid; i < p.top_k; i += kTkNT) idx_row[i] = i < n_keep ? keep_from + i : -1;
             if (hq == 0 && tid == 0) p.n_sel[b] = n_keep;
             return;
         }
@@ -825,10 +827,12 @@ magicdec_status launch_topk_select_attn(int B, int H_q, int H_kv, int D, int L_c
 
 // SnapKV selection over pooled prefix scores [B, H_kv, L_cap rounded to 4]:
 // rows (sequence, KV head); keeps budget - window prefix positions, appends
-// the window; idx [B, H_kv, budget], n_sel [B].
+// the window; idx [B, H_kv, budget], n_sel [B].  With `budgets`, sequence b
+// keeps budgets[b] (clamped to [window, budget]) and `budget` is the stride.
 magicdec_status launch_snapkv_pick(int B, int H_kv, int L_cap, const float *pooled, const int32_t *len, int window,
-                                   int budget, int32_t *idx, int32_t *n_sel, cudaStream_t st) {
+                                   int budget, const int32_t *budgets, int32_t *idx, int32_t *n_sel, cudaStream_t st) {
     TopkSelParams tp{};
+    tp.budgets = budgets;
     tp.score = pooled;
     tp.len = len;
     tp.idx = idx;

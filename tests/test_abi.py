@@ -80,6 +80,10 @@ def test_null_and_shape_errors_are_reported_before_launch(lib):
     assert lib.magicdec_snapkv_select(shape(), FAKE, FAKE, FAKE, 32, 6, 64, FAKE, FAKE, FAKE, 1 << 40, NULL) == -2
     assert lib.magicdec_snapkv_select(shape(), FAKE, FAKE, FAKE, 32, 7, 64, FAKE, FAKE, FAKE, 16, NULL) == -4
     assert lib.magicdec_snapkv_select(shape(), FAKE, FAKE, FAKE, 32, 11, 64, FAKE, FAKE, FAKE, 1 << 40, NULL) == -5
+    assert lib.magicdec_snapkv_select_budgets(shape(), FAKE, FAKE, FAKE, 32, 7, NULL, 64, FAKE, FAKE, FAKE, 1 << 40,
+                                              NULL) == -1
+    assert lib.magicdec_snapkv_select_budgets(shape(), FAKE, FAKE, FAKE, 32, 7, FAKE, 16, FAKE, FAKE, FAKE, 1 << 40,
+                                              NULL) == -2
     assert lib.magicdec_spec_accept(4, 3, 100, FAKE, NULL, FAKE, FAKE, FAKE, 0, FAKE, FAKE, NULL, FAKE,
                                     1 << 30, NULL) == -1
     assert lib.magicdec_spec_accept(0, 3, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, NULL, FAKE,

@@ -419,6 +419,29 @@ def test_topk_draft_attn_all_scores_equal():
     check_attention(bf16_out_to_f64(out), ref, "topk all-equal")
 
 
+def test_snapkv_select_with_a_budget_per_sequence():
+    """Heterogeneous budgets in one batch: each sequence equals the oracle run at its own budget
+    (band rule), rows padded with -1 to the largest budget."""
+    B, H_q, H_kv, d, L_cap, w, pool = 4, 32, 8, 128, 3000, 32, 7
+    budgets = np.array([512, 96, 32, 700], np.int32)
+    lens = np.array([3000, 2500, 2000, 600], np.int32)          # the last is shorter than its budget
+    wl = synth.Workload("case", B=B, H_q=H_q, H_kv=H_kv, d=d, L=L_cap, gamma=1, V=8, snap_window=w,
+                        snap_pool=pool, snap_budget=512, heavy_frac=0.005, seed=23)
+    k, _, dirs = synth.kv_cache(wl, "cpu")
+    q_win = synth.window_queries(wl, "cpu", heavy_dirs=dirs)
+    max_budget = int(budgets.max())
+    idx, n_sel = mb.magicdec_snapkv_select_budgets(q_win.to(DEV), k.to(DEV), torch.from_numpy(lens).to(DEV), w, pool,
+                                                   torch.from_numpy(budgets).to(DEV), max_budget)
+    torch.cuda.synchronize()
+    g_idx, g_n = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for b in range(B):
+        bud = int(budgets[b])
+        idx_o, n_sel_o, pooled = oracle.snapkv_select(to_u16(q_win[b:b + 1]), to_u16(k[b:b + 1]), lens[b:b + 1],
+                                                      pool, bud)
+        check_topk(g_idx[b:b + 1, :, :bud], g_n[b:b + 1], idx_o, n_sel_o, pooled, lens[b:b + 1], w, bud)
+        assert np.all(g_idx[b, :, bud:] == -1)
+
+
 # ------------------------------------------------------------------ acceptance
 ACCEPT_CASES = [
     ("tiny", 64, False), ("tiny", 64, True),
