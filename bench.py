@@ -557,26 +557,36 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dra_gbs = dbytes / (dra_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
 
-    def row(nbytes, ms):
+    def row(nbytes, ms, bound="hbm"):
         gbs = nbytes / (ms * 1e-3) / 1e9
         return {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "us": round(ms * 1e3, 2),
-                "algorithmic_bytes": nbytes}
+                "algorithmic_bytes": nbytes, "bound": bound}
     sg_bytes = 2.0 * 2 * w.B * pipe.cap * w.H_kv * w.d * 2       # gather: read + write K and V rows
     rows = {"verify_attn": row(vbytes, ver_ms), "draft_attn": row(dbytes, dra_ms),
             "streaming_select+gather_kv": row(sg_bytes, sel_ms), "spec_accept": row(pipe.accept_bytes(), acc_ms),
             "draft_cache_update (gamma appends + post-verification update, per layer)":
-                row(pipe.ring_update_bytes(), ring_ms)}
+                row(pipe.ring_update_bytes(), ring_ms, "launch latency (6 MB of row copies in 4 launches)")}
     if snap:
         rows["snapkv_select (once per prefill)"] = row(snap.pop("_snap_bytes"), snap.pop("_snap_ms"))
     if pq:
         pq_ms = pq.pop("_pq_ms")
-        rows["pq_draft_attn (LUT scores + select + exact attend, per draft step)"] = row(pq.pop("_pq_bytes"), pq_ms)
-        rows["pq_build (2 Lloyd iterations + encode, once per prefill)"] = row(pq.pop("_pq_build_bytes"),
-                                                                               pq.pop("_pq_build_ms"))
+        rows["pq_draft_attn (LUT scores + select + exact attend, per draft step)"] = row(
+            pq.pop("_pq_bytes"), pq_ms, "shared-memory lookup-table reads (score pass); latency (select)")
+        b_ms = pq.pop("_pq_build_ms")
+        rows["pq_build (2 Lloyd iterations + encode, once per prefill)"] = row(
+            pq.pop("_pq_build_bytes"), b_ms, "fp32 FMA (encode: nearest of C centroids per subspace)")
+        # encode: per (position, KV head, subspace, centroid) an 8-term dot product and a norm term
+        fl = 3.0 * w.B * w.L * w.H_kv * pq["pq_M"] * pq["pq_C"] * 9 * 2
+        alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        rows["pq_build (2 Lloyd iterations + encode, once per prefill)"]["alu"] = {
+            "tflops": round(fl / (b_ms * 1e-3) / 1e12, 2), "peak_tflops": round(alu_peak, 1),
+            "frac": round(fl / (b_ms * 1e-3) / 1e12 / alu_peak, 4),
+            "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz (nominal)"}
         pq["pq_over_verify"] = round(pq_ms / ver_ms, 4)
     if topk:
         tk_ms = topk.pop("_topk_ms")
-        rows["topk_draft_attn (scores + select + attend, per draft step)"] = row(topk.pop("_topk_bytes"), tk_ms)
+        rows["topk_draft_attn (scores + select + attend, per draft step)"] = row(
+            topk.pop("_topk_bytes"), tk_ms, "hbm (score pass, 0.93); latency (select)")
         topk["topk_over_verify"] = round(tk_ms / ver_ms, 4)
     result = {
         "metric": METRIC,
