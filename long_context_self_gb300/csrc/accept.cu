@@ -279,6 +279,17 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x;
     const int gamma = p.gamma, V = p.V;
+    // the draft tokens' target and draft logits, loaded before the record merge
+    // so that their latency overlaps it (warp 0, one position per lane)
+    float xt = 0.f, xd = 0.f;
+    int xtok = -1;
+    if (!p.greedy && warp == 0 && lane < gamma) {
+        xtok = __ldg(p.draft_tok + (long long)b * gamma + lane);
+        if (xtok >= 0 && xtok < V) {
+            xt = __ldg(row_ptr(p, b, lane) + xtok);
+            xd = __ldg(row_ptr(p, b, gamma + 1 + lane) + xtok);
+        }
+    }
     for (int r = warp; r < p.rows_per_b; r += kChainThreads / 32) {
         const RowStat *src = p.stats + ((long long)b * p.rows_per_b + r) * p.n_stat_chunks;
         float m = -INFINITY, t1 = -INFINITY, t2 = -INFINITY;
@@ -309,14 +320,14 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
     if (warp != 0) return;
     if (!p.greedy) {
         // ratio_i = p_i(x_i) / q_i(x_i); okq0: 1 = accept (q = 0 < p), 2 = reject
-        for (int i = lane; i < gamma; i += 32) {
-            const int x = __ldg(p.draft_tok + (long long)b * gamma + i);
+        if (lane < gamma) {               // gamma <= 32: position i = lane, logits prefetched
+            const int i = lane;
             double rt = -1.0;
             int oq = 0;
-            if (x >= 0 && x < V) {
+            if (xtok >= 0 && xtok < V) {
                 const RowAll ts = rs[i], ds = rs[gamma + 1 + i];
-                const double px = exp((double)__ldg(row_ptr(p, b, i) + x) - (double)ts.m) / ts.s;
-                const double qx = exp((double)__ldg(row_ptr(p, b, gamma + 1 + i) + x) - (double)ds.m) / ds.s;
+                const double px = exp((double)xt - (double)ts.m) / ts.s;
+                const double qx = exp((double)xd - (double)ds.m) / ds.s;
                 if (qx > 0.0) rt = px / qx;
                 else oq = px > 0.0 ? 1 : 2;
             } else {
@@ -600,10 +611,17 @@ __global__ void __launch_bounds__(kChkThreads) accept_chunk_kernel(const AcceptP
     acc = warp_sum_df(acc_done(acc));
     if (lane == 0) wred[warp] = acc;
     __syncthreads();
-    if (tid == 0) {
-        dflt t = wred[0];
-        for (int i = 1; i < kChkThreads / 32; ++i) t = df_add(t, wred[i]);
-        p.chunk_sum[(long long)b * p.n_chunks + c] = df_to_double(t);
+    if (warp == 0) {
+        // the 8 warp sums, combined by a fixed shuffle tree
+        dflt t = lane < kChkThreads / 32 ? wred[lane] : dflt{0.f, 0.f};
+#pragma unroll
+        for (int o = (kChkThreads / 32) / 2; o > 0; o >>= 1) {
+            dflt u;
+            u.hi = __shfl_down_sync(0xffffffffu, t.hi, o);
+            u.lo = __shfl_down_sync(0xffffffffu, t.lo, o);
+            t = df_add(t, u);
+        }
+        if (lane == 0) p.chunk_sum[(long long)b * p.n_chunks + c] = df_to_double(t);
     }
 }
 
