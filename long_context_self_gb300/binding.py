@@ -1,8 +1,8 @@
 """Thin Python binding of libmagicdec (ctypes).
 
 Every function here carries the name of the C entry point it calls
-(include/magicdec.h) and only marshals arguments: it checks dtypes, devices and
-contiguity of torch tensors, allocates outputs (and a zero-filled workspace)
+(include/magicdec.h) and only marshals arguments: it checks dtypes, devices,
+contiguity and shapes of torch tensors, allocates outputs (and a zero-filled workspace)
 when the caller passes none, and hands raw device pointers and the current
 CUDA stream to the library.  All compute happens in the library's kernels.
 There is no fallback: if libmagicdec.so is missing or cannot load, every call
@@ -112,6 +112,14 @@ def _need(t: torch.Tensor, name: str, dtype, device=None):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need_shape(t: torch.Tensor, name: str, dtype, device, shape):
+    """_need plus an exact shape: the kernels index these tensors by the shapes the other
+    arguments imply, so a mismatch is refused here rather than read out of bounds."""
+    _need(t, name, dtype, device)
+    if tuple(t.shape) != tuple(int(s) for s in shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 _ws_cache = {}
 
 
@@ -141,13 +149,15 @@ def magicdec_streaming_select(seq_len: torch.Tensor, H_kv: int, n_sink: int, n_r
                               stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     _need(seq_len, "seq_len", torch.int32)
     dev = seq_len.device
+    if seq_len.dim() != 1:
+        raise ValueError("seq_len must be [B]")
     B = seq_len.shape[0]
     if idx is None:
         idx = torch.empty((B, H_kv, n_sink + n_recent), dtype=torch.int32, device=dev)
     if n_sel is None:
         n_sel = torch.empty((B,), dtype=torch.int32, device=dev)
-    _need(idx, "idx", torch.int32, dev)
-    _need(n_sel, "n_sel", torch.int32, dev)
+    _need_shape(idx, "idx", torch.int32, dev, (B, H_kv, n_sink + n_recent))
+    _need_shape(n_sel, "n_sel", torch.int32, dev, (B,))
     _check("magicdec_streaming_select",
            lib().magicdec_streaming_select(_ptr(seq_len), B, H_kv, n_sink, n_recent, _ptr(idx), _ptr(n_sel),
                                            _stream(stream, dev)))
@@ -166,16 +176,18 @@ def magicdec_snapkv_select(q_win: torch.Tensor, k: torch.Tensor, seq_len: torch.
     _need(q_win, "q_win", torch.bfloat16)
     dev = q_win.device
     _need(k, "k", torch.bfloat16, dev)
-    _need(seq_len, "seq_len", torch.int32, dev)
     B, w, H_q, d = q_win.shape
     L_cap, H_kv = k.shape[1], k.shape[2]
     if w != window or k.shape[0] != B or k.shape[3] != d:
         raise ValueError("q_win / k shapes disagree")
+    _need_shape(seq_len, "seq_len", torch.int32, dev, (B,))
     shape = kv_shape(B, H_q, H_kv, d, L_cap)
     if idx is None:
         idx = torch.empty((B, H_kv, budget), dtype=torch.int32, device=dev)
     if n_sel is None:
         n_sel = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need_shape(idx, "idx", torch.int32, dev, (B, H_kv, budget))
+    _need_shape(n_sel, "n_sel", torch.int32, dev, (B,))
     need = magicdec_snapkv_workspace_size(shape, window)
     if ws is None:
         ws = workspace(need, dev, "snapkv")
@@ -196,19 +208,19 @@ def magicdec_snapkv_select_budgets(q_win: torch.Tensor, k: torch.Tensor, seq_len
     _need(q_win, "q_win", torch.bfloat16)
     dev = q_win.device
     _need(k, "k", torch.bfloat16, dev)
-    _need(seq_len, "seq_len", torch.int32, dev)
-    _need(budgets, "budgets", torch.int32, dev)
     B, w, H_q, d = q_win.shape
     L_cap, H_kv = k.shape[1], k.shape[2]
-    if w != window:
-        raise ValueError("q_win must hold `window` query rows")
+    if w != window or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("q_win / k shapes disagree")
+    _need_shape(seq_len, "seq_len", torch.int32, dev, (B,))
+    _need_shape(budgets, "budgets", torch.int32, dev, (B,))
     shape = kv_shape(B, H_q, H_kv, d, L_cap)
     if idx is None:
         idx = torch.empty((B, H_kv, max_budget), dtype=torch.int32, device=dev)
     if n_sel is None:
         n_sel = torch.empty((B,), dtype=torch.int32, device=dev)
-    _need(idx, "idx", torch.int32, dev)
-    _need(n_sel, "n_sel", torch.int32, dev)
+    _need_shape(idx, "idx", torch.int32, dev, (B, H_kv, max_budget))
+    _need_shape(n_sel, "n_sel", torch.int32, dev, (B,))
     if ws is None:
         ws = workspace(magicdec_snapkv_workspace_size(shape, window), dev, "snapkv")
     _check("magicdec_snapkv_select_budgets",
@@ -226,15 +238,17 @@ def magicdec_gather_kv(k: torch.Tensor, v: torch.Tensor, idx: torch.Tensor, cap:
     _need(k, "k", torch.bfloat16)
     dev = k.device
     _need(v, "v", torch.bfloat16, dev)
-    _need(idx, "idx", torch.int32, dev)
     B, L_cap, H_kv, d = k.shape
+    if v.shape != k.shape or idx.dim() != 3:
+        raise ValueError("k / v / idx shapes disagree")
     n_idx = idx.shape[2]
+    _need_shape(idx, "idx", torch.int32, dev, (B, H_kv, n_idx))
     if kc is None:
         kc = torch.zeros((B, H_kv, cap, d), dtype=torch.bfloat16, device=dev)
     if vc is None:
         vc = torch.zeros((B, H_kv, cap, d), dtype=torch.bfloat16, device=dev)
-    _need(kc, "kc", torch.bfloat16, dev)
-    _need(vc, "vc", torch.bfloat16, dev)
+    _need_shape(kc, "kc", torch.bfloat16, dev, (B, H_kv, cap, d))
+    _need_shape(vc, "vc", torch.bfloat16, dev, (B, H_kv, cap, d))
     shape = kv_shape(B, H_kv, H_kv, d, L_cap)
     _check("magicdec_gather_kv",
            lib().magicdec_gather_kv(shape, _ptr(k), _ptr(v), _ptr(idx), n_idx, cap, _ptr(kc), _ptr(vc),
@@ -254,15 +268,15 @@ def magicdec_draft_attn(q: torch.Tensor, kc: torch.Tensor, vc: torch.Tensor, dra
     dev = q.device
     _need(kc, "kc", torch.bfloat16, dev)
     _need(vc, "vc", torch.bfloat16, dev)
-    _need(draft_len, "draft_len", torch.int32, dev)
     B, one, H_q, d = q.shape
     H_kv, cap = kc.shape[1], kc.shape[2]
     if one != 1 or kc.shape != vc.shape or kc.shape[0] != B or kc.shape[3] != d:
         raise ValueError("q / kc / vc shapes disagree")
+    _need_shape(draft_len, "draft_len", torch.int32, dev, (B,))
     shape = kv_shape(B, H_q, H_kv, d, cap)
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, dev)
+    _need_shape(out, "out", torch.bfloat16, dev, q.shape)
     if ws is None:
         ws = workspace(magicdec_attn_workspace_size(shape, 1), dev, "attn")
     _check("magicdec_draft_attn",
@@ -279,15 +293,15 @@ def magicdec_verify_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_
     dev = q.device
     _need(k, "k", torch.bfloat16, dev)
     _need(v, "v", torch.bfloat16, dev)
-    _need(seq_len, "seq_len", torch.int32, dev)
     B, n_q, H_q, d = q.shape
     L_cap, H_kv = k.shape[1], k.shape[2]
     if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
         raise ValueError("q / k / v shapes disagree")
+    _need_shape(seq_len, "seq_len", torch.int32, dev, (B,))
     shape = kv_shape(B, H_q, H_kv, d, L_cap)
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, dev)
+    _need_shape(out, "out", torch.bfloat16, dev, q.shape)
     if ws is None:
         ws = workspace(magicdec_attn_workspace_size(shape, n_q), dev, "attn")
     _check("magicdec_verify_attn",
@@ -304,14 +318,14 @@ def magicdec_verify_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tens
     dev = q.device
     _need(k, "k", torch.bfloat16, dev)
     _need(v, "v", torch.bfloat16, dev)
-    _need(seq_len, "seq_len", torch.int32, dev)
     B, n_q, H_q, d = q.shape
     L_cap, H_kv = k.shape[1], k.shape[2]
     if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
         raise ValueError("q / k / v shapes disagree")
+    _need_shape(seq_len, "seq_len", torch.int32, dev, (B,))
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, dev)
+    _need_shape(out, "out", torch.bfloat16, dev, q.shape)
     _check("magicdec_verify_attn_noalloc",
            lib().magicdec_verify_attn_noalloc(kv_shape(B, H_q, H_kv, d, L_cap), n_q, _ptr(q), _ptr(k), _ptr(v),
                                               _ptr(seq_len), _ptr(out), _stream(stream, dev)))
@@ -330,17 +344,17 @@ def magicdec_draft_cache_update(k: torch.Tensor, v: torch.Tensor, kc: torch.Tens
     _need(v, "v", torch.bfloat16, dev)
     _need(kc, "kc", torch.bfloat16, dev)
     _need(vc, "vc", torch.bfloat16, dev)
-    for name, t in (("len_valid", len_valid), ("len_old", len_old), ("len_new", len_new), ("origin", origin)):
-        _need(t, name, torch.int32, dev)
-    if base is not None:
-        _need(base, "base", torch.int32, dev)
     B, L_cap, H_kv, d = k.shape
+    for name, t in (("len_valid", len_valid), ("len_old", len_old), ("len_new", len_new), ("origin", origin)):
+        _need_shape(t, name, torch.int32, dev, (B,))
+    if base is not None:
+        _need_shape(base, "base", torch.int32, dev, (B,))
     if v.shape != k.shape or kc.shape != vc.shape or kc.shape[0] != B or kc.shape[1] != H_kv or kc.shape[3] != d:
         raise ValueError("k / v / kc / vc shapes disagree")
     cap = kc.shape[2]
     if draft_len is None:
         draft_len = torch.empty((B,), dtype=torch.int32, device=dev)
-    _need(draft_len, "draft_len", torch.int32, dev)
+    _need_shape(draft_len, "draft_len", torch.int32, dev, (B,))
     shape = kv_shape(B, H_kv, H_kv, d, L_cap)
     _check("magicdec_draft_cache_update",
            lib().magicdec_draft_cache_update(shape, _ptr(k), _ptr(v), _ptr(len_valid), _ptr(len_old), _ptr(len_new),
@@ -365,7 +379,7 @@ def magicdec_pq_encode(k: torch.Tensor, codebook: torch.Tensor, codes: Optional[
     B, L_cap, H_kv, d, M, C = _pq_dims(k, codebook)
     if codes is None:
         codes = torch.empty((B, H_kv, L_cap, M), dtype=torch.uint8, device=dev)
-    _need(codes, "codes", torch.uint8, dev)
+    _need_shape(codes, "codes", torch.uint8, dev, (B, H_kv, L_cap, M))
     _check("magicdec_pq_encode", lib().magicdec_pq_encode(kv_shape(B, H_kv, H_kv, d, L_cap), _ptr(k), M, C,
                                                           _ptr(codebook), _ptr(codes), _stream(stream, dev)))
     return codes
@@ -376,10 +390,10 @@ def magicdec_pq_update(k: torch.Tensor, seq_len: torch.Tensor, codes: torch.Tens
     """One Lloyd update of codebook [B, H_kv, M, C, 8] fp32 in place from codes [B, H_kv, L_cap, M]."""
     _need(k, "k", torch.bfloat16)
     dev = k.device
-    _need(seq_len, "seq_len", torch.int32, dev)
-    _need(codes, "codes", torch.uint8, dev)
     _need(codebook, "codebook", torch.float32, dev)
     B, L_cap, H_kv, d, M, C = _pq_dims(k, codebook)
+    _need_shape(seq_len, "seq_len", torch.int32, dev, (B,))
+    _need_shape(codes, "codes", torch.uint8, dev, (B, H_kv, L_cap, M))
     _check("magicdec_pq_update", lib().magicdec_pq_update(kv_shape(B, H_kv, H_kv, d, L_cap), _ptr(k), _ptr(seq_len),
                                                           M, C, _ptr(codes), _ptr(codebook), _stream(stream, dev)))
     return codebook
@@ -398,17 +412,17 @@ def magicdec_pq_draft_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, se
     dev = q.device
     _need(k, "k", torch.bfloat16, dev)
     _need(v, "v", torch.bfloat16, dev)
-    _need(seq_len, "seq_len", torch.int32, dev)
     _need(codebook, "codebook", torch.float32, dev)
-    _need(codes, "codes", torch.uint8, dev)
     B, L_cap, H_kv, d, M, C = _pq_dims(k, codebook)
     H_q = q.shape[2]
     if q.shape[0] != B or q.shape[1] != 1 or q.shape[3] != d or v.shape != k.shape:
         raise ValueError("q / k / v shapes disagree")
+    _need_shape(seq_len, "seq_len", torch.int32, dev, (B,))
+    _need_shape(codes, "codes", torch.uint8, dev, (B, H_kv, L_cap, M))
     shape = kv_shape(B, H_q, H_kv, d, L_cap)
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, dev)
+    _need_shape(out, "out", torch.bfloat16, dev, q.shape)
     if idx is not None:
         _need(idx, "idx", torch.int32, dev)
         if tuple(idx.shape) != (B, H_q, int(top_k)):
@@ -435,15 +449,15 @@ def magicdec_topk_draft_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     dev = q.device
     _need(k, "k", torch.bfloat16, dev)
     _need(v, "v", torch.bfloat16, dev)
-    _need(seq_len, "seq_len", torch.int32, dev)
     B, one, H_q, d = q.shape
     L_cap, H_kv = k.shape[1], k.shape[2]
     if one != 1 or k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
         raise ValueError("q / k / v shapes disagree")
+    _need_shape(seq_len, "seq_len", torch.int32, dev, (B,))
     shape = kv_shape(B, H_q, H_kv, d, L_cap)
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, dev)
+    _need_shape(out, "out", torch.bfloat16, dev, q.shape)
     if idx is not None:
         _need(idx, "idx", torch.int32, dev)
         if tuple(idx.shape) != (B, H_q, int(top_k)):
@@ -469,20 +483,26 @@ def magicdec_spec_accept(target: torch.Tensor, draft: Optional[torch.Tensor], dr
     """target [B, g+1, V] f32, draft [B, g, V] f32 -> (n_acc [B], out_tok [B, g+1], n_amb [B]) int32."""
     _need(target, "target", torch.float32)
     dev = target.device
+    if target.dim() != 3:
+        raise ValueError("target must be [B, gamma+1, V]")
     B, gp1, V = target.shape
     gamma = gp1 - 1
     if draft is not None:
-        _need(draft, "draft", torch.float32, dev)
-    _need(draft_tok, "draft_tok", torch.int32, dev)
-    for name, t in (("u_acc", u_acc), ("u_res", u_res)):
-        if t is not None:
-            _need(t, name, torch.float32, dev)
+        _need_shape(draft, "draft", torch.float32, dev, (B, gamma, V))
+    _need_shape(draft_tok, "draft_tok", torch.int32, dev, (B, gamma))
+    if u_acc is not None:
+        _need_shape(u_acc, "u_acc", torch.float32, dev, (B, gamma))
+    if u_res is not None:
+        _need_shape(u_res, "u_res", torch.float32, dev, (B,))
     if n_acc is None:
         n_acc = torch.empty((B,), dtype=torch.int32, device=dev)
     if out_tok is None:
         out_tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     if n_amb is None:
         n_amb = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need_shape(n_acc, "n_acc", torch.int32, dev, (B,))
+    _need_shape(out_tok, "out_tok", torch.int32, dev, (B, gamma + 1))
+    _need_shape(n_amb, "n_amb", torch.int32, dev, (B,))
     if ws is None:
         ws = workspace(magicdec_spec_accept_workspace_size(B, gamma, V), dev, "accept")
     _check("magicdec_spec_accept",
