@@ -249,6 +249,40 @@ def test_pq_draft_attn_matches_oracle(B, H_q, H_kv, L, C, top_k, lens):
             assert torch.count_nonzero(out[b]) == 0
 
 
+def test_pq_head_dim_64():
+    """d = 64 (M = 8 subspaces, 8-byte code rows): encode under the margin rule, an exact update,
+    and PQ attention under the band rule."""
+    rng = np.random.default_rng(80)
+    B, H_q, H_kv, d, L, M, C, top_k = 2, 16, 4, 64, 1800, 8, 64, 128
+    q = rand_bf16((B, 1, H_q, d), 81)
+    k = rand_bf16((B, L, H_kv, d), 82)
+    v = rand_bf16((B, L, H_kv, d), 83)
+    cb = _pq_codebook(rng, B, H_kv, M, C)
+    codes_g = mb.magicdec_pq_encode(k.to(DEV), torch.from_numpy(cb).to(DEV))
+    torch.cuda.synchronize()
+    codes_o, gap = oracle.pq_encode(to_u16(k), cb, want_gap=True)
+    kf = bf16_out_to_f64(k).reshape(B, L, H_kv, M, 8).transpose(0, 2, 1, 3, 4)
+    kn = (kf ** 2).sum(-1)
+    cn = (cb.astype(np.float64) ** 2).sum(-1)
+    cbest = np.take_along_axis(cn[:, :, None, :, :], codes_o[..., None].astype(np.int64), axis=-1)[..., 0]
+    margin = gap <= PQ_MARGIN * (kn + cbest)
+    assert np.array_equal(codes_g.cpu().numpy()[~margin], codes_o[~margin])
+    sl = np.array([L, 1100], np.int32)
+    cb_g = torch.from_numpy(cb.copy()).to(DEV)
+    mb.magicdec_pq_update(k.to(DEV), torch.from_numpy(sl).to(DEV), torch.from_numpy(codes_o).to(DEV), cb_g)
+    torch.cuda.synchronize()
+    cb2 = oracle.pq_update(to_u16(k), sl, codes_o, cb)
+    np.testing.assert_array_equal(cb_g.cpu().numpy(), cb2)
+    codes2, _ = oracle.pq_encode(to_u16(k), cb2)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_pq_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV),
+                                    torch.from_numpy(cb2).to(DEV), torch.from_numpy(codes2).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, approx = oracle.pq_attn(to_u16(q), to_u16(k), to_u16(v), sl, cb2, codes2, top_k, want_approx=True)
+    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, approx, sl, top_k, "pq d64")
+    assert swapped <= 1
+
+
 def test_pq_lloyd_pipeline_on_planted_clusters():
     """GPU encode + update twice from one member per planted cluster: codes equal the oracle's and the
     planted labels, codebooks equal the oracle's."""
