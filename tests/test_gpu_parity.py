@@ -525,6 +525,28 @@ def test_spec_accept_edge_tokens():
     check_accept(tuple(t.cpu().numpy() for t in got0), ref0, "gamma=0")
 
 
+@pytest.mark.parametrize("V", [10003, 4097, 1021])
+@pytest.mark.parametrize("greedy", [False, True])
+def test_spec_accept_vocabulary_not_a_multiple_of_4(V, greedy):
+    """Scalar load paths of the statistics, chunk-sum and draw kernels (V % 4 != 0), several
+    4096-logit chunks and a partial last statistics record."""
+    B, gamma = 16, 3
+    g = torch.Generator().manual_seed(V)
+    target = torch.randn((B, gamma + 1, V), generator=g) * 2
+    draft = target[:, :gamma] + torch.randn((B, gamma, V), generator=g) * 0.5
+    tok = torch.distributions.Categorical(logits=draft).sample().to(torch.int32)
+    if greedy:
+        am = target[:, :gamma].argmax(-1).to(torch.int32)
+        tok = torch.where(torch.rand(tok.shape, generator=g) < 0.7, am, tok)
+    u_acc, u_res = torch.rand((B, gamma), generator=g), torch.rand((B,), generator=g)
+    got = mb.magicdec_spec_accept(target.to(DEV), draft.to(DEV), tok.to(DEV), u_acc.to(DEV), u_res.to(DEV), greedy)
+    torch.cuda.synchronize()
+    t, d, x, ua, ur = (a.numpy() for a in (target, draft, tok, u_acc, u_res))
+    ref = oracle.spec_accept(t, d, x, ua, ur, greedy)
+    n_amb = check_accept(tuple(a.cpu().numpy() for a in got), ref, f"V={V}", inputs=(t, d, ur))
+    assert n_amb <= 2
+
+
 def test_rows_past_the_length_never_reach_the_output():
     """Cache rows at or beyond a sequence's length may hold anything (here NaN): outputs
     must equal the oracle's, which never reads them."""
