@@ -395,6 +395,8 @@ TOPK_CASES = [
     (2, 16, 2, 64, 1500, 1, [1500, 1]),                                # G=8, top-1
     (2, 8, 2, 128, 70000, 2048, [70000, 41000]),                       # long rows
     (1, 40, 8, 128, 20000, 4096, [20000]),                             # G=5, a 4096 budget
+    (2, 4, 4, 128, 1500, 64, [1500, 900]),                             # MHA: G=1
+    (2, 4, 2, 64, 1000, 100, [1000, 999]),                             # G=2, d=64
 ]
 
 
