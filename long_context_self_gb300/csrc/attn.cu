@@ -25,6 +25,15 @@
 //    slots guarded by full/empty mbarriers.  Rows past the sequence end are
 //    masked (and their V rows zeroed in shared memory, so stale or
 //    uninitialised cache rows can never reach the output).
+//  * L2 priority of the K/V copies.  Draft: evict_first, so the copies do not
+//    push out the part of the compact cache (written by the gather or the
+//    draft-cache update just before, larger than L2) that stays resident
+//    across the gamma draft calls.  Verify: evict_normal.  The full cache is
+//    read once and gains nothing from L2, but with evict_first its lines may
+//    only take the ways that normal-priority lines (the draft cache the
+//    gather just wrote back, still dirty) leave free, which measurably slowed
+//    verification right after a gather (2.57 ms against 2.37 ms per call at
+//    B=128, L=32000).
 //  * 4*MT consumer warps: warp (mt, pq) owns query rows mt*16..mt*16+15 and
 //    key columns pq*16..pq*16+15 of each tile.  S = Q K^T and O += P V run on
 //    bf16 mma.sync m16n8k16 with fp32 accumulation (the contraction is
@@ -172,7 +181,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     if (warp == NCW) {
         // ------------------------------------------------------- producer (1 thread)
         if (lane != 0) return;
-        const uint64_t pol = policy_evict_first();
+        const uint64_t pol = p.head_major ? policy_evict_first() : policy_evict_normal();
         const uint64_t pol_q = policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;

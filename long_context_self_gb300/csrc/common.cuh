@@ -119,6 +119,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Tiled tensor copy (TMA) of one 4-D box described by a tensor map into
 // shared memory, completing on `bar`.  The innermost coordinate c0 times the
 // element size must be a multiple of 16 bytes.
