@@ -309,7 +309,7 @@ MAGICDEC_API magicdec_status magicdec_pq_draft_attn(magicdec_kv_shape shape, con
  * runtime, an engine whose memory plan is fixed before it starts, or a
  * process whose device memory is owned by another allocator).  Same
  * arguments, layouts and results as magicdec_verify_attn, without `ws`: its
- * scratch is a 16 MiB array inside the library, which every GPU that loads
+ * scratch is a 32 MiB array inside the library, which every GPU that loads
  * the library holds until the process exits.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address and synchronously zeroes the part that must

@@ -11,7 +11,7 @@
 namespace magicdec {
 magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, int n_q, int head_major,
                                    const void *q, const void *k, const void *v, const int32_t *len, void *out,
-                                   void *ws, cudaStream_t st);
+                                   void *ws, size_t ws_bytes, cudaStream_t st);
 size_t attn_workspace_bytes(int B, int H_kv, int D, int M);
 size_t topk_workspace_bytes(int B, int H_q, int L_cap);
 magicdec_status launch_pq_encode(int B, int H_kv, int D, int L_cap, int C, const void *k, const float *codebook,
@@ -236,7 +236,7 @@ magicdec_status magicdec_draft_attn(magicdec_kv_shape shape, const uint16_t *q, 
     magicdec_status s = attn_common(shape, 1, q, kc, vc, draft_len, out, ws, ws_bytes);
     if (s != MAGICDEC_OK) return s;
     return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, 1, 1, q, kc, vc,
-                                        draft_len, out, ws, static_cast<cudaStream_t>(stream));
+                                        draft_len, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n_q, const uint16_t *q, const uint16_t *k,
@@ -245,7 +245,7 @@ magicdec_status magicdec_verify_attn(magicdec_kv_shape shape, int n_q, const uin
     magicdec_status s = attn_common(shape, n_q, q, k, v, seq_len, out, ws, ws_bytes);
     if (s != MAGICDEC_OK) return s;
     return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, n_q, 0, q, k, v,
-                                        seq_len, out, ws, static_cast<cudaStream_t>(stream));
+                                        seq_len, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 magicdec_status magicdec_draft_cache_update(magicdec_kv_shape shape, const uint16_t *k, const uint16_t *v,

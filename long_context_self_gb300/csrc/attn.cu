@@ -47,15 +47,19 @@ namespace magicdec {
 constexpr int kTileN = 64;      // KV rows per pipeline stage
 constexpr int kMaxStages = 8;
 constexpr int kHalfBytes = kTileN * 128;   // one 64-row x 64-channel swizzled box
-constexpr int kMaxContrib = 32;            // contributors a merge lists in shared memory
+constexpr int kMaxContrib = 512;           // contributors a merge lists in shared memory (CTAs + tail)
+constexpr int kTailMinTiles = 64;          // pairs of at least this many tiles have a dynamic tail
+constexpr int kTailDiv = 16;               // ... of n / kTailDiv tiles
 
 struct AttnParams {
     const __nv_bfloat16 *q;     // [B, n_q, H_q, D]
     const int32_t *len;         // [B]
     __nv_bfloat16 *out;         // [B, n_q, H_q, D]
-    float *part_o;              // [C, 2, MT*16, D]
-    float *part_ml;             // [C, 2, MT*16, 2]
-    int *counters;              // [B * H_kv], zero between calls
+    float *part_o;              // [2*C + (tails ? 2*B*H_kv : 0), MT*16, D] partial outputs
+    float *part_ml;             // same slots, [.., MT*16, 2] (max, sum)
+    int *counters;              // [B * H_kv] merge arrivals, zero between calls
+    int *sched;                 // [0] tail claims, [1] CTAs finished; zero between calls
+    int tails;                  // 1: pairs of >= kTailMinTiles tiles hand their last n/kTailDiv to the pool
     int *err;
     int B, H_q, H_kv, G, n_q, L_cap, M;
     int head_major;             // 0: verify layout [B, L_cap, H_kv, D]; 1: draft [B, H_kv, cap, D]
@@ -68,10 +72,23 @@ struct Segment {
     long long pair_t0;          // global index of the pair's first tile
 };
 
-__device__ __forceinline__ int clamp_len(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
+// One run of consecutive tiles of one pair, handed from the producer to the
+// consumer warps through a two-entry ring in shared memory.
+struct SegDesc {
+    int b, h;                   // the pair
+    int ti0, nseg;              // first tile (within the pair) and tile count
+    int len;                    // the sequence's clamped length
+    int kind;                   // 0: part of the pair's head; 1: its whole tail; -1: no more work
+};
 
-// Pair and tile holding global tile t.  prefix[b] = tiles of sequences < b
-// (per KV head); pairs of sequence b occupy [H_kv*prefix[b], H_kv*prefix[b+1]).
+__device__ __forceinline__ int clamp_len(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
+__device__ __forceinline__ int tiles_of(int len) { return (len + kTileN - 1) / kTileN; }
+// Tiles at the end of an n-tile pair that go to the dynamic pool.
+__device__ __forceinline__ int tail_tiles(int n, int tails) { return (tails && n >= kTailMinTiles) ? n / kTailDiv : 0; }
+
+// Pair and tile holding global head tile t.  prefix[b] = head tiles of
+// sequences < b (per KV head); the heads of sequence b's pairs occupy
+// [H_kv*prefix[b], H_kv*prefix[b+1]).
 __device__ __forceinline__ Segment decode_tile(long long t, const int *prefix, const AttnParams &p) {
     int lo = 0, hi = p.B - 1;
     while (lo < hi) {
@@ -95,6 +112,76 @@ __device__ __forceinline__ int cta_of(long long t, long long T, int C) {
 }
 
 __device__ __forceinline__ long long cta_start(int c, long long T, int C) { return T * c / C; }
+
+// The last arriver's merge of a pair's partials (slots contrib[0..n_merge),
+// -1 = none): one pass with the running log-sum-exp rule.  Each thread loads
+// two contributors' partials of its output vector before using either, so
+// their L2 round trips overlap (more in flight costs the streaming loop
+// registers: at 201 for D = 128 two CTAs still fit on an SM).
+template <int D, int MT>
+__device__ __forceinline__ void merge_partials(const AttnParams &p, const int *contrib, int n_merge,
+                                            __nv_bfloat16 *ob, long long q_head_stride, int ctid, int NT) {
+    const float sl = p.scale_log2;
+    const float NEG_INF = -INFINITY;
+    constexpr int MP = 1;
+    const int n_items = p.M * (D / 4);
+    for (int base = 0; base < n_items; base += NT * MP) {
+        int ro[MP], co[MP];
+        float Mr[MP], Lr[MP];
+        float4 acc[MP];
+#pragma unroll
+        for (int k = 0; k < MP; ++k) {
+            const int idx = min(base + ctid + k * NT, n_items - 1);   // clamped duplicates are not stored
+            ro[k] = idx / (D / 4);
+            co[k] = (idx % (D / 4)) * 4;
+            Mr[k] = NEG_INF;
+            Lr[k] = 0.f;
+            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int j0 = 0; j0 < n_merge; j0 += 2) {
+            int sj[2];
+            float2 ml[2][MP];
+            float4 oc[2][MP];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                sj[u] = j0 + u < n_merge ? contrib[j0 + u] : -1;
+                if (sj[u] < 0) continue;
+#pragma unroll
+                for (int k = 0; k < MP; ++k) {
+                    const long long row = (long long)sj[u] * (MT * 16) + ro[k];
+                    ml[u][k] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + row * 2));
+                    oc[u][k] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row * D + co[k]));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (sj[u] < 0) continue;
+#pragma unroll
+                for (int k = 0; k < MP; ++k) {
+                    const float mn = fmaxf(Mr[k], ml[u][k].x);
+                    const float mu = mn == NEG_INF ? 0.f : mn;
+                    const float fa = fast_exp2((Mr[k] - mu) * sl), fb = fast_exp2((ml[u][k].x - mu) * sl);
+                    Lr[k] = Lr[k] * fa + ml[u][k].y * fb;
+                    acc[k].x = acc[k].x * fa + oc[u][k].x * fb;
+                    acc[k].y = acc[k].y * fa + oc[u][k].y * fb;
+                    acc[k].z = acc[k].z * fa + oc[u][k].z * fb;
+                    acc[k].w = acc[k].w * fa + oc[u][k].w * fb;
+                    Mr[k] = mn;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < MP; ++k) {
+            if (base + ctid + k * NT >= n_items) continue;
+            const int r = ro[k];
+            const float inv = Lr[k] > 0.f ? 1.f / Lr[k] : 0.f;
+            uint2 pk;
+            pk.x = pack_bf16(acc[k].x * inv, acc[k].y * inv);
+            pk.y = pack_bf16(acc[k].z * inv, acc[k].w * inv);
+            *reinterpret_cast<uint2 *>(ob + (r / p.G) * q_head_stride + (r % p.G) * D + co[k]) = pk;
+        }
+    }
+}
 
 template <int D, int MT>
 __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
@@ -126,7 +213,8 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     uint64_t *qfull_bar = empty_bar + kMaxStages;  // [2]
     uint64_t *qempty_bar = qfull_bar + 2;          // [2]
     int *flag = reinterpret_cast<int *>(qempty_bar + 2);
-    int *contrib = flag + 4;                       // [kMaxContrib] partial-slot bases of a merged pair
+    SegDesc *desc = reinterpret_cast<SegDesc *>(flag + 4);   // [2] ring beside the query slots
+    int *contrib = reinterpret_cast<int *>(desc + 2);        // [kMaxContrib] partial slots of a merged pair
     int *prefix = contrib + kMaxContrib;           // [B+1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -151,9 +239,12 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         reinterpret_cast<uint4 *>(qslots)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     pdl_wait();
-    // Tiles per sequence, loaded in parallel, then an exclusive scan by warp 0.
-    for (int b = tid; b < p.B; b += blockDim.x)
-        prefix[b] = (clamp_len(__ldg(p.len + b), p.L_cap) + kTileN - 1) / kTileN;
+    // Head tiles per sequence (all tiles less the dynamic tail), loaded in
+    // parallel, then an exclusive scan by warp 0.
+    for (int b = tid; b < p.B; b += blockDim.x) {
+        const int n = tiles_of(clamp_len(__ldg(p.len + b), p.L_cap));
+        prefix[b] = n - tail_tiles(n, p.tails);
+    }
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -185,43 +276,71 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         const uint64_t pol_q = policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;
-        int issued = 0, seg_no = 0, q_issued = 0;
+        int issued = 0, seg_no = 0;
         bool ok = true;
-        for (long long t = t_begin; t < t_end && ok; ++seg_no) {
-            const Segment s = decode_tile(t, prefix, p);
-            const int nseg = (int)min((long long)(s.ntiles - s.ti0), t_end - t);
-            {
-                // the segment's G*n_q query rows, one box per 64-channel half
-                const int qs = seg_no & 1;
-                if (!mbar_wait(&qempty_bar[qs], ((seg_no >> 1) & 1) ^ 1u, p.err)) { ok = false; break; }
+        // Hand one segment to the consumers: its descriptor, and for work its
+        // G*n_q query rows (one box per 64-channel half) on the same barrier.
+        auto publish = [&](const SegDesc &d) -> bool {
+            const int qs = seg_no & 1;
+            if (!mbar_wait(&qempty_bar[qs], ((seg_no >> 1) & 1) ^ 1u, p.err)) return false;
+            desc[qs] = d;
+            if (d.kind >= 0) {
                 mbar_arrive_expect_tx(&qfull_bar[qs], HALVES * p.M * 128);
 #pragma unroll
                 for (int hf = 0; hf < HALVES; ++hf)
-                    tma_load_4d(qslots + qs * QSLOT + hf * QHALF, &tmq, hf * 64, s.h * p.G, 0, s.b, &qfull_bar[qs],
+                    tma_load_4d(qslots + qs * QSLOT + hf * QHALF, &tmq, hf * 64, d.h * p.G, 0, d.b, &qfull_bar[qs],
                                 pol_q);
-                ++q_issued;
+            } else {
+                mbar_arrive(&qfull_bar[qs]);
             }
-            for (int i = 0; i < nseg; ++i) {
-                if (!mbar_wait(&empty_bar[stage], phase ^ 1u, p.err)) { ok = false; break; }
+            ++seg_no;
+            return true;
+        };
+        auto load_tiles = [&](const SegDesc &d) -> bool {
+            for (int i = 0; i < d.nseg; ++i) {
+                if (!mbar_wait(&empty_bar[stage], phase ^ 1u, p.err)) return false;
                 mbar_arrive_expect_tx(&full_bar[stage], TX_BYTES);
                 uint8_t *sk = stage_base + (size_t)stage * STAGE_BYTES;
                 uint8_t *sv = sk + TILE_BYTES;
-                const int pos0 = (s.ti0 + i) * kTileN;
+                const int pos0 = (d.ti0 + i) * kTileN;
 #pragma unroll
                 for (int hf = 0; hf < HALVES; ++hf) {
                     if (p.head_major) {
-                        tma_load_4d(sk + hf * kHalfBytes, &tmk, hf * 64, pos0, s.h, s.b, &full_bar[stage], pol);
-                        tma_load_4d(sv + hf * kHalfBytes, &tmv, hf * 64, pos0, s.h, s.b, &full_bar[stage], pol);
+                        tma_load_4d(sk + hf * kHalfBytes, &tmk, hf * 64, pos0, d.h, d.b, &full_bar[stage], pol);
+                        tma_load_4d(sv + hf * kHalfBytes, &tmv, hf * 64, pos0, d.h, d.b, &full_bar[stage], pol);
                     } else {
-                        tma_load_4d(sk + hf * kHalfBytes, &tmk, hf * 64, s.h, pos0, s.b, &full_bar[stage], pol);
-                        tma_load_4d(sv + hf * kHalfBytes, &tmv, hf * 64, s.h, pos0, s.b, &full_bar[stage], pol);
+                        tma_load_4d(sk + hf * kHalfBytes, &tmk, hf * 64, d.h, pos0, d.b, &full_bar[stage], pol);
+                        tma_load_4d(sv + hf * kHalfBytes, &tmv, hf * 64, d.h, pos0, d.b, &full_bar[stage], pol);
                     }
                 }
                 ++issued;
                 if (++stage == stages) { stage = 0; phase ^= 1u; }
             }
+            return true;
+        };
+        // This CTA's static share of the heads ...
+        for (long long t = t_begin; t < t_end && ok;) {
+            const Segment s = decode_tile(t, prefix, p);
+            const int nseg = (int)min((long long)(s.ntiles - s.ti0), t_end - t);
+            const SegDesc d{s.b, s.h, s.ti0, nseg, s.len, 0};
+            ok = publish(d) && load_tiles(d);
             t += nseg;
         }
+        // ... then tails claimed one pair at a time until none is left.
+        if (p.tails) {
+            const int n_pairs = p.B * p.H_kv;
+            while (ok) {
+                const int j = atomicAdd(p.sched, 1);
+                if (j >= n_pairs) break;
+                const int b = j / p.H_kv, h = j - b * p.H_kv;
+                const int len = clamp_len(__ldg(p.len + b), p.L_cap);
+                const int n = tiles_of(len), tl = tail_tiles(n, 1);
+                if (tl == 0) continue;
+                const SegDesc d{b, h, n - tl, tl, len, 1};
+                ok = publish(d) && load_tiles(d);
+            }
+        }
+        if (ok) ok = publish(SegDesc{0, 0, 0, 0, 0, -1});
         // Drain: do not leave the CTA while copies issued here may still land.
         int st = stage;
         uint32_t ph = phase;
@@ -229,7 +348,18 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
             if (st == 0) { st = stages - 1; ph ^= 1u; } else { --st; }
             mbar_wait(&full_bar[st], ph, p.err);
         }
-        for (int k = max(0, q_issued - 2); k < q_issued; ++k) mbar_wait(&qfull_bar[k & 1], (k >> 1) & 1, p.err);
+        // The query slots: the last two published segments hold the only copies
+        // that may still be in flight (the end marker's phase completes at once).
+        for (int k = max(0, seg_no - 2); k < seg_no; ++k) mbar_wait(&qfull_bar[k & 1], (k >> 1) & 1, p.err);
+        if (p.tails) {
+            // Every CTA has made its last claim before it counts itself here; the
+            // last one leaves both words zero for the next call.
+            const int old = atomic_add_acq_rel_gpu(p.sched + 1, 1);
+            if (old == (int)gridDim.x - 1) {
+                atomicExch(p.sched, 0);
+                atomicExch(p.sched + 1, 0);
+            }
+        }
         return;
     }
 
@@ -249,22 +379,25 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         for (int i = ctid; i < n16; i += NCW * 32) o[i] = make_uint4(0, 0, 0, 0);
     }
 
-    int stage = 0, seg_no = 0;
+    int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (long long t = t_begin; t < t_end; ++seg_no) {
-        const Segment s = decode_tile(t, prefix, p);
-        const int nseg = (int)min((long long)(s.ntiles - s.ti0), t_end - t);
+    for (int seg_no = 0;; ++seg_no) {
+        // The next segment from the producer (its wait failing has raised the
+        // error word; nothing more can be trusted, so stop).
+        const int qs = seg_no & 1;
+        if (!mbar_wait(&qfull_bar[qs], (seg_no >> 1) & 1, p.err)) break;
+        const SegDesc d = desc[qs];
+        if (d.kind < 0) break;
+        const int nseg = d.nseg;
 
         // Rows owned by this thread: r0 = mt*16+g, r1 = r0+8.  Row r is query
         // token r / G of head h*G + r % G and sees positions <= len-n_q+r/G.
         const int r0 = mt * 16 + g, r1 = r0 + 8;
-        const int lim0 = r0 < p.M ? s.len - p.n_q + r0 / p.G : s.len - 1;
-        const int lim1 = r1 < p.M ? s.len - p.n_q + r1 / p.G : s.len - 1;
+        const int lim0 = r0 < p.M ? d.len - p.n_q + r0 / p.G : d.len - 1;
+        const int lim1 = r1 < p.M ? d.len - p.n_q + r1 / p.G : d.len - 1;
         uint32_t qa[KS][4];
         {
-            const int qs = seg_no & 1;
-            if (ok) ok = mbar_wait(&qfull_bar[qs], (seg_no >> 1) & 1, p.err);
             const uint32_t qbase = smem_u32(qslots + qs * QSLOT);
             const int mat = lane >> 3, rr = lane & 7;
             const int row = mt * 16 + (mat & 1) * 8 + rr;
@@ -287,13 +420,13 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
             if (ok) {
                 uint8_t *kt = stage_base + (size_t)stage * STAGE_BYTES;
                 uint8_t *vt = kt + TILE_BYTES;
-                const int tile_pos = (s.ti0 + i) * kTileN;
-                if (tile_pos + kTileN > s.len) {
+                const int tile_pos = (d.ti0 + i) * kTileN;
+                if (tile_pos + kTileN > d.len) {
                     // Rows at or past the sequence end hold whatever the cache holds
                     // there: zero this warp's V rows so P = 0 meets finite values.
                     for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
                         const int r = pq * 16 + idx / (D / 8), ch = idx % (D / 8);
-                        if (tile_pos + r >= s.len)
+                        if (tile_pos + r >= d.len)
                             *reinterpret_cast<uint4 *>(vt + (ch >> 3) * kHalfBytes + swz128(r, ch & 7)) =
                                 make_uint4(0, 0, 0, 0);
                     }
@@ -316,7 +449,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
                         mma_bf16(sc[1], qa[ks], b2, b3);
                     }
                 }
-                if (tile_pos + kTileN - 1 > s.len - p.n_q) {
+                if (tile_pos + kTileN - 1 > d.len - p.n_q) {
                     const int pb = tile_pos + pq * 16 + 2 * t4;
 #pragma unroll
                     for (int n = 0; n < 2; ++n)
@@ -400,13 +533,27 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         }
         named_bar_sync(2 + mt, 128);
 
-        const int c_first = cta_of(s.pair_t0, T, C);
-        const int c_last = cta_of(s.pair_t0 + s.ntiles - 1, T, C);
-        const bool whole = c_first == c_last;
-        __nv_bfloat16 *ob = p.out + (long long)s.b * p.n_q * q_head_stride + (long long)s.h * p.G * D;
-        const int slot = (t_begin >= s.pair_t0) ? 0 : 1;
-        float *po = p.part_o + ((long long)c * 2 + slot) * (MT * 16) * D;
-        float *pml = p.part_ml + ((long long)c * 2 + slot) * (MT * 16) * 2;
+        // The pair's contributors: the CTAs whose static ranges overlap its head
+        // (with fewer head tiles than CTAs some ranges are empty, so at most
+        // `head` of them), plus its tail when it has one.
+        const int n_all = tiles_of(d.len), tl = tail_tiles(n_all, p.tails), head = n_all - tl;
+        const long long pair_t0 = (long long)p.H_kv * prefix[d.b] + (long long)d.h * head;
+        const int c_first = cta_of(pair_t0, T, C);
+        const int c_last = cta_of(pair_t0 + head - 1, T, C);
+        const int n_static = min(c_last - c_first + 1, head);
+        const int n_contrib = n_static + (tl > 0 ? 1 : 0);
+        const bool whole = n_contrib == 1;
+        const int pair = d.b * p.H_kv + d.h;
+        // Partial slots: CTA c keeps 2c (its first segment, when its range
+        // starts inside a head split across CTAs) and 2c+1 (its last segment);
+        // pair P keeps 2C+2P (its head, when one CTA holds all of it) and
+        // 2C+2P+1 (its tail).
+        const int slot_id = d.kind == 1 ? 2 * C + 2 * pair + 1
+                            : n_static == 1 ? 2 * C + 2 * pair
+                                            : 2 * c + (t_begin >= pair_t0 ? 0 : 1);
+        __nv_bfloat16 *ob = p.out + (long long)d.b * p.n_q * q_head_stride + (long long)d.h * p.G * D;
+        float *po = p.part_o + (long long)slot_id * (MT * 16) * D;
+        float *pml = p.part_ml + (long long)slot_id * (MT * 16) * 2;
         for (int idx = gtid; idx < 16 * (D / 8); idx += 128) {
             const int row = idx / (D / 8), col = (idx % (D / 8)) * 8;
             const int r = mt * 16 + row;
@@ -451,56 +598,36 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         } else {
             named_bar_sync(1, NCW * 32);
             if (ctid == 0) {
-                const int pair = s.b * p.H_kv + s.h;
-                // Contributors: the CTAs with a non-empty range in [c_first, c_last]
-                // (with fewer tiles than CTAs some ranges are empty).  A contributor
-                // whose range starts inside the pair published its first segment
-                // (slot 0), one that started before it its last segment (slot 1).
-                int n_contrib = 0;
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                    const long long st0 = cta_start(cc, T, C);
-                    if (cta_start(cc + 1, T, C) == st0) continue;
-                    if (n_contrib < kMaxContrib) contrib[n_contrib] = cc * 2 + (st0 >= s.pair_t0 ? 0 : 1);
-                    ++n_contrib;
-                }
                 // release: this CTA's partial (ordered by the barrier above);
                 // acquire: for the last arriver, every other contributor's partial
                 const int old = atomic_add_acq_rel_gpu(p.counters + pair, 1);
                 const int last = (old == n_contrib - 1);
-                if (old >= n_contrib || n_contrib > kMaxContrib) raise_error(p.err, kErrState);
+                if (old >= n_contrib) raise_error(p.err, kErrState);
                 if (last) p.counters[pair] = 0;
-                *flag = last ? n_contrib : 0;
+                *flag = last;
             }
             named_bar_sync(1, NCW * 32);
-            const int n_merge = min(*flag, kMaxContrib);
-            if (n_merge) {
-                for (int idx = ctid; idx < p.M * (D / 4); idx += NCW * 32) {
-                    const int r = idx / (D / 4), col = (idx % (D / 4)) * 4;
-                    float Mx = NEG_INF;
-                    for (int j = 0; j < n_merge; ++j)
-                        Mx = fmaxf(Mx, __ldcg(p.part_ml + ((long long)contrib[j] * (MT * 16) + r) * 2));
-                    const float Mu = Mx == NEG_INF ? 0.f : Mx;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    float Ls = 0.f;
-                    for (int j = 0; j < n_merge; ++j) {
-                        const long long base = (long long)contrib[j] * (MT * 16) + r;
-                        const float mc = __ldcg(p.part_ml + base * 2);
-                        const float lc = __ldcg(p.part_ml + base * 2 + 1);
-                        const float wgt = fast_exp2((mc - Mu) * sl);
-                        const float4 oc = __ldcg(reinterpret_cast<const float4 *>(p.part_o + base * D + col));
-                        Ls += wgt * lc;
-                        acc.x += wgt * oc.x; acc.y += wgt * oc.y; acc.z += wgt * oc.z; acc.w += wgt * oc.w;
+            if (*flag) {
+                // The last arriver lists the contributors' slots in a fixed order
+                // (CTAs ascending, then the tail; -1 for an empty CTA range) ...
+                const int n_list = n_static == 1 ? 1 : c_last - c_first + 1;
+                for (int i = ctid; i < n_list; i += NCW * 32) {
+                    int v = 2 * C + 2 * pair;
+                    if (n_static != 1) {
+                        const int cc = c_first + i;
+                        const long long st0 = cta_start(cc, T, C);
+                        v = cta_start(cc + 1, T, C) == st0 ? -1 : 2 * cc + (st0 >= pair_t0 ? 0 : 1);
                     }
-                    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                    uint2 pk;
-                    pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-                    pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2 *>(ob + (r / p.G) * q_head_stride + (r % p.G) * D + col) = pk;
+                    contrib[i] = v;
                 }
+                if (ctid == 0 && tl > 0) contrib[n_list] = 2 * C + 2 * pair + 1;
+                named_bar_sync(1, NCW * 32);
+                const int n_merge = n_list + (tl > 0 ? 1 : 0);
+                // ... and merges them.
+                merge_partials<D, MT>(p, contrib, n_merge, ob, q_head_stride, ctid, NCW * 32);
             }
             named_bar_sync(1, NCW * 32);
         }
-        t += nseg;
     }
 }
 
@@ -516,7 +643,7 @@ template <int D, int MT>
 static size_t attn_fixed_smem(int B) {
     return 1024 /* alignment slack */ + 2 * (size_t)(D / 64) * MT * 16 * 128 /* query ring */ +
            (size_t)MT * 4 * 16 * (D + 4) * 4 + (size_t)MT * 64 * 4 * 2 + (size_t)MT * 16 * 4 * 2 +
-           (2 * kMaxStages + 4) * 8 + 16 + kMaxContrib * 4 + (size_t)(B + 1) * 4;
+           (2 * kMaxStages + 4) * 8 + 16 + 2 * sizeof(SegDesc) + kMaxContrib * 4 + (size_t)(B + 1) * 4;
 }
 
 template <int D>
@@ -524,23 +651,29 @@ static constexpr size_t attn_stage_bytes() {
     return 2 * (size_t)(D / 64) * kHalfBytes;
 }
 
-// Workspace layout: [counters: kAttnMaxPairs int32, always left zero]
-//                   [part_o: C_max * 2 * 32 * D fp32][part_ml: C_max * 2 * 32 * 2 fp32]
-// The counter region has a fixed size so that calls of any shape can share one
-// workspace: every call leaves it zeroed and nothing else is ever stored there.
-size_t attn_workspace_bytes(int B, int H_kv, int D, int M) {
-    (void)B; (void)H_kv; (void)M;
-    const int C = magicdec_host::sm_count() * 2;   // room for up to 2 CTAs per SM
-    const int MP = 32;                              // largest row tile count * 16
-    size_t counters = (size_t)kAttnMaxPairs * 4;
-    size_t po = (size_t)C * 2 * MP * D * 4;
-    size_t pml = (size_t)C * 2 * MP * 2 * 4;
-    return counters + po + pml;
+// Workspace layout: [counters: kAttnMaxPairs int32 | scheduler: 64 int32],
+// always left zero, then the partial slots, part_o [n_slots][rows][D] fp32
+// and part_ml [n_slots][rows][2] fp32, rows = M rounded up to 16.  n_slots:
+// two per CTA (up to two CTAs per SM) and, when tails are on, two per pair.
+// The counter head has a fixed size so that calls of any shape can share
+// one workspace; every call leaves it zeroed.
+static size_t attn_slots(int B, int H_kv, bool tails) {
+    return (size_t)4 * magicdec_host::sm_count() + (tails ? (size_t)2 * B * H_kv : 0);
 }
+
+static size_t attn_ws_bytes(int B, int H_kv, int D, int M, bool tails) {
+    const size_t rows = (size_t)((M + 15) / 16) * 16, n = attn_slots(B, H_kv, tails);
+    return kAttnCounterBytes + n * rows * D * 4 + n * rows * 2 * 4;
+}
+
+// What the entry points ask of callers (room for tails).
+size_t attn_workspace_bytes(int B, int H_kv, int D, int M) { return attn_ws_bytes(B, H_kv, D, M, true); }
+// The least the kernel can run with (no tails).
+size_t attn_workspace_bytes_min(int B, int H_kv, int D, int M) { return attn_ws_bytes(B, H_kv, D, M, false); }
 
 template <int D, int MT>
 static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                   const CUtensorMap &tmq, int B, void *ws, cudaStream_t st) {
+                                   const CUtensorMap &tmq, int B, void *ws, bool tails, cudaStream_t st) {
     const size_t fixed = attn_fixed_smem<D, MT>(B);
     const size_t sb = attn_stage_bytes<D>();
     const int smem_cap = magicdec_host::max_smem_optin();
@@ -560,10 +693,13 @@ static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MAGICDEC_ERR_CUDA;
     const int C = magicdec_host::sm_count() * ctas_per_sm;
+    if (C + 1 > kMaxContrib) return MAGICDEC_ERR_UNSUPPORTED;   // a merge lists every CTA and a tail
     uint8_t *w = static_cast<uint8_t *>(ws);
     prm.counters = reinterpret_cast<int *>(w);
-    prm.part_o = reinterpret_cast<float *>(w + (size_t)kAttnMaxPairs * 4);
-    prm.part_ml = prm.part_o + (size_t)magicdec_host::sm_count() * 2 * 2 * 32 * D;
+    prm.sched = prm.counters + kAttnMaxPairs;
+    prm.part_o = reinterpret_cast<float *>(w + kAttnCounterBytes);
+    prm.part_ml = prm.part_o + attn_slots(B, prm.H_kv, tails) * (MT * 16) * D;
+    prm.tails = tails ? 1 : 0;
     prm.stages = stages;
     prm.err = magicdec_host::device_error_word();
     return magicdec_host::launch_pdl(kern, dim3(C), dim3((4 * MT + 1) * 32), smem, st, tmk, tmv, tmq, prm);
@@ -572,7 +708,7 @@ static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const
 // Shared launcher for draft (head_major = 1, n_q = 1) and verify attention.
 magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, int n_q, int head_major,
                                    const void *q, const void *k, const void *v, const int32_t *len, void *out,
-                                   void *ws, cudaStream_t st) {
+                                   void *ws, size_t ws_bytes, cudaStream_t st) {
     AttnParams prm{};
     prm.q = static_cast<const __nv_bfloat16 *>(q);
     prm.len = len;
@@ -611,13 +747,18 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
     const uint32_t qbox[4] = {64, (uint32_t)prm.G, (uint32_t)n_q, 1};
     if (!magicdec_host::encode_tmap_bf16_4d(&tmq, q, qdims, qstrides, qbox)) return MAGICDEC_ERR_CUDA;
 
+    // Dynamic tails: only where some pair can have one, and the workspace has
+    // their slots (MAGICDEC_ATTN_TAILS=0 turns them off).
+    if (ws_bytes < attn_ws_bytes(B, H_kv, D, prm.M, false)) return MAGICDEC_ERR_WORKSPACE;
+    const bool tails = L_cap >= kTailMinTiles * kTileN && ws_bytes >= attn_ws_bytes(B, H_kv, D, prm.M, true) &&
+                       env_int("MAGICDEC_ATTN_TAILS", 1) != 0;
     const int MT = (prm.M + 15) / 16;
     if (D == 128) {
-        if (MT == 1) return launch_impl<128, 1>(prm, tmk, tmv, tmq, B, ws, st);
-        if (MT == 2) return launch_impl<128, 2>(prm, tmk, tmv, tmq, B, ws, st);
+        if (MT == 1) return launch_impl<128, 1>(prm, tmk, tmv, tmq, B, ws, tails, st);
+        if (MT == 2) return launch_impl<128, 2>(prm, tmk, tmv, tmq, B, ws, tails, st);
     } else if (D == 64) {
-        if (MT == 1) return launch_impl<64, 1>(prm, tmk, tmv, tmq, B, ws, st);
-        if (MT == 2) return launch_impl<64, 2>(prm, tmk, tmv, tmq, B, ws, st);
+        if (MT == 1) return launch_impl<64, 1>(prm, tmk, tmv, tmq, B, ws, tails, st);
+        if (MT == 2) return launch_impl<64, 2>(prm, tmk, tmv, tmq, B, ws, tails, st);
     }
     return MAGICDEC_ERR_UNSUPPORTED;
 }

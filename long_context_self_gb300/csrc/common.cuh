@@ -27,6 +27,9 @@ constexpr int kErrCapacity = 3;
 // attention kernels keep one counter per (sequence, KV head) pair, the
 // acceptance kernels one per sequence.
 constexpr int kAttnMaxPairs = 65536;
+// Attention workspace head: the per-pair merge counters, then 64 words of
+// scheduler state; every call leaves all of it zero.
+constexpr size_t kAttnCounterBytes = ((size_t)kAttnMaxPairs + 64) * 4;
 constexpr int kAcceptMaxBatch = 65536;
 
 // Bounded waits give up after this many polls or this much wall time.

@@ -25,13 +25,13 @@
 namespace magicdec {
 magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, int n_q, int head_major,
                                    const void *q, const void *k, const void *v, const int32_t *len, void *out,
-                                   void *ws, cudaStream_t st);
-size_t attn_workspace_bytes(int B, int H_kv, int D, int M);
+                                   void *ws, size_t ws_bytes, cudaStream_t st);
+size_t attn_workspace_bytes_min(int B, int H_kv, int D, int M);
 }  // namespace magicdec
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+constexpr size_t kNoAllocScratchBytes = 32u << 20;   // 32 MiB
 
 // The scratch itself: zero at module load; every call leaves its counter
 // region zero again.
@@ -50,7 +50,7 @@ magicdec_status scratch_address(void **out) {
     if (!g_scratch_addr[dev]) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return MAGICDEC_ERR_CUDA;
-        if (cudaMemset(ptr, 0, (size_t)magicdec::kAttnMaxPairs * 4) != cudaSuccess) return MAGICDEC_ERR_CUDA;
+        if (cudaMemset(ptr, 0, magicdec::kAttnCounterBytes) != cudaSuccess) return MAGICDEC_ERR_CUDA;
         g_scratch_addr[dev] = ptr;
     }
     *out = g_scratch_addr[dev];
@@ -71,11 +71,13 @@ extern "C" magicdec_status magicdec_verify_attn_noalloc(magicdec_kv_shape shape,
     if (!magicdec_host::aligned16(q) || !magicdec_host::aligned16(k) || !magicdec_host::aligned16(v) ||
         !magicdec_host::aligned16(out))
         return MAGICDEC_ERR_ALIGN;
-    const size_t need = magicdec::attn_workspace_bytes(shape.B, shape.H_kv, shape.d, (shape.H_q / shape.H_kv) * n_q);
+    // The kernel runs without dynamic tails when their slots do not fit.
+    const size_t need =
+        magicdec::attn_workspace_bytes_min(shape.B, shape.H_kv, shape.d, (shape.H_q / shape.H_kv) * n_q);
     if (need > kNoAllocScratchBytes) return MAGICDEC_ERR_UNSUPPORTED;   // more SMs than the array covers
     void *ws = nullptr;
     const magicdec_status s = scratch_address(&ws);
     if (s != MAGICDEC_OK) return s;
     return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, n_q, 0, q, k, v,
-                                        seq_len, out, ws, static_cast<cudaStream_t>(stream));
+                                        seq_len, out, ws, kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
 }

@@ -41,6 +41,12 @@ VERIFY_CASES = [
     (2, 4, 4, 128, 300, 4, [300, 257]),                                # MHA: H_kv == H_q
     (2, 16, 2, 64, 400, 4, [400, 390]),                                # d=64, 32 rows
     (7, 32, 8, 128, 4100, 4, [4100, 4000, 3999, 128, 2050, 17, 4033]),  # many tiles and splits
+    # pairs of >= 64 tiles hand a dynamic tail to the pool
+    (2, 32, 8, 128, 6000, 4, [6000, 5000]),                            # tails on every pair
+    (2, 40, 8, 128, 4500, 5, [4500, 4096]),                            # tails with 25 rows (two row tiles)
+    (2, 16, 2, 64, 5000, 4, [5000, 4200]),                             # tails with d=64, 32 rows
+    (1, 8, 1, 128, 9000, 4, [9000]),                                   # one pair over every CTA, plus its tail
+    (3, 4, 1, 128, 20000, 2, [20000, 3, 19999]),                       # a few long pairs, one short
 ]
 
 
@@ -71,6 +77,25 @@ def test_verify_attn_is_deterministic_and_split_invariant(monkeypatch):
     c = mb.magicdec_verify_attn(q, k, v, sl)
     torch.cuda.synchronize()
     check_attention(bf16_out_to_f64(c), bf16_out_to_f64(a).astype(np.float64), "split invariance")
+
+
+def test_verify_attn_dynamic_tails_deterministic_and_match_static_schedule(monkeypatch):
+    """With dynamic tails (pairs of >= 64 tiles) which CTA takes a tail varies from call
+    to call, but the chunk boundaries and the merge order do not: repeated calls agree
+    bit for bit, and the static schedule (tails off) agrees within the tolerance."""
+    B, H_q, H_kv, d, L_cap, n_q = 4, 32, 8, 128, 7000, 4
+    q, k, v = rand_bf16((B, n_q, H_q, d), 14).to(DEV), rand_bf16((B, L_cap, H_kv, d), 15).to(DEV), \
+        rand_bf16((B, L_cap, H_kv, d), 16).to(DEV)
+    sl = torch.tensor([7000, 6500, 4096, 100], dtype=torch.int32, device=DEV)
+    runs = [mb.magicdec_verify_attn(q, k, v, sl) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert all(torch.equal(runs[0], r) for r in runs[1:])
+    monkeypatch.setenv("MAGICDEC_ATTN_TAILS", "0")
+    static = mb.magicdec_verify_attn(q, k, v, sl)
+    torch.cuda.synchronize()
+    check_attention(bf16_out_to_f64(runs[0]), bf16_out_to_f64(static).astype(np.float64), "tails vs static")
+    ref = oracle.verify_attn(to_u16(q.cpu()), to_u16(k.cpu()), to_u16(v.cpu()), sl.cpu().numpy(), n_q)
+    check_attention(bf16_out_to_f64(runs[0]), ref, "verify with tails")
 
 
 # ----------------------------------------------------------------------- draft

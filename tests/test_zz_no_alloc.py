@@ -29,9 +29,11 @@ def test_noalloc_verify_matches_workspace_entry_point_on_two_calls():
     from long_context_self_gb300 import binding as mb
     from long_context_self_gb300 import build
     build.build()
-    B, H_q, H_kv, d, L_cap, n_q = 6, 32, 8, 128, 2500, 4
-    cases = [(101, [2500, 1, 0, 64, 1777, 2049]), (102, [300, 2500, 2499, 65, 128, 4])]
-    for seed, lens in cases:
+    B, H_q, H_kv, d, n_q = 6, 32, 8, 128, 4
+    # the third case has pairs of >= 64 tiles (dynamic tails)
+    cases = [(101, 2500, [2500, 1, 0, 64, 1777, 2049]), (102, 2500, [300, 2500, 2499, 65, 128, 4]),
+             (103, 5000, [5000, 4500, 17, 4096, 0, 4999])]
+    for seed, L_cap, lens in cases:
         q, k, v = _inputs(seed, B, H_q, H_kv, d, L_cap, n_q)
         sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
         ref = mb.magicdec_verify_attn(q, k, v, sl)
