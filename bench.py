@@ -46,7 +46,7 @@ DEFAULT_WORKLOAD = "llama8b_b128_l32k"
 METRIC = "verify/draft attn achieved HBM GB/s (% of peak); spec steps/s at B=128 L=32k"
 LAYERS = 32
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_attn_llama8b_b128_l32k.md")
-ATTN_SRC = os.path.join(ROOT, "long_context_self_gb300", "csrc", "attn.cu")
+ATTN_SRC = os.path.join(ROOT, "long_context_self_gb300", "csrc", "attn_heads.cu")   # the verification kernel at this shape
 
 
 # --------------------------------------------------------------------- helpers
@@ -106,7 +106,7 @@ def recorded_traffic(workload: str):
         if ": " in line and line.strip().startswith("- "):
             key, _, val = line.strip()[2:].partition(": ")   # keys may contain ':' (e.g. "sha256[:16]")
             vals[key.strip()] = val.strip().strip("`")
-    if vals.get("workload") != workload or vals.get("attn.cu sha256[:16]") != file_sha(ATTN_SRC):
+    if vals.get("workload") != workload or vals.get("attn_heads.cu sha256[:16]") != file_sha(ATTN_SRC):
         return None
     try:
         return float(vals["dram bytes per launch (full workload)"])
@@ -611,7 +611,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "per_rank_batch": w.B, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (KV cache 16.8 GB per layer vs 129 MB L2)",
                    "step": "layers x (select, gather, gamma x draft_attn, verify_attn) + spec_accept"},
-        "roofline": {"bound": "hbm", "kernel": "decode_attn_kernel (verify)", "achieved": round(ver_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": "verify_heads_kernel", "achieved": round(ver_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(ver_gbs / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": vbytes, "peak_source": peak_kind},
         "rows_roofline": rows,

@@ -406,6 +406,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
                 const int ch = ks * 2 + (mat >> 1);
                 ldsm_x4(qbase + (ch >> 3) * QHALF + swz128(row, ch & 7), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
             }
+            fence_proxy_async_smem();   // reads done before TMA may refill the buffer
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty_bar[qs]);
         }
@@ -504,6 +505,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
                     }
                 }
             }
+            fence_proxy_async_smem();   // reads done before TMA may refill the buffer
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
             if (++stage == stages) { stage = 0; phase ^= 1u; }
@@ -666,8 +668,18 @@ static size_t attn_ws_bytes(int B, int H_kv, int D, int M, bool tails) {
     return kAttnCounterBytes + n * rows * D * 4 + n * rows * 2 * 4;
 }
 
-// What the entry points ask of callers (room for tails).
-size_t attn_workspace_bytes(int B, int H_kv, int D, int M) { return attn_ws_bytes(B, H_kv, D, M, true); }
+bool verify_heads_supported(int H_kv, int D, int M);
+size_t verify_heads_ws_bytes(int ctas);
+magicdec_status launch_verify_heads(int B, int H_q, int L_cap, int n_q, const void *q, const void *k, const void *v,
+                                    const int32_t *len, void *out, void *ws, size_t ws_bytes, cudaStream_t st);
+
+// What the entry points ask of callers: room for tails and, where the shape
+// allows it, for the all-heads verification kernel at two CTAs per SM.
+size_t attn_workspace_bytes(int B, int H_kv, int D, int M) {
+    const size_t per_pair = attn_ws_bytes(B, H_kv, D, M, true);
+    const size_t heads = verify_heads_supported(H_kv, D, M) ? verify_heads_ws_bytes(2 * magicdec_host::sm_count()) : 0;
+    return per_pair > heads ? per_pair : heads;
+}
 // The least the kernel can run with (no tails).
 size_t attn_workspace_bytes_min(int B, int H_kv, int D, int M) { return attn_ws_bytes(B, H_kv, D, M, false); }
 
@@ -722,6 +734,14 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
     prm.M = prm.G * n_q;
     prm.head_major = head_major;
     prm.scale_log2 = kLog2e / sqrtf((float)D);
+
+    // Verification of d = 128, eight KV heads and at most 16 query rows per KV
+    // head streams all heads of a sequence together (attn_heads.cu) unless the
+    // workspace cannot hold its partials (MAGICDEC_ATTN_HEADS=0 turns it off).
+    if (!head_major && verify_heads_supported(H_kv, D, prm.M) && env_int("MAGICDEC_ATTN_HEADS", 1) != 0) {
+        const magicdec_status s = launch_verify_heads(B, H_q, L_cap, n_q, q, k, v, len, out, ws, ws_bytes, st);
+        if (s != MAGICDEC_ERR_WORKSPACE) return s;
+    }
 
     // 4-D views, innermost first.  Verify: (d, H_kv, L_cap, B); draft: (d, cap, H_kv, B).
     CUtensorMap tmk, tmv;

@@ -144,8 +144,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
 
-// Order this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA) accesses of the same bytes.
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses of the same bytes: writes before a TMA store
+// reads them, and reads (ldmatrix of a TMA-filled buffer) before the buffer
+// is handed back to be refilled -- without it, a refill issued right after
+// the mbarrier release was seen to overwrite rows a warp was still reading.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

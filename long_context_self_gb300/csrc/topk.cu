@@ -213,6 +213,7 @@ __global__ void __launch_bounds__((kTkConsumers + 1) * 32, 2)
             ldsm_x4(base + (ch >> 3) * kTkHalfBytes + swz128(a_row, ch & 7), a[0], a[1], a[2], a[3]);
             mma_bf16(acc, a, bq[ks][0], bq[ks][1]);
         }
+        fence_proxy_async_smem();   // reads done before TMA may refill the buffer
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
 

@@ -47,6 +47,13 @@ VERIFY_CASES = [
     (2, 16, 2, 64, 5000, 4, [5000, 4200]),                             # tails with d=64, 32 rows
     (1, 8, 1, 128, 9000, 4, [9000]),                                   # one pair over every CTA, plus its tail
     (3, 4, 1, 128, 20000, 2, [20000, 3, 19999]),                       # a few long pairs, one short
+    # d = 128 with eight KV heads and <= 16 rows per KV head: the all-heads kernel
+    (3, 32, 8, 128, 2000, 3, [2000, 1999, 700]),                       # 12 rows per KV head
+    (2, 16, 8, 128, 1000, 4, [1000, 513]),                             # G = 2, 8 rows
+    (2, 8, 8, 128, 700, 16, [700, 650]),                               # G = 1, 16 speculated tokens
+    (4, 32, 8, 128, 64, 4, [64, 1, 0, 9]),                             # fewer tiles than CTAs
+    (1, 32, 8, 128, 9000, 4, [9000]),                                  # one sequence over every CTA
+    (2, 32, 8, 128, 3000, 1, [3000, 17]),                              # one query token
 ]
 
 
@@ -83,6 +90,7 @@ def test_verify_attn_dynamic_tails_deterministic_and_match_static_schedule(monke
     """With dynamic tails (pairs of >= 64 tiles) which CTA takes a tail varies from call
     to call, but the chunk boundaries and the merge order do not: repeated calls agree
     bit for bit, and the static schedule (tails off) agrees within the tolerance."""
+    monkeypatch.setenv("MAGICDEC_ATTN_HEADS", "0")                     # the per-pair kernel, which has tails
     B, H_q, H_kv, d, L_cap, n_q = 4, 32, 8, 128, 7000, 4
     q, k, v = rand_bf16((B, n_q, H_q, d), 14).to(DEV), rand_bf16((B, L_cap, H_kv, d), 15).to(DEV), \
         rand_bf16((B, L_cap, H_kv, d), 16).to(DEV)
@@ -96,6 +104,50 @@ def test_verify_attn_dynamic_tails_deterministic_and_match_static_schedule(monke
     check_attention(bf16_out_to_f64(runs[0]), bf16_out_to_f64(static).astype(np.float64), "tails vs static")
     ref = oracle.verify_attn(to_u16(q.cpu()), to_u16(k.cpu()), to_u16(v.cpu()), sl.cpu().numpy(), n_q)
     check_attention(bf16_out_to_f64(runs[0]), ref, "verify with tails")
+
+
+@pytest.mark.parametrize("heads", ["1", "0"])
+def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch, heads):
+    """Two CTAs per SM (a grid that runs in two waves) and two pipeline stages: short
+    sequence runs reuse the query slot and the stages right after releasing them, the
+    case where a refill issued without a proxy fence overwrote rows a warp was still
+    reading (a 64-position sequence split over three CTAs).  The schedule is fixed, so
+    every call must give the same bits, and match the oracle."""
+    monkeypatch.setenv("MAGICDEC_ATTN_HEADS", heads)
+    monkeypatch.setenv("MAGICDEC_ATTN_CTAS_PER_SM", "2")
+    monkeypatch.setenv("MAGICDEC_ATTN_STAGES", "2")
+    B, H_q, H_kv, d, L_cap, n_q = 6, 32, 8, 128, 3000, 4
+    q, k, v = rand_bf16((B, n_q, H_q, d), 4), rand_bf16((B, L_cap, H_kv, d), 5), rand_bf16((B, L_cap, H_kv, d), 6)
+    sl = torch.tensor([3000, 2999, 1500, 64, 700, 2222], dtype=torch.int32)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    first = mb.magicdec_verify_attn(qd, kd, vd, sld)
+    for _ in range(30):
+        again = mb.magicdec_verify_attn(qd, kd, vd, sld)
+        torch.cuda.synchronize()
+        assert torch.equal(first, again)
+    ref = oracle.verify_attn(to_u16(q), to_u16(k), to_u16(v), sl.numpy(), n_q)
+    check_attention(bf16_out_to_f64(first), ref, "verify, two waves of CTAs")
+
+
+def test_verify_attn_per_pair_and_all_heads_kernels_agree(monkeypatch):
+    """The Llama-3.1-8B verification shape runs the all-heads kernel; the per-pair
+    kernel (MAGICDEC_ATTN_HEADS=0) on the same inputs matches the oracle too, and the
+    two agree within the attention tolerance."""
+    B, H_q, H_kv, d, L_cap, n_q = 5, 32, 8, 128, 2600, 4
+    q = rand_bf16((B, n_q, H_q, d), 21)
+    k = rand_bf16((B, L_cap, H_kv, d), 22)
+    v = rand_bf16((B, L_cap, H_kv, d), 23)
+    k[:, ::53] *= 4
+    sl = torch.tensor([2600, 2, 1300, 0, 2599], dtype=torch.int32)
+    ref = oracle.verify_attn(to_u16(q), to_u16(k), to_u16(v), sl.numpy(), n_q)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    heads = mb.magicdec_verify_attn(qd, kd, vd, sld)
+    monkeypatch.setenv("MAGICDEC_ATTN_HEADS", "0")
+    pair = mb.magicdec_verify_attn(qd, kd, vd, sld)
+    torch.cuda.synchronize()
+    check_attention(bf16_out_to_f64(heads), ref, "verify, all-heads kernel")
+    check_attention(bf16_out_to_f64(pair), ref, "verify, per-pair kernel")
+    check_attention(bf16_out_to_f64(heads), bf16_out_to_f64(pair).astype(np.float64), "all-heads vs per-pair")
 
 
 # ----------------------------------------------------------------------- draft

@@ -40,8 +40,8 @@ def test_aggregate_rate_is_whole_job():
 
 
 def test_recorded_traffic_is_read_from_the_committed_profile():
-    """The bench reports the verification kernel's ncu DRAM bytes from profiles/ while attn.cu is the
-    source the capture was taken on; the recorded traffic equals the algorithmic bytes within 1 %."""
+    """The bench reports the verification kernel's ncu DRAM bytes from profiles/ while attn_heads.cu is
+    the source the capture was taken on; the recorded traffic equals the algorithmic bytes within 1 %."""
     t = bench.recorded_traffic("llama8b_b128_l32k")
     assert t is not None
     w = bench.synth.WORKLOADS["llama8b_b128_l32k"]
