@@ -231,6 +231,153 @@ __global__ void __launch_bounds__((kTkConsumers + 1) * 32, 2)
     }
 }
 
+// All eight KV heads of a sequence per stage (d = 128, H_kv = 8, G <= 8): a
+// stage is 16 positions x 8 heads of K, 32 KB contiguous in the
+// [B, L_cap, H_kv, d] cache, loaded as two TMA boxes of 64 channels x 16
+// positions x 8 heads from a tensor map whose position stride precedes its
+// head stride (each head's 16 rows are consecutive swizzled rows in shared
+// memory).  Consumer warp h forms S^T = K_h Q_h^T for head h's 16 positions
+// and G query heads.  The per-pair kernel above fetches 256-byte rows 2 KB
+// apart; this traversal streams the same bytes faster.
+constexpr int kTkHdHeads = 8, kTkHdPos = 16;
+constexpr int kTkHdHalf = kTkHdPos * kTkHdHeads * 128;   // 16 KB: one 64-channel half of a stage
+constexpr int kTkHdStage = 2 * kTkHdHalf;
+
+__global__ void __launch_bounds__((kTkHdHeads + 1) * 32, 2)
+    topk_scores_heads_kernel(const __grid_constant__ CUtensorMap tmk, const TopkScoreParams p) {
+    constexpr int D = 128, KS = D / 16;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *stage_base = smem;
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + (size_t)p.stages * kTkHdStage);
+    uint64_t *empty_bar = full_bar + kTkMaxStages;
+    int *prefix = reinterpret_cast<int *>(empty_bar + kTkMaxStages);   // [B + 1]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    pdl_trigger();
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kTkHdHeads);
+        }
+        mbar_fence_init();
+        prefetch_tensormap(&tmk);
+    }
+    pdl_wait();
+    for (int b = tid; b < p.B; b += blockDim.x)
+        prefix[b] = (tk_clamp_len(__ldg(p.len + b), p.L_cap) + kTkHdPos - 1) / kTkHdPos;
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            const int nt = b < p.B ? prefix[b] : 0;
+            int x = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (b < p.B) prefix[b] = run + x - nt;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) prefix[p.B] = run;
+    }
+    __syncthreads();
+
+    // flat list of 16-position tiles ordered (sequence, tile), split evenly across CTAs
+    const long long T = prefix[p.B];
+    const int C = gridDim.x, c = blockIdx.x;
+    const long long t_begin = T * c / C, t_end = T * (c + 1) / C;
+    const int n = (int)(t_end - t_begin);
+    if (n <= 0) return;
+    auto seq_of = [&](long long t) {
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+
+    if (warp == kTkHdHeads) {
+        // ------------------------------------------------------- producer (1 thread)
+        if (lane != 0) return;
+        const uint64_t pol = policy_evict_first();
+        int i = 0;
+        for (; i < n; ++i) {
+            const long long t = t_begin + i;
+            const int b = seq_of(t);
+            const int pos0 = (int)(t - prefix[b]) * kTkHdPos;
+            const int stage = i % p.stages;
+            const uint32_t phase = (uint32_t)(i / p.stages) & 1u;
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, p.err)) break;
+            mbar_arrive_expect_tx(&full_bar[stage], kTkHdStage);
+            uint8_t *dst = stage_base + (size_t)stage * kTkHdStage;
+            tma_load_4d(dst, &tmk, 0, pos0, 0, b, &full_bar[stage], pol);
+            tma_load_4d(dst + kTkHdHalf, &tmk, 64, pos0, 0, b, &full_bar[stage], pol);
+        }
+        // the copies issued last land before the CTA may exit
+        for (int k = i > p.stages ? i - p.stages : 0; k < i; ++k)
+            mbar_wait(&full_bar[k % p.stages], (uint32_t)(k / p.stages) & 1u, p.err);
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    // Warp h: A = K_h rows (16 positions x 16 channels per k-step) via
+    // ldmatrix; B = Q^T of head h's G query heads, loaded into fragments.
+    const int h = warp;
+    const int mat = lane >> 3, rr = lane & 7;
+    const int a_row = h * kTkHdPos + (mat & 1) * 8 + rr;
+    const int a_half = mat >> 1;
+    const int g0 = 2 * (lane & 3), key_l = lane >> 2;
+    int qb_b = -1;
+    uint32_t bq[KS][2];
+    for (int i = 0; i < n; ++i) {
+        const long long t = t_begin + i;
+        const int b = seq_of(t);
+        if (b != qb_b) {
+            qb_b = b;
+            const int nrow = lane >> 2;
+            const bool valid = nrow < p.G;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                p.q + ((long long)b * p.H_q + h * p.G + (valid ? nrow : 0)) * D);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                bq[ks][0] = valid ? __ldg(qrow + ks * 8 + (lane & 3)) : 0u;
+                bq[ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + (lane & 3)) : 0u;
+            }
+        }
+        const int stage = i % p.stages;
+        const uint32_t phase = (uint32_t)(i / p.stages) & 1u;
+        if (!mbar_wait(&full_bar[stage], phase, p.err)) break;
+        const uint32_t base = smem_u32(stage_base + (size_t)stage * kTkHdStage);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int ch = ks * 2 + a_half;     // 8-channel chunk index over D
+            uint32_t a[4];
+            ldsm_x4(base + (ch >> 3) * kTkHdHalf + swz128(a_row, ch & 7), a[0], a[1], a[2], a[3]);
+            mma_bf16(acc, a, bq[ks][0], bq[ks][1]);
+        }
+        fence_proxy_async_smem();   // reads done before TMA may refill the buffer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+
+        const int len = tk_clamp_len(__ldg(p.len + b), p.L_cap);
+        const int pos = (int)(t - prefix[b]) * kTkHdPos + key_l;
+        float *srow = p.score + ((long long)b * p.H_q + (long long)h * p.G) * p.L_sc;
+        if (g0 < p.G) {
+            if (pos < len) srow[(long long)g0 * p.L_sc + pos] = acc[0] * p.scale;
+            if (pos + 8 < len) srow[(long long)g0 * p.L_sc + pos + 8] = acc[2] * p.scale;
+        }
+        if (g0 + 1 < p.G) {
+            if (pos < len) srow[(long long)(g0 + 1) * p.L_sc + pos] = acc[1] * p.scale;
+            if (pos + 8 < len) srow[(long long)(g0 + 1) * p.L_sc + pos + 8] = acc[3] * p.scale;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- selection
 // Order-preserving key of an fp32 value (larger value -> larger key); 0 marks
 // "no position".
@@ -730,22 +877,33 @@ static magicdec_status launch_select_attn(TopkSelParams tp, int mode, cudaStream
 
 template <int D>
 static magicdec_status launch_topk_impl(const TopkScoreParams &sp, const TopkSelParams &tp, const CUtensorMap &tmk,
-                                        cudaStream_t st) {
-    constexpr int STAGE_BYTES = (D / 64) * kTkHalfBytes;
+                                        bool heads, cudaStream_t st) {
+    // heads: topk_scores_heads_kernel (32 KB stages of all eight heads); else
+    // the per-pair kernel (16 KB stages of one head).  Two CTAs per SM either way.
+    const int stage_bytes = heads ? kTkHdStage : (D / 64) * kTkHalfBytes;
     const int smem_cap = magicdec_host::max_smem_optin();
     const size_t fixed = 1024 + 2 * kTkMaxStages * sizeof(uint64_t) + (size_t)(sp.B + 1) * sizeof(int);
-    const size_t per_cta = (size_t)smem_cap / 2 - 1024;          // two CTAs per SM
-    if (per_cta <= fixed + 2 * STAGE_BYTES) return MAGICDEC_ERR_UNSUPPORTED;
-    int stages = (int)((per_cta - fixed) / STAGE_BYTES);
+    const size_t per_cta = (size_t)smem_cap / 2 - 1024;
+    if (per_cta <= fixed + 2 * (size_t)stage_bytes) return MAGICDEC_ERR_UNSUPPORTED;
+    int stages = (int)((per_cta - fixed) / stage_bytes);
     if (stages > kTkMaxStages) stages = kTkMaxStages;
     TopkScoreParams s1 = sp;
     s1.stages = stages;
-    const size_t smem1 = fixed + (size_t)stages * STAGE_BYTES;
-    auto k1 = topk_scores_kernel<D>;
-    if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) != cudaSuccess)
-        return MAGICDEC_ERR_CUDA;
-    magicdec_status s = magicdec_host::launch_pdl(k1, dim3(magicdec_host::sm_count() * 2),
-                                                  dim3((kTkConsumers + 1) * 32), smem1, st, tmk, s1);
+    const size_t smem1 = fixed + (size_t)stages * stage_bytes;
+    magicdec_status s;
+    if (heads) {
+        auto k1 = topk_scores_heads_kernel;
+        if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) != cudaSuccess)
+            return MAGICDEC_ERR_CUDA;
+        s = magicdec_host::launch_pdl(k1, dim3(magicdec_host::sm_count() * 2), dim3((kTkHdHeads + 1) * 32), smem1, st,
+                                      tmk, s1);
+    } else {
+        auto k1 = topk_scores_kernel<D>;
+        if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) != cudaSuccess)
+            return MAGICDEC_ERR_CUDA;
+        s = magicdec_host::launch_pdl(k1, dim3(magicdec_host::sm_count() * 2), dim3((kTkConsumers + 1) * 32), smem1, st,
+                                      tmk, s1);
+    }
     if (s != MAGICDEC_OK) return s;
 
     return launch_select_attn<D>(tp, kSelScores, st);
@@ -786,15 +944,26 @@ magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_ca
     tp.L_sc = L_sc;
     tp.top_k = top_k;
 
-    // K as (d, H_kv, L_cap, B); one box = 64 channels x 1 head x 64 positions
     CUtensorMap tmk;
     const uint64_t e = 2;
-    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H_kv, (uint64_t)L_cap, (uint64_t)B};
-    const uint64_t strides[3] = {(uint64_t)D * e, (uint64_t)H_kv * D * e, (uint64_t)L_cap * H_kv * D * e};
-    const uint32_t box[4] = {64, 1, kTkTileN, 1};
-    if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box)) return MAGICDEC_ERR_CUDA;
-    if (D == 128) return launch_topk_impl<128>(sp, tp, tmk, st);
-    if (D == 64) return launch_topk_impl<64>(sp, tp, tmk, st);
+    const char *env = getenv("MAGICDEC_TOPK_HEADS");
+    const bool heads = D == 128 && H_kv == kTkHdHeads && !(env && env[0] == '0');
+    if (heads) {
+        // K as (d, L_cap, H_kv, B), the position stride before the head stride;
+        // one box = 64 channels x 16 positions x 8 heads
+        const uint64_t dims[4] = {(uint64_t)D, (uint64_t)L_cap, (uint64_t)H_kv, (uint64_t)B};
+        const uint64_t strides[3] = {(uint64_t)H_kv * D * e, (uint64_t)D * e, (uint64_t)L_cap * H_kv * D * e};
+        const uint32_t box[4] = {64, (uint32_t)kTkHdPos, (uint32_t)kTkHdHeads, 1};
+        if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box)) return MAGICDEC_ERR_CUDA;
+    } else {
+        // K as (d, H_kv, L_cap, B); one box = 64 channels x 1 head x 64 positions
+        const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H_kv, (uint64_t)L_cap, (uint64_t)B};
+        const uint64_t strides[3] = {(uint64_t)D * e, (uint64_t)H_kv * D * e, (uint64_t)L_cap * H_kv * D * e};
+        const uint32_t box[4] = {64, 1, kTkTileN, 1};
+        if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box)) return MAGICDEC_ERR_CUDA;
+    }
+    if (D == 128) return launch_topk_impl<128>(sp, tp, tmk, heads, st);
+    if (D == 64) return launch_topk_impl<64>(sp, tp, tmk, false, st);
     return MAGICDEC_ERR_UNSUPPORTED;
 }
 

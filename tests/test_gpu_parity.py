@@ -474,6 +474,7 @@ TOPK_CASES = [
     (1, 40, 8, 128, 20000, 4096, [20000]),                             # G=5, a 4096 budget
     (2, 4, 4, 128, 1500, 64, [1500, 900]),                             # MHA: G=1
     (2, 4, 2, 64, 1000, 100, [1000, 999]),                             # G=2, d=64
+    (3, 64, 8, 128, 1700, 128, [1700, 15, 1009]),                      # G=8 over eight KV heads, ragged tiles
 ]
 
 
@@ -493,6 +494,26 @@ def test_topk_draft_attn_matches_oracle(B, H_q, H_kv, d, L_cap, top_k, lens):
     for b, L in enumerate(lens):
         if L == 0:
             assert torch.count_nonzero(out[b]) == 0
+
+
+def test_topk_scores_all_heads_and_per_pair_kernels_agree(monkeypatch):
+    """At d = 128 with eight KV heads the scores come from the kernel that streams all
+    heads of a sequence per stage; the per-pair kernel (MAGICDEC_TOPK_HEADS=0) runs the
+    same mma sequence per (position, query head), so the kept positions are identical
+    and the outputs equal."""
+    B, H_q, H_kv, d, L_cap, top_k = 3, 32, 8, 128, 2500, 256
+    q = rand_bf16((B, 1, H_q, d), 51).to(DEV)
+    k = rand_bf16((B, L_cap, H_kv, d), 52).to(DEV)
+    v = rand_bf16((B, L_cap, H_kv, d), 53).to(DEV)
+    sl = torch.tensor([2500, 1999, 300], dtype=torch.int32, device=DEV)
+    idx_h = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    idx_p = torch.empty_like(idx_h)
+    out_h = mb.magicdec_topk_draft_attn(q, k, v, sl, top_k, idx=idx_h)
+    monkeypatch.setenv("MAGICDEC_TOPK_HEADS", "0")
+    out_p = mb.magicdec_topk_draft_attn(q, k, v, sl, top_k, idx=idx_p)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_h, idx_p)
+    assert torch.equal(out_h, out_p)
 
 
 def test_topk_draft_attn_ties_go_to_smaller_positions():
