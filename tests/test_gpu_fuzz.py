@@ -1,0 +1,98 @@
+"""Randomised shapes and length mixes for the all-heads kernels (d = 128, eight KV
+heads): verification against the per-pair kernel and against itself across repeated
+calls, and the Top-K score pass against the per-pair score kernel.  Seeded; each case
+is small (a few MB), so the whole file runs in seconds."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from long_context_self_gb300 import binding as mb
+from parity_util import bf16_out_to_f64, check_attention
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from long_context_self_gb300 import build
+    build.build()
+    mb.lib()
+    yield
+    assert mb.magicdec_device_error() == 0
+
+
+def _lengths(rng, B, L_cap):
+    kinds = rng.integers(0, 5, size=B)
+    lens = []
+    for k in kinds:
+        if k == 0:
+            lens.append(int(L_cap))                      # full
+        elif k == 1:
+            lens.append(int(rng.integers(0, 9)))         # empty or shorter than a tile
+        elif k == 2:
+            lens.append(int(rng.integers(1, L_cap + 1)))
+        elif k == 3:
+            lens.append(int(max(0, L_cap - rng.integers(0, 17))))
+        else:
+            lens.append(int(rng.integers(1, 65)))
+    return [min(x, L_cap) for x in lens]
+
+
+def _case(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 24))
+    L_cap = int(rng.choice([8, 63, 200, 1000, 2500, 4100, 7000]))
+    G = int(rng.choice([1, 2, 4]))
+    n_q = int(rng.integers(1, 16 // G + 1)) if G < 4 else int(rng.integers(1, 5))
+    n_q = min(n_q, 4)
+    return rng, B, L_cap, G, n_q, _lengths(rng, B, L_cap)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_verify_all_heads_fuzz(seed, monkeypatch):
+    rng, B, L_cap, G, n_q, lens = _case(seed)
+    H_kv, d = 8, 128
+    H_q = G * H_kv
+    g = torch.Generator().manual_seed(1000 + seed)
+    q = torch.randn((B, n_q, H_q, d), generator=g).to(torch.bfloat16).to(DEV)
+    k = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16).to(DEV)
+    v = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16).to(DEV)
+    sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    monkeypatch.setenv("MAGICDEC_ATTN_CTAS_PER_SM", str(int(rng.integers(1, 3))))
+    monkeypatch.setenv("MAGICDEC_ATTN_STAGES", str(int(rng.choice([0, 2, 3]))))
+    a = mb.magicdec_verify_attn(q, k, v, sl)
+    b = mb.magicdec_verify_attn(q, k, v, sl)
+    monkeypatch.setenv("MAGICDEC_ATTN_HEADS", "0")
+    ref = mb.magicdec_verify_attn(q, k, v, sl)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b), "all-heads verification is not reproducible"
+    check_attention(bf16_out_to_f64(a), bf16_out_to_f64(ref).astype(np.float64),
+                    f"all-heads vs per-pair, B={B} L={L_cap} G={G} n_q={n_q} lens={lens}")
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(a[i]) == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_topk_scores_all_heads_fuzz(seed, monkeypatch):
+    rng, B, L_cap, G, _, lens = _case(seed)
+    H_kv, d = 8, 128
+    H_q = G * H_kv
+    top_k = int(rng.choice([1, 16, 100, 512]))
+    g = torch.Generator().manual_seed(2000 + seed)
+    q = torch.randn((B, 1, H_q, d), generator=g).to(torch.bfloat16).to(DEV)
+    k = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16).to(DEV)
+    v = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16).to(DEV)
+    sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    idx_h = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    idx_p = torch.empty_like(idx_h)
+    out_h = mb.magicdec_topk_draft_attn(q, k, v, sl, top_k, idx=idx_h)
+    monkeypatch.setenv("MAGICDEC_TOPK_HEADS", "0")
+    out_p = mb.magicdec_topk_draft_attn(q, k, v, sl, top_k, idx=idx_p)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_h, idx_p)
+    assert torch.equal(out_h, out_p)
