@@ -706,6 +706,9 @@ static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const
         return MAGICDEC_ERR_CUDA;
     const int C = magicdec_host::sm_count() * ctas_per_sm;
     if (C + 1 > kMaxContrib) return MAGICDEC_ERR_UNSUPPORTED;   // a merge lists every CTA and a tail
+    // One tail per pair: with fewer than two per CTA the few CTAs that take one
+    // finish after everyone else's static share, so the pool would unbalance.
+    if ((long long)B * prm.H_kv < 2LL * C) tails = false;
     uint8_t *w = static_cast<uint8_t *>(ws);
     prm.counters = reinterpret_cast<int *>(w);
     prm.sched = prm.counters + kAttnMaxPairs;
@@ -767,11 +770,13 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
     const uint32_t qbox[4] = {64, (uint32_t)prm.G, (uint32_t)n_q, 1};
     if (!magicdec_host::encode_tmap_bf16_4d(&tmq, q, qdims, qstrides, qbox)) return MAGICDEC_ERR_CUDA;
 
-    // Dynamic tails: only where some pair can have one, and the workspace has
-    // their slots (MAGICDEC_ATTN_TAILS=0 turns them off).
+    // Dynamic tails are opt-in (MAGICDEC_ATTN_TAILS=1): measured, they tighten
+    // the CTAs' finishing times but cost one more partial epilogue per pair, a
+    // wash at B=128 and 2.6 % slower at B=64 with 20 rows per KV head.  Only
+    // where some pair can have one and the workspace has their slots.
     if (ws_bytes < attn_ws_bytes(B, H_kv, D, prm.M, false)) return MAGICDEC_ERR_WORKSPACE;
     const bool tails = L_cap >= kTailMinTiles * kTileN && ws_bytes >= attn_ws_bytes(B, H_kv, D, prm.M, true) &&
-                       env_int("MAGICDEC_ATTN_TAILS", 1) != 0;
+                       env_int("MAGICDEC_ATTN_TAILS", 0) != 0;
     const int MT = (prm.M + 15) / 16;
     if (D == 128) {
         if (MT == 1) return launch_impl<128, 1>(prm, tmk, tmv, tmq, B, ws, tails, st);

@@ -87,23 +87,30 @@ def test_verify_attn_is_deterministic_and_split_invariant(monkeypatch):
 
 
 def test_verify_attn_dynamic_tails_deterministic_and_match_static_schedule(monkeypatch):
-    """With dynamic tails (pairs of >= 64 tiles) which CTA takes a tail varies from call
-    to call, but the chunk boundaries and the merge order do not: repeated calls agree
-    bit for bit, and the static schedule (tails off) agrees within the tolerance."""
-    monkeypatch.setenv("MAGICDEC_ATTN_HEADS", "0")                     # the per-pair kernel, which has tails
-    B, H_q, H_kv, d, L_cap, n_q = 4, 32, 8, 128, 7000, 4
-    q, k, v = rand_bf16((B, n_q, H_q, d), 14).to(DEV), rand_bf16((B, L_cap, H_kv, d), 15).to(DEV), \
-        rand_bf16((B, L_cap, H_kv, d), 16).to(DEV)
-    sl = torch.tensor([7000, 6500, 4096, 100], dtype=torch.int32, device=DEV)
-    runs = [mb.magicdec_verify_attn(q, k, v, sl) for _ in range(3)]
+    """With dynamic tails (per-pair kernel, pairs of >= 64 tiles, at least two pairs per
+    CTA) which CTA takes a tail varies from call to call, but the chunk boundaries and
+    the merge order do not: repeated calls agree bit for bit, the static schedule (tails
+    off) agrees within the tolerance, and sampled sequences match the oracle."""
+    monkeypatch.setenv("MAGICDEC_ATTN_HEADS", "0")
+    monkeypatch.setenv("MAGICDEC_ATTN_TAILS", "1")                     # opt-in
+    B, H_q, H_kv, d, L_cap, n_q = 40, 40, 8, 128, 4200, 4          # 320 pairs, 20 rows per KV head
+    g = torch.Generator().manual_seed(17)
+    lens = torch.randint(3000, L_cap + 1, (B,), generator=g)
+    lens[::7] = L_cap
+    lens[3] = 5
+    sl = lens.to(torch.int32)
+    q, k, v = rand_bf16((B, n_q, H_q, d), 14), rand_bf16((B, L_cap, H_kv, d), 15), rand_bf16((B, L_cap, H_kv, d), 16)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    runs = [mb.magicdec_verify_attn(qd, kd, vd, sld) for _ in range(3)]
     torch.cuda.synchronize()
     assert all(torch.equal(runs[0], r) for r in runs[1:])
     monkeypatch.setenv("MAGICDEC_ATTN_TAILS", "0")
-    static = mb.magicdec_verify_attn(q, k, v, sl)
+    static = mb.magicdec_verify_attn(qd, kd, vd, sld)
     torch.cuda.synchronize()
     check_attention(bf16_out_to_f64(runs[0]), bf16_out_to_f64(static).astype(np.float64), "tails vs static")
-    ref = oracle.verify_attn(to_u16(q.cpu()), to_u16(k.cpu()), to_u16(v.cpu()), sl.cpu().numpy(), n_q)
-    check_attention(bf16_out_to_f64(runs[0]), ref, "verify with tails")
+    pick = [0, 3, 7, 22, 39]
+    ref = oracle.verify_attn(to_u16(q[pick]), to_u16(k[pick]), to_u16(v[pick]), sl[pick].numpy(), n_q)
+    check_attention(bf16_out_to_f64(runs[0][pick]), ref, "verify with tails")
 
 
 @pytest.mark.parametrize("heads", ["1", "0"])
