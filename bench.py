@@ -578,14 +578,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             pq.pop("_pq_bytes"), pq_ms, "shared-memory lookup-table reads (score pass); latency (select)")
         b_ms = pq.pop("_pq_build_ms")
         rows["pq_build (2 Lloyd iterations + encode, once per prefill)"] = row(
-            pq.pop("_pq_build_bytes"), b_ms, "fp32 FMA (encode: nearest of C centroids per subspace)")
-        # encode: per (position, KV head, subspace, centroid) an 8-term dot product and a norm term
+            pq.pop("_pq_build_bytes"), b_ms,
+            "ALU issue (encode: argmin over C centroids per subspace; the dot products on the tensor cores)")
+        # encode: per (position, KV head, subspace, centroid) an 8-term dot product and a norm
+        # term, as FP32-FMA flops; the encoder runs the dot products as bf16 tensor-core MMAs
+        # over an exact three-piece split of the centroids, so this is the equivalent rate
         fl = 3.0 * w.B * w.L * w.H_kv * pq["pq_M"] * pq["pq_C"] * 9 * 2
         alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
         rows["pq_build (2 Lloyd iterations + encode, once per prefill)"]["alu"] = {
             "tflops": round(fl / (b_ms * 1e-3) / 1e12, 2), "peak_tflops": round(alu_peak, 1),
             "frac": round(fl / (b_ms * 1e-3) / 1e12 / alu_peak, 4),
-            "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz (nominal)"}
+            "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz (nominal); FP32-FMA-equivalent flops of "
+                           "the encodes, whose dot products run on the tensor cores"}
         pq["pq_over_verify"] = round(pq_ms / ver_ms, 4)
     if topk:
         tk_ms = topk.pop("_topk_ms")

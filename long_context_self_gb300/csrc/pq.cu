@@ -358,9 +358,192 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
 }
 
 // ------------------------------------------------------------------- host side
+// Nearest centroid on the tensor cores.  The dot products k_m . c of a
+// subspace are a (keys x 8) x (8 x C) contraction; each fp32 centroid is split
+// exactly into three bf16 pieces (hi = bf16(c), mid = bf16(c - hi),
+// lo = c - hi - mid), stored times -2 (exact), every product of a bf16 key
+// value with a piece is exact in fp32, and three m16n8k8 bf16 MMAs into an
+// accumulator started at |c|^2 leave |c|^2 - 2 k.c to fp32 accuracy.  The
+// argmin (ties: the smaller index) stays in fp32 on the ALU, which now bounds
+// the kernel.  Shared memory: the pieces
+// [3][M][CP][8] bf16 and the norms [M][CP] fp32 of one (sequence, KV head)
+// codebook, CP = C rounded up to 32 (padding centroids have an infinite norm
+// and are never chosen).
+__device__ __forceinline__ void pq_mma_k8(float (&c)[4], const uint32_t (&a)[2], uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(b0));
+}
+
+constexpr int kPqTcThreads = 512;
+constexpr int kPqTcKeys = 16;                      // keys per warp batch (one m16 tile)
+
+template <int D>
+__global__ void __launch_bounds__(kPqTcThreads, 1)
+    pq_encode_tc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ codebook,
+                        uint8_t *__restrict__ codes, int H_kv, int L_cap, int C, int CP) {
+    constexpr int M = D / kPqDs;
+    extern __shared__ __align__(128) uint8_t pq_tc_smem[];
+    uint8_t *pieces = pq_tc_smem;                                          // [3][M][CP][8] bf16
+    float *nrm = reinterpret_cast<float *>(pq_tc_smem + (size_t)3 * M * CP * 16);   // [M][CP]
+    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    pdl_wait();
+    const float *cbh = codebook + ((size_t)b * H_kv + h) * M * C * kPqDs;
+    for (int i = tid; i < M * CP; i += kPqTcThreads) {
+        const int m = i / CP, c = i - m * CP;
+        uint32_t w[3][4];
+        float n = INFINITY;
+        if (c < C) {
+            const float4 u0 = __ldg(reinterpret_cast<const float4 *>(cbh + ((size_t)m * C + c) * kPqDs));
+            const float4 u1 = __ldg(reinterpret_cast<const float4 *>(cbh + ((size_t)m * C + c) * kPqDs + 4));
+            const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            float s2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                float hi[2], mi[2], lo[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    hi[t] = __bfloat162float(__float2bfloat16_rn(x[e + t]));
+                    mi[t] = __bfloat162float(__float2bfloat16_rn(x[e + t] - hi[t]));
+                    lo[t] = x[e + t] - hi[t] - mi[t];
+                }
+                // pieces scaled by -2 (exact): with the accumulator started at
+                // |c|^2 the MMAs leave |c|^2 - 2 k.c
+                w[0][e / 2] = pack_bf16(-2.f * hi[0], -2.f * hi[1]);
+                w[1][e / 2] = pack_bf16(-2.f * mi[0], -2.f * mi[1]);
+                w[2][e / 2] = pack_bf16(-2.f * lo[0], -2.f * lo[1]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s2 = fmaf(x[e], x[e], s2);
+            n = s2;
+        } else {
+#pragma unroll
+            for (int pc = 0; pc < 3; ++pc) w[pc][0] = w[pc][1] = w[pc][2] = w[pc][3] = 0u;
+        }
+#pragma unroll
+        for (int pc = 0; pc < 3; ++pc)
+            *reinterpret_cast<uint4 *>(pieces + (((size_t)pc * M + m) * CP + c) * 16) =
+                make_uint4(w[pc][0], w[pc][1], w[pc][2], w[pc][3]);
+        nrm[i] = n;
+    }
+    __syncthreads();
+
+    const int g = lane >> 2, t4 = lane & 3;
+    const int j0 = chunk * kPqEncChunk, j1 = min(L_cap, j0 + kPqEncChunk);
+    const uint32_t pbase = smem_u32(pieces);
+    const int lrow = (lane >> 3) * 8 + (lane & 7);         // centroid row this lane addresses in an x4 load
+    constexpr int STRIDE = (kPqTcThreads / 32) * kPqTcKeys;
+    // A fragments (16 keys x 8 channels per subspace): rows g and g+8, channels
+    // 2*t4 and 2*t4+1 of each subspace; every subspace's words of a batch are
+    // loaded together, and the next batch's while this one is searched
+    auto load_a = [&](int base, uint32_t (&dst)[M][2]) {
+        const int ja = min(base + g, j1 - 1), jb = min(base + g + 8, j1 - 1);
+        const uint32_t *ka = reinterpret_cast<const uint32_t *>(k + (((size_t)b * L_cap + ja) * H_kv + h) * D);
+        const uint32_t *kb = reinterpret_cast<const uint32_t *>(k + (((size_t)b * L_cap + jb) * H_kv + h) * D);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            dst[m][0] = __ldg(ka + m * 4 + t4);
+            dst[m][1] = __ldg(kb + m * 4 + t4);
+        }
+    };
+    uint32_t a_cur[M][2], a_nxt[M][2];
+    if (j0 + warp * kPqTcKeys < j1) load_a(j0 + warp * kPqTcKeys, a_cur);
+    for (int base = j0 + warp * kPqTcKeys; base < j1; base += STRIDE) {
+        const int ja = base + g, jb = base + g + 8;
+        if (base + STRIDE < j1) load_a(base + STRIDE, a_nxt);
+        uint32_t pk_a[M / 4], pk_b[M / 4];
+#pragma unroll
+        for (int wi = 0; wi < M / 4; ++wi) pk_a[wi] = pk_b[wi] = 0u;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const uint32_t a[2] = {a_cur[m][0], a_cur[m][1]};
+            // two argmin chains per key row (centroid tiles j = 0, 2 and j = 1, 3 of
+            // each group of four), each in ascending centroid order
+            float best_a[2] = {INFINITY, INFINITY}, best_b[2] = {INFINITY, INFINITY};
+            int arg_a[2] = {0, 0}, arg_b[2] = {0, 0};
+            const float *nm = nrm + (size_t)m * CP;
+            for (int c4 = 0; c4 < CP; c4 += 32) {
+                uint32_t bp[3][4];
+#pragma unroll
+                for (int pc = 0; pc < 3; ++pc)
+                    ldsm_x4(pbase + (uint32_t)((((size_t)pc * M + m) * CP + c4 + lrow) * 16), bp[pc][0], bp[pc][1],
+                            bp[pc][2], bp[pc][3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c0 = c4 + j * 8 + 2 * t4;
+                    const float2 n = *reinterpret_cast<const float2 *>(nm + c0);
+                    float e[4] = {n.x, n.y, n.x, n.y};      // rows g, g+8 x columns c0, c0+1
+                    pq_mma_k8(e, a, bp[0][j]);
+                    pq_mma_k8(e, a, bp[1][j]);
+                    pq_mma_k8(e, a, bp[2][j]);
+                    const int ch = j & 1;
+                    if (e[0] < best_a[ch]) { best_a[ch] = e[0]; arg_a[ch] = c0; }   // strict: the smaller index keeps a tie
+                    if (e[1] < best_a[ch]) { best_a[ch] = e[1]; arg_a[ch] = c0 + 1; }
+                    if (e[2] < best_b[ch]) { best_b[ch] = e[2]; arg_b[ch] = c0; }
+                    if (e[3] < best_b[ch]) { best_b[ch] = e[3]; arg_b[ch] = c0 + 1; }
+                }
+            }
+            float bst_a = best_a[0], bst_b = best_b[0];
+            int ar_a = arg_a[0], ar_b = arg_b[0];
+            if (best_a[1] < bst_a || (best_a[1] == bst_a && arg_a[1] < ar_a)) { bst_a = best_a[1]; ar_a = arg_a[1]; }
+            if (best_b[1] < bst_b || (best_b[1] == bst_b && arg_b[1] < ar_b)) { bst_b = best_b[1]; ar_b = arg_b[1]; }
+            // the four lanes of a quad hold disjoint centroid columns
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                const float ob_a = __shfl_xor_sync(0xffffffffu, bst_a, o);
+                const int oa_a = __shfl_xor_sync(0xffffffffu, ar_a, o);
+                const float ob_b = __shfl_xor_sync(0xffffffffu, bst_b, o);
+                const int oa_b = __shfl_xor_sync(0xffffffffu, ar_b, o);
+                if (ob_a < bst_a || (ob_a == bst_a && oa_a < ar_a)) { bst_a = ob_a; ar_a = oa_a; }
+                if (ob_b < bst_b || (ob_b == bst_b && oa_b < ar_b)) { bst_b = ob_b; ar_b = oa_b; }
+            }
+#pragma unroll
+            for (int wi = 0; wi < M / 4; ++wi)
+                if (wi == (m >> 2)) {
+                    const uint32_t sh = 8u * (uint32_t)(m & 3);
+                    pk_a[wi] |= (uint32_t)ar_a << sh;
+                    pk_b[wi] |= (uint32_t)ar_b << sh;
+                }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            a_cur[m][0] = a_nxt[m][0];
+            a_cur[m][1] = a_nxt[m][1];
+        }
+        if (t4 == 0) {
+            uint8_t *cbase = codes + ((size_t)b * H_kv + h) * L_cap * M;
+            if (M == 16) {
+                if (ja < j1) *reinterpret_cast<uint4 *>(cbase + (size_t)ja * M) = make_uint4(pk_a[0], pk_a[1], pk_a[2], pk_a[3 % (M / 4)]);
+                if (jb < j1) *reinterpret_cast<uint4 *>(cbase + (size_t)jb * M) = make_uint4(pk_b[0], pk_b[1], pk_b[2], pk_b[3 % (M / 4)]);
+            } else {
+                if (ja < j1) *reinterpret_cast<uint2 *>(cbase + (size_t)ja * M) = make_uint2(pk_a[0], pk_a[1 % (M / 4)]);
+                if (jb < j1) *reinterpret_cast<uint2 *>(cbase + (size_t)jb * M) = make_uint2(pk_b[0], pk_b[1 % (M / 4)]);
+            }
+        }
+    }
+}
+
 magicdec_status launch_pq_encode(int B, int H_kv, int D, int L_cap, int C, const void *k, const float *codebook,
                                  uint8_t *codes, cudaStream_t st) {
     const int M = D / kPqDs;
+    const char *env = getenv("MAGICDEC_PQ_TC");
+    if (!(env && env[0] == '0')) {
+        // tensor-core search (MAGICDEC_PQ_TC=0: the FMA kernel below)
+        const int CP = (C + 31) & ~31;
+        const size_t smem_tc = (size_t)3 * M * CP * 16 + (size_t)M * CP * 4;
+        if (smem_tc <= (size_t)magicdec_host::max_smem_optin()) {
+            const dim3 grid((L_cap + kPqEncChunk - 1) / kPqEncChunk, H_kv, B);
+            auto kb = static_cast<const __nv_bfloat16 *>(k);
+            auto kern = D == 128 ? pq_encode_tc_kernel<128> : pq_encode_tc_kernel<64>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tc) != cudaSuccess)
+                return MAGICDEC_ERR_CUDA;
+            return magicdec_host::launch_pdl(kern, grid, dim3(kPqTcThreads), smem_tc, st, kb, codebook, codes, H_kv,
+                                             L_cap, C, CP);
+        }
+    }
     const size_t smem = (size_t)M * C * kPqDs * 4 + (size_t)M * C * 4;
     if (smem > (size_t)magicdec_host::max_smem_optin()) return MAGICDEC_ERR_UNSUPPORTED;
     const dim3 grid((L_cap + kPqEncChunk - 1) / kPqEncChunk, H_kv, B);
