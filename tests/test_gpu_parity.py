@@ -269,8 +269,10 @@ def _pq_codebook(rng, B, H_kv, M, C, scale=1.0):
     return (scale * rng.standard_normal((B, H_kv, M, C, 8))).astype(np.float32)
 
 
-@pytest.mark.parametrize("B,H_kv,L,C", [(2, 8, 3000, 64), (2, 2, 1500, 256), (1, 8, 700, 7)])
-def test_pq_encode_matches_oracle(B, H_kv, L, C):
+@pytest.mark.parametrize("tc", ["1", "0"])          # tensor-core encoder; the FMA encoder
+@pytest.mark.parametrize("B,H_kv,L,C", [(2, 8, 3000, 64), (2, 2, 1500, 256), (1, 8, 700, 7), (2, 4, 999, 200)])
+def test_pq_encode_matches_oracle(B, H_kv, L, C, tc, monkeypatch):
+    monkeypatch.setenv("MAGICDEC_PQ_TC", tc)
     rng = np.random.default_rng(71)
     d, M = 128, 16
     k = rand_bf16((B, L, H_kv, d), 72)
