@@ -8,7 +8,9 @@
 // [B, H_kv, cap, d].  Both are the same problem -- M = G * n_q query rows per
 // (sequence, KV head) pair streaming that pair's K/V rows once -- so one kernel
 // serves both; only the tensor maps (and the order of their coordinates)
-// differ.
+// differ.  Verification with d = 128, eight KV heads and M <= 16 runs the
+// kernel of attn_heads.cu instead, which streams all heads of a sequence per
+// stage (launch_decode_attn below picks it).
 //
 // Design (HBM-bound: every K/V byte is read exactly once):
 //  * Persistent grid, one CTA per SM.  The whole batch's work is a flat list of
@@ -18,7 +20,11 @@
 //    (max, sum, unnormalised output) triples that the last CTA to finish the
 //    pair merges with the log-sum-exp rule (flash-decoding split-KV; the paper
 //    cites flash decoding in section 2).  "Last arriver merges": an atomic
-//    counter per pair, never a spin-wait.
+//    counter per pair, never a spin-wait.  The producer hands each run of a
+//    pair's tiles (a segment) to the consumers as a descriptor in a two-entry
+//    shared-memory ring beside the query slots.  Optional dynamic tails
+//    (MAGICDEC_ATTN_TAILS=1): pairs of >= 64 tiles leave their last 1/16 to a
+//    pool that CTAs claim after their static share.
 //  * One producer thread issues TMA tiled copies: per 64-row tile, one 4-D box
 //    of 64 rows x 64 channels per 128-byte half of K and of V, 128-byte
 //    swizzled so ldmatrix reads are bank-conflict free, into a ring of STAGES
