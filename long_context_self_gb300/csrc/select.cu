@@ -20,26 +20,24 @@ namespace magicdec {
 __device__ __forceinline__ int clamp_len_s(int v, int hi) { return v < 0 ? 0 : (v > hi ? hi : v); }
 
 // ------------------------------------------------------------ StreamingLLM
-__global__ void streaming_select_kernel(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
-                                        int32_t *idx, int32_t *n_sel) {
+__global__ void streaming_select_kernel(const int32_t *seq_len, int H_kv, int n_sink, int n_recent, int32_t *idx,
+                                        int32_t *n_sel) {
+    // grid (index tiles, KV head, sequence): no index arithmetic beyond the tile
     pdl_trigger();
     pdl_wait();
     const int width = n_sink + n_recent;
-    const long long total = (long long)B * H_kv * width;
-    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
-         t += (long long)gridDim.x * blockDim.x) {
-        const int j = (int)(t % width);
-        const int b = (int)(t / ((long long)H_kv * width));
-        const int len = max(__ldg(seq_len + b), 0);
-        const int sinks = min(n_sink, len);
-        const int rec0 = max(n_sink, len - n_recent);
-        const int n = sinks + max(0, len - rec0);
+    const int j = blockIdx.x * blockDim.x + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int len = max(__ldg(seq_len + b), 0);
+    const int sinks = min(n_sink, len);
+    const int rec0 = max(n_sink, len - n_recent);
+    const int n = sinks + max(0, len - rec0);
+    if (j < width) {
         int v = -1;
         if (j < sinks) v = j;
         else if (j < n) v = rec0 + (j - sinks);
-        idx[t] = v;
-        if (j == 0 && (t / width) % H_kv == 0) n_sel[b] = n;
+        idx[((long long)b * H_kv + h) * width + j] = v;
     }
+    if (j == 0 && h == 0) n_sel[b] = n;
 }
 
 // ------------------------------------------------------------------ gather
@@ -135,11 +133,13 @@ __global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *__restric
 // ------------------------------------------------------------------- host side
 magicdec_status launch_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
                                         int32_t *idx, int32_t *n_sel, cudaStream_t st) {
-    const long long total = (long long)B * H_kv * (n_sink + n_recent);
+    const int width = n_sink + n_recent;
+    if (B <= 0 || H_kv <= 0 || width <= 0) return MAGICDEC_OK;
+    if (B > 65535 || H_kv > 65535) return MAGICDEC_ERR_UNSUPPORTED;
     const int threads = 256;
-    const int blocks = (int)std::min<long long>((total + threads - 1) / threads, 65535);
-    return magicdec_host::launch_pdl(streaming_select_kernel, dim3(blocks), dim3(threads), 0, st, seq_len, B, H_kv,
-                                     n_sink, n_recent, idx, n_sel);
+    const dim3 grid((width + threads - 1) / threads, H_kv, B);
+    return magicdec_host::launch_pdl(streaming_select_kernel, grid, dim3(threads), 0, st, seq_len, H_kv, n_sink,
+                                     n_recent, idx, n_sel);
 }
 
 magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *k, const void *v,
