@@ -103,6 +103,41 @@ def test_attention_special_cases():
     np.testing.assert_allclose(out[2, 0, 0], vf[2, 0, 11], rtol=1e-12, atol=1e-12)
 
 
+def test_split_merge_invariance():
+    """Attention over a set of keys equals the log-sum-exp weighted combine of attention over
+    any partition of that set (the identity a split-KV merge relies on).  Each part's
+    normaliser Z = sum_j exp(s_j) is read from the oracle itself: a probe cache holding the
+    part's keys plus one all-zero key whose value row is e_0 (every other value row zero)
+    gives out[0] = 1 / (1 + Z), because the zero key's logit is 0 whatever the scale.  The
+    recombined output must equal the oracle's unsplit result."""
+    rng = np.random.default_rng(11)
+    B, H_q, H_kv, d, n = 2, 8, 2, 64, 37
+    q = bf16_bits(rng.standard_normal((B, 1, H_q, d)))
+    kc = bf16_bits(rng.standard_normal((B, H_kv, n, d)))
+    vc = bf16_bits(rng.standard_normal((B, H_kv, n, d)))
+    full = oracle.draft_attn(q, kc, vc, np.full(B, n, np.int32))
+    one = bf16_bits(np.ones(1))[0]
+    for n_parts in (2, 3, 5):
+        part_of = rng.integers(0, n_parts, n)
+        part_of[:n_parts] = np.arange(n_parts)            # no part is empty
+        num = np.zeros_like(full)
+        den = np.zeros(full.shape[:3] + (1,))
+        for p in range(n_parts):
+            rows = np.flatnonzero(part_of == p)
+            m = rows.size
+            kp, vp = kc[:, :, rows], vc[:, :, rows]
+            o_p = oracle.draft_attn(q, kp, vp, np.full(B, m, np.int32))
+            k_probe = np.zeros((B, H_kv, m + 1, d), np.uint16)
+            v_probe = np.zeros((B, H_kv, m + 1, d), np.uint16)
+            k_probe[:, :, 1:] = kp
+            v_probe[:, :, 0, 0] = one
+            probe = oracle.draft_attn(q, k_probe, v_probe, np.full(B, m + 1, np.int32))
+            z = 1.0 / probe[..., :1] - 1.0
+            num += z * o_p
+            den += z
+        np.testing.assert_allclose(num / den, full, rtol=1e-10, atol=1e-12)
+
+
 def test_verify_equals_draft_on_last_row():
     """The last verification row sees the whole sequence: it is plain decode attention over
     the full prefix, which the draft kernel computes when its cache is the identity gather."""
