@@ -89,7 +89,7 @@ MAGICDEC_API magicdec_status magicdec_device_error(int32_t *out);
  *           len), ascending, identical for every KV head; -1 after n_sel[b].
  *   n_sel   [B] int32 out: number of valid entries per sequence.
  * Errors: NULL pointers, B <= 0, H_kv <= 0, n_sink < 0, n_recent < 0,
- * n_sink + n_recent == 0; MAGICDEC_ERR_UNSUPPORTED when B or H_kv exceeds
+ * n_sink + n_recent == 0 or above INT_MAX; MAGICDEC_ERR_UNSUPPORTED when B or H_kv exceeds
  * 65535 (the kernel's grid has one block row per KV head and sequence).
  */
 MAGICDEC_API magicdec_status magicdec_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink,

@@ -3,6 +3,7 @@
 // contract of every entry point are in include/magicdec.h.
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cstdlib>
 #include <mutex>
 
@@ -156,7 +157,9 @@ magicdec_status magicdec_device_error(int32_t *out) {
 magicdec_status magicdec_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
                                           int32_t *idx, int32_t *n_sel, void *stream) {
     if (!seq_len || !idx || !n_sel) return MAGICDEC_ERR_NULL;
-    if (B <= 0 || H_kv <= 0 || n_sink < 0 || n_recent < 0 || n_sink + n_recent <= 0) return MAGICDEC_ERR_SHAPE;
+    if (B <= 0 || H_kv <= 0 || n_sink < 0 || n_recent < 0) return MAGICDEC_ERR_SHAPE;
+    const long long width = (long long)n_sink + n_recent;   // the row width of idx must be a positive int
+    if (width <= 0 || width > INT_MAX) return MAGICDEC_ERR_SHAPE;
     return magicdec::launch_streaming_select(seq_len, B, H_kv, n_sink, n_recent, idx, n_sel,
                                              static_cast<cudaStream_t>(stream));
 }

@@ -76,6 +76,17 @@ def test_null_and_shape_errors_are_reported_before_launch(lib):
     assert lib.magicdec_streaming_select(FAKE, 0, 8, 16, 496, FAKE, FAKE, NULL) == -2
     assert lib.magicdec_streaming_select(FAKE, 4, 8, 0, 0, FAKE, FAKE, NULL) == -2
     assert lib.magicdec_streaming_select(NULL, 4, 8, 16, 496, FAKE, FAKE, NULL) == -1
+    assert lib.magicdec_streaming_select(FAKE, 4, 8, 2**31 - 1, 1, FAKE, FAKE, NULL) == -2   # width past INT_MAX
+    # one block row per (KV head, sequence): more than 65535 of either has no launch shape
+    assert lib.magicdec_streaming_select(FAKE, 70000, 8, 16, 496, FAKE, FAKE, NULL) == -5
+    assert lib.magicdec_streaming_select(FAKE, 4, 70000, 16, 496, FAKE, FAKE, NULL) == -5
+    assert lib.magicdec_device_error(NULL) == -1
+    # the no-allocation verification entry point validates like the workspace one
+    assert lib.magicdec_verify_attn_noalloc(shape(), 4, NULL, FAKE, FAKE, FAKE, FAKE, NULL) == -1
+    assert lib.magicdec_verify_attn_noalloc(shape(d=96), 4, FAKE, FAKE, FAKE, FAKE, FAKE, NULL) == -2
+    assert lib.magicdec_verify_attn_noalloc(shape(), 0, FAKE, FAKE, FAKE, FAKE, FAKE, NULL) == -2
+    assert lib.magicdec_verify_attn_noalloc(shape(H_q=16, H_kv=2), 5, FAKE, FAKE, FAKE, FAKE, FAKE, NULL) == -5
+    assert lib.magicdec_verify_attn_noalloc(shape(), 4, FAKE, FAKE, MISALIGNED, FAKE, FAKE, NULL) == -3
     assert lib.magicdec_snapkv_select(shape(), FAKE, FAKE, FAKE, 32, 7, 16, FAKE, FAKE, FAKE, 1 << 40, NULL) == -2
     assert lib.magicdec_snapkv_select(shape(), FAKE, FAKE, FAKE, 32, 6, 64, FAKE, FAKE, FAKE, 1 << 40, NULL) == -2
     assert lib.magicdec_snapkv_select(shape(), FAKE, FAKE, FAKE, 32, 7, 64, FAKE, FAKE, FAKE, 16, NULL) == -4
