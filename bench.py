@@ -79,6 +79,12 @@ def aggregate_rate(world: int, steps: int, ms_max: float) -> float:
     return world * steps / (ms_max * 1e-3)
 
 
+def rank_workload(w, rank: int):
+    """The workload one rank runs: rank r draws its own sequences (seed offset by 100·r), so
+    N replicas process N distinct batches; rank 0 keeps the workload's own seed."""
+    return w if rank == 0 else dataclasses.replace(w, seed=w.seed + 100 * rank)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -328,6 +334,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     w = synth.WORKLOADS[args.workload]
     if args.batch:
         w = dataclasses.replace(w, B=args.batch)
+    w = rank_workload(w, rank)
     pipe = Pipeline(w, device, args.layers)
     torch.cuda.synchronize()
 
@@ -613,6 +620,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "gamma": w.gamma, "V": w.V, "layers": args.layers,
                    "draft": f"StreamingLLM {w.n_sink}+{w.n_recent} (selection + gather every step)",
                    "per_rank_batch": w.B, "parallelism": f"replicas x{world}",
+                   "rank_seeds": "workload seed + 100 x rank (distinct sequences per rank)",
                    "l2": "inputs larger than L2 (KV cache 16.8 GB per layer vs 129 MB L2)",
                    "step": "layers x (select, gather, gamma x draft_attn, verify_attn) + spec_accept"},
         "roofline": {"bound": "hbm", "kernel": "verify_heads_kernel", "achieved": round(ver_gbs, 1),
