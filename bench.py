@@ -711,7 +711,7 @@ def run_reference(args, rank: int):
         return None
     import oracle
     w = synth.WORKLOADS[args.workload]
-    nb_attn, nb_acc = 8, 16
+    nb_attn, nb_acc = min(8, w.B), min(16, w.B)
     # inputs for the sampled sequences, drawn on the host with the same recipes
     sw = synth.Workload("sample", B=nb_attn, H_q=w.H_q, H_kv=w.H_kv, d=w.d, L=w.L, gamma=w.gamma, V=w.V,
                         n_sink=w.n_sink, n_recent=w.n_recent, boost_frac=w.boost_frac, boost=w.boost,
