@@ -809,7 +809,7 @@ int oracle_spec_accept(int B, int gamma, int V, const float *target, const float
         double *q = (double *)malloc(sizeof(double) * (size_t)V);
         double *wt = (double *)malloc(sizeof(double) * (size_t)V);
         int32_t *out = out_tok + (long)b * (gamma + 1);
-        int amb = 0, i, t, acc = gamma, emitted = -1;
+        int amb = 0, i, acc = gamma, emitted = -1;
         for (i = 0; i <= gamma; ++i) out[i] = -1;
         for (i = 0; i < gamma; ++i) {
             const float *tl = target + ((long)b * (gamma + 1) + i) * V;
