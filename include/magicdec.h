@@ -53,7 +53,7 @@ typedef enum {
     MAGICDEC_ERR_SHAPE = -2,       /* a size is out of range or inconsistent */
     MAGICDEC_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
     MAGICDEC_ERR_WORKSPACE = -4,   /* workspace smaller than *_workspace_size() */
-    MAGICDEC_ERR_UNSUPPORTED = -5, /* a valid shape this build has no kernel for */
+    MAGICDEC_ERR_UNSUPPORTED = -5, /* a valid shape the library has no kernel for */
     MAGICDEC_ERR_CUDA = -6         /* the CUDA runtime reported an error */
 } magicdec_status;
 

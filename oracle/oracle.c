@@ -9,8 +9,7 @@
  *
  * Every function restates, in plain loops and in double precision, a
  * definition from "MagicDec: Breaking the Latency-Throughput Tradeoff for Long
- * Context Generation with Speculative Decoding" (arXiv 2408.11049v5) and the
- * method statement that accompanies the build:
+ * Context Generation with Speculative Decoding" (arXiv 2408.11049v5):
  *   - verification attention: the gamma+1 speculated queries attend to the
  *     full KV cache, causal inside the speculated block (section 3.1, the
  *     verification cost T_V(B,S,gamma); section 3.2);
