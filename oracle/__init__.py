@@ -58,7 +58,7 @@ def _load():
             lib.oracle_snapkv_scores.argtypes = [I, I, I, I, I, I, P, P, P, P]
             lib.oracle_maxpool1d.argtypes = [P, I, I, P]
             lib.oracle_snapkv_select.argtypes = [I, I, I, I, I, P, P, P, I, I, I, P, P, P]
-            lib.oracle_spec_accept.argtypes = [I, I, I, P, P, P, P, P, I, P, P, P]
+            lib.oracle_spec_accept.argtypes = [I, I, I, P, P, P, P, P, I, P, P, P, P, P]
             lib.oracle_resample_weights.argtypes = [P, P, I, P]
             lib.oracle_topk_attn.argtypes = [I, I, I, I, I, P, P, P, P, I, P, P, P]
             lib.oracle_draft_cache_update.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I, I, P, P, P]
@@ -259,9 +259,11 @@ def pq_attn(q, k, v, seq_len, codebook, codes, top_k: int, want_approx: bool = F
     return out, idx, approx
 
 
-def spec_accept(target, draft, draft_tok, u_acc, u_res, greedy: bool):
+def spec_accept(target, draft, draft_tok, u_acc, u_res, greedy: bool, want_margins: bool = False):
     """target [B,g+1,V] f32, draft [B,g,V] f32, draft_tok [B,g] i32, u_acc [B,g], u_res [B]
-    -> (n_acc [B], out_tok [B,g+1], n_amb [B]) int32."""
+    -> (n_acc [B], out_tok [B,g+1], n_amb [B]) int32; with want_margins also
+    (acc_margin fp64 [B,g+1], draw_margin fp64 [B]): each decision's distance from its
+    boundary on the path taken (NaN where none was taken; see oracle_spec_accept)."""
     target = _c(target, np.float32)
     B, gp1, V = target.shape
     gamma = gp1 - 1
@@ -271,9 +273,14 @@ def spec_accept(target, draft, draft_tok, u_acc, u_res, greedy: bool):
     n_acc = np.empty((B,), np.int32)
     out_tok = np.empty((B, gamma + 1), np.int32)
     n_amb = np.empty((B,), np.int32)
+    acc_m = np.empty((B, gamma + 1), np.float64) if want_margins else None
+    draw_m = np.empty((B,), np.float64) if want_margins else None
     _check(_load().oracle_spec_accept(B, gamma, V, _ptr(target), _ptr(draft), _ptr(draft_tok),
                                       _ptr(u_acc), _ptr(u_res), int(bool(greedy)), _ptr(n_acc),
-                                      _ptr(out_tok), _ptr(n_amb)), "spec_accept")
+                                      _ptr(out_tok), _ptr(n_amb), _ptr(acc_m) if want_margins else None,
+                                      _ptr(draw_m) if want_margins else None), "spec_accept")
+    if want_margins:
+        return n_acc, out_tok, n_amb, acc_m, draw_m
     return n_acc, out_tok, n_amb
 
 

@@ -715,9 +715,11 @@ static void softmax_row(const float *logits, int V, double *p)
  * token of a 128K vocabulary is narrower than 1e-4 of the total, so the edge
  * margin is set by the precision of a single-precision evaluation of the same
  * sums (per-logit errors ~1e-6, normalisers and running sums carried in higher
- * precision), not by the 1e-4 acceptance margin.
+ * precision), not by the 1e-4 acceptance margin.  *edge (nullable) receives
+ * the distance from u*W to the nearer inner edge of the chosen token, divided
+ * by W (0 when the fallback was taken).
  */
-static int inverse_cdf(const double *wt, int V, double u, int *amb)
+static int inverse_cdf(const double *wt, int V, double u, int *amb, double *edge)
 {
     double W = 0.0, c = 0.0, prev;
     int t, last = V - 1;
@@ -728,21 +730,28 @@ static int inverse_cdf(const double *wt, int V, double u, int *amb)
         prev = c;
         c += wt[t];
         if (c > target) {
-            if ((t > 0 && target - prev < tol) || (t < V - 1 && c - target < tol)) ++*amb;
+            double e = INFINITY;
+            if (t > 0) e = target - prev;
+            if (t < V - 1 && c - target < e) e = c - target;
+            if (e < tol) ++*amb;
+            if (edge) *edge = e / W;
             return t;
         }
     }
     ++*amb;
+    if (edge) *edge = 0.0;
     return last;
 }
 
-static int argmax_row(const float *logits, int V, int *amb)
+/* Argmax (ties to the smaller token); *gap receives the top-2 logit gap. */
+static int argmax_row(const float *logits, int V, int *amb, double *gap)
 {
     int t, a = 0;
     for (t = 1; t < V; ++t) if (logits[t] > logits[a]) a = t;
     double second = -INFINITY;
     for (t = 0; t < V; ++t) if (t != a && (double)logits[t] > second) second = logits[t];
-    if ((double)logits[a] - second < 1e-4) ++*amb;
+    *gap = (double)logits[a] - second;
+    if (*gap < 1e-4) ++*amb;
     return a;
 }
 
@@ -795,10 +804,19 @@ int oracle_resample_weights(const float *target_row, const float *draft_row, int
  *   counts decisions taken near their boundary: |u - p(x)/q(x)| < 1e-4, a
  *   top-2 logit gap below 1e-4, or an inverse-CDF edge within 1e-7 of the
  *   total.
+ * Optional margin outputs (nullable), one value per decision on the path
+ * taken, NaN where no decision was taken: acc_margin [B, gamma+1] holds at
+ *   position i the distance of that position's decision from its boundary --
+ *   |u_acc - p(x)/q(x)| in sampling mode (+inf when the decision is exact:
+ *   x out of range or q(x) = 0), the top-2 logit gap in greedy mode (also
+ *   at the bonus position); draw_margin [B] holds the inverse-CDF edge
+ *   distance of the sampled token divided by the total weight (sampling
+ *   mode only).
  */
 int oracle_spec_accept(int B, int gamma, int V, const float *target, const float *draft,
                        const int32_t *draft_tok, const float *u_acc, const float *u_res,
-                       int greedy, int32_t *n_acc, int32_t *out_tok, int32_t *n_amb)
+                       int greedy, int32_t *n_acc, int32_t *out_tok, int32_t *n_amb,
+                       double *acc_margin, double *draw_margin)
 {
     if (B < 0 || gamma < 0 || V <= 0) return -1;
     int b;
@@ -809,19 +827,24 @@ int oracle_spec_accept(int B, int gamma, int V, const float *target, const float
         double *wt = (double *)malloc(sizeof(double) * (size_t)V);
         int32_t *out = out_tok + (long)b * (gamma + 1);
         int amb = 0, i, acc = gamma, emitted = -1;
+        double *am = acc_margin ? acc_margin + (long)b * (gamma + 1) : NULL;
+        double gap, edge = NAN;
         for (i = 0; i <= gamma; ++i) out[i] = -1;
+        if (am) for (i = 0; i <= gamma; ++i) am[i] = NAN;
         for (i = 0; i < gamma; ++i) {
             const float *tl = target + ((long)b * (gamma + 1) + i) * V;
             int x = draft_tok[(long)b * gamma + i];
             int ok;
             if (greedy) {
-                int a = argmax_row(tl, V, &amb);
+                int a = argmax_row(tl, V, &amb, &gap);
+                if (am) am[i] = gap;
                 ok = (x == a);
                 if (!ok) emitted = a;
             } else {
                 const float *dl = draft + ((long)b * gamma + i) * V;
                 softmax_row(tl, V, p);
                 softmax_row(dl, V, q);
+                if (am) am[i] = INFINITY;
                 if (x < 0 || x >= V) {
                     ok = 0;
                 } else if (q[x] > 0.0) {
@@ -829,12 +852,13 @@ int oracle_spec_accept(int B, int gamma, int V, const float *target, const float
                     double u = u_acc[(long)b * gamma + i];
                     ok = (u < ratio);
                     if (fabs(u - ratio) < 1e-4) ++amb;
+                    if (am) am[i] = fabs(u - ratio);
                 } else {
                     ok = (p[x] > 0.0);
                 }
                 if (!ok) {
                     resample_weights_into(tl, dl, V, p, q, wt);
-                    emitted = inverse_cdf(wt, V, u_res[b], &amb);
+                    emitted = inverse_cdf(wt, V, u_res[b], &amb, &edge);
                 }
             }
             if (!ok) { acc = i; break; }
@@ -843,12 +867,14 @@ int oracle_spec_accept(int B, int gamma, int V, const float *target, const float
         if (acc == gamma) {
             const float *tl = target + ((long)b * (gamma + 1) + gamma) * V;
             if (greedy) {
-                emitted = argmax_row(tl, V, &amb);
+                emitted = argmax_row(tl, V, &amb, &gap);
+                if (am) am[gamma] = gap;
             } else {
                 resample_weights_into(tl, NULL, V, p, q, wt);
-                emitted = inverse_cdf(wt, V, u_res[b], &amb);
+                emitted = inverse_cdf(wt, V, u_res[b], &amb, &edge);
             }
         }
+        if (draw_margin) draw_margin[b] = edge;
         out[acc] = emitted;
         n_acc[b] = acc;
         if (n_amb) n_amb[b] = amb;

@@ -707,3 +707,35 @@ def test_expected_tokens_matches_eq1(gamma):
     gen = n_acc + 1.0
     omega = (1 - alpha ** (gamma + 1)) / (1 - alpha)
     assert abs(gen.mean() - omega) < 4 * gen.std() / math.sqrt(B)
+
+
+def test_spec_accept_margins_at_planted_boundaries():
+    """The per-decision margins the parity tests exclude by, on inputs whose p, q and running
+    sums are exact dyadic numbers (logits 0 and -inf), so each margin is known in closed form:
+    target p = 1/4 each; draft q = (1/2, 1/2, 0, 0); residual max(0, p - q) = (0, 0, 1/4, 1/4)."""
+    V = 4
+    target = np.zeros((4, 2, V), np.float32)
+    draft = np.tile(np.array([0, 0, -np.inf, -np.inf], np.float32), (4, 1, 1))
+    tok = np.array([[0], [0], [2], [-1]], np.int32)
+    u_acc = np.array([[0.5 + 2.0 ** -24], [0.375], [0.9], [0.9]], np.float32)
+    u_res = np.array([0.25, 0.5 + 2.0 ** -24, 0.125, 0.75], np.float32)
+    n_acc, out, amb, acc_m, draw_m = oracle.spec_accept(target, draft, tok, u_acc, u_res, False, want_margins=True)
+    # seq 0: p/q = 1/2, u just above -> reject at margin 2^-24 (one fp32 ulp); draw 0.25*W = 1/8 lands in token 2,
+    #        1/8 from both of its edges (1/4 of W = 1/2)
+    # seq 1: accepted 1/8 from the boundary; the bonus draw from p lands 2^-24 past the 1/2 edge
+    # seq 2: q(x) = 0 < p(x): accepted exactly; bonus 1/8 -> token 0, 1/8 from its upper edge
+    # seq 3: x out of range: rejected exactly; 3/8 lands in token 3, 1/8 past its lower edge
+    assert n_acc.tolist() == [0, 1, 1, 0]
+    assert out.tolist() == [[2, -1], [0, 2], [2, 0], [3, -1]]
+    assert amb.tolist() == [1, 1, 0, 0]
+    assert acc_m[0, 0] == 2.0 ** -24 and acc_m[1, 0] == 0.125
+    assert np.isinf(acc_m[2, 0]) and np.isinf(acc_m[3, 0])
+    assert np.all(np.isnan(acc_m[:, 1]))
+    assert draw_m.tolist() == [0.25, 2.0 ** -24, 0.125, 0.25]
+    # greedy: the top-2 logit gap at each decided position, the bonus row included
+    tg = np.array([[[1.0, 1.0 - 2.0 ** -16, 0, 0], [0, 3, 1, 0]]], np.float32)
+    n_acc, out, amb, acc_m, draw_m = oracle.spec_accept(tg, None, np.array([[0]], np.int32),
+                                                        np.zeros((1, 1), np.float32), np.zeros(1, np.float32), True,
+                                                        want_margins=True)
+    assert n_acc.tolist() == [1] and out.tolist() == [[0, 1]] and amb.tolist() == [1]
+    assert acc_m.tolist() == [[2.0 ** -16, 2.0]] and np.isnan(draw_m[0])
