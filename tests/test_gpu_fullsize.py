@@ -20,7 +20,8 @@ import torch
 import oracle
 from long_context_self_gb300 import binding as mb
 from long_context_self_gb300 import synth
-from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, check_topk_attn, to_u16
+from parity_util import (bf16_out_to_f64, check_accept, check_attention, check_topk, check_topk_attn,
+                         oracle_accept, to_u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -238,6 +239,6 @@ def test_fullsize_spec_accept(name, greedy):
     got = mb.magicdec_spec_accept(target, draft, tok, u_acc, u_res, greedy)
     torch.cuda.synchronize()
     t, d, x, ua, ur = (a.cpu().numpy() for a in (target, draft, tok, u_acc, u_res))
-    ref = oracle.spec_accept(t, d, x, ua, ur, greedy)
-    n_amb = check_accept(tuple(a.cpu().numpy() for a in got), ref, name, inputs=(t, d, ur))
+    ref = oracle_accept(t, d, x, ua, ur, greedy)
+    n_amb = check_accept(tuple(a.cpu().numpy() for a in got), ref, name, inputs=(t, d, ur), greedy=greedy)
     assert n_amb <= max(2, w.B // 8)

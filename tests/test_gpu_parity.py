@@ -10,7 +10,8 @@ import torch
 import oracle
 from long_context_self_gb300 import binding as mb
 from long_context_self_gb300 import synth
-from parity_util import bf16_out_to_f64, check_accept, check_attention, check_topk, check_topk_attn, to_u16
+from parity_util import (bf16_out_to_f64, check_accept, check_attention, check_topk, check_topk_attn,
+                         oracle_accept, to_u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -604,9 +605,9 @@ def test_spec_accept_matches_oracle(name, B, greedy):
         tok = torch.where(pick, am, tok)
     got = mb.magicdec_spec_accept(target.to(DEV), draft.to(DEV), tok.to(DEV), u_acc.to(DEV), u_res.to(DEV), greedy)
     torch.cuda.synchronize()
-    ref = oracle.spec_accept(target.numpy(), draft.numpy(), tok.numpy(), u_acc.numpy(), u_res.numpy(), greedy)
+    ref = oracle_accept(target.numpy(), draft.numpy(), tok.numpy(), u_acc.numpy(), u_res.numpy(), greedy)
     gpu = tuple(t.cpu().numpy() for t in got)
-    n_amb = check_accept(gpu, ref, name, inputs=(target.numpy(), draft.numpy(), u_res.numpy()))
+    n_amb = check_accept(gpu, ref, name, inputs=(target.numpy(), draft.numpy(), u_res.numpy()), greedy=greedy)
     assert n_amb <= max(2, B // 4)
 
 
@@ -622,15 +623,15 @@ def test_spec_accept_edge_tokens():
     u_acc, u_res = torch.rand((B, 2), generator=g), torch.rand((B,), generator=g)
     got = mb.magicdec_spec_accept(target.to(DEV), draft.to(DEV), tok.to(DEV), u_acc.to(DEV), u_res.to(DEV), False)
     torch.cuda.synchronize()
-    ref = oracle.spec_accept(target.numpy(), draft.numpy(), tok.numpy(), u_acc.numpy(), u_res.numpy(), False)
+    ref = oracle_accept(target.numpy(), draft.numpy(), tok.numpy(), u_acc.numpy(), u_res.numpy(), False)
     check_accept(tuple(t.cpu().numpy() for t in got), ref)
     assert got[0][0].item() == 0 and got[0][1].item() == 0
     t0 = target[:, :1].contiguous()
     got0 = mb.magicdec_spec_accept(t0.to(DEV), None, torch.zeros((B, 0), dtype=torch.int32, device=DEV),
                                    torch.zeros((B, 0), device=DEV), u_res.to(DEV), False)
     torch.cuda.synchronize()
-    ref0 = oracle.spec_accept(t0.numpy(), np.zeros((B, 0, V), np.float32), np.zeros((B, 0), np.int32),
-                              np.zeros((B, 0), np.float32), u_res.numpy(), False)
+    ref0 = oracle_accept(t0.numpy(), np.zeros((B, 0, V), np.float32), np.zeros((B, 0), np.int32),
+                         np.zeros((B, 0), np.float32), u_res.numpy(), False)
     check_accept(tuple(t.cpu().numpy() for t in got0), ref0, "gamma=0")
 
 
@@ -651,8 +652,8 @@ def test_spec_accept_vocabulary_not_a_multiple_of_4(V, greedy):
     got = mb.magicdec_spec_accept(target.to(DEV), draft.to(DEV), tok.to(DEV), u_acc.to(DEV), u_res.to(DEV), greedy)
     torch.cuda.synchronize()
     t, d, x, ua, ur = (a.numpy() for a in (target, draft, tok, u_acc, u_res))
-    ref = oracle.spec_accept(t, d, x, ua, ur, greedy)
-    n_amb = check_accept(tuple(a.cpu().numpy() for a in got), ref, f"V={V}", inputs=(t, d, ur))
+    ref = oracle_accept(t, d, x, ua, ur, greedy)
+    n_amb = check_accept(tuple(a.cpu().numpy() for a in got), ref, f"V={V}", inputs=(t, d, ur), greedy=greedy)
     assert n_amb <= 2
 
 
