@@ -313,11 +313,16 @@ MAGICDEC_API magicdec_status magicdec_pq_draft_attn(magicdec_kv_shape shape, con
  * scratch is a 32 MiB array inside the library, which every GPU that loads
  * the library holds until the process exits.
  *  - The first call on a device, with that device current, looks up the
- *    array's device address and synchronously zeroes the part that must
- *    start at zero (the merge counters); make that first
- *    call before any stream capture.
- *  - All calls on a device share the array and leave it ready for the next
- *    call; calls that overlap on the GPU race, so order them (one stream).
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - Every call first clears the part of the array that must start at zero
+ *    (the merge counters and scheduler words, 256 KB) with cudaMemsetAsync
+ *    on `stream`, then launches on the same stream; so a call that gave up on
+ *    a bounded wait (device error word 1) leaves nothing that a later call
+ *    can trip over.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    contents; calls that overlap on the GPU race, so order them (one
+ *    stream).
  *  - Returns MAGICDEC_ERR_UNSUPPORTED, and enqueues nothing, when the
  *    kernel's scratch for the current device would not fit in the array.
  * Errors otherwise as magicdec_verify_attn.

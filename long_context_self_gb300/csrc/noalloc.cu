@@ -14,9 +14,13 @@
 // library holds kNoAllocScratchBytes of it until the process exits.  Host
 // code cannot use the array's name as a device address; the first call on a
 // device (with that device current) resolves the address with
-// cudaGetSymbolAddress and zeroes the counter region, and later calls reuse
-// the cached address.  All calls on a device share the one array: calls that
-// overlap on the GPU race and must be ordered (for example on one stream).
+// cudaGetSymbolAddress, and later calls reuse the cached address.  Every
+// call first clears the array's counter region with cudaMemsetAsync on the
+// caller's stream (no allocation), so the kernel always starts from zeroed
+// counters -- also after an earlier call that gave up on a bounded wait and
+// left counters behind -- and the clear is ordered with the launch on that
+// stream.  All calls on a device share the one array: calls that overlap on
+// the GPU race and must be ordered (for example on one stream).
 #include <cstring>
 #include <mutex>
 
@@ -33,16 +37,15 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = 32u << 20;   // 32 MiB
 
-// The scratch itself: zero at module load; every call leaves its counter
-// region zero again.
+// The scratch itself (zero at module load).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDev] = {nullptr};
 
-// Device address of the scratch array on the current device, resolved (and
-// its counter region cleared) the first time the device is seen.
+// Device address of the scratch array on the current device, resolved the
+// first time the device is seen.
 magicdec_status scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MAGICDEC_ERR_CUDA;
@@ -50,7 +53,6 @@ magicdec_status scratch_address(void **out) {
     if (!g_scratch_addr[dev]) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return MAGICDEC_ERR_CUDA;
-        if (cudaMemset(ptr, 0, magicdec::kAttnCounterBytes) != cudaSuccess) return MAGICDEC_ERR_CUDA;
         g_scratch_addr[dev] = ptr;
     }
     *out = g_scratch_addr[dev];
@@ -78,6 +80,9 @@ extern "C" magicdec_status magicdec_verify_attn_noalloc(magicdec_kv_shape shape,
     void *ws = nullptr;
     const magicdec_status s = scratch_address(&ws);
     if (s != MAGICDEC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // merge counters and scheduler words start at zero whatever an earlier call left
+    if (cudaMemsetAsync(ws, 0, magicdec::kAttnCounterBytes, st) != cudaSuccess) return MAGICDEC_ERR_CUDA;
     return magicdec::launch_decode_attn(shape.B, shape.H_q, shape.H_kv, shape.d, shape.L_cap, n_q, 0, q, k, v,
-                                        seq_len, out, ws, kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
+                                        seq_len, out, ws, kNoAllocScratchBytes, st);
 }
