@@ -25,16 +25,18 @@ __global__ void streaming_select_kernel(const int32_t *seq_len, int H_kv, int n_
     // grid (index tiles, KV head, sequence): no index arithmetic beyond the tile
     pdl_trigger();
     pdl_wait();
-    const int width = n_sink + n_recent;
-    const int j = blockIdx.x * blockDim.x + threadIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // 64-bit: the width may come within a block of INT_MAX
+    const long long width = (long long)n_sink + n_recent;
+    const long long j = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
     const int len = max(__ldg(seq_len + b), 0);
     const int sinks = min(n_sink, len);
     const int rec0 = max(n_sink, len - n_recent);
     const int n = sinks + max(0, len - rec0);
     if (j < width) {
         int v = -1;
-        if (j < sinks) v = j;
-        else if (j < n) v = rec0 + (j - sinks);
+        if (j < sinks) v = (int)j;
+        else if (j < n) v = rec0 + (int)(j - sinks);
         idx[((long long)b * H_kv + h) * width + j] = v;
     }
     if (j == 0 && h == 0) n_sel[b] = n;
@@ -133,11 +135,11 @@ __global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *__restric
 // ------------------------------------------------------------------- host side
 magicdec_status launch_streaming_select(const int32_t *seq_len, int B, int H_kv, int n_sink, int n_recent,
                                         int32_t *idx, int32_t *n_sel, cudaStream_t st) {
-    const int width = n_sink + n_recent;
+    const long long width = (long long)n_sink + n_recent;
     if (B <= 0 || H_kv <= 0 || width <= 0) return MAGICDEC_OK;
     if (B > 65535 || H_kv > 65535) return MAGICDEC_ERR_UNSUPPORTED;
     const int threads = 256;
-    const dim3 grid((width + threads - 1) / threads, H_kv, B);
+    const dim3 grid((unsigned)((width + threads - 1) / threads), H_kv, B);
     return magicdec_host::launch_pdl(streaming_select_kernel, grid, dim3(threads), 0, st, seq_len, H_kv, n_sink,
                                      n_recent, idx, n_sel);
 }

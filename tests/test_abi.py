@@ -80,6 +80,9 @@ def test_null_and_shape_errors_are_reported_before_launch(lib):
     # one block row per (KV head, sequence): more than 65535 of either has no launch shape
     assert lib.magicdec_streaming_select(FAKE, 70000, 8, 16, 496, FAKE, FAKE, NULL) == -5
     assert lib.magicdec_streaming_select(FAKE, 4, 70000, 16, 496, FAKE, FAKE, NULL) == -5
+    # a width of exactly INT_MAX passes the shape check (its grid and indices are 64-bit); the
+    # batch bound still refuses before anything is launched
+    assert lib.magicdec_streaming_select(FAKE, 70000, 8, 2**31 - 2, 1, FAKE, FAKE, NULL) == -5
     assert lib.magicdec_device_error(NULL) == -1
     # the no-allocation verification entry point validates like the workspace one
     assert lib.magicdec_verify_attn_noalloc(shape(), 4, NULL, FAKE, FAKE, FAKE, FAKE, NULL) == -1
