@@ -187,6 +187,28 @@ MAGICDEC_API magicdec_status magicdec_draft_cache_update(magicdec_kv_shape shape
                                                          const int32_t *base, int ring, int cap, uint16_t *kc,
                                                          uint16_t *vc, int32_t *draft_len, void *stream);
 
+/*
+ * Lengths of one speculative step (paper section 3.1: gamma draft steps, one
+ * verification of the gamma+1 block, then the sequence keeps its accepted
+ * prefix and the emitted token; section 4.4: the static draft caches take in
+ * each new position).  For every sequence b:
+ *   len = len_in[b] + (n_acc ? n_acc[b] + 1 : 0), clamped to [0, L_cap];
+ *   len_out[b] = len;  table[j * B + b] = min(len + j, L_cap), j = 0..gamma+1.
+ * With len the number of cached positions at the start of a step, the step's
+ * calls take: draft step g appends position len + g before attending,
+ * magicdec_draft_cache_update(table[g], table[g], table[g+1]); verification
+ * runs at seq_len = table[gamma+1] (the block's K/V at [len, len+gamma+1));
+ * after acceptance a second call with n_acc gives the next length, and
+ * magicdec_draft_cache_update(table[0], table[gamma], that length) refreshes
+ * the verified rows and drops the rejected ones.
+ *   len_in, n_acc (nullable: advance by 0), len_out [B] int32 device;
+ *   table [(gamma+2) * B] int32 device.  len_out may alias len_in.
+ * Errors: NULL pointers, B <= 0, gamma < 0 or > 1024, L_cap <= 0.
+ */
+MAGICDEC_API magicdec_status magicdec_step_lengths(int B, int gamma, int L_cap, const int32_t *len_in,
+                                                   const int32_t *n_acc, int32_t *len_out, int32_t *table,
+                                                   void *stream);
+
 /* Workspace bytes magicdec_draft_attn / magicdec_verify_attn need for this
  * shape and query count (n_q = 1 for draft) on the current device. */
 MAGICDEC_API size_t magicdec_attn_workspace_size(magicdec_kv_shape shape, int n_q);

@@ -50,6 +50,7 @@ _SIGNATURES = {
     "magicdec_verify_attn": ([KVShape, _I, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "magicdec_verify_attn_noalloc": ([KVShape, _I, _P, _P, _P, _P, _P, _P], _I),
     "magicdec_draft_cache_update": ([KVShape, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P], _I),
+    "magicdec_step_lengths": ([_I, _I, _I, _P, _P, _P, _P, _P], _I),
     "magicdec_pq_encode": ([KVShape, _P, _I, _I, _P, _P, _P], _I),
     "magicdec_pq_update": ([KVShape, _P, _P, _I, _I, _P, _P, _P], _I),
     "magicdec_pq_attn_workspace_size": ([KVShape], _S),
@@ -361,6 +362,29 @@ def magicdec_draft_cache_update(k: torch.Tensor, v: torch.Tensor, kc: torch.Tens
                                              _ptr(origin), _ptr(base), int(ring), int(cap), _ptr(kc), _ptr(vc),
                                              _ptr(draft_len), _stream(stream, dev)))
     return draft_len
+
+
+def magicdec_step_lengths(len_in: torch.Tensor, gamma: int, L_cap: int, n_acc: Optional[torch.Tensor] = None,
+                          len_out: Optional[torch.Tensor] = None, table: Optional[torch.Tensor] = None,
+                          stream=None):
+    """len_in [B] int32 (+ n_acc [B] int32) -> (len_out [B], table [gamma+2, B]) int32:
+    len_out = min(len_in + n_acc + 1, L_cap) (len_in when n_acc is None), table[j] = min(len_out + j, L_cap)."""
+    _need(len_in, "len_in", torch.int32)
+    dev = len_in.device
+    B = len_in.shape[0]
+    _need_shape(len_in, "len_in", torch.int32, dev, (B,))
+    if n_acc is not None:
+        _need_shape(n_acc, "n_acc", torch.int32, dev, (B,))
+    if len_out is None:
+        len_out = torch.empty((B,), dtype=torch.int32, device=dev)
+    if table is None:
+        table = torch.empty((gamma + 2, B), dtype=torch.int32, device=dev)
+    _need_shape(len_out, "len_out", torch.int32, dev, (B,))
+    _need_shape(table, "table", torch.int32, dev, (gamma + 2, B))
+    _check("magicdec_step_lengths",
+           lib().magicdec_step_lengths(int(B), int(gamma), int(L_cap), _ptr(len_in), _ptr(n_acc), _ptr(len_out),
+                                       _ptr(table), _stream(stream, dev)))
+    return len_out, table
 
 
 def _pq_dims(k: torch.Tensor, codebook: torch.Tensor):

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
             const int t = t0 + k2 * 128 + 4 * lane;
             float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             if (t < t1)
-                asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
                              : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
                              : "l"(x + t));
             v[4 * k2] = q.x; v[4 * k2 + 1] = q.y; v[4 * k2 + 2] = q.z; v[4 * k2 + 3] = q.w;
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
 #pragma unroll
         for (int k2 = 0; k2 < kAccPer; ++k2) {
             const int t = t0 + k2 * 32 + lane;
-            v[k2] = t < t1 ? __ldg(x + t) : -INFINITY;
+            v[k2] = t < t1 ? ld_dep_f(x + t) : -INFINITY;
         }
     }
     RowStat st;
@@ -284,10 +284,10 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
     float xt = 0.f, xd = 0.f;
     int xtok = -1;
     if (!p.greedy && warp == 0 && lane < gamma) {
-        xtok = __ldg(p.draft_tok + (long long)b * gamma + lane);
+        xtok = ld_dep(p.draft_tok + (long long)b * gamma + lane);
         if (xtok >= 0 && xtok < V) {
-            xt = __ldg(row_ptr(p, b, lane) + xtok);
-            xd = __ldg(row_ptr(p, b, gamma + 1 + lane) + xtok);
+            xt = ld_dep_f(row_ptr(p, b, lane) + xtok);
+            xd = ld_dep_f(row_ptr(p, b, gamma + 1 + lane) + xtok);
         }
     }
     for (int r = warp; r < p.rows_per_b; r += kChainThreads / 32) {
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
     JobInfo job{};
     int amb = 0, acc = gamma, emit = -1;
     for (int i = 0; i < gamma; ++i) {
-        const int x = __ldg(p.draft_tok + (long long)b * gamma + i);
+        const int x = ld_dep(p.draft_tok + (long long)b * gamma + i);
         bool ok;
         if (p.greedy) {
             const RowAll ts = rs[i];
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
                 ok = oq == 1;
             } else {
                 const double rt = ratio[i];
-                const double u = __ldg(p.u_acc + (long long)b * gamma + i);
+                const double u = ld_dep_f(p.u_acc + (long long)b * gamma + i);
                 ok = u < rt;
                 if (fabs(u - rt) < 1e-4) ++amb;
             }
@@ -432,7 +432,7 @@ __device__ __forceinline__ bool weight_positive(dflt d) { return d.hi != 0.f || 
 
 __device__ __forceinline__ dflt weight_at(const WeightCtx &w, int t) {
     const bool resid = !(w.kind == 2 || w.use_p);
-    return weight_of(w, __ldg(w.tr + t), resid ? __ldg(w.dr + t) : 0.f, resid);
+    return weight_of(w, ld_dep_f(w.tr + t), resid ? ld_dep_f(w.dr + t) : 0.f, resid);
 }
 
 // Running sum of non-negative unnormalised pairs: a two-sum of the high parts,
@@ -528,14 +528,14 @@ __device__ __forceinline__ void batch_chunk_sums(const WeightCtx &w, bool resid,
         xd[u] = none;
         if (c0 + u < n_chunks && t < V) {
             if (vec4) {
-                xt[u] = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
-                if (resid) xd[u] = __ldg(reinterpret_cast<const float4 *>(w.dr + t));
+                xt[u] = ld_dep_f4(reinterpret_cast<const float4 *>(w.tr + t));
+                if (resid) xd[u] = ld_dep_f4(reinterpret_cast<const float4 *>(w.dr + t));
             } else {
                 float a[4], d[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    a[e] = t + e < V ? __ldg(w.tr + t + e) : -INFINITY;
-                    d[e] = (resid && t + e < V) ? __ldg(w.dr + t + e) : -INFINITY;
+                    a[e] = t + e < V ? ld_dep_f(w.tr + t + e) : -INFINITY;
+                    d[e] = (resid && t + e < V) ? ld_dep_f(w.dr + t + e) : -INFINITY;
                 }
                 xt[u] = make_float4(a[0], a[1], a[2], a[3]);
                 xd[u] = make_float4(d[0], d[1], d[2], d[3]);
@@ -591,14 +591,14 @@ __global__ void __launch_bounds__(kChkThreads) accept_chunk_kernel(const AcceptP
         xd[i] = none;
         if (t < V) {
             if ((V & 3) == 0) {
-                xt[i] = __ldg(reinterpret_cast<const float4 *>(w.tr + t));
-                if (resid) xd[i] = __ldg(reinterpret_cast<const float4 *>(w.dr + t));
+                xt[i] = ld_dep_f4(reinterpret_cast<const float4 *>(w.tr + t));
+                if (resid) xd[i] = ld_dep_f4(reinterpret_cast<const float4 *>(w.dr + t));
             } else {
                 float a[4], d[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    a[e] = t + e < V ? __ldg(w.tr + t + e) : -INFINITY;
-                    d[e] = (resid && t + e < V) ? __ldg(w.dr + t + e) : -INFINITY;
+                    a[e] = t + e < V ? ld_dep_f(w.tr + t + e) : -INFINITY;
+                    d[e] = (resid && t + e < V) ? ld_dep_f(w.dr + t + e) : -INFINITY;
                 }
                 xt[i] = make_float4(a[0], a[1], a[2], a[3]);
                 xd[i] = make_float4(d[0], d[1], d[2], d[3]);
@@ -668,7 +668,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const Acc
         __syncthreads();
         W = s_W;
     }
-    const double u = __ldg(p.u_res + b);
+    const double u = ld_dep_f(p.u_res + b);
     const double target = u * W, tol = 1e-7 * W;
     int amb = job.amb;
     if (warp == 0) {
@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const Acc
     dflt wt[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-        wt[e] = my0 + e < ce ? weight_of(w, __ldg(w.tr + my0 + e), resid ? __ldg(w.dr + my0 + e) : 0.f, resid)
+        wt[e] = my0 + e < ce ? weight_of(w, ld_dep_f(w.tr + my0 + e), resid ? ld_dep_f(w.dr + my0 + e) : 0.f, resid)
                              : dflt{0.f, 0.f};
     dflt mine = {0.f, 0.f};
 #pragma unroll

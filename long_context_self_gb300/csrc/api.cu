@@ -26,6 +26,8 @@ magicdec_status launch_draft_cache_update(int B, int H_kv, int D, int L_cap, con
                                           const int32_t *len_valid, const int32_t *len_old, const int32_t *len_new,
                                           const int32_t *origin, const int32_t *base, int ring, int cap, void *kc,
                                           void *vc, int32_t *draft_len, cudaStream_t st);
+magicdec_status launch_step_lengths(int B, int gamma, int L_cap, const int32_t *len_in, const int32_t *n_acc,
+                                    int32_t *len_out, int32_t *table, cudaStream_t st);
 magicdec_status launch_topk_draft_attn(int B, int H_q, int H_kv, int D, int L_cap, const void *q, const void *k,
                                        const void *v, const int32_t *len, int top_k, void *out, int32_t *idx,
                                        void *ws, cudaStream_t st);
@@ -263,6 +265,14 @@ magicdec_status magicdec_draft_cache_update(magicdec_kv_shape shape, const uint1
     return magicdec::launch_draft_cache_update(shape.B, shape.H_kv, shape.d, shape.L_cap, k, v, len_valid, len_old,
                                                len_new, origin, base, ring, cap, kc, vc, draft_len,
                                                static_cast<cudaStream_t>(stream));
+}
+
+magicdec_status magicdec_step_lengths(int B, int gamma, int L_cap, const int32_t *len_in, const int32_t *n_acc,
+                                      int32_t *len_out, int32_t *table, void *stream) {
+    if (!len_in || !len_out || !table) return MAGICDEC_ERR_NULL;
+    if (B <= 0 || gamma < 0 || L_cap <= 0 || gamma > 1024) return MAGICDEC_ERR_SHAPE;
+    return magicdec::launch_step_lengths(B, gamma, L_cap, len_in, n_acc, len_out, table,
+                                         static_cast<cudaStream_t>(stream));
 }
 
 static magicdec_status pq_common(const magicdec_kv_shape &shape, const void *k, int M, int C, const void *codebook,

@@ -108,7 +108,7 @@ __device__ __forceinline__ Segment decode_tile(long long t, const int *prefix, c
     s.h = (int)(local / s.ntiles);
     s.ti0 = (int)(local - (long long)s.h * s.ntiles);
     s.pair_t0 = (long long)p.H_kv * prefix[lo] + (long long)s.h * s.ntiles;
-    s.len = clamp_len(__ldg(p.len + lo), p.L_cap);
+    s.len = clamp_len(ld_dep(p.len + lo), p.L_cap);
     return s;
 }
 
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     // Head tiles per sequence (all tiles less the dynamic tail), loaded in
     // parallel, then an exclusive scan by warp 0.
     for (int b = tid; b < p.B; b += blockDim.x) {
-        const int n = tiles_of(clamp_len(__ldg(p.len + b), p.L_cap));
+        const int n = tiles_of(clamp_len(ld_dep(p.len + b), p.L_cap));
         prefix[b] = n - tail_tiles(n, p.tails);
     }
     __syncthreads();
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
                 const int j = atomicAdd(p.sched, 1);
                 if (j >= n_pairs) break;
                 const int b = j / p.H_kv, h = j - b * p.H_kv;
-                const int len = clamp_len(__ldg(p.len + b), p.L_cap);
+                const int len = clamp_len(ld_dep(p.len + b), p.L_cap);
                 const int n = tiles_of(len), tl = tail_tiles(n, 1);
                 if (tl == 0) continue;
                 const SegDesc d{b, h, n - tl, tl, len, 1};

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__((kHdHeads + 1) * 32, 1)
     }
     pdl_wait();
     // 8-position tiles per sequence, loaded in parallel, then an exclusive scan by warp 0.
-    for (int b = tid; b < p.B; b += blockDim.x) prefix[b] = (hd_clamp(__ldg(p.len + b), p.L_cap) + kHdPos - 1) / kHdPos;
+    for (int b = tid; b < p.B; b += blockDim.x) prefix[b] = (hd_clamp(ld_dep(p.len + b), p.L_cap) + kHdPos - 1) / kHdPos;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__((kHdHeads + 1) * 32, 1)
         const int b = hd_seq_of(t, prefix, p.B);
         const int ti0 = (int)(t - prefix[b]);
         const int nseg = (int)min((long long)prefix[b + 1] - t, t_end - t);
-        const int len = hd_clamp(__ldg(p.len + b), p.L_cap);
+        const int len = hd_clamp(ld_dep(p.len + b), p.L_cap);
         const int lim0 = v0 ? len - p.n_q + r0 / p.G : len - 1;   // last position row r may see
         const int lim1 = v1 ? len - p.n_q + r1 / p.G : len - 1;
 

@@ -168,6 +168,51 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Loads of anything an earlier kernel in the stream may have written (lengths,
+// indices, scores, logits, codebooks).  They are volatile inline PTX, so they
+// keep their place after pdl_wait(): the read-only-path intrinsic __ldg is
+// treated as a load of memory that never changes, and the compiler may issue
+// it ahead of the grid-dependency wait -- before the previous kernel's writes
+// exist.  Small values go through L2 (relaxed, device scope); streamed data
+// is cached in L2 only (.cg), so no L1 line from before the wait is reused.
+__device__ __forceinline__ int ld_dep(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned char ld_dep_u8(const unsigned char *p) {
+    unsigned short v;
+    asm volatile("ld.relaxed.gpu.global.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+    return (unsigned char)v;
+}
+__device__ __forceinline__ float ld_dep_f(const float *p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dep_f4(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_dep_u4(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 ld_dep_u2(const uint2 *p) {
+    uint2 v;
+    asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned ld_dep_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Device-scope acquire-release add: publishes this thread's (and, through a
 // preceding CTA barrier, its CTA's) writes and, for the last arriver, makes
 // the other arrivers' published writes visible.

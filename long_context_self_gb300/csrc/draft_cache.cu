@@ -13,6 +13,9 @@
 // Per sequence the copies form at most three contiguous ranges of positions
 // (see dc_ranges below), so a warp takes (copy, KV head) items and moves one
 // K row and one V row with 16-byte lanes.
+//
+// The step-length kernel below turns (length, accepted count) into the next
+// step's lengths, so a multi-step loop keeps its bookkeeping on the device.
 #include "common.cuh"
 
 namespace magicdec {
@@ -41,10 +44,10 @@ struct DcRanges {
 
 __device__ __forceinline__ DcRanges dc_ranges(const DcParams &p, int b) {
     DcRanges r;
-    const int lo = dc_clamp(__ldg(p.len_old + b), p.L_cap);
-    const int ln = dc_clamp(__ldg(p.len_new + b), p.L_cap);
-    const int lv = min(dc_clamp(__ldg(p.len_valid + b), p.L_cap), min(lo, ln));
-    const int o = max(0, __ldg(p.origin + b));
+    const int lo = dc_clamp(ld_dep(p.len_old + b), p.L_cap);
+    const int ln = dc_clamp(ld_dep(p.len_new + b), p.L_cap);
+    const int lv = min(dc_clamp(ld_dep(p.len_valid + b), p.L_cap), min(lo, ln));
+    const int o = max(0, ld_dep(p.origin + b));
     r.o = o;
     if (p.ring > 0) {
         const int R = p.ring;
@@ -57,7 +60,7 @@ __device__ __forceinline__ DcRanges dc_ranges(const DcParams &p, int b) {
         r.c1 = max(r.c0, min(lo, min(ln + R, lv + R)));
         r.draft_len = ln <= o ? ln : o + min(ln - o, R);
     } else {
-        r.bs = max(0, __ldg(p.base + b));
+        r.bs = max(0, ld_dep(p.base + b));
         r.a0 = max(lv, o);
         r.a1 = max(r.a0, ln);
         r.b0 = r.b1 = r.c0 = r.c1 = 0;
@@ -96,9 +99,9 @@ __global__ void __launch_bounds__(kDcThreads) draft_cache_update_kernel(const Dc
         const long long from = (((long long)b * p.L_cap + src) * p.H_kv + h) * p.cpr;
         const long long to = (((long long)b * p.H_kv + h) * p.cap + slot) * p.cpr;
         if (lane < p.cpr) {
-            p.kc[to + lane] = __ldg(p.k + from + lane);
+            p.kc[to + lane] = ld_dep_u4(p.k + from + lane);
         } else if (lane < 2 * p.cpr) {
-            p.vc[to + lane - p.cpr] = __ldg(p.v + from + lane - p.cpr);
+            p.vc[to + lane - p.cpr] = ld_dep_u4(p.v + from + lane - p.cpr);
         }
     }
     if (blockIdx.y == 0 && threadIdx.x == 0) p.draft_len[b] = min(r.draft_len, p.cap);
@@ -127,6 +130,32 @@ magicdec_status launch_draft_cache_update(int B, int H_kv, int D, int L_cap, con
     p.cap = cap;
     p.cpr = D * 2 / 16;
     return magicdec_host::launch_pdl(draft_cache_update_kernel, dim3(B, kDcCtasPerSeq), dim3(kDcThreads), 0, st, p);
+}
+
+// ---------------------------------------------------------------- step lengths
+// Per sequence: len = clamp(len_in + (n_acc ? n_acc + 1 : 0), 0, L_cap), then
+// len_out = len and table[j][b] = min(len + j, L_cap) for j = 0 .. gamma+1:
+// the lengths one speculative step's calls take (draft step g appends
+// position len + g; verification sees len + gamma + 1).  len_out may alias
+// len_in (each thread reads its element before writing it).
+__global__ void step_lengths_kernel(int B, int gamma, int L_cap, const int32_t *len_in, const int32_t *n_acc,
+                                    int32_t *len_out, int32_t *table) {
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    long long len = ld_dep(len_in + b);
+    if (n_acc) len += (long long)ld_dep(n_acc + b) + 1;
+    const int l = (int)(len < 0 ? 0 : (len > L_cap ? L_cap : len));
+    len_out[b] = l;
+    for (int j = 0; j <= gamma + 1; ++j) table[(long long)j * B + b] = min(l + j, L_cap);
+}
+
+magicdec_status launch_step_lengths(int B, int gamma, int L_cap, const int32_t *len_in, const int32_t *n_acc,
+                                    int32_t *len_out, int32_t *table, cudaStream_t st) {
+    const int threads = 256;
+    return magicdec_host::launch_pdl(step_lengths_kernel, dim3((unsigned)((B + threads - 1) / threads)),
+                                     dim3(threads), 0, st, B, gamma, L_cap, len_in, n_acc, len_out, table);
 }
 
 }  // namespace magicdec

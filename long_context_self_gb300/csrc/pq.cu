@@ -60,8 +60,8 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 u, float (&x)[8]) {
 
 // ------------------------------------------------------------------ encode
 template <int D>
-__global__ void __launch_bounds__(kPqEncThreads) pq_encode_kernel(const __nv_bfloat16 *__restrict__ k,
-                                                                 const float *__restrict__ codebook,
+__global__ void __launch_bounds__(kPqEncThreads) pq_encode_kernel(const __nv_bfloat16 *k,
+                                                                 const float *codebook,
                                                                  uint8_t *__restrict__ codes, int H_kv, int L_cap,
                                                                  int C) {
     constexpr int M = D / kPqDs;
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kPqEncThreads) pq_encode_kernel(const __nv_bfl
     pdl_trigger();
     pdl_wait();
     const float4 *src = reinterpret_cast<const float4 *>(codebook + ((size_t)b * H_kv + h) * M * C * kPqDs);
-    for (int i = tid; i < M * C * kPqDs / 4; i += kPqEncThreads) reinterpret_cast<float4 *>(cb)[i] = __ldg(src + i);
+    for (int i = tid; i < M * C * kPqDs / 4; i += kPqEncThreads) reinterpret_cast<float4 *>(cb)[i] = ld_dep_f4(src + i);
     __syncthreads();
     for (int i = tid; i < M * C; i += kPqEncThreads) {
         const float *c = cb + (size_t)i * kPqDs;
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kPqEncThreads) pq_encode_kernel(const __nv_bfl
         for (int m = 0; m < M; ++m) {
             float x[KPT][8];
 #pragma unroll
-            for (int r = 0; r < KPT; ++r) bf16x8_to_float(__ldg(kr[r] + m), x[r]);
+            for (int r = 0; r < KPT; ++r) bf16x8_to_float(ld_dep_u4(kr[r] + m), x[r]);
             float best[KPT];
             int arg[KPT];
 #pragma unroll
@@ -152,9 +152,9 @@ __global__ void __launch_bounds__(kPqEncThreads) pq_encode_kernel(const __nv_bfl
 
 // ------------------------------------------------------------------ update
 template <int D>
-__global__ void __launch_bounds__(kPqUpdThreads) pq_update_kernel(const __nv_bfloat16 *__restrict__ k,
-                                                                 const int32_t *__restrict__ len_p,
-                                                                 const uint8_t *__restrict__ codes,
+__global__ void __launch_bounds__(kPqUpdThreads) pq_update_kernel(const __nv_bfloat16 *k,
+                                                                 const int32_t *len_p,
+                                                                 const uint8_t *codes,
                                                                  float *__restrict__ codebook, int H_kv, int L_cap,
                                                                  int C) {
     constexpr int M = D / kPqDs;
@@ -171,16 +171,16 @@ __global__ void __launch_bounds__(kPqUpdThreads) pq_update_kernel(const __nv_bfl
     for (int i = tid; i < MH * C * kPqDs; i += kPqUpdThreads) sum[i] = 0ull;
     for (int i = tid; i < MH * C; i += kPqUpdThreads) cnt[i] = 0;
     __syncthreads();
-    const int len = pq_clamp(__ldg(len_p + b), L_cap);
+    const int len = pq_clamp(ld_dep(len_p + b), L_cap);
     for (int j = tid; j < len; j += kPqUpdThreads) {
         const uint8_t *cr = codes + (((size_t)b * H_kv + h) * L_cap + j) * M + m0;
         const uint4 *kr = reinterpret_cast<const uint4 *>(k + (((size_t)b * L_cap + j) * H_kv + h) * D) + m0;
 #pragma unroll 1
         for (int mm = 0; mm < MH; ++mm) {
-            const int c = __ldg(cr + mm);
+            const int c = ld_dep_u8(cr + mm);
             if (c >= C) continue;
             float x[8];
-            bf16x8_to_float(__ldg(kr + mm), x);
+            bf16x8_to_float(ld_dep_u4(kr + mm), x);
             atomicAdd(cnt + mm * C + c, 1);
             unsigned long long *s = sum + (size_t)mm * kPqDs * C + c;
 #pragma unroll
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     pdl_trigger();
     pdl_wait();
     for (int b = tid; b < p.B; b += kPqScThreads)
-        prefix[b] = (pq_clamp(__ldg(p.len + b), p.L_cap) + kPqScTile - 1) / kPqScTile;
+        prefix[b] = (pq_clamp(ld_dep(p.len + b), p.L_cap) + kPqScTile - 1) / kPqScTile;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     auto load_codes = [&](long long tt, uint4 (&dst)[kPqScPer]) {
         int hh, tti;
         const int bb = pq_locate(tt, prefix, p.B, p.H_kv, hh, tti);
-        const int ll = pq_clamp(__ldg(p.len + bb), p.L_cap);
+        const int ll = pq_clamp(ld_dep(p.len + bb), p.L_cap);
         const uint8_t *cbase = p.codes + ((size_t)bb * p.H_kv + hh) * p.L_cap * M;
 #pragma unroll
         for (int i = 0; i < kPqScPer; ++i) {
@@ -259,9 +259,9 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
             dst[i] = make_uint4(0u, 0u, 0u, 0u);
             if (j < ll) {
                 if (M == 16) {
-                    dst[i] = __ldg(reinterpret_cast<const uint4 *>(cbase + (size_t)j * M));
+                    dst[i] = ld_dep_u4(reinterpret_cast<const uint4 *>(cbase + (size_t)j * M));
                 } else {
-                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(cbase + (size_t)j * M));
+                    const uint2 u = ld_dep_u2(reinterpret_cast<const uint2 *>(cbase + (size_t)j * M));
                     dst[i].x = u.x;
                     dst[i].y = u.y;
                 }
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     for (long long t = t0; t < t1; ++t) {
         int h, ti;
         const int b = pq_locate(t, prefix, p.B, p.H_kv, h, ti);
-        const int len = pq_clamp(__ldg(p.len + b), p.L_cap);
+        const int len = pq_clamp(ld_dep(p.len + b), p.L_cap);
         if (t + 1 < t1) load_codes(t + 1, nxt);
         if (b != cur_b || h != cur_h) {            // lookup table of this (sequence, KV head) for its G query heads
             __syncthreads();
@@ -292,8 +292,8 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
                 for (int u = 0; u < BATCH; ++u) {
                     const int mc = mc0 + u * kPqScThreads;
                     if (mc < M * C) {
-                        c0[u] = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs));
-                        c1[u] = __ldg(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs + 4));
+                        c0[u] = ld_dep_f4(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs));
+                        c1[u] = ld_dep_f4(reinterpret_cast<const float4 *>(cbh + (size_t)mc * kPqDs + 4));
                     }
                 }
 #pragma unroll
@@ -381,7 +381,7 @@ constexpr int kPqTcKeys = 16;                      // keys per warp batch (one m
 
 template <int D>
 __global__ void __launch_bounds__(kPqTcThreads, 1)
-    pq_encode_tc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ codebook,
+    pq_encode_tc_kernel(const __nv_bfloat16 *k, const float *codebook,
                         uint8_t *__restrict__ codes, int H_kv, int L_cap, int C, int CP) {
     constexpr int M = D / kPqDs;
     extern __shared__ __align__(128) uint8_t pq_tc_smem[];
@@ -397,8 +397,8 @@ __global__ void __launch_bounds__(kPqTcThreads, 1)
         uint32_t w[3][4];
         float n = INFINITY;
         if (c < C) {
-            const float4 u0 = __ldg(reinterpret_cast<const float4 *>(cbh + ((size_t)m * C + c) * kPqDs));
-            const float4 u1 = __ldg(reinterpret_cast<const float4 *>(cbh + ((size_t)m * C + c) * kPqDs + 4));
+            const float4 u0 = ld_dep_f4(reinterpret_cast<const float4 *>(cbh + ((size_t)m * C + c) * kPqDs));
+            const float4 u1 = ld_dep_f4(reinterpret_cast<const float4 *>(cbh + ((size_t)m * C + c) * kPqDs + 4));
             const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
             float s2 = 0.f;
 #pragma unroll
@@ -445,8 +445,8 @@ __global__ void __launch_bounds__(kPqTcThreads, 1)
         const uint32_t *kb = reinterpret_cast<const uint32_t *>(k + (((size_t)b * L_cap + jb) * H_kv + h) * D);
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            dst[m][0] = __ldg(ka + m * 4 + t4);
-            dst[m][1] = __ldg(kb + m * 4 + t4);
+            dst[m][0] = ld_dep_u32(ka + m * 4 + t4);
+            dst[m][1] = ld_dep_u32(kb + m * 4 + t4);
         }
     };
     uint32_t a_cur[M][2], a_nxt[M][2];

@@ -29,7 +29,7 @@ __global__ void streaming_select_kernel(const int32_t *seq_len, int H_kv, int n_
     const long long width = (long long)n_sink + n_recent;
     const long long j = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const int h = blockIdx.y, b = blockIdx.z;
-    const int len = max(__ldg(seq_len + b), 0);
+    const int len = max(ld_dep(seq_len + b), 0);
     const int sinks = min(n_sink, len);
     const int rec0 = max(n_sink, len - n_recent);
     const int n = sinks + max(0, len - rec0);
@@ -48,8 +48,8 @@ __global__ void streaming_select_kernel(const int32_t *seq_len, int H_kv, int n_
 // that RPI loads per lane are in flight.  The row -> (sequence, head, slot)
 // decode is done once per row by one lane and broadcast.
 template <int CPR, int RPI>
-__global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
-                                                       const int32_t *__restrict__ idx, int H_kv, int L_cap,
+__global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *k, const uint4 *v,
+                                                       const int32_t *idx, int H_kv, int L_cap,
                                                        int n_idx, int cap, int rows, uint4 *__restrict__ kc,
                                                        uint4 *__restrict__ vc) {
     constexpr int LPR = 2 * CPR;                 // lanes per row (K and V)
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict_
                 const int bh = (int)(row / n_idx);
                 const int i = (int)(row - (long long)bh * n_idx);
                 const int h = bh % H_kv, b = bh / H_kv;
-                const int pos = __ldg(idx + row);
+                const int pos = ld_dep(idx + row);
                 dst_off = ((long long)bh * cap + i) * CPR;
                 if (pos >= 0 && pos < L_cap) src_off = (((long long)b * L_cap + pos) * H_kv + h) * CPR;
             }
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict_
             val[r] = make_uint4(0, 0, 0, 0);
             if (dsto[r] >= 0 && so >= 0) {
                 const uint4 *src = (kv ? v : k) + so + ch;
-                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
                              : "=r"(val[r].x), "=r"(val[r].y), "=r"(val[r].z), "=r"(val[r].w)
                              : "l"(src));
             }
@@ -103,13 +103,13 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *__restrict_
 // [0, m), m = len - w (half <= 4); row stride L_sc (a multiple of 4 floats).
 // A thread pools 4 consecutive positions 4t..4t+3 from the three aligned
 // float4 groups around them.
-__global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *__restrict__ score,
-                                                         const int32_t *__restrict__ seq_len, int H_kv, int L_cap,
+__global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *score,
+                                                         const int32_t *seq_len, int H_kv, int L_cap,
                                                          int L_sc, int w, int half, float *__restrict__ pooled) {
     pdl_trigger();
     pdl_wait();
     const int h = blockIdx.y, b = blockIdx.z;
-    const int m = clamp_len_s(__ldg(seq_len + b), L_cap) - w;
+    const int m = clamp_len_s(ld_dep(seq_len + b), L_cap) - w;
     const float *sc = score + ((long long)b * H_kv + h) * L_cap;
     float *out = pooled + ((long long)b * H_kv + h) * L_sc;
     for (int g = blockIdx.x * blockDim.x + threadIdx.x; 4 * g < m; g += gridDim.x * blockDim.x) {
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256) snapkv_pool_kernel(const float *__restric
 #pragma unroll
         for (int e = 0; e < 12; ++e) {
             const int t = j0 - 4 + e;
-            x[e] = (t >= 0 && t < m) ? __ldg(sc + t) : -INFINITY;
+            x[e] = (t >= 0 && t < m) ? ld_dep_f(sc + t) : -INFINITY;
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__((kTkConsumers + 1) * 32, 2)
     }
     pdl_wait();
     for (int b = tid; b < p.B; b += blockDim.x)
-        prefix[b] = (tk_clamp_len(__ldg(p.len + b), p.L_cap) + kTkTileN - 1) / kTkTileN;
+        prefix[b] = (tk_clamp_len(ld_dep(p.len + b), p.L_cap) + kTkTileN - 1) / kTkTileN;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -197,8 +197,8 @@ __global__ void __launch_bounds__((kTkConsumers + 1) * 32, 2)
                 p.q + ((long long)qb_b * p.H_q + qb_h * p.G + (valid ? nrow : 0)) * D);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                bq[ks][0] = valid ? __ldg(qrow + ks * 8 + (lane & 3)) : 0u;
-                bq[ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + (lane & 3)) : 0u;
+                bq[ks][0] = valid ? ld_dep_u32(qrow + ks * 8 + (lane & 3)) : 0u;
+                bq[ks][1] = valid ? ld_dep_u32(qrow + ks * 8 + 4 + (lane & 3)) : 0u;
             }
         }
         const int stage = i % p.stages;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__((kTkConsumers + 1) * 32, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
 
-        const int len = tk_clamp_len(__ldg(p.len + cur.b), p.L_cap);
+        const int len = tk_clamp_len(ld_dep(p.len + cur.b), p.L_cap);
         const int pos = cur.ti * kTkTileN + warp * 16 + key_l;
         float *srow = p.score + ((long long)cur.b * p.H_q + (long long)cur.h * p.G) * p.L_sc;
         if (g0 < p.G) {
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__((kTkHdHeads + 1) * 32, 2)
     }
     pdl_wait();
     for (int b = tid; b < p.B; b += blockDim.x)
-        prefix[b] = (tk_clamp_len(__ldg(p.len + b), p.L_cap) + kTkHdPos - 1) / kTkHdPos;
+        prefix[b] = (tk_clamp_len(ld_dep(p.len + b), p.L_cap) + kTkHdPos - 1) / kTkHdPos;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -344,8 +344,8 @@ __global__ void __launch_bounds__((kTkHdHeads + 1) * 32, 2)
                 p.q + ((long long)b * p.H_q + h * p.G + (valid ? nrow : 0)) * D);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                bq[ks][0] = valid ? __ldg(qrow + ks * 8 + (lane & 3)) : 0u;
-                bq[ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + (lane & 3)) : 0u;
+                bq[ks][0] = valid ? ld_dep_u32(qrow + ks * 8 + (lane & 3)) : 0u;
+                bq[ks][1] = valid ? ld_dep_u32(qrow + ks * 8 + 4 + (lane & 3)) : 0u;
             }
         }
         const int stage = i % p.stages;
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__((kTkHdHeads + 1) * 32, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
 
-        const int len = tk_clamp_len(__ldg(p.len + b), p.L_cap);
+        const int len = tk_clamp_len(ld_dep(p.len + b), p.L_cap);
         const int pos = (int)(t - prefix[b]) * kTkHdPos + key_l;
         float *srow = p.score + ((long long)b * p.H_q + (long long)h * p.G) * p.L_sc;
         if (g0 < p.G) {
@@ -452,7 +452,7 @@ __device__ __forceinline__ void tk_find_digit(const int *hist, int remaining, in
 // at or past `hi` give key 0.  The row holds at least len rounded up to 4.
 __device__ __forceinline__ void tk_load4(const float *srow, int j, int hi, uint32_t (&k)[4]) {
     if (j < hi) {
-        const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + j));
+        const float4 f = ld_dep_f4(reinterpret_cast<const float4 *>(srow + j));
         k[0] = tk_key(f.x);
         k[1] = j + 1 < hi ? tk_key(f.y) : 0u;
         k[2] = j + 2 < hi ? tk_key(f.z) : 0u;
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
     pdl_wait();
-    const int full = tk_clamp_len(__ldg(p.len + b), p.L_cap);
+    const int full = tk_clamp_len(ld_dep(p.len + b), p.L_cap);
     const int kvh = hq / p.G;
     const long long row = (long long)b * p.H_q + hq;
     const float *srow = p.score + row * p.L_sc;
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
         // SnapKV: everything when the sequence fits the budget; else the
         // window is always kept and budget - window prefix positions compete
         const int w = p.len_sub;
-        const int budget = p.budgets ? min(max(__ldg(p.budgets + b), w), p.top_k) : p.top_k;
+        const int budget = p.budgets ? min(max(ld_dep(p.budgets + b), w), p.top_k) : p.top_k;
         if (full <= budget || budget == w) {
             const int keep_from = full <= budget ? 0 : full - w;
             const int n_keep = full - keep_from;
@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
         // channels sub*8 .. +7 of q and the K row, the group's lanes sum
         float qv[8];
         {
-            const uint4 qq = __ldg(reinterpret_cast<const uint4 *>(p.q + row * D + sub * 8));
+            const uint4 qq = ld_dep_u4(reinterpret_cast<const uint4 *>(p.q + row * D + sub * 8));
             const uint32_t w4[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -761,7 +761,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
             for (int u = 0; u < UK; ++u) {
                 const int i = warp + NW * (RPI * (t0 + u) + part);
                 raw[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < n) raw[u] = __ldg(reinterpret_cast<const uint4 *>(kb + (long long)sel[i] * kstride));
+                if (i < n) raw[u] = ld_dep_u4(reinterpret_cast<const uint4 *>(kb + (long long)sel[i] * kstride));
             }
 #pragma unroll
             for (int u = 0; u < UK; ++u) {
@@ -808,8 +808,8 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
             raw[u] = make_uint4(0u, 0u, 0u, 0u);
             if (i < n) {
                 const int j = sel[i];
-                sc[u] = EXACT ? ex[i] : __ldg(srow + j);
-                raw[u] = __ldg(reinterpret_cast<const uint4 *>(vb + (long long)j * vstride));
+                sc[u] = EXACT ? ex[i] : ld_dep_f(srow + j);
+                raw[u] = ld_dep_u4(reinterpret_cast<const uint4 *>(vb + (long long)j * vstride));
             }
         }
 #pragma unroll

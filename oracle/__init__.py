@@ -62,13 +62,14 @@ def _load():
             lib.oracle_resample_weights.argtypes = [P, P, I, P]
             lib.oracle_topk_attn.argtypes = [I, I, I, I, I, P, P, P, P, I, P, P, P]
             lib.oracle_draft_cache_update.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I, I, P, P, P]
+            lib.oracle_step_lengths.argtypes = [I, I, I, P, P, P, P]
             lib.oracle_pq_encode.argtypes = [I, I, I, I, P, I, I, P, P, P]
             lib.oracle_pq_update.argtypes = [I, I, I, I, P, P, I, I, P, P]
             lib.oracle_pq_attn.argtypes = [I, I, I, I, I, P, P, P, P, I, I, P, P, I, P, P, P]
             for name in ("oracle_verify_attn", "oracle_draft_attn", "oracle_streaming_select",
                          "oracle_gather_kv", "oracle_snapkv_scores", "oracle_maxpool1d",
                          "oracle_snapkv_select", "oracle_spec_accept", "oracle_resample_weights",
-                         "oracle_topk_attn", "oracle_draft_cache_update", "oracle_pq_encode",
+                         "oracle_topk_attn", "oracle_draft_cache_update", "oracle_step_lengths", "oracle_pq_encode",
                          "oracle_pq_update", "oracle_pq_attn"):
                 getattr(lib, name).restype = I
             _lib = lib
@@ -217,6 +218,18 @@ def draft_cache_update(k, v, kc, vc, len_valid, len_old, len_new, origin, base, 
     if rc < 0:
         raise ValueError("draft_cache_update: invalid arguments")
     return draft_len, int(rc)
+
+
+def step_lengths(len_in, gamma: int, L_cap: int, n_acc=None):
+    """-> (len_out int32 [B], table int32 [gamma+2, B]); see oracle_step_lengths."""
+    len_in = _c(len_in, np.int32)
+    B = len_in.shape[0]
+    na = _c(n_acc, np.int32) if n_acc is not None else None
+    len_out = np.empty((B,), np.int32)
+    table = np.empty((gamma + 2, B), np.int32)
+    _check(_load().oracle_step_lengths(B, int(gamma), int(L_cap), _ptr(len_in), _ptr(na) if na is not None else None,
+                                       _ptr(len_out), _ptr(table)), "step_lengths")
+    return len_out, table
 
 
 def pq_encode(k, codebook, want_gap: bool = False):

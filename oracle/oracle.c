@@ -386,6 +386,31 @@ int oracle_snapkv_select(int B, int H_q, int H_kv, int d, int L_cap,
 }
 
 /*
+ * Lengths of one speculative step (section 3.1: gamma draft tokens are
+ * verified together with the pending token, n_acc of the drafts are kept and
+ * one token is emitted, so the sequence gains n_acc + 1 cached positions).
+ * For each sequence: len = len_in + (n_acc ? n_acc + 1 : 0), clamped to
+ * [0, L_cap]; len_out = len; table[j * B + b] = min(len + j, L_cap) for
+ * j = 0 .. gamma+1 (the lengths that draft step j appends to and that the
+ * verification of the gamma+1 block sees).
+ */
+int oracle_step_lengths(int B, int gamma, int L_cap, const int32_t *len_in, const int32_t *n_acc, int32_t *len_out,
+                        int32_t *table)
+{
+    int b, j;
+    if (B <= 0 || gamma < 0 || L_cap <= 0) return -1;
+    for (b = 0; b < B; ++b) {
+        long len = len_in[b];
+        if (n_acc) len += (long)n_acc[b] + 1;
+        if (len < 0) len = 0;
+        if (len > L_cap) len = L_cap;
+        len_out[b] = (int32_t)len;
+        for (j = 0; j <= gamma + 1; ++j) table[(long)j * B + b] = (int32_t)(len + j < L_cap ? len + j : L_cap);
+    }
+    return 0;
+}
+
+/*
  * Draft-cache update: keeps the compact draft cache equal to the static
  * selection as the sequence grows by accepted tokens and shrinks when
  * speculated tokens are rejected (section 4.4: the static drafts select once

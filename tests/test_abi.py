@@ -124,6 +124,11 @@ def test_null_and_shape_errors_are_reported_before_launch(lib):
                                            NULL) == -2
     assert lib.magicdec_draft_cache_update(shape(), FAKE, FAKE, I32, I32, I32, I32, NULL, 16, 64, MISALIGNED, FAKE,
                                            I32, NULL) == -3
+    assert lib.magicdec_step_lengths(4, 3, 100, NULL, NULL, I32, I32, NULL) == -1
+    assert lib.magicdec_step_lengths(4, 3, 100, I32, NULL, I32, NULL, NULL) == -1
+    assert lib.magicdec_step_lengths(0, 3, 100, I32, NULL, I32, I32, NULL) == -2
+    assert lib.magicdec_step_lengths(4, -1, 100, I32, NULL, I32, I32, NULL) == -2
+    assert lib.magicdec_step_lengths(4, 3, 0, I32, NULL, I32, I32, NULL) == -2
     assert lib.magicdec_topk_draft_attn(shape(), NULL, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, big, NULL) == -1
     assert lib.magicdec_topk_draft_attn(shape(), FAKE, FAKE, FAKE, FAKE, 0, FAKE, NULL, FAKE, big, NULL) == -2
     assert lib.magicdec_topk_draft_attn(shape(d=96), FAKE, FAKE, FAKE, FAKE, 16, FAKE, NULL, FAKE, big, NULL) == -2

@@ -739,3 +739,28 @@ def test_spec_accept_margins_at_planted_boundaries():
                                                         want_margins=True)
     assert n_acc.tolist() == [1] and out.tolist() == [[0, 1]] and amb.tolist() == [1]
     assert acc_m.tolist() == [[2.0 ** -16, 2.0]] and np.isnan(draw_m[0])
+
+
+def test_step_lengths_follow_the_token_sequence():
+    """A sequence simulated token by token: a speculative step caches the pending token and the
+    accepted drafts and leaves the emitted token pending, so the cached length grows by
+    n_acc + 1; draft step g of the next step appends the (g+1)-th new position.  Lengths stop
+    at the cache capacity."""
+    rng = np.random.default_rng(12)
+    B, gamma, L_cap = 9, 4, 600
+    cached = [list(range(int(n))) for n in rng.integers(0, 560, B)]
+    lens = np.array([len(c) for c in cached], np.int32)
+    for _ in range(12):
+        n_acc = rng.integers(0, gamma + 1, B).astype(np.int32)
+        got, table = oracle.step_lengths(lens, gamma, L_cap, n_acc)
+        for b in range(B):
+            block = [len(cached[b]) + i for i in range(gamma + 1)]    # pending token + gamma drafts
+            kept = block[: n_acc[b] + 1]
+            cached[b] = (cached[b] + kept)[:L_cap]
+            assert got[b] == len(cached[b])
+            # the next step's draft appends positions len, len+1, ... and verifies len .. len+gamma
+            nxt = [p for p in range(len(cached[b]), len(cached[b]) + gamma + 2)]
+            assert table[:, b].tolist() == [min(p, L_cap) for p in nxt]
+        lens = got
+    same, t0 = oracle.step_lengths(lens, gamma, L_cap)
+    assert np.array_equal(same, lens) and np.array_equal(t0[0], lens)
