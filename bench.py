@@ -12,9 +12,20 @@ then acceptance):
     speculative accept / resample over the vocabulary
 
 Each layer reuses one layer's KV cache (16.8 GB at B=128, L=32000, far larger
-than the 129 MB L2, so no layer sees another's data in cache).  SnapKV selection
-runs once after prefill in the method; it is timed once per run and reported
-beside the step.  Inputs are synthetic (seeded; see long_context_self_gb300.synth).
+than the 129 MB L2, so no layer sees another's data in cache).  Inputs are
+synthetic (seeded; see long_context_self_gb300.synth).
+
+Beside the headline step the line carries:
+  snapkv_step   the same workload drafted by SnapKV (budget 512): selection
+                once after prefill (paper section A.1, Fig. 8), then 16 steps
+                of the loop in long_context_self_gb300.pipeline, whose lengths
+                diverge by each sequence's accepted count;
+  per_config    the other long-context configurations on the same GPU: B=32
+                StreamingLLM 16+496; B=64 SnapKV 2048 (select once, 16 steps);
+                B=16, L=100000, 40 query heads, SnapKV 4096 (select once,
+                16 steps);
+  rows_roofline every kernel row's GB/s against the measured copy peak and
+                against the 8 TB/s nominal HBM bandwidth (frac, frac_8tbs).
 
 `python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]` prints
 one JSON line.  Under torchrun each rank runs its own batch on its own GPU (the
@@ -45,8 +56,9 @@ from long_context_self_gb300 import synth  # noqa: E402
 DEFAULT_WORKLOAD = "llama8b_b128_l32k"
 METRIC = "verify/draft attn achieved HBM GB/s (% of peak); spec steps/s at B=128 L=32k"
 LAYERS = 32
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_attn_llama8b_b128_l32k.md")
-ATTN_SRC = os.path.join(ROOT, "long_context_self_gb300", "csrc", "attn_heads.cu")   # the verification kernel at this shape
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "verify_attn_llama8b_b128_l32k.json")
+NOMINAL_HBM_GBS = 8000.0    # GB300 HBM3e nominal bandwidth (8 TB/s): the second denominator of every fraction
+SPEC_LOOP_STEPS = 16        # draft+verify steps after one SnapKV selection (the SnapKV-drafted legs)
 
 
 # --------------------------------------------------------------------- helpers
@@ -95,28 +107,18 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def file_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
-
-
-def recorded_traffic(workload: str):
-    """Per-launch DRAM bytes of verify_attn from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def recorded_traffic(workload: str, record: str = TRAFFIC_RECORD):
+    """Per-launch DRAM bytes of the verification kernel from the committed ncu record
+    (written by long_context_self_gb300.ncu_record), if it was taken for this workload on the
+    current kernel source; else None."""
+    from long_context_self_gb300.ncu_record import source_sha16
     try:
-        text = open(PROFILE_TRAFFIC).read()
-    except OSError:
-        return None
-    vals = {}
-    for line in text.splitlines():
-        if ": " in line and line.strip().startswith("- "):
-            key, _, val = line.strip()[2:].partition(": ")   # keys may contain ':' (e.g. "sha256[:16]")
-            vals[key.strip()] = val.strip().strip("`")
-    if vals.get("workload") != workload or vals.get("attn_heads.cu sha256[:16]") != file_sha(ATTN_SRC):
-        return None
-    try:
-        return float(vals["dram bytes per launch (full workload)"])
-    except (KeyError, ValueError):
+        with open(record) as f:
+            rec = json.load(f)
+        if rec["workload"] != workload or rec["source_sha16"] != source_sha16(os.path.join(ROOT, rec["source"])):
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
         return None
 
 
@@ -185,7 +187,9 @@ class Pipeline:
         from long_context_self_gb300 import binding as mb
         self.mb = mb
         self.w, self.dev, self.layers = w, device, layers
-        self.k, self.v, _ = synth.kv_cache(w, device)
+        # room past L for the positions the SnapKV-drafted loop appends
+        self.L_cap = w.L + SPEC_LOOP_STEPS * (w.gamma + 1)
+        self.k, self.v, self.heavy_dirs = synth.kv_cache(w, device, L_cap=self.L_cap)
         self.seq_len = torch.full((w.B,), w.L, dtype=torch.int32, device=device)
         self.q_draft = synth.queries(w, 1, device, seed=w.seed * 7 + 1)
         self.q_verify = synth.queries(w, w.n_q, device, seed=w.seed * 7 + 2)
@@ -200,7 +204,7 @@ class Pipeline:
         self.n_acc = torch.empty((w.B,), dtype=torch.int32, device=device)
         self.out_tok = torch.empty((w.B, w.n_q), dtype=torch.int32, device=device)
         self.n_amb = torch.empty((w.B,), dtype=torch.int32, device=device)
-        shape = mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L)
+        shape = mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, self.L_cap)
         ws_attn = max(mb.magicdec_attn_workspace_size(shape, w.n_q),
                       mb.magicdec_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, self.cap), 1))
         self.ws_attn = torch.zeros(ws_attn, dtype=torch.uint8, device=device)
@@ -324,6 +328,156 @@ def time_graph(fn, reps: int) -> float:
     return e0.elapsed_time(e1) / reps
 
 
+def fractions(gbs: float, peak: float) -> dict:
+    """A bandwidth against both denominators: the measured copy peak and the 8 TB/s nominal."""
+    return {"frac": round(gbs / peak, 4), "frac_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+
+def config_dict(w: synth.Workload, layers: int, world: int) -> dict:
+    """The `config` of both arms' JSON lines."""
+    return {"workload": w.name, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
+            "gamma": w.gamma, "V": w.V, "layers": layers,
+            "draft": f"StreamingLLM {w.n_sink}+{w.n_recent} (selection + gather every step)",
+            "per_rank_batch": w.B, "parallelism": f"replicas x{world}",
+            "rank_seeds": "workload seed + 100 x rank (distinct sequences per rank)",
+            "l2": f"inputs larger than L2 (KV cache {2 * w.B * w.L * w.H_kv * w.d * 2 / 1e9:.1f} GB per layer "
+                  f"vs 129 MB L2)",
+            "step": "layers x (select, gather, gamma x draft_attn, verify_attn) + spec_accept"}
+
+
+def time_streaming_step(pipe: "Pipeline", steps: int, warmup: int, world: int, device):
+    """The StreamingLLM step: warm-up, then `steps` steps between barriers; returns (max-over-ranks
+    ms for all steps, mean verify ms from events around its launches, draft ms per call, accept
+    ms, select+gather ms)."""
+    mb, w = pipe.mb, pipe.w
+    for _ in range(warmup):
+        pipe.step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    pipe.verify_events = []
+    stream = torch.cuda.current_stream(device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        pipe.step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_total = max_over_ranks(t0.elapsed_time(t1), device)
+    ver_ms = statistics.mean(a.elapsed_time(b) for a, b in pipe.verify_events)
+    # draft launches are timed back to back outside the step (events between the
+    # step's kernels would serialise their programmatic-dependent launches): one
+    # step's gamma x layers calls replayed from a CUDA graph, so that the
+    # binding's host-side checks cannot set the pace of these ~50 us calls
+    n_dra = w.gamma * pipe.layers
+    dra_ms = time_graph(lambda: [mb.magicdec_draft_attn(pipe.q_draft, pipe.kc, pipe.vc, pipe.n_sel,
+                                                        out=pipe.out_d, ws=pipe.ws_attn) for _ in range(n_dra)],
+                        3) / n_dra
+    acc_ms = time_component(lambda: mb.magicdec_spec_accept(pipe.target, pipe.draft, pipe.tok, pipe.u_acc,
+                                                            pipe.u_res, False, n_acc=pipe.n_acc,
+                                                            out_tok=pipe.out_tok, n_amb=pipe.n_amb,
+                                                            ws=pipe.ws_acc), 5)
+    sel_ms = time_component(lambda: (mb.magicdec_streaming_select(pipe.seq_len, w.H_kv, w.n_sink, w.n_recent,
+                                                                  idx=pipe.idx, n_sel=pipe.n_sel),
+                                     mb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc,
+                                                           vc=pipe.vc)), 5)
+    return ms_total, ver_ms, dra_ms, acc_ms, sel_ms
+
+
+def snapkv_loop_leg(w: synth.Workload, k: torch.Tensor, v: torch.Tensor, layers: int, device, peak: float,
+                    heavy_dirs=None, world: int = 1) -> dict:
+    """Self-speculation with a static SnapKV draft: selection once after prefill, then
+    SPEC_LOOP_STEPS steps of (per layer: gamma x (append + draft attention), verification;
+    acceptance; the length bookkeeping; per layer the post-verification refresh), lengths
+    diverging by each sequence's accepted count.  One warm-up pass of the whole protocol, then a
+    timed one; the step rate is over the timed steps, the selection is reported beside it."""
+    from long_context_self_gb300 import binding as mb
+    from long_context_self_gb300.pipeline import SnapKVSpecLoop
+    prefill = torch.full((w.B,), w.L, dtype=torch.int32, device=device)
+    loop = SnapKVSpecLoop(k, v, prefill, w.H_q, w.gamma, w.snap_window, w.snap_pool, w.snap_budget, w.V,
+                          SPEC_LOOP_STEPS, layers)
+    q_win = synth.window_queries(w, device, heavy_dirs=heavy_dirs)
+    qd = [synth.queries(w, 1, device, seed=w.seed * 7 + 10 + g) for g in range(w.gamma)]
+    qv = synth.queries(w, w.n_q, device, seed=w.seed * 7 + 2)
+    target, draft, tok, u_acc, u_res = synth.logits(w, device)
+
+    def steps():
+        for _ in range(SPEC_LOOP_STEPS):
+            loop.step(qd, qv, target, draft, tok, u_acc, u_res)
+    loop.prefill(q_win)
+    steps()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record()
+    loop.prefill(q_win)
+    e1.record()
+    steps()
+    e2.record()
+    torch.cuda.synchronize()
+    sel_ms = e0.elapsed_time(e1)
+    steps_ms = max_over_ranks(e1.elapsed_time(e2), device)
+    # per-call component times at the loop's final state
+    vlen = loop.table[w.gamma + 1]
+    ver_ms = time_component(lambda: mb.magicdec_verify_attn(qv, k, v, vlen, out=loop.out_v, ws=loop.ws_attn), 5)
+    n_dra = w.gamma * layers
+    dra_ms = time_graph(lambda: [mb.magicdec_draft_attn(qd[0], loop.kc, loop.vc, loop.draft_len, out=loop.out_d[0],
+                                                        ws=loop.ws_attn) for _ in range(n_dra)], 3) / n_dra
+    acc_ms = time_component(lambda: mb.magicdec_spec_accept(target, draft, tok, u_acc, u_res, False,
+                                                            n_acc=loop.n_acc, out_tok=loop.out_tok,
+                                                            n_amb=loop.n_amb, ws=loop.ws_acc), 5)
+    row_b = w.H_kv * w.d * 2 * 2                                   # K and V bytes of one position, all KV heads
+    q_b = 2.0 * w.B * w.H_q * w.d * 2
+    ver_bytes = float(vlen.sum().item()) * row_b + 2.0 * w.B * w.n_q * w.H_q * w.d * 2
+    dra_bytes = float(loop.draft_len.sum().item()) * row_b + q_b
+    grown = (loop.len - w.L).cpu()
+    ver_gbs = ver_bytes / (ver_ms * 1e-3) / 1e9
+    dra_gbs = dra_bytes / (dra_ms * 1e-3) / 1e9
+    res = {"workload": w.name, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d, "gamma": w.gamma,
+           "V": w.V, "layers": layers,
+           "draft": f"SnapKV budget {w.snap_budget} (window {w.snap_window}, max-pool {w.snap_pool}), selected once",
+           "steps": SPEC_LOOP_STEPS,
+           "spec_steps_per_s": round(world * SPEC_LOOP_STEPS / (steps_ms * 1e-3), 4),
+           "ms_per_step": round(steps_ms / SPEC_LOOP_STEPS, 4),
+           "snapkv_select_gather_ms_per_layer": round(sel_ms, 4),
+           "verify_us_per_layer": round(ver_ms * 1e3, 2), "verify_gbs": round(ver_gbs, 1),
+           **{"verify_" + k2: v2 for k2, v2 in fractions(ver_gbs, peak).items()},
+           "draft_us_per_layer": round(dra_ms * 1e3, 2), "draft_gbs": round(dra_gbs, 1),
+           **{"draft_" + k2: v2 for k2, v2 in fractions(dra_gbs, peak).items()},
+           "accept_us": round(acc_ms * 1e3, 2),
+           "tokens_grown_per_sequence": {"min": int(grown.min()), "max": int(grown.max()),
+                                         "mean": round(float(grown.float().mean()), 2)},
+           "gpu_launches_per_step": loop.launches_per_step,
+           "device_error_word": mb.magicdec_device_error()}
+    del loop
+    torch.cuda.empty_cache()
+    return res
+
+
+def streaming_config_leg(w: synth.Workload, layers: int, steps: int, warmup: int, device, peak: float,
+                         world: int = 1) -> dict:
+    pipe = Pipeline(w, device, layers)
+    torch.cuda.synchronize()
+    ms_total, ver_ms, dra_ms, acc_ms, sel_ms = time_streaming_step(pipe, steps, warmup, world, device)
+    ver_gbs = pipe.verify_bytes() / (ver_ms * 1e-3) / 1e9
+    dra_gbs = pipe.draft_bytes() / (dra_ms * 1e-3) / 1e9
+    res = {"workload": w.name, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d, "gamma": w.gamma,
+           "V": w.V, "layers": layers, "draft": f"StreamingLLM {w.n_sink}+{w.n_recent} (selection + gather every step)",
+           "steps": steps, "spec_steps_per_s": round(aggregate_rate(world, steps, ms_total), 4),
+           "ms_per_step": round(ms_total / steps, 4),
+           "verify_us_per_layer": round(ver_ms * 1e3, 2), "verify_gbs": round(ver_gbs, 1),
+           **{"verify_" + k2: v2 for k2, v2 in fractions(ver_gbs, peak).items()},
+           "draft_us_per_layer": round(dra_ms * 1e3, 2), "draft_gbs": round(dra_gbs, 1),
+           **{"draft_" + k2: v2 for k2, v2 in fractions(dra_gbs, peak).items()},
+           "accept_us": round(acc_ms * 1e3, 2), "select_gather_us_per_layer": round(sel_ms * 1e3, 2),
+           "gpu_launches_per_step": pipe.launches_per_step}
+    del pipe
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     from long_context_self_gb300 import binding as mb
     from long_context_self_gb300 import build as lbuild
@@ -345,7 +499,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                             snap_window=w.snap_window, snap_pool=w.snap_pool, snap_budget=w.snap_budget,
                             seed=w.seed)
         q_win = synth.window_queries(sw, device)
-        ws_snap = torch.zeros(mb.magicdec_snapkv_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L),
+        ws_snap = torch.zeros(mb.magicdec_snapkv_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, pipe.L_cap),
                                                                  w.snap_window), dtype=torch.uint8, device=device)
         sidx = torch.empty((w.B, w.H_kv, w.snap_budget), dtype=torch.int32, device=device)
         sn = torch.empty((w.B,), dtype=torch.int32, device=device)
@@ -363,39 +517,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del q_win, ws_snap, sidx, sn, skc, svc
         torch.cuda.empty_cache()
 
-    for _ in range(args.warmup):
-        pipe.step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    stream = torch.cuda.current_stream(device)
     with ClockSampler(local_rank) as clocks:
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        t0.record(stream)
-        for _ in range(args.steps):
-            pipe.step(record=True)
-        t1.record(stream)
-        torch.cuda.synchronize()
-    ms_total = max_over_ranks(t0.elapsed_time(t1), device)
+        ms_total, ver_ms, dra_ms, acc_ms, sel_ms = time_streaming_step(pipe, args.steps, args.warmup, world, device)
     ms_step = ms_total / args.steps
-    ver_ms = statistics.mean(a.elapsed_time(b) for a, b in pipe.verify_events)
-    # draft launches are timed back to back outside the step (events between the
-    # step's kernels would serialise their programmatic-dependent launches): one
-    # step's gamma x layers calls replayed from a CUDA graph, so that the
-    # binding's host-side checks cannot set the pace of these ~50 us calls
-    n_dra = w.gamma * args.layers
-    dra_ms = time_graph(lambda: [mb.magicdec_draft_attn(pipe.q_draft, pipe.kc, pipe.vc, pipe.n_sel,
-                                                        out=pipe.out_d, ws=pipe.ws_attn) for _ in range(n_dra)],
-                        3) / n_dra
-    acc_ms = time_component(lambda: mb.magicdec_spec_accept(pipe.target, pipe.draft, pipe.tok, pipe.u_acc,
-                                                            pipe.u_res, False, n_acc=pipe.n_acc,
-                                                            out_tok=pipe.out_tok, n_amb=pipe.n_amb,
-                                                            ws=pipe.ws_acc), 5)
-    sel_ms = time_component(lambda: (mb.magicdec_streaming_select(pipe.seq_len, w.H_kv, w.n_sink, w.n_recent,
-                                                                  idx=pipe.idx, n_sel=pipe.n_sel),
-                                     mb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc,
-                                                           vc=pipe.vc)), 5)
+    peak, peak_kind = load_peaks()
     # PQCache-style draft at the same budget: codebook built once (2 Lloyd
     # iterations from seeded key samples, then the final encode), then the
     # per-draft-step search (LUT scores over the codes, select, exact attention)
@@ -408,7 +533,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         hidx = torch.arange(w.H_kv, device=device)[None, :, None]
         init = pipe.k[bidx, pick, hidx].float().reshape(w.B, w.H_kv, C, M, 8).permute(0, 1, 3, 2, 4).contiguous()
         cb = init.clone()
-        codes = torch.empty((w.B, w.H_kv, w.L, M), dtype=torch.uint8, device=device)
+        codes = torch.empty((w.B, w.H_kv, pipe.L_cap, M), dtype=torch.uint8, device=device)
 
         def pq_build():
             cb.copy_(init)
@@ -419,18 +544,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         build_ms = time_component(pq_build, 1)
         pq_idx = torch.empty((w.B, w.H_q, pipe.cap), dtype=torch.int32, device=device)
         pq_out = torch.empty_like(pipe.q_draft)
-        pq_ws = torch.empty(mb.magicdec_pq_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L)),
+        pq_ws = torch.empty(mb.magicdec_pq_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, pipe.L_cap)),
                             dtype=torch.uint8, device=device)
         pq_ms = time_component(lambda: mb.magicdec_pq_draft_attn(pipe.q_draft, pipe.k, pipe.v, pipe.seq_len, cb, codes,
                                                                  pipe.cap, out=pq_out, idx=pq_idx, ws=pq_ws), 5)
-        kv_bytes = float(w.B) * w.L * w.H_kv * w.d * 2
+        kv_bytes = float(w.B) * pipe.L_cap * w.H_kv * w.d * 2     # the encodes and updates cover every cache row
         pq = {"pq_draft_us_per_layer": round(pq_ms * 1e3, 2), "pq_build_ms_per_layer": round(build_ms, 3),
               "pq_M": M, "pq_C": C, "pq_lloyd_iterations": iters,
               "_pq_bytes": (float(w.B) * w.H_kv * w.L * M + float(w.B) * w.H_kv * M * C * 8 * 4
                             + 2.0 * w.B * w.H_q * pipe.cap * w.d * 2 + 2.0 * w.B * w.H_q * w.d * 2),
               "_pq_ms": pq_ms,
               # each encode and each update reads K once; codes written per encode
-              "_pq_build_bytes": (2 * iters + 1) * kv_bytes + (iters + 1) * float(w.B) * w.H_kv * w.L * M,
+              "_pq_build_bytes": (2 * iters + 1) * kv_bytes + (iters + 1) * float(w.B) * w.H_kv * pipe.L_cap * M,
               "_pq_build_ms": build_ms}
         del init, cb, codes, pq_idx, pq_out, pq_ws, pick
         torch.cuda.empty_cache()
@@ -459,7 +584,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if not args.no_topk:
         tk_idx = torch.empty((w.B, w.H_q, pipe.cap), dtype=torch.int32, device=device)
         tk_out = torch.empty_like(pipe.q_draft)
-        tk_ws = torch.empty(mb.magicdec_topk_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, w.L)),
+        tk_ws = torch.empty(mb.magicdec_topk_attn_workspace_size(mb.kv_shape(w.B, w.H_q, w.H_kv, w.d, pipe.L_cap)),
                             dtype=torch.uint8, device=device)
         tk_ms = time_component(lambda: mb.magicdec_topk_draft_attn(pipe.q_draft, pipe.k, pipe.v, pipe.seq_len,
                                                                    pipe.cap, out=tk_out, idx=tk_idx, ws=tk_ws), 5)
@@ -562,7 +687,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del g
     err_word = mb.magicdec_device_error()
 
-    peak, peak_kind = load_peaks()
+    # the same workload drafted by SnapKV (budget as the StreamingLLM draft's): selection
+    # once after prefill, then the multi-step loop with diverging lengths
+    snapkv_step = None
+    if w.snap_budget and not args.no_snapkv_step:
+        snapkv_step = snapkv_loop_leg(w, pipe.k, pipe.v, args.layers, device, peak, world=world)
+
     vbytes, dbytes = pipe.verify_bytes(), pipe.draft_bytes()
     ver_gbs = vbytes / (ver_ms * 1e-3) / 1e9
     dra_gbs = dbytes / (dra_ms * 1e-3) / 1e9
@@ -570,7 +700,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     def row(nbytes, ms, bound="hbm"):
         gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "us": round(ms * 1e3, 2),
+        return {"gbs": round(gbs, 1), **fractions(gbs, peak), "us": round(ms * 1e3, 2),
                 "algorithmic_bytes": nbytes, "bound": bound}
     sg_bytes = 2.0 * 2 * w.B * pipe.cap * w.H_kv * w.d * 2       # gather: read + write K and V rows
     rows = {"verify_attn": row(vbytes, ver_ms), "draft_attn": row(dbytes, dra_ms),
@@ -616,20 +746,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
-                   "gamma": w.gamma, "V": w.V, "layers": args.layers,
-                   "draft": f"StreamingLLM {w.n_sink}+{w.n_recent} (selection + gather every step)",
-                   "per_rank_batch": w.B, "parallelism": f"replicas x{world}",
-                   "rank_seeds": "workload seed + 100 x rank (distinct sequences per rank)",
-                   "l2": "inputs larger than L2 (KV cache 16.8 GB per layer vs 129 MB L2)",
-                   "step": "layers x (select, gather, gamma x draft_attn, verify_attn) + spec_accept"},
+        "config": config_dict(w, args.layers, world),
         "roofline": {"bound": "hbm", "kernel": "verify_heads_kernel", "achieved": round(ver_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(ver_gbs / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes": vbytes, "peak_source": peak_kind},
+                     "traffic": traffic, "algorithmic_bytes": vbytes, "peak_source": peak_kind,
+                     "peak_8tbs": NOMINAL_HBM_GBS, "frac_8tbs": round(ver_gbs / NOMINAL_HBM_GBS, 4)},
         "rows_roofline": rows,
         "verify_gbs": round(ver_gbs, 1), "verify_pct_peak": round(100 * ver_gbs / peak, 2),
+        "verify_pct_8tbs": round(100 * ver_gbs / NOMINAL_HBM_GBS, 2),
         "verify_ms_per_layer": round(ver_ms, 4),
         "draft_gbs": round(dra_gbs, 1), "draft_pct_peak": round(100 * dra_gbs / peak, 2),
+        "draft_pct_8tbs": round(100 * dra_gbs / NOMINAL_HBM_GBS, 2),
         "draft_us_per_layer": round(dra_ms * 1e3, 2),
         "accept_us": round(acc_ms * 1e3, 2),
         "accept_gbs": round(pipe.accept_bytes() / (acc_ms * 1e-3) / 1e9, 1),
@@ -646,11 +773,28 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "clocks": clocks.summary(),
     }
     result["ring_cache_step"] = ring_step
+    if snapkv_step:
+        result["snapkv_step"] = snapkv_step
     if graph:
         result["cuda_graph"] = graph
+    del pipe.kc, pipe.vc, pipe.rkc, pipe.rvc
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        del pipe.kc, pipe.vc
         result["cpu_baseline"] = cpu_baseline(w, args.layers, pipe)
+    if not args.no_configs:
+        # the other long-context configurations, one after another on the same GPU
+        pipe.k = pipe.v = None
+        torch.cuda.empty_cache()
+        cfgs = {"llama8b_b32_l32k": streaming_config_leg(rank_workload(synth.WORKLOADS["llama8b_b32_l32k"], rank),
+                                                         args.layers, args.steps, args.warmup, device, peak, world)}
+        for name in ("llama8b_b64_l32k_snapkv", "qwen32b_b16_l100k"):
+            wc = rank_workload(synth.WORKLOADS[name], rank)
+            kk, vv, dirs = synth.kv_cache(wc, device, L_cap=wc.L + SPEC_LOOP_STEPS * (wc.gamma + 1))
+            cfgs[name] = snapkv_loop_leg(wc, kk, vv, args.layers, device, peak, heavy_dirs=dirs, world=world)
+            del kk, vv, dirs
+            torch.cuda.empty_cache()
+        cfgs["qwen32b_b16_l100k"]["note"] = ("the pages give no layer count for this shape: the per-layer "
+                                             "figures are the measurement, the step rate assumes 32 layers")
+        result["per_config"] = cfgs
     return result
 
 
@@ -728,23 +872,29 @@ def run_reference(args, rank: int):
             "u_res": u_res.numpy()}
     for _ in range(args.warmup):
         oracle_step_sample(w, args.layers, host, nb_attn, nb_acc)
-    times, spent = [], 0.0
+    full, spent = [], []
     for _ in range(args.steps):
         per_step, _, s = oracle_step_sample(w, args.layers, host, nb_attn, nb_acc)
-        times.append(per_step)
-        spent += s
-    ms_step = 1e3 * statistics.mean(times)
-    value = 1e3 / ms_step
+        full.append(per_step)
+        spent.append(s)
+    # what was run and timed: args.steps samples; the rate is their scaling to one full step
+    ms_sample = 1e3 * statistics.mean(spent)
+    ms_full = 1e3 * statistics.mean(full)
+    value = 1e3 / ms_full
     sample = (f"per step: one step's calls on {nb_attn} of {w.B} sequences (attention, selection, gather; "
               f"{args.layers} layers from one layer's time) and {nb_acc} sequences (accept), scaled linearly "
               f"to B={w.B}")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "steps/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 2),
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_sample, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
-                       "gamma": w.gamma, "V": w.V, "layers": args.layers},
+            "config": config_dict(w, args.layers, args.gpus),
+            "extrapolated": {"sample": sample, "ms_per_sample": round(ms_sample, 4),
+                             "ms_per_full_step": round(ms_full, 4), "scale": round(ms_full / ms_sample, 3),
+                             "note": "steps and ms_per_step count the samples actually run; value is "
+                                     "1000 / ms_per_full_step"},
             "cpu_baseline": {"value": round(value, 8), "unit": "steps/s", "cores": oracle.num_threads(),
-                             "kind": "oracle", "sample": sample + f"; {spent:.1f} s of CPU time in total"},
+                             "kind": "oracle",
+                             "sample": sample + f"; {sum(spent):.1f} s of CPU time in total"},
             "e2e": {"value": round(value, 8), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -759,6 +909,9 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-topk", action="store_true", help="skip the Top-K attention draft row")
+    ap.add_argument("--no-snapkv-step", action="store_true", help="skip the SnapKV-drafted multi-step leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration legs (B=32 StreamingLLM, B=64 SnapKV, B=16 L=100000)")
     ap.add_argument("--no-pq", action="store_true", help="skip the PQCache-style draft rows")
     ap.add_argument("--graph", action="store_true", help="also time the step captured in a CUDA graph")
     ap.add_argument("--batch", type=int, default=0,

@@ -6,6 +6,8 @@ import os
 import subprocess
 import sys
 
+import bench
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -25,8 +27,13 @@ def test_reference_line_keeps_the_contract():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 1
     assert d["unit"] == "steps/s" and d["higher_is_better"] is True and d["value"] > 0
-    assert abs(d["ms_per_step"] - 1e3 / d["value"]) <= 1e-3 * d["ms_per_step"] + 0.01
-    assert d["config"]["workload"] == "tiny" and d["config"]["B"] == 2
+    # steps x ms_per_step is the time actually spent on samples; the rate is their stated scaling
+    ex = d["extrapolated"]
+    assert ex["ms_per_sample"] == d["ms_per_step"]
+    assert abs(ex["ms_per_full_step"] - 1e3 / d["value"]) <= 1e-3 * ex["ms_per_full_step"] + 0.01
+    assert abs(ex["scale"] - ex["ms_per_full_step"] / ex["ms_per_sample"]) <= 1e-2 * ex["scale"]
+    # the GPU arm's config dict
+    assert d["config"] == bench.config_dict(bench.synth.WORKLOADS["tiny"], 32, 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert "2 of 2 sequences" in cb["sample"]                 # the sample never exceeds the batch

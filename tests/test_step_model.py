@@ -39,12 +39,33 @@ def test_aggregate_rate_is_whole_job():
     assert math.isclose(bench.aggregate_rate(4, 10, 2000.0), 20.0)
 
 
-def test_recorded_traffic_is_read_from_the_committed_profile():
-    """The bench reports the verification kernel's ncu DRAM bytes from profiles/ while attn_heads.cu is
-    the source the capture was taken on; the recorded traffic equals the algorithmic bytes within 1 %."""
-    t = bench.recorded_traffic("llama8b_b128_l32k")
-    assert t is not None
+def test_recorded_traffic_follows_the_kernel_source(tmp_path):
+    """The bench reports the verification kernel's ncu DRAM bytes from a JSON record only while
+    the kernel's source is the one the capture was taken on; the committed record's traffic
+    equals the algorithmic bytes within 1 % (no re-reads)."""
+    import json
+    from long_context_self_gb300.ncu_record import source_sha16
+    rec = json.load(open(bench.TRAFFIC_RECORD))
     w = bench.synth.WORKLOADS["llama8b_b128_l32k"]
     algorithmic = 2.0 * w.B * w.L * w.H_kv * w.d * 2 + 2.0 * w.B * w.n_q * w.H_q * w.d * 2
-    assert abs(t / algorithmic - 1.0) < 0.01
-    assert bench.recorded_traffic("tiny") is None
+    assert rec["workload"] == "llama8b_b128_l32k"
+    assert abs(rec["dram_bytes_per_launch"] / algorithmic - 1.0) < 0.01
+    assert rec["dram_bytes_per_launch"] == rec["dram_bytes_per_captured_launch"] * rec["scale"]
+    current = dict(rec, source_sha16=source_sha16(os.path.join(bench.ROOT, rec["source"])))
+    path = tmp_path / "rec.json"
+    path.write_text(json.dumps(current))
+    assert bench.recorded_traffic("llama8b_b128_l32k", str(path)) == rec["dram_bytes_per_launch"]
+    assert bench.recorded_traffic("tiny", str(path)) is None
+    path.write_text(json.dumps(dict(current, source_sha16="0" * 16)))
+    assert bench.recorded_traffic("llama8b_b128_l32k", str(path)) is None
+
+
+def test_ncu_record_reads_raw_csv(tmp_path):
+    """ncu --page raw --csv: a header row, a units row, one row per launch."""
+    from long_context_self_gb300 import ncu_record
+    raw = tmp_path / "raw.csv"
+    raw.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
+                   '"","","Gbyte","Mbyte"\n'
+                   '"0","void magicdec::verify_heads_kernel(...)","4.20","7.00"\n'
+                   '"1","gather_kv_kernel","1.00","1.00"\n')
+    assert ncu_record.launch_traffic(str(raw), "verify_heads") == [4.20e9 + 7.00e6]
