@@ -4,19 +4,23 @@
 //
 // The step streams the target logits [B, gamma+1, V] and draft logits
 // [B, gamma, V] once (fp32, HBM-bound) and then touches one row pair per
-// sequence again for the resample.  Three launches:
-//   stats  per (row, 16K-logit chunk): chunk max, sum of exp(x - max) in
-//          double-float (an fp32 pair, ~48-bit significand), top-1 (smallest
-//          index among equals) and top-2 logits;
-//   chain  one thread per sequence: merge the chunk stats of its rows in
-//          fp64, evaluate p(x)/q(x) for each draft token in fp64, run the
-//          sequential accept chain (or the greedy argmax chain) and record the
-//          row to resample from;
-//   sample per (sequence, chunk): the chunk's sum of resample weights
-//          max(0, p - q) (or p for the bonus token), normalised in
-//          double-float; the last CTA of a sequence (atomic counter, no
-//          waiting) locates the chunk where the running sum crosses
-//          u * total and scans inside it in a fixed order.
+// sequence again for the resample.  Four launches (greedy mode: the first
+// two):
+//   stats  one CTA per (row, 4096 logits): for each of its four 1024-logit
+//          warp slices the max and sum of exp(x - max), merged into one
+//          record (double-float across lanes, fp64 across warps); greedy
+//          mode keeps top-1 (smallest index among equals), top-2 and argmax;
+//   chain  one CTA per sequence: a warp per row merges the row's records in
+//          fp64, warp 0 evaluates p(x)/q(x) for each draft token in fp64 and
+//          its thread 0 runs the sequential accept chain (or the greedy
+//          argmax chain) and records the row(s) to resample from;
+//   chunk  one CTA per (sequence, 4096-logit chunk) of the sampled row(s):
+//          the chunk's sum of resample weights max(0, p - q), or p for the
+//          bonus token, in reverse sequence order (the rows read last by the
+//          statistics pass are still in L2);
+//   draw   one CTA per sequence: finds the chunk where the running sum
+//          crosses u * total (shuffle scan + ballot) and walks it with
+//          double-float weights (fp64 block scan).
 // Only the per-logit exponentials are single precision (random ~1e-6 relative
 // errors that average out in the sums); normalisers, ratios and running sums
 // carry ~1e-12 relative error, so the drawn token agrees with an exact
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
             const int t = t0 + k2 * 128 + 4 * lane;
             float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             if (t < t1)
-                asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+                asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
                              : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
                              : "l"(x + t));
             v[4 * k2] = q.x; v[4 * k2 + 1] = q.y; v[4 * k2 + 2] = q.z; v[4 * k2 + 3] = q.w;
@@ -467,6 +471,29 @@ __device__ __forceinline__ void weight4_acc(dflt &acc, const WeightCtx &w, const
     acc_add(acc, weight_of(w, xt.w, xd.w, resid));
 }
 
+// Resample weight of one logit pair in fp32, for the chunk sums: each
+// normaliser's double-float reciprocal enters through one FMA, so the result
+// is the exact value rounded once or twice (unbiased, ~1e-7 relative: the
+// order of the exponential's own error); the sums are accumulated in
+// double-float.  The walk inside the chunk that holds the draw uses the
+// double-float weights above.
+__device__ __forceinline__ float weight_fast(const WeightCtx &w, float xt, float xd, bool resid) {
+    const float et = fast_exp2((xt - w.mt) * kLog2e);
+    const float pw = fmaf(et, w.inv_st.lo, et * w.inv_st.hi);
+    if (!resid) return pw;
+    const float ed = fast_exp2((xd - w.md) * kLog2e);
+    const float qw = fmaf(ed, w.inv_sd.lo, ed * w.inv_sd.hi);
+    return fmaxf(pw - qw, 0.f);
+}
+
+__device__ __forceinline__ void weight4_fast_acc(dflt &acc, const WeightCtx &w, const float4 xt, const float4 xd,
+                                                 bool resid) {
+    acc_add(acc, dflt{weight_fast(w, xt.x, xd.x, resid), 0.f});
+    acc_add(acc, dflt{weight_fast(w, xt.y, xd.y, resid), 0.f});
+    acc_add(acc, dflt{weight_fast(w, xt.z, xd.z, resid), 0.f});
+    acc_add(acc, dflt{weight_fast(w, xt.w, xd.w, resid), 0.f});
+}
+
 // Inclusive scan of one double per thread in thread order: shuffle scans in
 // each warp, a scan of the warp totals by warp 0, two barriers.
 __device__ double block_scan_warps(double v, double *wtot) {
@@ -561,12 +588,14 @@ __device__ __forceinline__ void batch_chunk_sums(const WeightCtx &w, bool resid,
 constexpr int kChkThreads = 256;
 constexpr int kChkPer = kSmpChunk / (4 * kChkThreads);   // float4 of each row per thread (4)
 
-// Weight sum of chunk blockIdx.x of sequence blockIdx.y into chunk_sum[b][c]
-// (kind 1: residual max(0, p - q); kind 2: p).  All loads of a thread are
-// issued before any arithmetic; the block sum is reduced in a fixed order.
+// Weight sum of chunk blockIdx.x of sequence B-1-blockIdx.y into
+// chunk_sum[b][c] (kind 1: residual max(0, p - q); kind 2: p), with the fp32
+// weights above.  Sequences go in reverse order: the statistics pass read the
+// last sequences' rows last, so those are still in L2.  All loads of a thread
+// are issued before any arithmetic; the block sum is reduced in a fixed order.
 __global__ void __launch_bounds__(kChkThreads) accept_chunk_kernel(const AcceptParams p) {
     __shared__ dflt wred[kChkThreads / 32];
-    const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, b = p.B - 1 - (int)blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
     pdl_wait();
     const JobInfo job = p.job[b];
@@ -607,7 +636,7 @@ __global__ void __launch_bounds__(kChkThreads) accept_chunk_kernel(const AcceptP
     }
     dflt acc = {0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < kChkPer; ++i) weight4_acc(acc, w, xt[i], xd[i], resid);
+    for (int i = 0; i < kChkPer; ++i) weight4_fast_acc(acc, w, xt[i], xd[i], resid);
     acc = warp_sum_df(acc_done(acc));
     if (lane == 0) wred[warp] = acc;
     __syncthreads();

@@ -173,8 +173,10 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // keep their place after pdl_wait(): the read-only-path intrinsic __ldg is
 // treated as a load of memory that never changes, and the compiler may issue
 // it ahead of the grid-dependency wait -- before the previous kernel's writes
-// exist.  Small values go through L2 (relaxed, device scope); streamed data
-// is cached in L2 only (.cg), so no L1 line from before the wait is reused.
+// exist.  Small values are relaxed device-scope loads; streamed data takes
+// the non-coherent path without allocating in L1 (.nc.L1::no_allocate), so no
+// L1 line can hold a copy from before the wait.  Data that other CTAs of the
+// same kernel write is read with plain loads instead.
 __device__ __forceinline__ int ld_dep(const int *p) {
     int v;
     asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -187,29 +189,33 @@ __device__ __forceinline__ unsigned char ld_dep_u8(const unsigned char *p) {
 }
 __device__ __forceinline__ float ld_dep_f(const float *p) {
     float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ float4 ld_dep_f4(const float4 *p) {
     float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p)
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
                  : "memory");
     return v;
 }
 __device__ __forceinline__ uint4 ld_dep_u4(const uint4 *p) {
     uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p)
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
                  : "memory");
     return v;
 }
 __device__ __forceinline__ uint2 ld_dep_u2(const uint2 *p) {
     uint2 v;
-    asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ unsigned ld_dep_u32(const unsigned *p) {
     unsigned v;
-    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 

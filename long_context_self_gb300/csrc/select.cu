@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *k, const ui
             val[r] = make_uint4(0, 0, 0, 0);
             if (dsto[r] >= 0 && so >= 0) {
                 const uint4 *src = (kv ? v : k) + so + ch;
-                asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                              : "=r"(val[r].x), "=r"(val[r].y), "=r"(val[r].z), "=r"(val[r].w)
                              : "l"(src));
             }
