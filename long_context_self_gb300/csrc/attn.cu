@@ -56,6 +56,7 @@ constexpr int kHalfBytes = kTileN * 128;   // one 64-row x 64-channel swizzled b
 constexpr int kMaxContrib = 512;           // contributors a merge lists in shared memory (CTAs + tail)
 constexpr int kTailMinTiles = 64;          // pairs of at least this many tiles have a dynamic tail
 constexpr int kTailDiv = 16;               // ... of n / kTailDiv tiles
+constexpr int kPrefetchTiles = 5;          // draft tiles per CTA prefetched into L2 before the dependency wait
 
 struct AttnParams {
     const __nv_bfloat16 *q;     // [B, n_q, H_q, D]
@@ -69,6 +70,7 @@ struct AttnParams {
     int *err;
     int B, H_q, H_kv, G, n_q, L_cap, M;
     int head_major;             // 0: verify layout [B, L_cap, H_kv, D]; 1: draft [B, H_kv, cap, D]
+    int prefetch;               // draft: tiles prefetched into L2 before the dependency wait (0: none)
     int stages;
     float scale_log2;           // log2(e) / sqrt(D)
 };
@@ -239,6 +241,31 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
         prefetch_tensormap(&tmq);
+        if (p.prefetch) {
+            // While the previous kernel drains (it may be writing this very
+            // cache: L2 keeps the prefetched lines coherent), start the first
+            // `prefetch` tiles of this CTA's range on their way into L2.  The
+            // range is the stream-K split computed as if every sequence had
+            // sequence 0's length (read before the wait, so possibly stale: a
+            // hint that only picks what to prefetch; the real schedule is
+            // computed after the wait).  The draft caches of a step usually
+            // have one length for the whole batch, and then the guess is exact.
+            const int n = tiles_of(clamp_len(ld_dep(p.len), p.L_cap));
+            if (n > 0) {
+                const long long T = (long long)p.B * p.H_kv * n;
+                const long long t0 = cta_start(blockIdx.x, T, gridDim.x);
+                const long long t1 = min(cta_start(blockIdx.x + 1, T, gridDim.x), t0 + p.prefetch);
+                for (long long t = t0; t < t1; ++t) {
+                    const long long pair = t / n;
+                    const int ti = (int)(t - pair * n), b = (int)(pair / p.H_kv), h = (int)(pair - (long long)b * p.H_kv);
+#pragma unroll
+                    for (int hf = 0; hf < HALVES; ++hf) {
+                        tma_prefetch_4d(&tmk, hf * 64, ti * kTileN, h, b);
+                        tma_prefetch_4d(&tmv, hf * 64, ti * kTileN, h, b);
+                    }
+                }
+            }
+        }
     }
     // Query rows past M stay zero in both slots (the TMA box writes rows < M only).
     for (int i = tid; i < 2 * QSLOT / 16; i += blockDim.x)
@@ -742,6 +769,7 @@ magicdec_status launch_decode_attn(int B, int H_q, int H_kv, int D, int L_cap, i
     prm.L_cap = L_cap;
     prm.M = prm.G * n_q;
     prm.head_major = head_major;
+    prm.prefetch = head_major ? env_int("MAGICDEC_ATTN_PREFETCH", kPrefetchTiles) : 0;
     prm.scale_log2 = kLog2e / sqrtf((float)D);
 
     // Verification of d = 128, eight KV heads and at most 16 query rows per KV

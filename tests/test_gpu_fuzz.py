@@ -1,6 +1,7 @@
-"""Randomised shapes and length mixes for the all-heads kernels (d = 128, eight KV
-heads): verification against the per-pair kernel and against itself across repeated
-calls, and the Top-K score pass against the per-pair score kernel.  Seeded; each case
+"""Randomised shapes and length mixes at d = 128 with eight KV heads: the all-heads
+verification kernel (up to 16 rows per KV head) against the per-pair kernel and against
+itself across repeated calls; the per-pair kernel's two-row-tile verification (17-32 rows)
+against the oracle; and the Top-K score pass against the per-pair score kernel.  Seeded; each case
 is small (a few MB), so the whole file runs in seconds."""
 import os
 
@@ -75,6 +76,46 @@ def test_verify_all_heads_fuzz(seed, monkeypatch):
     for i, L in enumerate(lens):
         if L == 0:
             assert torch.count_nonzero(a[i]) == 0
+
+
+def _case_two_tiles(seed):
+    """17 to 32 query rows per KV head (two 16-row tiles), the shapes of 4-5 speculated
+    tokens over 4-8 query heads per KV head."""
+    rng = np.random.default_rng(5000 + seed)
+    B = int(rng.integers(1, 10))
+    L_cap = int(rng.choice([8, 63, 200, 1000, 2500, 4100]))
+    G = int(rng.choice([1, 2, 4, 5, 8]))
+    n_q = int(rng.integers((17 + G - 1) // G, 32 // G + 1))
+    return rng, B, L_cap, G, n_q, _lengths(rng, B, L_cap)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_verify_two_row_tiles_fuzz(seed, monkeypatch):
+    """d = 128 with eight KV heads and 17-32 rows per KV head runs the per-pair kernel with
+    two row tiles: equal to the oracle, reproducible across calls and across schedules
+    (stage counts)."""
+    import oracle
+    from parity_util import to_u16
+    rng, B, L_cap, G, n_q, lens = _case_two_tiles(seed)
+    assert 17 <= G * n_q <= 32
+    H_kv, d = 8, 128
+    H_q = G * H_kv
+    g = torch.Generator().manual_seed(3000 + seed)
+    q = torch.randn((B, n_q, H_q, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    a = mb.magicdec_verify_attn(qd, kd, vd, sl)
+    b = mb.magicdec_verify_attn(qd, kd, vd, sl)
+    monkeypatch.setenv("MAGICDEC_ATTN_STAGES", str(int(rng.choice([2, 3]))))
+    c = mb.magicdec_verify_attn(qd, kd, vd, sl)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b), "verification is not reproducible"
+    ref = oracle.verify_attn(to_u16(q), to_u16(k), to_u16(v), np.array(lens, np.int32), n_q)
+    what = f"two row tiles, B={B} L={L_cap} G={G} n_q={n_q} lens={lens}"
+    check_attention(bf16_out_to_f64(a), ref, what)
+    check_attention(bf16_out_to_f64(c), ref, what + " (fewer stages)")
 
 
 @pytest.mark.parametrize("seed", range(12))

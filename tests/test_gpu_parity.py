@@ -55,6 +55,11 @@ VERIFY_CASES = [
     (4, 32, 8, 128, 64, 4, [64, 1, 0, 9]),                             # fewer tiles than CTAs
     (1, 32, 8, 128, 9000, 4, [9000]),                                  # one sequence over every CTA
     (2, 32, 8, 128, 3000, 1, [3000, 17]),                              # one query token
+    # ... and 17 to 32 rows per KV head: two row tiles, query fragments read from shared memory
+    (2, 64, 8, 128, 1000, 4, [1000, 333]),                             # G = 8: exactly 32 rows
+    (2, 8, 8, 128, 800, 17, [800, 17]),                                # G = 1, 17 rows (one in tile 2)
+    (5, 40, 8, 128, 3000, 5, [3000, 5, 0, 2999, 1]),                   # the Qwen-like shape, edge lengths
+    (1, 32, 8, 128, 9000, 5, [9000]),                                  # 20 rows, one sequence over every CTA
 ]
 
 
