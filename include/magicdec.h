@@ -75,8 +75,13 @@ MAGICDEC_API const char *magicdec_status_string(int status);
  * (synchronises the device).  Non-zero means a kernel gave up on a bounded
  * wait (value 1) or met an inconsistent internal state (value 2), and its
  * outputs are then undefined; or that magicdec_draft_cache_update skipped a
- * row whose slot was at or past the cache capacity (value 3).  The first
- * error since the last read is kept.  Returns MAGICDEC_OK or
+ * row whose slot was at or past the cache capacity (value 3).  In the
+ * range-checking build (libmagicdec_debug.so, compiled with
+ * MAGICDEC_DEBUG_CHECKS) value 4 means a kernel read a sequence length
+ * outside [0, capacity] or a gather index outside [0, L_cap) other than the
+ * -1 padding mark; that build still clamps or skips the value as documented
+ * for each call, so its outputs equal the release build's, which records
+ * nothing for it.  The first error since the last read is kept.  Returns MAGICDEC_OK or
  * MAGICDEC_ERR_CUDA. */
 MAGICDEC_API magicdec_status magicdec_device_error(int32_t *out);
 

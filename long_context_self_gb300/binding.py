@@ -17,7 +17,10 @@ from typing import Optional, Tuple
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmagicdec.so")
+# MAGICDEC_LIBRARY=debug loads the build whose kernels also record out-of-range
+# lengths and indices in the device error word (long_context_self_gb300.build --debug).
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                         "libmagicdec_debug.so" if os.environ.get("MAGICDEC_LIBRARY") == "debug" else "libmagicdec.so")
 _lib = None
 _lock = threading.Lock()
 

@@ -4,6 +4,12 @@ Each .cu under csrc/ compiles to an object in parallel; the objects link into
 ``long_context_self_gb300/libmagicdec.so`` with the CUDA runtime linked
 statically.  ``python -m long_context_self_gb300.build`` rebuilds when a source
 or header is newer than the library.
+
+``build(debug=True)`` (``--debug``) builds ``libmagicdec_debug.so`` from the
+same sources with ``-DMAGICDEC_DEBUG_CHECKS``: the kernels also record a
+length or index outside its range in the device error word (code 4) before
+clamping or skipping it as the release build does.  The binding loads it when
+``MAGICDEC_LIBRARY=debug``.
 """
 from __future__ import annotations
 
@@ -18,7 +24,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libmagicdec.so")
+OUT_DEBUG = os.path.join(PKG, "libmagicdec_debug.so")
 BUILD_DIR = os.path.join(PKG, "_build")
+BUILD_DIR_DEBUG = os.path.join(PKG, "_build_debug")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", os.path.join(ROOT, "include")]
@@ -40,22 +48,24 @@ def _deps():
                                                                    os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(OUT):
+def up_to_date(out: str = OUT) -> bool:
+    if not os.path.exists(out):
         return False
-    t = os.path.getmtime(OUT)
+    t = os.path.getmtime(out)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and up_to_date():
-        return OUT
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, debug: bool = False) -> str:
+    out = OUT_DEBUG if debug else OUT
+    if not force and up_to_date(out):
+        return out
+    bdir = BUILD_DIR_DEBUG if debug else BUILD_DIR
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_v else []
+    extra = (["-Xptxas", "-v"] if ptxas_v else []) + (["-DMAGICDEC_DEBUG_CHECKS"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,15 +78,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
         for obj, log in results:
             if log.strip():
                 print(f"--- {os.path.basename(obj)}\n{log}", file=sys.stderr)
-    tmp = OUT + f".{os.getpid()}.tmp"
+    tmp = out + f".{os.getpid()}.tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_v="--ptxas-v" in sys.argv)
-    print(OUT)
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="--ptxas-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -275,7 +275,7 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     // Head tiles per sequence (all tiles less the dynamic tail), loaded in
     // parallel, then an exclusive scan by warp 0.
     for (int b = tid; b < p.B; b += blockDim.x) {
-        const int n = tiles_of(clamp_len(ld_dep(p.len + b), p.L_cap));
+        const int n = tiles_of(clamp_len(checked(ld_dep(p.len + b), 0, p.L_cap, p.err), p.L_cap));
         prefix[b] = n - tail_tiles(n, p.tails);
     }
     __syncthreads();

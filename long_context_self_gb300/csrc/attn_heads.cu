@@ -114,7 +114,8 @@ __global__ void __launch_bounds__((kHdHeads + 1) * 32, 1)
     }
     pdl_wait();
     // 8-position tiles per sequence, loaded in parallel, then an exclusive scan by warp 0.
-    for (int b = tid; b < p.B; b += blockDim.x) prefix[b] = (hd_clamp(ld_dep(p.len + b), p.L_cap) + kHdPos - 1) / kHdPos;
+    for (int b = tid; b < p.B; b += blockDim.x)
+        prefix[b] = (hd_clamp(checked(ld_dep(p.len + b), 0, p.L_cap, p.err), p.L_cap) + kHdPos - 1) / kHdPos;
     __syncthreads();
     if (warp == 0) {
         int run = 0;

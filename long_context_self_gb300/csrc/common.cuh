@@ -18,10 +18,13 @@ namespace magicdec {
 
 // Device error word codes (the word itself lives in api.cu; kernels get its
 // address): 1 = a bounded wait gave up, 2 = inconsistent internal state,
-// 3 = a draft-cache copy needed a slot at or past the cache capacity.
+// 3 = a draft-cache copy needed a slot at or past the cache capacity,
+// 4 = (debug build only) a length or index outside the range the kernel
+// clamps or skips it to.
 constexpr int kErrTimeout = 1;
 constexpr int kErrState = 2;
 constexpr int kErrCapacity = 3;
+constexpr int kErrRange = 4;
 
 // Fixed-size counter regions at the start of the caller's workspaces: the
 // attention kernels keep one counter per (sequence, KV head) pair, the
@@ -48,6 +51,21 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 __device__ __forceinline__ void raise_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
+}
+
+// A length or index as loaded, checked against [lo, hi] in the debug build
+// (built with -DMAGICDEC_DEBUG_CHECKS): outside it, the device error word
+// records kErrRange.  Either build then clamps or skips the value exactly as
+// before -- the check never traps and never changes a result.
+__device__ __forceinline__ int checked(int v, int lo, int hi, int *err) {
+#ifdef MAGICDEC_DEBUG_CHECKS
+    if (v < lo || v > hi) raise_error(err, kErrRange);
+#else
+    (void)lo;
+    (void)hi;
+    (void)err;
+#endif
+    return v;
 }
 
 // ---------------------------------------------------------------- mbarrier

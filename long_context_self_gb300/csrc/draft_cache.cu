@@ -44,9 +44,9 @@ struct DcRanges {
 
 __device__ __forceinline__ DcRanges dc_ranges(const DcParams &p, int b) {
     DcRanges r;
-    const int lo = dc_clamp(ld_dep(p.len_old + b), p.L_cap);
-    const int ln = dc_clamp(ld_dep(p.len_new + b), p.L_cap);
-    const int lv = min(dc_clamp(ld_dep(p.len_valid + b), p.L_cap), min(lo, ln));
+    const int lo = dc_clamp(checked(ld_dep(p.len_old + b), 0, p.L_cap, p.err), p.L_cap);
+    const int ln = dc_clamp(checked(ld_dep(p.len_new + b), 0, p.L_cap, p.err), p.L_cap);
+    const int lv = min(dc_clamp(checked(ld_dep(p.len_valid + b), 0, p.L_cap, p.err), p.L_cap), min(lo, ln));
     const int o = max(0, ld_dep(p.origin + b));
     r.o = o;
     if (p.ring > 0) {

@@ -42,6 +42,7 @@ struct PqScoreParams {
     const uint8_t *codes;      // [B, H_kv, L_cap, M]
     const int32_t *len;
     float *score;              // [B, H_q, L_sc]
+    int *err;
     int B, H_q, H_kv, G, L_cap, L_sc, C;
     float scale;
 };
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     pdl_trigger();
     pdl_wait();
     for (int b = tid; b < p.B; b += kPqScThreads)
-        prefix[b] = (pq_clamp(ld_dep(p.len + b), p.L_cap) + kPqScTile - 1) / kPqScTile;
+        prefix[b] = (pq_clamp(checked(ld_dep(p.len + b), 0, p.L_cap, p.err), p.L_cap) + kPqScTile - 1) / kPqScTile;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -605,6 +606,7 @@ magicdec_status launch_pq_draft_attn(int B, int H_q, int H_kv, int D, int L_cap,
     p.L_sc = (L_cap + 3) & ~3;
     p.C = C;
     p.scale = 1.0f / sqrtf((float)D);
+    p.err = magicdec_host::device_error_word();
     const size_t smem = (size_t)M * C * G * 4 + (size_t)G * D * 4 + (size_t)(B + 1) * 4;
     if (smem > (size_t)magicdec_host::max_smem_optin()) return MAGICDEC_ERR_UNSUPPORTED;
     auto kern = D == 128 ? pq_scores_kernel<128> : pq_scores_kernel<64>;

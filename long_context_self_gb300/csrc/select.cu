@@ -51,7 +51,7 @@ template <int CPR, int RPI>
 __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *k, const uint4 *v,
                                                        const int32_t *idx, int H_kv, int L_cap,
                                                        int n_idx, int cap, int rows, uint4 *__restrict__ kc,
-                                                       uint4 *__restrict__ vc) {
+                                                       uint4 *__restrict__ vc, int *err) {
     constexpr int LPR = 2 * CPR;                 // lanes per row (K and V)
     constexpr int SLOTS = 32 / LPR;              // rows side by side in a warp
     constexpr int RPW = SLOTS * RPI;             // rows per warp per iteration
@@ -72,7 +72,10 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *k, const ui
                 const int bh = (int)(row / n_idx);
                 const int i = (int)(row - (long long)bh * n_idx);
                 const int h = bh % H_kv, b = bh / H_kv;
+                // -1 marks padding; any other index outside [0, L_cap) is a
+                // caller error, gathered as a zero row (recorded in the debug build)
                 const int pos = ld_dep(idx + row);
+                if (pos != -1) checked(pos, 0, L_cap - 1, err);
                 dst_off = ((long long)bh * cap + i) * CPR;
                 if (pos >= 0 && pos < L_cap) src_off = (((long long)b * L_cap + pos) * H_kv + h) * CPR;
             }
@@ -156,9 +159,10 @@ magicdec_status launch_gather_kv(int B, int H_kv, int D, int L_cap, const void *
     uint4 *kc4 = static_cast<uint4 *>(kc), *vc4 = static_cast<uint4 *>(vc);
     if (D == 128)
         return magicdec_host::launch_pdl(gather_kv_kernel<16, 8>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx,
-                                         H_kv, L_cap, n_idx, cap, (int)rows, kc4, vc4);
+                                         H_kv, L_cap, n_idx, cap, (int)rows, kc4, vc4,
+                                         magicdec_host::device_error_word());
     return magicdec_host::launch_pdl(gather_kv_kernel<8, 4>, dim3(blocks), dim3(threads), 0, st, k4, v4, idx, H_kv,
-                                     L_cap, n_idx, cap, (int)rows, kc4, vc4);
+                                     L_cap, n_idx, cap, (int)rows, kc4, vc4, magicdec_host::device_error_word());
 }
 
 size_t snapkv_tc_workspace_bytes(int B, int H_q, int H_kv, int L_cap, int w);

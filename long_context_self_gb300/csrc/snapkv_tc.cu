@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
     pdl_wait();
-    const int L = clamp_len_tc(ld_dep(p.len + b), p.L_cap);
+    const int L = clamp_len_tc(checked(ld_dep(p.len + b), 0, p.L_cap, p.err), p.L_cap);
     if (L < p.w) return;
     const int end = PASS == 1 ? L : L - p.w;
     const int pos_begin = chunk * kTcChunk;

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__((kTkConsumers + 1) * 32, 2)
     }
     pdl_wait();
     for (int b = tid; b < p.B; b += blockDim.x)
-        prefix[b] = (tk_clamp_len(ld_dep(p.len + b), p.L_cap) + kTkTileN - 1) / kTkTileN;
+        prefix[b] = (tk_clamp_len(checked(ld_dep(p.len + b), 0, p.L_cap, p.err), p.L_cap) + kTkTileN - 1) / kTkTileN;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__((kTkHdHeads + 1) * 32, 2)
     }
     pdl_wait();
     for (int b = tid; b < p.B; b += blockDim.x)
-        prefix[b] = (tk_clamp_len(ld_dep(p.len + b), p.L_cap) + kTkHdPos - 1) / kTkHdPos;
+        prefix[b] = (tk_clamp_len(checked(ld_dep(p.len + b), 0, p.L_cap, p.err), p.L_cap) + kTkHdPos - 1) / kTkHdPos;
     __syncthreads();
     if (warp == 0) {
         int run = 0;
