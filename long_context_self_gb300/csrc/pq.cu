@@ -21,7 +21,9 @@
 //                     (sequence, KV head); each (sequence, head) builds the
 //                     lookup table LUT[m][c][g] = scale * q_g,m . c_m,c for
 //                     its G query heads once, then a position's approximate
-//                     score for head g is sum_m LUT[m][code_m][g].
+//                     score for head g is sum_m LUT[m][code_m][g].  With G = 4
+//                     the table is laid out so that the lookups of a warp
+//                     meet no shared-memory bank conflicts whatever the codes.
 // Selection and exact attention over the kept positions run in the Top-K
 // select kernel (topk.cu) in its exact-score mode.
 #include "common.cuh"
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     constexpr int M = D / kPqDs;
     extern __shared__ __align__(16) float pq_sm[];
     const int G = p.G, C = p.C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float *lut = pq_sm;                                   // [M][C][G]
+    float *lut = pq_sm;                                   // [C][M][4] when G == 4, else [M][C][G]
     float *qs = lut + (size_t)M * C * G;                  // [G][D]
     int *prefix = reinterpret_cast<int *>(qs + (size_t)G * D);   // [B + 1]
     pdl_trigger();
@@ -301,7 +303,11 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
                 for (int u = 0; u < BATCH; ++u) {
                     const int mc = mc0 + u * kPqScThreads;
                     if (mc >= M * C) continue;
-                    const int m = mc / C;
+                    const int m = mc / C, cc = mc - m * C;
+                    // G == 4: entry (c, m) at [c][m][4], so the 16-byte entries of
+                    // the M subspaces of one centroid index fill consecutive bank
+                    // quads (see the lookups below); otherwise [m][c][G]
+                    const size_t at = G == 4 ? ((size_t)cc * M + m) * 4 : (size_t)mc * G;
                     for (int g = 0; g < G; ++g) {
                         const float *qq = qs + g * D + m * kPqDs;
                         float sdot = qq[0] * c0[u].x;
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
                         sdot = fmaf(qq[5], c1[u].y, sdot);
                         sdot = fmaf(qq[6], c1[u].z, sdot);
                         sdot = fmaf(qq[7], c1[u].w, sdot);
-                        lut[(size_t)mc * G + g] = sdot * p.scale;
+                        lut[at + g] = sdot * p.scale;
                     }
                 }
             }
@@ -328,12 +334,40 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
             const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
             float *srow = srow0 + j;
             if (G == 4) {
+                // A 16-byte lookup is served a quarter-warp (8 lanes) at a time,
+                // one wavefront per bank quad touched.  Entry (c, m) lies in bank
+                // quad m % 8 whatever c is, and lane l takes the subspaces in the
+                // order m = (r + l) mod M (r = 0 .. M-1, l = the position's lane),
+                // so the 8 lanes of a quarter-warp always touch 8 different quads:
+                // 4 wavefronts per warp-wide lookup instead of about 11 for
+                // arbitrary codes.  The codes are rotated once so that step r
+                // reads byte r of the rotated vector.
+                const int rot = lane & (M - 1);
+                uint32_t x0 = w[0], x1 = w[1], x2 = w[2], x3 = w[3];
+                uint32_t v[4];
+                if (M == 16) {
+                    const int sw = rot >> 2;
+                    if (sw & 1) { const uint32_t tt = x0; x0 = x1; x1 = x2; x2 = x3; x3 = tt; }
+                    if (sw & 2) { const uint32_t t0 = x0, t1 = x1; x0 = x2; x1 = x3; x2 = t0; x3 = t1; }
+                    const int sh = (rot & 3) * 8;
+                    v[0] = __funnelshift_r(x0, x1, sh);
+                    v[1] = __funnelshift_r(x1, x2, sh);
+                    v[2] = __funnelshift_r(x2, x3, sh);
+                    v[3] = __funnelshift_r(x3, x0, sh);
+                } else {                                     // M == 8: codes in w[0], w[1]
+                    if (rot >> 2) { const uint32_t tt = x0; x0 = x1; x1 = tt; }
+                    const int sh = (rot & 3) * 8;
+                    v[0] = __funnelshift_r(x0, x1, sh);
+                    v[1] = __funnelshift_r(x1, x0, sh);
+                    v[2] = v[3] = 0u;
+                }
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    int c = (int)((w[m >> 2] >> (8 * (m & 3))) & 255u);
+                for (int r = 0; r < M; ++r) {
+                    const int m = (r + rot) & (M - 1);
+                    int c = (int)((v[r >> 2] >> (8 * (r & 3))) & 255u);
                     c = c < C ? c : 0;
-                    const float4 l = *reinterpret_cast<const float4 *>(lut + ((size_t)m * C + c) * 4);
+                    const float4 l = *reinterpret_cast<const float4 *>(lut + ((size_t)c * M + m) * 4);
                     acc.x += l.x; acc.y += l.y; acc.z += l.z; acc.w += l.w;
                 }
                 srow[0] = acc.x;
