@@ -535,7 +535,6 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     int *cand_pos = hist + kTkBins;                                   // [cand_cap]
     uint32_t *cand_key = reinterpret_cast<uint32_t *>(cand_pos + p.cand_cap);   // [cand_cap]
     int *sel = reinterpret_cast<int *>(cand_key + p.cand_cap);        // [top_k]
-    float *ex = reinterpret_cast<float *>(sel + ((p.top_k + 3) & ~3)); // [top_k] exact scores (EXACT)
     // (in kSelOnly mode p.top_k is the budget, an upper bound of the kept count)
     __shared__ int wsum[32], woff[NW], wcnt[NW];
     __shared__ float s_exmax[NW];
@@ -736,10 +735,12 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
     constexpr int LPR = D / 8;
     constexpr int RPI = 32 / LPR;
     const int sub = lane % LPR, part = lane / LPR;
-    float m_log2 = tk_unkey(s_maxkey) * kLog2e;
     if (EXACT) {
-        // exact scaled scores of the kept rows: lane `sub` of a row group dots
-        // channels sub*8 .. +7 of q and the K row, the group's lanes sum
+        // exact scaled scores of the kept rows, and in the same pass the
+        // softmax-weighted sum of their V rows: lane `sub` of a row group dots
+        // channels sub*8 .. +7 of q and the K row (the group's lanes sum), then
+        // folds the row into its running (max, sum, output) with the online
+        // rule; the row groups merge with the log-sum-exp rule at the end
         float qv[8];
         {
             const uint4 qq = ld_dep_u4(reinterpret_cast<const uint4 *>(p.q + row * D + sub * 8));
@@ -751,46 +752,89 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
                 qv[2 * c + 1] = f.y;
             }
         }
-        const __nv_bfloat16 *kb = p.k + ((long long)b * p.L_cap * p.H_kv + kvh) * D + sub * 8;
-        const long long kstride = (long long)p.H_kv * D;
-        float mx = -INFINITY;
-        constexpr int UK = 2;
-        for (int t0 = 0; warp + NW * RPI * t0 < n; t0 += UK) {
-            uint4 raw[UK];
+        const long long base = ((long long)b * p.L_cap * p.H_kv + kvh) * D + sub * 8;
+        const __nv_bfloat16 *kb = p.k + base, *vb = p.v + base;
+        const long long kvstride = (long long)p.H_kv * D;
+        const float sl = p.scale * kLog2e;
+        float acc[8];
 #pragma unroll
-            for (int u = 0; u < UK; ++u) {
-                const int i = warp + NW * (RPI * (t0 + u) + part);
-                raw[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < n) raw[u] = ld_dep_u4(reinterpret_cast<const uint4 *>(kb + (long long)sel[i] * kstride));
+        for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+        float z = 0.f, mr = -INFINITY;                       // running max in log2 units
+        for (int t = 0; warp + NW * RPI * t < n; ++t) {
+            const int i = warp + NW * (RPI * t + part);
+            uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
+            if (i < n) {
+                const long long off = (long long)sel[i] * kvstride;
+                kr = ld_dep_u4(reinterpret_cast<const uint4 *>(kb + off));
+                vr = ld_dep_u4(reinterpret_cast<const uint4 *>(vb + off));
+            }
+            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            float dot = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kw[c]));
+                dot = fmaf(qv[2 * c], f.x, dot);
+                dot = fmaf(qv[2 * c + 1], f.y, dot);
             }
 #pragma unroll
-            for (int u = 0; u < UK; ++u) {
-                const int i = warp + NW * (RPI * (t0 + u) + part);
-                const uint32_t w4[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-                float dot = 0.f;
+            for (int o2 = LPR / 2; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o2);
+            if (i < n) {
+                const float s2 = dot * sl, mn = fmaxf(mr, s2);
+                const float al = fast_exp2(mr - mn), wgt = fast_exp2(s2 - mn);
+                z = fmaf(z, al, wgt);
+                const uint32_t vw[4] = {vr.x, vr.y, vr.z, vr.w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[c]));
-                    dot = fmaf(qv[2 * c], f.x, dot);
-                    dot = fmaf(qv[2 * c + 1], f.y, dot);
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vw[c]));
+                    acc[2 * c] = fmaf(wgt, f.x, acc[2 * c] * al);
+                    acc[2 * c + 1] = fmaf(wgt, f.y, acc[2 * c + 1] * al);
                 }
-#pragma unroll
-                for (int o2 = LPR / 2; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o2);
-                if (i < n) {
-                    const float sc = dot * p.scale;
-                    mx = fmaxf(mx, sc);
-                    if (sub == 0) ex[i] = sc;
-                }
+                mr = mn;
             }
         }
-        mx = warp_max(mx);
-        if (lane == 0) s_exmax[warp] = mx;
-        __syncthreads();
-        float m = s_exmax[0];
+        // merge the row groups of the warp, then the warps
 #pragma unroll
-        for (int w = 1; w < NW; ++w) m = fmaxf(m, s_exmax[w]);
-        m_log2 = m * kLog2e;
+        for (int o2 = LPR; o2 < 32; o2 <<= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, mr, o2), zo = __shfl_xor_sync(0xffffffffu, z, o2);
+            const float mn = fmaxf(mr, mo), mu = mn == -INFINITY ? 0.f : mn;
+            const float fa = fast_exp2(mr - mu), fb = fast_exp2(mo - mu);
+            z = z * fa + zo * fb;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float ao = __shfl_xor_sync(0xffffffffu, acc[c], o2);
+                acc[c] = acc[c] * fa + ao * fb;
+            }
+            mr = mn;
+        }
+        float *red = reinterpret_cast<float *>(hist);   // [NW][D]; the histogram is no longer read
+        if (part == 0) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) red[warp * D + sub * 8 + c] = acc[c];
+        }
+        if (lane == 0) {
+            zsum[warp] = z;
+            s_exmax[warp] = mr;
+        }
+        __syncthreads();
+        if (tid < D) {
+            float mm = s_exmax[0];
+#pragma unroll
+            for (int w = 1; w < NW; ++w) mm = fmaxf(mm, s_exmax[w]);
+            float sacc = 0.f, zz = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float f = fast_exp2(s_exmax[w] - mm);   // a warp without rows: exp2(-inf) = 0
+                sacc = fmaf(red[w * D + tid], f, sacc);
+                zz = fmaf(zsum[w], f, zz);
+            }
+            o[tid] = __float2bfloat16(sacc / zz);
+        }
+        if (idx_row)
+            for (int i = tid; i < p.top_k; i += kTkNT) idx_row[i] = i < n ? sel[i] : -1;
+        return;
     }
+    // Top-K: the selection scores are the exact scaled scores, the largest key's is the maximum
+    const float m_log2 = tk_unkey(s_maxkey) * kLog2e;
     float acc[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[c] = 0.f;
@@ -808,7 +852,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
             raw[u] = make_uint4(0u, 0u, 0u, 0u);
             if (i < n) {
                 const int j = sel[i];
-                sc[u] = EXACT ? ex[i] : ld_dep_f(srow + j);
+                sc[u] = ld_dep_f(srow + j);
                 raw[u] = ld_dep_u4(reinterpret_cast<const uint4 *>(vb + (long long)j * vstride));
             }
         }
@@ -865,7 +909,7 @@ static magicdec_status launch_select_attn(TopkSelParams tp, int mode, cudaStream
     const int smem_cap = magicdec_host::max_smem_optin();
     tp.cand_cap = tp.top_k + 4096;
     const size_t k4 = (size_t)((tp.top_k + 3) & ~3) * 4;
-    const size_t smem2 = (size_t)kTkBins * 4 + (size_t)tp.cand_cap * 8 + k4 + (mode == kSelExact ? k4 : 0);
+    const size_t smem2 = (size_t)kTkBins * 4 + (size_t)tp.cand_cap * 8 + k4;
     if (smem2 + 2048 > (size_t)smem_cap) return MAGICDEC_ERR_UNSUPPORTED;
     auto k2 = mode == kSelExact  ? topk_select_attn_kernel<D, kSelExact>
               : mode == kSelOnly ? topk_select_attn_kernel<D, kSelOnly>
