@@ -166,6 +166,13 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *tm, int c0, i
                  : "memory");
 }
 
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into L2
+// without waiting for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }

@@ -17,15 +17,18 @@
 //                            stores the fp32 scores [B, H_q, L_sc].
 //   topk_select_attn_kernel  one CTA per (sequence, query head): radix select of
 //                            the top_k scores on the order-preserving 32-bit key
-//                            (12 + 12 + 8 bit digits).  The first digit is
-//                            histogrammed from the only DRAM read of the row;
-//                            one L2 re-read collects the positions at or above
-//                            the threshold bin, in ascending order, into a
-//                            short shared-memory list, on which the last two
-//                            digits and the ordered selection run (the whole
-//                            row is searched when the list overflows).  Then the
-//                            softmax over the kept scores and the weighted sum
-//                            of the kept V rows.
+//                            (12 + 12 + 8 bit digits).  A long row takes a low
+//                            enough threshold bin from a 2048-key sample and
+//                            reads the row once (prefetched to L2), collecting
+//                            the positions at or above that bin, in ascending
+//                            order, into a short shared-memory list; the exact
+//                            first digit, the last two digits and the ordered
+//                            selection run on that list.  A shorter row, or one
+//                            where the sample leaves too few candidates or too
+//                            many, histograms the whole row first (the whole
+//                            row is searched when the list overflows).  Then
+//                            the softmax over the kept scores and the weighted
+//                            sum of the kept V rows.
 #include "common.cuh"
 
 namespace magicdec {
@@ -39,6 +42,7 @@ constexpr int kTkNW = kTkNT / 32;
 constexpr int kTkBins = 4096;
 constexpr int kTkMaxTopK = 8192;
 constexpr int kTkMaxGroup = 8;                   // query heads per KV head (the mma N extent)
+constexpr int kTkSampleMinLen = 8192;            // rows at least this long (and >= 8 top_k) sample the first digit
 constexpr int kSelScores = 0, kSelExact = 1, kSelOnly = 2;   // modes of the select kernel
 
 struct TopkScoreParams {
@@ -576,43 +580,85 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
         return;
     }
     const bool select = len > top_k;
+    if (select && tid == 0 && (reinterpret_cast<uintptr_t>(srow) & 15) == 0) {
+        // the two passes below read the row with a few loads in flight per lane:
+        // start the whole row towards L2 now so that they wait on L2, not DRAM
+        const uint32_t bytes = (uint32_t)((len + 3) & ~3) * 4u;
+        for (uint32_t o = 0; o < bytes; o += 16384u)
+            bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(srow) + o, min(16384u, bytes - o));
+    }
     // warp w owns positions [lo, hi): contiguous segments keep the ascending order
     const int seg = (((len + NW - 1) / NW) + 3) & ~3;
     const int lo = min(len, warp * seg), hi = min(len, lo + seg);
 
-    // 1. first-digit histogram and the largest key (the scores' only DRAM read)
+    // 1. first-digit histogram and the largest key.  A long row samples it: one
+    //    128-key block per warp at evenly spaced positions (2048 keys) gives the
+    //    lowest bin d_lo that still holds about 1.25 top_k (+16) of the row's
+    //    keys at or above it, and the exact first digit is then taken over the
+    //    candidates (every key of the top_k lies at or above d_lo whenever at
+    //    least top_k candidates are found).  A row where that leaves fewer than
+    //    top_k candidates, or more than a warp's slots, counts the whole row and
+    //    runs the whole-row search.  Shorter rows count the whole row directly.
+    const bool sampled = select && len >= kTkSampleMinLen && len >= 8 * top_k;
+    auto count_row = [&](bool count) {   // whole-row histogram (when `count`) and the largest key
+        uint32_t mk = 0u;
+        for (int base = lo; base < hi; base += 4 * 128) {
+            uint32_t kk[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tk_load4(srow, base + 128 * u + 4 * lane, hi, kk[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (kk[u][e] == 0u) continue;
+                    mk = max(mk, kk[u][e]);
+                    if (count) atomicAdd(&hist[kk[u][e] >> 20], 1);
+                }
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o2));
+        if (lane == 0) atomicMax(&s_maxkey, mk);
+        __syncthreads();
+    };
     for (int i = tid; i < kTkBins; i += kTkNT) hist[i] = 0;
-    if (tid == 0) s_maxkey = 0u;
-    __syncthreads();
-    uint32_t mk = 0u;
-    for (int base = lo; base < hi; base += 4 * 128) {
-        uint32_t kk[4][4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) tk_load4(srow, base + 128 * u + 4 * lane, hi, kk[u]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (kk[u][e] == 0u) continue;
-                mk = max(mk, kk[u][e]);
-                if (select) atomicAdd(&hist[kk[u][e] >> 20], 1);
-            }
+    if (tid == 0) {
+        s_maxkey = 0u;
+        s_digit = 0;   // a search for more keys than were counted leaves these
+        s_rem = 0;
     }
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o2));
-    if (lane == 0) atomicMax(&s_maxkey, mk);
     __syncthreads();
+    int d_lo = 0;
+    if (sampled) {
+        const int sb = (int)((long long)len * warp / NW) & ~3;   // sb + 128 <= len
+        uint32_t kk[4];
+        tk_load4(srow, sb + 4 * lane, sb + 128, kk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (kk[e] != 0u) atomicAdd(&hist[kk[e] >> 20], 1);
+        __syncthreads();
+        constexpr int S = NW * 128;
+        const int r_s = min(S, (int)((5LL * top_k * S) / (4LL * len)) + 16);
+        int r_left;
+        tk_find_digit(hist, r_s, wsum, &s_digit, &s_rem, d_lo, r_left);
+    } else {
+        count_row(select);
+    }
 
     if (select) {
-        int d1, rem1;
-        tk_find_digit(hist, top_k, wsum, &s_digit, &s_rem, d1, rem1);
-        // 2. candidates = positions whose first digit is >= d1.  One L2 re-read;
-        //    warp w appends its segment's candidates, in ascending order, to its
-        //    own R slots of the list.
+        int d1 = 0, rem1 = 0;
+        if (!sampled) {
+            tk_find_digit(hist, top_k, wsum, &s_digit, &s_rem, d1, rem1);
+            d_lo = d1;
+        }
+        // 2. candidates = positions whose first digit is >= d_lo.  One pass over
+        //    the row; warp w appends its segment's candidates, in ascending order,
+        //    to its own R slots of the list (a sampled row also takes the largest
+        //    key here: it is always a candidate).
         const int R = p.cand_cap / NW;
         int *my_pos = cand_pos + warp * R;
         uint32_t *my_key = cand_key + warp * R;
         int cnt = 0;
+        uint32_t mk = 0u;
         for (int base = lo; base < hi; base += 4 * 128) {
             uint32_t kk[4][4];
 #pragma unroll
@@ -621,7 +667,7 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
             for (int u = 0; u < 4; ++u) {
                 int c = 0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) c += kk[u][e] != 0u && (int)(kk[u][e] >> 20) >= d1;
+                for (int e = 0; e < 4; ++e) c += kk[u][e] != 0u && (int)(kk[u][e] >> 20) >= d_lo;
                 int x = c;
 #pragma unroll
                 for (int o2 = 1; o2 < 32; o2 <<= 1) {
@@ -631,7 +677,8 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
                 int at = cnt + x - c;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (kk[u][e] != 0u && (int)(kk[u][e] >> 20) >= d1) {
+                    if (kk[u][e] != 0u && (int)(kk[u][e] >> 20) >= d_lo) {
+                        mk = max(mk, kk[u][e]);
                         if (at < R) {
                             my_pos[at] = base + 128 * u + 4 * lane + e;
                             my_key[at] = kk[u][e];
@@ -640,6 +687,11 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
                     }
                 cnt += __shfl_sync(0xffffffffu, x, 31);
             }
+        }
+        if (sampled) {
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o2));
+            if (lane == 0) atomicMax(&s_maxkey, mk);
         }
         if (lane == 0) wcnt[warp] = cnt;
         __syncthreads();
@@ -659,6 +711,25 @@ __global__ void __launch_bounds__(kTkNT, 3) topk_select_attn_kernel(const TopkSe
             }
         }
         __syncthreads();
+        if (sampled) {
+            for (int i = tid; i < kTkBins; i += kTkNT) hist[i] = 0;
+            __syncthreads();
+            if (s_over || s_total < top_k) {
+                // the sample missed: count the whole row, search the whole row
+                count_row(true);
+                tk_find_digit(hist, top_k, wsum, &s_digit, &s_rem, d1, rem1);
+                if (tid == 0) s_over = 1;
+                __syncthreads();
+            } else {
+                // the exact first digit, over the candidates
+                for (int i = tid; i < NW * R; i += kTkNT) {
+                    if (i - (i / R) * R >= wcnt[i / R]) continue;
+                    atomicAdd(&hist[cand_key[i] >> 20], 1);
+                }
+                __syncthreads();
+                tk_find_digit(hist, top_k, wsum, &s_digit, &s_rem, d1, rem1);
+            }
+        }
         const int n_cand = s_total;
         if (s_over) {
             tk_select_full_row(srow, len, top_k, d1, rem1, hist, sel, wsum, &s_digit, &s_rem);

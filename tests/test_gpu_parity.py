@@ -568,6 +568,50 @@ def test_topk_draft_attn_all_scores_equal():
     check_attention(bf16_out_to_f64(out), ref, "topk all-equal")
 
 
+def test_topk_long_row_all_scores_equal():
+    """A row long enough for the sampled threshold (L >= 8192 and >= 8 top_k) with every score
+    tied: the candidates overflow the slots, so the whole row is counted and searched, and the
+    first top_k positions are kept."""
+    B, H_q, H_kv, d, L, top_k = 1, 4, 1, 128, 9000, 100
+    q = rand_bf16((B, 1, H_q, d), 51)
+    k = rand_bf16((B, 1, H_kv, d), 52).expand(B, L, H_kv, d).contiguous()
+    v = rand_bf16((B, L, H_kv, d), 53)
+    sl = np.array([L], np.int32)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_topk_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, _ = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, top_k)
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    check_attention(bf16_out_to_f64(out), ref, "topk long all-equal")
+
+
+def test_topk_sampled_threshold_miss_falls_back_to_the_whole_row():
+    """The sampled threshold reads one 128-key block per warp at positions len * w / 16 (w < 16).
+    Keys there are made the largest of the row (spread over several first-digit bins), so the
+    sample's threshold keeps fewer than top_k candidates; the kernel must notice, count the
+    whole row and still keep exactly the oracle's top_k."""
+    B, H_q, H_kv, d, L, top_k = 1, 4, 1, 128, 32768, 4096
+    q = rand_bf16((B, 1, H_q, d), 54)
+    k = rand_bf16((B, L, H_kv, d), 55)
+    v = rand_bf16((B, L, H_kv, d), 56)
+    qd = q[0, 0, 0].float()
+    unit = qd / qd.norm()
+    for w in range(16):
+        sb = (L * w // 16) & ~3
+        scale = torch.linspace(2.0, 6.0, 128) * (1.0 + 0.01 * w)
+        k[0, sb:sb + 128, 0, :] = (unit.unsqueeze(0) * scale.unsqueeze(1) * 3.0).to(torch.bfloat16)
+    sl = np.array([L], np.int32)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_topk_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, scores = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, top_k, want_scores=True)
+    g = idx.cpu().numpy()
+    # head 0's sample-block keys are all kept (they are its 2048 largest scores)
+    blocks = np.concatenate([np.arange((L * w // 16) & ~3, ((L * w // 16) & ~3) + 128) for w in range(16)])
+    assert np.isin(blocks, g[0, 0]).all()
+    check_topk_attn(bf16_out_to_f64(out), g, ref, idx_o, scores, sl, top_k, "topk sampled-threshold miss")
+
+
 def test_snapkv_select_with_a_budget_per_sequence():
     """Heterogeneous budgets in one batch: each sequence equals the oracle run at its own budget
     (band rule), rows padded with -1 to the largest budget."""
