@@ -702,7 +702,7 @@ static size_t attn_ws_bytes(int B, int H_kv, int D, int M, bool tails) {
 }
 
 bool verify_heads_supported(int H_kv, int D, int M);
-size_t verify_heads_ws_bytes(int ctas);
+size_t verify_heads_ws_bytes(int ctas, int M);
 magicdec_status launch_verify_heads(int B, int H_q, int L_cap, int n_q, const void *q, const void *k, const void *v,
                                     const int32_t *len, void *out, void *ws, size_t ws_bytes, cudaStream_t st);
 
@@ -710,7 +710,7 @@ magicdec_status launch_verify_heads(int B, int H_q, int L_cap, int n_q, const vo
 // allows it, for the all-heads verification kernel at two CTAs per SM.
 size_t attn_workspace_bytes(int B, int H_kv, int D, int M) {
     const size_t per_pair = attn_ws_bytes(B, H_kv, D, M, true);
-    const size_t heads = verify_heads_supported(H_kv, D, M) ? verify_heads_ws_bytes(2 * magicdec_host::sm_count()) : 0;
+    const size_t heads = verify_heads_supported(H_kv, D, M) ? verify_heads_ws_bytes(2 * magicdec_host::sm_count(), M) : 0;
     return per_pair > heads ? per_pair : heads;
 }
 // The least the kernel can run with (no tails).

@@ -1,7 +1,8 @@
 """Randomised shapes and length mixes at d = 128 with eight KV heads: the all-heads
 verification kernel (up to 16 rows per KV head) against the per-pair kernel and against
-itself across repeated calls; the per-pair kernel's two-row-tile verification (17-32 rows)
-against the oracle; and the Top-K score pass against the per-pair score kernel.  Seeded; each case
+itself across repeated calls; verification at 17-32 rows per KV head (17-24 in the
+swapped-operand all-heads kernel, 25-32 in the per-pair kernel's two row tiles) against the
+oracle; and the Top-K score pass against the per-pair score kernel.  Seeded; each case
 is small (a few MB), so the whole file runs in seconds."""
 import os
 
@@ -91,9 +92,10 @@ def _case_two_tiles(seed):
 
 @pytest.mark.parametrize("seed", range(16))
 def test_verify_two_row_tiles_fuzz(seed, monkeypatch):
-    """d = 128 with eight KV heads and 17-32 rows per KV head runs the per-pair kernel with
-    two row tiles: equal to the oracle, reproducible across calls and across schedules
-    (stage counts)."""
+    """d = 128 with eight KV heads and 17-32 rows per KV head (17-24: the swapped-operand
+    all-heads kernel; 25-32: the per-pair kernel with two row tiles): equal to the oracle,
+    reproducible across calls and across schedules (stage counts); the per-pair kernel on the
+    same inputs equals the oracle too."""
     import oracle
     from parity_util import to_u16
     rng, B, L_cap, G, n_q, lens = _case_two_tiles(seed)
@@ -110,12 +112,19 @@ def test_verify_two_row_tiles_fuzz(seed, monkeypatch):
     b = mb.magicdec_verify_attn(qd, kd, vd, sl)
     monkeypatch.setenv("MAGICDEC_ATTN_STAGES", str(int(rng.choice([2, 3]))))
     c = mb.magicdec_verify_attn(qd, kd, vd, sl)
+    monkeypatch.setenv("MAGICDEC_ATTN_HEADS", "0")
+    monkeypatch.delenv("MAGICDEC_ATTN_STAGES")
+    pp = mb.magicdec_verify_attn(qd, kd, vd, sl)
     torch.cuda.synchronize()
     assert torch.equal(a, b), "verification is not reproducible"
     ref = oracle.verify_attn(to_u16(q), to_u16(k), to_u16(v), np.array(lens, np.int32), n_q)
-    what = f"two row tiles, B={B} L={L_cap} G={G} n_q={n_q} lens={lens}"
+    what = f"17-32 rows, B={B} L={L_cap} G={G} n_q={n_q} lens={lens}"
     check_attention(bf16_out_to_f64(a), ref, what)
     check_attention(bf16_out_to_f64(c), ref, what + " (fewer stages)")
+    check_attention(bf16_out_to_f64(pp), ref, what + " (per-pair kernel)")
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(a[i]) == 0
 
 
 @pytest.mark.parametrize("seed", range(12))

@@ -55,7 +55,8 @@ VERIFY_CASES = [
     (4, 32, 8, 128, 64, 4, [64, 1, 0, 9]),                             # fewer tiles than CTAs
     (1, 32, 8, 128, 9000, 4, [9000]),                                  # one sequence over every CTA
     (2, 32, 8, 128, 3000, 1, [3000, 17]),                              # one query token
-    # ... and 17 to 32 rows per KV head: two row tiles, query fragments read from shared memory
+    # ... and 17 to 32 rows per KV head: 17-24 through the swapped-operand all-heads kernel
+    # (three 8-row n-tiles), 25-32 through the per-pair kernel's two row tiles
     (2, 64, 8, 128, 1000, 4, [1000, 333]),                             # G = 8: exactly 32 rows
     (2, 8, 8, 128, 800, 17, [800, 17]),                                # G = 1, 17 rows (one in tile 2)
     (5, 40, 8, 128, 3000, 5, [3000, 5, 0, 2999, 1]),                   # the Qwen-like shape, edge lengths
@@ -119,17 +120,18 @@ def test_verify_attn_dynamic_tails_deterministic_and_match_static_schedule(monke
     check_attention(bf16_out_to_f64(runs[0][pick]), ref, "verify with tails")
 
 
-@pytest.mark.parametrize("heads", ["1", "0"])
-def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch, heads):
+@pytest.mark.parametrize("heads,n_q", [("1", 4), ("0", 4), ("1", 5)])
+def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch, heads, n_q):
     """Two CTAs per SM (a grid that runs in two waves) and two pipeline stages: short
     sequence runs reuse the query slot and the stages right after releasing them, the
     case where a refill issued without a proxy fence overwrote rows a warp was still
     reading (a 64-position sequence split over three CTAs).  The schedule is fixed, so
-    every call must give the same bits, and match the oracle."""
+    every call must give the same bits, and match the oracle.  16 rows per KV head in
+    both kernels; 20 in the swapped-operand all-heads kernel."""
     monkeypatch.setenv("MAGICDEC_ATTN_HEADS", heads)
     monkeypatch.setenv("MAGICDEC_ATTN_CTAS_PER_SM", "2")
     monkeypatch.setenv("MAGICDEC_ATTN_STAGES", "2")
-    B, H_q, H_kv, d, L_cap, n_q = 6, 32, 8, 128, 3000, 4
+    B, H_q, H_kv, d, L_cap = 6, 32, 8, 128, 3000
     q, k, v = rand_bf16((B, n_q, H_q, d), 4), rand_bf16((B, L_cap, H_kv, d), 5), rand_bf16((B, L_cap, H_kv, d), 6)
     sl = torch.tensor([3000, 2999, 1500, 64, 700, 2222], dtype=torch.int32)
     qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
@@ -142,11 +144,12 @@ def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch
     check_attention(bf16_out_to_f64(first), ref, "verify, two waves of CTAs")
 
 
-def test_verify_attn_per_pair_and_all_heads_kernels_agree(monkeypatch):
-    """The Llama-3.1-8B verification shape runs the all-heads kernel; the per-pair
-    kernel (MAGICDEC_ATTN_HEADS=0) on the same inputs matches the oracle too, and the
-    two agree within the attention tolerance."""
-    B, H_q, H_kv, d, L_cap, n_q = 5, 32, 8, 128, 2600, 4
+@pytest.mark.parametrize("n_q", [4, 5])
+def test_verify_attn_per_pair_and_all_heads_kernels_agree(monkeypatch, n_q):
+    """The Llama-3.1-8B verification shapes (16 and 20 rows per KV head) run the all-heads
+    kernels; the per-pair kernel (MAGICDEC_ATTN_HEADS=0) on the same inputs matches the
+    oracle too, and the two agree within the attention tolerance."""
+    B, H_q, H_kv, d, L_cap = 5, 32, 8, 128, 2600
     q = rand_bf16((B, n_q, H_q, d), 21)
     k = rand_bf16((B, L_cap, H_kv, d), 22)
     v = rand_bf16((B, L_cap, H_kv, d), 23)

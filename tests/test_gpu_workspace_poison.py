@@ -49,9 +49,10 @@ def rand_bf16(shape, seed):
     return torch.randn(shape, generator=g).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("H_q,H_kv,d,n_q", [(32, 8, 128, 4), (40, 8, 128, 5), (16, 2, 64, 4)])
+@pytest.mark.parametrize("H_q,H_kv,d,n_q", [(32, 8, 128, 4), (32, 8, 128, 5), (40, 8, 128, 5), (16, 2, 64, 4)])
 def test_verify_with_poisoned_partials(H_q, H_kv, d, n_q):
-    """Both verification kernels (all-heads at d = 128 / 8 KV heads / 16 rows; per-pair otherwise)."""
+    """Every verification kernel (all-heads at d = 128 / 8 KV heads / 16 and 20 rows;
+    per-pair otherwise)."""
     B, L_cap = 4, 5000
     lens = np.array([5000, 3, 4100, 2500], np.int32)
     q, k, v = rand_bf16((B, n_q, H_q, d), 61), rand_bf16((B, L_cap, H_kv, d), 62), rand_bf16((B, L_cap, H_kv, d), 63)

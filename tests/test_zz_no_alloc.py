@@ -6,10 +6,10 @@ scratch is an array inside the library instead of a caller workspace.
 Checked through the C ABI against magicdec_verify_attn on the same inputs, within the
 attention tolerance the parity tests use, on two calls in a row (different inputs, so
 the second call also shows the shared scratch was left ready), and against the CPU
-oracle.  Both verification kernels run through it: the all-heads kernel (d = 128,
-8 KV heads, 16 query rows per KV head) and the per-pair kernel (40 query heads over 8
-KV heads with 5 speculated rows, and d = 64), which splits long pairs across CTAs and
-merges them through the array's counters.  Collected last so that a stop at the first
+oracle.  Every verification kernel runs through it: the all-heads kernels (d = 128,
+8 KV heads, 16 and 20 query rows per KV head) and the per-pair kernel (40 query heads
+over 8 KV heads with 5 speculated rows, and d = 64), which splits long pairs across CTAs
+and merges them through the array's counters.  Collected last so that a stop at the first
 failure has already run every other test."""
 import numpy as np
 import pytest
@@ -31,8 +31,9 @@ def _inputs(seed, B, H_q, H_kv, d, L_cap, n_q):
     return q, k, v
 
 
-# (H_q, H_kv, d, n_q): all-heads kernel; per-pair kernel at 25 rows per KV head; per-pair at d = 64
-SHAPES = [(32, 8, 128, 4), (40, 8, 128, 5), (32, 8, 64, 4)]
+# (H_q, H_kv, d, n_q): all-heads kernels at 16 and 20 rows per KV head; per-pair kernel at
+# 25 rows per KV head; per-pair at d = 64
+SHAPES = [(32, 8, 128, 4), (32, 8, 128, 5), (40, 8, 128, 5), (32, 8, 64, 4)]
 
 
 @pytest.mark.parametrize("H_q,H_kv,d,n_q", SHAPES)
