@@ -378,10 +378,13 @@ def time_streaming_step(pipe: "Pipeline", steps: int, warmup: int, world: int, d
                                                             pipe.u_res, False, n_acc=pipe.n_acc,
                                                             out_tok=pipe.out_tok, n_amb=pipe.n_amb,
                                                             ws=pipe.ws_acc), 5)
-    sel_ms = time_component(lambda: (mb.magicdec_streaming_select(pipe.seq_len, w.H_kv, w.n_sink, w.n_recent,
-                                                                  idx=pipe.idx, n_sel=pipe.n_sel),
-                                     mb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc,
-                                                           vc=pipe.vc)), 5)
+    # selection + gather: one step's layers x (select, gather) replayed from a CUDA graph,
+    # for the same reason as the draft (two short calls per layer)
+    sel_ms = time_graph(lambda: [(mb.magicdec_streaming_select(pipe.seq_len, w.H_kv, w.n_sink, w.n_recent,
+                                                               idx=pipe.idx, n_sel=pipe.n_sel),
+                                  mb.magicdec_gather_kv(pipe.k, pipe.v, pipe.idx, pipe.cap, kc=pipe.kc,
+                                                        vc=pipe.vc)) for _ in range(pipe.layers)],
+                        3) / pipe.layers
     return ms_total, ver_ms, dra_ms, acc_ms, sel_ms
 
 
