@@ -588,7 +588,9 @@ __global__ void __launch_bounds__(kHdTThreads, 1)
     // The B-operand rows a lane supplies to ldmatrix: row nt*8 + rr (rows past
     // M read row 0 and are zeroed); the rows whose S^T / O^T columns it holds:
     // nt*8 + 2*t4 + e, e = 0, 1.
-    auto qrow = [&](int r) { return (r / p.G) * p.H_q + h * p.G + r % p.G; };
+    // The query slot of this kernel is head-major: row (query head, token).
+    auto qrow = [&](int r) { return (h * p.G + r % p.G) * p.n_q + r / p.G; };
+    const uint32_t qbase = smem_u32(qslot);
 
     int stage = 0, seg_no = 0;
     uint32_t phase = 0;
@@ -598,17 +600,15 @@ __global__ void __launch_bounds__(kHdTThreads, 1)
         const int ti0 = (int)(t - prefix[b]);
         const int nseg = (int)min((long long)prefix[b + 1] - t, t_end - t);
         const int len = hd_clamp(ld_dep(p.len + b), p.L_cap);
-        // The query rows as B fragments (k = channels, n = rows), held for the run:
-        // per k-step and n-tile, chunk 2*ks from lanes 0-7 and 2*ks + 1 from 8-15
-        // address rows nt*8 + rr of the slot; the lanes holding rows past M zero them.
+        // The query rows as B fragments (k = channels, n = rows), held in registers
+        // for the run (the slot is released at once).  Lanes address rows nt*8 + rr
+        // of the slot; the lanes whose fragments hold a row past M zero them.
         uint32_t qb[KS][NT][2];
+        if (ok) ok = mbar_wait(qfull, (uint32_t)(seg_no & 1), p.err);
         {
-            if (ok) ok = mbar_wait(qfull, (uint32_t)(seg_no & 1), p.err);
-            const uint32_t qbase = smem_u32(qslot);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int r = nt * 8 + rr;
-                const int qr = r < p.M ? qrow(r) : 0;
+                const int qr = nt * 8 + rr < p.M ? qrow(nt * 8 + rr) : 0;
                 const bool valid = nt * 8 + g < p.M;
 #pragma unroll
                 for (int k2 = 0; k2 < KS / 2; ++k2) {
@@ -925,8 +925,9 @@ magicdec_status launch_verify_heads(int B, int H_q, int L_cap, int n_q, const vo
     const size_t smem = fixed + (size_t)stages * kHdStage;
     // 17 to 24 rows: the swapped-operand kernel (three 8-row n-tiles)
     const bool swapped = prm.M > kHdRows;
-    if (cudaFuncSetAttribute(swapped ? verify_heads_t_kernel<3> : verify_heads_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    auto kern_t = verify_heads_t_kernel<3>;
+    if (cudaFuncSetAttribute(swapped ? kern_t : verify_heads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
         return MAGICDEC_ERR_CUDA;
 
     prm.q = static_cast<const __nv_bfloat16 *>(q);
@@ -955,14 +956,19 @@ magicdec_status launch_verify_heads(int B, int H_q, int L_cap, int n_q, const vo
     if (!magicdec_host::encode_tmap_bf16_4d(&tmk, k, dims, strides, box) ||
         !magicdec_host::encode_tmap_bf16_4d(&tmv, v, dims, strides, box))
         return MAGICDEC_ERR_CUDA;
-    // Queries as (d, H_q, n_q, B); one box = every query row of the sequence.
-    const uint64_t qdims[4] = {(uint64_t)kHdD, (uint64_t)H_q, (uint64_t)n_q, (uint64_t)B};
-    const uint64_t qstrides[3] = {(uint64_t)kHdD * e, (uint64_t)H_q * kHdD * e, (uint64_t)n_q * H_q * kHdD * e};
-    const uint32_t qbox[4] = {64, (uint32_t)H_q, (uint32_t)n_q, 1};
+    // Queries as (d, H_q, n_q, B); one box = every query row of the sequence,
+    // token-major.  The swapped-operand kernel takes them as (d, n_q, H_q, B),
+    // head-major: a head's rows then sit at consecutive slot rows, whose
+    // swizzle phases differ, so its 8-row ldmatrix reads meet few bank conflicts.
+    const uint64_t qdims[4] = {(uint64_t)kHdD, (uint64_t)(swapped ? n_q : H_q), (uint64_t)(swapped ? H_q : n_q),
+                               (uint64_t)B};
+    const uint64_t qstrides[3] = {swapped ? (uint64_t)H_q * kHdD * e : (uint64_t)kHdD * e,
+                                  swapped ? (uint64_t)kHdD * e : (uint64_t)H_q * kHdD * e,
+                                  (uint64_t)n_q * H_q * kHdD * e};
+    const uint32_t qbox[4] = {64, (uint32_t)(swapped ? n_q : H_q), (uint32_t)(swapped ? H_q : n_q), 1};
     if (!magicdec_host::encode_tmap_bf16_4d(&tmq, q, qdims, qstrides, qbox)) return MAGICDEC_ERR_CUDA;
     if (swapped)
-        return magicdec_host::launch_pdl(verify_heads_t_kernel<3>, dim3(C), dim3(kHdTThreads), smem, st, tmk, tmv,
-                                         tmq, prm);
+        return magicdec_host::launch_pdl(kern_t, dim3(C), dim3(kHdTThreads), smem, st, tmk, tmv, tmq, prm);
     return magicdec_host::launch_pdl(verify_heads_kernel, dim3(C), dim3((kHdHeads + 1) * 32), smem, st, tmk, tmv, tmq,
                                      prm);
 }

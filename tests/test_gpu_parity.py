@@ -120,8 +120,8 @@ def test_verify_attn_dynamic_tails_deterministic_and_match_static_schedule(monke
     check_attention(bf16_out_to_f64(runs[0][pick]), ref, "verify with tails")
 
 
-@pytest.mark.parametrize("heads,n_q", [("1", 4), ("0", 4), ("1", 5)])
-def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch, heads, n_q):
+@pytest.mark.parametrize("heads,H_q,n_q", [("1", 32, 4), ("0", 32, 4), ("1", 32, 5)])
+def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch, heads, H_q, n_q):
     """Two CTAs per SM (a grid that runs in two waves) and two pipeline stages: short
     sequence runs reuse the query slot and the stages right after releasing them, the
     case where a refill issued without a proxy fence overwrote rows a warp was still
@@ -131,7 +131,7 @@ def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch
     monkeypatch.setenv("MAGICDEC_ATTN_HEADS", heads)
     monkeypatch.setenv("MAGICDEC_ATTN_CTAS_PER_SM", "2")
     monkeypatch.setenv("MAGICDEC_ATTN_STAGES", "2")
-    B, H_q, H_kv, d, L_cap = 6, 32, 8, 128, 3000
+    B, H_kv, d, L_cap = 6, 8, 128, 3000
     q, k, v = rand_bf16((B, n_q, H_q, d), 4), rand_bf16((B, L_cap, H_kv, d), 5), rand_bf16((B, L_cap, H_kv, d), 6)
     sl = torch.tensor([3000, 2999, 1500, 64, 700, 2222], dtype=torch.int32)
     qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
@@ -144,12 +144,12 @@ def test_verify_attn_repeated_calls_identical_with_two_waves_of_ctas(monkeypatch
     check_attention(bf16_out_to_f64(first), ref, "verify, two waves of CTAs")
 
 
-@pytest.mark.parametrize("n_q", [4, 5])
-def test_verify_attn_per_pair_and_all_heads_kernels_agree(monkeypatch, n_q):
+@pytest.mark.parametrize("H_q,n_q", [(32, 4), (32, 5)])
+def test_verify_attn_per_pair_and_all_heads_kernels_agree(monkeypatch, H_q, n_q):
     """The Llama-3.1-8B verification shapes (16 and 20 rows per KV head) run the all-heads
     kernels; the per-pair kernel (MAGICDEC_ATTN_HEADS=0) on the same inputs matches the
     oracle too, and the two agree within the attention tolerance."""
-    B, H_q, H_kv, d, L_cap = 5, 32, 8, 128, 2600
+    B, H_kv, d, L_cap = 5, 8, 128, 2600
     q = rand_bf16((B, n_q, H_q, d), 21)
     k = rand_bf16((B, L_cap, H_kv, d), 22)
     v = rand_bf16((B, L_cap, H_kv, d), 23)

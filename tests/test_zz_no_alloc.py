@@ -8,8 +8,8 @@ attention tolerance the parity tests use, on two calls in a row (different input
 the second call also shows the shared scratch was left ready), and against the CPU
 oracle.  Every verification kernel runs through it: the all-heads kernels (d = 128,
 8 KV heads, 16 and 20 query rows per KV head) and the per-pair kernel (40 query heads
-over 8 KV heads with 5 speculated rows, and d = 64), which splits long pairs across CTAs
-and merges them through the array's counters.  Collected last so that a stop at the first
+over 8 KV heads with 5 speculated rows, and d = 64), which splits long pairs across CTAs and merges them through
+the array's counters.  Collected last so that a stop at the first
 failure has already run every other test."""
 import numpy as np
 import pytest
