@@ -57,6 +57,7 @@ constexpr int kMaxContrib = 512;           // contributors a merge lists in shar
 constexpr int kTailMinTiles = 64;          // pairs of at least this many tiles have a dynamic tail
 constexpr int kTailDiv = 16;               // ... of n / kTailDiv tiles
 constexpr int kPrefetchTiles = 5;          // draft tiles per CTA prefetched into L2 before the dependency wait
+constexpr int kDraftStages = 4;   // stage ring depth of the draft (head-major) launches
 
 struct AttnParams {
     const __nv_bfloat16 *q;     // [B, n_q, H_q, D]
@@ -730,6 +731,10 @@ static magicdec_status launch_impl(AttnParams prm, const CUtensorMap &tmk, const
     int stages = (int)((per_cta_cap - fixed) / sb);
     const int want = env_int("MAGICDEC_ATTN_STAGES", 0);
     if (want > 0 && want < stages) stages = want;
+    // The draft (head-major compact cache) measured 0.3-1 % faster with four
+    // stages than with the five that fit, on every draft shape of the bench
+    // (B=32..128, budgets 512..4096; CUDA graphs of 96 calls, same GPU).
+    else if (want <= 0 && prm.head_major && stages > kDraftStages) stages = kDraftStages;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return MAGICDEC_ERR_UNSUPPORTED;
     const size_t smem = fixed + (size_t)stages * sb;
