@@ -217,6 +217,16 @@ __device__ __forceinline__ int pq_locate(long long t, const int *prefix, int B, 
     return lo;
 }
 
+// a0 += b0, a1 += b1 as one packed fp32x2 add (two independent round-to-nearest
+// single-precision adds, the same results as two scalar adds)
+__device__ __forceinline__ void pq_add2(float &a0, float &a1, float b0, float b1) {
+    unsigned long long a, b;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScoreParams p) {
     constexpr int M = D / kPqDs;
@@ -250,11 +260,31 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     const long long T = (long long)p.H_kv * prefix[p.B];
     const long long t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
     int cur_b = -1, cur_h = -1;
+    // Location (sequence, KV head, tile) of a flat tile: a binary search at the
+    // start of the range and when a step leaves a sequence, else one step on.
+    struct Loc { int b, h, ti, nt, len; };
+    auto locate = [&](long long tt) {
+        Loc l;
+        l.b = pq_locate(tt, prefix, p.B, p.H_kv, l.h, l.ti);
+        l.nt = prefix[l.b + 1] - prefix[l.b];
+        l.len = pq_clamp(ld_dep(p.len + l.b), p.L_cap);
+        return l;
+    };
+    auto advance = [&](const Loc &l, long long tt_next) {
+        Loc n = l;
+        if (l.ti + 1 < l.nt) {
+            n.ti = l.ti + 1;
+        } else if (l.h + 1 < p.H_kv) {
+            n.h = l.h + 1;
+            n.ti = 0;
+        } else {
+            n = locate(tt_next);
+        }
+        return n;
+    };
     // codes of tile t are loaded during tile t-1 (software pipeline)
-    auto load_codes = [&](long long tt, uint4 (&dst)[kPqScPer]) {
-        int hh, tti;
-        const int bb = pq_locate(tt, prefix, p.B, p.H_kv, hh, tti);
-        const int ll = pq_clamp(ld_dep(p.len + bb), p.L_cap);
+    auto load_codes = [&](const Loc &lc, uint4 (&dst)[kPqScPer]) {
+        const int bb = lc.b, hh = lc.h, tti = lc.ti, ll = lc.len;
         const uint8_t *cbase = p.codes + ((size_t)bb * p.H_kv + hh) * p.L_cap * M;
 #pragma unroll
         for (int i = 0; i < kPqScPer; ++i) {
@@ -274,12 +304,18 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
     uint4 raw[kPqScPer], nxt[kPqScPer];
 #pragma unroll
     for (int i = 0; i < kPqScPer; ++i) raw[i] = nxt[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (t0 < t1) load_codes(t0, raw);
+    Loc cur{};
+    if (t0 < t1) {
+        cur = locate(t0);
+        load_codes(cur, raw);
+    }
     for (long long t = t0; t < t1; ++t) {
-        int h, ti;
-        const int b = pq_locate(t, prefix, p.B, p.H_kv, h, ti);
-        const int len = pq_clamp(ld_dep(p.len + b), p.L_cap);
-        if (t + 1 < t1) load_codes(t + 1, nxt);
+        const int b = cur.b, h = cur.h, ti = cur.ti, len = cur.len;
+        Loc nxl = cur;
+        if (t + 1 < t1) {
+            nxl = advance(cur, t + 1);
+            load_codes(nxl, nxt);
+        }
         if (b != cur_b || h != cur_h) {            // lookup table of this (sequence, KV head) for its G query heads
             __syncthreads();
             for (int i = tid; i < G * D; i += kPqScThreads) {
@@ -362,13 +398,29 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
                     v[2] = v[3] = 0u;
                 }
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (M == 16 && C == 256) {
+                    // every byte is a valid code: the entry's byte offset c*256 + m*16
+                    // is one byte permute (code r into bits 8-15) plus the subspace's
+                    // offset, which depends only on r and the lane
+                    const char *lutb = reinterpret_cast<const char *>(lut);
+                    const uint32_t rot16 = (uint32_t)rot << 4;
 #pragma unroll
-                for (int r = 0; r < M; ++r) {
-                    const int m = (r + rot) & (M - 1);
-                    int c = (int)((v[r >> 2] >> (8 * (r & 3))) & 255u);
-                    c = c < C ? c : 0;
-                    const float4 l = *reinterpret_cast<const float4 *>(lut + ((size_t)c * M + m) * 4);
-                    acc.x += l.x; acc.y += l.y; acc.z += l.z; acc.w += l.w;
+                    for (int r = 0; r < M; ++r) {
+                        const uint32_t off = __byte_perm(v[r >> 2], 0u, 0x4404u | ((uint32_t)(r & 3) << 4)) +
+                                             (((uint32_t)r * 16u + rot16) & 0xF0u);
+                        const float4 l = *reinterpret_cast<const float4 *>(lutb + off);
+                        pq_add2(acc.x, acc.y, l.x, l.y);
+                        pq_add2(acc.z, acc.w, l.z, l.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < M; ++r) {
+                        const int m = (r + rot) & (M - 1);
+                        int c = (int)((v[r >> 2] >> (8 * (r & 3))) & 255u);
+                        c = c < C ? c : 0;
+                        const float4 l = *reinterpret_cast<const float4 *>(lut + ((size_t)c * M + m) * 4);
+                        acc.x += l.x; acc.y += l.y; acc.z += l.z; acc.w += l.w;
+                    }
                 }
                 srow[0] = acc.x;
                 srow[(size_t)p.L_sc] = acc.y;
@@ -389,6 +441,7 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
         }
 #pragma unroll
         for (int i = 0; i < kPqScPer; ++i) raw[i] = nxt[i];
+        cur = nxl;
     }
 }
 
