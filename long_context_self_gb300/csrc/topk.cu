@@ -309,9 +309,10 @@ __global__ void __launch_bounds__((kTkHdHeads + 1) * 32, 2)
         if (lane != 0) return;
         const uint64_t pol = policy_evict_first();
         int i = 0;
+        int b = seq_of(t_begin);                       // steps on with t (a sequence's tiles are consecutive)
         for (; i < n; ++i) {
             const long long t = t_begin + i;
-            const int b = seq_of(t);
+            while (t >= prefix[b + 1]) ++b;
             const int pos0 = (int)(t - prefix[b]) * kTkHdPos;
             const int stage = i % p.stages;
             const uint32_t phase = (uint32_t)(i / p.stages) & 1u;
@@ -337,9 +338,10 @@ __global__ void __launch_bounds__((kTkHdHeads + 1) * 32, 2)
     const int g0 = 2 * (lane & 3), key_l = lane >> 2;
     int qb_b = -1;
     uint32_t bq[KS][2];
+    int b = seq_of(t_begin);
     for (int i = 0; i < n; ++i) {
         const long long t = t_begin + i;
-        const int b = seq_of(t);
+        while (t >= prefix[b + 1]) ++b;
         if (b != qb_b) {
             qb_b = b;
             const int nrow = lane >> 2;
