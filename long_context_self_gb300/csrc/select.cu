@@ -69,8 +69,10 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4 *k, const ui
         {
             const long long row = base + lane;
             if (lane < RPW && row < rows) {
-                const int bh = (int)(row / n_idx);
-                const int i = (int)(row - (long long)bh * n_idx);
+                // rows < 2^31 (checked at launch): 32-bit divisions
+                const int r32 = (int)row;
+                const int bh = r32 / n_idx;
+                const int i = r32 - bh * n_idx;
                 const int h = bh % H_kv, b = bh / H_kv;
                 // -1 marks padding; any other index outside [0, L_cap) is a
                 // caller error, gathered as a zero row (recorded in the debug build)
