@@ -344,6 +344,27 @@ __global__ void __launch_bounds__(kPqScThreads) pq_scores_kernel(const PqScorePa
                     // the M subspaces of one centroid index fill consecutive bank
                     // quads (see the lookups below); otherwise [m][c][G]
                     const size_t at = G == 4 ? ((size_t)cc * M + m) * 4 : (size_t)mc * G;
+                    if (G == 4) {
+                        // the warp shares m: the query slices are broadcast reads, and
+                        // the entry is one 16-byte store
+                        float sd[4];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const float4 qa = *reinterpret_cast<const float4 *>(qs + g * D + m * kPqDs);
+                            const float4 qb4 = *reinterpret_cast<const float4 *>(qs + g * D + m * kPqDs + 4);
+                            float sdot = qa.x * c0[u].x;
+                            sdot = fmaf(qa.y, c0[u].y, sdot);
+                            sdot = fmaf(qa.z, c0[u].z, sdot);
+                            sdot = fmaf(qa.w, c0[u].w, sdot);
+                            sdot = fmaf(qb4.x, c1[u].x, sdot);
+                            sdot = fmaf(qb4.y, c1[u].y, sdot);
+                            sdot = fmaf(qb4.z, c1[u].z, sdot);
+                            sdot = fmaf(qb4.w, c1[u].w, sdot);
+                            sd[g] = sdot * p.scale;
+                        }
+                        *reinterpret_cast<float4 *>(lut + at) = make_float4(sd[0], sd[1], sd[2], sd[3]);
+                        continue;
+                    }
                     for (int g = 0; g < G; ++g) {
                         const float *qq = qs + g * D + m * kPqDs;
                         float sdot = qq[0] * c0[u].x;
