@@ -72,6 +72,13 @@ def main():
     res["verify_attn"] = run(lambda: mb.magicdec_verify_attn(q, k, v, i32([L_cap, 200])).clone(),
                              lambda: mb.magicdec_verify_attn(q, k, v, i32([L_cap + 5, 200])).clone(), same)
 
+    # the all-heads verification kernels (eight KV heads, d = 128): 16 and 20 rows per KV head
+    k8, v8 = bf16((B, L_cap, 8, d), 12), bf16((B, L_cap, 8, d), 13)
+    for n_q8, name in ((4, "verify_attn_heads16"), (5, "verify_attn_heads20")):
+        q8 = bf16((B, n_q8, 32, d), 14 + n_q8)
+        res[name] = run(lambda: mb.magicdec_verify_attn(q8, k8, v8, i32([L_cap, 200])).clone(),
+                        lambda: mb.magicdec_verify_attn(q8, k8, v8, i32([L_cap + 5, 200])).clone(), same)
+
     # draft attention over a compact cache: lengths below 0 and past the capacity
     kc, vc = bf16((B, H_kv, 64, d), 5), bf16((B, H_kv, 64, d), 6)
     q1 = bf16((B, 1, H_q, d), 7)

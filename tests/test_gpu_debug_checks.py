@@ -12,8 +12,8 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-CASES = ("gather_kv", "verify_attn", "draft_attn", "draft_cache_update", "snapkv_select", "topk_draft_attn",
-         "pq_draft_attn")
+CASES = ("gather_kv", "verify_attn", "verify_attn_heads16", "verify_attn_heads20", "draft_attn", "draft_cache_update",
+         "snapkv_select", "topk_draft_attn", "pq_draft_attn")
 
 
 def child(library):
