@@ -39,7 +39,8 @@ constexpr int kHdD = 128;
 constexpr int kHdHalf = kHdPos * kHdHeads * 128;   // one 64-channel half of K (or V) per stage: 8 KB
 constexpr int kHdStage = 4 * kHdHalf;              // K and V, two halves each: 32 KB
 constexpr int kHdMaxStages = 8;
-constexpr int kHdMaxContrib = 512;                 // contributors a merge lists in shared memory
+constexpr int kHdDefaultStages = 5;               // stage ring depth unless overridden
+constexpr int kHdMaxContrib = 512;                 // CTAs at most (a merge lists one slot per CTA in shared memory)
 constexpr int kHdRows = 16;                        // query rows per KV head (one m16 tile)
 
 struct HeadsParams {
@@ -96,8 +97,8 @@ __global__ void __launch_bounds__((kHdHeads + 1) * 32, 1)
     uint64_t *qfull = empty_bar + kHdMaxStages;
     uint64_t *qempty = qfull + 1;
     int *flag = reinterpret_cast<int *>(qempty + 1);
-    int *contrib = flag + 4;                   // [kHdMaxContrib]
-    int *prefix = contrib + kHdMaxContrib;     // [B+1]
+    int *contrib = flag + 4;                   // [gridDim.x + 1]
+    int *prefix = contrib + gridDim.x + 1;     // [B+1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
@@ -478,8 +479,8 @@ __global__ void __launch_bounds__(kHdTThreads, 1)
     uint64_t *qfull = empty_bar + kHdMaxStages;
     uint64_t *qempty = qfull + 1;
     int *flag = reinterpret_cast<int *>(qempty + 1);
-    int *contrib = flag + 4;                   // [kHdMaxContrib]
-    int *prefix = contrib + kHdMaxContrib;     // [B+1]
+    int *contrib = flag + 4;                   // [gridDim.x + 1]
+    int *prefix = contrib + gridDim.x + 1;     // [B+1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
@@ -913,13 +914,18 @@ magicdec_status launch_verify_heads(int B, int H_q, int L_cap, int n_q, const vo
     if (ws_bytes < verify_heads_ws_bytes(C, prm.M)) return MAGICDEC_ERR_WORKSPACE;
     const size_t qhalf = (size_t)H_q * n_q * 128;
     const size_t fixed = 1024 /* alignment slack */ + 2 * qhalf + (2 * kHdMaxStages + 2) * 8 + 16 +
-                         kHdMaxContrib * 4 + (size_t)(B + 1) * 4;
+                         (size_t)(C + 1) * 4 + (size_t)(B + 1) * 4;
     const int smem_cap = magicdec_host::max_smem_optin();
     const size_t per_cta_cap = ctas_per_sm == 1 ? (size_t)smem_cap : (size_t)(smem_cap / 2 - 1024);
     if (per_cta_cap <= fixed) return MAGICDEC_ERR_UNSUPPORTED;
+    // Five stages (160 KB of K/V in flight per SM) unless MAGICDEC_ATTN_STAGES asks
+    // otherwise.  Measured at B=32 and 128 with 2, 3 and 4 query tokens: a sixth
+    // stage, where shared memory has room for it, is 4-5 % slower; four are
+    // within 1.5 % (slower at B=32 and with 4 tokens); three are 4-5 % slower.
     int stages = (int)((per_cta_cap - fixed) / kHdStage);
     const int want = hd_env_int("MAGICDEC_ATTN_STAGES", 0);
-    if (want > 0 && want < stages) stages = want;
+    const int cap = want > 0 ? want : kHdDefaultStages;
+    if (cap < stages) stages = cap;
     if (stages > kHdMaxStages) stages = kHdMaxStages;
     if (stages < 2) return MAGICDEC_ERR_UNSUPPORTED;
     const size_t smem = fixed + (size_t)stages * kHdStage;

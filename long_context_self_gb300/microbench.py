@@ -1,6 +1,6 @@
 """Time one entry point of libmagicdec on a named synthetic workload.
 
-    python -m long_context_self_gb300.microbench <entry> [--workload NAME] [--batch B]
+    python -m long_context_self_gb300.microbench <entry> [--workload NAME] [--batch B] [--gamma G]
                                                  [--reps N] [--warmup W] [--budget K]
 
 entry: verify | draft | topk | pq | pq_build | accept | accept_greedy | snapkv | gather | draft_cache
@@ -46,6 +46,7 @@ def main(argv=None) -> None:
     ap.add_argument("--pq-iters", type=int, default=2)
     ap.add_argument("--workload", default="llama8b_b128_l32k", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size")
+    ap.add_argument("--gamma", type=int, default=0, help="override the workload's draft length (verify: gamma+1 rows)")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--budget", type=int, default=0, help="draft / Top-K / SnapKV budget (default: the workload's)")
@@ -58,6 +59,8 @@ def main(argv=None) -> None:
     w = synth.WORKLOADS[args.workload]
     if args.batch:
         w = dataclasses.replace(w, B=args.batch)
+    if args.gamma:
+        w = dataclasses.replace(w, gamma=args.gamma)
     budget = args.budget or w.stream_budget or w.snap_budget
     sl = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
     info = {"entry": args.entry, "workload": w.name, "B": w.B, "L": w.L, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d}
