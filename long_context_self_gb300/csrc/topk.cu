@@ -37,6 +37,7 @@ constexpr int kTkTileN = 64;                     // positions per K tile
 constexpr int kTkHalfBytes = kTkTileN * 128;     // 64 positions x 64 channels, bf16
 constexpr int kTkConsumers = 4;                  // warps, 16 positions each
 constexpr int kTkMaxStages = 8;
+constexpr size_t kTkInflightBytes = 128 * 1024;   // score-pass stages per SM (both CTAs), by default
 constexpr int kTkNT = 512;                       // threads of the select kernel
 constexpr int kTkNW = kTkNT / 32;
 constexpr int kTkBins = 4096;
@@ -1002,7 +1003,16 @@ static magicdec_status launch_topk_impl(const TopkScoreParams &sp, const TopkSel
     const size_t fixed = 1024 + 2 * kTkMaxStages * sizeof(uint64_t) + (size_t)(sp.B + 1) * sizeof(int);
     const size_t per_cta = (size_t)smem_cap / 2 - 1024;
     if (per_cta <= fixed + 2 * (size_t)stage_bytes) return MAGICDEC_ERR_UNSUPPORTED;
+    // Stages: as many as fit, up to 128 KB of K in flight per SM (two CTAs), unless
+    // MAGICDEC_TOPK_STAGES asks otherwise.  At B=128, L=32000 the score pass with
+    // more in flight was slower on the same GPU: whole Top-K draft 1.833 ms with
+    // three 32 KB all-heads stages per CTA against 1.784-1.792 ms with two, and
+    // 1.853-1.857 ms with six 16 KB per-pair stages against 1.829 ms with four.
     int stages = (int)((per_cta - fixed) / stage_bytes);
+    const char *want_s = getenv("MAGICDEC_TOPK_STAGES");
+    const int want = want_s && *want_s ? atoi(want_s) : 0;
+    const int cap = want >= 2 ? want : (int)(kTkInflightBytes / (2 * (size_t)stage_bytes));
+    if (cap >= 2 && cap < stages) stages = cap;
     if (stages > kTkMaxStages) stages = kTkMaxStages;
     TopkScoreParams s1 = sp;
     s1.stages = stages;
