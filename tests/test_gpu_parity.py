@@ -93,6 +93,25 @@ def test_verify_attn_is_deterministic_and_split_invariant(monkeypatch):
     check_attention(bf16_out_to_f64(c), bf16_out_to_f64(a).astype(np.float64), "split invariance")
 
 
+@pytest.mark.parametrize("n_q", [2, 4])
+def test_verify_attn_all_heads_stage_depth_does_not_change_bits(monkeypatch, n_q):
+    """The all-heads kernel runs five stages unless MAGICDEC_ATTN_STAGES asks otherwise;
+    six (where shared memory has room) and three give the same bits, since the ring's
+    depth changes only when a tile arrives, not the order of the arithmetic."""
+    B, H_q, H_kv, d, L_cap = 5, 32, 8, 128, 2000
+    q, k, v = rand_bf16((B, n_q, H_q, d), 61), rand_bf16((B, L_cap, H_kv, d), 62), rand_bf16((B, L_cap, H_kv, d), 63)
+    sl = torch.tensor([2000, 1999, 64, 1, 1234], dtype=torch.int32)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    base = mb.magicdec_verify_attn(qd, kd, vd, sld)
+    for st in ("6", "3"):
+        monkeypatch.setenv("MAGICDEC_ATTN_STAGES", st)
+        other = mb.magicdec_verify_attn(qd, kd, vd, sld)
+        torch.cuda.synchronize()
+        assert torch.equal(base, other), st
+    ref = oracle.verify_attn(to_u16(q), to_u16(k), to_u16(v), sl.numpy(), n_q)
+    check_attention(bf16_out_to_f64(base), ref, "verify, all-heads stage depths")
+
+
 def test_verify_attn_dynamic_tails_deterministic_and_match_static_schedule(monkeypatch):
     """With dynamic tails (per-pair kernel, pairs of >= 64 tiles, at least two pairs per
     CTA) which CTA takes a tail varies from call to call, but the chunk boundaries and
@@ -514,11 +533,15 @@ def test_topk_draft_attn_matches_oracle(B, H_q, H_kv, d, L_cap, top_k, lens):
             assert torch.count_nonzero(out[b]) == 0
 
 
-def test_topk_scores_all_heads_and_per_pair_kernels_agree(monkeypatch):
+@pytest.mark.parametrize("stages", ["", "3"])
+def test_topk_scores_all_heads_and_per_pair_kernels_agree(monkeypatch, stages):
     """At d = 128 with eight KV heads the scores come from the kernel that streams all
     heads of a sequence per stage; the per-pair kernel (MAGICDEC_TOPK_HEADS=0) runs the
     same mma sequence per (position, query head), so the kept positions are identical
-    and the outputs equal."""
+    and the outputs equal, whatever the score pass's stage depth (MAGICDEC_TOPK_STAGES:
+    the default and three per CTA)."""
+    if stages:
+        monkeypatch.setenv("MAGICDEC_TOPK_STAGES", stages)
     B, H_q, H_kv, d, L_cap, top_k = 3, 32, 8, 128, 2500, 256
     q = rand_bf16((B, 1, H_q, d), 51).to(DEV)
     k = rand_bf16((B, L_cap, H_kv, d), 52).to(DEV)
