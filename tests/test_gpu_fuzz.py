@@ -2,8 +2,9 @@
 verification kernel (up to 16 rows per KV head) against the per-pair kernel and against
 itself across repeated calls; verification at 17-32 rows per KV head (17-24 in the
 swapped-operand all-heads kernel, 25-32 in the per-pair kernel's two row tiles) against the
-oracle; and the Top-K score pass against the per-pair score kernel.  Seeded; each case
-is small (a few MB), so the whole file runs in seconds."""
+oracle; the Top-K score pass against the per-pair score kernel; draft attention over
+random compact caches and speculative accept over random vocabularies against the
+oracle.  Seeded; each case is small (a few MB), so the whole file runs in seconds."""
 import os
 
 import numpy as np
@@ -146,3 +147,71 @@ def test_topk_scores_all_heads_fuzz(seed, monkeypatch):
     torch.cuda.synchronize()
     assert torch.equal(idx_h, idx_p)
     assert torch.equal(out_h, out_p)
+
+
+def _draft_case(seed):
+    """Draft attention over a compact cache [B, H_kv, cap, d]: random batch, head shape,
+    capacity (one tile to several per pair) and lengths (empty, partial tile, full)."""
+    rng = np.random.default_rng(9000 + seed)
+    B = int(rng.integers(1, 20))
+    H_kv = int(rng.choice([1, 2, 8]))
+    G = int(rng.choice([1, 4, 5, 8]))
+    d = int(rng.choice([64, 128]))
+    cap = int(rng.choice([16, 64, 100, 512, 1000, 2048]))
+    lens = [min(x, cap) for x in _lengths(rng, B, cap)]
+    return B, G * H_kv, H_kv, d, cap, lens
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_draft_attn_fuzz(seed, monkeypatch):
+    """The draft's per-pair kernel (head-major cache, L2 prefetch before the dependency
+    wait, four stages or a random cap) against the oracle; empty rows are zero."""
+    import oracle
+    from parity_util import to_u16
+    B, H_q, H_kv, d, cap, lens = _draft_case(seed)
+    rng = np.random.default_rng(9500 + seed)
+    monkeypatch.setenv("MAGICDEC_ATTN_STAGES", str(int(rng.choice([0, 2, 3]))))
+    g = torch.Generator().manual_seed(4000 + seed)
+    q = torch.randn((B, 1, H_q, d), generator=g).to(torch.bfloat16)
+    kc = torch.randn((B, H_kv, cap, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, H_kv, cap, d), generator=g).to(torch.bfloat16)
+    dl = torch.tensor(lens, dtype=torch.int32)
+    out = mb.magicdec_draft_attn(q.to(DEV), kc.to(DEV), vc.to(DEV), dl.to(DEV))
+    again = mb.magicdec_draft_attn(q.to(DEV), kc.to(DEV), vc.to(DEV), dl.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(out, again), "draft attention is not reproducible"
+    ref = oracle.draft_attn(to_u16(q), to_u16(kc), to_u16(vc), dl.numpy())
+    check_attention(bf16_out_to_f64(out), ref, f"draft B={B} H_q={H_q} H_kv={H_kv} d={d} cap={cap} lens={lens}")
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(out[b]) == 0
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_spec_accept_fuzz(seed):
+    """Speculative accept on random batch, draft length, vocabulary (one statistics record
+    to many, multiples of 4 or not), logit scale and draft noise, sampling or greedy; only
+    the fp64 oracle's margins exclude a sequence."""
+    from parity_util import check_accept, oracle_accept
+    rng = np.random.default_rng(7000 + seed)
+    B = int(rng.integers(1, 41))
+    gamma = int(rng.integers(1, 9))
+    V = int(rng.choice([5, 33, 1000, 4096, 4097, 8191, 20000, 50021]))
+    sigma = float(rng.choice([0.5, 2.0, 4.0]))
+    noise = float(rng.choice([0.1, 0.5, 1.5]))
+    greedy = bool(rng.integers(0, 2))
+    g = torch.Generator().manual_seed(7500 + seed)
+    target = torch.randn((B, gamma + 1, V), generator=g) * sigma
+    draft = target[:, :gamma] + torch.randn((B, gamma, V), generator=g) * noise
+    tok = torch.distributions.Categorical(logits=draft).sample().to(torch.int32)
+    if greedy:
+        am = target[:, :gamma].argmax(-1).to(torch.int32)
+        tok = torch.where(torch.rand(tok.shape, generator=g) < 0.7, am, tok)
+    u_acc, u_res = torch.rand((B, gamma), generator=g), torch.rand((B,), generator=g)
+    got = mb.magicdec_spec_accept(target.to(DEV), draft.to(DEV), tok.to(DEV), u_acc.to(DEV), u_res.to(DEV), greedy)
+    torch.cuda.synchronize()
+    t, d_, x, ua, ur = (a.numpy() for a in (target, draft, tok, u_acc, u_res))
+    ref = oracle_accept(t, d_, x, ua, ur, greedy)
+    what = f"accept B={B} gamma={gamma} V={V} sigma={sigma} noise={noise} greedy={greedy}"
+    n_excl = check_accept(tuple(a.cpu().numpy() for a in got), ref, what, inputs=(t, d_, ur), greedy=greedy)
+    assert n_excl <= max(2, B // 4), what
