@@ -215,3 +215,54 @@ def test_spec_accept_fuzz(seed):
     what = f"accept B={B} gamma={gamma} V={V} sigma={sigma} noise={noise} greedy={greedy}"
     n_excl = check_accept(tuple(a.cpu().numpy() for a in got), ref, what, inputs=(t, d_, ur), greedy=greedy)
     assert n_excl <= max(2, B // 4), what
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_snapkv_select_fuzz(seed):
+    """SnapKV selection (tensor-core window scores, max-pool, per-KV-head top-k) on random
+    head shapes (G up to 8, w*G up to 256 window rows), head sizes, windows, pool widths,
+    budgets and lengths (shorter than the budget, equal, longer), with and without planted
+    heavy hitters, under the oracle's band rule."""
+    import oracle
+    from long_context_self_gb300 import synth
+    from parity_util import check_topk, to_u16
+    rng = np.random.default_rng(11000 + seed)
+    B = int(rng.integers(1, 5))
+    H_kv = int(rng.choice([1, 2, 8]))
+    G = int(rng.choice([1, 2, 4, 5, 8]))
+    d = int(rng.choice([64, 128]))
+    w = int(rng.choice([w_ for w_ in (1, 4, 8, 16, 32) if w_ * G <= 256]))
+    pool = int(rng.choice([1, 3, 5, 7, 9]))
+    L_cap = int(rng.choice([100, 700, 3000, 9000]))
+    budget = int(rng.integers(w, max(w + 1, L_cap // 2)))
+    lens = []
+    for _ in range(B):
+        kind = int(rng.integers(0, 4))
+        lens.append(L_cap if kind == 0 else int(rng.integers(0, budget + 1)) if kind == 1 else
+                    budget if kind == 2 else int(rng.integers(budget + 1, L_cap + 1)))
+    lens = [min(x, L_cap) for x in lens]
+    heavy = bool(rng.integers(0, 2))
+    wl = synth.Workload("fuzz", B=B, H_q=G * H_kv, H_kv=H_kv, d=d, L=L_cap, gamma=1, V=8, snap_window=w,
+                        snap_pool=pool, snap_budget=budget, heavy_frac=0.005 if heavy else 0.0, seed=40 + seed)
+    k, _, dirs = synth.kv_cache(wl, "cpu")
+    q_win = synth.window_queries(wl, "cpu", heavy_dirs=dirs)
+    sl = np.array(lens, np.int32)
+    idx, n_sel = mb.magicdec_snapkv_select(q_win.to(DEV), k.to(DEV), torch.from_numpy(sl).to(DEV), w, pool, budget)
+    torch.cuda.synchronize()
+    idx_o, n_sel_o, pooled = oracle.snapkv_select(to_u16(q_win), to_u16(k), sl, pool, budget)
+    band = check_topk(idx.cpu().numpy(), n_sel.cpu().numpy(), idx_o, n_sel_o, pooled, sl, w, budget)
+    what = f"snapkv B={B} H_kv={H_kv} G={G} d={d} w={w} pool={pool} L={L_cap} budget={budget} lens={lens}"
+    # The band must leave the comparison meaningful.  Positions tied exactly with the k-th
+    # pooled score (planted heavy hitters share one key, so their pooled plateaus tie) may
+    # all sit in it; beyond those, a plateau or two per (sequence, KV head), or 1 % of the
+    # competing positions where the budget puts the threshold in the dense middle of the
+    # score distribution.
+    ties, compared = 0, 0
+    for b, L in enumerate(lens):
+        if L <= budget or budget == w:
+            continue
+        for h in range(H_kv):
+            pl = pooled[b, h, :L - w]
+            ties += int(np.count_nonzero(pl == np.sort(pl)[::-1][budget - w - 1]))
+            compared += L - w
+    assert band - ties <= max(2 * pool * B * H_kv + 8, 0.01 * compared), what
