@@ -3,8 +3,9 @@ verification kernel (up to 16 rows per KV head) against the per-pair kernel and 
 itself across repeated calls; verification at 17-32 rows per KV head (17-24 in the
 swapped-operand all-heads kernel, 25-32 in the per-pair kernel's two row tiles) against the
 oracle; the Top-K score pass against the per-pair score kernel; draft attention over
-random compact caches and speculative accept over random vocabularies against the
-oracle.  Seeded; each case is small (a few MB), so the whole file runs in seconds."""
+random compact caches, speculative accept over random vocabularies, SnapKV selection,
+the Top-K draft and the gather against the oracle.  Seeded; each case is small (a few
+MB), so the whole file runs in well under a minute."""
 import os
 
 import numpy as np
@@ -266,3 +267,62 @@ def test_snapkv_select_fuzz(seed):
             ties += int(np.count_nonzero(pl == np.sort(pl)[::-1][budget - w - 1]))
             compared += L - w
     assert band - ties <= max(2 * pool * B * H_kv + 8, 0.01 * compared), what
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_topk_draft_attn_fuzz(seed):
+    """Top-K attention draft on random head shapes, head sizes, lengths (empty, shorter than
+    top_k, long enough for the sampled threshold) and budgets, with a few dominant keys,
+    against the oracle under the band rule."""
+    import oracle
+    from parity_util import check_topk_attn, to_u16
+    rng = np.random.default_rng(13000 + seed)
+    B = int(rng.integers(1, 6))
+    H_kv = int(rng.choice([1, 2, 8]))
+    G = int(rng.choice([1, 2, 4, 5, 8]))
+    d = int(rng.choice([64, 128]))
+    L_cap = int(rng.choice([64, 700, 3000, 9000, 20000]))
+    top_k = int(rng.integers(1, min(L_cap, 4096) + 1))
+    lens = _lengths(rng, B, L_cap)
+    H_q = G * H_kv
+    g = torch.Generator().manual_seed(13500 + seed)
+    q = torch.randn((B, 1, H_q, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16)
+    k[:, ::int(rng.integers(50, 200))] *= 4
+    sl = np.array(lens, np.int32)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_topk_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, scores = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, top_k, want_scores=True)
+    what = f"topk B={B} H_q={H_q} H_kv={H_kv} d={d} L={L_cap} top_k={top_k} lens={lens}"
+    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, scores, sl, top_k, what)
+    assert swapped <= max(1, B * H_q // 50), what
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(out[b]) == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_gather_kv_fuzz(seed):
+    """Gather into the compact cache: random shapes, capacities, index lists (any order,
+    repeats, -1 padding), bit for bit against the oracle."""
+    import oracle
+    from parity_util import to_u16
+    rng = np.random.default_rng(15000 + seed)
+    B = int(rng.integers(1, 6))
+    H_kv = int(rng.choice([1, 2, 8]))
+    d = int(rng.choice([64, 128]))
+    L_cap = int(rng.choice([1, 17, 300, 4000]))
+    n_idx = int(rng.integers(1, 700))
+    cap = int(n_idx + rng.integers(0, 40))
+    idx = rng.integers(0, L_cap, size=(B, H_kv, n_idx)).astype(np.int32)
+    idx[rng.random(idx.shape) < 0.1] = -1
+    g = torch.Generator().manual_seed(15500 + seed)
+    k = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, L_cap, H_kv, d), generator=g).to(torch.bfloat16)
+    kc, vc = mb.magicdec_gather_kv(k.to(DEV), v.to(DEV), torch.from_numpy(idx).to(DEV), cap)
+    torch.cuda.synchronize()
+    kc_o, vc_o = oracle.gather_kv(to_u16(k), to_u16(v), idx, cap)
+    assert np.array_equal(to_u16(kc), kc_o)
+    assert np.array_equal(to_u16(vc), vc_o)
