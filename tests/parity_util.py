@@ -70,14 +70,17 @@ def check_topk(idx_gpu: np.ndarray, n_sel_gpu: np.ndarray, idx_ora: np.ndarray, 
 
 
 def check_topk_attn(out_gpu: np.ndarray, idx_gpu: np.ndarray, out_ora: np.ndarray, idx_ora: np.ndarray,
-                    scores: np.ndarray, seq_len: np.ndarray, top_k: int, what: str = "topk attention"):
+                    scores: np.ndarray, seq_len: np.ndarray, top_k: int, what: str = "topk attention", qkv=None):
     """Top-K attention draft under the band rule.  Outside the band |s - tau| <= MARGIN * max(|tau|, 1)
     (tau = the oracle's top_k-th score) membership must match exactly; inside it only the count.
-    Heads whose kept set differs from the oracle's (inside the band) are left out of the element-wise
-    output comparison.  Returns (heads with a band swap, band positions)."""
+    A head whose kept set differs from the oracle's (inside the band, so the kernel's set is
+    as valid) is compared with the oracle's attention over the kernel's own kept positions when
+    `qkv` = (q, k, v) (bf16 bits, [B, 1, H_q, d] and [B, L, H_kv, d]) is given, and left out of
+    the element-wise comparison otherwise.  Returns (heads with a band swap, band positions)."""
     B, H, _ = idx_ora.shape
     swapped, band_total = 0, 0
     keep = np.ones((B, H), bool)
+    own = []
     for b in range(B):
         L = int(seq_len[b])
         n = min(L, top_k)
@@ -101,7 +104,20 @@ def check_topk_attn(out_gpu: np.ndarray, idx_gpu: np.ndarray, out_ora: np.ndarra
             if not np.array_equal(sel_g, sel_o):
                 swapped += 1
                 keep[b, h] = False
+                own.append((b, h, gs))
     check_attention(out_gpu[:, 0][keep], out_ora[:, 0][keep], what)
+    if qkv is not None and own:
+        import oracle
+        q, k, v = qkv
+        G = H // k.shape[2]
+        got, ref = [], []
+        for b, h, gs in own:
+            kc = np.ascontiguousarray(k[b, gs, h // G][None, None])       # [1, 1, n, d]: the kernel's rows
+            vc = np.ascontiguousarray(v[b, gs, h // G][None, None])
+            qh = np.ascontiguousarray(q[b:b + 1, :, h:h + 1])
+            ref.append(oracle.draft_attn(qh, kc, vc, np.array([gs.size], np.int32))[0, 0, 0])
+            got.append(out_gpu[b, 0, h])
+        check_attention(np.array(got), np.array(ref), what + " (heads with a band swap, over their own kept set)")
     return swapped, band_total
 
 

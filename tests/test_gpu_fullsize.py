@@ -136,10 +136,10 @@ def test_fullsize_topk_draft_sampled(name, top_k):
         b = int(b)
         L = int(sl[b])
         sl_o = np.array([L], np.int32)
-        ref, idx_o, scores = oracle.topk_attn(to_u16(qd[b:b + 1]), to_u16(k[b:b + 1, :L]), to_u16(v[b:b + 1, :L]),
-                                              sl_o, top_k, want_scores=True)
+        qkv = (to_u16(qd[b:b + 1]), to_u16(k[b:b + 1, :L]), to_u16(v[b:b + 1, :L]))
+        ref, idx_o, scores = oracle.topk_attn(*qkv, sl_o, top_k, want_scores=True)
         sw, _ = check_topk_attn(bf16_out_to_f64(out[b:b + 1]), idx[b:b + 1].cpu().numpy(), ref, idx_o, scores, sl_o,
-                                top_k, f"{name} topk b={b}")
+                                top_k, f"{name} topk b={b}", qkv=qkv)
         swapped += sw
     assert swapped <= 2
     del k, v
@@ -184,11 +184,11 @@ def test_fullsize_pq_sampled():
     for b in rng.choice(w.B, size=2, replace=False):
         b = int(b)
         sl_o = np.array([w.L], np.int32)
-        ref, idx_o, approx = oracle.pq_attn(to_u16(qd[b:b + 1]), to_u16(k[b:b + 1]), to_u16(v[b:b + 1]), sl_o,
-                                            cb[b:b + 1].cpu().numpy(), rand_codes[b:b + 1].numpy(), top_k,
+        qkv = (to_u16(qd[b:b + 1]), to_u16(k[b:b + 1]), to_u16(v[b:b + 1]))
+        ref, idx_o, approx = oracle.pq_attn(*qkv, sl_o, cb[b:b + 1].cpu().numpy(), rand_codes[b:b + 1].numpy(), top_k,
                                             want_approx=True)
         sw, _ = check_topk_attn(bf16_out_to_f64(out[b:b + 1]), idx[b:b + 1].cpu().numpy(), ref, idx_o, approx, sl_o,
-                                top_k, f"pq b={b}")
+                                top_k, f"pq b={b}", qkv=qkv)
         assert sw <= 2
     del k, v, cb, codes, rand_codes
     torch.cuda.empty_cache()

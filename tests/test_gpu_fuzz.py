@@ -296,8 +296,8 @@ def test_topk_draft_attn_fuzz(seed):
     torch.cuda.synchronize()
     ref, idx_o, scores = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, top_k, want_scores=True)
     what = f"topk B={B} H_q={H_q} H_kv={H_kv} d={d} L={L_cap} top_k={top_k} lens={lens}"
-    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, scores, sl, top_k, what)
-    assert swapped <= max(1, B * H_q // 50), what
+    check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, scores, sl, top_k, what,
+                    qkv=(to_u16(q), to_u16(k), to_u16(v)))
     for b, L in enumerate(lens):
         if L == 0:
             assert torch.count_nonzero(out[b]) == 0
@@ -326,3 +326,64 @@ def test_gather_kv_fuzz(seed):
     kc_o, vc_o = oracle.gather_kv(to_u16(k), to_u16(v), idx, cap)
     assert np.array_equal(to_u16(kc), kc_o)
     assert np.array_equal(to_u16(vc), vc_o)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_pq_fuzz(seed, monkeypatch):
+    """PQCache-style draft on random shapes: the encode (tensor-core or FMA) under the
+    distance-margin rule, one Lloyd update bit for bit, and PQ attention over the oracle's
+    codes under the band rule (G up to 8, d 64/128, C 2-256, budgets, ragged and empty
+    lengths)."""
+    import oracle
+    from parity_util import check_topk_attn, to_u16
+    rng = np.random.default_rng(17000 + seed)
+    B = int(rng.integers(1, 4))
+    H_kv = int(rng.choice([1, 2, 8]))
+    G = int(rng.choice([1, 4, 5, 8]))
+    d = int(rng.choice([64, 128]))
+    M = d // 8
+    C = int(rng.choice([2, 7, 32, 64, 200, 256]))
+    L = int(rng.choice([100, 999, 3000]))
+    top_k = int(rng.integers(1, min(L, 1024) + 1))
+    lens = [x if x > 0 or rng.random() < 0.5 else 1 for x in _lengths(rng, B, L)]
+    monkeypatch.setenv("MAGICDEC_PQ_TC", str(int(rng.integers(0, 2))))
+    H_q = G * H_kv
+    g = torch.Generator().manual_seed(17500 + seed)
+    q = torch.randn((B, 1, H_q, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, L, H_kv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, L, H_kv, d), generator=g).to(torch.bfloat16)
+    k[:, ::int(rng.integers(40, 120))] *= 3
+    cb = rng.standard_normal((B, H_kv, M, C, 8)).astype(np.float32)
+    what = f"pq B={B} H_q={H_q} H_kv={H_kv} d={d} C={C} L={L} top_k={top_k} lens={lens}"
+    # encode under the margin rule
+    codes_g = mb.magicdec_pq_encode(k.to(DEV), torch.from_numpy(cb).to(DEV))
+    torch.cuda.synchronize()
+    codes_o, gap = oracle.pq_encode(to_u16(k), cb, want_gap=True)
+    kf = bf16_out_to_f64(k).reshape(B, L, H_kv, M, 8).transpose(0, 2, 1, 3, 4)
+    kn = (kf ** 2).sum(-1)
+    cn = (cb.astype(np.float64) ** 2).sum(-1)
+    cbest = np.take_along_axis(cn[:, :, None, :, :], codes_o[..., None].astype(np.int64), axis=-1)[..., 0]
+    margin = gap <= 1e-5 * (kn + cbest)
+    assert np.array_equal(codes_g.cpu().numpy()[~margin], codes_o[~margin]), what
+    # one Lloyd update over each sequence's own length, bit for bit
+    sl = np.array(lens, np.int32)
+    cb_g = torch.from_numpy(cb.copy()).to(DEV)
+    mb.magicdec_pq_update(k.to(DEV), torch.from_numpy(sl).to(DEV), torch.from_numpy(codes_o).to(DEV), cb_g)
+    torch.cuda.synchronize()
+    cb2 = oracle.pq_update(to_u16(k), sl, codes_o, cb)
+    np.testing.assert_array_equal(cb_g.cpu().numpy(), cb2, err_msg=what)
+    # PQ attention over the oracle's codes for the updated codebook
+    codes2, _ = oracle.pq_encode(to_u16(k), cb2)
+    idx = torch.empty((B, H_q, top_k), dtype=torch.int32, device=DEV)
+    out = mb.magicdec_pq_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV),
+                                    torch.from_numpy(cb2).to(DEV), torch.from_numpy(codes2).to(DEV), top_k, idx=idx)
+    torch.cuda.synchronize()
+    ref, idx_o, approx = oracle.pq_attn(to_u16(q), to_u16(k), to_u16(v), sl, cb2, codes2, top_k, want_approx=True)
+    # a small codebook (C = 2: at most 2^M distinct approximate scores) ties many positions
+    # at the threshold, broken by rounding-level differences of the score sums: heads that
+    # swap inside the band are checked over their own kept positions
+    check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, approx, sl, top_k, what,
+                    qkv=(to_u16(q), to_u16(k), to_u16(v)))
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.count_nonzero(out[b]) == 0

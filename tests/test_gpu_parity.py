@@ -356,7 +356,8 @@ def test_pq_draft_attn_matches_oracle(B, H_q, H_kv, L, C, top_k, lens):
                                     torch.from_numpy(cb).to(DEV), torch.from_numpy(codes).to(DEV), top_k, idx=idx)
     torch.cuda.synchronize()
     ref, idx_o, approx = oracle.pq_attn(to_u16(q), to_u16(k), to_u16(v), sl, cb, codes, top_k, want_approx=True)
-    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, approx, sl, top_k, "pq")
+    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, approx, sl, top_k, "pq",
+                                 qkv=(to_u16(q), to_u16(k), to_u16(v)))
     assert swapped <= max(1, B * H_q // 50)
     for b, n in enumerate(lens):
         if n == 0:
@@ -393,7 +394,8 @@ def test_pq_head_dim_64():
                                     torch.from_numpy(cb2).to(DEV), torch.from_numpy(codes2).to(DEV), top_k, idx=idx)
     torch.cuda.synchronize()
     ref, idx_o, approx = oracle.pq_attn(to_u16(q), to_u16(k), to_u16(v), sl, cb2, codes2, top_k, want_approx=True)
-    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, approx, sl, top_k, "pq d64")
+    swapped, _ = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, approx, sl, top_k, "pq d64",
+                                 qkv=(to_u16(q), to_u16(k), to_u16(v)))
     assert swapped <= 1
 
 
@@ -526,7 +528,8 @@ def test_topk_draft_attn_matches_oracle(B, H_q, H_kv, d, L_cap, top_k, lens):
     out = mb.magicdec_topk_draft_attn(q.to(DEV), k.to(DEV), v.to(DEV), torch.from_numpy(sl).to(DEV), top_k, idx=idx)
     torch.cuda.synchronize()
     ref, idx_o, scores = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), sl, top_k, want_scores=True)
-    swapped, band = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, scores, sl, top_k)
+    swapped, band = check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), ref, idx_o, scores, sl, top_k,
+                                    qkv=(to_u16(q), to_u16(k), to_u16(v)))
     assert swapped <= max(1, B * H_q // 50), f"{swapped} heads swapped a position inside the band"
     for b, L in enumerate(lens):
         if L == 0:
@@ -635,7 +638,8 @@ def test_topk_sampled_threshold_miss_falls_back_to_the_whole_row():
     # head 0's sample-block keys are all kept (they are its 2048 largest scores)
     blocks = np.concatenate([np.arange((L * w // 16) & ~3, ((L * w // 16) & ~3) + 128) for w in range(16)])
     assert np.isin(blocks, g[0, 0]).all()
-    check_topk_attn(bf16_out_to_f64(out), g, ref, idx_o, scores, sl, top_k, "topk sampled-threshold miss")
+    check_topk_attn(bf16_out_to_f64(out), g, ref, idx_o, scores, sl, top_k, "topk sampled-threshold miss",
+                    qkv=(to_u16(q), to_u16(k), to_u16(v)))
 
 
 def test_snapkv_select_with_a_budget_per_sequence():

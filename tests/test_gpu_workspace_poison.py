@@ -107,7 +107,7 @@ def test_topk_draft_with_poisoned_workspace():
     torch.cuda.synchronize()
     out_o, idx_o, scores = oracle.topk_attn(to_u16(q), to_u16(k), to_u16(v), lens, top_k, want_scores=True)
     check_topk_attn(bf16_out_to_f64(out), idx.cpu().numpy(), out_o, idx_o, scores, lens, top_k,
-                    "topk over a poisoned workspace")
+                    "topk over a poisoned workspace", qkv=(to_u16(q), to_u16(k), to_u16(v)))
 
 
 @pytest.mark.parametrize("greedy", [False, True])
