@@ -20,7 +20,8 @@
 //          statistics pass are still in L2);
 //   draw   one CTA per sequence: finds the chunk where the running sum
 //          crosses u * total (shuffle scan + ballot) and walks it with
-//          double-float weights (fp64 block scan).
+//          double-float weights; the chunk sums, scans and comparisons of the
+//          draw are double-float on the FP32 pipes (fp64 throughput is scarce).
 // Only the per-logit exponentials are single precision (random ~1e-6 relative
 // errors that average out in the sums); normalisers, ratios and running sums
 // carry ~1e-12 relative error, so the drawn token agrees with an exact
@@ -87,6 +88,20 @@ __device__ __forceinline__ dflt warp_sum_df(dflt a) {
     return a;
 }
 
+__device__ __forceinline__ dflt df_sub(dflt a, dflt b) { return df_add(a, dflt{-b.hi, -b.lo}); }
+
+// Order of normalised double-float values (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool df_lt(dflt a, dflt b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ bool df_le(dflt a, dflt b) { return a.hi < b.hi || (a.hi == b.hi && a.lo <= b.lo); }
+__device__ __forceinline__ bool df_positive(dflt a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
+
+__device__ __forceinline__ dflt df_shfl_up(dflt a, int o) {
+    return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ dflt df_shfl(dflt a, int src) {
+    return {__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+
 // ------------------------------------------------------------------- stats
 struct RowStat {
     double s;          // sum over the chunk of exp(x - m)
@@ -117,7 +132,7 @@ struct AcceptParams {
     RowStat *stats;           // [B, rows_per_b, n_stat_chunks]: one record per 4 slices of 1024 logits
     JobInfo *job;             // [B]
     int *err;
-    double *chunk_sum;        // [B, n_chunks] weight sums of the sampled row(s)
+    dflt *chunk_sum;          // [B, n_chunks] weight sums of the sampled row(s), double-float
     int B, gamma, V, n_chunks, n_stat_chunks, rows_per_b, greedy;
 };
 
@@ -330,10 +345,16 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
             int oq = 0;
             if (xtok >= 0 && xtok < V) {
                 const RowAll ts = rs[i], ds = rs[gamma + 1 + i];
-                const double px = exp((double)xt - (double)ts.m) / ts.s;
-                const double qx = exp((double)xd - (double)ds.m) / ds.s;
-                if (qx > 0.0) rt = px / qx;
-                else oq = px > 0.0 ? 1 : 2;
+                const double dp = (double)xt - (double)ts.m, dq = (double)xd - (double)ds.m;
+                if (dp > -700.0 && dq > -700.0) {
+                    // p / q as one exponential and one division (fp64 is narrow here)
+                    rt = exp(dp - dq) * (ds.s / ts.s);
+                } else {
+                    // an exponential may underflow: q = 0 < p accepts, p = q = 0 rejects
+                    const double px = exp(dp) / ts.s, qx = exp(dq) / ds.s;
+                    if (qx > 0.0) rt = px / qx;
+                    else oq = px > 0.0 ? 1 : 2;
+                }
             } else {
                 oq = 2;
             }
@@ -494,45 +515,47 @@ __device__ __forceinline__ void weight4_fast_acc(dflt &acc, const WeightCtx &w, 
     acc_add(acc, dflt{weight_fast(w, xt.w, xd.w, resid), 0.f});
 }
 
-// Inclusive scan of one double per thread in thread order: shuffle scans in
-// each warp, a scan of the warp totals by warp 0, two barriers.
-__device__ double block_scan_warps(double v, double *wtot) {
+// Inclusive scan of one double-float per thread in thread order: shuffle
+// scans in each warp, a scan of the warp totals by warp 0, two barriers.  The
+// sums of the draw run on the FP32 pipes in double-float (~1e-14 relative)
+// rather than in fp64, whose pipe is narrow on this GPU.
+__device__ dflt block_scan_df(dflt v, dflt *wtot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    double x = v;
+    dflt x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const dflt y = df_shfl_up(x, o);
+        if (lane >= o) x = df_add(x, y);
     }
     if (lane == 31) wtot[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        double t = lane < nw ? wtot[lane] : 0.0;
+        dflt t = lane < nw ? wtot[lane] : dflt{0.f, 0.f};
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= o) t += y;
+            const dflt y = df_shfl_up(t, o);
+            if (lane >= o) t = df_add(t, y);
         }
         if (lane < nw) wtot[lane] = t;
     }
     __syncthreads();
-    return x + (warp ? wtot[warp - 1] : 0.0);
+    return warp ? df_add(x, wtot[warp - 1]) : x;
 }
 
 // Sum of the chunk sums in a fixed order, computed by one warp (every lane
 // returns it): lane l adds its contiguous block, then a shuffle scan.
-__device__ double warp_chunk_total(const double *csum, int n, int lane) {
+__device__ dflt warp_chunk_total(const dflt *csum, int n, int lane) {
     const int per = (n + 31) / 32;
     const int lo = min(n, lane * per), hi = min(n, lo + per);
-    double part = 0.0;
-    for (int c = lo; c < hi; ++c) part += csum[c];
-    double incl = part;
+    dflt part = {0.f, 0.f};
+    for (int c = lo; c < hi; ++c) part = df_add(part, csum[c]);
+    dflt incl = part;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        const dflt y = df_shfl_up(incl, o);
+        if (lane >= o) incl = df_add(incl, y);
     }
-    return __shfl_sync(0xffffffffu, incl, 31);
+    return df_shfl(incl, 31);
 }
 
 constexpr int kSmpThreads = 1024;
@@ -544,7 +567,7 @@ constexpr int kSmpMaxChunks = 256;
 // Thread t holds logits 4t .. 4t+3 of each chunk; a chunk's per-thread sums
 // are reduced in a fixed order (warps by shuffles, then warp 0's lanes).
 __device__ __forceinline__ void batch_chunk_sums(const WeightCtx &w, bool resid, int V, bool vec4, int c0,
-                                                 int n_chunks, dflt (*wred)[32], double *csum) {
+                                                 int n_chunks, dflt (*wred)[32], dflt *csum) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float4 xt[kSmpBatch], xd[kSmpBatch];
     const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -580,7 +603,7 @@ __device__ __forceinline__ void batch_chunk_sums(const WeightCtx &w, bool resid,
     if (warp < kSmpBatch) {
         dflt v = wred[warp][lane];
         v = warp_sum_df(v);
-        if (lane == 0 && c0 + warp < n_chunks) csum[c0 + warp] = df_to_double(v);
+        if (lane == 0 && c0 + warp < n_chunks) csum[c0 + warp] = v;
     }
     __syncthreads();
 }
@@ -650,7 +673,7 @@ __global__ void __launch_bounds__(kChkThreads) accept_chunk_kernel(const AcceptP
             u.lo = __shfl_down_sync(0xffffffffu, t.lo, o);
             t = df_add(t, u);
         }
-        if (lane == 0) p.chunk_sum[(long long)b * p.n_chunks + c] = df_to_double(t);
+        if (lane == 0) p.chunk_sum[(long long)b * p.n_chunks + c] = t;
     }
 }
 
@@ -660,10 +683,10 @@ __global__ void __launch_bounds__(kChkThreads) accept_chunk_kernel(const AcceptP
 // cumulative weight passes u * total and walks it.  An empty residual (p == q
 // up to rounding) is redrawn from p, whose chunk sums this CTA recomputes.
 __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const AcceptParams p) {
-    __shared__ double csum[kSmpMaxChunks];
+    __shared__ dflt csum[kSmpMaxChunks];
     __shared__ dflt wred[kSmpBatch][32];
-    __shared__ double wtot[32];
-    __shared__ double s_W, s_before;
+    __shared__ dflt wtot[32];
+    __shared__ dflt s_W, s_before;
     __shared__ int s_cstar, s_amb;
     __shared__ int found_token, found_amb;
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -687,8 +710,8 @@ __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const Acc
     __syncthreads();
     if (warp == 0) s_W = warp_chunk_total(csum, n_chunks, lane);
     __syncthreads();
-    double W = s_W;
-    if (!(W > 0.0)) {
+    dflt W = s_W;
+    if (!df_positive(W)) {
         // Residual empty (p == q up to rounding): draw from p instead.
         w.use_p = true;
         resid = false;
@@ -697,31 +720,32 @@ __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const Acc
         __syncthreads();
         W = s_W;
     }
-    const double u = ld_dep_f(p.u_res + b);
-    const double target = u * W, tol = 1e-7 * W;
+    const float u = ld_dep_f(p.u_res + b);
+    const dflt target = df_mul_f(u, W);
+    const float tol = 1e-7f * W.hi;
     int amb = job.amb;
     if (warp == 0) {
         // lane l sums its contiguous block of chunks; a shuffle scan over the
         // lanes and a ballot find the lane whose block holds the crossing
         const int per = (n_chunks + 31) / 32;
         const int lo = min(n_chunks, lane * per), hi = min(n_chunks, lo + per);
-        double part = 0.0;
-        for (int c = lo; c < hi; ++c) part += csum[c];
-        double incl = part;
+        dflt part = {0.f, 0.f};
+        for (int c = lo; c < hi; ++c) part = df_add(part, csum[c]);
+        dflt incl = part;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            const dflt y = df_shfl_up(incl, o);
+            if (lane >= o) incl = df_add(incl, y);
         }
-        const double excl = incl - part;
-        const unsigned own = __ballot_sync(0xffffffffu, hi > lo && excl <= target && target < incl);
+        const dflt excl = df_sub(incl, part);
+        const unsigned own = __ballot_sync(0xffffffffu, hi > lo && df_le(excl, target) && df_lt(target, incl));
         int cs = -1;
-        double before = 0.0;
         if (own && lane == __ffs(own) - 1) {
-            before = excl;
+            dflt before = excl;
             for (int c = lo; c < hi; ++c) {
-                if (before + csum[c] > target) { cs = c; break; }
-                before += csum[c];
+                const dflt nb = df_add(before, csum[c]);
+                if (df_lt(target, nb)) { cs = c; break; }
+                before = nb;
             }
             if (cs >= 0) {
                 s_cstar = cs;
@@ -734,10 +758,10 @@ __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const Acc
             // rounding pushed the target past the total: the last chunk with weight
             int last = -1;
             for (int c = 0; c < n_chunks; ++c)
-                if (csum[c] > 0.0) last = c;
+                if (df_positive(csum[c])) last = c;
             if (last < 0) last = n_chunks - 1;
-            double bf = 0.0;
-            for (int c = 0; c < last; ++c) bf += csum[c];
+            dflt bf = {0.f, 0.f};
+            for (int c = 0; c < last; ++c) bf = df_add(bf, csum[c]);
             s_cstar = last;
             s_before = bf;
             s_amb = 1;
@@ -746,12 +770,12 @@ __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const Acc
     if (tid == 0) { found_token = -1; found_amb = 0; }
     __syncthreads();
     const int cstar = s_cstar;
-    const double before = s_before;
+    const dflt before = s_before;
     amb += s_amb;
     if (tid == 0) { found_token = -1; found_amb = 0; }
-    // Walk chunk cstar: thread t owns its logits 4t .. 4t+3; an fp64 block scan
-    // of the per-thread sums tells every thread where its run starts, and the
-    // one run containing the crossing walks its four weights.
+    // Walk chunk cstar: thread t owns its logits 4t .. 4t+3; a double-float
+    // block scan of the per-thread sums tells every thread where its run
+    // starts, and the one run containing the crossing walks its four weights.
     const int cb = cstar * kSmpChunk, ce = min(cb + kSmpChunk, V);
     const int my0 = cb + 4 * tid;
     dflt wt[4];
@@ -762,20 +786,21 @@ __global__ void __launch_bounds__(kSmpThreads, 1) accept_sample_kernel(const Acc
     dflt mine = {0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc_add(mine, wt[e]);
-    const double my_sum = df_to_double(acc_done(mine));
-    const double incl = block_scan_warps(my_sum, wtot);
-    const double start = before + (incl - my_sum);
-    if (my0 < ce && start <= target && target < before + incl) {
-        double prev = start;
+    const dflt my_sum = acc_done(mine);
+    const dflt incl = block_scan_df(my_sum, wtot);
+    const dflt start = df_add(before, df_sub(incl, my_sum));
+    if (my0 < ce && df_le(start, target) && df_lt(target, df_add(before, incl))) {
+        dflt prev = start;
         int tok = -1, last_pos = -1;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             if (weight_positive(wt[e])) last_pos = e;
-            const double nxt = prev + df_to_double(wt[e]);
-            if (tok < 0 && nxt > target) {
+            const dflt nxt = df_add(prev, wt[e]);
+            if (tok < 0 && df_lt(target, nxt)) {
                 tok = e;
                 const int t = my0 + e;
-                found_amb = ((t > 0 && target - prev < tol) || (t < V - 1 && nxt - target < tol)) ? 1 : 0;
+                found_amb = ((t > 0 && df_sub(target, prev).hi < tol) || (t < V - 1 && df_sub(nxt, target).hi < tol))
+                                ? 1 : 0;
             }
             if (tok < 0) prev = nxt;
         }
@@ -812,7 +837,7 @@ size_t accept_workspace_bytes(int B, int gamma, int V) {
     const int n_chunks = (V + kSmpChunk - 1) / kSmpChunk;
     const int rows = 2 * gamma + 1;
     return align256a((size_t)B * rows * n_stat * sizeof(RowStat)) + align256a((size_t)B * sizeof(JobInfo)) +
-           align256a((size_t)B * n_chunks * sizeof(double));
+           align256a((size_t)B * n_chunks * sizeof(dflt));
 }
 
 magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target, const float *draft,
@@ -842,7 +867,7 @@ magicdec_status launch_spec_accept(int B, int gamma, int V, const float *target,
     w += align256a((size_t)B * rows_alloc * prm.n_stat_chunks * sizeof(RowStat));
     prm.job = reinterpret_cast<JobInfo *>(w);
     w += align256a((size_t)B * sizeof(JobInfo));
-    prm.chunk_sum = reinterpret_cast<double *>(w);
+    prm.chunk_sum = reinterpret_cast<dflt *>(w);
 
     magicdec_status s = magicdec_host::launch_pdl(greedy ? accept_stats_kernel<true> : accept_stats_kernel<false>,
                                                   dim3((unsigned)(B * prm.rows_per_b), (unsigned)prm.n_stat_chunks),
