@@ -8,7 +8,7 @@
 // two):
 //   stats  one CTA per (row, 4096 logits): for each of its four 1024-logit
 //          warp slices the max and sum of exp(x - max), merged into one
-//          record (double-float across lanes, fp64 across warps); greedy
+//          record (double-float across lanes and warps); greedy
 //          mode keeps top-1 (smallest index among equals), top-2 and argmax;
 //   chain  one CTA per sequence: a warp per row merges the row's records in
 //          fp64, warp 0 evaluates p(x)/q(x) for each draft token in fp64 and
@@ -104,7 +104,7 @@ __device__ __forceinline__ dflt df_shfl(dflt a, int src) {
 
 // ------------------------------------------------------------------- stats
 struct RowStat {
-    double s;          // sum over the chunk of exp(x - m)
+    dflt s;            // sum over the chunk of exp(x - m), double-float
     float m;           // chunk max
     float top1, top2;
     int arg;
@@ -160,7 +160,7 @@ __device__ __forceinline__ void top_merge(float &t1, float &t2, int &arg, float 
 // load instruction is coalesced.  Sampling mode records the CTA's max m and
 // S = sum exp(x - m): the warps agree on m through shared memory, each lane
 // sums its 32 exponentials pairwise in fp32 (error ~1e-7 relative, the order
-// of the exponential's own), lanes merge in double-float and warps in fp64, in
+// of the exponential's own), lanes and warps merge in double-float, in
 // a fixed order.
 // Greedy mode records only the top two logits and the argmax (smallest index
 // on ties).
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
     constexpr int NW = kAccThreads / 32;
     __shared__ float s_max[NW], s_t1[NW], s_t2[NW];
     __shared__ int s_arg[NW];
-    __shared__ double s_sum[NW];
+    __shared__ dflt s_sum[NW];
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
         __syncthreads();
         if (threadIdx.x != 0) return;
         for (int w2 = 1; w2 < NW; ++w2) top_merge(top1, top2, arg, s_t1[w2], s_t2[w2], s_arg[w2]);
-        st.s = 0.0;
+        st.s = dflt{0.f, 0.f};
         st.m = top1;
         st.top1 = top1;
         st.top2 = top2;
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
         float m = s_max[0];
 #pragma unroll
         for (int w2 = 1; w2 < NW; ++w2) m = fmaxf(m, s_max[w2]);
-        double sum = 0.0;
+        dflt sum = {0.f, 0.f};
         if (m != -INFINITY) {
             const float mb = m * kLog2e;
             float e[kAccPer];
@@ -258,14 +258,15 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
             for (int w = kAccPer / 2; w > 0; w >>= 1)
 #pragma unroll
                 for (int i = 0; i < w; ++i) e[i] += e[i + w];
-            // lanes merge in double-float on the FP32 pipe (fp64 throughput is scarce)
-            sum = df_to_double(warp_sum_df(dflt{e[0], 0.f}));
+            // lanes and warps merge in double-float on the FP32 pipes (fp64
+            // throughput is scarce on this GPU)
+            sum = warp_sum_df(dflt{e[0], 0.f});
         }
         if (lane == 0) s_sum[warp] = sum;
         __syncthreads();
         if (threadIdx.x != 0) return;
-        double S = s_sum[0];
-        for (int w2 = 1; w2 < NW; ++w2) S += s_sum[w2];
+        dflt S = s_sum[0];
+        for (int w2 = 1; w2 < NW; ++w2) S = df_add(S, s_sum[w2]);
         st.s = S;
         st.m = m;
         st.top1 = m;
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
         double sum = 0.0;
         for (int c = lane; c < p.n_stat_chunks; c += 32) {
             const RowStat st = src[c];
-            if (st.m != -INFINITY) sum += st.s * exp((double)st.m - (double)m);
+            if (st.m != -INFINITY) sum += df_to_double(st.s) * exp((double)st.m - (double)m);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
