@@ -27,80 +27,13 @@
 // carry ~1e-12 relative error, so the drawn token agrees with an exact
 // evaluation except when u * total falls within ~1e-9 of a token boundary.
 #include "common.cuh"
+#include "dfloat.cuh"
 
 namespace magicdec {
 
 constexpr int kStatChunk = 1024;      // logits per statistics record (one warp)
 constexpr int kAccThreads = 128;     // statistics CTA: 4 warps, one record per 4 slices
 constexpr int kAccPer = kStatChunk / 32;  // 32 logits per lane of a statistics warp, held in registers
-
-// ------------------------------------------------------------ double-float
-struct dflt {
-    float hi, lo;
-};
-
-__device__ __forceinline__ dflt quick_two_sum(float a, float b) {
-    const float s = a + b;
-    return {s, b - (s - a)};
-}
-
-__device__ __forceinline__ dflt two_sum(float a, float b) {
-    const float s = a + b;
-    const float bb = s - a;
-    return {s, (a - (s - bb)) + (b - bb)};
-}
-
-__device__ __forceinline__ dflt df_add_f(dflt a, float b) {
-    dflt s = two_sum(a.hi, b);
-    s.lo += a.lo;
-    return quick_two_sum(s.hi, s.lo);
-}
-
-__device__ __forceinline__ dflt df_add(dflt a, dflt b) {
-    dflt s = two_sum(a.hi, b.hi);
-    s.lo += a.lo + b.lo;
-    return quick_two_sum(s.hi, s.lo);
-}
-
-// float x double-float -> double-float
-__device__ __forceinline__ dflt df_mul_f(float a, dflt b) {
-    const float p = a * b.hi;
-    const float e = fmaf(a, b.hi, -p) + a * b.lo;
-    return quick_two_sum(p, e);
-}
-
-__device__ __forceinline__ dflt df_from_double(double x) {
-    const float hi = (float)x;
-    return {hi, (float)(x - (double)hi)};
-}
-
-__device__ __forceinline__ double df_to_double(dflt a) { return (double)a.hi + (double)a.lo; }
-
-// Warp sum of double-float values in a fixed butterfly order (fp32 pipe only).
-__device__ __forceinline__ dflt warp_sum_df(dflt a) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        dflt b;
-        b.hi = __shfl_xor_sync(0xffffffffu, a.hi, o);
-        b.lo = __shfl_xor_sync(0xffffffffu, a.lo, o);
-        a = df_add(a, b);
-    }
-    return a;
-}
-
-__device__ __forceinline__ dflt df_sub(dflt a, dflt b) { return df_add(a, dflt{-b.hi, -b.lo}); }
-
-// Order of normalised double-float values (|lo| at most half an ulp of hi).
-__device__ __forceinline__ bool df_lt(dflt a, dflt b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
-__device__ __forceinline__ bool df_le(dflt a, dflt b) { return a.hi < b.hi || (a.hi == b.hi && a.lo <= b.lo); }
-__device__ __forceinline__ bool df_positive(dflt a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
-
-__device__ __forceinline__ dflt df_shfl_up(dflt a, int o) {
-    return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
-}
-__device__ __forceinline__ dflt df_shfl(dflt a, int src) {
-    return {__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
-}
 
 // ------------------------------------------------------------------- stats
 struct RowStat {
@@ -327,14 +260,14 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
             const int ua = __shfl_xor_sync(0xffffffffu, arg, o);
             top_merge(t1, t2, arg, u1, u2, ua);
         }
-        double sum = 0.0;
+        // S = sum of s_c exp(m_c - m), in double-float on the FP32 pipes
+        dflt sum = {0.f, 0.f};
         for (int c = lane; c < p.n_stat_chunks; c += 32) {
             const RowStat st = src[c];
-            if (st.m != -INFINITY) sum += df_to_double(st.s) * exp((double)st.m - (double)m);
+            if (st.m != -INFINITY) sum = df_add(sum, df_mul(st.s, df_exp_diff(st.m, m)));
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) rs[r] = RowAll{sum, m, t1, t2, arg};
+        sum = warp_sum_df(sum);
+        if (lane == 0) rs[r] = RowAll{df_to_double(sum), m, t1, t2, arg};
     }
     __syncthreads();
     if (warp != 0) return;
