@@ -44,8 +44,8 @@ struct RowStat {
 };
 
 struct JobInfo {
-    double st, sd;     // target / draft normalisers relative to mt / md
-    float inv_st_hi, inv_st_lo, inv_sd_hi, inv_sd_lo;   // 1/st, 1/sd as double-float (one division per sequence)
+    // 1/S_t, 1/S_d as double-float: the target / draft normalisers relative to mt / md
+    float inv_st_hi, inv_st_lo, inv_sd_hi, inv_sd_lo;
     float mt, md;
     int kind;          // 0 = nothing to sample, 1 = residual at row acc, 2 = bonus from target row gamma
     int acc;
@@ -209,9 +209,9 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const AcceptP
     p.stats[row * p.n_stat_chunks + rec] = st;
 }
 
-// Whole-row statistics, merged in fp64: max m and S = sum exp(x - m).
+// Whole-row statistics: max m and S = sum exp(x - m) (double-float).
 struct RowAll {
-    double s;
+    dflt s;
     float m, top1, top2;
     int arg;
 };
@@ -220,12 +220,15 @@ constexpr int kMaxRows = 2 * 32 + 1;     // rows per sequence (gamma <= 32)
 constexpr int kChainThreads = 256;
 
 // One CTA per sequence.  Warp r merges row r's chunk records (lane c takes
-// chunk c: one fp64 exponential per lane, fixed-order butterfly sum); warp 0
-// then evaluates p(x)/q(x) for the gamma draft tokens (one position per
-// lane), and thread 0 runs the sequential accept chain on those numbers.
+// chunk c: one double-float exponential per lane, fixed-order butterfly sum);
+// warp 0 then evaluates p(x)/q(x) for the gamma draft tokens (one position
+// per lane), and thread 0 runs the sequential accept chain on those numbers.
+// All of it is double-float on the FP32 pipes, but for ratios whose
+// exponentials could underflow (logits more than 80 below their row's
+// maximum), which take the fp64 path.
 __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const AcceptParams p) {
     __shared__ RowAll rs[kMaxRows];
-    __shared__ double ratio[32];
+    __shared__ dflt ratio[32];
     __shared__ int okq0[32];
     pdl_trigger();
     pdl_wait();
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
             if (st.m != -INFINITY) sum = df_add(sum, df_mul(st.s, df_exp_diff(st.m, m)));
         }
         sum = warp_sum_df(sum);
-        if (lane == 0) rs[r] = RowAll{df_to_double(sum), m, t1, t2, arg};
+        if (lane == 0) rs[r] = RowAll{sum, m, t1, t2, arg};
     }
     __syncthreads();
     if (warp != 0) return;
@@ -275,18 +278,18 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
         // ratio_i = p_i(x_i) / q_i(x_i); okq0: 1 = accept (q = 0 < p), 2 = reject
         if (lane < gamma) {               // gamma <= 32: position i = lane, logits prefetched
             const int i = lane;
-            double rt = -1.0;
+            dflt rt = {-1.f, 0.f};
             int oq = 0;
             if (xtok >= 0 && xtok < V) {
                 const RowAll ts = rs[i], ds = rs[gamma + 1 + i];
-                const double dp = (double)xt - (double)ts.m, dq = (double)xd - (double)ds.m;
-                if (dp > -700.0 && dq > -700.0) {
-                    // p / q as one exponential and one division (fp64 is narrow here)
-                    rt = exp(dp - dq) * (ds.s / ts.s);
+                if (xt - ts.m > -80.f && xd - ds.m > -80.f) {
+                    // p / q = exp(xt - mt) S_d / (exp(xd - md) S_t)
+                    rt = df_div(df_mul(df_exp_diff(xt, ts.m), ds.s), df_mul(df_exp_diff(xd, ds.m), ts.s));
                 } else {
                     // an exponential may underflow: q = 0 < p accepts, p = q = 0 rejects
-                    const double px = exp(dp) / ts.s, qx = exp(dq) / ds.s;
-                    if (qx > 0.0) rt = px / qx;
+                    const double dp = (double)xt - (double)ts.m, dq = (double)xd - (double)ds.m;
+                    const double px = exp(dp) / df_to_double(ts.s), qx = exp(dq) / df_to_double(ds.s);
+                    if (qx > 0.0) rt = df_from_double(px / qx);
                     else oq = px > 0.0 ? 1 : 2;
                 }
             } else {
@@ -314,16 +317,21 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
             if (oq) {
                 ok = oq == 1;
             } else {
-                const double rt = ratio[i];
-                const double u = ld_dep_f(p.u_acc + (long long)b * gamma + i);
-                ok = u < rt;
-                if (fabs(u - rt) < 1e-4) ++amb;
+                const dflt rt = ratio[i];
+                const float u = ld_dep_f(p.u_acc + (long long)b * gamma + i);
+                ok = df_lt(dflt{u, 0.f}, rt);
+                if (fabsf(df_sub(rt, dflt{u, 0.f}).hi) < 1e-4f) ++amb;
             }
             if (!ok) {
                 const RowAll ts = rs[i], ds = rs[gamma + 1 + i];
                 job.kind = 1;
-                job.mt = ts.m; job.st = ts.s;
-                job.md = ds.m; job.sd = ds.s;
+                job.mt = ts.m;
+                job.md = ds.m;
+                const dflt it = df_div(dflt{1.f, 0.f}, ts.s), id = df_div(dflt{1.f, 0.f}, ds.s);
+                job.inv_st_hi = it.hi;
+                job.inv_st_lo = it.lo;
+                job.inv_sd_hi = id.hi;
+                job.inv_sd_lo = id.lo;
             }
         }
         if (!ok) { acc = i; break; }
@@ -336,7 +344,10 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
             emit = ts.arg;
         } else {
             job.kind = 2;
-            job.mt = ts.m; job.st = ts.s;
+            job.mt = ts.m;
+            const dflt it = df_div(dflt{1.f, 0.f}, ts.s);
+            job.inv_st_hi = it.hi;
+            job.inv_st_lo = it.lo;
         }
     }
     for (int i = acc + 1; i <= gamma; ++i) out[i] = -1;
@@ -347,14 +358,6 @@ __global__ void __launch_bounds__(kChainThreads) accept_chain_kernel(const Accep
     }
     job.acc = acc;
     job.amb = amb;
-    if (job.kind != 0) {
-        const dflt it = df_from_double(1.0 / job.st);
-        job.inv_st_hi = it.hi;
-        job.inv_st_lo = it.lo;
-        const dflt id = df_from_double(job.kind == 1 ? 1.0 / job.sd : 0.0);
-        job.inv_sd_hi = id.hi;
-        job.inv_sd_lo = id.lo;
-    }
     p.job[b] = job;
 }
 

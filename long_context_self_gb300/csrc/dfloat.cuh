@@ -70,6 +70,18 @@ __device__ __forceinline__ dflt df_mul(dflt a, dflt b) {
     return quick_two_sum(p, fmaf(a.hi, b.hi, -p) + (a.hi * b.lo + a.lo * b.hi));
 }
 
+// a / b by long division in double-float (as in Bailey's double-double
+// library): a single-precision quotient digit, the exact remainder, and two
+// correction digits from it; ~1e-14 relative.
+__device__ __forceinline__ dflt df_div(dflt a, dflt b) {
+    const float q1 = a.hi / b.hi;
+    const dflt r1 = df_sub(a, df_mul_f(q1, b));
+    const float q2 = r1.hi / b.hi;
+    const dflt r2 = df_sub(r1, df_mul_f(q2, b));
+    const float q3 = r2.hi / b.hi;
+    return df_add_f(quick_two_sum(q1, q2), q3);
+}
+
 // exp(a - b) for fp32 a <= b as a double-float on the FP32 pipes: within
 // 1e-11 relative down to exp(-70); below that the low part is subnormal and
 // the error stays under an absolute 2e-38.  The difference as an exact

@@ -1,6 +1,6 @@
-// Accuracy check of df_exp_diff (long_context_self_gb300/csrc/dfloat.cuh): the
-// double-float exp(a - b) of the accept kernels' record merges against the
-// host's long-double exp of the same float inputs.  Prints the largest
+// Accuracy check of df_exp_diff and df_div (long_context_self_gb300/csrc/dfloat.cuh):
+// the double-float exp(a - b) and quotient of the accept kernels against the
+// host's long-double arithmetic on the same inputs.  Prints the largest
 // errors and exits non-zero when they exceed the bounds stated below.
 #include <cmath>
 #include <cstdint>
@@ -12,6 +12,16 @@
 #include "../long_context_self_gb300/csrc/dfloat.cuh"
 
 using magicdec::dflt;
+
+__global__ void div_kernel(const float *ah, const float *al, const float *bh, const float *bl, float *qh, float *ql,
+                           int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        const dflt q = magicdec::df_div(dflt{ah[i], al[i]}, dflt{bh[i], bl[i]});
+        qh[i] = q.hi;
+        ql[i] = q.lo;
+    }
+}
 
 __global__ void exp_diff_kernel(const float *a, const float *b, float *hi, float *lo, int n) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -72,5 +82,42 @@ int main() {
     }
     printf("checked %d max_rel %.3Le at a-b %.6Lf; tail %d max_abs %.3Le\n", checked, max_rel, worst_d, tail,
            max_abs_tail);
-    return (max_rel < 1e-11L && max_abs_tail < 2e-38L) ? 0 : 1;
+
+    // df_div on normalised double-float pairs over magnitudes 2^-40 .. 2^40:
+    // 1e-13 relative against long double.
+    const int m = 200000;
+    std::vector<float> ah(m), al(m), bh(m), bl(m), qh(m), ql(m);
+    std::vector<long double> av(m), bv(m);
+    for (int i = 0; i < m; ++i) {
+        for (int w = 0; w < 2; ++w) {
+            st = st * 6364136223846793005ull + 1442695040888963407ull;
+            const double frac = 1.0 + (double)(st >> 11) / 9007199254740992.0;          // [1, 2), 53 bits
+            st = st * 6364136223846793005ull + 1442695040888963407ull;
+            const double x = frac * std::ldexp(1.0, (int)((st >> 33) % 80) - 40);
+            const float h = (float)x, l = (float)(x - (double)h);
+            (w ? bh : ah)[i] = h;
+            (w ? bl : al)[i] = l;
+            (w ? bv : av)[i] = (long double)h + (long double)l;
+        }
+    }
+    float *dah, *dal, *dbh, *dbl, *dqh, *dql;
+    if (cudaMalloc(&dah, m * 4) || cudaMalloc(&dal, m * 4) || cudaMalloc(&dbh, m * 4) || cudaMalloc(&dbl, m * 4) ||
+        cudaMalloc(&dqh, m * 4) || cudaMalloc(&dql, m * 4))
+        return 2;
+    cudaMemcpy(dah, ah.data(), m * 4, cudaMemcpyHostToDevice);
+    cudaMemcpy(dal, al.data(), m * 4, cudaMemcpyHostToDevice);
+    cudaMemcpy(dbh, bh.data(), m * 4, cudaMemcpyHostToDevice);
+    cudaMemcpy(dbl, bl.data(), m * 4, cudaMemcpyHostToDevice);
+    div_kernel<<<(m + 255) / 256, 256>>>(dah, dal, dbh, dbl, dqh, dql, m);
+    if (cudaDeviceSynchronize() != cudaSuccess) return 2;
+    cudaMemcpy(qh.data(), dqh, m * 4, cudaMemcpyDeviceToHost);
+    cudaMemcpy(ql.data(), dql, m * 4, cudaMemcpyDeviceToHost);
+    long double max_rel_div = 0.0L;
+    for (int i = 0; i < m; ++i) {
+        const long double ref = av[i] / bv[i];
+        const long double rel = fabsl(((long double)qh[i] + (long double)ql[i]) - ref) / fabsl(ref);
+        if (rel > max_rel_div) max_rel_div = rel;
+    }
+    printf("div checked %d max_rel %.3Le\n", m, max_rel_div);
+    return (max_rel < 1e-11L && max_abs_tail < 2e-38L && max_rel_div < 1e-13L) ? 0 : 1;
 }

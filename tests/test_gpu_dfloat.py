@@ -1,9 +1,10 @@
-"""The double-float exponential of the accept kernels' record merges
-(long_context_self_gb300/csrc/dfloat.cuh, df_exp_diff) against the host's
-long-double exp: tests/dfloat_check.cu is compiled for sm_103a and run; it
+"""The double-float exponential and division of the accept kernels
+(long_context_self_gb300/csrc/dfloat.cuh, df_exp_diff and df_div) against the
+host's long-double arithmetic: tests/dfloat_check.cu is compiled for sm_103a and run; it
 checks ~300 000 float pairs (differences 0-90, dense and random, ten
 magnitudes of the larger operand): 1e-11 relative down to exp(-70), an
-absolute 2e-38 below (the merged sums it feeds are at least 1)."""
+absolute 2e-38 below (the merged sums it feeds are at least 1); and 200 000
+quotients of double-float pairs over magnitudes 2^-40 .. 2^40 to 1e-13."""
 import os
 import subprocess
 import tempfile
